@@ -1,0 +1,283 @@
+"""fp64 reference definitions of the fused LoRA / QLoRA projection.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline / reference legs of ``bench.py``; never by the library.
+
+Sources (web pages about Unsloth; cited by title and section):
+
+* [P1] "UnSloth加速微调体验：在LoRA基础上再提速3倍的秘密" — sections
+  算子融合 (operator fusion, eq. ``y = Wx + ΔWx = Wx + BAx``),
+  反向传播优化 (backward with recomputation, gradient equations),
+  RoPE缓存集成 (RoPE cache fused into the Q/K projection).
+* [P2] "微调太慢？试试Unsloth：实测训练速度翻倍，显存占用减半" — §5.1
+  (inference with the adapter merged into the weight).
+* [P3] "Unsloth教程：本地微调大模型速度提升数倍，显存节省60%" — 底层内核优化
+  (fused kernels are mathematically equivalent to the unfused ops) and
+  显存优化策略 (QLoRA: 4-bit NormalFloat4 base weight, only the adapter
+  trained; 4096x4096 at rank 16 -> about 1.3e5 trainable parameters).
+* [P5] "Unsloth自动化优化：无需手动调参的实现原理" — §3.2 (fused kernel also
+  described as ``A@B + original_weight``), §3.3/§5 (NF4 is the default).
+* [QLoRA] Dettmers et al. 2023, "QLoRA: Efficient Finetuning of Quantized
+  LLMs", §3 "4-bit NormalFloat Quantization" and the NF4 table in its
+  appendix: the pages name NF4 but do not give its levels.
+
+Conventions (row-vector form of [P1] 算子融合, which writes column vectors):
+``x [M,k]``, ``W [n,k]`` (out x in), ``A [r,k]``, ``B [n,r]``,
+``y, dY [M,n]``; the LoRA scale is ``s = alpha / r``.  The pages print the
+forward without ``s`` and list ``lora_alpha`` and ``r`` only as API
+arguments; the standard LoRA reading ``s = alpha/r`` is taken.
+
+All arithmetic is numpy float64.  Inputs are expected to already hold the
+values the GPU receives (bf16-rounded), so the upcast to fp64 is exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+from scipy.stats import norm
+
+__all__ = [
+    "lora_scale", "lora_fwd", "lora_bwd", "merged_weight", "lora_param_count",
+    "bf16_round", "nf4_codebook", "nf4_quantize", "nf4_unpack", "nf4_dequant",
+    "rope_inv_freq", "rope_cos_sin", "rope_apply", "rope_apply_inverse",
+    "qk_rope_fwd", "qk_rope_bwd",
+]
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# LoRA projection
+# ---------------------------------------------------------------------------
+def lora_scale(alpha: float, r: int) -> float:
+    """LoRA branch scale ``s = alpha / r`` (reading: the pages pass
+    ``lora_alpha`` and ``r`` to ``get_peft_model`` in [P1] and never write the
+    formula)."""
+    return float(alpha) / float(r)
+
+
+def lora_fwd(x, W, A, B, alpha: float):
+    """Forward of the LoRA projection, [P1] 算子融合, eq. ``y = Wx + BAx``.
+
+    Row form: ``v = x·Aᵀ`` (the rank-r down-projection), then
+    ``y = x·Wᵀ + s·v·Bᵀ``.  Returns ``y`` [M,n] in fp64.
+    """
+    x, W, A, B = _f64(x), _f64(W), _f64(A), _f64(B)
+    s = lora_scale(alpha, A.shape[0])
+    v = x @ A.T
+    return x @ W.T + s * (v @ B.T)
+
+
+def lora_bwd(x, W, A, B, dy, alpha: float):
+    """Backward of :func:`lora_fwd`, [P1] 反向传播优化.
+
+    The page prints ``∂L/∂A = ∂L/∂y·xᵀBᵀ`` and ``∂L/∂B = ∂L/∂y·A·xᵀ``; that
+    operand order does not type-check and the scale is missing.  Derived
+    from the forward instead (W is frozen: only the adapter trains, [P3]
+    显存优化策略), with ``v = x·Aᵀ`` recomputed rather than cached as the
+    section describes::
+
+        u  = dY·B
+        dX = dY·W + s·u·A
+        dA = s·uᵀ·x
+        dB = s·dYᵀ·v
+
+    Returns ``(dX [M,k], dA [r,k], dB [n,r])`` in fp64.
+    """
+    x, W, A, B, dy = _f64(x), _f64(W), _f64(A), _f64(B), _f64(dy)
+    s = lora_scale(alpha, A.shape[0])
+    u = dy @ B
+    v = x @ A.T                      # recomputed, not taken from the forward
+    dx = dy @ W + s * (u @ A)
+    dA = s * (u.T @ x)
+    dB = s * (dy.T @ v)
+    return dx, dA, dB
+
+
+def merged_weight(W, A, B, alpha: float):
+    """Adapter merged into the base weight, ``W' = W + s·B·A``
+    ([P2] §5.1; [P5] §3.2 "A@B + original_weight")."""
+    W, A, B = _f64(W), _f64(A), _f64(B)
+    return W + lora_scale(alpha, A.shape[0]) * (B @ A)
+
+
+def lora_param_count(k: int, n: int, r: int) -> int:
+    """Trainable adapter parameters ``r·(k+n)`` ([P3] 显存优化策略)."""
+    return int(r) * (int(k) + int(n))
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding (for the NF4 block scale, which is stored as bf16)
+# ---------------------------------------------------------------------------
+def bf16_round(a):
+    """Round fp64 values to the nearest bfloat16 (ties to even), in fp64.
+
+    bfloat16 keeps 8 significant bits and fp32's exponent range, so the
+    spacing of representable values around ``|a|`` is
+    ``2**(max(floor(log2|a|), -126) - 7)``; ``np.rint`` rounds half to even.
+    Values beyond the largest finite bf16 become ``inf``.
+    """
+    a = _f64(a)
+    out = np.zeros_like(a)
+    nz = (a != 0) & np.isfinite(a)
+    e = np.floor(np.log2(np.abs(a[nz])))
+    e = np.maximum(e, -126.0)
+    q = np.exp2(e - 7.0)
+    out[nz] = np.rint(a[nz] / q) * q
+    out[~np.isfinite(a)] = a[~np.isfinite(a)]
+    big = np.abs(out) > 3.3895313892515355e38   # largest finite bf16
+    out[big] = np.sign(out[big]) * np.inf
+    return out
+
+
+# ---------------------------------------------------------------------------
+# NF4 (QLoRA NormalFloat4) — [P3] 显存优化策略, [P5] §3.3/§5, [QLoRA] §3
+# ---------------------------------------------------------------------------
+def nf4_codebook():
+    """The 16 NF4 levels, built as [QLoRA] §3 describes.
+
+    Quantiles of N(0,1) are taken at equally spaced probabilities that stop
+    short of the tails by ``delta = (1/32 + 1/30)/2``: 8 levels for the
+    positive half (9 points from ``1-delta`` to 1/2, the 1/2 point dropped)
+    and 7 for the negative half (8 points, 1/2 dropped), plus an exact zero;
+    the set is sorted and divided by its maximum so it spans [-1, 1].
+    """
+    delta = 0.5 * (1.0 / 32.0 + 1.0 / 30.0)
+    hi = 1.0 - delta
+    pos = norm.ppf(np.linspace(hi, 0.5, 9)[:-1])
+    neg = -norm.ppf(np.linspace(hi, 0.5, 8)[:-1])
+    levels = np.sort(np.concatenate([neg, [0.0], pos]))
+    return levels / levels.max()
+
+
+def nf4_quantize(W, blocksize: int = 64, decision: str = "fp64"):
+    """Blockwise NF4 quantisation of a row-major ``W [n,k]``.
+
+    Reading (the pages give only the name NormalFloat4): blocks are
+    ``blocksize`` consecutive elements along k; the block scale is
+    ``absmax = max|w|`` stored as bf16 (round to nearest even); each element
+    takes the index of the nearest level of :func:`nf4_codebook` to
+    ``w/absmax`` (clamped to [-1,1]; ties to the lower index; a block with
+    ``absmax == 0`` is all code 7, the exact zero).  Byte ``j`` of a row
+    holds element ``2j`` in its high nibble and ``2j+1`` in its low nibble.
+
+    ``decision`` selects the precision of the nearest-level decision:
+    ``"fp64"`` (plain definition) or ``"fp32"`` (IEEE single-precision
+    division and distances, the precision a GPU quantiser uses).
+
+    Returns ``(codes uint8 [n, k/2], absmax float64 [n, k/blocksize])``.
+    """
+    W = _f64(W)
+    n, k = W.shape
+    assert k % blocksize == 0 and blocksize % 2 == 0
+    blocks = W.reshape(n, k // blocksize, blocksize)
+    absmax = bf16_round(np.max(np.abs(blocks), axis=2))
+    levels = nf4_codebook()
+    safe = np.where(absmax == 0.0, 1.0, absmax)[:, :, None]
+    if decision == "fp64":
+        ratio = np.clip(blocks / safe, -1.0, 1.0)
+        dist = np.abs(ratio[..., None] - levels)
+    elif decision == "fp32":
+        ratio = (blocks.astype(np.float32) / safe.astype(np.float32))
+        ratio = np.clip(ratio, np.float32(-1.0), np.float32(1.0))
+        dist = np.abs(ratio[..., None] - levels.astype(np.float32))
+    else:
+        raise ValueError(decision)
+    code = np.argmin(dist, axis=-1).astype(np.uint8)     # first minimum wins
+    code[absmax == 0.0] = 7
+    code = code.reshape(n, k)
+    packed = (code[:, 0::2] << 4) | code[:, 1::2]
+    return packed.astype(np.uint8), absmax
+
+
+def nf4_unpack(codes):
+    """Split packed bytes into 4-bit indices: high nibble first."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    n, kh = codes.shape
+    out = np.empty((n, 2 * kh), dtype=np.uint8)
+    out[:, 0::2] = codes >> 4
+    out[:, 1::2] = codes & 0xF
+    return out
+
+
+def nf4_dequant(codes, absmax, blocksize: int = 64):
+    """``W[i,j] = c[code(i,j)] · absmax[i, j // blocksize]`` in fp64."""
+    idx = nf4_unpack(codes)
+    absmax = _f64(absmax)
+    levels = nf4_codebook()
+    scale = np.repeat(absmax, blocksize, axis=1)
+    return levels[idx] * scale
+
+
+# ---------------------------------------------------------------------------
+# RoPE — [P1] RoPE缓存集成
+# ---------------------------------------------------------------------------
+def rope_inv_freq(head_dim: int, theta: float):
+    """``theta ** (-2i/D)`` for ``i = 0 .. D/2-1`` (reading: Llama/Qwen
+    rotary embedding; the section does not state the frequencies)."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return float(theta) ** (-2.0 * i / head_dim)
+
+
+def rope_cos_sin(positions, head_dim: int, theta: float):
+    """Per-position cos/sin table ``[len(positions), D/2]`` (the contiguous
+    cache of the section), angles ``pos · theta**(-2i/D)`` in fp64."""
+    pos = np.asarray(positions, dtype=np.float64)
+    ang = pos[:, None] * rope_inv_freq(head_dim, theta)[None, :]
+    return np.cos(ang), np.sin(ang)
+
+
+def rope_apply(y, positions, head_dim: int, theta: float):
+    """Rotate each ``head_dim``-wide head of ``y [M, H*D]`` by its row's
+    position: pairs ``(i, i+D/2)`` (the rotate-half pairing of Llama/Qwen);
+    ``y'[i] = y[i]cos − y[i+D/2]sin``, ``y'[i+D/2] = y[i+D/2]cos + y[i]sin``."""
+    y = _f64(y)
+    M, N = y.shape
+    D, h = head_dim, head_dim // 2
+    assert N % D == 0
+    c, s = rope_cos_sin(positions, D, theta)
+    yh = y.reshape(M, N // D, D)
+    a, b = yh[:, :, :h], yh[:, :, h:]
+    c, s = c[:, None, :], s[:, None, :]
+    out = np.concatenate([a * c - b * s, b * c + a * s], axis=2)
+    return out.reshape(M, N)
+
+
+def rope_apply_inverse(y, positions, head_dim: int, theta: float):
+    """Transpose (= inverse) of :func:`rope_apply`: rotation by the negative
+    angle.  This is the backward of the rotation."""
+    y = _f64(y)
+    M, N = y.shape
+    D, h = head_dim, head_dim // 2
+    c, s = rope_cos_sin(positions, D, theta)
+    yh = y.reshape(M, N // D, D)
+    a, b = yh[:, :, :h], yh[:, :, h:]
+    c, s = c[:, None, :], s[:, None, :]
+    out = np.concatenate([a * c + b * s, b * c - a * s], axis=2)
+    return out.reshape(M, N)
+
+
+def qk_rope_fwd(x, Wq, Aq, Bq, Wk, Ak, Bk, alpha, positions, theta,
+                head_dim: int = 128):
+    """q/k projections with RoPE applied after the LoRA sum
+    ([P1] RoPE缓存集成: the rotation happens while computing
+    ``q_proj(x) + lora_q(x)``).  Returns ``(q, k)`` in fp64."""
+    q = rope_apply(lora_fwd(x, Wq, Aq, Bq, alpha), positions, head_dim, theta)
+    k = rope_apply(lora_fwd(x, Wk, Ak, Bk, alpha), positions, head_dim, theta)
+    return q, k
+
+
+def qk_rope_bwd(x, Wq, Aq, Bq, Wk, Ak, Bk, dq, dk, alpha, positions, theta,
+                head_dim: int = 128):
+    """Backward of :func:`qk_rope_fwd`: undo the rotation on the incoming
+    gradients, then :func:`lora_bwd` per projection; dX is summed over q
+    and k because both read the same x.
+
+    Returns ``(dX, dAq, dBq, dAk, dBk)`` in fp64."""
+    dq_pre = rope_apply_inverse(dq, positions, head_dim, theta)
+    dk_pre = rope_apply_inverse(dk, positions, head_dim, theta)
+    dxq, dAq, dBq = lora_bwd(x, Wq, Aq, Bq, dq_pre, alpha)
+    dxk, dAk, dBk = lora_bwd(x, Wk, Ak, Bk, dk_pre, alpha)
+    return dxq + dxk, dAq, dBq, dAk, dBk
+

@@ -1,0 +1,306 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each test ties an oracle function to something independent of its own code:
+a special case that reduces to a library routine, an algebraic identity
+that takes a different route, finite differences, invariants of rotations,
+a published table, brute force on tiny inputs, or a hand-derived example.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as ref
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(12345)
+
+
+def _rand(*shape, scale=1.0):
+    return rng.standard_normal(shape) * scale
+
+
+def _golden_kv(name):
+    out = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *vals = line.split()
+        out[key] = vals
+    return out
+
+
+# --------------------------------------------------------------------------
+# forward
+# --------------------------------------------------------------------------
+def test_worked_example_forward_and_backward():
+    g = _golden_kv("lora_worked_example.txt")
+    f = lambda k: np.array([float(v) for v in g[k]])
+    x = f("x").reshape(1, 2)
+    W = f("W").reshape(2, 2)
+    A = f("A").reshape(2, 2)
+    B = f("B").reshape(2, 2)
+    alpha = float(g["alpha"][0])
+    y = ref.lora_fwd(x, W, A, B, alpha)
+    np.testing.assert_array_equal(y, f("y").reshape(1, 2))
+    dx, dA, dB = ref.lora_bwd(x, W, A, B, f("dY").reshape(1, 2), alpha)
+    np.testing.assert_array_equal(dx, f("dX").reshape(1, 2))
+    np.testing.assert_array_equal(dA, f("dA").reshape(2, 2))
+    np.testing.assert_array_equal(dB, f("dB").reshape(2, 2))
+
+
+@pytest.mark.parametrize("M,k,n,r", [(5, 7, 3, 2), (16, 32, 24, 8)])
+def test_b_zero_is_plain_linear(M, k, n, r):
+    """B = 0 removes the adapter: y is torch's F.linear, dX its autograd
+    gradient, and dA = 0."""
+    x, W, A = _rand(M, k), _rand(n, k), _rand(r, k)
+    B = np.zeros((n, r))
+    y = ref.lora_fwd(x, W, A, B, alpha=16.0)
+    xt = torch.tensor(x, requires_grad=True)
+    yt = torch.nn.functional.linear(xt, torch.tensor(W))
+    np.testing.assert_allclose(y, yt.detach().numpy(), rtol=0, atol=1e-12)
+    G = _rand(M, n)
+    yt.backward(torch.tensor(G))
+    dx, dA, dB = ref.lora_bwd(x, W, A, B, G, alpha=16.0)
+    np.testing.assert_allclose(dx, xt.grad.numpy(), rtol=0, atol=1e-12)
+    assert np.all(dA == 0.0)
+    # dB = s·dYᵀ·(x·Aᵀ) does not vanish when B = 0
+    assert np.abs(dB).max() > 0
+
+
+def test_merged_weight_identity():
+    """y equals the plain linear map with the adapter folded into W
+    (different association of the same product)."""
+    M, k, n, r, alpha = 9, 12, 10, 3, 6.0
+    x, W, A, B = _rand(M, k), _rand(n, k), _rand(r, k), _rand(n, r)
+    s = alpha / r
+    Wm = np.array(W)
+    for i in range(n):                       # W + s·B·A by explicit loops
+        for j in range(k):
+            Wm[i, j] += s * sum(B[i, l] * A[l, j] for l in range(r))
+    y_merged = torch.nn.functional.linear(torch.tensor(x), torch.tensor(Wm)).numpy()
+    np.testing.assert_allclose(ref.lora_fwd(x, W, A, B, alpha), y_merged, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ref.merged_weight(W, A, B, alpha), Wm, rtol=1e-13, atol=1e-13)
+
+
+def test_w_zero_and_alpha_linearity():
+    M, k, n, r = 6, 8, 5, 2
+    x, W, A, B = _rand(M, k), _rand(n, k), _rand(r, k), _rand(n, r)
+    y0 = ref.lora_fwd(x, W, A, B, 0.0)
+    y1 = ref.lora_fwd(x, W, A, B, 3.0)
+    y2 = ref.lora_fwd(x, W, A, B, 6.0)
+    np.testing.assert_allclose(y2 - y0, 2.0 * (y1 - y0), rtol=1e-12, atol=1e-12)
+    # W = 0 leaves only the adapter; with r = 1 it is a rank-one outer product
+    A1, B1 = _rand(1, k), _rand(n, 1)
+    yz = ref.lora_fwd(x, np.zeros((n, k)), A1, B1, 5.0)
+    outer = 5.0 * np.outer(x @ A1[0], B1[:, 0])
+    np.testing.assert_allclose(yz, outer, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# backward: central finite differences of L = sum(G ⊙ y)
+# --------------------------------------------------------------------------
+def _fd_grad(fun, P, h=1e-6):
+    g = np.zeros_like(P)
+    for idx in np.ndindex(P.shape):
+        old = P[idx]
+        P[idx] = old + h
+        fp = fun()
+        P[idx] = old - h
+        fm = fun()
+        P[idx] = old
+        g[idx] = (fp - fm) / (2 * h)
+    return g
+
+
+def test_backward_matches_finite_differences():
+    M, k, n, r, alpha = 3, 8, 6, 2, 5.0
+    x, W, A, B, G = _rand(M, k), _rand(n, k), _rand(r, k), _rand(n, r), _rand(M, n)
+    L = lambda: float(np.sum(G * ref.lora_fwd(x, W, A, B, alpha)))
+    dx, dA, dB = ref.lora_bwd(x, W, A, B, G, alpha)
+    for P, an in ((x, dx), (A, dA), (B, dB)):
+        num = _fd_grad(L, P)
+        np.testing.assert_allclose(an, num, rtol=1e-7, atol=1e-7)
+
+
+def test_qk_rope_backward_matches_finite_differences():
+    M, k, D, r, alpha, theta = 3, 8, 4, 2, 4.0, 100.0
+    nq, nk = 2 * D, D
+    x = _rand(M, k)
+    Wq, Aq, Bq = _rand(nq, k), _rand(r, k), _rand(nq, r)
+    Wk, Ak, Bk = _rand(nk, k), _rand(r, k), _rand(nk, r)
+    Gq, Gk = _rand(M, nq), _rand(M, nk)
+    pos = np.array([0, 3, 7])
+
+    def L():
+        q, kk = ref.qk_rope_fwd(x, Wq, Aq, Bq, Wk, Ak, Bk, alpha, pos, theta, head_dim=D)
+        return float(np.sum(Gq * q) + np.sum(Gk * kk))
+
+    dx, dAq, dBq, dAk, dBk = ref.qk_rope_bwd(x, Wq, Aq, Bq, Wk, Ak, Bk, Gq, Gk, alpha, pos,
+                                             theta, head_dim=D)
+    for P, an in ((x, dx), (Aq, dAq), (Bq, dBq), (Ak, dAk), (Bk, dBk)):
+        np.testing.assert_allclose(an, _fd_grad(L, P), rtol=1e-7, atol=1e-7)
+
+
+# --------------------------------------------------------------------------
+# RoPE
+# --------------------------------------------------------------------------
+D, THETA = 128, 500000.0
+
+
+def test_rope_position_zero_is_identity():
+    y = _rand(4, 2 * D)
+    np.testing.assert_array_equal(ref.rope_apply(y, np.zeros(4), D, THETA), y)
+
+
+def test_rope_preserves_pair_norms():
+    y = _rand(5, 3 * D)
+    pos = np.array([1, 17, 400, 8191, 3])
+    z = ref.rope_apply(y, pos, D, THETA)
+    h = D // 2
+    yn = y.reshape(5, 3, D)
+    zn = z.reshape(5, 3, D)
+    np.testing.assert_allclose(yn[..., :h] ** 2 + yn[..., h:] ** 2,
+                               zn[..., :h] ** 2 + zn[..., h:] ** 2, rtol=1e-12)
+
+
+def test_rope_relative_position():
+    """<R_m q, R_n k> depends only on m - n."""
+    q, k = _rand(1, D), _rand(1, D)
+    for m, n, t in ((5, 2, 100), (8191, 10, -7), (0, 0, 4000)):
+        a = ref.rope_apply(q, [m], D, THETA) @ ref.rope_apply(k, [n], D, THETA).T
+        b = ref.rope_apply(q, [m + t], D, THETA) @ ref.rope_apply(k, [n + t], D, THETA).T
+        assert abs(a.item() - b.item()) < 1e-9
+
+
+def test_rope_single_frequency_closed_form():
+    """A unit vector in pair (i, i+D/2) rotates by p·theta^(-2i/D)."""
+    for i in (0, 1, 31, 63):
+        for p in (1, 5, 1000, 8191):
+            y = np.zeros((1, D))
+            y[0, i] = 1.0
+            z = ref.rope_apply(y, [p], D, THETA)
+            phi = p * THETA ** (-2.0 * i / D)
+            assert abs(z[0, i] - math.cos(phi)) < 1e-12
+            assert abs(z[0, i + D // 2] - math.sin(phi)) < 1e-12
+            z[0, i] = z[0, i + D // 2] = 0.0
+            assert np.all(z == 0.0)
+
+
+def test_rope_inverse_is_transpose():
+    pos = np.array([0, 1, 2, 999])
+    y = _rand(4, 2 * D)
+    np.testing.assert_allclose(ref.rope_apply_inverse(ref.rope_apply(y, pos, D, THETA), pos, D,
+                                                      THETA), y, rtol=1e-12, atol=1e-12)
+    # <R y, z> == <y, R^T z>
+    z = _rand(4, 2 * D)
+    lhs = np.sum(ref.rope_apply(y, pos, D, THETA) * z)
+    rhs = np.sum(y * ref.rope_apply_inverse(z, pos, D, THETA))
+    assert abs(lhs - rhs) < 1e-9
+
+
+# --------------------------------------------------------------------------
+# NF4
+# --------------------------------------------------------------------------
+def test_nf4_codebook_matches_published_table():
+    pub = np.array([float(v[0]) for k, v in _golden_kv("nf4_codebook_qlora.txt").items()])
+    c = ref.nf4_codebook()
+    assert c.shape == (16,)
+    np.testing.assert_allclose(c, pub, rtol=0, atol=3e-7)
+    assert np.all(np.diff(c) > 0)
+    assert c[0] == -1.0 and c[7] == 0.0 and c[15] == 1.0
+
+
+def test_nf4_hand_example_packing():
+    g = _golden_kv("nf4_packing_example.txt")
+    w = np.zeros((1, 64))
+    w[0, :4] = [-2.0, 2.0, 0.0, 1.0]
+    codes, absmax = ref.nf4_quantize(w)
+    assert absmax[0, 0] == float(g["absmax"][0])
+    assert codes[0, 0] == int(g["byte0"][0], 16)
+    assert codes[0, 1] == int(g["byte1"][0], 16)
+    assert np.all(codes[0, 2:] == int(g["rest"][0], 16))
+
+
+def test_nf4_round_trip_on_levels():
+    c = ref.nf4_codebook()
+    a = 0.8125                             # a bf16 value
+    for decision in ("fp64", "fp32"):
+        idx = np.tile(np.arange(16), 4)      # 64 elements, every level
+        w = (c[idx] * a).reshape(1, 64)
+        w[0, 15] = a                         # keep the block's absmax exactly a
+        codes, absmax = ref.nf4_quantize(w, decision=decision)
+        assert absmax[0, 0] == a
+        np.testing.assert_array_equal(ref.nf4_unpack(codes)[0], idx)
+        np.testing.assert_array_equal(ref.nf4_dequant(codes, absmax), w)
+
+
+def test_nf4_absmax_element_maps_to_an_end():
+    w = _rand(8, 256)
+    w = ref.bf16_round(w)
+    codes, absmax = ref.nf4_quantize(w)
+    idx = ref.nf4_unpack(codes).reshape(8, 4, 64)
+    blocks = w.reshape(8, 4, 64)
+    for i in range(8):
+        for b in range(4):
+            j = int(np.argmax(np.abs(blocks[i, b])))
+            assert idx[i, b, j] == (15 if blocks[i, b, j] > 0 else 0)
+
+
+def test_nf4_zero_block_is_code_7():
+    w = np.zeros((2, 128))
+    w[1, 64:] = _rand(64)
+    codes, absmax = ref.nf4_quantize(w)
+    assert absmax[0, 0] == 0 and absmax[0, 1] == 0 and absmax[1, 0] == 0
+    idx = ref.nf4_unpack(codes)
+    assert np.all(idx[0] == 7) and np.all(idx[1, :64] == 7)
+
+
+@pytest.mark.parametrize("decision", ["fp64", "fp32"])
+def test_nf4_quantiser_is_brute_force_nearest(decision):
+    w = ref.bf16_round(_rand(3, 128, scale=0.05))
+    codes, absmax = ref.nf4_quantize(w, decision=decision)
+    idx = ref.nf4_unpack(codes)
+    c = ref.nf4_codebook()
+    for i in range(3):
+        for j in range(128):
+            a = absmax[i, j // 64]
+            if decision == "fp32":
+                ratio = np.float32(w[i, j]) / np.float32(a)
+                best, bestd = 0, None
+                for t in range(16):
+                    d = abs(ratio - np.float32(c[t]))
+                    if bestd is None or d < bestd:
+                        best, bestd = t, d
+            else:
+                ratio = w[i, j] / a
+                best = min(range(16), key=lambda t: (abs(ratio - c[t]), t))
+            assert idx[i, j] == best
+
+
+def test_nf4_dequant_error_bound():
+    """Dequantised weights are within half the widest level gap (times
+    absmax) of the originals."""
+    w = ref.bf16_round(_rand(4, 512, scale=0.02))
+    codes, absmax = ref.nf4_quantize(w)
+    wd = ref.nf4_dequant(codes, absmax)
+    gap = np.max(np.diff(ref.nf4_codebook())) / 2
+    bound = np.repeat(absmax, 64, axis=1) * gap
+    assert np.all(np.abs(wd - w) <= bound + 1e-15)
+
+
+def test_bf16_round_matches_torch():
+    v = rng.standard_normal(10000).astype(np.float32) * np.float32(10.0) ** rng.integers(
+        -30, 30, 10000).astype(np.float32)
+    mine = ref.bf16_round(v.astype(np.float64))
+    theirs = torch.tensor(v).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(mine, theirs)
+
+
+def test_param_count_closed_form():
+    """4096x4096 at rank 16: 2 x 4096 x 16 = 131072 trainable parameters
+    (the page's "约13万")."""
+    assert ref.lora_param_count(4096, 4096, 16) == 131072

@@ -1,0 +1,206 @@
+/*
+ * lora_b300.h — C ABI of the fused LoRA / QLoRA projection library for
+ * NVIDIA B300 (sm_103a).
+ *
+ * Sources of the operations (web pages about Unsloth, cited by title and
+ * section):
+ *   [P1] "UnSloth加速微调体验：在LoRA基础上再提速3倍的秘密":
+ *        算子融合 (y = Wx + BAx computed in one pass, no intermediate in HBM),
+ *        反向传播优化 (backward that recomputes Ax instead of caching it),
+ *        RoPE缓存集成 (RoPE from a contiguous cos/sin cache applied inside the
+ *        Q/K projection kernel).
+ *   [P3] "Unsloth教程：本地微调大模型速度提升数倍，显存节省60%":
+ *        显存优化策略 (QLoRA: frozen 4-bit NormalFloat4 base weight, only the
+ *        adapter is trained).
+ *   [QLoRA] Dettmers et al. 2023, §3 (the NF4 levels; the pages only name
+ *        the format).
+ *
+ * Conventions shared by every entry point
+ *   - Row-major, contiguous tensors: x [M,k], W [n,k] (out x in), A [r,k],
+ *     B [n,r], y and dY [M,n], dX [M,k], dA [r,k], dB [n,r].  The pages write
+ *     column vectors (y = Wx + BAx); this is the same map in row form.
+ *   - LoRA scale s = alpha / r multiplies the adapter branch.
+ *   - x, W (bf16 form), A, B, y, dY, dX are bfloat16; dA, dB are float32;
+ *     accumulation is float32 on the tensor cores; rounding to bf16 is
+ *     round-to-nearest-even.
+ *   - Every pointer is a DEVICE pointer owned by the caller, 16-byte
+ *     aligned.  The library allocates no memory and keeps no state between
+ *     calls other than a host-side cache of TMA descriptors keyed by pointer
+ *     and shape (safe to drop; it never dereferences stale pointers because
+ *     every key includes the pointer and extents passed in the call).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Argument errors are returned before anything is
+ *     launched.  LORA_ERR_CUDA reports a launch error seen immediately.
+ *   - Device-side failures (an internal pipeline wait that exceeded its
+ *     time limit, a position outside the RoPE cache) are recorded in a
+ *     32-bit status word at the start of the caller's workspace; read it
+ *     with lora_read_device_status() after the stream has finished.  The
+ *     word is sticky: it is only cleared by lora_clear_device_status().
+ *   - Shape limits: k % 64 == 0, n % 64 == 0, 1 <= M <= 2^30, r in
+ *     {8, 16, 32, 64}, head_dim == 128; NF4 needs blocksize == 64.
+ *   - Calls on the same workspace must not overlap on the GPU (use one
+ *     stream, or one workspace per stream).
+ */
+#ifndef LORA_B300_H
+#define LORA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st *lora_stream_t;
+
+typedef enum {
+  LORA_OK = 0,
+  LORA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad shape or value */
+  LORA_ERR_UNSUPPORTED = 2, /* valid request outside the supported limits  */
+  LORA_ERR_WORKSPACE = 3,   /* ws_bytes below lora_workspace_size()        */
+  LORA_ERR_ARCH = 4,        /* current device is not sm_103                */
+  LORA_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed           */
+  LORA_ERR_TIMEOUT = 6      /* device status: a pipeline wait timed out    */
+} lora_status_t;
+
+/* Bits of the device status word (see lora_read_device_status). */
+#define LORA_DEVSTAT_TIMEOUT 0x1u     /* an mbarrier wait exceeded its limit */
+#define LORA_DEVSTAT_BAD_POSITION 0x2u /* a RoPE position was outside [0,max_pos) */
+
+/* Base weight descriptor.
+ *   type == LORA_WEIGHT_BF16: w -> bf16 [n,k]; absmax NULL; blocksize ignored.
+ *   type == LORA_WEIGHT_NF4 : w -> uint8 codes [n, k/2] (byte j of a row holds
+ *     element 2j in the high nibble, 2j+1 in the low nibble); absmax -> bf16
+ *     [n, k/blocksize], the per-block scale; blocksize must be 64.  An element
+ *     decodes to level[code] * absmax with the 16 NF4 levels of [QLoRA]. */
+enum { LORA_WEIGHT_BF16 = 0, LORA_WEIGHT_NF4 = 1 };
+typedef struct {
+  int type;
+  const void *w;
+  const void *absmax;
+  int blocksize;
+} lora_weight_t;
+
+/* Operation ids for lora_workspace_size(). */
+enum {
+  LORA_OP_FWD = 0,
+  LORA_OP_BWD = 1,
+  LORA_OP_QK_ROPE_FWD = 2,
+  LORA_OP_QK_ROPE_BWD = 3
+};
+
+/* Bytes of workspace an operation needs (always >= 256: the status word
+ * lives at offset 0).  For the q/k operations pass k = hidden and
+ * n = (n_q_heads + n_kv_heads) * head_dim.  Returns 0 for an unknown op or
+ * out-of-range sizes.  Pure host function. */
+size_t lora_workspace_size(int op, int M, int k, int n, int r);
+
+/* Fused forward, [P1] 算子融合:  y = x·Wᵀ + s·(x·Aᵀ)·Bᵀ.
+ * One persistent kernel: per output tile the base GEMM x·Wᵀ and the rank-r
+ * down-projection v = x·Aᵀ accumulate in tensor memory, then (s·v)·Bᵀ is
+ * added to the same accumulator before the single bf16 store of y.  No
+ * intermediate goes to HBM.  An NF4 W is decoded tile by tile in shared
+ * memory ([P3] 显存优化策略).
+ *   x [M,k] bf16, W per lora_weight_t, A [r,k] bf16, B [n,r] bf16,
+ *   y [M,n] bf16 (overwritten).  ws: >= lora_workspace_size(LORA_OP_FWD,...). */
+lora_status_t lora_linear_fwd(const void *x, lora_weight_t W, const void *A,
+                              const void *B, void *y, int M, int k, int n,
+                              int r, float alpha, void *ws, size_t ws_bytes,
+                              lora_stream_t stream);
+
+/* Fused backward, [P1] 反向传播优化 (gradients derived from the forward; the
+ * page's printed formulas have a garbled operand order and no scale):
+ *   u  = dY·B                      (computed inside the dX kernel)
+ *   dX = dY·W + s·u·A              (accumulate_dx != 0: dX += that)
+ *   v  = x·Aᵀ                      (recomputed here, never cached)
+ *   dA = s·uᵀ·x,   dB = s·dYᵀ·v    (overwritten, float32)
+ * W is frozen: no weight gradient.  x [M,k], dy [M,n], dx [M,k] bf16;
+ * dA [r,k], dB [n,r] float32.  ws: >= lora_workspace_size(LORA_OP_BWD,...). */
+lora_status_t lora_linear_bwd(const void *x, lora_weight_t W, const void *A,
+                              const void *B, const void *dy, void *dx,
+                              int accumulate_dx, float *dA, float *dB, int M,
+                              int k, int n, int r, float alpha, void *ws,
+                              size_t ws_bytes, lora_stream_t stream);
+
+/* q/k projections with RoPE, [P1] RoPE缓存集成: q = R(pos)·(x·Wqᵀ + s·(x·Aqᵀ)·Bqᵀ)
+ * and the same for k, in ONE launch (both projections read the same x).
+ * The rotation is applied in the epilogue to each 128-wide head, pairing
+ * columns (i, i+64): y'[i] = y[i]·cos − y[i+64]·sin, y'[i+64] = y[i+64]·cos +
+ * y[i]·sin, angle = pos[m]·theta^(−2i/128).
+ *   x [M,hidden]; q [M, n_q_heads*128]; k_out [M, n_kv_heads*128] (bf16).
+ *   positions int32 [M], each in [0, max_pos).
+ *   cos_sin_cache float32 [max_pos, head_dim]: row p holds cos of the 64
+ *     angles then their sin (see lora_rope_cache_build).  If NULL the call
+ *     first builds it from rope_theta inside the workspace, which then needs
+ *     lora_rope_cache_bytes(max_pos, head_dim) more bytes. */
+lora_status_t lora_qk_rope_fwd(const void *x, lora_weight_t Wq, const void *Aq,
+                               const void *Bq, lora_weight_t Wk, const void *Ak,
+                               const void *Bk, void *q, void *k_out, int M,
+                               int hidden, int n_q_heads, int n_kv_heads,
+                               int head_dim, int r, float alpha,
+                               double rope_theta, const int32_t *positions,
+                               const float *cos_sin_cache, int max_pos,
+                               void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/* Backward of lora_qk_rope_fwd: the incoming dq, dk are rotated back by the
+ * transposed rotation R(pos)ᵀ, then each projection runs the backward of
+ * lora_linear_bwd; dX sums both projections (accumulate_dx != 0: dX += the
+ * sum).  dAq, dBq, dAk, dBk float32, overwritten.  Cache rules as in
+ * lora_qk_rope_fwd. */
+lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq,
+                               const void *Bq, lora_weight_t Wk, const void *Ak,
+                               const void *Bk, const void *dq, const void *dk,
+                               void *dx, int accumulate_dx, float *dAq,
+                               float *dBq, float *dAk, float *dBk, int M,
+                               int hidden, int n_q_heads, int n_kv_heads,
+                               int head_dim, int r, float alpha,
+                               double rope_theta, const int32_t *positions,
+                               const float *cos_sin_cache, int max_pos,
+                               void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/* Standalone NF4 dequantisation ([P3] 显存优化策略, [QLoRA] §3):
+ *   w_out[i,j] = bf16( level[code(i,j)] * absmax[i, j/64] ), product in fp32.
+ * codes uint8 [n, k/2], absmax bf16 [n, k/64], w_out bf16 [n,k]. */
+lora_status_t nf4_dequant(const uint8_t *codes, const void *absmax, void *w_out,
+                          int n, int k, int blocksize, lora_stream_t stream);
+
+/* NF4 quantisation of a bf16 W [n,k] (the inverse step of nf4_dequant):
+ * absmax = bf16(max|w|) per 64-block; code = index of the nearest level to
+ * w/absmax, decided in IEEE fp32 (ties to the lower index; an all-zero block
+ * is code 7).  Packing as in lora_weight_t. */
+lora_status_t nf4_quantize(const void *w, uint8_t *codes, void *absmax, int n,
+                           int k, int blocksize, lora_stream_t stream);
+
+/* Bytes of a cos/sin cache for max_pos positions. */
+size_t lora_rope_cache_bytes(int max_pos, int head_dim);
+
+/* Build the contiguous RoPE cache ([P1] RoPE缓存集成): cos_sin [max_pos,
+ * head_dim] float32, row p = cos(p·f_i) for i < head_dim/2, then sin(p·f_i),
+ * f_i = theta^(−2i/head_dim).  Angles and trigonometry in fp64, stored
+ * rounded to fp32. */
+lora_status_t lora_rope_cache_build(float *cos_sin, int max_pos, int head_dim,
+                                    double theta, lora_stream_t stream);
+
+/* Synchronise `stream`, then copy the device status word at the start of
+ * `ws` to *status_out (0 = no device-side failure).  Returns
+ * LORA_ERR_TIMEOUT if the timeout bit is set, else LORA_OK (or
+ * LORA_ERR_CUDA). */
+lora_status_t lora_read_device_status(const void *ws, uint32_t *status_out,
+                                      lora_stream_t stream);
+
+/* Zero the device status word (asynchronous on `stream`). */
+lora_status_t lora_clear_device_status(void *ws, lora_stream_t stream);
+
+/* Number of kernels this library has launched in the calling process
+ * (monotonic; a diagnostic for counting launches per step). */
+uint64_t lora_kernel_launch_count(void);
+
+/* Human-readable name of a status code. */
+const char *lora_status_string(lora_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_B300_H */

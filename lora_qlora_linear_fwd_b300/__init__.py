@@ -1,0 +1,210 @@
+"""Thin Python binding of the fused LoRA / QLoRA projection library.
+
+Each function here has the name of a C entry point of
+``include/lora_b300.h`` and only marshals arguments: shapes come from the
+tensors, pointers from ``tensor.data_ptr()``, the stream from torch's current
+stream.  All computation runs in the CUDA kernels of
+``_lib/liblora_b300.so``; there is no fallback.  Importing the package fails
+if the library has not been built (``python
+lora_qlora_linear_fwd_b300/build.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import lib_path
+
+__all__ = [
+    "LoraError", "Weight", "bf16_weight", "nf4_weight", "workspace", "workspace_size",
+    "lora_linear_fwd", "lora_linear_bwd", "lora_qk_rope_fwd", "lora_qk_rope_bwd",
+    "nf4_dequant", "nf4_quantize", "lora_rope_cache_build", "lora_rope_cache_bytes",
+    "lora_read_device_status", "lora_clear_device_status", "lora_status_string",
+    "lora_kernel_launch_count",
+    "OP_FWD", "OP_BWD", "OP_QK_ROPE_FWD", "OP_QK_ROPE_BWD", "EXPORTS", "library",
+]
+
+OP_FWD, OP_BWD, OP_QK_ROPE_FWD, OP_QK_ROPE_BWD = 0, 1, 2, 3
+WEIGHT_BF16, WEIGHT_NF4 = 0, 1
+STATUS_NAMES = ["LORA_OK", "LORA_ERR_INVALID_ARG", "LORA_ERR_UNSUPPORTED", "LORA_ERR_WORKSPACE",
+                "LORA_ERR_ARCH", "LORA_ERR_CUDA", "LORA_ERR_TIMEOUT"]
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"{where}: {name}")
+
+
+class Weight(ctypes.Structure):
+    """``lora_weight_t``."""
+    _fields_ = [("type", ctypes.c_int), ("w", ctypes.c_void_p), ("absmax", ctypes.c_void_p),
+                ("blocksize", ctypes.c_int)]
+
+
+_P, _I, _F, _D, _Z, _U32P = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double,
+                             ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint32))
+
+# name -> (restype, argtypes); mirrors include/lora_b300.h
+EXPORTS = {
+    "lora_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "lora_linear_fwd": (_I, [_P, Weight, _P, _P, _P, _I, _I, _I, _I, _F, _P, _Z, _P]),
+    "lora_linear_bwd": (_I, [_P, Weight, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _F, _P, _Z,
+                             _P]),
+    "lora_qk_rope_fwd": (_I, [_P, Weight, _P, _P, Weight, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                              _F, _D, _P, _P, _I, _P, _Z, _P]),
+    "lora_qk_rope_bwd": (_I, [_P, Weight, _P, _P, Weight, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
+                              _I, _I, _I, _I, _I, _I, _F, _D, _P, _P, _I, _P, _Z, _P]),
+    "nf4_dequant": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+    "nf4_quantize": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+    "lora_rope_cache_bytes": (_Z, [_I, _I]),
+    "lora_rope_cache_build": (_I, [_P, _I, _I, _D, _P]),
+    "lora_read_device_status": (_I, [_P, _U32P, _P]),
+    "lora_clear_device_status": (_I, [_P, _P]),
+    "lora_kernel_launch_count": (ctypes.c_uint64, []),
+    "lora_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+def _load():
+    path = lib_path()
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python "
+                          "lora_qlora_linear_fwd_b300/build.py` (no fallback exists)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in EXPORTS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+library = _load()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise LoraError(status, where)
+
+
+def bf16_weight(w: torch.Tensor) -> Weight:
+    return Weight(WEIGHT_BF16, w.data_ptr(), None, 0)
+
+
+def nf4_weight(codes: torch.Tensor, absmax: torch.Tensor, blocksize: int = 64) -> Weight:
+    return Weight(WEIGHT_NF4, codes.data_ptr(), absmax.data_ptr(), blocksize)
+
+
+def _weight(W) -> Weight:
+    return W if isinstance(W, Weight) else bf16_weight(W)
+
+
+def workspace_size(op: int, M: int, k: int, n: int, r: int) -> int:
+    return int(library.lora_workspace_size(op, M, k, n, r))
+
+
+def workspace(op: int, M: int, k: int, n: int, r: int, device="cuda", extra: int = 0):
+    """A zeroed workspace (status word cleared) of the size the op needs."""
+    nbytes = workspace_size(op, M, k, n, r)
+    if nbytes == 0:
+        raise LoraError(1, "lora_workspace_size")
+    return torch.zeros(nbytes + extra, dtype=torch.uint8, device=device)
+
+
+def lora_kernel_launch_count() -> int:
+    return int(library.lora_kernel_launch_count())
+
+
+def lora_status_string(s: int) -> str:
+    return library.lora_status_string(s).decode()
+
+
+def lora_linear_fwd(x, W, A, B, y, alpha: float, ws, stream=None):
+    M, k = x.shape
+    n, r = y.shape[1], A.shape[0]
+    _check(library.lora_linear_fwd(_ptr(x), _weight(W), _ptr(A), _ptr(B), _ptr(y), M, k, n, r,
+                                   float(alpha), _ptr(ws), ws.numel(), _stream(stream)),
+           "lora_linear_fwd")
+
+
+def lora_linear_bwd(x, W, A, B, dy, dx, dA, dB, alpha: float, ws, accumulate_dx: bool = False,
+                    stream=None):
+    M, k = x.shape
+    n, r = dy.shape[1], A.shape[0]
+    _check(library.lora_linear_bwd(_ptr(x), _weight(W), _ptr(A), _ptr(B), _ptr(dy), _ptr(dx),
+                                   int(bool(accumulate_dx)), _ptr(dA), _ptr(dB), M, k, n, r,
+                                   float(alpha), _ptr(ws), ws.numel(), _stream(stream)),
+           "lora_linear_bwd")
+
+
+def lora_qk_rope_fwd(x, Wq, Aq, Bq, Wk, Ak, Bk, q, k_out, alpha: float, rope_theta: float,
+                     positions, cos_sin_cache, max_pos: int, ws, head_dim: int = 128,
+                     stream=None):
+    M, hidden = x.shape
+    r = Aq.shape[0]
+    _check(library.lora_qk_rope_fwd(
+        _ptr(x), _weight(Wq), _ptr(Aq), _ptr(Bq), _weight(Wk), _ptr(Ak), _ptr(Bk), _ptr(q),
+        _ptr(k_out), M, hidden, q.shape[1] // head_dim, k_out.shape[1] // head_dim, head_dim, r,
+        float(alpha), float(rope_theta), _ptr(positions), _ptr(cos_sin_cache), int(max_pos),
+        _ptr(ws), ws.numel(), _stream(stream)), "lora_qk_rope_fwd")
+
+
+def lora_qk_rope_bwd(x, Wq, Aq, Bq, Wk, Ak, Bk, dq, dk, dx, dAq, dBq, dAk, dBk, alpha: float,
+                     rope_theta: float, positions, cos_sin_cache, max_pos: int, ws,
+                     head_dim: int = 128, accumulate_dx: bool = False, stream=None):
+    M, hidden = x.shape
+    r = Aq.shape[0]
+    _check(library.lora_qk_rope_bwd(
+        _ptr(x), _weight(Wq), _ptr(Aq), _ptr(Bq), _weight(Wk), _ptr(Ak), _ptr(Bk), _ptr(dq),
+        _ptr(dk), _ptr(dx), int(bool(accumulate_dx)), _ptr(dAq), _ptr(dBq), _ptr(dAk),
+        _ptr(dBk), M, hidden, dq.shape[1] // head_dim, dk.shape[1] // head_dim, head_dim, r,
+        float(alpha), float(rope_theta), _ptr(positions), _ptr(cos_sin_cache), int(max_pos),
+        _ptr(ws), ws.numel(), _stream(stream)), "lora_qk_rope_bwd")
+
+
+def nf4_dequant(codes, absmax, w_out, blocksize: int = 64, stream=None):
+    n, k = w_out.shape
+    _check(library.nf4_dequant(_ptr(codes), _ptr(absmax), _ptr(w_out), n, k, blocksize,
+                               _stream(stream)), "nf4_dequant")
+
+
+def nf4_quantize(w, codes, absmax, blocksize: int = 64, stream=None):
+    n, k = w.shape
+    _check(library.nf4_quantize(_ptr(w), _ptr(codes), _ptr(absmax), n, k, blocksize,
+                                _stream(stream)), "nf4_quantize")
+
+
+def lora_rope_cache_bytes(max_pos: int, head_dim: int = 128) -> int:
+    return int(library.lora_rope_cache_bytes(max_pos, head_dim))
+
+
+def lora_rope_cache_build(cos_sin, max_pos: int, head_dim: int, theta: float, stream=None):
+    _check(library.lora_rope_cache_build(_ptr(cos_sin), int(max_pos), int(head_dim),
+                                         float(theta), _stream(stream)), "lora_rope_cache_build")
+
+
+def lora_read_device_status(ws, stream=None) -> int:
+    out = ctypes.c_uint32(0)
+    s = library.lora_read_device_status(_ptr(ws), ctypes.byref(out), _stream(stream))
+    if s not in (0, 6):
+        raise LoraError(s, "lora_read_device_status")
+    return int(out.value)
+
+
+def lora_clear_device_status(ws, stream=None):
+    _check(library.lora_clear_device_status(_ptr(ws), _stream(stream)), "lora_clear_device_status")

@@ -1,0 +1,595 @@
+// C ABI of the library (declared in include/lora_b300.h): argument checks,
+// TMA descriptor encoding, workspace carving and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "lora_b300.h"
+
+using namespace lora;
+
+namespace lora {
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace lora
+
+namespace {
+
+// ------------------------------------------------------------- device info
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+lora_status_t device_info(DeviceInfo *out) {
+  static thread_local int cached_dev = -1;
+  static thread_local DeviceInfo cached;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+  if (dev != cached_dev) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return LORA_ERR_CUDA;
+    cached.sms = sms;
+    cached.ok = (major == 10 && minor == 3);
+    cached_dev = dev;
+  }
+  if (!cached.ok) return LORA_ERR_ARCH;
+  *out = cached;
+  return LORA_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+CUtensorMapSwizzle swizzle_for(int inner_bytes) {
+  switch (inner_bytes) {
+    case 128: return CU_TENSOR_MAP_SWIZZLE_128B;
+    case 64: return CU_TENSOR_MAP_SWIZZLE_64B;
+    case 32: return CU_TENSOR_MAP_SWIZZLE_32B;
+    default: return CU_TENSOR_MAP_SWIZZLE_NONE;
+  }
+}
+
+// 2-D map over a row-major matrix [outer, inner] with row pitch `pitch_bytes`.
+bool make_map(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *ptr, uint64_t inner,
+              uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+              bool swizzle) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw =
+      swizzle ? swizzle_for((int)(box_inner * esize)) : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return fn(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr CUtensorMapDataType kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+constexpr CUtensorMapDataType kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+
+// ---------------------------------------------------------------- checks
+bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int rank_pad(int r) { return r <= 16 ? 16 : (r <= 32 ? 32 : 64); }
+bool rank_ok(int r) { return r == 8 || r == 16 || r == 32 || r == 64; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr int kBN = 256;
+
+lora_status_t check_weight(const lora_weight_t &W, int n, int k) {
+  if (W.type == LORA_WEIGHT_BF16) {
+    if (!aligned16(W.w)) return LORA_ERR_INVALID_ARG;
+  } else if (W.type == LORA_WEIGHT_NF4) {
+    if (!aligned16(W.w) || !W.absmax || (reinterpret_cast<uintptr_t>(W.absmax) & 1u))
+      return LORA_ERR_INVALID_ARG;
+    if (W.blocksize != 64) return LORA_ERR_UNSUPPORTED;
+  } else {
+    return LORA_ERR_INVALID_ARG;
+  }
+  (void)n;
+  (void)k;
+  return LORA_OK;
+}
+
+lora_status_t check_shape(int M, int k, int n, int r) {
+  if (M < 1 || k < 1 || n < 1 || M > (1 << 30) || k > (1 << 20) || n > (1 << 20))
+    return LORA_ERR_INVALID_ARG;
+  if (k % 64 || n % 64) return LORA_ERR_UNSUPPORTED;
+  if (!rank_ok(r)) return LORA_ERR_UNSUPPORTED;
+  return LORA_OK;
+}
+
+// ------------------------------------------------------------- schedule
+Schedule pick_schedule(int m_blocks, int n_tiles, int sms, double rank_cost) {
+  Schedule best{1, 1, m_blocks, n_tiles};
+  double best_cost = 1e300;
+  for (int gm = 1; gm <= std::min(m_blocks, sms); ++gm) {
+    const int gn = std::min(n_tiles, sms / gm);
+    if (gn < 1) break;
+    const int per_m = (m_blocks + gm - 1) / gm;
+    const int per_n = (n_tiles + gn - 1) / gn;
+    const double cost = (double)per_m * per_n + per_m * rank_cost;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = Schedule{gm, gn, m_blocks, n_tiles};
+    }
+  }
+  return best;
+}
+
+// --------------------------------------------------------- workspace plan
+struct BwdPlan {
+  int rp, Mp;
+  int v_slices, v_chunks_per_slice;
+  int g_slices, g_chunks_per_slice;
+  size_t off_bt, off_ut_hi, off_ut_lo, off_vt_hi, off_vt_lo, off_part_v, off_part_a,
+      off_part_b, total;
+};
+
+void plan_slices(int tiles, int chunks, int target, int *slices, int *per) {
+  int s = std::max(1, std::min(chunks, (target + tiles - 1) / tiles));
+  int cps = (chunks + s - 1) / s;
+  s = (chunks + cps - 1) / cps;  // no empty slice
+  *slices = s;
+  *per = cps;
+}
+
+BwdPlan plan_bwd(int M, int k, int n, int r, size_t start) {
+  BwdPlan b{};
+  b.rp = rank_pad(r);
+  b.Mp = (M + 63) & ~63;
+  const int target = 2 * 148;
+  plan_slices((M + 127) / 128, k / 64, target, &b.v_slices, &b.v_chunks_per_slice);
+  plan_slices((k + 127) / 128 + (n + 127) / 128, (M + 63) / 64, target, &b.g_slices,
+              &b.g_chunks_per_slice);
+  size_t o = align256(start);
+  b.off_bt = o;       o = align256(o + (size_t)r * n * 2);
+  b.off_ut_hi = o;    o = align256(o + (size_t)b.rp * b.Mp * 2);
+  b.off_ut_lo = o;    o = align256(o + (size_t)b.rp * b.Mp * 2);
+  b.off_vt_hi = o;    o = align256(o + (size_t)b.rp * b.Mp * 2);
+  b.off_vt_lo = o;    o = align256(o + (size_t)b.rp * b.Mp * 2);
+  b.off_part_v = o;   o = align256(o + (size_t)b.v_slices * M * b.rp * 4);
+  b.off_part_a = o;   o = align256(o + (size_t)b.g_slices * k * b.rp * 4);
+  b.off_part_b = o;   o = align256(o + (size_t)b.g_slices * n * b.rp * 4);
+  b.total = o;
+  return b;
+}
+
+constexpr size_t kStatusBytes = 256;
+
+lora_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+// ------------------------------------------------------ fused GEMM set-up
+struct GroupArgs {
+  lora_weight_t W;
+  const void *r1;  // FWD: A [r,k]; DX: Bt [r,n]
+  const void *r2;  // FWD: B [n,r]; DX: A [r,k]
+  void *out;
+  int ncols;       // output columns
+};
+
+// FWD: act = x [M, k], W [n, k]; DX: act = dY [M, n], W [n, k] read MN-major.
+lora_status_t run_gemm(int mode, const void *act, int M, int Kred, const GroupArgs *ga, int ng,
+                       int r, float alpha, bool rope, const int32_t *positions,
+                       const float *cos_sin, int max_pos, void *ut_hi, void *ut_lo,
+                       int accumulate, uint32_t *status, cudaStream_t st) {
+  DeviceInfo di;
+  lora_status_t s = device_info(&di);
+  if (s != LORA_OK) return s;
+  const int rp = rank_pad(r);
+  const bool nf4 = ga[0].W.type == LORA_WEIGHT_NF4;
+  const bool dx = mode == kModeDx;
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  // activation: [M, Kred] K-major, box 64 x 128
+  if (!make_map(&p.tm_act, kBF16, 2, act, Kred, M, (uint64_t)Kred * 2, 64, 128, true))
+    return LORA_ERR_CUDA;
+  int tiles = 0;
+  for (int g = 0; g < ng; ++g) {
+    GemmGroup &G = p.grp[g];
+    const GroupArgs &a = ga[g];
+    const int ncols = a.ncols;
+    if (!dx) {
+      const int n = ncols, k = Kred;
+      if (nf4) {
+        if (!make_map(&G.tm_w, kU8, 1, a.W.w, k / 2, n, (uint64_t)k / 2, 32, kBN, false))
+          return LORA_ERR_CUDA;
+      } else if (!make_map(&G.tm_w, kBF16, 2, a.W.w, k, n, (uint64_t)k * 2, 64, kBN, true)) {
+        return LORA_ERR_CUDA;
+      }
+      if (!make_map(&G.tm_r1, kBF16, 2, a.r1, k, r, (uint64_t)k * 2, 64, rp, true) ||
+          !make_map(&G.tm_r2, kBF16, 2, a.r2, r, n, (uint64_t)r * 2, rp, kBN, true))
+        return LORA_ERR_CUDA;
+      G.ld_absmax = k / 64;
+    } else {
+      const int n = Kred, k = ncols;
+      if (nf4) {
+        if (!make_map(&G.tm_w, kU8, 1, a.W.w, k / 2, n, (uint64_t)k / 2, kBN / 2, 64, false))
+          return LORA_ERR_CUDA;
+      } else if (!make_map(&G.tm_w, kBF16, 2, a.W.w, k, n, (uint64_t)k * 2, 64, 64, true)) {
+        return LORA_ERR_CUDA;
+      }
+      if (!make_map(&G.tm_r1, kBF16, 2, a.r1, n, r, (uint64_t)n * 2, 64, rp, true) ||
+          !make_map(&G.tm_r2, kBF16, 2, a.r2, k, r, (uint64_t)k * 2, 64, rp, true))
+        return LORA_ERR_CUDA;
+      G.ld_absmax = k / 64;
+    }
+    G.out = static_cast<__nv_bfloat16 *>(a.out);
+    G.absmax = static_cast<const __nv_bfloat16 *>(a.W.absmax);
+    G.ncols = ncols;
+    G.n_tiles = (ncols + kBN - 1) / kBN;
+    G.tile_begin = tiles;
+    tiles += G.n_tiles;
+  }
+  p.num_groups = ng;
+  p.M = M;
+  p.K = Kred;
+  p.scale = alpha / (float)r;
+  const int m_blocks = (M + 127) / 128;
+  p.sched = pick_schedule(m_blocks, tiles, di.sms, (double)rp / kBN + 0.02);
+  p.ut_hi = static_cast<__nv_bfloat16 *>(ut_hi);
+  p.ut_lo = static_cast<__nv_bfloat16 *>(ut_lo);
+  p.accumulate = accumulate;
+  p.positions = positions;
+  p.cos_sin = cos_sin;
+  p.max_pos = max_pos;
+  p.status = status;
+  const int grid = p.sched.gm * p.sched.gn;
+  return cuda_status(launch_gemm(p, mode, rp, rope, nf4, grid, st));
+}
+
+// Backward of one projection.  dy [M, n] (already un-rotated for q/k).
+lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void *B,
+                      const void *dy, void *dx, int accumulate, float *dA, float *dB, int M,
+                      int k, int n, int r, float alpha, uint8_t *ws, size_t plan_start,
+                      uint32_t *status, cudaStream_t st) {
+  const BwdPlan b = plan_bwd(M, k, n, r, plan_start);
+  auto *Bt = reinterpret_cast<__nv_bfloat16 *>(ws + b.off_bt);
+  auto *ut_hi = reinterpret_cast<__nv_bfloat16 *>(ws + b.off_ut_hi);
+  auto *ut_lo = reinterpret_cast<__nv_bfloat16 *>(ws + b.off_ut_lo);
+  auto *vt_hi = reinterpret_cast<__nv_bfloat16 *>(ws + b.off_vt_hi);
+  auto *vt_lo = reinterpret_cast<__nv_bfloat16 *>(ws + b.off_vt_lo);
+  auto *part_v = reinterpret_cast<float *>(ws + b.off_part_v);
+  auto *part_a = reinterpret_cast<float *>(ws + b.off_part_a);
+  auto *part_b = reinterpret_cast<float *>(ws + b.off_part_b);
+  const float scale = alpha / (float)r;
+  lora_status_t s;
+
+  // (1) Bᵀ for the u = dY·B operand
+  if ((s = cuda_status(launch_transpose_rank(static_cast<const __nv_bfloat16 *>(B), Bt, n, r, st))))
+    return s;
+  // (2) dX = dY·W + s·(dY·B)·A, exporting uᵀ = (dY·B)ᵀ as bf16 hi+lo
+  GroupArgs ga{W, Bt, A, dx, k};
+  if ((s = run_gemm(kModeDx, dy, M, n, &ga, 1, r, alpha, false, nullptr, nullptr, 0, ut_hi,
+                    ut_lo, accumulate, status, st)))
+    return s;
+  // (3) v = x·Aᵀ, recomputed (split over k), then hi/lo split and transpose
+  {
+    SkinnyParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    SkinnyProblem &P = sp.pr[0];
+    if (!make_map(&P.tm_p, kBF16, 2, x, k, M, (uint64_t)k * 2, 64, 128, true) ||
+        !make_map(&P.tm_q_hi, kBF16, 2, A, k, r, (uint64_t)k * 2, 64, b.rp, true))
+      return LORA_ERR_CUDA;
+    P.tm_q_lo = P.tm_q_hi;
+    P.part = part_v;
+    P.rows = M;
+    P.red = k;
+    P.row_tiles = (M + 127) / 128;
+    P.slices = b.v_slices;
+    P.chunks_per_slice = b.v_chunks_per_slice;
+    P.cta_begin = 0;
+    sp.num_problems = 1;
+    sp.status = status;
+    if ((s = cuda_status(launch_skinny(sp, false, b.rp, P.row_tiles * P.slices, st)))) return s;
+    if ((s = cuda_status(launch_v_finalize(part_v, b.v_slices, M, b.rp, vt_hi, vt_lo, st))))
+      return s;
+  }
+  // (4) dA = s·uᵀ·x and dB = s·dYᵀ·v, reduced over tokens (one launch)
+  {
+    SkinnyParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    SkinnyProblem &PA = sp.pr[0];
+    SkinnyProblem &PB = sp.pr[1];
+    if (!make_map(&PA.tm_p, kBF16, 2, x, k, M, (uint64_t)k * 2, 64, 64, true) ||
+        !make_map(&PA.tm_q_hi, kBF16, 2, ut_hi, M, b.rp, (uint64_t)b.Mp * 2, 64, b.rp, true) ||
+        !make_map(&PA.tm_q_lo, kBF16, 2, ut_lo, M, b.rp, (uint64_t)b.Mp * 2, 64, b.rp, true) ||
+        !make_map(&PB.tm_p, kBF16, 2, dy, n, M, (uint64_t)n * 2, 64, 64, true) ||
+        !make_map(&PB.tm_q_hi, kBF16, 2, vt_hi, M, b.rp, (uint64_t)b.Mp * 2, 64, b.rp, true) ||
+        !make_map(&PB.tm_q_lo, kBF16, 2, vt_lo, M, b.rp, (uint64_t)b.Mp * 2, 64, b.rp, true))
+      return LORA_ERR_CUDA;
+    PA.part = part_a;
+    PA.rows = k;
+    PA.red = M;
+    PA.row_tiles = (k + 127) / 128;
+    PA.slices = b.g_slices;
+    PA.chunks_per_slice = b.g_chunks_per_slice;
+    PA.cta_begin = 0;
+    PB.part = part_b;
+    PB.rows = n;
+    PB.red = M;
+    PB.row_tiles = (n + 127) / 128;
+    PB.slices = b.g_slices;
+    PB.chunks_per_slice = b.g_chunks_per_slice;
+    PB.cta_begin = PA.row_tiles * PA.slices;
+    sp.num_problems = 2;
+    sp.status = status;
+    const int grid = PB.cta_begin + PB.row_tiles * PB.slices;
+    if ((s = cuda_status(launch_skinny(sp, true, b.rp, grid, st)))) return s;
+    if ((s = cuda_status(launch_grad_finalize(part_a, b.g_slices, k, b.rp, r, scale, true, dA, st))))
+      return s;
+    if ((s = cuda_status(launch_grad_finalize(part_b, b.g_slices, n, b.rp, r, scale, false, dB, st))))
+      return s;
+  }
+  return LORA_OK;
+}
+
+size_t bwd_bytes(int M, int k, int n, int r) { return plan_bwd(M, k, n, r, 0).total; }
+
+// Largest backward area over every projection width n' <= n (multiple of 64):
+// the q/k backward runs each projection in the same area.
+size_t bwd_bytes_upto(int M, int k, int n, int r) {
+  size_t best = 0;
+  for (int np = 64; np <= n; np += 64) best = std::max(best, bwd_bytes(M, k, np, r));
+  return best;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+uint64_t lora_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *lora_status_string(lora_status_t s) {
+  switch (s) {
+    case LORA_OK: return "LORA_OK";
+    case LORA_ERR_INVALID_ARG: return "LORA_ERR_INVALID_ARG";
+    case LORA_ERR_UNSUPPORTED: return "LORA_ERR_UNSUPPORTED";
+    case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE";
+    case LORA_ERR_ARCH: return "LORA_ERR_ARCH";
+    case LORA_ERR_CUDA: return "LORA_ERR_CUDA";
+    case LORA_ERR_TIMEOUT: return "LORA_ERR_TIMEOUT";
+  }
+  return "LORA_ERR_UNKNOWN";
+}
+
+size_t lora_workspace_size(int op, int M, int k, int n, int r) {
+  if (M < 1 || k < 1 || n < 1 || !rank_ok(r) || M > (1 << 30)) return 0;
+  switch (op) {
+    case LORA_OP_FWD:
+    case LORA_OP_QK_ROPE_FWD:
+      return kStatusBytes;
+    case LORA_OP_BWD:
+      return kStatusBytes + bwd_bytes(M, k, n, r);
+    case LORA_OP_QK_ROPE_BWD:
+      // rotated dq|dk, then the per-projection backward area (reused by q and k)
+      if (n % 64) return 0;
+      return align256(kStatusBytes + (size_t)M * n * 2) + bwd_bytes_upto(M, k, n, r);
+  }
+  return 0;
+}
+
+size_t lora_rope_cache_bytes(int max_pos, int head_dim) {
+  if (max_pos < 1 || head_dim < 2) return 0;
+  return align256((size_t)max_pos * head_dim * 4);
+}
+
+lora_status_t lora_linear_fwd(const void *x, lora_weight_t W, const void *A, const void *B,
+                              void *y, int M, int k, int n, int r, float alpha, void *ws,
+                              size_t ws_bytes, lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = check_shape(M, k, n, r))) return s;
+  if ((s = check_weight(W, n, k))) return s;
+  if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(y) || !aligned16(ws))
+    return LORA_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha)) return LORA_ERR_INVALID_ARG;
+  if (ws_bytes < lora_workspace_size(LORA_OP_FWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
+  GroupArgs ga{W, A, B, y, n};
+  return run_gemm(kModeFwd, x, M, k, &ga, 1, r, alpha, false, nullptr, nullptr, 0, nullptr,
+                  nullptr, 0, static_cast<uint32_t *>(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
+lora_status_t lora_linear_bwd(const void *x, lora_weight_t W, const void *A, const void *B,
+                              const void *dy, void *dx, int accumulate_dx, float *dA, float *dB,
+                              int M, int k, int n, int r, float alpha, void *ws, size_t ws_bytes,
+                              lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = check_shape(M, k, n, r))) return s;
+  if ((s = check_weight(W, n, k))) return s;
+  if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(dy) || !aligned16(dx) ||
+      !aligned16(dA) || !aligned16(dB) || !aligned16(ws))
+    return LORA_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha)) return LORA_ERR_INVALID_ARG;
+  if (ws_bytes < lora_workspace_size(LORA_OP_BWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
+  DeviceInfo di;
+  if ((s = device_info(&di))) return s;
+  return run_bwd(x, W, A, B, dy, dx, accumulate_dx, dA, dB, M, k, n, r, alpha,
+                 static_cast<uint8_t *>(ws), kStatusBytes, static_cast<uint32_t *>(ws),
+                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+static lora_status_t check_qk(const void *x, lora_weight_t Wq, const void *Aq, const void *Bq,
+                              lora_weight_t Wk, const void *Ak, const void *Bk, int M, int hidden,
+                              int nqh, int nkh, int head_dim, int r, float alpha,
+                              const int32_t *positions, const float *cache, int max_pos,
+                              double theta, void *ws) {
+  lora_status_t s;
+  if (head_dim != 128) return LORA_ERR_UNSUPPORTED;
+  if (nqh < 1 || nkh < 1 || nqh > 4096 || nkh > 4096 || max_pos < 1) return LORA_ERR_INVALID_ARG;
+  if ((s = check_shape(M, hidden, nqh * head_dim, r))) return s;
+  if ((s = check_weight(Wq, nqh * head_dim, hidden))) return s;
+  if ((s = check_weight(Wk, nkh * head_dim, hidden))) return s;
+  if (Wq.type != Wk.type) return LORA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(Aq) || !aligned16(Bq) || !aligned16(Ak) || !aligned16(Bk) ||
+      !aligned16(ws) || !positions || (reinterpret_cast<uintptr_t>(positions) & 3u))
+    return LORA_ERR_INVALID_ARG;
+  if (cache && !aligned16(cache)) return LORA_ERR_INVALID_ARG;
+  if (!cache && !(theta > 0.0 && std::isfinite(theta))) return LORA_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha)) return LORA_ERR_INVALID_ARG;
+  return LORA_OK;
+}
+
+lora_status_t lora_qk_rope_fwd(const void *x, lora_weight_t Wq, const void *Aq, const void *Bq,
+                               lora_weight_t Wk, const void *Ak, const void *Bk, void *q,
+                               void *k_out, int M, int hidden, int n_q_heads, int n_kv_heads,
+                               int head_dim, int r, float alpha, double rope_theta,
+                               const int32_t *positions, const float *cos_sin_cache, int max_pos,
+                               void *ws, size_t ws_bytes, lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = check_qk(x, Wq, Aq, Bq, Wk, Ak, Bk, M, hidden, n_q_heads, n_kv_heads, head_dim, r,
+                    alpha, positions, cos_sin_cache, max_pos, rope_theta, ws)))
+    return s;
+  if (!aligned16(q) || !aligned16(k_out)) return LORA_ERR_INVALID_ARG;
+  const int nq = n_q_heads * head_dim, nk = n_kv_heads * head_dim;
+  size_t need = lora_workspace_size(LORA_OP_QK_ROPE_FWD, M, hidden, nq + nk, r);
+  const size_t cache_off = align256(need);
+  if (!cos_sin_cache) need = cache_off + lora_rope_cache_bytes(max_pos, head_dim);
+  if (ws_bytes < need) return LORA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DeviceInfo di;
+  if ((s = device_info(&di))) return s;
+  const float *cache = cos_sin_cache;
+  if (!cache) {
+    float *c = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + cache_off);
+    if ((s = cuda_status(launch_rope_cache(c, max_pos, head_dim, rope_theta, st)))) return s;
+    cache = c;
+  }
+  GroupArgs ga[2] = {{Wq, Aq, Bq, q, nq}, {Wk, Ak, Bk, k_out, nk}};
+  return run_gemm(kModeFwd, x, M, hidden, ga, 2, r, alpha, true, positions, cache,
+                  max_pos, nullptr, nullptr, 0, static_cast<uint32_t *>(ws), st);
+}
+
+lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq, const void *Bq,
+                               lora_weight_t Wk, const void *Ak, const void *Bk, const void *dq,
+                               const void *dk, void *dx, int accumulate_dx, float *dAq,
+                               float *dBq, float *dAk, float *dBk, int M, int hidden,
+                               int n_q_heads, int n_kv_heads, int head_dim, int r, float alpha,
+                               double rope_theta, const int32_t *positions,
+                               const float *cos_sin_cache, int max_pos, void *ws,
+                               size_t ws_bytes, lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = check_qk(x, Wq, Aq, Bq, Wk, Ak, Bk, M, hidden, n_q_heads, n_kv_heads, head_dim, r,
+                    alpha, positions, cos_sin_cache, max_pos, rope_theta, ws)))
+    return s;
+  if (!aligned16(dq) || !aligned16(dk) || !aligned16(dx) || !aligned16(dAq) || !aligned16(dBq) ||
+      !aligned16(dAk) || !aligned16(dBk))
+    return LORA_ERR_INVALID_ARG;
+  const int nq = n_q_heads * head_dim, nk = n_kv_heads * head_dim;
+  size_t need = lora_workspace_size(LORA_OP_QK_ROPE_BWD, M, hidden, nq + nk, r);
+  const size_t cache_off = align256(need);
+  if (!cos_sin_cache) need = cache_off + lora_rope_cache_bytes(max_pos, head_dim);
+  if (ws_bytes < need) return LORA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DeviceInfo di;
+  if ((s = device_info(&di))) return s;
+  uint8_t *w8 = static_cast<uint8_t *>(ws);
+  uint32_t *status = static_cast<uint32_t *>(ws);
+  const float *cache = cos_sin_cache;
+  if (!cache) {
+    float *c = reinterpret_cast<float *>(w8 + cache_off);
+    if ((s = cuda_status(launch_rope_cache(c, max_pos, head_dim, rope_theta, st)))) return s;
+    cache = c;
+  }
+  auto *dq_pre = reinterpret_cast<__nv_bfloat16 *>(w8 + kStatusBytes);
+  auto *dk_pre = dq_pre + (size_t)M * nq;
+  if ((s = cuda_status(launch_rope_bwd(static_cast<const __nv_bfloat16 *>(dq), dq_pre, M, nq,
+                                       positions, cache, max_pos, status, st))))
+    return s;
+  if ((s = cuda_status(launch_rope_bwd(static_cast<const __nv_bfloat16 *>(dk), dk_pre, M, nk,
+                                       positions, cache, max_pos, status, st))))
+    return s;
+  const size_t area = align256(kStatusBytes + (size_t)M * (nq + nk) * 2);
+  if ((s = run_bwd(x, Wq, Aq, Bq, dq_pre, dx, accumulate_dx, dAq, dBq, M, hidden, nq, r, alpha,
+                   w8, area, status, st)))
+    return s;
+  return run_bwd(x, Wk, Ak, Bk, dk_pre, dx, 1, dAk, dBk, M, hidden, nk, r, alpha, w8, area,
+                 status, st);
+}
+
+lora_status_t nf4_dequant(const uint8_t *codes, const void *absmax, void *w_out, int n, int k,
+                          int blocksize, lora_stream_t stream) {
+  if (blocksize != 64) return LORA_ERR_UNSUPPORTED;
+  if (n < 1 || k < 1 || k % 64) return LORA_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !absmax || (reinterpret_cast<uintptr_t>(absmax) & 1u) ||
+      !aligned16(w_out))
+    return LORA_ERR_INVALID_ARG;
+  DeviceInfo di;
+  lora_status_t s;
+  if ((s = device_info(&di))) return s;
+  return cuda_status(launch_nf4_dequant(codes, static_cast<const __nv_bfloat16 *>(absmax),
+                                        static_cast<__nv_bfloat16 *>(w_out), n, k,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t nf4_quantize(const void *w, uint8_t *codes, void *absmax, int n, int k,
+                           int blocksize, lora_stream_t stream) {
+  if (blocksize != 64) return LORA_ERR_UNSUPPORTED;
+  if (n < 1 || k < 1 || k % 64) return LORA_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(codes) || !absmax ||
+      (reinterpret_cast<uintptr_t>(absmax) & 1u))
+    return LORA_ERR_INVALID_ARG;
+  DeviceInfo di;
+  lora_status_t s;
+  if ((s = device_info(&di))) return s;
+  return cuda_status(launch_nf4_quantize(static_cast<const __nv_bfloat16 *>(w), codes,
+                                         static_cast<__nv_bfloat16 *>(absmax), n, k,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_rope_cache_build(float *cos_sin, int max_pos, int head_dim, double theta,
+                                    lora_stream_t stream) {
+  if (!aligned16(cos_sin) || max_pos < 1 || head_dim < 2 || head_dim % 2 ||
+      !(theta > 0.0 && std::isfinite(theta)))
+    return LORA_ERR_INVALID_ARG;
+  DeviceInfo di;
+  lora_status_t s;
+  if ((s = device_info(&di))) return s;
+  return cuda_status(
+      launch_rope_cache(cos_sin, max_pos, head_dim, theta, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_read_device_status(const void *ws, uint32_t *status_out, lora_stream_t stream) {
+  if (!ws || !status_out) return LORA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return LORA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return LORA_ERR_CUDA;
+  *status_out = v;
+  return (v & kDevTimeout) ? LORA_ERR_TIMEOUT : LORA_OK;
+}
+
+lora_status_t lora_clear_device_status(void *ws, lora_stream_t stream) {
+  if (!ws) return LORA_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+// Internal interface between the C-ABI host code (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace lora {
+
+// One projection inside a fused GEMM launch.
+//   FWD mode: W [n,k] bf16 (K-major operand), r1 = A [r,k] (down-projection
+//             operand), r2 = B [n,r] (up-projection operand), out = y [M,n].
+//   DX  mode: W [n,k] bf16 read as an MN-major operand (dY·W), r1 = Bᵀ [r,n]
+//             (u = dY·B), r2 = A [r,k] read MN-major (s·u·A), out = dX [M,k].
+// NF4 weights: tm_w maps the codes [n, k/2] bytes and absmax points at the
+// bf16 block scales [n, k/64].
+struct alignas(64) GemmGroup {
+  CUtensorMap tm_w;
+  CUtensorMap tm_r1;
+  CUtensorMap tm_r2;
+  __nv_bfloat16 *out;
+  const __nv_bfloat16 *absmax;
+  int ncols;       // output columns of this group (n in FWD, k in DX)
+  int n_tiles;     // ceil(ncols / 256)
+  int tile_begin;  // first global n-tile index of this group
+  int ld_absmax;   // k / 64 (NF4)
+};
+
+struct alignas(64) GemmParams {
+  CUtensorMap tm_act;  // x [M,k] (FWD) or dY [M,n] (DX): K-major, box 64 x 128
+  GemmGroup grp[kMaxGroups];
+  int num_groups;
+  int M;
+  int K;          // reduction length: k (FWD) or n (DX)
+  float scale;    // s = alpha / r
+  Schedule sched;
+  // DX mode
+  __nv_bfloat16 *ut_hi;  // uᵀ [RP, M] high bf16 part (unscaled), written once per m-block
+  __nv_bfloat16 *ut_lo;  // uᵀ low part: u - hi
+  int accumulate;        // dX += result instead of overwrite
+  // RoPE epilogue (FWD mode)
+  const int32_t *positions;
+  const float *cos_sin;
+  int max_pos;
+  uint32_t *status;
+};
+
+enum GemmMode { kModeFwd = 0, kModeDx = 1 };
+
+// Count of kernel launches issued by the library (see lora_kernel_launch_count).
+void note_launch();
+
+cudaError_t launch_gemm(const GemmParams &p, int mode, int rp, bool rope, bool nf4, int grid,
+                        cudaStream_t st);
+int gemm_smem_bytes(int mode, int rp, bool nf4);
+
+// Skinny rank-r GEMMs on the tensor cores (fp32 partial sums per K-slice):
+//   KMAJOR  (v):     part[s][t][j]  = Σ_{c in slice s} P[t,c]·Q[j,c]   P = x [T,k]
+//   MNMAJOR (dA,dB): part[s][o][j]  = Σ_{t in slice s} P[t,o]·(Qhi+Qlo)[j,t]
+struct alignas(64) SkinnyProblem {
+  CUtensorMap tm_p;
+  CUtensorMap tm_q_hi;
+  CUtensorMap tm_q_lo;
+  float *part;     // [slices, rows, RP]
+  int rows;        // output rows (T for KMAJOR, Mo for MNMAJOR)
+  int red;         // reduction length
+  int row_tiles;   // ceil(rows / 128)
+  int slices;
+  int chunks_per_slice;  // 64-wide reduction chunks per slice
+  int cta_begin;   // first CTA index of this problem
+};
+
+struct alignas(64) SkinnyParams {
+  SkinnyProblem pr[2];
+  int num_problems;
+  uint32_t *status;
+};
+
+cudaError_t launch_skinny(const SkinnyParams &p, bool mn_major, int rp, int grid, cudaStream_t st);
+
+// Elementwise / small helpers.
+cudaError_t launch_transpose_rank(const __nv_bfloat16 *B, __nv_bfloat16 *Bt, int n, int r,
+                                  cudaStream_t st);
+cudaError_t launch_v_finalize(const float *part, int slices, int T, int rp, __nv_bfloat16 *vt_hi,
+                              __nv_bfloat16 *vt_lo, cudaStream_t st);
+cudaError_t launch_grad_finalize(const float *part, int slices, int rows, int rp, int r,
+                                 float scale, bool transpose_out, float *out, cudaStream_t st);
+cudaError_t launch_rope_bwd(const __nv_bfloat16 *dy, __nv_bfloat16 *out, int M, int ncols,
+                            const int32_t *pos, const float *cos_sin, int max_pos,
+                            uint32_t *status, cudaStream_t st);
+cudaError_t launch_rope_cache(float *cos_sin, int max_pos, int head_dim, double theta,
+                              cudaStream_t st);
+cudaError_t launch_nf4_dequant(const uint8_t *codes, const __nv_bfloat16 *absmax,
+                               __nv_bfloat16 *w, int n, int k, cudaStream_t st);
+cudaError_t launch_nf4_quantize(const __nv_bfloat16 *w, uint8_t *codes, __nv_bfloat16 *absmax,
+                                int n, int k, cudaStream_t st);
+
+}  // namespace lora

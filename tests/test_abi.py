@@ -1,0 +1,116 @@
+"""C-ABI boundary tests that need no GPU: the library loads, exports every
+function the public header declares, and rejects bad arguments before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import lora_qlora_linear_fwd_b300 as L
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "lora_b300.h")
+lib = L.library
+FAKE = 0x10000          # 16-byte aligned, never dereferenced by these calls
+MIS = 0x10008           # 8-byte aligned only
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for must in ("lora_linear_fwd", "lora_linear_bwd", "lora_qk_rope_fwd", "lora_qk_rope_bwd",
+                 "nf4_dequant", "lora_workspace_size", "lora_rope_cache_build",
+                 "lora_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(L.EXPORTS)
+
+
+def test_status_strings():
+    for i, name in enumerate(L.STATUS_NAMES):
+        assert L.lora_status_string(i) == name
+    assert L.lora_status_string(99) == "LORA_ERR_UNKNOWN"
+
+
+def test_workspace_sizes():
+    assert L.workspace_size(L.OP_FWD, 256, 512, 512, 8) == 256
+    b = L.workspace_size(L.OP_BWD, 256, 512, 512, 8)
+    assert b > 256 and b % 256 == 0
+    assert L.workspace_size(L.OP_BWD, 8192, 4096, 4096, 64) > L.workspace_size(
+        L.OP_BWD, 4096, 4096, 4096, 64)
+    qk = L.workspace_size(L.OP_QK_ROPE_BWD, 8192, 4096, 5120, 64)
+    assert qk >= 256 + 8192 * 5120 * 2
+    for bad in ((L.OP_FWD, 0, 64, 64, 8), (L.OP_FWD, 64, 64, 64, 12), (9, 64, 64, 64, 8)):
+        assert L.workspace_size(*bad) == 0
+    assert L.lora_rope_cache_bytes(8192, 128) == 8192 * 128 * 4
+
+
+def _w(ptr=FAKE, typ=0, absmax=None, bs=0):
+    return L.Weight(typ, ptr, absmax, bs)
+
+
+def _fwd(M=256, k=512, n=512, r=8, x=FAKE, W=None, A=FAKE, B=FAKE, y=FAKE, ws=FAKE, wsb=256,
+         alpha=16.0):
+    return lib.lora_linear_fwd(x, W or _w(), A, B, y, M, k, n, r, alpha, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(M=0), 1), (dict(k=-64), 1), (dict(k=100), 2), (dict(n=96), 2), (dict(r=12), 2),
+    (dict(r=128), 2), (dict(x=0), 1), (dict(x=MIS), 1), (dict(y=MIS), 1), (dict(A=0), 1),
+    (dict(ws=0), 1), (dict(wsb=255), 3), (dict(alpha=float("nan")), 1),
+    (dict(W=L.Weight(7, FAKE, None, 0)), 1),
+    (dict(W=L.Weight(1, FAKE, None, 64)), 1),            # NF4 without absmax
+    (dict(W=L.Weight(1, FAKE, FAKE, 128)), 2),           # NF4 block size other than 64
+])
+def test_fwd_rejects_bad_arguments(kw, expect):
+    assert _fwd(**kw) == expect
+
+
+def test_bwd_rejects_bad_arguments():
+    need = L.workspace_size(L.OP_BWD, 256, 512, 512, 8)
+    args = lambda **o: lib.lora_linear_bwd(
+        o.get("x", FAKE), _w(), FAKE, FAKE, o.get("dy", FAKE), o.get("dx", FAKE), 0,
+        o.get("dA", FAKE), FAKE, 256, 512, 512, 8, 16.0, FAKE, o.get("wsb", need), None)
+    assert args(dy=MIS) == 1
+    assert args(dA=0) == 1
+    assert args(wsb=need - 1) == 3
+
+
+def test_qk_rope_rejects_bad_arguments():
+    def call(head_dim=128, nqh=2, nkh=1, pos=FAKE, cache=FAKE, theta=5e5, wsb=1 << 20, max_pos=64):
+        return lib.lora_qk_rope_fwd(FAKE, _w(), FAKE, FAKE, _w(), FAKE, FAKE, FAKE, FAKE, 64, 256,
+                                    nqh, nkh, head_dim, 16, 16.0, theta, pos, cache, max_pos,
+                                    FAKE, wsb, None)
+    assert call(head_dim=64) == 2
+    assert call(nqh=0) == 1
+    assert call(pos=0) == 1
+    assert call(cache=0, theta=-1.0) == 1
+    assert call(max_pos=0) == 1
+    assert call(cache=0, wsb=256) == 3       # cache built in the workspace needs room
+
+
+def test_nf4_and_cache_reject_bad_arguments():
+    assert lib.nf4_dequant(FAKE, FAKE, FAKE, 64, 64, 32, None) == 2
+    assert lib.nf4_dequant(FAKE, FAKE, FAKE, 64, 100, 64, None) == 1
+    assert lib.nf4_dequant(MIS, FAKE, FAKE, 64, 64, 64, None) == 1
+    assert lib.nf4_quantize(FAKE, FAKE, 0, 64, 64, 64, None) == 1
+    assert lib.lora_rope_cache_build(FAKE, 0, 128, 1e4, None) == 1
+    assert lib.lora_rope_cache_build(FAKE, 16, 128, 0.0, None) == 1
+    assert lib.lora_read_device_status(None, None, None) == 1
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_call_without_gpu_fails_loudly():
+    """No CPU fallback: a well-formed call on a machine without a GPU
+    returns a CUDA error instead of computing anything."""
+    assert _fwd() in (4, 5)

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -100,6 +101,17 @@ constexpr CUtensorMapDataType kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 // ---------------------------------------------------------------- checks
 bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int rank_pad(int r) { return r <= 16 ? 16 : (r <= 32 ? 32 : 64); }
+// The pair MMA needs N a multiple of 32, so its rank accumulator is >= 32 wide.
+int rank_pad_pair(int r) { return r <= 32 ? 32 : 64; }
+// GEMM variant: the two-SM kernel unless LORA_GEMM_VARIANT=1 selects the
+// one-SM kernel (kept for comparison and testing).
+bool use_pair_kernel() {
+  static const bool pair = [] {
+    const char *v = std::getenv("LORA_GEMM_VARIANT");
+    return !(v && v[0] == '1');
+  }();
+  return pair;
+}
 bool rank_ok(int r) { return r == 8 || r == 16 || r == 32 || r == 64; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 constexpr int kBN = 256;
@@ -151,34 +163,41 @@ struct BwdPlan {
   int v_slices, v_chunks_per_slice;
   int g_slices, g_chunks_per_slice;
   size_t off_bt, off_ut_hi, off_ut_lo, off_vt_hi, off_vt_lo, off_part_v, off_part_a,
-      off_part_b, total;
+      off_part_b, off_counters, counters_bytes, total;
 };
 
-void plan_slices(int tiles, int chunks, int target, int *slices, int *per) {
-  int s = std::max(1, std::min(chunks, (target + tiles - 1) / tiles));
+// Split a reduction of `chunks` 64-wide pieces into slices so that
+// tiles x slices fills `slots` CTA slots (two per SM) without an empty slice.
+void plan_slices(int tiles, int chunks, int slots, int *slices, int *per) {
+  int s = std::max(1, std::min(chunks, slots / std::max(1, tiles)));
   int cps = (chunks + s - 1) / s;
-  s = (chunks + cps - 1) / cps;  // no empty slice
+  s = (chunks + cps - 1) / cps;
   *slices = s;
   *per = cps;
 }
+
+constexpr int kSkinnySlots = 2 * 148;
 
 BwdPlan plan_bwd(int M, int k, int n, int r, size_t start) {
   BwdPlan b{};
   b.rp = rank_pad(r);
   b.Mp = (M + 63) & ~63;
-  const int target = 2 * 148;
-  plan_slices((M + 127) / 128, k / 64, target, &b.v_slices, &b.v_chunks_per_slice);
-  plan_slices((k + 127) / 128 + (n + 127) / 128, (M + 63) / 64, target, &b.g_slices,
-              &b.g_chunks_per_slice);
+  const int mt = (M + 127) / 128, kt = (k + 127) / 128, nt = (n + 127) / 128;
+  plan_slices(mt, k / 64, kSkinnySlots, &b.v_slices, &b.v_chunks_per_slice);
+  plan_slices(kt + nt, (M + 63) / 64, kSkinnySlots, &b.g_slices, &b.g_chunks_per_slice);
   size_t o = align256(start);
   b.off_bt = o;       o = align256(o + (size_t)r * n * 2);
-  b.off_ut_hi = o;    o = align256(o + (size_t)b.rp * b.Mp * 2);
-  b.off_ut_lo = o;    o = align256(o + (size_t)b.rp * b.Mp * 2);
+  const int ut_rows = std::max(b.rp, rank_pad_pair(r));  // rows the dX kernel may write
+  b.off_ut_hi = o;    o = align256(o + (size_t)ut_rows * b.Mp * 2);
+  b.off_ut_lo = o;    o = align256(o + (size_t)ut_rows * b.Mp * 2);
   b.off_vt_hi = o;    o = align256(o + (size_t)b.rp * b.Mp * 2);
   b.off_vt_lo = o;    o = align256(o + (size_t)b.rp * b.Mp * 2);
   b.off_part_v = o;   o = align256(o + (size_t)b.v_slices * M * b.rp * 4);
   b.off_part_a = o;   o = align256(o + (size_t)b.g_slices * k * b.rp * 4);
   b.off_part_b = o;   o = align256(o + (size_t)b.g_slices * n * b.rp * 4);
+  b.off_counters = o;
+  b.counters_bytes = (size_t)(mt + kt + nt) * 4;
+  o = align256(o + b.counters_bytes);
   b.total = o;
   return b;
 }
@@ -204,9 +223,12 @@ lora_status_t run_gemm(int mode, const void *act, int M, int Kred, const GroupAr
   DeviceInfo di;
   lora_status_t s = device_info(&di);
   if (s != LORA_OK) return s;
-  const int rp = rank_pad(r);
+  const bool pair = use_pair_kernel();
+  const int rp = pair ? rank_pad_pair(r) : rank_pad(r);
   const bool nf4 = ga[0].W.type == LORA_WEIGHT_NF4;
   const bool dx = mode == kModeDx;
+  const uint32_t wrows = pair ? kBN / 2 : kBN;   // W / B rows staged per CTA
+  const uint32_t r1rows = pair ? rp / 2 : rp;    // rank-operand rows per CTA
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   // activation: [M, Kred] K-major, box 64 x 128
@@ -220,24 +242,24 @@ lora_status_t run_gemm(int mode, const void *act, int M, int Kred, const GroupAr
     if (!dx) {
       const int n = ncols, k = Kred;
       if (nf4) {
-        if (!make_map(&G.tm_w, kU8, 1, a.W.w, k / 2, n, (uint64_t)k / 2, 32, kBN, false))
+        if (!make_map(&G.tm_w, kU8, 1, a.W.w, k / 2, n, (uint64_t)k / 2, 32, wrows, false))
           return LORA_ERR_CUDA;
-      } else if (!make_map(&G.tm_w, kBF16, 2, a.W.w, k, n, (uint64_t)k * 2, 64, kBN, true)) {
+      } else if (!make_map(&G.tm_w, kBF16, 2, a.W.w, k, n, (uint64_t)k * 2, 64, wrows, true)) {
         return LORA_ERR_CUDA;
       }
-      if (!make_map(&G.tm_r1, kBF16, 2, a.r1, k, r, (uint64_t)k * 2, 64, rp, true) ||
-          !make_map(&G.tm_r2, kBF16, 2, a.r2, r, n, (uint64_t)r * 2, rp, kBN, true))
+      if (!make_map(&G.tm_r1, kBF16, 2, a.r1, k, r, (uint64_t)k * 2, 64, r1rows, true) ||
+          !make_map(&G.tm_r2, kBF16, 2, a.r2, r, n, (uint64_t)r * 2, rp, wrows, true))
         return LORA_ERR_CUDA;
       G.ld_absmax = k / 64;
     } else {
       const int n = Kred, k = ncols;
       if (nf4) {
-        if (!make_map(&G.tm_w, kU8, 1, a.W.w, k / 2, n, (uint64_t)k / 2, kBN / 2, 64, false))
+        if (!make_map(&G.tm_w, kU8, 1, a.W.w, k / 2, n, (uint64_t)k / 2, wrows / 2, 64, false))
           return LORA_ERR_CUDA;
       } else if (!make_map(&G.tm_w, kBF16, 2, a.W.w, k, n, (uint64_t)k * 2, 64, 64, true)) {
         return LORA_ERR_CUDA;
       }
-      if (!make_map(&G.tm_r1, kBF16, 2, a.r1, n, r, (uint64_t)n * 2, 64, rp, true) ||
+      if (!make_map(&G.tm_r1, kBF16, 2, a.r1, n, r, (uint64_t)n * 2, 64, r1rows, true) ||
           !make_map(&G.tm_r2, kBF16, 2, a.r2, k, r, (uint64_t)k * 2, 64, rp, true))
         return LORA_ERR_CUDA;
       G.ld_absmax = k / 64;
@@ -253,8 +275,13 @@ lora_status_t run_gemm(int mode, const void *act, int M, int Kred, const GroupAr
   p.M = M;
   p.K = Kred;
   p.scale = alpha / (float)r;
-  const int m_blocks = (M + 127) / 128;
-  p.sched = pick_schedule(m_blocks, tiles, di.sms, (double)rp / kBN + 0.02);
+  int slots = di.sms;
+  if (pair) {
+    slots = gemm_pair_capacity(mode, rp, rope, nf4);
+    if (slots < 1) return LORA_ERR_CUDA;
+  }
+  const int m_blocks = pair ? (M + 255) / 256 : (M + 127) / 128;
+  p.sched = pick_schedule(m_blocks, tiles, slots, (double)rp / kBN + 0.02);
   p.ut_hi = static_cast<__nv_bfloat16 *>(ut_hi);
   p.ut_lo = static_cast<__nv_bfloat16 *>(ut_lo);
   p.accumulate = accumulate;
@@ -263,6 +290,7 @@ lora_status_t run_gemm(int mode, const void *act, int M, int Kred, const GroupAr
   p.max_pos = max_pos;
   p.status = status;
   const int grid = p.sched.gm * p.sched.gn;
+  if (pair) return cuda_status(launch_gemm_pair(p, mode, rp, rope, nf4, grid, st));
   return cuda_status(launch_gemm(p, mode, rp, rope, nf4, grid, st));
 }
 
@@ -291,7 +319,9 @@ lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void 
   if ((s = run_gemm(kModeDx, dy, M, n, &ga, 1, r, alpha, false, nullptr, nullptr, 0, ut_hi,
                     ut_lo, accumulate, status, st)))
     return s;
-  // (3) v = x·Aᵀ, recomputed (split over k), then hi/lo split and transpose
+  // (3) v = x·Aᵀ, recomputed (split over k, reduced in-kernel) -> vᵀ hi/lo
+  auto *counters = reinterpret_cast<uint32_t *>(ws + b.off_counters);
+  if ((s = cuda_status(cudaMemsetAsync(counters, 0, b.counters_bytes, st)))) return s;
   {
     SkinnyParams sp;
     std::memset(&sp, 0, sizeof(sp));
@@ -301,6 +331,13 @@ lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void 
       return LORA_ERR_CUDA;
     P.tm_q_lo = P.tm_q_hi;
     P.part = part_v;
+    P.counter = counters;
+    P.out_kind = kOutVt;
+    P.out_hi = vt_hi;
+    P.out_lo = vt_lo;
+    P.out_ld = b.Mp;
+    P.r = r;
+    P.scale = 1.0f;
     P.rows = M;
     P.red = k;
     P.row_tiles = (M + 127) / 128;
@@ -310,8 +347,6 @@ lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void 
     sp.num_problems = 1;
     sp.status = status;
     if ((s = cuda_status(launch_skinny(sp, false, b.rp, P.row_tiles * P.slices, st)))) return s;
-    if ((s = cuda_status(launch_v_finalize(part_v, b.v_slices, M, b.rp, vt_hi, vt_lo, st))))
-      return s;
   }
   // (4) dA = s·uᵀ·x and dB = s·dYᵀ·v, reduced over tokens (one launch)
   {
@@ -326,7 +361,13 @@ lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void 
         !make_map(&PB.tm_q_hi, kBF16, 2, vt_hi, M, b.rp, (uint64_t)b.Mp * 2, 64, b.rp, true) ||
         !make_map(&PB.tm_q_lo, kBF16, 2, vt_lo, M, b.rp, (uint64_t)b.Mp * 2, 64, b.rp, true))
       return LORA_ERR_CUDA;
+    const int mt = (M + 127) / 128;
     PA.part = part_a;
+    PA.counter = counters + mt;
+    PA.out_kind = kOutRowT;
+    PA.out_f32 = dA;
+    PA.r = r;
+    PA.scale = scale;
     PA.rows = k;
     PA.red = M;
     PA.row_tiles = (k + 127) / 128;
@@ -334,6 +375,11 @@ lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void 
     PA.chunks_per_slice = b.g_chunks_per_slice;
     PA.cta_begin = 0;
     PB.part = part_b;
+    PB.counter = counters + mt + PA.row_tiles;
+    PB.out_kind = kOutRow;
+    PB.out_f32 = dB;
+    PB.r = r;
+    PB.scale = scale;
     PB.rows = n;
     PB.red = M;
     PB.row_tiles = (n + 127) / 128;
@@ -344,10 +390,6 @@ lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void 
     sp.status = status;
     const int grid = PB.cta_begin + PB.row_tiles * PB.slices;
     if ((s = cuda_status(launch_skinny(sp, true, b.rp, grid, st)))) return s;
-    if ((s = cuda_status(launch_grad_finalize(part_a, b.g_slices, k, b.rp, r, scale, true, dA, st))))
-      return s;
-    if ((s = cuda_status(launch_grad_finalize(part_b, b.g_slices, n, b.rp, r, scale, false, dB, st))))
-      return s;
   }
   return LORA_OK;
 }

@@ -1,0 +1,432 @@
+// Two-SM variant of the fused LoRA GEMM (see gemm.cu for the math):
+//   FWD  y  = x·Wᵀ + s·(x·Aᵀ)·Bᵀ     DX  dX = dY·W + s·(dY·B)·A
+//
+// A cluster of two CTAs computes one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2: CTA r (r = 0, 1) holds rows [128r, 128r+128) of
+// the activation tile, rows [128r, 128r+128) of the W tile (the N half) and
+// half of the rank-r operands, and the tensor cores of both SMs work on the
+// pair tile.  Per SM this halves the W bytes staged per MMA flop compared
+// with a one-SM 128 x 256 tile, which buys a deeper TMA pipeline, and an NF4
+// W tile is decoded half by each SM.
+//
+// Roles (both CTAs unless noted):
+//   warp 0     TMA producer: own halves of x/dY, W (or NF4 codes), A or Bᵀ;
+//              completion counted on the even CTA's barriers.
+//   warp 1     TMEM owner (pair allocation); in the even CTA also the single
+//              MMA issuer, whose commits are multicast to both CTAs.
+//   warps 2-5  epilogue of the CTA's own 128 rows (TMEM lanes 0-127).
+//   warps 6-9  NF4 only: decode the CTA's own W half.
+#include "gemm_common.cuh"
+
+namespace lora {
+
+template <int RP, bool NF4>
+struct PairSmem {
+  static constexpr int X_BYTES = 128 * 128;       // own 128 rows x 64 K
+  static constexpr int W_BYTES = 128 * 128;       // own 128 N-rows x 64 K
+  static constexpr int R1_BYTES = (RP / 2) * 128; // own RP/2 rank rows x 64 K
+  static constexpr int C_BYTES = NF4 ? 128 * 32 : 0;
+  static constexpr int OFF_W = X_BYTES;
+  static constexpr int OFF_R1 = OFF_W + W_BYTES;
+  static constexpr int OFF_C = OFF_R1 + R1_BYTES;
+  static constexpr int STAGE_BYTES = OFF_C + C_BYTES;
+  static constexpr int R2_BYTES = 128 * RP * 2;   // own half of B (FWD) or A (DX)
+  static constexpr int SR_BYTES = 128 * RP * 2;   // s·rank of own rows, bf16
+  static constexpr int MISC_BYTES = 1024;
+  static constexpr int FIXED = R2_BYTES + SR_BYTES + MISC_BYTES + 1024;
+  static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int OFF_R2 = STAGES * STAGE_BYTES;
+  static constexpr int OFF_SR = OFF_R2 + R2_BYTES;
+  static constexpr int OFF_MISC = OFF_SR + SR_BYTES;
+  static constexpr int TOTAL = OFF_MISC + MISC_BYTES + 1024;
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(STAGES >= 3, "pipeline depth");
+  static_assert(TOTAL <= kSmemLimit, "shared memory budget");
+  static_assert(RP == 32 || RP == 64, "pair MMA needs N a multiple of 32");
+};
+
+template <int MODE, int RP, bool NF4, bool ROPE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
+    lora_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  using L = PairSmem<RP, NF4>;
+  constexpr int STAGES = L::STAGES;
+  constexpr int BN = 256;
+  constexpr int RB = RP * 2;
+  constexpr uint32_t SWR = swz_mode_for_row_bytes(RB);
+  constexpr bool DX = MODE == kModeDx;
+  constexpr int NUM_DEC_WARPS = NF4 ? 4 : 0;
+  constexpr uint16_t kBoth = 0x3;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_addr(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_base);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = crank == 0;
+  const int pair = blockIdx.x >> 1;
+
+  const uint32_t bar_full = base + L::OFF_MISC;       // [S] leader: TMA of both CTAs
+  const uint32_t bar_empty = bar_full + 8 * STAGES;   // [S] both: pair MMA done
+  const uint32_t bar_raw = bar_empty + 8 * STAGES;    // [S] both: own NF4 codes landed
+  const uint32_t bar_dec = bar_raw + 8 * STAGES;      // [S] leader: both halves decoded
+  const uint32_t bar_r2_full = bar_dec + 8 * STAGES;  // leader
+  const uint32_t bar_r2_empty = bar_r2_full + 8;      // both
+  const uint32_t bar_rank_full = bar_r2_empty + 8;    // both
+  const uint32_t bar_sr_ready = bar_rank_full + 8;    // leader: 8 warps
+  const uint32_t bar_acc_full = bar_sr_ready + 8;     // both
+  const uint32_t bar_acc_empty = bar_acc_full + 8;    // leader: 8 warps
+  const uint32_t bar_drain = bar_acc_empty + 8;       // leader
+  const int misc_words = (8 * (4 * STAGES + 7)) / 4;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC) + misc_words;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+  float *levels = reinterpret_cast<float *>(tmem_holder + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_raw + 8 * s, 1);
+      mbar_init(bar_dec + 8 * s, NUM_DEC_WARPS > 0 ? 2 * NUM_DEC_WARPS : 1);
+    }
+    mbar_init(bar_r2_full, 1);
+    mbar_init(bar_r2_empty, 1);
+    mbar_init(bar_rank_full, 1);
+    mbar_init(bar_sr_ready, 8);
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, 8);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (NF4 && threadIdx.x < 16) levels[threadIdx.x] = kNf4Levels[threadIdx.x];
+  if (warp == 1) {  // one warp in each CTA of the pair allocates together
+    tmem_alloc_pair(smem_addr(tmem_holder), 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const int nk = p.K / kBK;
+  // the even CTA's copies of the barriers the pair shares
+  const uint32_t lead_full = map_shared_rank(bar_full, 0);
+  const uint32_t lead_dec = map_shared_rank(bar_dec, 0);
+  const uint32_t lead_r2_full = map_shared_rank(bar_r2_full, 0);
+  const uint32_t lead_sr_ready = map_shared_rank(bar_sr_ready, 0);
+  const uint32_t lead_acc_empty = map_shared_rank(bar_acc_empty, 0);
+
+  if (warp == 0) {
+    // ================================================================ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_act);
+      int stage = 0;
+      uint32_t phase = 0;
+      int tile_count = 0, prev_g = -1;
+      int fills[STAGES];
+      for (int s = 0; s < STAGES; ++s) fills[s] = 0;
+      bool ok = true;
+      TileIter it;
+      for (it.init(p.sched, pair); ok && it.valid(); it.next(), ++tile_count) {
+        const int m = it.m(), nt = it.nt();
+        const int g = group_of(p, nt);
+        const bool need_rank = it.first_of_m() || g != prev_g;
+        prev_g = g;
+        const GemmGroup &G = p.grp[g];
+        const int n0 = (nt - G.tile_begin) * BN;
+        const int nh = n0 + (int)crank * 128;  // first N index of this CTA's half
+        const int row0 = m * 256 + (int)crank * 128;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sx = base + stage * L::STAGE_BYTES;
+          const uint32_t fb = lead_full + 8 * stage;
+          if (leader)
+            mbar_arrive_expect_tx(bar_full + 8 * stage,
+                                  2 * (L::X_BYTES + (NF4 ? 0 : L::W_BYTES) +
+                                       (need_rank ? L::R1_BYTES : 0)));
+          tma_load_2d_pair(sx, &p.tm_act, fb, kb * kBK, row0);
+          if constexpr (NF4) {
+            const uint32_t rb = bar_raw + 8 * stage;
+            mbar_arrive_expect_tx(rb, L::C_BYTES);
+            if constexpr (DX)  // codes [64 rows of W, 64 bytes = 128 k-columns]
+              tma_load_2d(sx + L::OFF_C, &G.tm_w, rb, nh / 2, kb * kBK);
+            else               // codes [128 rows of W, 32 bytes]
+              tma_load_2d(sx + L::OFF_C, &G.tm_w, rb, kb * (kBK / 2), nh);
+          } else {
+            if constexpr (DX) {  // W as MN-major operand: 2 boxes [64 rows x 64]
+              tma_load_2d_pair(sx + L::OFF_W, &G.tm_w, fb, nh, kb * kBK);
+              tma_load_2d_pair(sx + L::OFF_W + 8192, &G.tm_w, fb, nh + 64, kb * kBK);
+            } else {
+              tma_load_2d_pair(sx + L::OFF_W, &G.tm_w, fb, kb * kBK, nh);
+            }
+          }
+          if (need_rank)
+            tma_load_2d_pair(sx + L::OFF_R1, &G.tm_r1, fb, kb * kBK, (int)crank * (RP / 2));
+          ++fills[stage];
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+        }
+        if (!ok) break;
+        if (!mbar_wait(bar_r2_empty, (tile_count & 1) ^ 1, abort_flag, p.status)) break;
+        if (leader) mbar_arrive_expect_tx(bar_r2_full, 2 * L::R2_BYTES);
+        if constexpr (DX) {  // A [r, k] read MN-major: 2 boxes [RP rows x 64]
+          tma_load_2d_pair(base + L::OFF_R2, &G.tm_r2, lead_r2_full, nh, 0);
+          tma_load_2d_pair(base + L::OFF_R2 + RP * 128, &G.tm_r2, lead_r2_full, nh + 64, 0);
+        } else {  // B [n, r]: own 128 rows x RP
+          tma_load_2d_pair(base + L::OFF_R2, &G.tm_r2, lead_r2_full, 0, nh);
+        }
+      }
+      // Let every completion the leader multicasts to this CTA land before
+      // the CTA may exit (bounded: after an abort some never come).
+      const uint64_t lim = *abort_flag ? 20000000ull : 1000000000ull;
+      for (int s = 0; s < STAGES; ++s)
+        if (fills[s] > 0) mbar_wait_quiet(bar_empty + 8 * s, (uint32_t)((fills[s] - 1) & 1), lim);
+      if (tile_count > 0) mbar_wait_quiet(bar_r2_empty, (uint32_t)((tile_count - 1) & 1), lim);
+    }
+  } else if (warp == 1) {
+    // ===================================================== MMA (even CTA)
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc_main = make_idesc_bf16(256, BN, false, DX);
+      constexpr uint32_t idesc_rank = make_idesc_bf16(256, RP, false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int tile_count = 0, rank_count = 0, prev_g = -1;
+      bool ok = true;
+      TileIter it;
+      for (it.init(p.sched, pair); ok && it.valid(); it.next(), ++tile_count) {
+        const int g = group_of(p, it.nt());
+        const bool need_rank = it.first_of_m() || g != prev_g;
+        prev_g = g;
+        if (!mbar_wait_cluster(bar_acc_empty, (tile_count & 1) ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (NF4 && !mbar_wait_cluster(bar_dec + 8 * stage, phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sx = base + stage * L::STAGE_BYTES;
+          const uint32_t sw = sx + L::OFF_W;
+          const uint32_t sr = sx + L::OFF_R1;
+#pragma unroll
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            const uint64_t da = make_sdesc(sx + ks * 32, 16, 1024, kSw128);
+            uint64_t dw;
+            if constexpr (DX)  // MN-major: 16 K-rows per step; two 64-wide blocks 8 KB apart
+              dw = make_sdesc(sw + ks * 2048, 8192, 1024, kSw128);
+            else
+              dw = make_sdesc(sw + ks * 32, 16, 1024, kSw128);
+            const uint32_t accum = (kb | ks) != 0;
+            tc_mma_pair(tmem, da, dw, idesc_main, accum);
+            if (need_rank)
+              tc_mma_pair(tmem + BN, da, make_sdesc(sr + ks * 32, 16, 1024, kSw128), idesc_rank,
+                          accum);
+          }
+          tc_commit_pair(bar_empty + 8 * stage, kBoth);
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+        }
+        if (!ok) break;
+        if (need_rank) {
+          tc_commit_pair(bar_rank_full, kBoth);
+          if (!mbar_wait_cluster(bar_sr_ready, rank_count & 1, abort_flag, p.status)) break;
+          ++rank_count;
+          tc_fence_after();
+        }
+        if (!mbar_wait(bar_r2_full, tile_count & 1, abort_flag, p.status)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kr = 0; kr < RP / 16; ++kr) {
+          const uint64_t dsr = make_sdesc(base + L::OFF_SR + kr * 32, 16, 8 * RB, SWR);
+          uint64_t db;
+          if constexpr (DX)  // A tile MN-major: two boxes of RP rows, 16 K-rows per step
+            db = make_sdesc(base + L::OFF_R2 + kr * 2048, RP * 128, 1024, kSw128);
+          else
+            db = make_sdesc(base + L::OFF_R2 + kr * 32, 16, 8 * RB, SWR);
+          tc_mma_pair(tmem, dsr, db, idesc_main, 1u);
+        }
+        tc_commit_pair(bar_r2_empty, kBoth);
+        tc_commit_pair(bar_acc_full, kBoth);
+      }
+      if (*abort_flag) {
+        tc_commit_pair(bar_drain, 0x1);
+        mbar_wait_quiet(bar_drain, 0, 100000000ull);
+      }
+    }
+  } else if (warp < 6) {
+    // ================================================================ epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(q * 32) << 16;
+    const int Mp = (p.M + 63) & ~63;
+    int tile_count = 0, rank_count = 0, prev_g = -1;
+    TileIter it;
+    for (it.init(p.sched, pair); it.valid(); it.next(), ++tile_count) {
+      const int m = it.m(), nt = it.nt();
+      const int g = group_of(p, nt);
+      const bool need_rank = it.first_of_m() || g != prev_g;
+      prev_g = g;
+      const GemmGroup &G = p.grp[g];
+      const int n0 = (nt - G.tile_begin) * BN;
+      const int grow = m * 256 + (int)crank * 128 + row;
+      const bool row_ok = grow < p.M;
+      if (need_rank) {
+        if (!warp_wait(bar_rank_full, rank_count & 1, abort_flag, p.status)) break;
+        ++rank_count;
+        tc_fence_after();
+        epi_rank_to_smem<RP>(tmem + t_lane + BN, base + L::OFF_SR, row, p.scale,
+                             DX && nt == 0 && row_ok, p.ut_hi, p.ut_lo, Mp, grow);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lead_sr_ready);
+      }
+      if (!warp_wait(bar_acc_full, tile_count & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int ncols = min(BN, G.ncols - n0);
+      __nv_bfloat16 *orow = G.out + (size_t)(row_ok ? grow : 0) * G.ncols + n0;
+      const float *cs = ROPE ? rope_row(p, grow, row_ok) : nullptr;
+      epi_store_tile<BN, ROPE>(tmem + t_lane, orow, row_ok, ncols, DX && p.accumulate, cs);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(lead_acc_empty);
+    }
+  } else if constexpr (NF4) {
+    // ============================================================= NF4 decode
+    // FWD: piece dt = row dt of this CTA's W half [128 rows x 64].
+    // DX:  the half is [64 n-rows x 128 k-columns] = two boxes of [64 x 64];
+    //      piece dt = row (dt % 64) of box (dt / 64).
+    const int dt = threadIdx.x - 192;  // 0..127
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    TileIter it;
+    for (it.init(p.sched, pair); ok && it.valid(); it.next()) {
+      const int nt = it.nt();
+      const GemmGroup &G = p.grp[group_of(p, nt)];
+      const int nh = (nt - G.tile_begin) * BN + (int)crank * 128;
+      for (int kb = 0; kb < nk; ++kb) {
+        int wrow, kblk;
+        if constexpr (DX) {
+          wrow = kb * kBK + (dt & 63);
+          kblk = (nh >> 6) + (dt >> 6);
+        } else {
+          wrow = nh + dt;
+          kblk = kb;
+        }
+        const bool in = DX ? (kblk < G.ld_absmax) : (wrow < G.ncols);
+        const float amax =
+            in ? __bfloat162float(G.absmax[(size_t)wrow * G.ld_absmax + kblk]) : 0.0f;
+        if (!warp_wait(bar_raw + 8 * stage, phase, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sx = base + stage * L::STAGE_BYTES;
+        uint32_t src, dst;
+        if constexpr (DX) {
+          src = sx + L::OFF_C + (dt & 63) * 64 + (dt >> 6) * 32;
+          dst = sx + L::OFF_W + (dt >> 6) * 8192 + (dt & 63) * 128;
+        } else {
+          src = sx + L::OFF_C + dt * 32;
+          dst = sx + L::OFF_W + dt * 128;
+        }
+        nf4_decode_piece(src, dst, amax, levels);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lead_dec + 8 * stage);
+        if (++stage == STAGES) stage = 0, phase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  cluster_sync_all();  // no remote arrival may target a CTA that has exited
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+template <int MODE, int RP, bool NF4, bool ROPE>
+static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t st) {
+  using L = PairSmem<RP, NF4>;
+  auto kern = lora_gemm_pair_kernel<MODE, RP, NF4, ROPE>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<2 * pairs, NF4 ? 320 : 192, L::TOTAL, st>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <int MODE, int RP, bool NF4, bool ROPE>
+static int pair_capacity() {
+  using L = PairSmem<RP, NF4>;
+  auto kern = lora_gemm_pair_kernel<MODE, RP, NF4, ROPE>;
+  static int cached = -1;
+  if (cached < 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL) !=
+        cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(NF4 ? 320 : 192, 1, 1);
+    cfg.dynamicSmemBytes = L::TOTAL;
+    int n = 0;  // cluster shape comes from the kernel's compile-time cluster dims
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    cached = n;
+  }
+  return cached;
+}
+
+template <int MODE, int RP, bool NF4>
+static cudaError_t pair_dispatch_rope(const GemmParams &p, bool rope, int pairs, int *cap,
+                                      cudaStream_t st) {
+  if (rope && MODE == kModeFwd) {
+    if (cap) { *cap = pair_capacity<MODE, RP, NF4, true>(); return cudaSuccess; }
+    return launch_pair_one<MODE, RP, NF4, MODE == kModeFwd>(p, pairs, st);
+  }
+  if (cap) { *cap = pair_capacity<MODE, RP, NF4, false>(); return cudaSuccess; }
+  return launch_pair_one<MODE, RP, NF4, false>(p, pairs, st);
+}
+
+template <int MODE>
+static cudaError_t pair_dispatch(const GemmParams &p, int rp, bool rope, bool nf4, int pairs,
+                                 int *cap, cudaStream_t st) {
+  if (rp == 32)
+    return nf4 ? pair_dispatch_rope<MODE, 32, true>(p, rope, pairs, cap, st)
+               : pair_dispatch_rope<MODE, 32, false>(p, rope, pairs, cap, st);
+  if (rp == 64)
+    return nf4 ? pair_dispatch_rope<MODE, 64, true>(p, rope, pairs, cap, st)
+               : pair_dispatch_rope<MODE, 64, false>(p, rope, pairs, cap, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_pair(const GemmParams &p, int mode, int rp, bool rope, bool nf4, int pairs,
+                             cudaStream_t st) {
+  return mode == kModeFwd ? pair_dispatch<kModeFwd>(p, rp, rope, nf4, pairs, nullptr, st)
+                          : pair_dispatch<kModeDx>(p, rp, rope, nf4, pairs, nullptr, st);
+}
+
+int gemm_pair_capacity(int mode, int rp, bool rope, bool nf4) {
+  int cap = 0;
+  GemmParams dummy;
+  if (mode == kModeFwd)
+    pair_dispatch<kModeFwd>(dummy, rp, rope, nf4, 0, &cap, nullptr);
+  else
+    pair_dispatch<kModeDx>(dummy, rp, rope, nf4, 0, &cap, nullptr);
+  return cap;
+}
+
+}  // namespace lora

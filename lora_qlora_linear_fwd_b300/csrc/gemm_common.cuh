@@ -1,0 +1,201 @@
+// Device helpers shared by the one-SM and two-SM fused GEMM kernels:
+// the NF4 level table and row decode, the rank-r epilogue (s·rank -> bf16
+// operand tile in shared memory, plus the uᵀ export of the dX mode) and the
+// output epilogue (TMEM -> optional rotate-half RoPE -> bf16 -> global).
+#pragma once
+
+#include "kernels.h"
+
+namespace lora {
+
+// The 16 NormalFloat4 levels (QLoRA, Dettmers et al. 2023, appendix table),
+// ascending; index 7 is the exact zero.
+static __constant__ float kNf4Levels[16] = {
+    -1.0f, -0.6961928009986877f, -0.5250730514526367f, -0.39491748809814453f,
+    -0.28444138169288635f, -0.18477343022823334f, -0.09105003625154495f, 0.0f,
+    0.07958029955625534f, 0.16093020141124725f, 0.24611230194568634f, 0.33791524171829224f,
+    0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
+
+constexpr uint32_t swz_mode_for_row_bytes(int rb) {
+  return rb == 128 ? kSw128 : (rb == 64 ? kSw64 : kSw32);
+}
+
+LORA_DEV bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                        uint32_t *status) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+LORA_DEV int group_of(const GemmParams &p, int nt) {
+  return (p.num_groups > 1 && nt >= p.grp[1].tile_begin) ? 1 : 0;
+}
+
+LORA_DEV uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// Decode one 64-element row piece: 32 code bytes at `src` (shared), block
+// scale `a`, into a 128-byte row of a 128-byte-swizzled tile at `dst`.
+// Byte j holds element 2j in its high nibble and 2j+1 in its low nibble.
+LORA_DEV void nf4_decode_piece(uint32_t src, uint32_t dst, float a, const float *levels) {
+  const uint4 c01 = ld_shared_v4(src);
+  const uint4 c23 = ld_shared_v4(src + 16);
+  const uint32_t words[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
+  const uint32_t phase = (dst >> 7) & 7u;
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    const uint32_t w = words[ch];
+    uint32_t o[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t byte = (w >> (8 * b)) & 0xFFu;
+      o[b] = pack_bf16x2(levels[byte >> 4] * a, levels[byte & 0xFu] * a);
+    }
+    st_shared_v4(dst + ((((uint32_t)ch) ^ phase) << 4), o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Rank epilogue for one thread (= one row of the CTA's 128 accumulator
+// lanes): read the RP fp32 columns at `t_rank`, write s·rank as bf16 into
+// row `row` of the K-major operand tile at `sr` (row width 2·RP bytes,
+// matching swizzle), and in the dX mode optionally export the unscaled
+// value as uᵀ hi/lo parts at token `grow`.
+template <int RP>
+LORA_DEV void epi_rank_to_smem(uint32_t t_rank, uint32_t sr, int row, float scale, bool write_ut,
+                               __nv_bfloat16 *ut_hi, __nv_bfloat16 *ut_lo, int Mp, int grow) {
+  constexpr int RB = RP * 2;
+#pragma unroll
+  for (int c = 0; c < RP / 16; ++c) {
+    uint32_t r[16];
+    tmem_ld16(t_rank + c * 16, r);
+    tmem_ld_wait();
+    uint32_t pk[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * scale, __uint_as_float(r[2 * j + 1]) * scale);
+    st_shared_v4(sr + swz_offset(row, 2 * c, RB), pk[0], pk[1], pk[2], pk[3]);
+    st_shared_v4(sr + swz_offset(row, 2 * c + 1, RB), pk[4], pk[5], pk[6], pk[7]);
+    if (write_ut) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float u = __uint_as_float(r[j]);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(u);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(u - __bfloat162float(hi));
+        const size_t idx = (size_t)(c * 16 + j) * Mp + grow;
+        ut_hi[idx] = hi;
+        ut_lo[idx] = lo;
+      }
+    }
+  }
+}
+
+// Output epilogue for one thread: BN accumulator columns at `t_acc` of one
+// output row -> bf16 at `orow` (ncols valid columns).  accumulate: add the
+// bf16 values already there.  ROPE: rotate-half per 128-wide head with the
+// cos/sin row `cs` (64 cos then 64 sin); columns (i, i+64) of a head are in
+// the same thread, so the pair is rotated in registers.
+template <int BN, bool ROPE>
+LORA_DEV void epi_store_tile(uint32_t t_acc, __nv_bfloat16 *orow, bool row_ok, int ncols,
+                             bool accumulate, const float *cs) {
+  if constexpr (!ROPE) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(t_acc + c * 32, r);
+      tmem_ld_wait();
+      if (row_ok && c * 32 < ncols) {
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+        if (accumulate) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 old = dst[j];
+            const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&ow[e]);
+              f[8 * j + 2 * e] += __low2float(h);
+              f[8 * j + 2 * e + 1] += __high2float(h);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 w;
+          w.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
+          w.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
+          w.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
+          w.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
+          dst[j] = w;
+        }
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int h = 0; h < BN / 128; ++h) {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const int c0 = h * 128 + half * 32;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(t_acc + c0, ra);
+        tmem_ld32(t_acc + c0 + 64, rb);
+        tmem_ld_wait();
+        if (row_ok && c0 < ncols) {
+          const float4 *cp = reinterpret_cast<const float4 *>(cs + half * 32);
+          const float4 *sp = reinterpret_cast<const float4 *>(cs + 64 + half * 32);
+          uint4 *da = reinterpret_cast<uint4 *>(orow + c0);
+          uint4 *db = reinterpret_cast<uint4 *>(orow + c0 + 64);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 c_lo = __ldg(cp + 2 * j), c_hi = __ldg(cp + 2 * j + 1);
+            const float4 s_lo = __ldg(sp + 2 * j), s_hi = __ldg(sp + 2 * j + 1);
+            const float co[8] = {c_lo.x, c_lo.y, c_lo.z, c_lo.w, c_hi.x, c_hi.y, c_hi.z, c_hi.w};
+            const float si[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+            float oa[8], ob[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float a = __uint_as_float(ra[8 * j + e]);
+              const float b = __uint_as_float(rb[8 * j + e]);
+              oa[e] = a * co[e] - b * si[e];
+              ob[e] = b * co[e] + a * si[e];
+            }
+            uint4 wa, wb;
+            wa.x = pack_bf16x2(oa[0], oa[1]);
+            wa.y = pack_bf16x2(oa[2], oa[3]);
+            wa.z = pack_bf16x2(oa[4], oa[5]);
+            wa.w = pack_bf16x2(oa[6], oa[7]);
+            wb.x = pack_bf16x2(ob[0], ob[1]);
+            wb.y = pack_bf16x2(ob[2], ob[3]);
+            wb.z = pack_bf16x2(ob[4], ob[5]);
+            wb.w = pack_bf16x2(ob[6], ob[7]);
+            da[j] = wa;
+            db[j] = wb;
+          }
+        }
+      }
+    }
+  }
+}
+
+// Position of output row `grow` for the RoPE epilogue; an out-of-range
+// position is reported in the status word and replaced by 0 (no read
+// outside the cache).
+LORA_DEV const float *rope_row(const GemmParams &p, int grow, bool row_ok) {
+  int pos = 0;
+  if (row_ok) {
+    pos = __ldg(p.positions + grow);
+    if (pos < 0 || pos >= p.max_pos) {
+      atomicOr(p.status, kDevBadPosition);
+      pos = 0;
+    }
+  }
+  return p.cos_sin + (size_t)pos * 128;
+}
+
+}  // namespace lora

@@ -55,22 +55,41 @@ void note_launch();
 
 cudaError_t launch_gemm(const GemmParams &p, int mode, int rp, bool rope, bool nf4, int grid,
                         cudaStream_t st);
-int gemm_smem_bytes(int mode, int rp, bool nf4);
+// Two-SM (CTA pair) variant: 256 x 256 tiles, m-blocks of 256 rows, rp 32 or 64.
+cudaError_t launch_gemm_pair(const GemmParams &p, int mode, int rp, bool rope, bool nf4,
+                             int pairs, cudaStream_t st);
+int gemm_pair_capacity(int mode, int rp, bool rope, bool nf4);  // max co-resident pairs
 
-// Skinny rank-r GEMMs on the tensor cores (fp32 partial sums per K-slice):
-//   KMAJOR  (v):     part[s][t][j]  = Σ_{c in slice s} P[t,c]·Q[j,c]   P = x [T,k]
-//   MNMAJOR (dA,dB): part[s][o][j]  = Σ_{t in slice s} P[t,o]·(Qhi+Qlo)[j,t]
+// Skinny rank-r GEMMs on the tensor cores, reduced over K-slices in-kernel:
+//   KMAJOR  (v):     v[t][j]   = Σ_c P[t,c]·Q[j,c]             P = x [T,k], Q = A
+//   MNMAJOR (dA,dB): g[o][j]   = Σ_t P[t,o]·(Qhi+Qlo)[j,t]     P = x or dY
+// Every CTA writes the fp32 partial of its slice; the last CTA to finish a
+// row tile (atomic counter) adds the slices in slice order (deterministic)
+// and writes the final output:
+//   kOutVt:   vᵀ as bf16 hi/lo [RP, ld] (the operand of the dB pass)
+//   kOutRowT: out[j][o] = scale·g[o][j], j < r   (dA [r, k])
+//   kOutRow:  out[o][j] = scale·g[o][j], j < r   (dB [n, r])
+enum SkinnyOut { kOutVt = 0, kOutRowT = 1, kOutRow = 2 };
+
 struct alignas(64) SkinnyProblem {
   CUtensorMap tm_p;
   CUtensorMap tm_q_hi;
   CUtensorMap tm_q_lo;
-  float *part;     // [slices, rows, RP]
-  int rows;        // output rows (T for KMAJOR, Mo for MNMAJOR)
-  int red;         // reduction length
-  int row_tiles;   // ceil(rows / 128)
+  float *part;           // [slices, rows, RP] fp32 partials
+  uint32_t *counter;     // [row_tiles] arrival counters (zero on entry, reset on exit)
+  float *out_f32;        // kOutRowT / kOutRow
+  __nv_bfloat16 *out_hi; // kOutVt
+  __nv_bfloat16 *out_lo;
+  int out_kind;
+  int out_ld;            // leading dimension of the vᵀ output (Mp)
+  int r;                 // real rank (columns written)
+  float scale;
+  int rows;              // output rows (T for KMAJOR, Mo for MNMAJOR)
+  int red;               // reduction length
+  int row_tiles;         // ceil(rows / 128)
   int slices;
   int chunks_per_slice;  // 64-wide reduction chunks per slice
-  int cta_begin;   // first CTA index of this problem
+  int cta_begin;         // first CTA index of this problem
 };
 
 struct alignas(64) SkinnyParams {
@@ -84,10 +103,6 @@ cudaError_t launch_skinny(const SkinnyParams &p, bool mn_major, int rp, int grid
 // Elementwise / small helpers.
 cudaError_t launch_transpose_rank(const __nv_bfloat16 *B, __nv_bfloat16 *Bt, int n, int r,
                                   cudaStream_t st);
-cudaError_t launch_v_finalize(const float *part, int slices, int T, int rp, __nv_bfloat16 *vt_hi,
-                              __nv_bfloat16 *vt_lo, cudaStream_t st);
-cudaError_t launch_grad_finalize(const float *part, int slices, int rows, int rp, int r,
-                                 float scale, bool transpose_out, float *out, cudaStream_t st);
 cudaError_t launch_rope_bwd(const __nv_bfloat16 *dy, __nv_bfloat16 *out, int M, int ncols,
                             const int32_t *pos, const float *cos_sin, int max_pos,
                             uint32_t *status, cudaStream_t st);

@@ -31,78 +31,6 @@ cudaError_t launch_transpose_rank(const __nv_bfloat16 *B, __nv_bfloat16 *Bt, int
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------- v = Σ slices, split
-// part [slices, T, rp] fp32  ->  vt_hi/vt_lo [rp, Tp] bf16 (hi = bf16(v),
-// lo = bf16(v - hi)).  Block: 64 tokens x rp, transposed through shared memory.
-__global__ void v_finalize_kernel(const float *__restrict__ part, int slices, int T, int rp,
-                                  __nv_bfloat16 *__restrict__ vt_hi,
-                                  __nv_bfloat16 *__restrict__ vt_lo) {
-  __shared__ float tile[64][65];
-  const int t0 = blockIdx.x * 64;
-  const int Tp = (T + 63) & ~63;
-  for (int i = threadIdx.x; i < 64 * rp; i += blockDim.x) {
-    const int t = i / rp, j = i % rp;
-    float acc = 0.0f;
-    if (t0 + t < T)
-      for (int s = 0; s < slices; ++s) acc += part[((size_t)s * T + t0 + t) * rp + j];
-    tile[j][t] = acc;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 64 * rp; i += blockDim.x) {
-    const int j = i / 64, t = i % 64;
-    if (t0 + t < T) {
-      const float v = tile[j][t];
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-      vt_hi[(size_t)j * Tp + t0 + t] = hi;
-      vt_lo[(size_t)j * Tp + t0 + t] = __float2bfloat16_rn(v - __bfloat162float(hi));
-    }
-  }
-}
-
-cudaError_t launch_v_finalize(const float *part, int slices, int T, int rp, __nv_bfloat16 *vt_hi,
-                              __nv_bfloat16 *vt_lo, cudaStream_t st) {
-  v_finalize_kernel<<<(T + 63) / 64, 256, 0, st>>>(part, slices, T, rp, vt_hi, vt_lo);
-  note_launch();
-  return cudaGetLastError();
-}
-
-// ------------------------------------------------------ dA / dB = s · Σ slices
-// part [slices, rows, rp]; transpose_out: out [r, rows] (dA), else out [rows, r]
-// (dB).  Only the first r of the rp columns are real.
-__global__ void grad_finalize_kernel(const float *__restrict__ part, int slices, int rows, int rp,
-                                     int r, float scale, int transpose_out,
-                                     float *__restrict__ out) {
-  __shared__ float tile[64][65];
-  const int o0 = blockIdx.x * 64;
-  for (int i = threadIdx.x; i < 64 * rp; i += blockDim.x) {
-    const int o = i / rp, j = i % rp;
-    float acc = 0.0f;
-    if (o0 + o < rows)
-      for (int s = 0; s < slices; ++s) acc += part[((size_t)s * rows + o0 + o) * rp + j];
-    tile[j][o] = acc * scale;
-  }
-  __syncthreads();
-  if (transpose_out) {
-    for (int i = threadIdx.x; i < 64 * r; i += blockDim.x) {
-      const int j = i / 64, o = i % 64;
-      if (o0 + o < rows) out[(size_t)j * rows + o0 + o] = tile[j][o];
-    }
-  } else {
-    for (int i = threadIdx.x; i < 64 * r; i += blockDim.x) {
-      const int o = i / r, j = i % r;
-      if (o0 + o < rows) out[(size_t)(o0 + o) * r + j] = tile[j][o];
-    }
-  }
-}
-
-cudaError_t launch_grad_finalize(const float *part, int slices, int rows, int rp, int r,
-                                 float scale, bool transpose_out, float *out, cudaStream_t st) {
-  grad_finalize_kernel<<<(rows + 63) / 64, 256, 0, st>>>(part, slices, rows, rp, r, scale,
-                                                         transpose_out ? 1 : 0, out);
-  note_launch();
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------- RoPE backward
 // out = R(pos)ᵀ · dy per 128-wide head (inverse rotate-half), bf16 in/out.
 // One thread per (row, head, group of 8 pair indices).

@@ -4,11 +4,12 @@
 //   dB = s·dYᵀ·v       (MNMAJOR mode: reduce over tokens)
 // Each CTA owns a 128-row output tile [128 x RP] and one slice of the
 // reduction; it streams its operand tiles through a TMA ring into a tcgen05
-// accumulator and writes an fp32 partial sum.  A finalize kernel adds the
-// slices (fixed order: deterministic).  In MNMAJOR mode the bf16 right-hand
-// operand comes as two parts (hi + lo = the fp32 value to ~2^-17) and both
-// are multiplied, so the result keeps near-fp32 accuracy while the large
-// operand (x or dY) streams once from HBM.
+// accumulator.  CTAs of one row tile meet through an arrival counter: each
+// writes its fp32 partial, and the last to arrive adds all slices in slice
+// order (deterministic) and writes the final output.  In MNMAJOR mode the
+// bf16 right-hand operand comes as two parts (hi + lo = the fp32 value to
+// about 2^-17 relative) and both are multiplied, so the result keeps
+// near-fp32 accuracy while the large operand (x or dY) streams once.
 #include "kernels.h"
 
 namespace lora {
@@ -18,14 +19,44 @@ struct SkinnySmem {
   static constexpr int P_BYTES = 128 * 128;  // [128 x 64] bf16 either way
   static constexpr int Q_BYTES = RP * 128;
   static constexpr int STAGE_BYTES = P_BYTES + (MN ? 2 : 1) * Q_BYTES;
-  static constexpr int STAGES = 4;
+  // small enough that two CTAs share an SM
+  static constexpr int STAGES_FIT = (110 * 1024 - 2048) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int OFF_MISC = STAGES * STAGE_BYTES;
   static constexpr int TOTAL = OFF_MISC + 256 + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(STAGES >= 3, "pipeline depth");
 };
 
+LORA_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Final values of columns [j0, j0+16) of output row `orow`.
+LORA_DEV void skinny_store16(const SkinnyProblem &P, int orow, int j0, const float (&v)[16]) {
+  if (orow >= P.rows) return;
+  if (P.out_kind == kOutVt) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v[j]);
+      P.out_hi[(size_t)(j0 + j) * P.out_ld + orow] = hi;
+      P.out_lo[(size_t)(j0 + j) * P.out_ld + orow] =
+          __float2bfloat16_rn(v[j] - __bfloat162float(hi));
+    }
+  } else if (P.out_kind == kOutRowT) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j0 + j < P.r) P.out_f32[(size_t)(j0 + j) * P.rows + orow] = v[j] * P.scale;
+  } else {
+    float4 *dst = reinterpret_cast<float4 *>(P.out_f32 + (size_t)orow * P.r + j0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j0 + 4 * j < P.r)
+        dst[j] = make_float4(v[4 * j] * P.scale, v[4 * j + 1] * P.scale, v[4 * j + 2] * P.scale,
+                             v[4 * j + 3] * P.scale);
+  }
+}
+
 template <bool MN, int RP>
-__global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_constant__ SkinnyParams p) {
+__global__ void __launch_bounds__(192, 2) lora_skinny_kernel(const __grid_constant__ SkinnyParams p) {
   using L = SkinnySmem<MN, RP>;
   constexpr int STAGES = L::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -40,6 +71,8 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   const uint32_t bar_drain = bar_acc + 8;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC + 8 * (2 * STAGES + 2));
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+  volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_holder + 2);
+  volatile int *epi_fail = reinterpret_cast<volatile int *>(tmem_holder + 3);
 
   const int pi = (p.num_problems > 1 && (int)blockIdx.x >= p.pr[1].cta_begin) ? 1 : 0;
   const SkinnyProblem &P = p.pr[pi];
@@ -58,6 +91,8 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
     mbar_init(bar_acc, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
+    *last_flag = 0;
+    *epi_fail = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -71,6 +106,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
 
   if (warp == 0) {
     if (lane == 0) {
+      tma_prefetch_desc(&P.tm_p);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t fill_parity[STAGES];
@@ -136,24 +172,74 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
       }
     }
   } else {
+    // ------------------------------------------------ epilogue + reduction
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int orow = rt * 128 + row;
-    const bool ok = mbar_wait(bar_acc, 0, abort_flag, p.status);
-    if (__all_sync(0xffffffffu, ok)) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_acc, 0, abort_flag, p.status));
+    if (!ok && lane == 0) *epi_fail = 1;
+    epi_bar();                 // every epilogue warp takes the same branch below
+    if (!*epi_fail) {
       tc_fence_after();
-      float *dst = P.part + ((size_t)slice * P.rows + orow) * RP;
+      float v[RP];
 #pragma unroll
       for (int c = 0; c < RP / 16; ++c) {
         uint32_t r[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c * 16, r);
         tmem_ld_wait();
-        if (orow < P.rows) {
-          float4 *d4 = reinterpret_cast<float4 *>(dst + c * 16);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        for (int j = 0; j < 16; ++j) v[c * 16 + j] = __uint_as_float(r[j]);
+      }
+      if (P.slices == 1) {
+#pragma unroll
+        for (int c = 0; c < RP / 16; ++c) {
+          float t[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) t[j] = v[c * 16 + j];
+          skinny_store16(P, orow, c * 16, t);
+        }
+      } else {
+        if (orow < P.rows) {
+          float4 *dst = reinterpret_cast<float4 *>(P.part + ((size_t)slice * P.rows + orow) * RP);
+#pragma unroll
+          for (int j = 0; j < RP / 4; ++j)
+            dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+        __threadfence();
+        epi_bar();
+        if (threadIdx.x == 64)
+          *last_flag = (atomicAdd(P.counter + rt, 1u) == (uint32_t)(P.slices - 1)) ? 1 : 0;
+        epi_bar();
+        if (*last_flag) {
+          __threadfence();
+          // add the slices in slice order, 16 columns at a time
+#pragma unroll
+          for (int c = 0; c < RP / 16; ++c) {
+            float sum[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sum[j] = 0.0f;
+            if (orow < P.rows) {
+              for (int s = 0; s < P.slices; ++s) {
+                if (s == slice) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) sum[j] += v[c * 16 + j];
+                } else {
+                  const float4 *src = reinterpret_cast<const float4 *>(
+                      P.part + ((size_t)s * P.rows + orow) * RP + c * 16);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const float4 t = __ldcg(src + j);
+                    sum[4 * j] += t.x;
+                    sum[4 * j + 1] += t.y;
+                    sum[4 * j + 2] += t.z;
+                    sum[4 * j + 3] += t.w;
+                  }
+                }
+              }
+            }
+            skinny_store16(P, orow, c * 16, sum);
+          }
+          if (threadIdx.x == 64) P.counter[rt] = 0u;   // ready for the next call
         }
       }
     }

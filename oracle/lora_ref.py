@@ -36,7 +36,8 @@ import numpy as np
 from scipy.stats import norm
 
 __all__ = [
-    "lora_scale", "lora_fwd", "lora_bwd", "merged_weight", "lora_param_count",
+    "lora_scale", "lora_fwd", "lora_bwd", "lora_adapter_grads", "merged_weight",
+    "lora_param_count",
     "bf16_round", "nf4_codebook", "nf4_quantize", "nf4_unpack", "nf4_dequant",
     "rope_inv_freq", "rope_cos_sin", "rope_apply", "rope_apply_inverse",
     "qk_rope_fwd", "qk_rope_bwd",
@@ -88,11 +89,19 @@ def lora_bwd(x, W, A, B, dy, alpha: float):
     x, W, A, B, dy = _f64(x), _f64(W), _f64(A), _f64(B), _f64(dy)
     s = lora_scale(alpha, A.shape[0])
     u = dy @ B
-    v = x @ A.T                      # recomputed, not taken from the forward
     dx = dy @ W + s * (u @ A)
-    dA = s * (u.T @ x)
-    dB = s * (dy.T @ v)
+    dA, dB = lora_adapter_grads(x, A, B, dy, alpha)
     return dx, dA, dB
+
+
+def lora_adapter_grads(x, A, B, dy, alpha: float):
+    """The adapter part of :func:`lora_bwd` alone (no dX):
+    ``dA = s·(dY·B)ᵀ·x`` and ``dB = s·dYᵀ·(x·Aᵀ)`` with ``x·Aᵀ`` recomputed."""
+    x, A, B, dy = _f64(x), _f64(A), _f64(B), _f64(dy)
+    s = lora_scale(alpha, A.shape[0])
+    u = dy @ B
+    v = x @ A.T                      # recomputed, not taken from the forward
+    return s * (u.T @ x), s * (dy.T @ v)
 
 
 def merged_weight(W, A, B, alpha: float):
@@ -151,7 +160,7 @@ def nf4_codebook():
     return levels / levels.max()
 
 
-def nf4_quantize(W, blocksize: int = 64, decision: str = "fp64"):
+def nf4_quantize(W, blocksize: int = 64, decision: str = "fp64", rows_per_pass=None):
     """Blockwise NF4 quantisation of a row-major ``W [n,k]``.
 
     Reading (the pages give only the name NormalFloat4): blocks are
@@ -166,29 +175,37 @@ def nf4_quantize(W, blocksize: int = 64, decision: str = "fp64"):
     ``"fp64"`` (plain definition) or ``"fp32"`` (IEEE single-precision
     division and distances, the precision a GPU quantiser uses).
 
+    Rows are processed ``rows_per_pass`` at a time (default: about 4M
+    elements) only to bound memory; each row's result does not depend on it.
+
     Returns ``(codes uint8 [n, k/2], absmax float64 [n, k/blocksize])``.
     """
-    W = _f64(W)
+    W = np.asarray(W)
     n, k = W.shape
     assert k % blocksize == 0 and blocksize % 2 == 0
-    blocks = W.reshape(n, k // blocksize, blocksize)
-    absmax = bf16_round(np.max(np.abs(blocks), axis=2))
-    levels = nf4_codebook()
-    safe = np.where(absmax == 0.0, 1.0, absmax)[:, :, None]
-    if decision == "fp64":
-        ratio = np.clip(blocks / safe, -1.0, 1.0)
-        dist = np.abs(ratio[..., None] - levels)
-    elif decision == "fp32":
-        ratio = (blocks.astype(np.float32) / safe.astype(np.float32))
-        ratio = np.clip(ratio, np.float32(-1.0), np.float32(1.0))
-        dist = np.abs(ratio[..., None] - levels.astype(np.float32))
-    else:
+    if decision not in ("fp64", "fp32"):
         raise ValueError(decision)
-    code = np.argmin(dist, axis=-1).astype(np.uint8)     # first minimum wins
-    code[absmax == 0.0] = 7
-    code = code.reshape(n, k)
-    packed = (code[:, 0::2] << 4) | code[:, 1::2]
-    return packed.astype(np.uint8), absmax
+    levels = nf4_codebook()
+    packed = np.empty((n, k // 2), dtype=np.uint8)
+    absmax = np.empty((n, k // blocksize), dtype=np.float64)
+    rows = rows_per_pass or max(1, (1 << 22) // k)   # bounds the distance array
+    for r0 in range(0, n, rows):
+        blocks = _f64(W[r0:r0 + rows]).reshape(-1, k // blocksize, blocksize)
+        am = bf16_round(np.max(np.abs(blocks), axis=2))
+        safe = np.where(am == 0.0, 1.0, am)[:, :, None]
+        if decision == "fp64":
+            ratio = np.clip(blocks / safe, -1.0, 1.0)
+            dist = np.abs(ratio[..., None] - levels)
+        else:
+            ratio = blocks.astype(np.float32) / safe.astype(np.float32)
+            ratio = np.clip(ratio, np.float32(-1.0), np.float32(1.0))
+            dist = np.abs(ratio[..., None] - levels.astype(np.float32))
+        code = np.argmin(dist, axis=-1).astype(np.uint8)     # first minimum wins
+        code[am == 0.0] = 7
+        code = code.reshape(-1, k)
+        packed[r0:r0 + rows] = (code[:, 0::2] << 4) | code[:, 1::2]
+        absmax[r0:r0 + rows] = am
+    return packed, absmax
 
 
 def nf4_unpack(codes):

@@ -281,6 +281,15 @@ def test_nf4_quantiser_is_brute_force_nearest(decision):
             assert idx[i, j] == best
 
 
+def test_nf4_row_passes_do_not_change_the_result():
+    w = ref.bf16_round(_rand(10, 128, scale=0.1))
+    for decision in ("fp64", "fp32"):
+        c1, a1 = ref.nf4_quantize(w, decision=decision)
+        c2, a2 = ref.nf4_quantize(w, decision=decision, rows_per_pass=3)
+        np.testing.assert_array_equal(c1, c2)
+        np.testing.assert_array_equal(a1, a2)
+
+
 def test_nf4_dequant_error_bound():
     """Dequantised weights are within half the widest level gap (times
     absmax) of the originals."""

@@ -159,6 +159,25 @@ lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq,
                                const float *cos_sin_cache, int max_pos,
                                void *ws, size_t ws_bytes, lora_stream_t stream);
 
+/* lora_linear_bwd without a workspace argument, for callers that cannot
+ * allocate device memory where they run the backward (a plugin inside another
+ * framework's runtime that is handed only its tensors; a latency-critical
+ * loop that must not enter the driver's allocator).  The pages have no
+ * counterpart: this is a packaging of lora_linear_bwd, same arguments and
+ * results, minus ws/ws_bytes.
+ *   Scratch: one fixed 32 MiB array in the library's device memory, held on
+ *     every GPU that loads the library until the process exits.  Shapes
+ *     needing more (lora_workspace_size(LORA_OP_BWD, ...) > 32 MiB) return
+ *     LORA_ERR_WORKSPACE before any launch.
+ *   The first call on a device looks up the array's address for that device
+ *     (make it before any stream capture).  Calls share the array: calls
+ *     that overlap on the GPU race and must be serialised.  Device-side
+ *     timeouts are recorded in the array and not reported here. */
+lora_status_t lora_linear_bwd_noalloc(const void *x, lora_weight_t W, const void *A,
+                                      const void *B, const void *dy, void *dx,
+                                      int accumulate_dx, float *dA, float *dB, int M, int k,
+                                      int n, int r, float alpha, lora_stream_t stream);
+
 /* Standalone NF4 dequantisation ([P3] 显存优化策略, [QLoRA] §3):
  *   w_out[i,j] = bf16( level[code(i,j)] * absmax[i, j/64] ), product in fp32.
  * codes uint8 [n, k/2], absmax bf16 [n, k/64], w_out bf16 [n,k]. */

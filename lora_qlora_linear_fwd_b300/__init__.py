@@ -19,7 +19,8 @@ from .build import lib_path
 
 __all__ = [
     "LoraError", "Weight", "bf16_weight", "nf4_weight", "workspace", "workspace_size",
-    "lora_linear_fwd", "lora_linear_bwd", "lora_qk_rope_fwd", "lora_qk_rope_bwd",
+    "lora_linear_fwd", "lora_linear_bwd", "lora_linear_bwd_noalloc", "lora_qk_rope_fwd",
+    "lora_qk_rope_bwd",
     "nf4_dequant", "nf4_quantize", "lora_rope_cache_build", "lora_rope_cache_bytes",
     "lora_read_device_status", "lora_clear_device_status", "lora_status_string",
     "lora_kernel_launch_count",
@@ -58,6 +59,8 @@ EXPORTS = {
                               _F, _D, _P, _P, _I, _P, _Z, _P]),
     "lora_qk_rope_bwd": (_I, [_P, Weight, _P, _P, Weight, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
                               _I, _I, _I, _I, _I, _I, _F, _D, _P, _P, _I, _P, _Z, _P]),
+    "lora_linear_bwd_noalloc": (_I, [_P, Weight, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _F,
+                                     _P]),
     "nf4_dequant": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "nf4_quantize": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "lora_rope_cache_bytes": (_Z, [_I, _I]),
@@ -150,6 +153,18 @@ def lora_linear_bwd(x, W, A, B, dy, dx, dA, dB, alpha: float, ws, accumulate_dx:
                                    int(bool(accumulate_dx)), _ptr(dA), _ptr(dB), M, k, n, r,
                                    float(alpha), _ptr(ws), ws.numel(), _stream(stream)),
            "lora_linear_bwd")
+
+
+def lora_linear_bwd_noalloc(x, W, A, B, dy, dx, dA, dB, alpha: float,
+                            accumulate_dx: bool = False, stream=None):
+    """lora_linear_bwd without a workspace (the library's fixed device
+    scratch is used instead; see the C header for its limits)."""
+    M, k = x.shape
+    n, r = dy.shape[1], A.shape[0]
+    _check(library.lora_linear_bwd_noalloc(_ptr(x), _weight(W), _ptr(A), _ptr(B), _ptr(dy),
+                                           _ptr(dx), int(bool(accumulate_dx)), _ptr(dA),
+                                           _ptr(dB), M, k, n, r, float(alpha), _stream(stream)),
+           "lora_linear_bwd_noalloc")
 
 
 def lora_qk_rope_fwd(x, Wq, Aq, Bq, Wk, Ak, Bk, q, k_out, alpha: float, rope_theta: float,

@@ -140,61 +140,86 @@ lora_status_t check_shape(int M, int k, int n, int r) {
 }
 
 // ------------------------------------------------------------- schedule
-Schedule pick_schedule(int m_blocks, int n_tiles, int sms, double rank_cost) {
-  Schedule best{1, 1, m_blocks, n_tiles};
+// Static schedule for `slots` persistent workers over m_blocks x n_tiles
+// tiles.  Cost model in tile times: each tile costs 1, forming the rank
+// accumulator costs rank_cost more.  The grid schedule's makespan is
+// ceil(Mb/gm)*ceil(Nt/gn) tiles; the contiguous one's is ceil(T/W) plus at
+// most two rank formations, but it keeps the whole problem in flight, so it
+// is used only when the streamed operands fit comfortably in L2.
+Schedule pick_schedule(int m_blocks, int n_tiles, int slots, double rank_cost,
+                       double operand_bytes) {
+  Schedule best{1, 1, m_blocks, n_tiles, 0, 1};
   double best_cost = 1e300;
-  for (int gm = 1; gm <= std::min(m_blocks, sms); ++gm) {
-    const int gn = std::min(n_tiles, sms / gm);
+  for (int gm = 1; gm <= std::min(m_blocks, slots); ++gm) {
+    const int gn = std::min(n_tiles, slots / gm);
     if (gn < 1) break;
     const int per_m = (m_blocks + gm - 1) / gm;
     const int per_n = (n_tiles + gn - 1) / gn;
     const double cost = (double)per_m * per_n + per_m * rank_cost;
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
-      best = Schedule{gm, gn, m_blocks, n_tiles};
+      best = Schedule{gm, gn, m_blocks, n_tiles, 0, gm * gn};
     }
   }
+  const long long total = (long long)m_blocks * n_tiles;
+  const int workers = (int)std::min<long long>(slots, total);
+  const double per = (double)((total + workers - 1) / workers);
+  const double cont_cost = per + std::min(2.0, 1.0 + per / n_tiles) * rank_cost;
+  constexpr double kL2Comfortable = 96.0 * (1 << 20);
+  // LORA_SCHEDULE=grid|contiguous overrides the choice (for measurements).
+  static const int forced = [] {
+    const char *v = std::getenv("LORA_SCHEDULE");
+    if (!v) return -1;
+    return v[0] == 'g' ? 0 : (v[0] == 'c' ? 1 : -1);
+  }();
+  const bool contiguous = forced >= 0 ? forced == 1
+                                      : (operand_bytes <= kL2Comfortable &&
+                                         cont_cost < best_cost - 0.5);
+  if (contiguous) best = Schedule{1, 1, m_blocks, n_tiles, 1, workers};
   return best;
 }
 
 // --------------------------------------------------------- workspace plan
 struct BwdPlan {
   int rp, Mp;
-  int v_slices, v_chunks_per_slice;
-  int g_slices, g_chunks_per_slice;
+  int v_grid, v_max_segs;
+  int g_grid, g_max_segs;
   size_t off_bt, off_ut_hi, off_ut_lo, off_vt_hi, off_vt_lo, off_part_v, off_part_a,
       off_part_b, off_counters, counters_bytes, total;
 };
 
-// Split a reduction of `chunks` 64-wide pieces into slices so that
-// tiles x slices fills `slots` CTA slots (two per SM) without an empty slice.
-void plan_slices(int tiles, int chunks, int slots, int *slices, int *per) {
-  int s = std::max(1, std::min(chunks, slots / std::max(1, tiles)));
-  int cps = (chunks + s - 1) / s;
-  s = (chunks + cps - 1) / cps;
-  *slices = s;
-  *per = cps;
+// Persistent skinny launch over `items` work items: the grid, and the most
+// CTAs whose contiguous item ranges can touch one row tile of `chunks` items.
+int stream_grid(long long items) {
+  return (int)std::max<long long>(1, std::min<long long>(kSkinnyCtas, items));
 }
-
-constexpr int kSkinnySlots = 2 * 148;
+int max_segs_for(int chunks, long long items, int grid) {
+  const long long per = std::max<long long>(1, items / grid);
+  return (int)((chunks + per - 1) / per + 1);
+}
 
 BwdPlan plan_bwd(int M, int k, int n, int r, size_t start) {
   BwdPlan b{};
   b.rp = rank_pad(r);
   b.Mp = (M + 63) & ~63;
   const int mt = (M + 127) / 128, kt = (k + 127) / 128, nt = (n + 127) / 128;
-  plan_slices(mt, k / 64, kSkinnySlots, &b.v_slices, &b.v_chunks_per_slice);
-  plan_slices(kt + nt, (M + 63) / 64, kSkinnySlots, &b.g_slices, &b.g_chunks_per_slice);
+  const int v_chunks = k / 64, g_chunks = (M + 63) / 64;
+  const long long v_items = (long long)mt * v_chunks;
+  const long long g_items = (long long)(kt + nt) * g_chunks;
+  b.v_grid = stream_grid(v_items);
+  b.g_grid = stream_grid(g_items);
+  b.v_max_segs = max_segs_for(v_chunks, v_items, b.v_grid);
+  b.g_max_segs = max_segs_for(g_chunks, g_items, b.g_grid);
   size_t o = align256(start);
-  b.off_bt = o;       o = align256(o + (size_t)r * n * 2);
   const int ut_rows = std::max(b.rp, rank_pad_pair(r));  // rows the dX kernel may write
+  b.off_bt = o;       o = align256(o + (size_t)r * n * 2);
   b.off_ut_hi = o;    o = align256(o + (size_t)ut_rows * b.Mp * 2);
   b.off_ut_lo = o;    o = align256(o + (size_t)ut_rows * b.Mp * 2);
   b.off_vt_hi = o;    o = align256(o + (size_t)b.rp * b.Mp * 2);
   b.off_vt_lo = o;    o = align256(o + (size_t)b.rp * b.Mp * 2);
-  b.off_part_v = o;   o = align256(o + (size_t)b.v_slices * M * b.rp * 4);
-  b.off_part_a = o;   o = align256(o + (size_t)b.g_slices * k * b.rp * 4);
-  b.off_part_b = o;   o = align256(o + (size_t)b.g_slices * n * b.rp * 4);
+  b.off_part_v = o;   o = align256(o + (size_t)mt * b.v_max_segs * 128 * b.rp * 4);
+  b.off_part_a = o;   o = align256(o + (size_t)kt * b.g_max_segs * 128 * b.rp * 4);
+  b.off_part_b = o;   o = align256(o + (size_t)nt * b.g_max_segs * 128 * b.rp * 4);
   b.off_counters = o;
   b.counters_bytes = (size_t)(mt + kt + nt) * 4;
   o = align256(o + b.counters_bytes);
@@ -281,7 +306,10 @@ lora_status_t run_gemm(int mode, const void *act, int M, int Kred, const GroupAr
     if (slots < 1) return LORA_ERR_CUDA;
   }
   const int m_blocks = pair ? (M + 255) / 256 : (M + 127) / 128;
-  p.sched = pick_schedule(m_blocks, tiles, slots, (double)rp / kBN + 0.02);
+  double operand_bytes = (double)M * Kred * 2;   // activation
+  for (int g = 0; g < ng; ++g)                     // weights
+    operand_bytes += (double)ga[g].ncols * Kred * (nf4 ? 0.5 + 1.0 / 32 : 2.0);
+  p.sched = pick_schedule(m_blocks, tiles, slots, (double)rp / kBN + 0.02, operand_bytes);
   p.ut_hi = static_cast<__nv_bfloat16 *>(ut_hi);
   p.ut_lo = static_cast<__nv_bfloat16 *>(ut_lo);
   p.accumulate = accumulate;
@@ -289,7 +317,7 @@ lora_status_t run_gemm(int mode, const void *act, int M, int Kred, const GroupAr
   p.cos_sin = cos_sin;
   p.max_pos = max_pos;
   p.status = status;
-  const int grid = p.sched.gm * p.sched.gn;
+  const int grid = p.sched.workers;
   if (pair) return cuda_status(launch_gemm_pair(p, mode, rp, rope, nf4, grid, st));
   return cuda_status(launch_gemm(p, mode, rp, rope, nf4, grid, st));
 }
@@ -339,14 +367,13 @@ lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void 
     P.r = r;
     P.scale = 1.0f;
     P.rows = M;
-    P.red = k;
     P.row_tiles = (M + 127) / 128;
-    P.slices = b.v_slices;
-    P.chunks_per_slice = b.v_chunks_per_slice;
-    P.cta_begin = 0;
+    P.chunks = k / 64;
+    P.max_segs = b.v_max_segs;
     sp.num_problems = 1;
+    sp.total_items = (long long)P.row_tiles * P.chunks;
     sp.status = status;
-    if ((s = cuda_status(launch_skinny(sp, false, b.rp, P.row_tiles * P.slices, st)))) return s;
+    if ((s = cuda_status(launch_skinny(sp, false, b.rp, b.v_grid, st)))) return s;
   }
   // (4) dA = s·uᵀ·x and dB = s·dYᵀ·v, reduced over tokens (one launch)
   {
@@ -369,11 +396,9 @@ lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void 
     PA.r = r;
     PA.scale = scale;
     PA.rows = k;
-    PA.red = M;
     PA.row_tiles = (k + 127) / 128;
-    PA.slices = b.g_slices;
-    PA.chunks_per_slice = b.g_chunks_per_slice;
-    PA.cta_begin = 0;
+    PA.chunks = (M + 63) / 64;
+    PA.max_segs = b.g_max_segs;
     PB.part = part_b;
     PB.counter = counters + mt + PA.row_tiles;
     PB.out_kind = kOutRow;
@@ -381,15 +406,13 @@ lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void 
     PB.r = r;
     PB.scale = scale;
     PB.rows = n;
-    PB.red = M;
     PB.row_tiles = (n + 127) / 128;
-    PB.slices = b.g_slices;
-    PB.chunks_per_slice = b.g_chunks_per_slice;
-    PB.cta_begin = PA.row_tiles * PA.slices;
+    PB.chunks = (M + 63) / 64;
+    PB.max_segs = b.g_max_segs;
     sp.num_problems = 2;
+    sp.total_items = (long long)(PA.row_tiles + PB.row_tiles) * PA.chunks;
     sp.status = status;
-    const int grid = PB.cta_begin + PB.row_tiles * PB.slices;
-    if ((s = cuda_status(launch_skinny(sp, true, b.rp, grid, st)))) return s;
+    if ((s = cuda_status(launch_skinny(sp, true, b.rp, b.g_grid, st)))) return s;
   }
   return LORA_OK;
 }

@@ -16,6 +16,8 @@
 //              MMA issuer, whose commits are multicast to both CTAs.
 //   warps 2-5  epilogue of the CTA's own 128 rows (TMEM lanes 0-127).
 //   warps 6-9  NF4 only: decode the CTA's own W half.
+#include <cstdlib>
+
 #include "gemm_common.cuh"
 
 namespace lora {
@@ -46,7 +48,7 @@ struct PairSmem {
   static_assert(RP == 32 || RP == 64, "pair MMA needs N a multiple of 32");
 };
 
-template <int MODE, int RP, bool NF4, bool ROPE>
+template <int MODE, int RP, bool NF4, bool ROPE, bool DB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
     lora_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   using L = PairSmem<RP, NF4>;
@@ -77,10 +79,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
   const uint32_t bar_r2_empty = bar_r2_full + 8;      // both
   const uint32_t bar_rank_full = bar_r2_empty + 8;    // both
   const uint32_t bar_sr_ready = bar_rank_full + 8;    // leader: 8 warps
-  const uint32_t bar_acc_full = bar_sr_ready + 8;     // both
-  const uint32_t bar_acc_empty = bar_acc_full + 8;    // leader: 8 warps
-  const uint32_t bar_drain = bar_acc_empty + 8;       // leader
-  const int misc_words = (8 * (4 * STAGES + 7)) / 4;
+  const uint32_t bar_acc_full = bar_sr_ready + 8;     // [2] both: accumulator b ready
+  const uint32_t bar_acc_empty = bar_acc_full + 16;   // [2] leader: 8 warps drained b
+  const uint32_t bar_drain = bar_acc_empty + 16;      // leader
+  const int misc_words = (8 * (4 * STAGES + 9)) / 4;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC) + misc_words;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   float *levels = reinterpret_cast<float *>(tmem_holder + 4);
@@ -97,7 +99,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
     mbar_init(bar_rank_full, 1);
     mbar_init(bar_sr_ready, 8);
     mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_full + 8, 1);
     mbar_init(bar_acc_empty, 8);
+    mbar_init(bar_acc_empty + 8, 8);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -196,13 +200,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
       int stage = 0;
       uint32_t phase = 0;
       int tile_count = 0, rank_count = 0, prev_g = -1;
+      int used[2] = {0, 0};  // tiles issued into each accumulator buffer
       bool ok = true;
       TileIter it;
       for (it.init(p.sched, pair); ok && it.valid(); it.next(), ++tile_count) {
         const int g = group_of(p, it.nt());
         const bool need_rank = it.first_of_m() || g != prev_g;
         prev_g = g;
-        if (!mbar_wait_cluster(bar_acc_empty, (tile_count & 1) ^ 1, abort_flag, p.status)) break;
+        // Accumulators alternate between TMEM columns [0,256) and [256,512)
+        // so a tile's epilogue overlaps the next tile's main loop.  A tile
+        // that forms the rank accumulator puts it in the other buffer, which
+        // must be drained first.
+        const int buf = DB ? (tile_count & 1) : 0;
+        const uint32_t t_acc = tmem + buf * BN;
+        const uint32_t t_rank = tmem + (buf ^ 1) * BN;
+        if (used[buf] > 0 &&
+            !mbar_wait_cluster(bar_acc_empty + 8 * buf, (used[buf] - 1) & 1, abort_flag, p.status))
+          break;
+        if (DB && need_rank && used[buf ^ 1] > 0 &&
+            !mbar_wait_cluster(bar_acc_empty + 8 * (buf ^ 1), (used[buf ^ 1] - 1) & 1, abort_flag,
+                               p.status))
+          break;
+        ++used[buf];
         tc_fence_after();
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) {
@@ -226,9 +245,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
             else
               dw = make_sdesc(sw + ks * 32, 16, 1024, kSw128);
             const uint32_t accum = (kb | ks) != 0;
-            tc_mma_pair(tmem, da, dw, idesc_main, accum);
+            tc_mma_pair(t_acc, da, dw, idesc_main, accum);
             if (need_rank)
-              tc_mma_pair(tmem + BN, da, make_sdesc(sr + ks * 32, 16, 1024, kSw128), idesc_rank,
+              tc_mma_pair(t_rank, da, make_sdesc(sr + ks * 32, 16, 1024, kSw128), idesc_rank,
                           accum);
           }
           tc_commit_pair(bar_empty + 8 * stage, kBoth);
@@ -251,10 +270,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
             db = make_sdesc(base + L::OFF_R2 + kr * 2048, RP * 128, 1024, kSw128);
           else
             db = make_sdesc(base + L::OFF_R2 + kr * 32, 16, 8 * RB, SWR);
-          tc_mma_pair(tmem, dsr, db, idesc_main, 1u);
+          tc_mma_pair(t_acc, dsr, db, idesc_main, 1u);
         }
         tc_commit_pair(bar_r2_empty, kBoth);
-        tc_commit_pair(bar_acc_full, kBoth);
+        tc_commit_pair(bar_acc_full + 8 * buf, kBoth);
       }
       if (*abort_flag) {
         tc_commit_pair(bar_drain, 0x1);
@@ -278,26 +297,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
       const int n0 = (nt - G.tile_begin) * BN;
       const int grow = m * 256 + (int)crank * 128 + row;
       const bool row_ok = grow < p.M;
+      const int buf = DB ? (tile_count & 1) : 0;
       if (need_rank) {
         if (!warp_wait(bar_rank_full, rank_count & 1, abort_flag, p.status)) break;
         ++rank_count;
         tc_fence_after();
-        epi_rank_to_smem<RP>(tmem + t_lane + BN, base + L::OFF_SR, row, p.scale,
+        epi_rank_to_smem<RP>(tmem + t_lane + (buf ^ 1) * BN, base + L::OFF_SR, row, p.scale,
                              DX && nt == 0 && row_ok, p.ut_hi, p.ut_lo, Mp, grow);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(lead_sr_ready);
       }
-      if (!warp_wait(bar_acc_full, tile_count & 1, abort_flag, p.status)) break;
+      if (!warp_wait(bar_acc_full + 8 * buf, (DB ? (tile_count >> 1) : tile_count) & 1, abort_flag,
+                     p.status))
+        break;
       tc_fence_after();
       const int ncols = min(BN, G.ncols - n0);
       __nv_bfloat16 *orow = G.out + (size_t)(row_ok ? grow : 0) * G.ncols + n0;
       const float *cs = ROPE ? rope_row(p, grow, row_ok) : nullptr;
-      epi_store_tile<BN, ROPE>(tmem + t_lane, orow, row_ok, ncols, DX && p.accumulate, cs);
+      epi_store_tile<BN, ROPE>(tmem + t_lane + buf * BN, orow, row_ok, ncols, DX && p.accumulate,
+                               cs);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(lead_acc_empty);
+      if (lane == 0) mbar_arrive_cluster(lead_acc_empty + 8 * buf);
     }
   } else if constexpr (NF4) {
     // ============================================================= NF4 decode
@@ -355,10 +378,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
   }
 }
 
-template <int MODE, int RP, bool NF4, bool ROPE>
-static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t st) {
+// LORA_PAIR_ACC=1 keeps one accumulator buffer (no epilogue overlap); the
+// default alternates two.  Read once.
+static bool pair_double_buffer() {
+  static const bool db = [] {
+    const char *v = std::getenv("LORA_PAIR_ACC");
+    return !(v && v[0] == '1');
+  }();
+  return db;
+}
+
+template <int MODE, int RP, bool NF4, bool ROPE, bool DB>
+static cudaError_t launch_pair_db(const GemmParams &p, int pairs, cudaStream_t st) {
   using L = PairSmem<RP, NF4>;
-  auto kern = lora_gemm_pair_kernel<MODE, RP, NF4, ROPE>;
+  auto kern = lora_gemm_pair_kernel<MODE, RP, NF4, ROPE, DB>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
@@ -371,9 +404,15 @@ static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t 
 }
 
 template <int MODE, int RP, bool NF4, bool ROPE>
+static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t st) {
+  return pair_double_buffer() ? launch_pair_db<MODE, RP, NF4, ROPE, true>(p, pairs, st)
+                              : launch_pair_db<MODE, RP, NF4, ROPE, false>(p, pairs, st);
+}
+
+template <int MODE, int RP, bool NF4, bool ROPE>
 static int pair_capacity() {
   using L = PairSmem<RP, NF4>;
-  auto kern = lora_gemm_pair_kernel<MODE, RP, NF4, ROPE>;
+  auto kern = lora_gemm_pair_kernel<MODE, RP, NF4, ROPE, true>;
   static int cached = -1;
   if (cached < 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL) !=

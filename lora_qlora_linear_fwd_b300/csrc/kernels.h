@@ -75,7 +75,7 @@ struct alignas(64) SkinnyProblem {
   CUtensorMap tm_p;
   CUtensorMap tm_q_hi;
   CUtensorMap tm_q_lo;
-  float *part;           // [slices, rows, RP] fp32 partials
+  float *part;           // [row_tiles, max_segs, 128, RP] fp32 partials
   uint32_t *counter;     // [row_tiles] arrival counters (zero on entry, reset on exit)
   float *out_f32;        // kOutRowT / kOutRow
   __nv_bfloat16 *out_hi; // kOutVt
@@ -85,18 +85,21 @@ struct alignas(64) SkinnyProblem {
   int r;                 // real rank (columns written)
   float scale;
   int rows;              // output rows (T for KMAJOR, Mo for MNMAJOR)
-  int red;               // reduction length
   int row_tiles;         // ceil(rows / 128)
-  int slices;
-  int chunks_per_slice;  // 64-wide reduction chunks per slice
-  int cta_begin;         // first CTA index of this problem
+  int chunks;            // 64-wide reduction chunks per row tile
+  int max_segs;          // most CTAs that can share one row tile
 };
 
 struct alignas(64) SkinnyParams {
   SkinnyProblem pr[2];
   int num_problems;
+  long long total_items;  // Σ row_tiles · chunks over the problems
   uint32_t *status;
 };
+
+// Persistent CTAs of the skinny kernel (one per SM of a B300); the workspace
+// plan depends on it, so it is a constant rather than a device query.
+constexpr int kSkinnyCtas = 148;
 
 cudaError_t launch_skinny(const SkinnyParams &p, bool mn_major, int rp, int grid, cudaStream_t st);
 

@@ -40,6 +40,10 @@
  *     {8, 16, 32, 64}, head_dim == 128; NF4 needs blocksize == 64.
  *   - Calls on the same workspace must not overlap on the GPU (use one
  *     stream, or one workspace per stream).
+ *   - The backward entry points run their rank-r passes partly on a helper
+ *     stream (one per calling thread and device, created on first use with
+ *     two events), forked from and joined back into `stream` with events:
+ *     all their work is ordered before later work on `stream`.
  */
 #ifndef LORA_B300_H
 #define LORA_B300_H

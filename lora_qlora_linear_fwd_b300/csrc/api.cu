@@ -100,9 +100,10 @@ constexpr CUtensorMapDataType kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 
 // ---------------------------------------------------------------- checks
 bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-int rank_pad(int r) { return r <= 16 ? 16 : (r <= 32 ? 32 : 64); }
-// The pair MMA needs N a multiple of 32, so its rank accumulator is >= 32 wide.
-int rank_pad_pair(int r) { return r <= 32 ? 32 : 64; }
+// Rank padded to a tensor-core N: 16/32/64 (and 128 for two merged rank-64
+// projections).  The pair MMA needs N a multiple of 32.
+int rank_pad(int r) { return r <= 16 ? 16 : (r <= 32 ? 32 : (r <= 64 ? 64 : 128)); }
+int rank_pad_pair(int r) { return r <= 32 ? 32 : (r <= 64 ? 64 : 128); }
 // GEMM variant: the two-SM kernel unless LORA_GEMM_VARIANT=1 selects the
 // one-SM kernel (kept for comparison and testing).
 bool use_pair_kernel() {
@@ -234,57 +235,80 @@ lora_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : L
 // ------------------------------------------------------ fused GEMM set-up
 struct GroupArgs {
   lora_weight_t W;
-  const void *r1;  // FWD: A [r,k]; DX: Bt [r,n]
+  const void *r1;  // FWD: A [r,k]; DX: Bᵀ [r,n]
   const void *r2;  // FWD: B [n,r]; DX: A [r,k]
   void *out;
   int ncols;       // output columns
 };
 
-// FWD: act = x [M, k], W [n, k]; DX: act = dY [M, n], W [n, k] read MN-major.
-lora_status_t run_gemm(int mode, const void *act, int M, int Kred, const GroupArgs *ga, int ng,
-                       int r, float alpha, bool rope, const int32_t *positions,
-                       const float *cos_sin, int max_pos, void *ut_hi, void *ut_lo,
-                       int accumulate, uint32_t *status, cudaStream_t st) {
+struct GemmOpts {
+  int mode = kModeFwd;
+  const void *act = nullptr;  // FWD: x [M, k]; DX: dY [M, n]
+  int M = 0, Kred = 0;        // rows; reduction length (k in FWD, n in DX)
+  const GroupArgs *ga = nullptr;
+  int ng = 1;                 // projections along N (FWD)
+  // DX: a second projection along the reduction: its W holds rows
+  // [ksplit*64, Kred) of the combined reduction
+  const lora_weight_t *W2 = nullptr;
+  int ksplit = 0;
+  int r_layout = 0;           // rank of the rank-r operands (r, or 2r merged)
+  float scale = 0.0f;         // alpha / r of one projection
+  bool merged_rank = false;
+  bool rope = false;
+  const int32_t *positions = nullptr;
+  const float *cos_sin = nullptr;
+  int max_pos = 0;
+  void *ut_hi = nullptr, *ut_lo = nullptr;
+  int accumulate = 0;
+  bool need_pair = false;     // merged shapes exist only in the pair kernel
+  uint32_t *status = nullptr;
+};
+
+bool make_w_map(CUtensorMap *m, const lora_weight_t &W, bool dx, bool nf4, int n, int k,
+                uint32_t wrows) {
+  if (!dx) {
+    if (nf4) return make_map(m, kU8, 1, W.w, k / 2, n, (uint64_t)k / 2, 32, wrows, false);
+    return make_map(m, kBF16, 2, W.w, k, n, (uint64_t)k * 2, 64, wrows, true);
+  }
+  if (nf4) return make_map(m, kU8, 1, W.w, k / 2, n, (uint64_t)k / 2, wrows / 2, 64, false);
+  return make_map(m, kBF16, 2, W.w, k, n, (uint64_t)k * 2, 64, 64, true);
+}
+
+lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
   DeviceInfo di;
   lora_status_t s = device_info(&di);
   if (s != LORA_OK) return s;
-  const bool pair = use_pair_kernel();
+  const bool pair = o.need_pair || use_pair_kernel();
+  const int r = o.r_layout;
   const int rp = pair ? rank_pad_pair(r) : rank_pad(r);
-  const bool nf4 = ga[0].W.type == LORA_WEIGHT_NF4;
-  const bool dx = mode == kModeDx;
+  if (!pair && rp > 64) return LORA_ERR_UNSUPPORTED;
+  const bool nf4 = o.ga[0].W.type == LORA_WEIGHT_NF4;
+  const bool dx = o.mode == kModeDx;
   const uint32_t wrows = pair ? kBN / 2 : kBN;   // W / B rows staged per CTA
   const uint32_t r1rows = pair ? rp / 2 : rp;    // rank-operand rows per CTA
+  const uint32_t r2cols = rp > 64 ? 64 : rp;     // FWD B tile: column block width
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   // activation: [M, Kred] K-major, box 64 x 128
-  if (!make_map(&p.tm_act, kBF16, 2, act, Kred, M, (uint64_t)Kred * 2, 64, 128, true))
+  if (!make_map(&p.tm_act, kBF16, 2, o.act, o.Kred, o.M, (uint64_t)o.Kred * 2, 64, 128, true))
     return LORA_ERR_CUDA;
   int tiles = 0;
-  for (int g = 0; g < ng; ++g) {
+  for (int g = 0; g < o.ng; ++g) {
     GemmGroup &G = p.grp[g];
-    const GroupArgs &a = ga[g];
+    const GroupArgs &a = o.ga[g];
     const int ncols = a.ncols;
     if (!dx) {
-      const int n = ncols, k = Kred;
-      if (nf4) {
-        if (!make_map(&G.tm_w, kU8, 1, a.W.w, k / 2, n, (uint64_t)k / 2, 32, wrows, false))
-          return LORA_ERR_CUDA;
-      } else if (!make_map(&G.tm_w, kBF16, 2, a.W.w, k, n, (uint64_t)k * 2, 64, wrows, true)) {
-        return LORA_ERR_CUDA;
-      }
-      if (!make_map(&G.tm_r1, kBF16, 2, a.r1, k, r, (uint64_t)k * 2, 64, r1rows, true) ||
-          !make_map(&G.tm_r2, kBF16, 2, a.r2, r, n, (uint64_t)r * 2, rp, wrows, true))
+      const int n = ncols, k = o.Kred;
+      if (!make_w_map(&G.tm_w, a.W, false, nf4, n, k, wrows) ||
+          !make_map(&G.tm_r1, kBF16, 2, a.r1, k, r, (uint64_t)k * 2, 64, r1rows, true) ||
+          !make_map(&G.tm_r2, kBF16, 2, a.r2, r, n, (uint64_t)r * 2, r2cols, wrows, true))
         return LORA_ERR_CUDA;
       G.ld_absmax = k / 64;
     } else {
-      const int n = Kred, k = ncols;
-      if (nf4) {
-        if (!make_map(&G.tm_w, kU8, 1, a.W.w, k / 2, n, (uint64_t)k / 2, wrows / 2, 64, false))
-          return LORA_ERR_CUDA;
-      } else if (!make_map(&G.tm_w, kBF16, 2, a.W.w, k, n, (uint64_t)k * 2, 64, 64, true)) {
-        return LORA_ERR_CUDA;
-      }
-      if (!make_map(&G.tm_r1, kBF16, 2, a.r1, n, r, (uint64_t)n * 2, 64, r1rows, true) ||
+      const int n = o.W2 ? o.ksplit * 64 : o.Kred, k = ncols;
+      if (!make_w_map(&G.tm_w, a.W, true, nf4, n, k, wrows) ||
+          !make_map(&G.tm_r1, kBF16, 2, a.r1, o.Kred, r, (uint64_t)o.Kred * 2, 64, r1rows,
+                    true) ||
           !make_map(&G.tm_r2, kBF16, 2, a.r2, k, r, (uint64_t)k * 2, 64, rp, true))
         return LORA_ERR_CUDA;
       G.ld_absmax = k / 64;
@@ -296,135 +320,257 @@ lora_status_t run_gemm(int mode, const void *act, int M, int Kred, const GroupAr
     G.tile_begin = tiles;
     tiles += G.n_tiles;
   }
-  p.num_groups = ng;
-  p.M = M;
-  p.K = Kred;
-  p.scale = alpha / (float)r;
+  p.num_groups = o.ng;
+  if (dx && o.W2) {  // second projection along the reduction
+    GemmGroup &G1 = p.grp[1];
+    const int k = o.ga[0].ncols, n2 = o.Kred - o.ksplit * 64;
+    if (!make_w_map(&G1.tm_w, *o.W2, true, nf4, n2, k, wrows)) return LORA_ERR_CUDA;
+    G1.absmax = static_cast<const __nv_bfloat16 *>(o.W2->absmax);
+    G1.ld_absmax = k / 64;
+    G1.ncols = k;
+    p.kgroups = 2;
+    p.ksplit = o.ksplit;
+  } else {
+    p.kgroups = 1;
+  }
+  p.merged_rank = o.merged_rank ? 1 : 0;
+  p.M = o.M;
+  p.K = o.Kred;
+  p.scale = o.scale;
   int slots = di.sms;
   if (pair) {
-    slots = gemm_pair_capacity(mode, rp, rope, nf4);
+    slots = gemm_pair_capacity(o.mode, rp, o.rope, nf4);
     if (slots < 1) return LORA_ERR_CUDA;
   }
-  const int m_blocks = pair ? (M + 255) / 256 : (M + 127) / 128;
-  double operand_bytes = (double)M * Kred * 2;   // activation
-  for (int g = 0; g < ng; ++g)                     // weights
-    operand_bytes += (double)ga[g].ncols * Kred * (nf4 ? 0.5 + 1.0 / 32 : 2.0);
+  const int m_blocks = pair ? (o.M + 255) / 256 : (o.M + 127) / 128;
+  double operand_bytes = (double)o.M * o.Kred * 2;   // activation
+  for (int g = 0; g < o.ng; ++g)                        // weights
+    operand_bytes += (double)o.ga[g].ncols * o.Kred * (nf4 ? 0.5 + 1.0 / 32 : 2.0);
   p.sched = pick_schedule(m_blocks, tiles, slots, (double)rp / kBN + 0.02, operand_bytes);
-  p.ut_hi = static_cast<__nv_bfloat16 *>(ut_hi);
-  p.ut_lo = static_cast<__nv_bfloat16 *>(ut_lo);
-  p.accumulate = accumulate;
-  p.positions = positions;
-  p.cos_sin = cos_sin;
-  p.max_pos = max_pos;
-  p.status = status;
+  p.ut_hi = static_cast<__nv_bfloat16 *>(o.ut_hi);
+  p.ut_lo = static_cast<__nv_bfloat16 *>(o.ut_lo);
+  p.accumulate = o.accumulate;
+  p.positions = o.positions;
+  p.cos_sin = o.cos_sin;
+  p.max_pos = o.max_pos;
+  p.status = o.status;
   const int grid = p.sched.workers;
-  if (pair) return cuda_status(launch_gemm_pair(p, mode, rp, rope, nf4, grid, st));
-  return cuda_status(launch_gemm(p, mode, rp, rope, nf4, grid, st));
+  if (pair) return cuda_status(launch_gemm_pair(p, o.mode, rp, o.rope, nf4, grid, st));
+  return cuda_status(launch_gemm(p, o.mode, rp, o.rope, nf4, grid, st));
 }
 
-// Backward of one projection.  dy [M, n] (already un-rotated for q/k).
-lora_status_t run_bwd(const void *x, lora_weight_t W, const void *A, const void *B,
-                      const void *dy, void *dx, int accumulate, float *dA, float *dB, int M,
-                      int k, int n, int r, float alpha, uint8_t *ws, size_t plan_start,
-                      uint32_t *status, cudaStream_t st) {
-  const BwdPlan b = plan_bwd(M, k, n, r, plan_start);
-  auto *Bt = reinterpret_cast<__nv_bfloat16 *>(ws + b.off_bt);
-  auto *ut_hi = reinterpret_cast<__nv_bfloat16 *>(ws + b.off_ut_hi);
-  auto *ut_lo = reinterpret_cast<__nv_bfloat16 *>(ws + b.off_ut_lo);
-  auto *vt_hi = reinterpret_cast<__nv_bfloat16 *>(ws + b.off_vt_hi);
-  auto *vt_lo = reinterpret_cast<__nv_bfloat16 *>(ws + b.off_vt_lo);
-  auto *part_v = reinterpret_cast<float *>(ws + b.off_part_v);
-  auto *part_a = reinterpret_cast<float *>(ws + b.off_part_a);
-  auto *part_b = reinterpret_cast<float *>(ws + b.off_part_b);
-  const float scale = alpha / (float)r;
-  lora_status_t s;
+// ------------------------------------------------------ backward phases
+// The backward of one projection -- or of two projections sharing x, taken
+// as one projection of rank 2r with A = [A1; A2] and B = diag(B1, B2) --
+// split into phases that the caller orders on two streams:
+//   v      v = x·Aᵀ recomputed -> vᵀ hi/lo   (needs x, A only)
+//   dx     dX (+)= dY·W + s·(dY·B)·A, exports uᵀ = (dY·B)ᵀ hi/lo
+//   grads  dA = s·uᵀ·x, dB = s·dYᵀ·v        (needs v and dx done)
+struct BwdCall {
+  const void *x, *A, *Bt, *dy;   // A [rl, k]; Bᵀ [rl, n] (prepared); dY [M, n]
+  lora_weight_t W;               // W [n1, k] (the whole n unless merged)
+  lora_weight_t W2;              // merged: W of projection 2, [n - n1, k]
+  bool merged;
+  void *dx;
+  int accumulate;
+  float *dA, *dB, *dA2, *dB2;    // per projection
+  int M, k, n, n1;               // n: total reduction of dX; n1: rows of projection 1
+  int r;                         // rank of one projection
+  int rl;                        // layout rank (r, or 2r merged)
+  float scale;
+  uint32_t *status;
+  BwdPlan b;
+  uint8_t *ws;
+  template <typename T>
+  T *at(size_t off) const { return reinterpret_cast<T *>(ws + off); }
+};
 
-  // (1) Bᵀ for the u = dY·B operand
-  if ((s = cuda_status(launch_transpose_rank(static_cast<const __nv_bfloat16 *>(B), Bt, n, r, st))))
-    return s;
-  // (2) dX = dY·W + s·(dY·B)·A, exporting uᵀ = (dY·B)ᵀ as bf16 hi+lo
-  GroupArgs ga{W, Bt, A, dx, k};
-  if ((s = run_gemm(kModeDx, dy, M, n, &ga, 1, r, alpha, false, nullptr, nullptr, 0, ut_hi,
-                    ut_lo, accumulate, status, st)))
-    return s;
-  // (3) v = x·Aᵀ, recomputed (split over k, reduced in-kernel) -> vᵀ hi/lo
-  auto *counters = reinterpret_cast<uint32_t *>(ws + b.off_counters);
-  if ((s = cuda_status(cudaMemsetAsync(counters, 0, b.counters_bytes, st)))) return s;
-  {
-    SkinnyParams sp;
-    std::memset(&sp, 0, sizeof(sp));
-    SkinnyProblem &P = sp.pr[0];
-    if (!make_map(&P.tm_p, kBF16, 2, x, k, M, (uint64_t)k * 2, 64, 128, true) ||
-        !make_map(&P.tm_q_hi, kBF16, 2, A, k, r, (uint64_t)k * 2, 64, b.rp, true))
-      return LORA_ERR_CUDA;
-    P.tm_q_lo = P.tm_q_hi;
-    P.part = part_v;
-    P.counter = counters;
-    P.out_kind = kOutVt;
-    P.out_hi = vt_hi;
-    P.out_lo = vt_lo;
-    P.out_ld = b.Mp;
-    P.r = r;
-    P.scale = 1.0f;
-    P.rows = M;
-    P.row_tiles = (M + 127) / 128;
-    P.chunks = k / 64;
-    P.max_segs = b.v_max_segs;
-    sp.num_problems = 1;
-    sp.total_items = (long long)P.row_tiles * P.chunks;
-    sp.status = status;
-    if ((s = cuda_status(launch_skinny(sp, false, b.rp, b.v_grid, st)))) return s;
+lora_status_t bwd_v(const BwdCall &c, cudaStream_t st) {
+  const BwdPlan &b = c.b;
+  SkinnyParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  SkinnyProblem &P = sp.pr[0];
+  if (!make_map(&P.tm_p, kBF16, 2, c.x, c.k, c.M, (uint64_t)c.k * 2, 64, 128, true) ||
+      !make_map(&P.tm_q_hi, kBF16, 2, c.A, c.k, c.rl, (uint64_t)c.k * 2, 64, b.rp, true))
+    return LORA_ERR_CUDA;
+  P.tm_q_lo = P.tm_q_hi;
+  P.part = c.at<float>(b.off_part_v);
+  P.counter = c.at<uint32_t>(b.off_counters);
+  P.out_kind = kOutVt;
+  P.out_hi = c.at<__nv_bfloat16>(b.off_vt_hi);
+  P.out_lo = c.at<__nv_bfloat16>(b.off_vt_lo);
+  P.out_ld = b.Mp;
+  P.r = c.rl;
+  P.nproj = 1;
+  P.scale = 1.0f;
+  P.rows = c.M;
+  P.row_tiles = (c.M + 127) / 128;
+  P.chunks = c.k / 64;
+  P.max_segs = b.v_max_segs;
+  sp.num_problems = 1;
+  sp.total_items = (long long)P.row_tiles * P.chunks;
+  sp.status = c.status;
+  return cuda_status(launch_skinny(sp, false, b.rp, b.v_grid, st));
+}
+
+lora_status_t bwd_dx(const BwdCall &c, cudaStream_t st) {
+  GroupArgs ga{c.W, c.Bt, c.A, c.dx, c.k};
+  GemmOpts o;
+  o.mode = kModeDx;
+  o.act = c.dy;
+  o.M = c.M;
+  o.Kred = c.n;
+  o.ga = &ga;
+  o.ng = 1;
+  if (c.merged) {
+    o.W2 = &c.W2;
+    o.ksplit = c.n1 / 64;
+    o.merged_rank = true;
+    o.need_pair = true;
   }
-  // (4) dA = s·uᵀ·x and dB = s·dYᵀ·v, reduced over tokens (one launch)
-  {
-    SkinnyParams sp;
-    std::memset(&sp, 0, sizeof(sp));
-    SkinnyProblem &PA = sp.pr[0];
-    SkinnyProblem &PB = sp.pr[1];
-    if (!make_map(&PA.tm_p, kBF16, 2, x, k, M, (uint64_t)k * 2, 64, 64, true) ||
-        !make_map(&PA.tm_q_hi, kBF16, 2, ut_hi, M, b.rp, (uint64_t)b.Mp * 2, 64, b.rp, true) ||
-        !make_map(&PA.tm_q_lo, kBF16, 2, ut_lo, M, b.rp, (uint64_t)b.Mp * 2, 64, b.rp, true) ||
-        !make_map(&PB.tm_p, kBF16, 2, dy, n, M, (uint64_t)n * 2, 64, 64, true) ||
-        !make_map(&PB.tm_q_hi, kBF16, 2, vt_hi, M, b.rp, (uint64_t)b.Mp * 2, 64, b.rp, true) ||
-        !make_map(&PB.tm_q_lo, kBF16, 2, vt_lo, M, b.rp, (uint64_t)b.Mp * 2, 64, b.rp, true))
+  o.r_layout = c.rl;
+  o.scale = c.scale;
+  o.ut_hi = c.at<__nv_bfloat16>(c.b.off_ut_hi);
+  o.ut_lo = c.at<__nv_bfloat16>(c.b.off_ut_lo);
+  o.accumulate = c.accumulate;
+  o.status = c.status;
+  return run_gemm(o, st);
+}
+
+lora_status_t bwd_grads(const BwdCall &c, cudaStream_t st) {
+  const BwdPlan &b = c.b;
+  const int M = c.M, k = c.k, n = c.n;
+  SkinnyParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  SkinnyProblem &PA = sp.pr[0];
+  SkinnyProblem &PB = sp.pr[1];
+  if (!make_map(&PA.tm_p, kBF16, 2, c.x, k, M, (uint64_t)k * 2, 64, 64, true) ||
+      !make_map(&PA.tm_q_hi, kBF16, 2, c.at<void>(b.off_ut_hi), M, b.rp, (uint64_t)b.Mp * 2, 64,
+                b.rp, true) ||
+      !make_map(&PA.tm_q_lo, kBF16, 2, c.at<void>(b.off_ut_lo), M, b.rp, (uint64_t)b.Mp * 2, 64,
+                b.rp, true) ||
+      !make_map(&PB.tm_p, kBF16, 2, c.dy, n, M, (uint64_t)n * 2, 64, 64, true) ||
+      !make_map(&PB.tm_q_hi, kBF16, 2, c.at<void>(b.off_vt_hi), M, b.rp, (uint64_t)b.Mp * 2, 64,
+                b.rp, true) ||
+      !make_map(&PB.tm_q_lo, kBF16, 2, c.at<void>(b.off_vt_lo), M, b.rp, (uint64_t)b.Mp * 2, 64,
+                b.rp, true))
+    return LORA_ERR_CUDA;
+  const int mt = (M + 127) / 128;
+  uint32_t *counters = c.at<uint32_t>(b.off_counters);
+  const int nproj = c.merged ? 2 : 1;
+  PA.part = c.at<float>(b.off_part_a);
+  PA.counter = counters + mt;
+  PA.out_kind = kOutRowT;
+  PA.out_f32 = c.dA;
+  PA.out_f32b = c.dA2;
+  PA.r = c.r;
+  PA.nproj = nproj;
+  PA.scale = c.scale;
+  PA.rows = k;
+  PA.row_tiles = (k + 127) / 128;
+  PA.chunks = (M + 63) / 64;
+  PA.max_segs = b.g_max_segs;
+  PB.part = c.at<float>(b.off_part_b);
+  PB.counter = counters + mt + PA.row_tiles;
+  PB.out_kind = kOutRow;
+  PB.out_f32 = c.dB;
+  PB.out_f32b = c.dB2;
+  PB.r = c.r;
+  PB.nproj = nproj;
+  PB.split_row = c.n1;
+  PB.scale = c.scale;
+  PB.rows = n;
+  PB.row_tiles = (n + 127) / 128;
+  PB.chunks = (M + 63) / 64;
+  PB.max_segs = b.g_max_segs;
+  sp.num_problems = 2;
+  sp.total_items = (long long)(PA.row_tiles + PB.row_tiles) * PA.chunks;
+  sp.status = c.status;
+  return cuda_status(launch_skinny(sp, true, b.rp, b.g_grid, st));
+}
+
+// A helper stream (and events to order it against the caller's stream),
+// created once per calling thread and device; the recomputation of
+// v = x·Aᵀ runs on it while the dX GEMM runs on the caller's stream.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+};
+
+lora_status_t side_stream(SideStream **out) {
+  constexpr int kMaxDev = 64;
+  static thread_local SideStream per_dev[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return LORA_ERR_CUDA;
+  SideStream &ss = per_dev[dev];
+  if (!ss.s) {
+    if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess)
       return LORA_ERR_CUDA;
-    const int mt = (M + 127) / 128;
-    PA.part = part_a;
-    PA.counter = counters + mt;
-    PA.out_kind = kOutRowT;
-    PA.out_f32 = dA;
-    PA.r = r;
-    PA.scale = scale;
-    PA.rows = k;
-    PA.row_tiles = (k + 127) / 128;
-    PA.chunks = (M + 63) / 64;
-    PA.max_segs = b.g_max_segs;
-    PB.part = part_b;
-    PB.counter = counters + mt + PA.row_tiles;
-    PB.out_kind = kOutRow;
-    PB.out_f32 = dB;
-    PB.r = r;
-    PB.scale = scale;
-    PB.rows = n;
-    PB.row_tiles = (n + 127) / 128;
-    PB.chunks = (M + 63) / 64;
-    PB.max_segs = b.g_max_segs;
-    sp.num_problems = 2;
-    sp.total_items = (long long)(PA.row_tiles + PB.row_tiles) * PA.chunks;
-    sp.status = status;
-    if ((s = cuda_status(launch_skinny(sp, true, b.rp, b.g_grid, st)))) return s;
+    for (auto &e : ss.ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+        return LORA_ERR_CUDA;
   }
+  *out = &ss;
   return LORA_OK;
+}
+
+// `to` waits for everything issued on `from` so far (event `e`).
+lora_status_t order_after(cudaStream_t to, cudaStream_t from, cudaEvent_t e) {
+  if (cudaEventRecord(e, from) != cudaSuccess) return LORA_ERR_CUDA;
+  return cuda_status(cudaStreamWaitEvent(to, e, 0));
+}
+
+// Run the phases: the x stream for v beside the dX GEMM, then dA/dB.
+// Counters and Bᵀ must already be prepared on `st`.
+lora_status_t run_bwd_phases(const BwdCall &c, cudaStream_t st) {
+  SideStream *side = nullptr;
+  lora_status_t s;
+  if ((s = side_stream(&side))) return s;
+  if ((s = order_after(side->s, st, side->ev[0]))) return s;   // fork
+  if ((s = bwd_v(c, side->s))) return s;
+  if ((s = bwd_dx(c, st))) return s;
+  if ((s = order_after(st, side->s, side->ev[1]))) return s;   // join
+  return bwd_grads(c, st);
 }
 
 size_t bwd_bytes(int M, int k, int n, int r) { return plan_bwd(M, k, n, r, 0).total; }
 
-// Largest backward area over every projection width n' <= n (multiple of 64):
-// the q/k backward runs each projection in the same area.
-size_t bwd_bytes_upto(int M, int k, int n, int r) {
-  size_t best = 0;
-  for (int np = 64; np <= n; np += 64) best = std::max(best, bwd_bytes(M, k, np, r));
-  return best;
+// q/k as one projection of rank 2r: A_qk = [Aq; Ak] [2r, hidden],
+// B_qk = diag(Bq, Bk) [nq+nk, 2r] (forward) or its transpose (backward).
+// Forward workspace: status | A_qk | B_qk.
+struct QkFwdPlan {
+  size_t off_a, off_b, total;
+};
+QkFwdPlan plan_qk_fwd(int k, int n, int r) {
+  QkFwdPlan q{};
+  size_t o = kStatusBytes;
+  q.off_a = o;  o = align256(o + (size_t)2 * r * k * 2);
+  q.off_b = o;  o = align256(o + (size_t)n * 2 * r * 2);
+  q.total = o;
+  return q;
+}
+// Backward workspace: status | rotated dY_qk [M, nq+nk] | A_qk | the
+// rank-2r backward area (whose Bᵀ slot holds diag(Bq, Bk)ᵀ).
+struct QkBwdPlan {
+  size_t off_dy, off_a, off_area, total;
+};
+QkBwdPlan plan_qk_bwd(int M, int k, int n, int r) {
+  QkBwdPlan q{};
+  size_t o = kStatusBytes;
+  q.off_dy = o;   o = align256(o + (size_t)M * n * 2);
+  q.off_a = o;    o = align256(o + (size_t)2 * r * k * 2);
+  q.off_area = o; o += bwd_bytes(M, k, n, 2 * r);
+  q.total = o;
+  return q;
+}
+
+lora_status_t build_a_qk(const void *Aq, const void *Ak, void *A_qk, int r, int k,
+                         cudaStream_t st) {
+  const size_t bytes = (size_t)r * k * 2;
+  lora_status_t s;
+  if ((s = cuda_status(cudaMemcpyAsync(A_qk, Aq, bytes, cudaMemcpyDeviceToDevice, st)))) return s;
+  return cuda_status(cudaMemcpyAsync(static_cast<uint8_t *>(A_qk) + bytes, Ak, bytes,
+                                     cudaMemcpyDeviceToDevice, st));
 }
 
 }  // namespace
@@ -451,14 +597,13 @@ size_t lora_workspace_size(int op, int M, int k, int n, int r) {
   if (M < 1 || k < 1 || n < 1 || !rank_ok(r) || M > (1 << 30)) return 0;
   switch (op) {
     case LORA_OP_FWD:
-    case LORA_OP_QK_ROPE_FWD:
       return kStatusBytes;
     case LORA_OP_BWD:
       return kStatusBytes + bwd_bytes(M, k, n, r);
+    case LORA_OP_QK_ROPE_FWD:
+      return plan_qk_fwd(k, n, r).total;
     case LORA_OP_QK_ROPE_BWD:
-      // rotated dq|dk, then the per-projection backward area (reused by q and k)
-      if (n % 64) return 0;
-      return align256(kStatusBytes + (size_t)M * n * 2) + bwd_bytes_upto(M, k, n, r);
+      return plan_qk_bwd(M, k, n, r).total;
   }
   return 0;
 }
@@ -479,8 +624,17 @@ lora_status_t lora_linear_fwd(const void *x, lora_weight_t W, const void *A, con
   if (!std::isfinite(alpha)) return LORA_ERR_INVALID_ARG;
   if (ws_bytes < lora_workspace_size(LORA_OP_FWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
   GroupArgs ga{W, A, B, y, n};
-  return run_gemm(kModeFwd, x, M, k, &ga, 1, r, alpha, false, nullptr, nullptr, 0, nullptr,
-                  nullptr, 0, static_cast<uint32_t *>(ws), reinterpret_cast<cudaStream_t>(stream));
+  GemmOpts o;
+  o.mode = kModeFwd;
+  o.act = x;
+  o.M = M;
+  o.Kred = k;
+  o.ga = &ga;
+  o.ng = 1;
+  o.r_layout = r;
+  o.scale = alpha / (float)r;
+  o.status = static_cast<uint32_t *>(ws);
+  return run_gemm(o, reinterpret_cast<cudaStream_t>(stream));
 }
 
 lora_status_t lora_linear_bwd(const void *x, lora_weight_t W, const void *A, const void *B,
@@ -497,9 +651,36 @@ lora_status_t lora_linear_bwd(const void *x, lora_weight_t W, const void *A, con
   if (ws_bytes < lora_workspace_size(LORA_OP_BWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
   DeviceInfo di;
   if ((s = device_info(&di))) return s;
-  return run_bwd(x, W, A, B, dy, dx, accumulate_dx, dA, dB, M, k, n, r, alpha,
-                 static_cast<uint8_t *>(ws), kStatusBytes, static_cast<uint32_t *>(ws),
-                 reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *w8 = static_cast<uint8_t *>(ws);
+  BwdCall c{};
+  c.x = x;
+  c.A = A;
+  c.dy = dy;
+  c.W = W;
+  c.merged = false;
+  c.dx = dx;
+  c.accumulate = accumulate_dx;
+  c.dA = dA;
+  c.dB = dB;
+  c.M = M;
+  c.k = k;
+  c.n = n;
+  c.n1 = n;
+  c.r = r;
+  c.rl = r;
+  c.scale = alpha / (float)r;
+  c.status = static_cast<uint32_t *>(ws);
+  c.b = plan_bwd(M, k, n, r, kStatusBytes);
+  c.ws = w8;
+  c.Bt = c.at<void>(c.b.off_bt);
+  if ((s = cuda_status(cudaMemsetAsync(c.at<uint32_t>(c.b.off_counters), 0, c.b.counters_bytes,
+                                       st))))
+    return s;
+  if ((s = cuda_status(launch_transpose_rank(static_cast<const __nv_bfloat16 *>(B),
+                                             c.at<__nv_bfloat16>(c.b.off_bt), n, r, st))))
+    return s;
+  return run_bwd_phases(c, st);
 }
 
 static lora_status_t check_qk(const void *x, lora_weight_t Wq, const void *Aq, const void *Bq,
@@ -548,9 +729,35 @@ lora_status_t lora_qk_rope_fwd(const void *x, lora_weight_t Wq, const void *Aq, 
     if ((s = cuda_status(launch_rope_cache(c, max_pos, head_dim, rope_theta, st)))) return s;
     cache = c;
   }
-  GroupArgs ga[2] = {{Wq, Aq, Bq, q, nq}, {Wk, Ak, Bk, k_out, nk}};
-  return run_gemm(kModeFwd, x, M, hidden, ga, 2, r, alpha, true, positions, cache,
-                  max_pos, nullptr, nullptr, 0, static_cast<uint32_t *>(ws), st);
+  // one projection of rank 2r over both weights: the rank accumulator
+  // x·A_qkᵀ is formed once per row block and serves the q and k tiles
+  const QkFwdPlan qp = plan_qk_fwd(hidden, nq + nk, r);
+  uint8_t *w8 = static_cast<uint8_t *>(ws);
+  auto *B_qk = reinterpret_cast<__nv_bfloat16 *>(w8 + qp.off_b);
+  if ((s = build_a_qk(Aq, Ak, w8 + qp.off_a, r, hidden, st))) return s;
+  if ((s = cuda_status(launch_blockdiag_rank(static_cast<const __nv_bfloat16 *>(Bq),
+                                             static_cast<const __nv_bfloat16 *>(Bk), B_qk, nq,
+                                             nk, r, false, st))))
+    return s;
+  GroupArgs ga[2] = {{Wq, w8 + qp.off_a, B_qk, q, nq},
+                     {Wk, w8 + qp.off_a, B_qk + (size_t)nq * 2 * r, k_out, nk}};
+  GemmOpts o;
+  o.mode = kModeFwd;
+  o.act = x;
+  o.M = M;
+  o.Kred = hidden;
+  o.ga = ga;
+  o.ng = 2;
+  o.r_layout = 2 * r;
+  o.scale = alpha / (float)r;
+  o.merged_rank = true;
+  o.need_pair = true;
+  o.rope = true;
+  o.positions = positions;
+  o.cos_sin = cache;
+  o.max_pos = max_pos;
+  o.status = static_cast<uint32_t *>(ws);
+  return run_gemm(o, st);
 }
 
 lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq, const void *Bq,
@@ -584,20 +791,52 @@ lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq, 
     if ((s = cuda_status(launch_rope_cache(c, max_pos, head_dim, rope_theta, st)))) return s;
     cache = c;
   }
-  auto *dq_pre = reinterpret_cast<__nv_bfloat16 *>(w8 + kStatusBytes);
-  auto *dk_pre = dq_pre + (size_t)M * nq;
-  if ((s = cuda_status(launch_rope_bwd(static_cast<const __nv_bfloat16 *>(dq), dq_pre, M, nq,
+  // rotate dq, dk back (RoPE is orthogonal) into one [M, nq+nk] gradient
+  const int n = nq + nk;
+  const QkBwdPlan qp = plan_qk_bwd(M, hidden, n, r);
+  auto *dy_qk = reinterpret_cast<__nv_bfloat16 *>(w8 + qp.off_dy);
+  if ((s = cuda_status(launch_rope_bwd(static_cast<const __nv_bfloat16 *>(dq), dy_qk, M, nq, n,
                                        positions, cache, max_pos, status, st))))
     return s;
-  if ((s = cuda_status(launch_rope_bwd(static_cast<const __nv_bfloat16 *>(dk), dk_pre, M, nk,
-                                       positions, cache, max_pos, status, st))))
+  if ((s = cuda_status(launch_rope_bwd(static_cast<const __nv_bfloat16 *>(dk), dy_qk + nq, M, nk,
+                                       n, positions, cache, max_pos, status, st))))
     return s;
-  const size_t area = align256(kStatusBytes + (size_t)M * (nq + nk) * 2);
-  if ((s = run_bwd(x, Wq, Aq, Bq, dq_pre, dx, accumulate_dx, dAq, dBq, M, hidden, nq, r, alpha,
-                   w8, area, status, st)))
+  // then the backward of one projection of rank 2r, W = [Wq; Wk] along the
+  // reduction of dX, with dA/dB split back per projection
+  BwdCall c{};
+  c.x = x;
+  c.A = w8 + qp.off_a;
+  c.dy = dy_qk;
+  c.W = Wq;
+  c.W2 = Wk;
+  c.merged = true;
+  c.dx = dx;
+  c.accumulate = accumulate_dx;
+  c.dA = dAq;
+  c.dB = dBq;
+  c.dA2 = dAk;
+  c.dB2 = dBk;
+  c.M = M;
+  c.k = hidden;
+  c.n = n;
+  c.n1 = nq;
+  c.r = r;
+  c.rl = 2 * r;
+  c.scale = alpha / (float)r;
+  c.status = status;
+  c.b = plan_bwd(M, hidden, n, 2 * r, 0);
+  c.ws = w8 + qp.off_area;
+  c.Bt = c.at<void>(c.b.off_bt);
+  if ((s = build_a_qk(Aq, Ak, w8 + qp.off_a, r, hidden, st))) return s;
+  if ((s = cuda_status(launch_blockdiag_rank(static_cast<const __nv_bfloat16 *>(Bq),
+                                             static_cast<const __nv_bfloat16 *>(Bk),
+                                             c.at<__nv_bfloat16>(c.b.off_bt), nq, nk, r, true,
+                                             st))))
     return s;
-  return run_bwd(x, Wk, Ak, Bk, dk_pre, dx, 1, dAk, dBk, M, hidden, nk, r, alpha, w8, area,
-                 status, st);
+  if ((s = cuda_status(cudaMemsetAsync(c.at<uint32_t>(c.b.off_counters), 0, c.b.counters_bytes,
+                                       st))))
+    return s;
+  return run_bwd_phases(c, st);
 }
 
 lora_status_t nf4_dequant(const uint8_t *codes, const void *absmax, void *w_out, int n, int k,

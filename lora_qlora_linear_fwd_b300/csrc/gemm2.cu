@@ -16,8 +16,6 @@
 //              MMA issuer, whose commits are multicast to both CTAs.
 //   warps 2-5  epilogue of the CTA's own 128 rows (TMEM lanes 0-127).
 //   warps 6-9  NF4 only: decode the CTA's own W half.
-#include <cstdlib>
-
 #include "gemm_common.cuh"
 
 namespace lora {
@@ -34,6 +32,9 @@ struct PairSmem {
   static constexpr int STAGE_BYTES = OFF_C + C_BYTES;
   static constexpr int R2_BYTES = 128 * RP * 2;   // own half of B (FWD) or A (DX)
   static constexpr int SR_BYTES = 128 * RP * 2;   // s·rank of own rows, bf16
+  // K-major rank tiles are stored in column blocks of at most 64 bf16
+  static constexpr int RPB = RP > 64 ? 64 : RP;
+  static constexpr int BLK_BYTES = 128 * RPB * 2;  // one column block of 128 rows
   static constexpr int MISC_BYTES = 1024;
   static constexpr int FIXED = R2_BYTES + SR_BYTES + MISC_BYTES + 1024;
   static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
@@ -45,16 +46,18 @@ struct PairSmem {
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 3, "pipeline depth");
   static_assert(TOTAL <= kSmemLimit, "shared memory budget");
-  static_assert(RP == 32 || RP == 64, "pair MMA needs N a multiple of 32");
+  static_assert(RP == 32 || RP == 64 || RP == 128, "pair MMA needs N a multiple of 32");
 };
 
-template <int MODE, int RP, bool NF4, bool ROPE, bool DB>
+template <int MODE, int RP, bool NF4, bool ROPE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
     lora_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  constexpr bool DB = true;  // two accumulator buffers
   using L = PairSmem<RP, NF4>;
   constexpr int STAGES = L::STAGES;
   constexpr int BN = 256;
-  constexpr int RB = RP * 2;
+  constexpr int RPB = L::RPB;
+  constexpr int RB = RPB * 2;  // bytes per row of one rank column block
   constexpr uint32_t SWR = swz_mode_for_row_bytes(RB);
   constexpr bool DX = MODE == kModeDx;
   constexpr int NUM_DEC_WARPS = NF4 ? 4 : 0;
@@ -137,7 +140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
       for (it.init(p.sched, pair); ok && it.valid(); it.next(), ++tile_count) {
         const int m = it.m(), nt = it.nt();
         const int g = group_of(p, nt);
-        const bool need_rank = it.first_of_m() || g != prev_g;
+        const bool need_rank = it.first_of_m() || (!p.merged_rank && g != prev_g);
         prev_g = g;
         const GemmGroup &G = p.grp[g];
         const int n0 = (nt - G.tile_begin) * BN;
@@ -155,19 +158,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
                                   2 * (L::X_BYTES + (NF4 ? 0 : L::W_BYTES) +
                                        (need_rank ? L::R1_BYTES : 0)));
           tma_load_2d_pair(sx, &p.tm_act, fb, kb * kBK, row0);
+          // DX: the reduction may run over two projections' W (K-groups)
+          const int gk = (DX && p.kgroups > 1 && kb >= p.ksplit) ? 1 : 0;
+          const CUtensorMap *tw = DX ? &p.grp[gk].tm_w : &G.tm_w;
+          const int wk = kb - (gk ? p.ksplit : 0);
           if constexpr (NF4) {
             const uint32_t rb = bar_raw + 8 * stage;
             mbar_arrive_expect_tx(rb, L::C_BYTES);
             if constexpr (DX)  // codes [64 rows of W, 64 bytes = 128 k-columns]
-              tma_load_2d(sx + L::OFF_C, &G.tm_w, rb, nh / 2, kb * kBK);
+              tma_load_2d(sx + L::OFF_C, tw, rb, nh / 2, wk * kBK);
             else               // codes [128 rows of W, 32 bytes]
-              tma_load_2d(sx + L::OFF_C, &G.tm_w, rb, kb * (kBK / 2), nh);
+              tma_load_2d(sx + L::OFF_C, tw, rb, kb * (kBK / 2), nh);
           } else {
             if constexpr (DX) {  // W as MN-major operand: 2 boxes [64 rows x 64]
-              tma_load_2d_pair(sx + L::OFF_W, &G.tm_w, fb, nh, kb * kBK);
-              tma_load_2d_pair(sx + L::OFF_W + 8192, &G.tm_w, fb, nh + 64, kb * kBK);
+              tma_load_2d_pair(sx + L::OFF_W, tw, fb, nh, wk * kBK);
+              tma_load_2d_pair(sx + L::OFF_W + 8192, tw, fb, nh + 64, wk * kBK);
             } else {
-              tma_load_2d_pair(sx + L::OFF_W, &G.tm_w, fb, kb * kBK, nh);
+              tma_load_2d_pair(sx + L::OFF_W, tw, fb, kb * kBK, nh);
             }
           }
           if (need_rank)
@@ -181,8 +188,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
         if constexpr (DX) {  // A [r, k] read MN-major: 2 boxes [RP rows x 64]
           tma_load_2d_pair(base + L::OFF_R2, &G.tm_r2, lead_r2_full, nh, 0);
           tma_load_2d_pair(base + L::OFF_R2 + RP * 128, &G.tm_r2, lead_r2_full, nh + 64, 0);
-        } else {  // B [n, r]: own 128 rows x RP
-          tma_load_2d_pair(base + L::OFF_R2, &G.tm_r2, lead_r2_full, 0, nh);
+        } else {  // B [n, r]: own 128 rows x RP, in column blocks of RPB
+#pragma unroll
+          for (int blk = 0; blk < RP / RPB; ++blk)
+            tma_load_2d_pair(base + L::OFF_R2 + blk * L::BLK_BYTES, &G.tm_r2, lead_r2_full,
+                             blk * RPB, nh);
         }
       }
       // Let every completion the leader multicasts to this CTA land before
@@ -205,7 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
       TileIter it;
       for (it.init(p.sched, pair); ok && it.valid(); it.next(), ++tile_count) {
         const int g = group_of(p, it.nt());
-        const bool need_rank = it.first_of_m() || g != prev_g;
+        const bool need_rank = it.first_of_m() || (!p.merged_rank && g != prev_g);
         prev_g = g;
         // Accumulators alternate between TMEM columns [0,256) and [256,512)
         // so a tile's epilogue overlaps the next tile's main loop.  A tile
@@ -264,12 +274,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
         tc_fence_after();
 #pragma unroll
         for (int kr = 0; kr < RP / 16; ++kr) {
-          const uint64_t dsr = make_sdesc(base + L::OFF_SR + kr * 32, 16, 8 * RB, SWR);
+          const int blk = kr / (RPB / 16), kk = kr % (RPB / 16);
+          const uint64_t dsr =
+              make_sdesc(base + L::OFF_SR + blk * L::BLK_BYTES + kk * 32, 16, 8 * RB, SWR);
           uint64_t db;
           if constexpr (DX)  // A tile MN-major: two boxes of RP rows, 16 K-rows per step
             db = make_sdesc(base + L::OFF_R2 + kr * 2048, RP * 128, 1024, kSw128);
           else
-            db = make_sdesc(base + L::OFF_R2 + kr * 32, 16, 8 * RB, SWR);
+            db = make_sdesc(base + L::OFF_R2 + blk * L::BLK_BYTES + kk * 32, 16, 8 * RB, SWR);
           tc_mma_pair(t_acc, dsr, db, idesc_main, 1u);
         }
         tc_commit_pair(bar_r2_empty, kBoth);
@@ -291,7 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
     for (it.init(p.sched, pair); it.valid(); it.next(), ++tile_count) {
       const int m = it.m(), nt = it.nt();
       const int g = group_of(p, nt);
-      const bool need_rank = it.first_of_m() || g != prev_g;
+      const bool need_rank = it.first_of_m() || (!p.merged_rank && g != prev_g);
       prev_g = g;
       const GemmGroup &G = p.grp[g];
       const int n0 = (nt - G.tile_begin) * BN;
@@ -334,12 +346,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
     TileIter it;
     for (it.init(p.sched, pair); ok && it.valid(); it.next()) {
       const int nt = it.nt();
-      const GemmGroup &G = p.grp[group_of(p, nt)];
-      const int nh = (nt - G.tile_begin) * BN + (int)crank * 128;
+      const GemmGroup &GN = p.grp[group_of(p, nt)];
+      const int nh = (nt - GN.tile_begin) * BN + (int)crank * 128;
       for (int kb = 0; kb < nk; ++kb) {
+        const int gk = (DX && p.kgroups > 1 && kb >= p.ksplit) ? 1 : 0;
+        const GemmGroup &G = DX ? p.grp[gk] : GN;
         int wrow, kblk;
         if constexpr (DX) {
-          wrow = kb * kBK + (dt & 63);
+          wrow = (kb - (gk ? p.ksplit : 0)) * kBK + (dt & 63);
           kblk = (nh >> 6) + (dt >> 6);
         } else {
           wrow = nh + dt;
@@ -378,20 +392,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
   }
 }
 
-// LORA_PAIR_ACC=1 keeps one accumulator buffer (no epilogue overlap); the
-// default alternates two.  Read once.
-static bool pair_double_buffer() {
-  static const bool db = [] {
-    const char *v = std::getenv("LORA_PAIR_ACC");
-    return !(v && v[0] == '1');
-  }();
-  return db;
-}
-
-template <int MODE, int RP, bool NF4, bool ROPE, bool DB>
-static cudaError_t launch_pair_db(const GemmParams &p, int pairs, cudaStream_t st) {
+template <int MODE, int RP, bool NF4, bool ROPE>
+static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t st) {
   using L = PairSmem<RP, NF4>;
-  auto kern = lora_gemm_pair_kernel<MODE, RP, NF4, ROPE, DB>;
+  auto kern = lora_gemm_pair_kernel<MODE, RP, NF4, ROPE>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
@@ -404,15 +408,9 @@ static cudaError_t launch_pair_db(const GemmParams &p, int pairs, cudaStream_t s
 }
 
 template <int MODE, int RP, bool NF4, bool ROPE>
-static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t st) {
-  return pair_double_buffer() ? launch_pair_db<MODE, RP, NF4, ROPE, true>(p, pairs, st)
-                              : launch_pair_db<MODE, RP, NF4, ROPE, false>(p, pairs, st);
-}
-
-template <int MODE, int RP, bool NF4, bool ROPE>
 static int pair_capacity() {
   using L = PairSmem<RP, NF4>;
-  auto kern = lora_gemm_pair_kernel<MODE, RP, NF4, ROPE, true>;
+  auto kern = lora_gemm_pair_kernel<MODE, RP, NF4, ROPE>;
   static int cached = -1;
   if (cached < 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL) !=
@@ -449,6 +447,9 @@ static cudaError_t pair_dispatch(const GemmParams &p, int rp, bool rope, bool nf
   if (rp == 64)
     return nf4 ? pair_dispatch_rope<MODE, 64, true>(p, rope, pairs, cap, st)
                : pair_dispatch_rope<MODE, 64, false>(p, rope, pairs, cap, st);
+  if (rp == 128)
+    return nf4 ? pair_dispatch_rope<MODE, 128, true>(p, rope, pairs, cap, st)
+               : pair_dispatch_rope<MODE, 128, false>(p, rope, pairs, cap, st);
   return cudaErrorInvalidValue;
 }
 

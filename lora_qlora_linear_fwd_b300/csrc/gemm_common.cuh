@@ -61,13 +61,15 @@ LORA_DEV void nf4_decode_piece(uint32_t src, uint32_t dst, float a, const float 
 
 // Rank epilogue for one thread (= one row of the CTA's 128 accumulator
 // lanes): read the RP fp32 columns at `t_rank`, write s·rank as bf16 into
-// row `row` of the K-major operand tile at `sr` (row width 2·RP bytes,
-// matching swizzle), and in the dX mode optionally export the unscaled
-// value as uᵀ hi/lo parts at token `grow`.
+// row `row` of the K-major operand tile at `sr`, and in the dX mode
+// optionally export the unscaled value as uᵀ hi/lo parts at token `grow`.
+// The tile is stored in column blocks of at most 64 bf16 (one 128-byte
+// swizzle row): block b holds columns [64b, 64b+64) of all 128 rows.
 template <int RP>
 LORA_DEV void epi_rank_to_smem(uint32_t t_rank, uint32_t sr, int row, float scale, bool write_ut,
                                __nv_bfloat16 *ut_hi, __nv_bfloat16 *ut_lo, int Mp, int grow) {
-  constexpr int RB = RP * 2;
+  constexpr int RPB = RP > 64 ? 64 : RP;  // columns per block
+  constexpr int RB = RPB * 2;             // bytes per block row
 #pragma unroll
   for (int c = 0; c < RP / 16; ++c) {
     uint32_t r[16];
@@ -77,8 +79,11 @@ LORA_DEV void epi_rank_to_smem(uint32_t t_rank, uint32_t sr, int row, float scal
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * scale, __uint_as_float(r[2 * j + 1]) * scale);
-    st_shared_v4(sr + swz_offset(row, 2 * c, RB), pk[0], pk[1], pk[2], pk[3]);
-    st_shared_v4(sr + swz_offset(row, 2 * c + 1, RB), pk[4], pk[5], pk[6], pk[7]);
+    const int blk = (c * 16) / RPB;
+    const int cc = ((c * 16) % RPB) / 8;  // 16-byte chunk within the block row
+    const uint32_t sb = sr + blk * (128 * RB);
+    st_shared_v4(sb + swz_offset(row, cc, RB), pk[0], pk[1], pk[2], pk[3]);
+    st_shared_v4(sb + swz_offset(row, cc + 1, RB), pk[4], pk[5], pk[6], pk[7]);
     if (write_ut) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {

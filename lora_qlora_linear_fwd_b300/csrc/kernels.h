@@ -36,6 +36,14 @@ struct alignas(64) GemmParams {
   int M;
   int K;          // reduction length: k (FWD) or n (DX)
   float scale;    // s = alpha / r
+  // Two projections sharing x as ONE projection of rank 2r (A = [A1; A2],
+  // B = diag(B1, B2)): the rank accumulator is formed once per m-block
+  // rather than again at the group switch.
+  int merged_rank;
+  // DX mode: W rows (the reduction) come from grp[0].tm_w for 64-chunks
+  // [0, ksplit) and from grp[1].tm_w after, when kgroups == 2.
+  int kgroups;
+  int ksplit;
   Schedule sched;
   // DX mode
   __nv_bfloat16 *ut_hi;  // uᵀ [RP, M] high bf16 part (unscaled), written once per m-block
@@ -67,8 +75,10 @@ int gemm_pair_capacity(int mode, int rp, bool rope, bool nf4);  // max co-reside
 // row tile (atomic counter) adds the slices in slice order (deterministic)
 // and writes the final output:
 //   kOutVt:   vᵀ as bf16 hi/lo [RP, ld] (the operand of the dB pass)
-//   kOutRowT: out[j][o] = scale·g[o][j], j < r   (dA [r, k])
-//   kOutRow:  out[o][j] = scale·g[o][j], j < r   (dB [n, r])
+//   kOutRowT: out[j][o] = scale·g[o][j], j < r   (dA [r, k]); merged q/k:
+//             columns [r, 2r) go to out_f32b
+//   kOutRow:  out[o][j] = scale·g[o][j], j < r   (dB [n, r]); merged q/k:
+//             rows >= split_row go to out_f32b from columns [r, 2r)
 enum SkinnyOut { kOutVt = 0, kOutRowT = 1, kOutRow = 2 };
 
 struct alignas(64) SkinnyProblem {
@@ -77,12 +87,15 @@ struct alignas(64) SkinnyProblem {
   CUtensorMap tm_q_lo;
   float *part;           // [row_tiles, max_segs, 128, RP] fp32 partials
   uint32_t *counter;     // [row_tiles] arrival counters (zero on entry, reset on exit)
-  float *out_f32;        // kOutRowT / kOutRow
+  float *out_f32;        // kOutRowT / kOutRow: projection 0
+  float *out_f32b;       // kOutRowT / kOutRow: projection 1 (merged q/k), else null
   __nv_bfloat16 *out_hi; // kOutVt
   __nv_bfloat16 *out_lo;
   int out_kind;
   int out_ld;            // leading dimension of the vᵀ output (Mp)
-  int r;                 // real rank (columns written)
+  int r;                 // rank of one projection (columns written per projection)
+  int nproj;             // 1, or 2 for two projections merged as rank 2r
+  int split_row;         // kOutRow with nproj == 2: first output row of projection 1
   float scale;
   int rows;              // output rows (T for KMAJOR, Mo for MNMAJOR)
   int row_tiles;         // ceil(rows / 128)
@@ -107,8 +120,11 @@ cudaError_t launch_skinny(const SkinnyParams &p, bool mn_major, int rp, int grid
 cudaError_t launch_transpose_rank(const __nv_bfloat16 *B, __nv_bfloat16 *Bt, int n, int r,
                                   cudaStream_t st);
 cudaError_t launch_rope_bwd(const __nv_bfloat16 *dy, __nv_bfloat16 *out, int M, int ncols,
-                            const int32_t *pos, const float *cos_sin, int max_pos,
+                            int out_ld, const int32_t *pos, const float *cos_sin, int max_pos,
                             uint32_t *status, cudaStream_t st);
+cudaError_t launch_blockdiag_rank(const __nv_bfloat16 *B1, const __nv_bfloat16 *B2,
+                                  __nv_bfloat16 *out, int n1, int n2, int r, bool transpose,
+                                  cudaStream_t st);
 cudaError_t launch_rope_cache(float *cos_sin, int max_pos, int head_dim, double theta,
                               cudaStream_t st);
 cudaError_t launch_nf4_dequant(const uint8_t *codes, const __nv_bfloat16 *absmax,

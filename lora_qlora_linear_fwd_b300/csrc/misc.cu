@@ -33,9 +33,11 @@ cudaError_t launch_transpose_rank(const __nv_bfloat16 *B, __nv_bfloat16 *Bt, int
 
 // ------------------------------------------------------------- RoPE backward
 // out = R(pos)ᵀ · dy per 128-wide head (inverse rotate-half), bf16 in/out.
-// One thread per (row, head, group of 8 pair indices).
+// dy rows have ncols elements; out rows start out_ld elements apart (so two
+// projections can be written side by side).  One thread per (row, head,
+// group of 8 pair indices).
 __global__ void rope_bwd_kernel(const __nv_bfloat16 *__restrict__ dy,
-                                __nv_bfloat16 *__restrict__ out, int M, int ncols,
+                                __nv_bfloat16 *__restrict__ out, int M, int ncols, int out_ld,
                                 const int32_t *__restrict__ pos, const float *__restrict__ cs,
                                 int max_pos, uint32_t *status) {
   const int heads = ncols / 128;
@@ -54,6 +56,7 @@ __global__ void rope_bwd_kernel(const __nv_bfloat16 *__restrict__ dy,
     const float *c = cs + (size_t)p * 128 + g * 8;
     const float *s = c + 64;
     const size_t o = (size_t)m * ncols + h * 128 + g * 8;
+    const size_t oo = (size_t)m * out_ld + h * 128 + g * 8;
     const uint4 ua = *reinterpret_cast<const uint4 *>(dy + o);
     const uint4 ub = *reinterpret_cast<const uint4 *>(dy + o + 64);
     const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&ua);
@@ -73,17 +76,54 @@ __global__ void rope_bwd_kernel(const __nv_bfloat16 *__restrict__ dy,
       oa[e] = pack_bf16x2(a0 * x0 + b0 * y0, a1 * x1 + b1 * y1);
       ob[e] = pack_bf16x2(b0 * x0 - a0 * y0, b1 * x1 - a1 * y1);
     }
-    *reinterpret_cast<uint4 *>(out + o) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-    *reinterpret_cast<uint4 *>(out + o + 64) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    *reinterpret_cast<uint4 *>(out + oo) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    *reinterpret_cast<uint4 *>(out + oo + 64) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
   }
 }
 
 cudaError_t launch_rope_bwd(const __nv_bfloat16 *dy, __nv_bfloat16 *out, int M, int ncols,
-                            const int32_t *pos, const float *cos_sin, int max_pos,
+                            int out_ld, const int32_t *pos, const float *cos_sin, int max_pos,
                             uint32_t *status, cudaStream_t st) {
   const size_t total = (size_t)M * (ncols / 128) * 8;
   const int grid = grid_for(total, 256, 148 * 16);
-  rope_bwd_kernel<<<grid, 256, 0, st>>>(dy, out, M, ncols, pos, cos_sin, max_pos, status);
+  rope_bwd_kernel<<<grid, 256, 0, st>>>(dy, out, M, ncols, out_ld, pos, cos_sin, max_pos, status);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------ block-diagonal pair of B factors
+// Two projections sharing x taken as one projection of rank 2r:
+// B = diag(B1, B2) with B1 [n1, r], B2 [n2, r].  transpose == 0 writes
+// B [n1+n2, 2r]; transpose == 1 writes Bᵀ [2r, n1+n2].
+__global__ void blockdiag_rank_kernel(const __nv_bfloat16 *__restrict__ B1,
+                                      const __nv_bfloat16 *__restrict__ B2,
+                                      __nv_bfloat16 *__restrict__ out, int n1, int n2, int r,
+                                      int transpose) {
+  const int n = n1 + n2, r2 = 2 * r;
+  const size_t total = (size_t)n * r2;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    int o, j;
+    if (transpose) {
+      j = (int)(i / n);
+      o = (int)(i % n);
+    } else {
+      o = (int)(i / r2);
+      j = (int)(i % r2);
+    }
+    __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
+    if (o < n1 && j < r) v = B1[(size_t)o * r + j];
+    else if (o >= n1 && j >= r) v = B2[(size_t)(o - n1) * r + (j - r)];
+    out[i] = v;
+  }
+}
+
+cudaError_t launch_blockdiag_rank(const __nv_bfloat16 *B1, const __nv_bfloat16 *B2,
+                                  __nv_bfloat16 *out, int n1, int n2, int r, bool transpose,
+                                  cudaStream_t st) {
+  const size_t total = (size_t)(n1 + n2) * 2 * r;
+  blockdiag_rank_kernel<<<grid_for(total, 256, 4096), 256, 0, st>>>(B1, B2, out, n1, n2, r,
+                                                                    transpose ? 1 : 0);
   note_launch();
   return cudaGetLastError();
 }

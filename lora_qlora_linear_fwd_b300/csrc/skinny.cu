@@ -67,15 +67,31 @@ LORA_DEV void skinny_store16(const SkinnyProblem &P, int orow, int j0, const flo
     }
   } else if (P.out_kind == kOutRowT) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j0 + j < P.r) P.out_f32[(size_t)(j0 + j) * P.rows + orow] = v[j] * P.scale;
+    for (int j = 0; j < 16; ++j) {
+      const int jg = j0 + j;
+      if (jg < P.nproj * P.r) {
+        const int pr = jg / P.r, jj = jg % P.r;
+        float *out = pr ? P.out_f32b : P.out_f32;
+        out[(size_t)jj * P.rows + orow] = v[j] * P.scale;
+      }
+    }
   } else {
-    float4 *dst = reinterpret_cast<float4 *>(P.out_f32 + (size_t)orow * P.r + j0);
+    // dB: only the diagonal block of a merged pair is a real gradient
+    const int pr = (P.nproj > 1 && orow >= P.split_row) ? 1 : 0;
+    const int lo = pr * P.r;
+    if (j0 + 16 <= lo || j0 >= lo + P.r) return;
+    float *out = (pr ? P.out_f32b : P.out_f32) + (size_t)(orow - pr * P.split_row) * P.r;
+    if (j0 >= lo && j0 + 16 <= lo + P.r) {
+      float4 *dst = reinterpret_cast<float4 *>(out + (j0 - lo));
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (j0 + 4 * j < P.r)
+      for (int j = 0; j < 4; ++j)
         dst[j] = make_float4(v[4 * j] * P.scale, v[4 * j + 1] * P.scale, v[4 * j + 2] * P.scale,
                              v[4 * j + 3] * P.scale);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j0 + j >= lo && j0 + j < lo + P.r) out[j0 + j - lo] = v[j] * P.scale;
+    }
   }
 }
 
@@ -248,34 +264,31 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
       epi_bar();  // read before any warp can reach the next segment's wait
       if (failed) break;
       tc_fence_after();
-      float v[RP];
+      float *part_tile = P.part + (size_t)ip0.rt * P.max_segs * 128 * RP;
+      float *my_part = part_tile + ((size_t)slot * 128 + row) * RP;
+      // drain the accumulator 16 columns at a time: final values if this CTA
+      // is the row tile's only contributor, else its fp32 partial
 #pragma unroll
       for (int c = 0; c < RP / 16; ++c) {
         uint32_t r[16];
         tmem_ld16(tmem + t_lane + b * RP + c * 16, r);
         tmem_ld_wait();
+        float t[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[c * 16 + j] = __uint_as_float(r[j]);
+        for (int j = 0; j < 16; ++j) t[j] = __uint_as_float(r[j]);
+        if (nseg == 1) {
+          skinny_store16(P, orow, c * 16, t);
+        } else if (orow < P.rows) {
+          float4 *dst = reinterpret_cast<float4 *>(my_part + c * 16);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_float4(t[4 * j], t[4 * j + 1], t[4 * j + 2], t[4 * j + 3]);
+        }
       }
       tc_fence_before();
       mbar_arrive(bar_acc_empty + 8 * b);  // TMEM buffer b is free again
 
-      if (nseg == 1) {
-#pragma unroll
-        for (int c = 0; c < RP / 16; ++c) {
-          float t[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) t[j] = v[c * 16 + j];
-          skinny_store16(P, orow, c * 16, t);
-        }
-      } else {
-        float *part_tile = P.part + (size_t)ip0.rt * P.max_segs * 128 * RP;
-        if (orow < P.rows) {
-          float4 *dst = reinterpret_cast<float4 *>(part_tile + ((size_t)slot * 128 + row) * RP);
-#pragma unroll
-          for (int j = 0; j < RP / 4; ++j)
-            dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        }
+      if (nseg > 1) {
         __threadfence();
         epi_bar();
         if (threadIdx.x == 64)
@@ -284,27 +297,22 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
         if (*last_flag) {
           __threadfence();
           // add the segments in segment order, 16 columns at a time
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < RP / 16; ++c) {
             float sum[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) sum[j] = 0.0f;
             if (orow < P.rows) {
               for (int s = 0; s < nseg; ++s) {
-                if (s == slot) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    part_tile + ((size_t)s * 128 + row) * RP + c * 16);
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) sum[j] += v[c * 16 + j];
-                } else {
-                  const float4 *src = reinterpret_cast<const float4 *>(
-                      part_tile + ((size_t)s * 128 + row) * RP + c * 16);
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    const float4 t = __ldcg(src + j);
-                    sum[4 * j] += t.x;
-                    sum[4 * j + 1] += t.y;
-                    sum[4 * j + 2] += t.z;
-                    sum[4 * j + 3] += t.w;
-                  }
+                for (int j = 0; j < 4; ++j) {
+                  const float4 t = __ldcg(src + j);
+                  sum[4 * j] += t.x;
+                  sum[4 * j + 1] += t.y;
+                  sum[4 * j + 2] += t.z;
+                  sum[4 * j + 3] += t.w;
                 }
               }
             }
@@ -345,6 +353,7 @@ cudaError_t launch_skinny(const SkinnyParams &p, bool mn_major, int rp, int grid
     case 16: return mn_major ? launch_skinny_t<true, 16>(p, grid, st) : launch_skinny_t<false, 16>(p, grid, st);
     case 32: return mn_major ? launch_skinny_t<true, 32>(p, grid, st) : launch_skinny_t<false, 32>(p, grid, st);
     case 64: return mn_major ? launch_skinny_t<true, 64>(p, grid, st) : launch_skinny_t<false, 64>(p, grid, st);
+    case 128: return mn_major ? launch_skinny_t<true, 128>(p, grid, st) : launch_skinny_t<false, 128>(p, grid, st);
   }
   return cudaErrorInvalidValue;
 }

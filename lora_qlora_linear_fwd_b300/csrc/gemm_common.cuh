@@ -1,7 +1,6 @@
-// Device helpers shared by the one-SM and two-SM fused GEMM kernels:
-// the NF4 level table and row decode, the rank-r epilogue (s·rank -> bf16
-// operand tile in shared memory, plus the uᵀ export of the dX mode) and the
-// output epilogue (TMEM -> optional rotate-half RoPE -> bf16 -> global).
+// Device helpers of the fused GEMM kernel: the NF4 level table and row
+// decode, and the output epilogue (TMEM -> optional rotate-half RoPE ->
+// bf16 -> global).
 #pragma once
 
 #include "kernels.h"
@@ -15,10 +14,6 @@ static __constant__ float kNf4Levels[16] = {
     -0.28444138169288635f, -0.18477343022823334f, -0.09105003625154495f, 0.0f,
     0.07958029955625534f, 0.16093020141124725f, 0.24611230194568634f, 0.33791524171829224f,
     0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
-
-constexpr uint32_t swz_mode_for_row_bytes(int rb) {
-  return rb == 128 ? kSw128 : (rb == 64 ? kSw64 : kSw32);
-}
 
 LORA_DEV bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                         uint32_t *status) {
@@ -56,45 +51,6 @@ LORA_DEV void nf4_decode_piece(uint32_t src, uint32_t dst, float a, const float 
       o[b] = pack_bf16x2(levels[byte >> 4] * a, levels[byte & 0xFu] * a);
     }
     st_shared_v4(dst + ((((uint32_t)ch) ^ phase) << 4), o[0], o[1], o[2], o[3]);
-  }
-}
-
-// Rank epilogue for one thread (= one row of the CTA's 128 accumulator
-// lanes): read the RP fp32 columns at `t_rank`, write s·rank as bf16 into
-// row `row` of the K-major operand tile at `sr`, and in the dX mode
-// optionally export the unscaled value as uᵀ hi/lo parts at token `grow`.
-// The tile is stored in column blocks of at most 64 bf16 (one 128-byte
-// swizzle row): block b holds columns [64b, 64b+64) of all 128 rows.
-template <int RP>
-LORA_DEV void epi_rank_to_smem(uint32_t t_rank, uint32_t sr, int row, float scale, bool write_ut,
-                               __nv_bfloat16 *ut_hi, __nv_bfloat16 *ut_lo, int Mp, int grow) {
-  constexpr int RPB = RP > 64 ? 64 : RP;  // columns per block
-  constexpr int RB = RPB * 2;             // bytes per block row
-#pragma unroll
-  for (int c = 0; c < RP / 16; ++c) {
-    uint32_t r[16];
-    tmem_ld16(t_rank + c * 16, r);
-    tmem_ld_wait();
-    uint32_t pk[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * scale, __uint_as_float(r[2 * j + 1]) * scale);
-    const int blk = (c * 16) / RPB;
-    const int cc = ((c * 16) % RPB) / 8;  // 16-byte chunk within the block row
-    const uint32_t sb = sr + blk * (128 * RB);
-    st_shared_v4(sb + swz_offset(row, cc, RB), pk[0], pk[1], pk[2], pk[3]);
-    st_shared_v4(sb + swz_offset(row, cc + 1, RB), pk[4], pk[5], pk[6], pk[7]);
-    if (write_ut) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float u = __uint_as_float(r[j]);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(u);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(u - __bfloat162float(hi));
-        const size_t idx = (size_t)(c * 16 + j) * Mp + grow;
-        ut_hi[idx] = hi;
-        ut_lo[idx] = lo;
-      }
-    }
   }
 }
 

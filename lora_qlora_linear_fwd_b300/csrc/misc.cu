@@ -1,6 +1,6 @@
-// Small kernels around the fused GEMMs: slice reductions of the rank-r
-// passes, the inverse RoPE rotation of incoming gradients, the cos/sin cache
-// builder, the Bᵀ copy, and the standalone NF4 dequantise / quantise.
+// Small kernels around the fused GEMMs: the backward set-up (inverse RoPE
+// rotation of incoming gradients, merged A and Bᵀ), the cos/sin
+// cache builder, and the standalone NF4 dequantise / quantise.
 #include "kernels.h"
 
 namespace lora {
@@ -10,120 +10,83 @@ static int grid_for(size_t items, int per_block, int cap) {
   return (int)(g < (size_t)cap ? (g > 0 ? g : 1) : (size_t)cap);
 }
 
-// ---------------------------------------------------------------- Bᵀ copy
-// Bt [r, n] <- B [n, r]
-__global__ void transpose_rank_kernel(const __nv_bfloat16 *__restrict__ B,
-                                      __nv_bfloat16 *__restrict__ Bt, int n, int r) {
-  const size_t total = (size_t)n * r;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const int j = (int)(i / n), c = (int)(i % n);  // output index: row j, column c
-    Bt[i] = B[(size_t)c * r + j];
+// ------------------------------------------------------- backward set-up
+// Everything the backward needs before its GEMM and rank-r passes, in one
+// launch (three independent jobs over one flat index space):
+//   rope     dY[:, :n1] = R(pos)ᵀ·dy1, dY[:, n1:] = R(pos)ᵀ·dy2 (inverse
+//            rotate-half per 128-wide head; one item = one row, head and
+//            group of 8 pair indices)
+//   A        A_out = [A1; A2] (two projections merged as rank 2r)
+//   Bᵀ       Bt [nproj·r, n] = diag(B1, B2)ᵀ (just B1ᵀ for one projection)
+LORA_DEV void rope_bwd_item(const BwdPrep &p, size_t i) {
+  const int hq = p.n1 / 128, hk = p.n2 / 128, heads = hq + hk;
+  const int g = (int)(i % 8);
+  const size_t mh = i / 8;
+  const int h = (int)(mh % heads);
+  const int m = (int)(mh / heads);
+  int pos = p.pos[m];
+  if (pos < 0 || pos >= p.max_pos) {
+    atomicOr(p.status, kDevBadPosition);
+    pos = 0;
   }
-}
-
-cudaError_t launch_transpose_rank(const __nv_bfloat16 *B, __nv_bfloat16 *Bt, int n, int r,
-                                  cudaStream_t st) {
-  const size_t total = (size_t)n * r;
-  const int grid = grid_for(total, 256, 4096);
-  transpose_rank_kernel<<<grid, 256, 0, st>>>(B, Bt, n, r);
-  note_launch();
-  return cudaGetLastError();
-}
-
-// ------------------------------------------------------------- RoPE backward
-// out = R(pos)ᵀ · dy per 128-wide head (inverse rotate-half), bf16 in/out.
-// dy rows have ncols elements; out rows start out_ld elements apart (so two
-// projections can be written side by side).  One thread per (row, head,
-// group of 8 pair indices).
-__global__ void rope_bwd_kernel(const __nv_bfloat16 *__restrict__ dy,
-                                __nv_bfloat16 *__restrict__ out, int M, int ncols, int out_ld,
-                                const int32_t *__restrict__ pos, const float *__restrict__ cs,
-                                int max_pos, uint32_t *status) {
-  const int heads = ncols / 128;
-  const size_t total = (size_t)M * heads * 8;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const int g = (int)(i % 8);
-    const size_t mh = i / 8;
-    const int h = (int)(mh % heads);
-    const int m = (int)(mh / heads);
-    int p = pos[m];
-    if (p < 0 || p >= max_pos) {
-      atomicOr(status, kDevBadPosition);
-      p = 0;
-    }
-    const float *c = cs + (size_t)p * 128 + g * 8;
-    const float *s = c + 64;
-    const size_t o = (size_t)m * ncols + h * 128 + g * 8;
-    const size_t oo = (size_t)m * out_ld + h * 128 + g * 8;
-    const uint4 ua = *reinterpret_cast<const uint4 *>(dy + o);
-    const uint4 ub = *reinterpret_cast<const uint4 *>(dy + o + 64);
-    const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&ua);
-    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&ub);
-    const float4 c0 = *reinterpret_cast<const float4 *>(c);
-    const float4 c1 = *reinterpret_cast<const float4 *>(c + 4);
-    const float4 s0 = *reinterpret_cast<const float4 *>(s);
-    const float4 s1 = *reinterpret_cast<const float4 *>(s + 4);
-    const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-    uint32_t oa[4], ob[4];
+  const float *c = p.cos_sin + (size_t)pos * 128 + g * 8;
+  const float *s = c + 64;
+  const __nv_bfloat16 *src = h < hq ? p.dy1 + (size_t)m * p.n1 + h * 128
+                                    : p.dy2 + (size_t)m * p.n2 + (h - hq) * 128;
+  __nv_bfloat16 *dst = p.dy_out + (size_t)m * (p.n1 + p.n2) + h * 128;
+  const uint4 ua = *reinterpret_cast<const uint4 *>(src + g * 8);
+  const uint4 ub = *reinterpret_cast<const uint4 *>(src + g * 8 + 64);
+  const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&ua);
+  const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&ub);
+  const float4 c0 = *reinterpret_cast<const float4 *>(c);
+  const float4 c1 = *reinterpret_cast<const float4 *>(c + 4);
+  const float4 s0 = *reinterpret_cast<const float4 *>(s);
+  const float4 s1 = *reinterpret_cast<const float4 *>(s + 4);
+  const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  uint32_t oa[4], ob[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float a0 = __low2float(a2[e]), a1 = __high2float(a2[e]);
-      const float b0 = __low2float(b2[e]), b1 = __high2float(b2[e]);
-      const float x0 = cc[2 * e], x1 = cc[2 * e + 1], y0 = ss[2 * e], y1 = ss[2 * e + 1];
-      oa[e] = pack_bf16x2(a0 * x0 + b0 * y0, a1 * x1 + b1 * y1);
-      ob[e] = pack_bf16x2(b0 * x0 - a0 * y0, b1 * x1 - a1 * y1);
-    }
-    *reinterpret_cast<uint4 *>(out + oo) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-    *reinterpret_cast<uint4 *>(out + oo + 64) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  for (int e = 0; e < 4; ++e) {
+    const float a0 = __low2float(a2[e]), a1 = __high2float(a2[e]);
+    const float b0 = __low2float(b2[e]), b1 = __high2float(b2[e]);
+    const float x0 = cc[2 * e], x1 = cc[2 * e + 1], y0 = ss[2 * e], y1 = ss[2 * e + 1];
+    oa[e] = pack_bf16x2(a0 * x0 + b0 * y0, a1 * x1 + b1 * y1);
+    ob[e] = pack_bf16x2(b0 * x0 - a0 * y0, b1 * x1 - a1 * y1);
   }
+  *reinterpret_cast<uint4 *>(dst + g * 8) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+  *reinterpret_cast<uint4 *>(dst + g * 8 + 64) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
 }
 
-cudaError_t launch_rope_bwd(const __nv_bfloat16 *dy, __nv_bfloat16 *out, int M, int ncols,
-                            int out_ld, const int32_t *pos, const float *cos_sin, int max_pos,
-                            uint32_t *status, cudaStream_t st) {
-  const size_t total = (size_t)M * (ncols / 128) * 8;
-  const int grid = grid_for(total, 256, 148 * 16);
-  rope_bwd_kernel<<<grid, 256, 0, st>>>(dy, out, M, ncols, out_ld, pos, cos_sin, max_pos, status);
-  note_launch();
-  return cudaGetLastError();
-}
-
-// ------------------------------------------ block-diagonal pair of B factors
-// Two projections sharing x taken as one projection of rank 2r:
-// B = diag(B1, B2) with B1 [n1, r], B2 [n2, r].  transpose == 0 writes
-// B [n1+n2, 2r]; transpose == 1 writes Bᵀ [2r, n1+n2].
-__global__ void blockdiag_rank_kernel(const __nv_bfloat16 *__restrict__ B1,
-                                      const __nv_bfloat16 *__restrict__ B2,
-                                      __nv_bfloat16 *__restrict__ out, int n1, int n2, int r,
-                                      int transpose) {
-  const int n = n1 + n2, r2 = 2 * r;
-  const size_t total = (size_t)n * r2;
+__global__ void bwd_prep_kernel(const BwdPrep p) {
+  const int n = p.n1 + p.n2, rl = p.nproj * p.r;
+  const size_t n_rope = p.dy1 ? (size_t)p.M * (n / 128) * 8 : 0;
+  const size_t n_a = p.nproj > 1 ? (size_t)rl * p.k / 8 : 0;   // 16-byte pieces
+  const size_t n_b = (size_t)rl * n;
+  const size_t total = n_rope + n_a + n_b;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
        i += (size_t)gridDim.x * blockDim.x) {
-    int o, j;
-    if (transpose) {
-      j = (int)(i / n);
-      o = (int)(i % n);
+    if (i < n_rope) {
+      rope_bwd_item(p, i);
+    } else if (i < n_rope + n_a) {
+      const size_t q = i - n_rope, half = (size_t)p.r * p.k / 8;
+      const uint4 *src = reinterpret_cast<const uint4 *>(q < half ? p.A1 : p.A2);
+      reinterpret_cast<uint4 *>(p.A_out)[q] = src[q < half ? q : q - half];
     } else {
-      o = (int)(i / r2);
-      j = (int)(i % r2);
+      const size_t q = i - n_rope - n_a;
+      const int j = (int)(q / n), o = (int)(q % n);   // Bt row j (rank), column o
+      __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
+      if (o < p.n1 && j < p.r) v = p.B1[(size_t)o * p.r + j];
+      else if (o >= p.n1 && j >= p.r) v = p.B2[(size_t)(o - p.n1) * p.r + (j - p.r)];
+      p.Bt[q] = v;
     }
-    __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
-    if (o < n1 && j < r) v = B1[(size_t)o * r + j];
-    else if (o >= n1 && j >= r) v = B2[(size_t)(o - n1) * r + (j - r)];
-    out[i] = v;
   }
 }
 
-cudaError_t launch_blockdiag_rank(const __nv_bfloat16 *B1, const __nv_bfloat16 *B2,
-                                  __nv_bfloat16 *out, int n1, int n2, int r, bool transpose,
-                                  cudaStream_t st) {
-  const size_t total = (size_t)(n1 + n2) * 2 * r;
-  blockdiag_rank_kernel<<<grid_for(total, 256, 4096), 256, 0, st>>>(B1, B2, out, n1, n2, r,
-                                                                    transpose ? 1 : 0);
+cudaError_t launch_bwd_prep(const BwdPrep &p, cudaStream_t st) {
+  const int n = p.n1 + p.n2, rl = p.nproj * p.r;
+  const size_t total = (p.dy1 ? (size_t)p.M * (n / 128) * 8 : 0) +
+                       (p.nproj > 1 ? (size_t)rl * p.k / 8 : 0) + (size_t)rl * n;
+  bwd_prep_kernel<<<grid_for(total, 256, 148 * 16), 256, 0, st>>>(p);
   note_launch();
   return cudaGetLastError();
 }

@@ -204,7 +204,7 @@ LORA_DEV void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 LORA_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 
-// -------------------------------------------------- CTA pairs (clusters of 2)
+// ------------------------------------------------------------ clusters
 LORA_DEV uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -249,7 +249,17 @@ LORA_DEV bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int *abo
     }
   }
 }
-// All threads of both CTAs of the pair.
+// 16-byte load from the shared memory of another CTA of the cluster
+// (address from map_shared_rank).
+LORA_DEV float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+// All threads of every CTA of the cluster.
 LORA_DEV void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");

@@ -43,7 +43,9 @@ def test_status_strings():
 
 
 def test_workspace_sizes():
-    assert L.workspace_size(L.OP_FWD, 256, 512, 512, 8) == 256
+    # forward: status word + the rank block s·x·Aᵀ [M, r] bf16
+    assert L.workspace_size(L.OP_FWD, 256, 512, 512, 8) == 256 + 256 * 8 * 2
+    assert L.workspace_size(L.OP_QK_ROPE_FWD, 256, 512, 512, 8) == 256 + 256 * 16 * 2
     b = L.workspace_size(L.OP_BWD, 256, 512, 512, 8)
     assert b > 256 and b % 256 == 0
     assert L.workspace_size(L.OP_BWD, 8192, 4096, 4096, 64) > L.workspace_size(
@@ -59,7 +61,7 @@ def _w(ptr=FAKE, typ=0, absmax=None, bs=0):
     return L.Weight(typ, ptr, absmax, bs)
 
 
-def _fwd(M=256, k=512, n=512, r=8, x=FAKE, W=None, A=FAKE, B=FAKE, y=FAKE, ws=FAKE, wsb=256,
+def _fwd(M=256, k=512, n=512, r=8, x=FAKE, W=None, A=FAKE, B=FAKE, y=FAKE, ws=FAKE, wsb=1 << 20,
          alpha=16.0):
     return lib.lora_linear_fwd(x, W or _w(), A, B, y, M, k, n, r, alpha, ws, wsb, None)
 
@@ -67,7 +69,7 @@ def _fwd(M=256, k=512, n=512, r=8, x=FAKE, W=None, A=FAKE, B=FAKE, y=FAKE, ws=FA
 @pytest.mark.parametrize("kw,expect", [
     (dict(M=0), 1), (dict(k=-64), 1), (dict(k=100), 2), (dict(n=96), 2), (dict(r=12), 2),
     (dict(r=128), 2), (dict(x=0), 1), (dict(x=MIS), 1), (dict(y=MIS), 1), (dict(A=0), 1),
-    (dict(ws=0), 1), (dict(wsb=255), 3), (dict(alpha=float("nan")), 1),
+    (dict(ws=0), 1), (dict(wsb=4351), 3), (dict(alpha=float("nan")), 1),
     (dict(W=L.Weight(7, FAKE, None, 0)), 1),
     (dict(W=L.Weight(1, FAKE, None, 64)), 1),            # NF4 without absmax
     (dict(W=L.Weight(1, FAKE, FAKE, 128)), 2),           # NF4 block size other than 64

@@ -24,10 +24,10 @@
  *     accumulation is float32 on the tensor cores; rounding to bf16 is
  *     round-to-nearest-even.
  *   - Every pointer is a DEVICE pointer owned by the caller, 16-byte
- *     aligned.  The library allocates no memory and keeps no state between
- *     calls other than a host-side cache of TMA descriptors keyed by pointer
- *     and shape (safe to drop; it never dereferences stale pointers because
- *     every key includes the pointer and extents passed in the call).
+ *     aligned.  The library allocates no device memory (except the fixed
+ *     scratch of lora_linear_bwd_noalloc) and keeps no state between calls
+ *     other than per-device properties; TMA descriptors are encoded from
+ *     the arguments on every call.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  Argument errors are returned before anything is
  *     launched.  LORA_ERR_CUDA reports a launch error seen immediately.
@@ -39,11 +39,8 @@
  *   - Shape limits: k % 64 == 0, n % 64 == 0, 1 <= M <= 2^30, r in
  *     {8, 16, 32, 64}, head_dim == 128; NF4 needs blocksize == 64.
  *   - Calls on the same workspace must not overlap on the GPU (use one
- *     stream, or one workspace per stream).
- *   - The backward entry points run their rank-r passes partly on a helper
- *     stream (one per calling thread and device, created on first use with
- *     two events), forked from and joined back into `stream` with events:
- *     all their work is ordered before later work on `stream`.
+ *     stream, or one workspace per stream).  Every launch of a call goes to
+ *     `stream`, in order.
  */
 #ifndef LORA_B300_H
 #define LORA_B300_H
@@ -101,11 +98,13 @@ enum {
 size_t lora_workspace_size(int op, int M, int k, int n, int r);
 
 /* Fused forward, [P1] 算子融合:  y = x·Wᵀ + s·(x·Aᵀ)·Bᵀ.
- * One persistent kernel: per output tile the base GEMM x·Wᵀ and the rank-r
- * down-projection v = x·Aᵀ accumulate in tensor memory, then (s·v)·Bᵀ is
- * added to the same accumulator before the single bf16 store of y.  No
- * intermediate goes to HBM.  An NF4 W is decoded tile by tile in shared
- * memory ([P3] 显存优化策略).
+ * Two launches.  The rank pass streams x once and writes the rank block
+ * s·v = s·x·Aᵀ [M,r] (bf16, in the workspace: 2·M·r bytes, 1/(k/r) of x).
+ * The fused GEMM then reduces each output tile over the concatenated axis
+ * y = [x | s·v]·[W | B]ᵀ: base product and adapter land in the same fp32
+ * tensor-memory accumulator before the single bf16 store of y, so neither
+ * x·Wᵀ nor the adapter output goes to HBM.  An NF4 W is decoded tile by tile
+ * in shared memory ([P3] 显存优化策略).
  *   x [M,k] bf16, W per lora_weight_t, A [r,k] bf16, B [n,r] bf16,
  *   y [M,n] bf16 (overwritten).  ws: >= lora_workspace_size(LORA_OP_FWD,...). */
 lora_status_t lora_linear_fwd(const void *x, lora_weight_t W, const void *A,
@@ -115,10 +114,9 @@ lora_status_t lora_linear_fwd(const void *x, lora_weight_t W, const void *A,
 
 /* Fused backward, [P1] 反向传播优化 (gradients derived from the forward; the
  * page's printed formulas have a garbled operand order and no scale):
- *   u  = dY·B                      (computed inside the dX kernel)
- *   dX = dY·W + s·u·A              (accumulate_dx != 0: dX += that)
- *   v  = x·Aᵀ                      (recomputed here, never cached)
- *   dA = s·uᵀ·x,   dB = s·dYᵀ·v    (overwritten, float32)
+ *   u  = dY·B, v = x·Aᵀ            (one rank pass; v recomputed, never cached)
+ *   dX = [dY | s·u]·[W ; A]        (= dY·W + s·u·A; accumulate_dx != 0: dX += that)
+ *   dA = s·uᵀ·x,   dB = s·dYᵀ·v    (one pass; overwritten, float32)
  * W is frozen: no weight gradient.  x [M,k], dy [M,n], dx [M,k] bf16;
  * dA [r,k], dB [n,r] float32.  ws: >= lora_workspace_size(LORA_OP_BWD,...). */
 lora_status_t lora_linear_bwd(const void *x, lora_weight_t W, const void *A,
@@ -128,7 +126,8 @@ lora_status_t lora_linear_bwd(const void *x, lora_weight_t W, const void *A,
                               size_t ws_bytes, lora_stream_t stream);
 
 /* q/k projections with RoPE, [P1] RoPE缓存集成: q = R(pos)·(x·Wqᵀ + s·(x·Aqᵀ)·Bqᵀ)
- * and the same for k, in ONE launch (both projections read the same x).
+ * and the same for k: one rank pass for both (s·x·[Aq; Ak]ᵀ, [M,2r] in the
+ * workspace), then ONE fused GEMM launch over both weights.
  * The rotation is applied in the epilogue to each 128-wide head, pairing
  * columns (i, i+64): y'[i] = y[i]·cos − y[i+64]·sin, y'[i+64] = y[i+64]·cos +
  * y[i]·sin, angle = pos[m]·theta^(−2i/128).
@@ -148,9 +147,10 @@ lora_status_t lora_qk_rope_fwd(const void *x, lora_weight_t Wq, const void *Aq,
                                void *ws, size_t ws_bytes, lora_stream_t stream);
 
 /* Backward of lora_qk_rope_fwd: the incoming dq, dk are rotated back by the
- * transposed rotation R(pos)ᵀ, then each projection runs the backward of
- * lora_linear_bwd; dX sums both projections (accumulate_dx != 0: dX += the
- * sum).  dAq, dBq, dAk, dBk float32, overwritten.  Cache rules as in
+ * transposed rotation R(pos)ᵀ into one [M, nq+nk] gradient; q and k then
+ * run as ONE projection of rank 2r (A = [Aq; Ak], B = diag(Bq, Bk), exact)
+ * through the passes of lora_linear_bwd, with dX reduced over [Wq; Wk] in
+ * one GEMM (accumulate_dx != 0: dX += the sum).  dAq, dBq, dAk, dBk float32, overwritten.  Cache rules as in
  * lora_qk_rope_fwd. */
 lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq,
                                const void *Bq, lora_weight_t Wk, const void *Ak,

@@ -151,9 +151,9 @@ Schedule make_schedule(int m_blocks, int n_tiles, int slots) {
 
 // CTAs per cluster of the rank pass: split the reduction while the grid
 // still fits on the SMs at one CTA each and every CTA keeps >= 8 chunks.
-int pick_split(int tiles, int min_chunks, int sms) {
+int pick_split(int tiles, int min_chunks, int sms, int max_split) {
   int s = 1;
-  while (s < 8 && tiles * s * 2 <= sms && min_chunks >= 8 * s * 2) s *= 2;
+  while (2 * s <= max_split && tiles * s * 2 <= sms && min_chunks >= 8 * s * 2) s *= 2;
   return s;
 }
 
@@ -309,7 +309,7 @@ lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, uint32_t *status, cu
     tiles += sp.pr[q].row_tiles;
     min_chunks = std::min(min_chunks, sp.pr[q].chunks);
   }
-  sp.split = pick_split(tiles, min_chunks, di.sms);
+  sp.split = pick_split(tiles, min_chunks, di.sms, skinny_max_split(mn, rp));
   sp.status = status;
   return cuda_status(launch_skinny(sp, mn, rp, st));
 }

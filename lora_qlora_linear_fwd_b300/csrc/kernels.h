@@ -22,7 +22,7 @@ namespace lora {
 //        out = dX [M, k].
 // NF4 weights: tm_w maps the codes [n, k/2] bytes and absmax points at the
 // bf16 block scales [n, k/64].
-struct alignas(64) GemmGroup {
+struct GemmGroup {
   CUtensorMap tm_w;
   CUtensorMap tm_b;
   __nv_bfloat16 *out;
@@ -35,7 +35,7 @@ struct alignas(64) GemmGroup {
   int n_extra;     // extra 64-wide K-blocks (ceil(rank / 64))
 };
 
-struct alignas(64) GemmParams {
+struct GemmParams {
   CUtensorMap tm_act;  // x [M,k] (FWD) or dY [M,n] (DX): K-major, box 64 x 128
   CUtensorMap tm_sv;   // s·v or s·u [M, rl] bf16: K-major, box 64 x 128
   GemmGroup grp[kMaxGroups];
@@ -83,7 +83,7 @@ int gemm_pair_capacity(int mode, bool rope, bool nf4);  // max co-resident pairs
 //                rows >= split_row go to out_f32b from columns [r, 2r)
 enum SkinnyOut { kOutVt = 1, kOutRowBf16 = 2, kOutRowT = 4, kOutRow = 8 };
 
-struct alignas(64) SkinnyProblem {
+struct SkinnyProblem {
   CUtensorMap tm_p;
   CUtensorMap tm_q;      // Q (MNMAJOR: its hi part)
   CUtensorMap tm_q2;     // MNMAJOR: lo part; KMAJOR with q_rows1 > 0: Q rows [q_rows1, 2·q_rows1)
@@ -106,7 +106,7 @@ struct alignas(64) SkinnyProblem {
   int tile_begin;        // first cluster of this problem
 };
 
-struct alignas(64) SkinnyParams {
+struct SkinnyParams {
   SkinnyProblem pr[2];
   int num_problems;
   int split;             // CTAs per cluster (1, 2, 4 or 8)
@@ -114,6 +114,9 @@ struct alignas(64) SkinnyParams {
 };
 
 cudaError_t launch_skinny(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st);
+// Largest `split` the (mn_major, rp) kernel supports (its epilogue buffers
+// must fit in its pipeline ring).
+int skinny_max_split(bool mn_major, int rp);
 
 // Elementwise / small helpers.
 // Backward set-up (one launch): inverse RoPE of dy1|dy2 into dy_out (when

@@ -259,6 +259,13 @@ LORA_DEV float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
                : "memory");
   return v;
 }
+// 16-byte store into the shared memory of another CTA of the cluster.
+LORA_DEV void st_shared_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c,
+                                   uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
 // All threads of every CTA of the cluster.
 LORA_DEV void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"

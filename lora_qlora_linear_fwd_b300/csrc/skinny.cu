@@ -25,78 +25,133 @@ struct SkinnySmem {
   static constexpr int STAGE_BYTES = P_BYTES + (MN ? 2 : 1) * Q_BYTES;
   static constexpr int STAGES_FIT = (kSmemLimit - 4096) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
-  // fp32 partial of a non-leader CTA: 128 rows, padded by 16 bytes so that
-  // the rows of one 16-byte access pattern fall in different banks
-  static constexpr int RED_STRIDE = RP * 4 + 16;
-  static constexpr int RED_BYTES = 128 * RED_STRIDE;
   static constexpr int OFF_MISC = STAGES * STAGE_BYTES;
   static constexpr int TOTAL = OFF_MISC + 512 + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 4, "pipeline depth");
-  static_assert(RED_BYTES <= OFF_MISC, "partial fits in the ring");
   static_assert(TOTAL <= kSmemLimit, "shared memory budget");
 };
 
-// Columns [j0, j0+16) of output row `orow` (raw sums v) in every output
-// form the problem asks for.
-LORA_DEV void skinny_store16(const SkinnyProblem &P, int orow, int j0, const float (&v)[16]) {
-  if (orow >= P.rows) return;
+// Epilogue buffers, laid over the (then idle) TMA ring.  A CTA of a cluster
+// of S finalises the column block [CW·rank, CW·rank + CW), CW = RP / S:
+//   recv    [S][128][CW + 4] fp32: slot s holds CTA s's partial of this block
+//   stage_t [CW][128 + 4] fp32:   final values, transposed (kOutVt, kOutRowT)
+//   stage_r [128][CW + 4] fp32:   final values, row-major (kOutRowBf16, kOutRow)
+// Rows are padded by 16 bytes so the 16-byte accesses of a warp hit distinct
+// banks.
+struct SkinnyEpi {
+  int cw, recv_stride, off_stage_t, off_stage_r, bytes;
+  __host__ __device__ constexpr SkinnyEpi(int rp, int split)
+      : cw(rp / split),
+        recv_stride(rp / split + 4),
+        off_stage_t(split > 1 ? split * 128 * (rp / split + 4) * 4 : 0),
+        off_stage_r((split > 1 ? split * 128 * (rp / split + 4) * 4 : 0) +
+                    (rp / split) * (128 + 4) * 4),
+        bytes((split > 1 ? split * 128 * (rp / split + 4) * 4 : 0) +
+              (rp / split) * (128 + 4) * 4 + 128 * (rp / split + 4) * 4) {}
+};
+
+
+LORA_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Copy-out of one CTA's column block [col0, col0 + cw) of row tile rt from
+// the staging buffers, by the 128 epilogue threads (e = 0..127).  Every
+// warp-wide store covers contiguous runs of 256 to 512 bytes.
+LORA_DEV void skinny_copy_out(const SkinnyProblem &P, int rt, int col0, int cw,
+                              const float *stage_t, const float *stage_r, int e) {
   const int cols = P.nproj * P.r;  // valid rank columns
-  if (P.out_kind & kOutVt) {
+  const int row0 = rt * 128;
+  const int w = e >> 5, l = e & 31;
+  // transposed outputs: warp w takes block columns j = w, w + 4, ...; lane l
+  // takes rows [4l, 4l + 4) of the tile
+  if (P.out_kind & (kOutVt | kOutRowT)) {
+    const int orow = row0 + 4 * l;
+    const bool full = orow + 4 <= P.rows;
+    for (int j = w; j < cw; j += 4) {
+      const float4 t = *reinterpret_cast<const float4 *>(stage_t + j * 132 + 4 * l);
+      const float f[4] = {t.x, t.y, t.z, t.w};
+      const int jg = col0 + j;
+      if (P.out_kind & kOutVt) {
+        __nv_bfloat16 hi[4], lo[4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v[j]);
-      P.out_hi[(size_t)(j0 + j) * P.ld_t + orow] = hi;
-      P.out_lo[(size_t)(j0 + j) * P.ld_t + orow] = __float2bfloat16_rn(v[j] - __bfloat162float(hi));
+        for (int q = 0; q < 4; ++q) {
+          hi[q] = __float2bfloat16_rn(f[q]);
+          lo[q] = __float2bfloat16_rn(f[q] - __bfloat162float(hi[q]));
+        }
+        __nv_bfloat16 *dh = P.out_hi + (size_t)jg * P.ld_t + orow;
+        __nv_bfloat16 *dl = P.out_lo + (size_t)jg * P.ld_t + orow;
+        if (full) {
+          *reinterpret_cast<uint2 *>(dh) = *reinterpret_cast<const uint2 *>(hi);
+          *reinterpret_cast<uint2 *>(dl) = *reinterpret_cast<const uint2 *>(lo);
+        } else {
+          for (int q = 0; q < 4; ++q)
+            if (orow + q < P.rows) dh[q] = hi[q], dl[q] = lo[q];
+        }
+      }
+      if ((P.out_kind & kOutRowT) && jg < cols) {
+        const int pr = jg / P.r, jj = jg - pr * P.r;
+        float *dst = (pr ? P.out_f32b : P.out_f32) + (size_t)jj * P.rows + orow;
+        if (full) {
+          *reinterpret_cast<float4 *>(dst) =
+              make_float4(f[0] * P.scale, f[1] * P.scale, f[2] * P.scale, f[3] * P.scale);
+        } else {
+          for (int q = 0; q < 4; ++q)
+            if (orow + q < P.rows) dst[q] = f[q] * P.scale;
+        }
+      }
     }
   }
+  // row-major outputs: a row is cw columns; lanes cover 8 (bf16) or 4 (fp32)
+  // consecutive columns, several rows per warp-wide store
   if (P.out_kind & kOutRowBf16) {
-    __nv_bfloat16 *dst = P.out_bf16 + (size_t)orow * P.ld_row + j0;
-    if (j0 + 16 <= cols) {
-      uint4 w0, w1;
-      w0.x = pack_bf16x2(v[0] * P.scale, v[1] * P.scale);
-      w0.y = pack_bf16x2(v[2] * P.scale, v[3] * P.scale);
-      w0.z = pack_bf16x2(v[4] * P.scale, v[5] * P.scale);
-      w0.w = pack_bf16x2(v[6] * P.scale, v[7] * P.scale);
-      w1.x = pack_bf16x2(v[8] * P.scale, v[9] * P.scale);
-      w1.y = pack_bf16x2(v[10] * P.scale, v[11] * P.scale);
-      w1.z = pack_bf16x2(v[12] * P.scale, v[13] * P.scale);
-      w1.w = pack_bf16x2(v[14] * P.scale, v[15] * P.scale);
-      reinterpret_cast<uint4 *>(dst)[0] = w0;
-      reinterpret_cast<uint4 *>(dst)[1] = w1;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j0 + j < cols) dst[j] = __float2bfloat16_rn(v[j] * P.scale);
-    }
-  }
-  if (P.out_kind & kOutRowT) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int jg = j0 + j;
-      if (jg < cols) {
-        const int pr = jg / P.r, jj = jg % P.r;
-        float *out = pr ? P.out_f32b : P.out_f32;
-        out[(size_t)jj * P.rows + orow] = v[j] * P.scale;
+    const int lpr = cw / 8;  // lanes per row (cw >= 16)
+    const int rpw = 32 / lpr;
+    const int c = (l % lpr) * 8;
+    for (int rr = w * rpw + l / lpr; rr < 128; rr += 4 * rpw) {
+      const int orow = row0 + rr;
+      if (orow >= P.rows) break;
+      const float *src = stage_r + rr * (cw + 4) + c;
+      const float4 a = *reinterpret_cast<const float4 *>(src);
+      const float4 b = *reinterpret_cast<const float4 *>(src + 4);
+      __nv_bfloat16 *dst = P.out_bf16 + (size_t)orow * P.ld_row + col0 + c;
+      if (col0 + c + 8 <= cols) {
+        uint4 o;
+        o.x = pack_bf16x2(a.x * P.scale, a.y * P.scale);
+        o.y = pack_bf16x2(a.z * P.scale, a.w * P.scale);
+        o.z = pack_bf16x2(b.x * P.scale, b.y * P.scale);
+        o.w = pack_bf16x2(b.z * P.scale, b.w * P.scale);
+        *reinterpret_cast<uint4 *>(dst) = o;
+      } else {
+        const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        for (int q = 0; q < 8; ++q)
+          if (col0 + c + q < cols) dst[q] = __float2bfloat16_rn(f[q] * P.scale);
       }
     }
   }
   if (P.out_kind & kOutRow) {
     // dB: only the diagonal block of a merged pair is a real gradient
-    const int pr = (P.nproj > 1 && orow >= P.split_row) ? 1 : 0;
-    const int lo = pr * P.r;
-    if (j0 + 16 <= lo || j0 >= lo + P.r) return;
-    float *out = (pr ? P.out_f32b : P.out_f32) + (size_t)(orow - pr * P.split_row) * P.r;
-    if (j0 >= lo && j0 + 16 <= lo + P.r) {
-      float4 *dst = reinterpret_cast<float4 *>(out + (j0 - lo));
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        dst[j] = make_float4(v[4 * j] * P.scale, v[4 * j + 1] * P.scale, v[4 * j + 2] * P.scale,
-                             v[4 * j + 3] * P.scale);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j0 + j >= lo && j0 + j < lo + P.r) out[j0 + j - lo] = v[j] * P.scale;
+    const int lpr = cw / 4;
+    const int rpw = lpr >= 32 ? 1 : 32 / lpr;
+    for (int cb = 0; cb < cw; cb += 128) {   // column groups of 32 lanes x 4
+      const int c = cb + (l % (lpr >= 32 ? 32 : lpr)) * 4;
+      if (c >= cw) continue;
+      for (int rr = w * rpw + (lpr >= 32 ? 0 : l / lpr); rr < 128; rr += 4 * rpw) {
+        const int orow = row0 + rr;
+        if (orow >= P.rows) break;
+        const int pr = (P.nproj > 1 && orow >= P.split_row) ? 1 : 0;
+        const int jg = col0 + c, lo = pr * P.r;
+        if (jg < lo || jg >= lo + P.r) continue;
+        const float4 t = *reinterpret_cast<const float4 *>(stage_r + rr * (cw + 4) + c);
+        float *dst = (pr ? P.out_f32b : P.out_f32) + (size_t)(orow - pr * P.split_row) * P.r +
+                     (jg - lo);
+        if (jg + 4 <= lo + P.r) {
+          *reinterpret_cast<float4 *>(dst) =
+              make_float4(t.x * P.scale, t.y * P.scale, t.z * P.scale, t.w * P.scale);
+        } else {
+          const float f[4] = {t.x, t.y, t.z, t.w};
+          for (int q = 0; q < 4 && jg + q < lo + P.r; ++q) dst[q] = f[q] * P.scale;
+        }
+      }
     }
   }
 }
@@ -104,6 +159,7 @@ LORA_DEV void skinny_store16(const SkinnyProblem &P, int orow, int j0, const flo
 template <bool MN, int RP>
 __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_constant__ SkinnyParams p) {
   using L = SkinnySmem<MN, RP>;
+  static_assert(SkinnyEpi(RP, 1).bytes <= L::OFF_MISC, "epilogue buffers fit in the ring");
   constexpr int STAGES = L::STAGES;
   constexpr uint32_t kTmemCols = RP >= 32 ? RP : 32;
   extern __shared__ uint8_t smem_raw[];
@@ -119,7 +175,11 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   const SkinnyProblem &P = p.pr[pi];
   const int rt = cid - P.tile_begin;
   const int c_begin = (int)((long long)P.chunks * srank / S);
-  const int c_end = (int)((long long)P.chunks * (srank + 1) / S);
+  const int n_chunks = (int)((long long)P.chunks * (srank + 1) / S) - c_begin;
+  // Row tiles start at staggered chunks of their slice (and wrap around), so
+  // the CTAs in flight read different Q chunks instead of all hitting the
+  // same L2 lines at once; the order is fixed, so results stay deterministic.
+  const int c_rot = n_chunks > 0 ? (int)(((long long)rt * n_chunks) / P.row_tiles) % n_chunks : 0;
 
   const uint32_t bar_full = base + L::OFF_MISC;
   const uint32_t bar_empty = bar_full + 8 * STAGES;
@@ -155,7 +215,8 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
       uint32_t phase = 0;
       int fills[STAGES];
       for (int s = 0; s < STAGES; ++s) fills[s] = 0;
-      for (int c = c_begin; c < c_end; ++c) {
+      for (int i = 0; i < n_chunks; ++i) {
+        const int c = c_begin + (i + c_rot) % n_chunks;
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) break;
         const uint32_t sp = base + stage * L::STAGE_BYTES;
         const uint32_t sq = sp + L::P_BYTES;
@@ -191,7 +252,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int c = c_begin; c < c_end; ++c) {
+      for (int i = 0; i < n_chunks; ++i) {
         if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) {
           ok = false;
           break;
@@ -201,7 +262,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
         const uint32_t sq = sp + L::P_BYTES;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t accum = (c != c_begin || ks != 0) ? 1u : 0u;
+          const uint32_t accum = (i != 0 || ks != 0) ? 1u : 0u;
           uint64_t da;
           if constexpr (MN)
             da = make_sdesc(sp + ks * 2048, 8192, 1024, kSw128);
@@ -223,60 +284,91 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   }
 
   // ---------------------------------------------- epilogue (warps 2-5)
+  // 1. every CTA's accumulator is complete (its ring is idle)
+  // 2. each CTA pushes its partial of the other CTAs' column blocks into
+  //    their recv slots (distributed shared memory stores)
+  // 3. each CTA adds the S partials of its own block in cluster-rank order
+  //    (deterministic), stages the result and copies it out
   const bool epi = warp >= 2;
   const int row = (warp & 3) * 32 + lane;
   const uint32_t t_lane = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t my_red = base + row * L::RED_STRIDE;
+  const SkinnyEpi E(RP, S);
+  const int CW = E.cw;
+  float *recv = reinterpret_cast<float *>(smem);
+  float *stage_t = reinterpret_cast<float *>(smem + E.off_stage_t);
+  float *stage_r = reinterpret_cast<float *>(smem + E.off_stage_r);
   bool acc_ok = false;
   if (epi) {
     acc_ok = __all_sync(0xffffffffu, mbar_wait(bar_acc_full, 0, abort_flag, p.status));
     if (acc_ok) tc_fence_after();
-    if (acc_ok && srank != 0) {
-      // park the partial: the ring is idle (every MMA reading it completed)
+  }
+  __syncwarp();
+  if (S > 1) cluster_sync_all();  // every ring of the cluster is idle
+  if (epi && acc_ok && S > 1) {
+    const uint32_t my_slot = smem_addr(recv + ((size_t)srank * 128 + row) * E.recv_stride);
+    for (int b = 0; b < S; ++b) {
+      if (b == srank) continue;
+      const uint32_t dst = map_shared_rank(my_slot, (uint32_t)b);
 #pragma unroll 1
-      for (int c = 0; c < RP / 16; ++c) {
+      for (int c = 0; c < CW / 16; ++c) {
         uint32_t r[16];
-        tmem_ld16(tmem + t_lane + c * 16, r);
+        tmem_ld16(tmem + t_lane + b * CW + c * 16, r);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          st_shared_v4(my_red + c * 64 + j * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2],
-                       r[4 * j + 3]);
+          st_shared_cluster_v4(dst + c * 64 + j * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2],
+                               r[4 * j + 3]);
       }
     }
   }
   __syncwarp();
-  if (S > 1) cluster_sync_all();  // partials visible to the leader
-  if (epi && srank == 0 && acc_ok) {
-    const int orow = rt * 128 + row;
+  if (S > 1) cluster_sync_all();  // pushed partials have landed
+  const bool want_t = (P.out_kind & (kOutVt | kOutRowT)) != 0;
+  const bool want_r = (P.out_kind & (kOutRowBf16 | kOutRow)) != 0;
+  if (epi && acc_ok) {
 #pragma unroll 1
-    for (int c = 0; c < RP / 16; ++c) {
+    for (int c = 0; c < CW / 16; ++c) {
       uint32_t r[16];
-      tmem_ld16(tmem + t_lane + c * 16, r);
+      tmem_ld16(tmem + t_lane + srank * CW + c * 16, r);
       tmem_ld_wait();
       float v[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-      for (int s = 1; s < S; ++s) {
-        const uint32_t src = map_shared_rank(my_red + c * 64, (uint32_t)s);
+      for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+      for (int s = 0; s < S; ++s) {
+        if (s == srank) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float4 t = ld_shared_cluster_v4(src + j * 16);
-          v[4 * j] += t.x;
-          v[4 * j + 1] += t.y;
-          v[4 * j + 2] += t.z;
-          v[4 * j + 3] += t.w;
+          for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
+        } else {
+          const float4 *src = reinterpret_cast<const float4 *>(
+              recv + ((size_t)s * 128 + row) * E.recv_stride + c * 16);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 t = src[j];
+            v[4 * j] += t.x;
+            v[4 * j + 1] += t.y;
+            v[4 * j + 2] += t.z;
+            v[4 * j + 3] += t.w;
+          }
         }
       }
-      skinny_store16(P, orow, c * 16, v);
+      if (want_t) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stage_t[(c * 16 + j) * 132 + row] = v[j];
+      }
+      if (want_r) {
+        float4 *dst = reinterpret_cast<float4 *>(stage_r + row * (CW + 4) + c * 16);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
     }
   }
+  if (epi) {
+    epi_bar();
+    if (acc_ok) skinny_copy_out(P, rt, srank * CW, CW, stage_t, stage_r, threadIdx.x - 64);
+  }
   tc_fence_before();
-  __syncwarp();
-  if (S > 1)
-    cluster_sync_all();  // the leader has read every partial before any CTA exits
-  else
-    __syncthreads();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -312,8 +404,27 @@ static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+template <bool MN, int RP>
+static int max_split_t() {
+  using L = SkinnySmem<MN, RP>;
+  int s = 1;
+  while (s < 8 && RP / (2 * s) >= 16 && SkinnyEpi(RP, 2 * s).bytes <= L::OFF_MISC) s *= 2;
+  return s;
+}
+
+int skinny_max_split(bool mn_major, int rp) {
+  switch (rp) {
+    case 16: return mn_major ? max_split_t<true, 16>() : max_split_t<false, 16>();
+    case 32: return mn_major ? max_split_t<true, 32>() : max_split_t<false, 32>();
+    case 64: return mn_major ? max_split_t<true, 64>() : max_split_t<false, 64>();
+    case 128: return mn_major ? max_split_t<true, 128>() : max_split_t<false, 128>();
+  }
+  return 1;
+}
+
 cudaError_t launch_skinny(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st) {
   if (p.split != 1 && p.split != 2 && p.split != 4 && p.split != 8) return cudaErrorInvalidValue;
+  if (p.split > skinny_max_split(mn_major, rp)) return cudaErrorInvalidValue;
   switch (rp) {
     case 16: return mn_major ? launch_skinny_t<true, 16>(p, st) : launch_skinny_t<false, 16>(p, st);
     case 32: return mn_major ? launch_skinny_t<true, 32>(p, st) : launch_skinny_t<false, 32>(p, st);

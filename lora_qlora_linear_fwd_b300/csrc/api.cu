@@ -227,6 +227,8 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
         return LORA_ERR_CUDA;
       G.ld_absmax = k / 64;
     }
+    if (!make_map(&G.tm_out, kBF16, 2, a.out, ncols, o.M, (uint64_t)ncols * 2, 32, 32, true))
+      return LORA_ERR_CUDA;
     G.out = static_cast<__nv_bfloat16 *>(a.out);
     G.absmax = static_cast<const __nv_bfloat16 *>(a.W.absmax);
     G.ncols = ncols;

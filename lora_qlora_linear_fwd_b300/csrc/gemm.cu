@@ -25,7 +25,9 @@
 //              256-column buffers so a tile's epilogue overlaps the next
 //              tile's main loop.
 //   warps 2-5  epilogue of the CTA's own 128 rows: TMEM -> (RoPE) -> bf16
-//              -> global (dX: optionally += the values already there).
+//              -> shared-memory staging -> TMA bulk store of whole lines
+//              (dX with accumulate: plain loads/stores adding to the values
+//              already there).
 //   warps 6-9  NF4 only: decode the CTA's own half of the W tile through the
 //              16-entry NF4 codebook, scaled by the block absmax ("Unsloth教程"
 //              §显存优化策略: NF4 base weight).
@@ -41,11 +43,13 @@ struct PairSmem {
   static constexpr int OFF_W = X_BYTES;
   static constexpr int OFF_C = OFF_W + W_BYTES;
   static constexpr int STAGE_BYTES = OFF_C + C_BYTES;
+  static constexpr int EPI_BYTES = 4 * 4 * 2048;  // per epilogue warp: four 2 KB staging buffers
   static constexpr int MISC_BYTES = 1024;
-  static constexpr int FIXED = MISC_BYTES + 1024;
+  static constexpr int FIXED = EPI_BYTES + MISC_BYTES + 1024;
   static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int OFF_MISC = STAGES * STAGE_BYTES;
+  static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
+  static constexpr int OFF_MISC = OFF_EPI + EPI_BYTES;
   static constexpr int TOTAL = OFF_MISC + MISC_BYTES + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 3, "pipeline depth");
@@ -246,6 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t t_lane = (uint32_t)(q * 32) << 16;
+    const uint32_t epi_buf = base + L::OFF_EPI + (uint32_t)q * 8192u;
     int tile_count = 0;
     TileIter it;
     for (it.init(p.sched, pair); it.valid(); it.next(), ++tile_count) {
@@ -258,14 +263,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
       if (!warp_wait(bar_acc_full + 8 * buf, (tile_count >> 1) & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const int ncols = min(BN, G.ncols - n0);
-      __nv_bfloat16 *orow = G.out + (size_t)(row_ok ? grow : 0) * G.ncols + n0;
       const float *cs = ROPE ? rope_row(p, grow, row_ok) : nullptr;
-      epi_store_tile<BN, ROPE>(tmem + t_lane + buf * BN, orow, row_ok, ncols, DX && p.accumulate,
-                               cs);
+      if (DX && p.accumulate) {  // read-modify-write of dX: plain loads and stores
+        __nv_bfloat16 *orow = G.out + (size_t)(row_ok ? grow : 0) * G.ncols + n0;
+        epi_store_tile<BN, false>(tmem + t_lane + buf * BN, orow, row_ok, ncols, true, nullptr);
+      } else {
+        epi_store_tile_tma<BN, ROPE>(tmem + t_lane + buf * BN, epi_buf, &G.tm_out, n0,
+                                     m * 256 + (int)crank * 128 + q * 32, ncols, cs, lane);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lead_acc_empty + 8 * buf);
     }
+    if (lane == 0) bulk_wait_all();  // every output store has completed
+    __syncwarp();
   } else if constexpr (NF4) {
     // ============================================================= NF4 decode
     // FWD: piece dt = row dt of this CTA's W half [128 rows x 64].

@@ -144,6 +144,91 @@ LORA_DEV void epi_store_tile(uint32_t t_acc, __nv_bfloat16 *orow, bool row_ok, i
   }
 }
 
+// Output epilogue through shared memory and TMA for one warp (32 rows of
+// the CTA's 128): per 32-column chunk, TMEM -> (RoPE) -> bf16 into one of
+// four 2 KB staging buffers [32 rows x 64 bytes, 64-byte swizzle, the layout
+// the output tensor map names], then lane 0 stores the chunk with one bulk
+// tensor copy (whole lines, clipped at the tensor's extent).  `buf` is the
+// warp's staging area; `cs` the cos/sin row of this lane's output row.
+template <int BN, bool ROPE>
+LORA_DEV void epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap *tm_out,
+                                 int col0, int row0, int ncols, const float *cs, int lane) {
+  // byte offset of 16-byte chunk q of this lane's row in a staging buffer
+  auto at = [&](int q) -> uint32_t {
+    return (uint32_t)(lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4));
+  };
+  if constexpr (!ROPE) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(t_acc + c * 32, r);
+      tmem_ld_wait();
+      if (c * 32 >= ncols) continue;
+      const uint32_t b = buf + (uint32_t)(c & 3) * 2048u;
+      if (lane == 0) bulk_wait_read<3>();  // buffer (c & 3) no longer read by an older copy
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(b + at(q), pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1])),
+                     pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
+                     pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
+                     pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm_out, b, col0 + c * 32, row0);
+        bulk_commit();
+      }
+    }
+  } else {
+    int pair = 0;
+#pragma unroll 1
+    for (int h = 0; h < BN / 128; ++h) {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half, ++pair) {
+        const int c0 = h * 128 + half * 32;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(t_acc + c0, ra);
+        tmem_ld32(t_acc + c0 + 64, rb);
+        tmem_ld_wait();
+        if (c0 >= ncols) continue;
+        const uint32_t ba = buf + (uint32_t)(pair & 1) * 4096u;
+        const uint32_t bb = ba + 2048u;
+        if (lane == 0) bulk_wait_read<1>();  // this pair of buffers is free again
+        __syncwarp();
+        const float4 *cp = reinterpret_cast<const float4 *>(cs + half * 32);
+        const float4 *sp = reinterpret_cast<const float4 *>(cs + 64 + half * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 c_lo = __ldg(cp + 2 * q), c_hi = __ldg(cp + 2 * q + 1);
+          const float4 s_lo = __ldg(sp + 2 * q), s_hi = __ldg(sp + 2 * q + 1);
+          const float co[8] = {c_lo.x, c_lo.y, c_lo.z, c_lo.w, c_hi.x, c_hi.y, c_hi.z, c_hi.w};
+          const float si[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+          float oa[8], ob[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float a = __uint_as_float(ra[8 * q + e]);
+            const float bv = __uint_as_float(rb[8 * q + e]);
+            oa[e] = a * co[e] - bv * si[e];
+            ob[e] = bv * co[e] + a * si[e];
+          }
+          st_shared_v4(ba + at(q), pack_bf16x2(oa[0], oa[1]), pack_bf16x2(oa[2], oa[3]),
+                       pack_bf16x2(oa[4], oa[5]), pack_bf16x2(oa[6], oa[7]));
+          st_shared_v4(bb + at(q), pack_bf16x2(ob[0], ob[1]), pack_bf16x2(ob[2], ob[3]),
+                       pack_bf16x2(ob[4], ob[5]), pack_bf16x2(ob[6], ob[7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(tm_out, ba, col0 + c0, row0);
+          tma_store_2d(tm_out, bb, col0 + c0 + 64, row0);
+          bulk_commit();
+        }
+      }
+    }
+  }
+}
+
 // Position of output row `grow` for the RoPE epilogue; an out-of-range
 // position is reported in the status word and replaced by 0 (no read
 // outside the cache).

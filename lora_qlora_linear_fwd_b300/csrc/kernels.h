@@ -25,6 +25,7 @@ namespace lora {
 struct GemmGroup {
   CUtensorMap tm_w;
   CUtensorMap tm_b;
+  CUtensorMap tm_out;  // out [M, ncols] bf16: box 32 x 32, 64-byte swizzle
   __nv_bfloat16 *out;
   const __nv_bfloat16 *absmax;
   int ncols;       // output columns of this group (n in FWD, k in DX)

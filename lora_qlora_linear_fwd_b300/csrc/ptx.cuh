@@ -204,6 +204,25 @@ LORA_DEV void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 LORA_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 
+// 2-D tiled bulk copy shared -> global (bulk-group completion).  The box is
+// clipped at the tensor's extent; x must be a multiple of 16 bytes and
+// neither coordinate may be negative.
+LORA_DEV void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+LORA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+LORA_DEV void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all of this thread's bulk groups have completed.
+LORA_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ------------------------------------------------------------ clusters
 LORA_DEV uint32_t cluster_ctarank() {
   uint32_t r;

@@ -334,7 +334,9 @@ def run_gpu(args, world, rank, local):
     fk = fwd_kernel_flops(wl, M) / len(wl.projections) if not wl.rope else fwd_kernel_flops(wl, M)
     fwd_launch_ms = fwd_ms_mean / (1 if wl.rope else len(wl.projections))
     achieved = fk / (fwd_launch_ms / 1e3) / 1e12
-    roofline = {"kernel": "lora_gemm_kernel<FWD>", "bound": "tensor",
+    fwd_name = ("lora_qk_rope_fwd" if wl.rope else "lora_linear_fwd") + \
+        " (rank pass + fused GEMM, 2 launches)"
+    roofline = {"kernel": fwd_name, "bound": "tensor",
                 "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),

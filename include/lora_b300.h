@@ -73,7 +73,8 @@ typedef enum {
  *   type == LORA_WEIGHT_BF16: w -> bf16 [n,k]; absmax NULL; blocksize ignored.
  *   type == LORA_WEIGHT_NF4 : w -> uint8 codes [n, k/2] (byte j of a row holds
  *     element 2j in the high nibble, 2j+1 in the low nibble); absmax -> bf16
- *     [n, k/blocksize], the per-block scale; blocksize must be 64.  An element
+ *     [n, k/blocksize], the per-block scale (16-byte aligned, like every
+ *     other pointer); blocksize must be 64.  An element
  *     decodes to level[code] * absmax with the 16 NF4 levels of [QLoRA]. */
 enum { LORA_WEIGHT_BF16 = 0, LORA_WEIGHT_NF4 = 1 };
 typedef struct {

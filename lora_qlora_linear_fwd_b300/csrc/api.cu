@@ -112,8 +112,7 @@ lora_status_t check_weight(const lora_weight_t &W) {
   if (W.type == LORA_WEIGHT_BF16) {
     if (!aligned16(W.w)) return LORA_ERR_INVALID_ARG;
   } else if (W.type == LORA_WEIGHT_NF4) {
-    if (!aligned16(W.w) || !W.absmax || (reinterpret_cast<uintptr_t>(W.absmax) & 1u))
-      return LORA_ERR_INVALID_ARG;
+    if (!aligned16(W.w) || !aligned16(W.absmax)) return LORA_ERR_INVALID_ARG;
     if (W.blocksize != 64) return LORA_ERR_UNSUPPORTED;
   } else {
     return LORA_ERR_INVALID_ARG;

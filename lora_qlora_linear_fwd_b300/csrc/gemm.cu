@@ -28,12 +28,16 @@
 //              -> shared-memory staging -> TMA bulk store of whole lines
 //              (dX with accumulate: plain loads/stores adding to the values
 //              already there).
-//   warps 6-9  NF4 only: decode the CTA's own half of the W tile through the
+//   warps 6-13 NF4 only: decode the CTA's own half of the W tile through the
 //              16-entry NF4 codebook, scaled by the block absmax ("Unsloth教程"
-//              §显存优化策略: NF4 base weight).
+//              §显存优化策略: NF4 base weight); two threads per 64-element
+//              row piece.
 #include "gemm_common.cuh"
 
 namespace lora {
+
+// Threads per CTA: producer, MMA, 4 epilogue warps (+ 8 NF4 decode warps).
+constexpr int pair_threads(bool nf4) { return nf4 ? 448 : 192; }
 
 template <bool NF4>
 struct PairSmem {
@@ -44,12 +48,15 @@ struct PairSmem {
   static constexpr int OFF_C = OFF_W + W_BYTES;
   static constexpr int STAGE_BYTES = OFF_C + C_BYTES;
   static constexpr int EPI_BYTES = 4 * 4 * 2048;  // per epilogue warp: four 2 KB staging buffers
+  static constexpr int AMAX_PRE = 8;               // NF4: absmax prefetch distance (K-blocks)
+  static constexpr int AMAX_BYTES = NF4 ? AMAX_PRE * 256 * 4 : 0;
   static constexpr int MISC_BYTES = 1024;
-  static constexpr int FIXED = EPI_BYTES + MISC_BYTES + 1024;
+  static constexpr int FIXED = EPI_BYTES + AMAX_BYTES + MISC_BYTES + 1024;
   static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
-  static constexpr int OFF_MISC = OFF_EPI + EPI_BYTES;
+  static constexpr int OFF_AMAX = OFF_EPI + EPI_BYTES;
+  static constexpr int OFF_MISC = OFF_AMAX + AMAX_BYTES;
   static constexpr int TOTAL = OFF_MISC + MISC_BYTES + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 3, "pipeline depth");
@@ -57,13 +64,13 @@ struct PairSmem {
 };
 
 template <int MODE, bool NF4, bool ROPE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1)
     lora_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   using L = PairSmem<NF4>;
   constexpr int STAGES = L::STAGES;
   constexpr int BN = 256;
   constexpr bool DX = MODE == kModeDx;
-  constexpr int NUM_DEC_WARPS = NF4 ? 4 : 0;
+  constexpr int NUM_DEC_WARPS = (pair_threads(NF4) - 192) / 32;
   constexpr uint16_t kBoth = 0x3;
 
   extern __shared__ uint8_t smem_raw[];
@@ -279,64 +286,105 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NF4 ? 320 : 192, 1)
     __syncwarp();
   } else if constexpr (NF4) {
     // ============================================================= NF4 decode
-    // FWD: piece dt = row dt of this CTA's W half [128 rows x 64].
+    // Thread dt decodes half h = dt & 1 of row piece pc = dt >> 1:
+    // FWD: piece pc = row pc of this CTA's W half [128 rows x 64].
     // DX:  the half is [64 n-rows x 128 k-columns] = two boxes of [64 x 64];
-    //      piece dt = row (dt % 64) of box (dt / 64).
+    //      piece pc = row (pc % 64) of box (pc / 64).
     // Rank K-blocks carry no codes: the decoders only pass them on.
-    const int dt = threadIdx.x - 192;  // 0..127
+    // The absmax of a piece is fetched AMAX_PRE K-blocks ahead (cp.async
+    // into a per-thread shared ring, walked by a second tile iterator):
+    // loaded at decode time it would stall every stage by a memory latency,
+    // since the stage's codes usually land first.
+    const int dt = threadIdx.x - 192;  // 0..255
+    const int pc = dt >> 1, hh = dt & 1;
+    constexpr int PRE = L::AMAX_PRE;
+    const uint32_t ring = base + L::OFF_AMAX + (uint32_t)dt * 4u;  // slot j at ring + 1024 j
+    const uint32_t lv = smem_addr(levels);
+    // absmax element of piece pc at K-block kb of tile nt (-1: none)
+    auto amax_index = [&](int nt, int kb) -> long long {
+      const GemmGroup &GN = p.grp[group_of(p, nt)];
+      const int nh = (nt - GN.tile_begin) * BN + (int)crank * 128;
+      const int gk = (DX && p.kgroups > 1 && kb >= p.ksplit) ? 1 : 0;
+      const GemmGroup &G = DX ? p.grp[gk] : GN;
+      int wrow, kblk;
+      if constexpr (DX) {
+        wrow = (kb - (gk ? p.ksplit : 0)) * kBK + (pc & 63);
+        kblk = (nh >> 6) + (pc >> 6);
+      } else {
+        wrow = nh + pc;
+        kblk = kb;
+      }
+      const bool in = DX ? (kblk < G.ld_absmax) : (wrow < G.ncols);
+      return in ? (long long)wrow * G.ld_absmax + kblk : -1;
+    };
+    TileIter ahead;
+    ahead.init(p.sched, pair);
+    int kb_a = 0;
+    // prefetch for the look-ahead position, then advance it by one K-block
+    auto prefetch = [&](uint32_t slot) {
+      if (ahead.valid()) {
+        const int nt = ahead.nt();
+        const GemmGroup &GA = p.grp[group_of(p, nt)];
+        if (kb_a < nk) {
+          const long long idx = amax_index(nt, kb_a);
+          if (idx >= 0) {
+            const int gk = (DX && p.kgroups > 1 && kb_a >= p.ksplit) ? 1 : 0;
+            const GemmGroup &G = DX ? p.grp[gk] : GA;
+            cp_async_4(ring + slot * 1024u, G.absmax + (idx & ~1ll));  // the aligned word
+          }
+        }
+        if (++kb_a == nk + (DX ? p.grp[0].n_extra : GA.n_extra)) {
+          kb_a = 0;
+          ahead.next();
+        }
+      }
+      cp_async_commit();
+    };
+    for (int j = 0; j < PRE; ++j) prefetch((uint32_t)j);
     int stage = 0;
     uint32_t phase = 0;
+    uint32_t slot = 0;
     bool ok = true;
     TileIter it;
     for (it.init(p.sched, pair); ok && it.valid(); it.next()) {
       const int nt = it.nt();
       const GemmGroup &GN = p.grp[group_of(p, nt)];
-      const int nh = (nt - GN.tile_begin) * BN + (int)crank * 128;
       const int ne = DX ? p.grp[0].n_extra : GN.n_extra;
       for (int kb = 0; kb < nk + ne; ++kb) {
-        if (kb >= nk) {
-          if (!warp_wait(bar_raw + 8 * stage, phase, abort_flag, p.status)) {
-            ok = false;
-            break;
+        cp_async_wait<PRE - 1>();  // this K-block's absmax has landed
+        float amax = 0.0f;
+        if (kb < nk) {
+          const long long idx = amax_index(nt, kb);
+          if (idx >= 0) {
+            const uint32_t w = ld_shared_u32(ring + slot * 1024u);
+            amax = __uint_as_float(((idx & 1) ? (w >> 16) : (w & 0xFFFFu)) << 16);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(lead_dec + 8 * stage);
-          if (++stage == STAGES) stage = 0, phase ^= 1u;
-          continue;
         }
-        const int gk = (DX && p.kgroups > 1 && kb >= p.ksplit) ? 1 : 0;
-        const GemmGroup &G = DX ? p.grp[gk] : GN;
-        int wrow, kblk;
-        if constexpr (DX) {
-          wrow = (kb - (gk ? p.ksplit : 0)) * kBK + (dt & 63);
-          kblk = (nh >> 6) + (dt >> 6);
-        } else {
-          wrow = nh + dt;
-          kblk = kb;
-        }
-        const bool in = DX ? (kblk < G.ld_absmax) : (wrow < G.ncols);
-        const float amax =
-            in ? __bfloat162float(G.absmax[(size_t)wrow * G.ld_absmax + kblk]) : 0.0f;
+        prefetch(slot);  // the slot just read refills for K-block kb + PRE
+        if (++slot == (uint32_t)PRE) slot = 0;
         if (!warp_wait(bar_raw + 8 * stage, phase, abort_flag, p.status)) {
           ok = false;
           break;
         }
-        const uint32_t sx = base + stage * L::STAGE_BYTES;
-        uint32_t src, dst;
-        if constexpr (DX) {
-          src = sx + L::OFF_C + (dt & 63) * 64 + (dt >> 6) * 32;
-          dst = sx + L::OFF_W + (dt >> 6) * 8192 + (dt & 63) * 128;
-        } else {
-          src = sx + L::OFF_C + dt * 32;
-          dst = sx + L::OFF_W + dt * 128;
+        if (kb < nk) {
+          const uint32_t sx = base + stage * L::STAGE_BYTES;
+          uint32_t src, dst;
+          if constexpr (DX) {
+            src = sx + L::OFF_C + (pc & 63) * 64 + (pc >> 6) * 32 + hh * 16;
+            dst = sx + L::OFF_W + (pc >> 6) * 8192 + (pc & 63) * 128;
+          } else {
+            src = sx + L::OFF_C + pc * 32 + hh * 16;
+            dst = sx + L::OFF_W + pc * 128;
+          }
+          nf4_decode_half(src, dst, hh, amax, lv);
+          fence_proxy_async_smem();
         }
-        nf4_decode_piece(src, dst, amax, levels);
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(lead_dec + 8 * stage);
+        if (lane == 0) mbar_arrive_remote(lead_dec + 8 * stage);
         if (++stage == STAGES) stage = 0, phase ^= 1u;
       }
     }
+    cp_async_wait<0>();  // no copy may land after the CTA exits
   }
 
   __syncthreads();
@@ -357,7 +405,7 @@ static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<2 * pairs, NF4 ? 320 : 192, L::TOTAL, st>>>(p);
+  kern<<<2 * pairs, pair_threads(NF4), L::TOTAL, st>>>(p);
   note_launch();
   return cudaGetLastError();
 }
@@ -373,7 +421,7 @@ static int pair_capacity() {
       return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(NF4 ? 320 : 192, 1, 1);
+    cfg.blockDim = dim3(pair_threads(NF4), 1, 1);
     cfg.dynamicSmemBytes = L::TOTAL;
     int n = 0;  // cluster shape comes from the kernel's compile-time cluster dims
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;

@@ -33,24 +33,32 @@ LORA_DEV uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
-// Decode one 64-element row piece: 32 code bytes at `src` (shared), block
-// scale `a`, into a 128-byte row of a 128-byte-swizzled tile at `dst`.
-// Byte j holds element 2j in its high nibble and 2j+1 in its low nibble.
-LORA_DEV void nf4_decode_piece(uint32_t src, uint32_t dst, float a, const float *levels) {
-  const uint4 c01 = ld_shared_v4(src);
-  const uint4 c23 = ld_shared_v4(src + 16);
-  const uint32_t words[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
+// Decode half of a 64-element row piece: 16 code bytes at `src` (shared)
+// with block scale `a`, into the 16-byte chunks [4h, 4h+4) of a 128-byte
+// row of a 128-byte-swizzled tile at `dst` (h = which half).  Byte j of a
+// row holds element 2j in its high nibble and 2j+1 in its low nibble; each
+// element is the fp32 product level·a rounded once to bf16.  `lv` is the
+// shared-memory address of the 16 fp32 levels.
+LORA_DEV float ld_level(uint32_t lv, uint32_t nib) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(lv + (nib << 2)));
+  return v;
+}
+LORA_DEV void nf4_decode_half(uint32_t src, uint32_t dst, int h, float a, uint32_t lv) {
+  const uint4 c = ld_shared_v4(src);
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
   const uint32_t phase = (dst >> 7) & 7u;
 #pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    const uint32_t w = words[ch];
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t w = words[q];
     uint32_t o[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const uint32_t byte = (w >> (8 * b)) & 0xFFu;
-      o[b] = pack_bf16x2(levels[byte >> 4] * a, levels[byte & 0xFu] * a);
+      const uint32_t hi = (w >> (8 * b + 4)) & 0xFu, lo = (w >> (8 * b)) & 0xFu;
+      o[b] = pack_bf16x2(ld_level(lv, hi) * a, ld_level(lv, lo) * a);
     }
-    st_shared_v4(dst + ((((uint32_t)ch) ^ phase) << 4), o[0], o[1], o[2], o[3]);
+    const uint32_t ch = (uint32_t)(4 * h + q);
+    st_shared_v4(dst + ((ch ^ phase) << 4), o[0], o[1], o[2], o[3]);
   }
 }
 

@@ -223,6 +223,22 @@ LORA_DEV void bulk_wait_read() {
 // Wait until all of this thread's bulk groups have completed.
 LORA_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// 4-byte asynchronous copy global -> shared (LDGSTS), grouped per thread.
+LORA_DEV void cp_async_4(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+LORA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's cp.async groups are pending.
+template <int N>
+LORA_DEV void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+LORA_DEV uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------ clusters
 LORA_DEV uint32_t cluster_ctarank() {
   uint32_t r;
@@ -234,6 +250,20 @@ LORA_DEV uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+// Arrive on an mbarrier that may live in the peer CTA (cluster address)
+// after shared-memory writes that the arriving CTA's own SM will read
+// through the async proxy (a pair MMA reads each CTA's operand half from
+// that CTA's shared memory).  The writers have already executed
+// fence.proxy.async; a CTA-scope release fence then orders those writes
+// before the arrive, which itself is relaxed at cluster scope.  Used on
+// every pipeline stage: a cluster-scope release arrive costs about as much
+// as the stage's work.
+LORA_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile(
+      "fence.acq_rel.cta;\n\t"
+      "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+      : "memory");
 }
 // Arrive on an mbarrier that may live in the peer CTA (cluster address).
 LORA_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {

@@ -72,6 +72,7 @@ def _fwd(M=256, k=512, n=512, r=8, x=FAKE, W=None, A=FAKE, B=FAKE, y=FAKE, ws=FA
     (dict(ws=0), 1), (dict(wsb=4351), 3), (dict(alpha=float("nan")), 1),
     (dict(W=L.Weight(7, FAKE, None, 0)), 1),
     (dict(W=L.Weight(1, FAKE, None, 64)), 1),            # NF4 without absmax
+    (dict(W=L.Weight(1, FAKE, MIS, 64)), 1),             # NF4 absmax not 16-byte aligned
     (dict(W=L.Weight(1, FAKE, FAKE, 128)), 2),           # NF4 block size other than 64
 ])
 def test_fwd_rejects_bad_arguments(kw, expect):

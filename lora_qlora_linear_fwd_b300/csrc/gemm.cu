@@ -63,6 +63,57 @@ struct PairSmem {
   static_assert(TOTAL <= kSmemLimit, "shared memory budget");
 };
 
+// Walk of one NF4 decode thread over its absmax elements, K-block by
+// K-block, across the tiles of its CTA pair (FWD: row nh + pc, column kb;
+// DX: row kb·64 + pc % 64 of the K-group's W, column nh/64 + pc/64).
+template <bool DX>
+struct Nf4Cursor {
+  TileIter it;
+  int kb, len;                        // K-block in the tile; K-blocks per tile
+  const __nv_bfloat16 *p0, *p1;       // element at K-block 0 of each K-group
+  long long step;                     // elements per K-block
+  int split;                          // first K-block of the second K-group
+  bool in;                            // the piece lies inside W
+  __device__ void tile(const GemmParams &p, int pc, int crank, int nk) {
+    const int nt = it.nt();
+    const GemmGroup &G = p.grp[group_of(p, nt)];
+    const int nh = (nt - G.tile_begin) * 256 + crank * 128;
+    len = nk + (DX ? p.grp[0].n_extra : G.n_extra);
+    if constexpr (DX) {
+      const int ld = p.grp[0].ld_absmax;
+      const int kblk = (nh >> 6) + (pc >> 6);
+      in = kblk < ld;
+      step = 64ll * ld;
+      p0 = p.grp[0].absmax + (long long)(pc & 63) * ld + kblk;
+      p1 = p.kgroups > 1 ? p.grp[1].absmax + (long long)(pc & 63) * ld + kblk : p0;
+      split = p.kgroups > 1 ? p.ksplit : nk;
+    } else {
+      const int wrow = nh + pc;
+      in = wrow < G.ncols;
+      step = 1;
+      p0 = p1 = G.absmax + (long long)(in ? wrow : 0) * G.ld_absmax;
+      split = nk;
+    }
+  }
+  __device__ void init(const GemmParams &p, int worker, int pc, int crank, int nk) {
+    it.init(p.sched, worker);
+    kb = 0;
+    if (it.valid()) tile(p, pc, crank, nk);
+  }
+  __device__ bool valid() const { return it.valid(); }
+  __device__ const __nv_bfloat16 *elem() const {
+    return kb < split ? p0 + kb * step : p1 + (kb - split) * step;
+  }
+  __device__ void advance(const GemmParams &p, int pc, int crank, int nk) {
+    if (!it.valid()) return;
+    if (++kb == len) {
+      kb = 0;
+      it.next();
+      if (it.valid()) tile(p, pc, crank, nk);
+    }
+  }
+};
+
 template <int MODE, bool NF4, bool ROPE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1)
     lora_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
@@ -94,7 +145,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   const int misc_words = (8 * (4 * STAGES + 5)) / 4;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC) + misc_words;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
-  float *levels = reinterpret_cast<float *>(tmem_holder + 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -111,7 +161,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (NF4 && threadIdx.x < 16) levels[threadIdx.x] = kNf4Levels[threadIdx.x];
   if (warp == 1) {  // one warp in each CTA of the pair allocates together
     tmem_alloc_pair(smem_addr(tmem_holder), 512);
     tmem_relinquish_pair();
@@ -292,97 +341,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     //      piece pc = row (pc % 64) of box (pc / 64).
     // Rank K-blocks carry no codes: the decoders only pass them on.
     // The absmax of a piece is fetched AMAX_PRE K-blocks ahead (cp.async
-    // into a per-thread shared ring, walked by a second tile iterator):
-    // loaded at decode time it would stall every stage by a memory latency,
-    // since the stage's codes usually land first.
+    // into a per-thread shared ring) by a look-ahead cursor: loaded at decode
+    // time it would stall every stage by a memory latency, since the stage's
+    // codes usually land first.
     const int dt = threadIdx.x - 192;  // 0..255
     const int pc = dt >> 1, hh = dt & 1;
     constexpr int PRE = L::AMAX_PRE;
     const uint32_t ring = base + L::OFF_AMAX + (uint32_t)dt * 4u;  // slot j at ring + 1024 j
-    const uint32_t lv = smem_addr(levels);
-    // absmax element of piece pc at K-block kb of tile nt (-1: none)
-    auto amax_index = [&](int nt, int kb) -> long long {
-      const GemmGroup &GN = p.grp[group_of(p, nt)];
-      const int nh = (nt - GN.tile_begin) * BN + (int)crank * 128;
-      const int gk = (DX && p.kgroups > 1 && kb >= p.ksplit) ? 1 : 0;
-      const GemmGroup &G = DX ? p.grp[gk] : GN;
-      int wrow, kblk;
-      if constexpr (DX) {
-        wrow = (kb - (gk ? p.ksplit : 0)) * kBK + (pc & 63);
-        kblk = (nh >> 6) + (pc >> 6);
-      } else {
-        wrow = nh + pc;
-        kblk = kb;
-      }
-      const bool in = DX ? (kblk < G.ld_absmax) : (wrow < G.ncols);
-      return in ? (long long)wrow * G.ld_absmax + kblk : -1;
-    };
-    TileIter ahead;
-    ahead.init(p.sched, pair);
-    int kb_a = 0;
-    // prefetch for the look-ahead position, then advance it by one K-block
+    float lvl[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) lvl[i] = kNf4Levels[i];
+    Nf4Cursor<DX> cur, ahead;
+    cur.init(p, pair, pc, (int)crank, nk);
+    ahead = cur;
     auto prefetch = [&](uint32_t slot) {
-      if (ahead.valid()) {
-        const int nt = ahead.nt();
-        const GemmGroup &GA = p.grp[group_of(p, nt)];
-        if (kb_a < nk) {
-          const long long idx = amax_index(nt, kb_a);
-          if (idx >= 0) {
-            const int gk = (DX && p.kgroups > 1 && kb_a >= p.ksplit) ? 1 : 0;
-            const GemmGroup &G = DX ? p.grp[gk] : GA;
-            cp_async_4(ring + slot * 1024u, G.absmax + (idx & ~1ll));  // the aligned word
-          }
-        }
-        if (++kb_a == nk + (DX ? p.grp[0].n_extra : GA.n_extra)) {
-          kb_a = 0;
-          ahead.next();
-        }
-      }
+      if (ahead.valid() && ahead.kb < nk && ahead.in)
+        cp_async_4(ring + slot * 1024u,
+                   reinterpret_cast<const void *>(reinterpret_cast<uintptr_t>(ahead.elem()) &
+                                                  ~uintptr_t(3)));
       cp_async_commit();
+      ahead.advance(p, pc, (int)crank, nk);
     };
     for (int j = 0; j < PRE; ++j) prefetch((uint32_t)j);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t slot = 0;
-    bool ok = true;
-    TileIter it;
-    for (it.init(p.sched, pair); ok && it.valid(); it.next()) {
-      const int nt = it.nt();
-      const GemmGroup &GN = p.grp[group_of(p, nt)];
-      const int ne = DX ? p.grp[0].n_extra : GN.n_extra;
-      for (int kb = 0; kb < nk + ne; ++kb) {
-        cp_async_wait<PRE - 1>();  // this K-block's absmax has landed
-        float amax = 0.0f;
-        if (kb < nk) {
-          const long long idx = amax_index(nt, kb);
-          if (idx >= 0) {
-            const uint32_t w = ld_shared_u32(ring + slot * 1024u);
-            amax = __uint_as_float(((idx & 1) ? (w >> 16) : (w & 0xFFFFu)) << 16);
-          }
-        }
-        prefetch(slot);  // the slot just read refills for K-block kb + PRE
-        if (++slot == (uint32_t)PRE) slot = 0;
-        if (!warp_wait(bar_raw + 8 * stage, phase, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        if (kb < nk) {
-          const uint32_t sx = base + stage * L::STAGE_BYTES;
-          uint32_t src, dst;
-          if constexpr (DX) {
-            src = sx + L::OFF_C + (pc & 63) * 64 + (pc >> 6) * 32 + hh * 16;
-            dst = sx + L::OFF_W + (pc >> 6) * 8192 + (pc & 63) * 128;
-          } else {
-            src = sx + L::OFF_C + pc * 32 + hh * 16;
-            dst = sx + L::OFF_W + pc * 128;
-          }
-          nf4_decode_half(src, dst, hh, amax, lv);
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(lead_dec + 8 * stage);
-        if (++stage == STAGES) stage = 0, phase ^= 1u;
+    while (cur.valid()) {
+      const int kb = cur.kb;
+      cp_async_wait<PRE - 1>();  // this K-block's absmax has landed
+      float amax = 0.0f;
+      if (kb < nk && cur.in) {
+        const uint32_t w = ld_shared_u32(ring + slot * 1024u);
+        const bool high = (reinterpret_cast<uintptr_t>(cur.elem()) & 2u) != 0;
+        amax = __uint_as_float((high ? (w >> 16) : (w & 0xFFFFu)) << 16);
       }
+      prefetch(slot);  // the slot just read refills for K-block kb + PRE
+      if (++slot == (uint32_t)PRE) slot = 0;
+      if (!warp_wait(bar_raw + 8 * stage, phase, abort_flag, p.status)) break;
+      if (kb < nk) {
+        const Nf4Table tab = nf4_table(lvl, amax);
+        const uint32_t sx = base + stage * L::STAGE_BYTES;
+        uint32_t src, dst;
+        if constexpr (DX) {
+          src = sx + L::OFF_C + (pc & 63) * 64 + (pc >> 6) * 32 + hh * 16;
+          dst = sx + L::OFF_W + (pc >> 6) * 8192 + (pc & 63) * 128;
+        } else {
+          src = sx + L::OFF_C + pc * 32 + hh * 16;
+          dst = sx + L::OFF_W + pc * 128;
+        }
+        nf4_decode_half(src, dst, hh, tab);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(lead_dec + 8 * stage);
+      if (++stage == STAGES) stage = 0, phase ^= 1u;
+      cur.advance(p, pc, (int)crank, nk);
     }
     cp_async_wait<0>();  // no copy may land after the CTA exits
   }

@@ -33,30 +33,57 @@ LORA_DEV uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
-// Decode half of a 64-element row piece: 16 code bytes at `src` (shared)
-// with block scale `a`, into the 16-byte chunks [4h, 4h+4) of a 128-byte
-// row of a 128-byte-swizzled tile at `dst` (h = which half).  Byte j of a
-// row holds element 2j in its high nibble and 2j+1 in its low nibble; each
-// element is the fp32 product level·a rounded once to bf16.  `lv` is the
-// shared-memory address of the 16 fp32 levels.
-LORA_DEV float ld_level(uint32_t lv, uint32_t nib) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(lv + (nib << 2)));
-  return v;
+// NF4 decode without shared-memory lookups.  Per K-block each decode
+// thread forms the 16 values level_i·a of its row (fp32 product rounded once
+// to bf16) and keeps them as two byte planes in registers: lo[q] holds the
+// low bytes of values 4q..4q+3, hi[q] their high bytes.  A 4-bit code then
+// selects its two bytes with byte permutes (prmt picks any of 8 bytes, so
+// values 0-7 and 8-15 are picked separately and merged by the code's top
+// bit).
+struct Nf4Table {
+  uint32_t lo[4], hi[4];
+};
+
+LORA_DEV Nf4Table nf4_table(const float (&lv)[16], float a) {
+  uint32_t pk[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) pk[j] = pack_bf16x2(lv[2 * j] * a, lv[2 * j + 1] * a);
+  Nf4Table t;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    t.lo[q] = __byte_perm(pk[2 * q], pk[2 * q + 1], 0x6420);
+    t.hi[q] = __byte_perm(pk[2 * q], pk[2 * q + 1], 0x7531);
+  }
+  return t;
 }
-LORA_DEV void nf4_decode_half(uint32_t src, uint32_t dst, int h, float a, uint32_t lv) {
+
+// Four codes, the nibbles of the 16-bit value c = [e1 | e0 << 4 | e3 << 8 |
+// e2 << 12] (two code bytes: element 2j in a byte's high nibble), to the
+// bf16 pairs (e0, e1) and (e2, e3).
+LORA_DEV void nf4_lookup4(const Nf4Table &t, uint32_t c, uint32_t &p01, uint32_t &p23) {
+  const uint32_t s7 = c & 0x7777u;                        // index within a half table
+  const uint32_t sel = 0x3210u | ((c >> 1) & 0x4444u);    // which half, per byte
+  const uint32_t lo = __byte_perm(__byte_perm(t.lo[0], t.lo[1], s7),
+                                  __byte_perm(t.lo[2], t.lo[3], s7), sel);
+  const uint32_t hi = __byte_perm(__byte_perm(t.hi[0], t.hi[1], s7),
+                                  __byte_perm(t.hi[2], t.hi[3], s7), sel);
+  // lo/hi bytes are in code order e1, e0, e3, e2
+  p01 = __byte_perm(lo, hi, 0x5140 ^ 0x1111);  // bytes lo.1, hi.1, lo.0, hi.0 -> (e0, e1)
+  p23 = __byte_perm(lo, hi, 0x7362 ^ 0x1111);  // bytes lo.3, hi.3, lo.2, hi.2 -> (e2, e3)
+}
+
+// Decode half h of a 64-element row piece: 16 code bytes at `src` (shared)
+// into the 16-byte chunks [4h, 4h+4) of a 128-byte row of a
+// 128-byte-swizzled tile at `dst`.
+LORA_DEV void nf4_decode_half(uint32_t src, uint32_t dst, int h, const Nf4Table &t) {
   const uint4 c = ld_shared_v4(src);
   const uint32_t words[4] = {c.x, c.y, c.z, c.w};
   const uint32_t phase = (dst >> 7) & 7u;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint32_t w = words[q];
     uint32_t o[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t hi = (w >> (8 * b + 4)) & 0xFu, lo = (w >> (8 * b)) & 0xFu;
-      o[b] = pack_bf16x2(ld_level(lv, hi) * a, ld_level(lv, lo) * a);
-    }
+    nf4_lookup4(t, words[q] & 0xFFFFu, o[0], o[1]);
+    nf4_lookup4(t, words[q] >> 16, o[2], o[3]);
     const uint32_t ch = (uint32_t)(4 * h + q);
     st_shared_v4(dst + ((ch ^ phase) << 4), o[0], o[1], o[2], o[3]);
   }

@@ -30,8 +30,9 @@
 //              already there).
 //   warps 6-13 NF4 only: decode the CTA's own half of the W tile through the
 //              16-entry NF4 codebook, scaled by the block absmax ("Unsloth教程"
-//              §显存优化策略: NF4 base weight); two threads per 64-element
-//              row piece.
+//              §显存优化策略: NF4 base weight).  Two groups of four warps take
+//              alternate K-blocks, one thread per 64-element row piece, so
+//              each group has two stage times per K-block it decodes.
 #include "gemm_common.cuh"
 
 namespace lora {
@@ -49,7 +50,7 @@ struct PairSmem {
   static constexpr int STAGE_BYTES = OFF_C + C_BYTES;
   static constexpr int EPI_BYTES = 4 * 4 * 2048;  // per epilogue warp: four 2 KB staging buffers
   static constexpr int AMAX_PRE = 8;               // NF4: absmax prefetch distance (K-blocks)
-  static constexpr int AMAX_BYTES = NF4 ? AMAX_PRE * 256 * 4 : 0;
+  static constexpr int AMAX_BYTES = NF4 ? AMAX_PRE * 256 * 4 : 0;  // per decode thread
   static constexpr int MISC_BYTES = 1024;
   static constexpr int FIXED = EPI_BYTES + AMAX_BYTES + MISC_BYTES + 1024;
   static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
@@ -151,7 +152,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
       mbar_init(bar_raw + 8 * s, 1);
-      mbar_init(bar_dec + 8 * s, NUM_DEC_WARPS > 0 ? 2 * NUM_DEC_WARPS : 1);
+      mbar_init(bar_dec + 8 * s, NUM_DEC_WARPS > 0 ? NUM_DEC_WARPS : 1);  // one group, 2 CTAs
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_full + 8, 1);
@@ -335,17 +336,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     __syncwarp();
   } else if constexpr (NF4) {
     // ============================================================= NF4 decode
-    // Thread dt decodes half h = dt & 1 of row piece pc = dt >> 1:
+    // Group gr = 0 / 1 (warps 6-9 / 10-13) decodes the K-blocks whose running
+    // index across the CTA's tiles is even / odd; thread pc of a group
+    // decodes row piece pc:
     // FWD: piece pc = row pc of this CTA's W half [128 rows x 64].
     // DX:  the half is [64 n-rows x 128 k-columns] = two boxes of [64 x 64];
     //      piece pc = row (pc % 64) of box (pc / 64).
-    // Rank K-blocks carry no codes: the decoders only pass them on.
-    // The absmax of a piece is fetched AMAX_PRE K-blocks ahead (cp.async
-    // into a per-thread shared ring) by a look-ahead cursor: loaded at decode
-    // time it would stall every stage by a memory latency, since the stage's
-    // codes usually land first.
+    // Rank K-blocks carry no codes: their group only passes them on.
+    // The absmax of a piece is fetched AMAX_PRE of the group's K-blocks
+    // ahead (cp.async into a per-thread shared ring) by a look-ahead cursor:
+    // loaded at decode time it would stall every stage by a memory latency,
+    // since the stage's codes usually land first.
     const int dt = threadIdx.x - 192;  // 0..255
-    const int pc = dt >> 1, hh = dt & 1;
+    const int gr = dt >> 7, pc = dt & 127;
     constexpr int PRE = L::AMAX_PRE;
     const uint32_t ring = base + L::OFF_AMAX + (uint32_t)dt * 4u;  // slot j at ring + 1024 j
     float lvl[16];
@@ -353,6 +356,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     for (int i = 0; i < 16; ++i) lvl[i] = kNf4Levels[i];
     Nf4Cursor<DX> cur, ahead;
     cur.init(p, pair, pc, (int)crank, nk);
+    if (gr) cur.advance(p, pc, (int)crank, nk);  // group 1 starts at the second K-block
     ahead = cur;
     auto prefetch = [&](uint32_t slot) {
       if (ahead.valid() && ahead.kb < nk && ahead.in)
@@ -361,10 +365,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
                                                   ~uintptr_t(3)));
       cp_async_commit();
       ahead.advance(p, pc, (int)crank, nk);
+      ahead.advance(p, pc, (int)crank, nk);
     };
     for (int j = 0; j < PRE; ++j) prefetch((uint32_t)j);
-    int stage = 0;
+    int stage = gr;  // the group's K-blocks use every other stage of the ring
     uint32_t phase = 0;
+    if (stage >= STAGES) stage -= STAGES, phase ^= 1u;
     uint32_t slot = 0;
     while (cur.valid()) {
       const int kb = cur.kb;
@@ -375,7 +381,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
         const bool high = (reinterpret_cast<uintptr_t>(cur.elem()) & 2u) != 0;
         amax = __uint_as_float((high ? (w >> 16) : (w & 0xFFFFu)) << 16);
       }
-      prefetch(slot);  // the slot just read refills for K-block kb + PRE
+      prefetch(slot);  // the slot just read refills for the group's K-block PRE ahead
       if (++slot == (uint32_t)PRE) slot = 0;
       if (!warp_wait(bar_raw + 8 * stage, phase, abort_flag, p.status)) break;
       if (kb < nk) {
@@ -383,18 +389,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
         const uint32_t sx = base + stage * L::STAGE_BYTES;
         uint32_t src, dst;
         if constexpr (DX) {
-          src = sx + L::OFF_C + (pc & 63) * 64 + (pc >> 6) * 32 + hh * 16;
+          src = sx + L::OFF_C + (pc & 63) * 64 + (pc >> 6) * 32;
           dst = sx + L::OFF_W + (pc >> 6) * 8192 + (pc & 63) * 128;
         } else {
-          src = sx + L::OFF_C + pc * 32 + hh * 16;
+          src = sx + L::OFF_C + pc * 32;
           dst = sx + L::OFF_W + pc * 128;
         }
-        nf4_decode_half(src, dst, hh, tab);
+        nf4_decode_row(src, dst, tab);
         fence_proxy_async_smem();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(lead_dec + 8 * stage);
-      if (++stage == STAGES) stage = 0, phase ^= 1u;
+      // next K-block of this group: two stages on
+      stage += 2;
+      if (stage >= STAGES) stage -= STAGES, phase ^= 1u;
+      cur.advance(p, pc, (int)crank, nk);
       cur.advance(p, pc, (int)crank, nk);
     }
     cp_async_wait<0>();  // no copy may land after the CTA exits

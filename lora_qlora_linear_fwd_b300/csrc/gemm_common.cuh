@@ -72,20 +72,19 @@ LORA_DEV void nf4_lookup4(const Nf4Table &t, uint32_t c, uint32_t &p01, uint32_t
   p23 = __byte_perm(lo, hi, 0x7362 ^ 0x1111);  // bytes lo.3, hi.3, lo.2, hi.2 -> (e2, e3)
 }
 
-// Decode half h of a 64-element row piece: 16 code bytes at `src` (shared)
-// into the 16-byte chunks [4h, 4h+4) of a 128-byte row of a
-// 128-byte-swizzled tile at `dst`.
-LORA_DEV void nf4_decode_half(uint32_t src, uint32_t dst, int h, const Nf4Table &t) {
-  const uint4 c = ld_shared_v4(src);
-  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+// Decode one 64-element row piece: 32 code bytes at `src` (shared) into a
+// 128-byte row of a 128-byte-swizzled tile at `dst`.
+LORA_DEV void nf4_decode_row(uint32_t src, uint32_t dst, const Nf4Table &t) {
+  const uint4 c01 = ld_shared_v4(src);
+  const uint4 c23 = ld_shared_v4(src + 16);
+  const uint32_t words[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
   const uint32_t phase = (dst >> 7) & 7u;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 8; ++q) {
     uint32_t o[4];
     nf4_lookup4(t, words[q] & 0xFFFFu, o[0], o[1]);
     nf4_lookup4(t, words[q] >> 16, o[2], o[3]);
-    const uint32_t ch = (uint32_t)(4 * h + q);
-    st_shared_v4(dst + ((ch ^ phase) << 4), o[0], o[1], o[2], o[3]);
+    st_shared_v4(dst + ((((uint32_t)q) ^ phase) << 4), o[0], o[1], o[2], o[3]);
   }
 }
 

@@ -125,39 +125,54 @@ __constant__ float kNf4LevelsMisc[16] = {
     0.07958029955625534f, 0.16093020141124725f, 0.24611230194568634f, 0.33791524171829224f,
     0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
 
-// One thread per 16 code bytes (32 elements; half of a 64-element block).
-// HBM-bound: reads n·k/2 + n·k/32 bytes, writes 2·n·k bytes.
+// One thread per 32-bit code word (8 elements, 16 output bytes), so a
+// warp's code loads are 128 contiguous bytes and its stores 512; the eight
+// threads of a 64-element block read the same absmax.  Each element is the
+// fp32 product level·absmax rounded once to bf16, the level read from a
+// 16-entry shared table (conflict-free: 16 banks, equal codes broadcast).
+// Four words per thread per trip keep more loads in flight.  HBM-bound:
+// reads n·k/2 + n·k/32 bytes, writes 2·n·k bytes.
+__device__ __forceinline__ uint4 dq_word(uint32_t c, float a, const float *lv) {
+  uint32_t o[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t byte = (c >> (8 * b)) & 0xFFu;
+    o[b] = pack_bf16x2(lv[byte >> 4] * a, lv[byte & 0xFu] * a);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t *__restrict__ codes,
                                                           const __nv_bfloat16 *__restrict__ absmax,
                                                           __nv_bfloat16 *__restrict__ w,
-                                                          size_t n_chunks) {
+                                                          size_t n_words) {
   __shared__ float lv[16];
   if (threadIdx.x < 16) lv[threadIdx.x] = kNf4LevelsMisc[threadIdx.x];
   __syncthreads();
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n_chunks;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const uint4 c = __ldg(reinterpret_cast<const uint4 *>(codes) + i);
-    const float a = __bfloat162float(absmax[i >> 1]);
-    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-    uint4 *dst = reinterpret_cast<uint4 *>(w) + 4 * i;
+  const uint32_t *c32 = reinterpret_cast<const uint32_t *>(codes);
+  uint4 *w4 = reinterpret_cast<uint4 *>(w);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n_words; i += 4 * stride) {
+    uint32_t c[4];
+    float a[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t o[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t byte = (words[q] >> (8 * b)) & 0xFFu;
-        o[b] = pack_bf16x2(lv[byte >> 4] * a, lv[byte & 0xFu] * a);
-      }
-      dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int u = 0; u < 4; ++u) {
+      c[u] = __ldcs(c32 + i + u * stride);
+      a[u] = __bfloat162float(absmax[(i + u * stride) >> 3]);
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) __stcs(w4 + i + u * stride, dq_word(c[u], a[u], lv));
   }
+  for (; i < n_words; i += stride)
+    __stcs(w4 + i, dq_word(__ldcs(c32 + i), __bfloat162float(absmax[i >> 3]), lv));
 }
 
 cudaError_t launch_nf4_dequant(const uint8_t *codes, const __nv_bfloat16 *absmax,
                                __nv_bfloat16 *w, int n, int k, cudaStream_t st) {
-  const size_t chunks = (size_t)n * k / 32;
-  const int grid = grid_for(chunks, 256, 148 * 8);
-  nf4_dequant_kernel<<<grid, 256, 0, st>>>(codes, absmax, w, chunks);
+  const size_t words = (size_t)n * k / 8;
+  const int grid = grid_for(words, 256, 148 * 8);
+  nf4_dequant_kernel<<<grid, 256, 0, st>>>(codes, absmax, w, words);
   note_launch();
   return cudaGetLastError();
 }

@@ -170,6 +170,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   cluster_sync_all();  // barriers of both CTAs initialised before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dep_launch();
+  grid_dep_wait();  // the previous kernel's outputs (s·v, dY) are complete
   const int nk = p.K / kBK;  // main K-blocks
   // the even CTA's copies of the barriers the pair shares
   const uint32_t lead_full = map_shared_rank(bar_full, 0);
@@ -427,9 +429,7 @@ static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<2 * pairs, pair_threads(NF4), L::TOTAL, st>>>(p);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(2 * pairs), dim3(pair_threads(NF4)), L::TOTAL, st, 0u, p);
 }
 
 template <int MODE, bool NF4, bool ROPE>

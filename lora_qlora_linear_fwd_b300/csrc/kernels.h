@@ -62,6 +62,37 @@ enum GemmMode { kModeFwd = 0, kModeDx = 1 };
 // Count of kernel launches issued by the library (see lora_kernel_launch_count).
 void note_launch();
 
+// Launch with programmatic stream serialization (the kernel calls
+// grid_dep_wait() before touching global memory), and optionally cluster
+// dimensions (cluster_x > 0; kernels with compile-time cluster dimensions
+// pass 0).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster_x > 0) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster_x;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  note_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Two-SM (CTA pair) fused GEMM: 256 x 256 tiles over `pairs` persistent pairs.
 cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int pairs,
                              cudaStream_t st);

@@ -58,6 +58,8 @@ LORA_DEV void rope_bwd_item(const BwdPrep &p, size_t i) {
 }
 
 __global__ void bwd_prep_kernel(const BwdPrep p) {
+  grid_dep_launch();
+  grid_dep_wait();
   const int n = p.n1 + p.n2, rl = p.nproj * p.r;
   const size_t n_rope = p.dy1 ? (size_t)p.M * (n / 128) * 8 : 0;
   const size_t n_a = p.nproj > 1 ? (size_t)rl * p.k / 8 : 0;   // 16-byte pieces
@@ -86,9 +88,8 @@ cudaError_t launch_bwd_prep(const BwdPrep &p, cudaStream_t st) {
   const int n = p.n1 + p.n2, rl = p.nproj * p.r;
   const size_t total = (p.dy1 ? (size_t)p.M * (n / 128) * 8 : 0) +
                        (p.nproj > 1 ? (size_t)rl * p.k / 8 : 0) + (size_t)rl * n;
-  bwd_prep_kernel<<<grid_for(total, 256, 148 * 16), 256, 0, st>>>(p);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(bwd_prep_kernel, dim3(grid_for(total, 256, 148 * 16)), dim3(256), 0, st, 0u,
+                    p);
 }
 
 // --------------------------------------------------------------- RoPE cache

@@ -239,6 +239,15 @@ LORA_DEV uint32_t ld_shared_u32(uint32_t addr) {
   return v;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream is still
+// running; it calls grid_dep_wait() before its first global-memory access,
+// which returns once every prerequisite grid has completed and its writes
+// are visible.  grid_dep_launch() lets this kernel's own dependents start
+// launching (they still wait for this grid to complete).
+LORA_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+LORA_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------ clusters
 LORA_DEV uint32_t cluster_ctarank() {
   uint32_t r;

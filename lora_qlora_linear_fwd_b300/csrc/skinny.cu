@@ -206,6 +206,8 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dep_launch();
+  grid_dep_wait();  // the previous kernel's outputs are complete
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -387,21 +389,8 @@ static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
   }
   int tiles = 0;
   for (int q = 0; q < p.num_problems; ++q) tiles += p.pr[q].row_tiles;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * p.split), 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
-  cfg.dynamicSmemBytes = L::TOTAL;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)p.split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
-  note_launch();
-  return e != cudaSuccess ? e : cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)(tiles * p.split)), dim3(192), L::TOTAL, st,
+                    (unsigned)p.split, p);
 }
 
 template <bool MN, int RP>

@@ -15,7 +15,7 @@
 // the tensor cores of both SMs work on the pair tile, and each SM stages
 // half of the W bytes a one-SM 128 x 256 tile would need.
 //
-// Roles (both CTAs unless noted):
+// Roles (both CTAs unless noted; NF4 rings as in PairSmem):
 //   warp 0     TMA producer: own halves of x/dY and of W (or NF4 codes) per
 //              main K-block; own halves of s·v / s·u and of B / A per rank
 //              K-block.  Completion is counted on the even CTA's barriers.
@@ -40,27 +40,43 @@ namespace lora {
 // Threads per CTA: producer, MMA, 4 epilogue warps (+ 8 NF4 decode warps).
 constexpr int pair_threads(bool nf4) { return nf4 ? 448 : 192; }
 
+// Shared-memory layout.  bf16 W: each pipeline stage holds the x tile and
+// the W tile.  NF4 W: the TMA ring holds the x tile and the code bytes, and
+// the decoded W tiles have a ring of their own (decoding sits between the
+// copy landing and the MMA, so the copies need the deeper ring); a rank
+// K-block's B or A tile is copied straight into the W ring.  The two NF4
+// decode groups take alternate K-blocks, so both rings have an even number
+// of slots: each slot then belongs to one group, which waits on every
+// phase of its slots in order (a parity wait is only unambiguous for a
+// waiter at most one phase ahead).
 template <bool NF4>
 struct PairSmem {
   static constexpr int X_BYTES = 128 * 128;  // own 128 rows x 64 K
   static constexpr int W_BYTES = 128 * 128;  // own 128 N-rows x 64 K
   static constexpr int C_BYTES = NF4 ? 128 * 32 : 0;
-  static constexpr int OFF_W = X_BYTES;
-  static constexpr int OFF_C = OFF_W + W_BYTES;
-  static constexpr int STAGE_BYTES = OFF_C + C_BYTES;
+  static constexpr int OFF_W = X_BYTES;      // bf16: W inside the stage
+  static constexpr int OFF_C = X_BYTES;      // NF4: codes inside the stage
+  static constexpr int STAGE_BYTES = X_BYTES + (NF4 ? C_BYTES : W_BYTES);
+  static constexpr int W_STAGES = NF4 ? 4 : 0;
+  static constexpr int WRING_BYTES = W_STAGES * W_BYTES;
   static constexpr int EPI_BYTES = 4 * 4 * 2048;  // per epilogue warp: four 2 KB staging buffers
-  static constexpr int AMAX_PRE = 8;               // NF4: absmax prefetch distance (K-blocks)
-  static constexpr int AMAX_BYTES = NF4 ? AMAX_PRE * 256 * 4 : 0;  // per decode thread
+  static constexpr int AMAX_PRE = NF4 ? 4 : 0;    // absmax prefetch distance (a group's K-blocks)
+  static constexpr int AMAX_BYTES = AMAX_PRE * 256 * 4;  // per decode thread
   static constexpr int MISC_BYTES = 1024;
-  static constexpr int FIXED = EPI_BYTES + AMAX_BYTES + MISC_BYTES + 1024;
+  static constexpr int FIXED = WRING_BYTES + EPI_BYTES + AMAX_BYTES + MISC_BYTES + 1024;
   static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
+  static constexpr int STAGES_CAP = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int STAGES = NF4 ? (STAGES_CAP & ~1) : STAGES_CAP;
+  static constexpr int OFF_WRING = STAGES * STAGE_BYTES;
+  static constexpr int OFF_EPI = OFF_WRING + WRING_BYTES;
   static constexpr int OFF_AMAX = OFF_EPI + EPI_BYTES;
   static constexpr int OFF_MISC = OFF_AMAX + AMAX_BYTES;
   static constexpr int TOTAL = OFF_MISC + MISC_BYTES + 1024;
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * W_STAGES + 5;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-  static_assert(STAGES >= 3, "pipeline depth");
+  static_assert(STAGES >= 3 && (!NF4 || W_STAGES >= 4), "pipeline depth");
+  static_assert(!NF4 || (STAGES % 2 == 0 && W_STAGES % 2 == 0), "one decode group per slot");
+  static_assert(8 * NUM_BARS + 16 <= MISC_BYTES, "barriers fit");
   static_assert(TOTAL <= kSmemLimit, "shared memory budget");
 };
 
@@ -136,14 +152,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   const bool leader = crank == 0;
   const int pair = blockIdx.x >> 1;
 
+  constexpr int WST = L::W_STAGES;
   const uint32_t bar_full = base + L::OFF_MISC;       // [S] leader: TMA of both CTAs
   const uint32_t bar_empty = bar_full + 8 * STAGES;   // [S] both: pair MMA done
-  const uint32_t bar_raw = bar_empty + 8 * STAGES;    // [S] both: own NF4 codes landed
-  const uint32_t bar_dec = bar_raw + 8 * STAGES;      // [S] leader: both halves decoded
-  const uint32_t bar_acc_full = bar_dec + 8 * STAGES; // [2] both: accumulator b ready
+  const uint32_t bar_raw = bar_empty + 8 * STAGES;    // [S] both: own NF4 codes (or B) landed
+  const uint32_t bar_wfull = bar_raw + 8 * STAGES;    // [WST] leader: W slot of both CTAs ready
+  const uint32_t bar_wempty = bar_wfull + 8 * WST;    // [WST] both: pair MMA done with W slot
+  const uint32_t bar_acc_full = bar_wempty + 8 * WST; // [2] both: accumulator b ready
   const uint32_t bar_acc_empty = bar_acc_full + 16;   // [2] leader: 8 warps drained b
   const uint32_t bar_drain = bar_acc_empty + 16;      // leader
-  const int misc_words = (8 * (4 * STAGES + 5)) / 4;
+  const int misc_words = (8 * L::NUM_BARS) / 4;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC) + misc_words;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
@@ -152,7 +170,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
       mbar_init(bar_raw + 8 * s, 1);
-      mbar_init(bar_dec + 8 * s, NUM_DEC_WARPS > 0 ? NUM_DEC_WARPS : 1);  // one group, 2 CTAs
+    }
+    for (int w = 0; w < WST; ++w) {
+      mbar_init(bar_wfull + 8 * w, NUM_DEC_WARPS);  // one decode group in each of 2 CTAs
+      mbar_init(bar_wempty + 8 * w, 1);
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_full + 8, 1);
@@ -175,7 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   const int nk = p.K / kBK;  // main K-blocks
   // the even CTA's copies of the barriers the pair shares
   const uint32_t lead_full = map_shared_rank(bar_full, 0);
-  const uint32_t lead_dec = map_shared_rank(bar_dec, 0);
+  const uint32_t lead_wfull = map_shared_rank(bar_wfull, 0);
   const uint32_t lead_acc_empty = map_shared_rank(bar_acc_empty, 0);
 
   if (warp == 0) {
@@ -231,15 +252,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
             // rank K-block e: s·v (or s·u) columns and the matching B (or A)
             const int e = kb - nk;
             const GemmGroup &R = DX ? p.grp[0] : G;
-            if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (L::X_BYTES + L::W_BYTES));
-            tma_load_2d_pair(sx, &p.tm_sv, fb, R.sv_col + e * kBK, row0);
-            if constexpr (DX) {  // A [rl, k] MN-major: 2 boxes [64 k-columns x 64 rank rows]
-              tma_load_2d_pair(sx + L::OFF_W, &R.tm_b, fb, nh, e * kBK);
-              tma_load_2d_pair(sx + L::OFF_W + 8192, &R.tm_b, fb, nh + 64, e * kBK);
-            } else {             // B [n, r] K-major: own 128 rows x 64
-              tma_load_2d_pair(sx + L::OFF_W, &R.tm_b, fb, e * kBK, nh);
+            if constexpr (NF4) {
+              // B / A goes straight into the W ring: the decode group that
+              // owns the slot copies it once the slot is free; its landing is
+              // counted on this stage's raw barrier, armed here
+              if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * L::X_BYTES);
+              tma_load_2d_pair(sx, &p.tm_sv, fb, R.sv_col + e * kBK, row0);
+              mbar_arrive_expect_tx(bar_raw + 8 * stage, L::W_BYTES);
+            } else {
+              if (leader)
+                mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (L::X_BYTES + L::W_BYTES));
+              tma_load_2d_pair(sx, &p.tm_sv, fb, R.sv_col + e * kBK, row0);
+              if constexpr (DX) {  // A [rl, k] MN-major: 2 boxes [64 k-columns x 64 rank rows]
+                tma_load_2d_pair(sx + L::OFF_W, &R.tm_b, fb, nh, e * kBK);
+                tma_load_2d_pair(sx + L::OFF_W + 8192, &R.tm_b, fb, nh + 64, e * kBK);
+              } else {             // B [n, r] K-major: own 128 rows x 64
+                tma_load_2d_pair(sx + L::OFF_W, &R.tm_b, fb, e * kBK, nh);
+              }
             }
-            if constexpr (NF4) mbar_arrive(bar_raw + 8 * stage);  // no codes: decoders pass
           }
           ++fills[stage];
           if (++stage == STAGES) stage = 0, phase ^= 1u;
@@ -257,6 +287,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       constexpr uint32_t idesc = make_idesc_bf16(256, BN, false, DX);
       int stage = 0;
       uint32_t phase = 0;
+      int wslot = 0;
+      uint32_t wphase = 0;
       int tile_count = 0;
       int used[2] = {0, 0};  // tiles issued into each accumulator buffer
       bool ok = true;
@@ -276,13 +308,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
             ok = false;
             break;
           }
-          if (NF4 && !mbar_wait_cluster(bar_dec + 8 * stage, phase, abort_flag, p.status)) {
+          if (NF4 && !mbar_wait_cluster(bar_wfull + 8 * wslot, wphase, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sx = base + stage * L::STAGE_BYTES;
-          const uint32_t sw = sx + L::OFF_W;
+          const uint32_t sw = NF4 ? base + L::OFF_WRING + wslot * L::W_BYTES : sx + L::OFF_W;
 #pragma unroll
           for (int ks = 0; ks < kBK / 16; ++ks) {
             const uint64_t da = make_sdesc(sx + ks * 32, 16, 1024, kSw128);
@@ -295,6 +327,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
           }
           tc_commit_pair(bar_empty + 8 * stage, kBoth);
           if (++stage == STAGES) stage = 0, phase ^= 1u;
+          if constexpr (NF4) {
+            tc_commit_pair(bar_wempty + 8 * wslot, kBoth);
+            if (++wslot == WST) wslot = 0, wphase ^= 1u;
+          }
         }
         if (!ok) break;
         tc_commit_pair(bar_acc_full + 8 * buf, kBoth);
@@ -344,7 +380,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     // FWD: piece pc = row pc of this CTA's W half [128 rows x 64].
     // DX:  the half is [64 n-rows x 128 k-columns] = two boxes of [64 x 64];
     //      piece pc = row (pc % 64) of box (pc / 64).
-    // Rank K-blocks carry no codes: their group only passes them on.
+    // A rank K-block's B / A tile is copied into the W slot by one lane of
+    // the group (counted on the stage's raw barrier); the group waits for
+    // it and passes the slot on.
+    // Decoded tiles go to the W ring (slot g % WST for running K-block g),
+    // whose slots the MMA releases through bar_wempty.
     // The absmax of a piece is fetched AMAX_PRE of the group's K-blocks
     // ahead (cp.async into a per-thread shared ring) by a look-ahead cursor:
     // loaded at decode time it would stall every stage by a memory latency,
@@ -373,6 +413,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     int stage = gr;  // the group's K-blocks use every other stage of the ring
     uint32_t phase = 0;
     if (stage >= STAGES) stage -= STAGES, phase ^= 1u;
+    int wslot = gr;  // and every other slot of the W ring
+    uint32_t wphase = 0;
+    int wuses[WST / 2];  // uses of the group's W slots gr, gr + 2, ...
+    for (int j = 0; j < WST / 2; ++j) wuses[j] = 0;
     uint32_t slot = 0;
     while (cur.valid()) {
       const int kb = cur.kb;
@@ -385,30 +429,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       }
       prefetch(slot);  // the slot just read refills for the group's K-block PRE ahead
       if (++slot == (uint32_t)PRE) slot = 0;
+      // the W slot is free once the MMA of its previous use has completed
+      if (!warp_wait(bar_wempty + 8 * wslot, wphase ^ 1u, abort_flag, p.status)) break;
+      ++wuses[wslot >> 1];
+      if (kb >= nk && (warp & 3) == 2 && lane == 0) {
+        // rank K-block e: this CTA's half of B [n, r] (K-major) or of A [rl, k]
+        // (MN-major) into the W slot
+        const int e = kb - nk;
+        const int nt = cur.it.nt();
+        const GemmGroup &G = p.grp[group_of(p, nt)];
+        const GemmGroup &R = DX ? p.grp[0] : G;
+        const int nh = (nt - G.tile_begin) * BN + (int)crank * 128;
+        const uint32_t sw = base + L::OFF_WRING + wslot * L::W_BYTES;
+        const uint32_t rb = bar_raw + 8 * stage;
+        if constexpr (DX) {
+          tma_load_2d(sw, &R.tm_b, rb, nh, e * kBK);
+          tma_load_2d(sw + 8192, &R.tm_b, rb, nh + 64, e * kBK);
+        } else {
+          tma_load_2d(sw, &R.tm_b, rb, e * kBK, nh);
+        }
+      }
       if (!warp_wait(bar_raw + 8 * stage, phase, abort_flag, p.status)) break;
       if (kb < nk) {
         const Nf4Table tab = nf4_table(lvl, amax);
         const uint32_t sx = base + stage * L::STAGE_BYTES;
+        const uint32_t sw = base + L::OFF_WRING + wslot * L::W_BYTES;
         uint32_t src, dst;
         if constexpr (DX) {
           src = sx + L::OFF_C + (pc & 63) * 64 + (pc >> 6) * 32;
-          dst = sx + L::OFF_W + (pc >> 6) * 8192 + (pc & 63) * 128;
+          dst = sw + (pc >> 6) * 8192 + (pc & 63) * 128;
         } else {
           src = sx + L::OFF_C + pc * 32;
-          dst = sx + L::OFF_W + pc * 128;
+          dst = sw + pc * 128;
         }
         nf4_decode_row(src, dst, tab);
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(lead_dec + 8 * stage);
-      // next K-block of this group: two stages on
+      if (lane == 0) mbar_arrive_remote(lead_wfull + 8 * wslot);
+      // next K-block of this group: two stages (and W slots) on
       stage += 2;
       if (stage >= STAGES) stage -= STAGES, phase ^= 1u;
+      wslot += 2;
+      if (wslot >= WST) wslot -= WST, wphase ^= 1u;
       cur.advance(p, pc, (int)crank, nk);
       cur.advance(p, pc, (int)crank, nk);
     }
     cp_async_wait<0>();  // no copy may land after the CTA exits
+    // and no release of the group's W slots (multicast by the MMA) may
+    // still be in flight (bounded: after an abort some never come)
+    if (lane == 0) {
+      const uint64_t lim = *abort_flag ? 20000000ull : 1000000000ull;
+      for (int j = 0; j < WST / 2; ++j)
+        if (wuses[j] > 0)
+          mbar_wait_quiet(bar_wempty + 8 * (gr + 2 * j), (uint32_t)((wuses[j] - 1) & 1), lim);
+    }
   }
 
   __syncthreads();

@@ -45,10 +45,12 @@ constexpr int pair_threads(bool nf4) { return nf4 ? 448 : 192; }
 // the decoded W tiles have a ring of their own (decoding sits between the
 // copy landing and the MMA, so the copies need the deeper ring); a rank
 // K-block's B or A tile is copied straight into the W ring.  The two NF4
-// decode groups take alternate K-blocks, so both rings have an even number
-// of slots: each slot then belongs to one group, which waits on every
-// phase of its slots in order (a parity wait is only unambiguous for a
-// waiter at most one phase ahead).
+// decode groups take alternate K-blocks.  A parity wait is only
+// unambiguous for a waiter at most one phase ahead of the barrier, so each
+// waiter must see every phase of its barrier: the W ring has an even
+// number of slots (each slot belongs to one group), and the code-landing
+// barrier of a TMA stage is split in two, one per group, armed by the
+// producer for the group of the K-block.
 template <bool NF4>
 struct PairSmem {
   static constexpr int X_BYTES = 128 * 128;  // own 128 rows x 64 K
@@ -59,23 +61,22 @@ struct PairSmem {
   static constexpr int STAGE_BYTES = X_BYTES + (NF4 ? C_BYTES : W_BYTES);
   static constexpr int W_STAGES = NF4 ? 4 : 0;
   static constexpr int WRING_BYTES = W_STAGES * W_BYTES;
-  static constexpr int EPI_BYTES = 4 * 4 * 2048;  // per epilogue warp: four 2 KB staging buffers
+  static constexpr int EPI_BYTES = 4 * 2 * 2048;  // per epilogue warp: two 2 KB staging buffers
   static constexpr int AMAX_PRE = NF4 ? 4 : 0;    // absmax prefetch distance (a group's K-blocks)
   static constexpr int AMAX_BYTES = AMAX_PRE * 256 * 4;  // per decode thread
   static constexpr int MISC_BYTES = 1024;
   static constexpr int FIXED = WRING_BYTES + EPI_BYTES + AMAX_BYTES + MISC_BYTES + 1024;
   static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
-  static constexpr int STAGES_CAP = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int STAGES = NF4 ? (STAGES_CAP & ~1) : STAGES_CAP;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int OFF_WRING = STAGES * STAGE_BYTES;
   static constexpr int OFF_EPI = OFF_WRING + WRING_BYTES;
   static constexpr int OFF_AMAX = OFF_EPI + EPI_BYTES;
   static constexpr int OFF_MISC = OFF_AMAX + AMAX_BYTES;
   static constexpr int TOTAL = OFF_MISC + MISC_BYTES + 1024;
-  static constexpr int NUM_BARS = 3 * STAGES + 2 * W_STAGES + 5;
+  static constexpr int NUM_BARS = 4 * STAGES + 2 * W_STAGES + 5;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 3 && (!NF4 || W_STAGES >= 4), "pipeline depth");
-  static_assert(!NF4 || (STAGES % 2 == 0 && W_STAGES % 2 == 0), "one decode group per slot");
+  static_assert(!NF4 || W_STAGES % 2 == 0, "one decode group per W slot");
   static_assert(8 * NUM_BARS + 16 <= MISC_BYTES, "barriers fit");
   static_assert(TOTAL <= kSmemLimit, "shared memory budget");
 };
@@ -87,7 +88,8 @@ template <bool DX>
 struct Nf4Cursor {
   TileIter it;
   int kb, len;                        // K-block in the tile; K-blocks per tile
-  const __nv_bfloat16 *p0, *p1;       // element at K-block 0 of each K-group
+  const __nv_bfloat16 *e;             // absmax element of K-block kb
+  const __nv_bfloat16 *p1;            // element at the first K-block of the second K-group
   long long step;                     // elements per K-block
   int split;                          // first K-block of the second K-group
   bool in;                            // the piece lies inside W
@@ -101,14 +103,14 @@ struct Nf4Cursor {
       const int kblk = (nh >> 6) + (pc >> 6);
       in = kblk < ld;
       step = 64ll * ld;
-      p0 = p.grp[0].absmax + (long long)(pc & 63) * ld + kblk;
-      p1 = p.kgroups > 1 ? p.grp[1].absmax + (long long)(pc & 63) * ld + kblk : p0;
+      e = p.grp[0].absmax + (long long)(pc & 63) * ld + kblk;
+      p1 = p.kgroups > 1 ? p.grp[1].absmax + (long long)(pc & 63) * ld + kblk : e;
       split = p.kgroups > 1 ? p.ksplit : nk;
     } else {
       const int wrow = nh + pc;
       in = wrow < G.ncols;
       step = 1;
-      p0 = p1 = G.absmax + (long long)(in ? wrow : 0) * G.ld_absmax;
+      e = p1 = G.absmax + (long long)(in ? wrow : 0) * G.ld_absmax;
       split = nk;
     }
   }
@@ -118,15 +120,17 @@ struct Nf4Cursor {
     if (it.valid()) tile(p, pc, crank, nk);
   }
   __device__ bool valid() const { return it.valid(); }
-  __device__ const __nv_bfloat16 *elem() const {
-    return kb < split ? p0 + kb * step : p1 + (kb - split) * step;
-  }
+  __device__ const __nv_bfloat16 *elem() const { return e; }
   __device__ void advance(const GemmParams &p, int pc, int crank, int nk) {
     if (!it.valid()) return;
     if (++kb == len) {
       kb = 0;
       it.next();
       if (it.valid()) tile(p, pc, crank, nk);
+    } else if (kb == split) {
+      e = p1;
+    } else {
+      e += step;
     }
   }
 };
@@ -155,8 +159,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   constexpr int WST = L::W_STAGES;
   const uint32_t bar_full = base + L::OFF_MISC;       // [S] leader: TMA of both CTAs
   const uint32_t bar_empty = bar_full + 8 * STAGES;   // [S] both: pair MMA done
-  const uint32_t bar_raw = bar_empty + 8 * STAGES;    // [S] both: own NF4 codes (or B) landed
-  const uint32_t bar_wfull = bar_raw + 8 * STAGES;    // [WST] leader: W slot of both CTAs ready
+  const uint32_t bar_raw = bar_empty + 8 * STAGES;    // [S][2] both: own NF4 codes (or B) landed,
+                                                      //   one barrier per decode group
+  const uint32_t bar_wfull = bar_raw + 16 * STAGES;   // [WST] leader: W slot of both CTAs ready
   const uint32_t bar_wempty = bar_wfull + 8 * WST;    // [WST] both: pair MMA done with W slot
   const uint32_t bar_acc_full = bar_wempty + 8 * WST; // [2] both: accumulator b ready
   const uint32_t bar_acc_empty = bar_acc_full + 16;   // [2] leader: 8 warps drained b
@@ -169,7 +174,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
-      mbar_init(bar_raw + 8 * s, 1);
+      mbar_init(bar_raw + 16 * s, 1);
+      mbar_init(bar_raw + 16 * s + 8, 1);
     }
     for (int w = 0; w < WST; ++w) {
       mbar_init(bar_wfull + 8 * w, NUM_DEC_WARPS);  // one decode group in each of 2 CTAs
@@ -206,6 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       tma_prefetch_desc(&p.tm_sv);
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t kpar = 0;  // parity of the running K-block index: its decode group
       int fills[STAGES];
       for (int s = 0; s < STAGES; ++s) fills[s] = 0;
       bool ok = true;
@@ -234,7 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
             const CUtensorMap *tw = DX ? &p.grp[gk].tm_w : &G.tm_w;
             const int wk = kb - (gk ? p.ksplit : 0);
             if constexpr (NF4) {
-              const uint32_t rb = bar_raw + 8 * stage;
+              const uint32_t rb = bar_raw + 16 * stage + 8 * kpar;
               mbar_arrive_expect_tx(rb, L::C_BYTES);
               if constexpr (DX)  // codes [64 rows of W, 64 bytes = 128 k-columns]
                 tma_load_2d(sx + L::OFF_C, tw, rb, nh / 2, wk * kBK);
@@ -258,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
               // counted on this stage's raw barrier, armed here
               if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * L::X_BYTES);
               tma_load_2d_pair(sx, &p.tm_sv, fb, R.sv_col + e * kBK, row0);
-              mbar_arrive_expect_tx(bar_raw + 8 * stage, L::W_BYTES);
+              mbar_arrive_expect_tx(bar_raw + 16 * stage + 8 * kpar, L::W_BYTES);
             } else {
               if (leader)
                 mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (L::X_BYTES + L::W_BYTES));
@@ -273,6 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
           }
           ++fills[stage];
           if (++stage == STAGES) stage = 0, phase ^= 1u;
+          kpar ^= 1u;
         }
       }
       // Let every completion the leader multicasts to this CTA land before
@@ -345,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t t_lane = (uint32_t)(q * 32) << 16;
-    const uint32_t epi_buf = base + L::OFF_EPI + (uint32_t)q * 8192u;
+    const uint32_t epi_buf = base + L::OFF_EPI + (uint32_t)q * 4096u;
     int tile_count = 0;
     TileIter it;
     for (it.init(p.sched, pair); it.valid(); it.next(), ++tile_count) {
@@ -410,9 +418,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       ahead.advance(p, pc, (int)crank, nk);
     };
     for (int j = 0; j < PRE; ++j) prefetch((uint32_t)j);
-    int stage = gr;  // the group's K-blocks use every other stage of the ring
-    uint32_t phase = 0;
-    if (stage >= STAGES) stage -= STAGES, phase ^= 1u;
+    // running K-block index of this group (gr, gr + 2, ...): its TMA stage
+    // is gk % S; the group visits a stage every RAW_PERIOD K-blocks, so its
+    // raw barrier's phase is (gk / RAW_PERIOD) & 1
+    constexpr int RAW_PERIOD = (STAGES % 2) ? 2 * STAGES : STAGES;
+    int gk = gr;
     int wslot = gr;  // and every other slot of the W ring
     uint32_t wphase = 0;
     int wuses[WST / 2];  // uses of the group's W slots gr, gr + 2, ...
@@ -420,6 +430,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     uint32_t slot = 0;
     while (cur.valid()) {
       const int kb = cur.kb;
+      const int stage = gk % STAGES;
+      const uint32_t rphase = (uint32_t)(gk / RAW_PERIOD) & 1u;
+      const uint32_t rbar = bar_raw + 16 * stage + 8 * gr;
       cp_async_wait<PRE - 1>();  // this K-block's absmax has landed
       float amax = 0.0f;
       if (kb < nk && cur.in) {
@@ -434,22 +447,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       ++wuses[wslot >> 1];
       if (kb >= nk && (warp & 3) == 2 && lane == 0) {
         // rank K-block e: this CTA's half of B [n, r] (K-major) or of A [rl, k]
-        // (MN-major) into the W slot
+        // (MN-major) into the W slot, counted on the group's raw barrier of
+        // the stage (armed by the producer)
         const int e = kb - nk;
         const int nt = cur.it.nt();
         const GemmGroup &G = p.grp[group_of(p, nt)];
         const GemmGroup &R = DX ? p.grp[0] : G;
         const int nh = (nt - G.tile_begin) * BN + (int)crank * 128;
         const uint32_t sw = base + L::OFF_WRING + wslot * L::W_BYTES;
-        const uint32_t rb = bar_raw + 8 * stage;
         if constexpr (DX) {
-          tma_load_2d(sw, &R.tm_b, rb, nh, e * kBK);
-          tma_load_2d(sw + 8192, &R.tm_b, rb, nh + 64, e * kBK);
+          tma_load_2d(sw, &R.tm_b, rbar, nh, e * kBK);
+          tma_load_2d(sw + 8192, &R.tm_b, rbar, nh + 64, e * kBK);
         } else {
-          tma_load_2d(sw, &R.tm_b, rb, e * kBK, nh);
+          tma_load_2d(sw, &R.tm_b, rbar, e * kBK, nh);
         }
       }
-      if (!warp_wait(bar_raw + 8 * stage, phase, abort_flag, p.status)) break;
+      // this K-block's codes (or rank tile) landed
+      if (!warp_wait(rbar, rphase, abort_flag, p.status)) break;
       if (kb < nk) {
         const Nf4Table tab = nf4_table(lvl, amax);
         const uint32_t sx = base + stage * L::STAGE_BYTES;
@@ -468,8 +482,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(lead_wfull + 8 * wslot);
       // next K-block of this group: two stages (and W slots) on
-      stage += 2;
-      if (stage >= STAGES) stage -= STAGES, phase ^= 1u;
+      gk += 2;
       wslot += 2;
       if (wslot >= WST) wslot -= WST, wphase ^= 1u;
       cur.advance(p, pc, (int)crank, nk);

@@ -180,10 +180,11 @@ LORA_DEV void epi_store_tile(uint32_t t_acc, __nv_bfloat16 *orow, bool row_ok, i
 
 // Output epilogue through shared memory and TMA for one warp (32 rows of
 // the CTA's 128): per 32-column chunk, TMEM -> (RoPE) -> bf16 into one of
-// four 2 KB staging buffers [32 rows x 64 bytes, 64-byte swizzle, the layout
+// two 2 KB staging buffers [32 rows x 64 bytes, 64-byte swizzle, the layout
 // the output tensor map names], then lane 0 stores the chunk with one bulk
 // tensor copy (whole lines, clipped at the tensor's extent).  `buf` is the
-// warp's staging area; `cs` the cos/sin row of this lane's output row.
+// warp's staging area; `cs` the cos/sin row of this lane's output row.  The
+// epilogue of a tile overlaps the next tile's K loop, so two buffers do.
 template <int BN, bool ROPE>
 LORA_DEV void epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap *tm_out,
                                  int col0, int row0, int ncols, const float *cs, int lane) {
@@ -198,8 +199,8 @@ LORA_DEV void epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap
       tmem_ld32(t_acc + c * 32, r);
       tmem_ld_wait();
       if (c * 32 >= ncols) continue;
-      const uint32_t b = buf + (uint32_t)(c & 3) * 2048u;
-      if (lane == 0) bulk_wait_read<3>();  // buffer (c & 3) no longer read by an older copy
+      const uint32_t b = buf + (uint32_t)(c & 1) * 2048u;
+      if (lane == 0) bulk_wait_read<1>();  // buffer (c & 1) no longer read by an older copy
       __syncwarp();
 #pragma unroll
       for (int q = 0; q < 4; ++q)
@@ -215,20 +216,19 @@ LORA_DEV void epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap
       }
     }
   } else {
-    int pair = 0;
 #pragma unroll 1
     for (int h = 0; h < BN / 128; ++h) {
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half, ++pair) {
+      for (int half = 0; half < 2; ++half) {
         const int c0 = h * 128 + half * 32;
         uint32_t ra[32], rb[32];
         tmem_ld32(t_acc + c0, ra);
         tmem_ld32(t_acc + c0 + 64, rb);
         tmem_ld_wait();
         if (c0 >= ncols) continue;
-        const uint32_t ba = buf + (uint32_t)(pair & 1) * 4096u;
-        const uint32_t bb = ba + 2048u;
-        if (lane == 0) bulk_wait_read<1>();  // this pair of buffers is free again
+        const uint32_t ba = buf;
+        const uint32_t bb = buf + 2048u;
+        if (lane == 0) bulk_wait_read<0>();  // both buffers are free again
         __syncwarp();
         const float4 *cp = reinterpret_cast<const float4 *>(cs + half * 32);
         const float4 *sp = reinterpret_cast<const float4 *>(cs + 64 + half * 32);

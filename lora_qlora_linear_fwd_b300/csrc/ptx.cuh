@@ -264,15 +264,12 @@ LORA_DEV uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
 // after shared-memory writes that the arriving CTA's own SM will read
 // through the async proxy (a pair MMA reads each CTA's operand half from
 // that CTA's shared memory).  The writers have already executed
-// fence.proxy.async; a CTA-scope release fence then orders those writes
-// before the arrive, which itself is relaxed at cluster scope.  Used on
-// every pipeline stage: a cluster-scope release arrive costs about as much
-// as the stage's work.
+// fence.proxy.async; the arrive has the default semantics of
+// mbarrier.arrive (release at CTA scope), which orders those writes before
+// it.  Used on every pipeline stage: a cluster-scope release arrive costs
+// about as much as the stage's work.
 LORA_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile(
-      "fence.acq_rel.cta;\n\t"
-      "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-      : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // Arrive on an mbarrier that may live in the peer CTA (cluster address).
 LORA_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {

@@ -59,7 +59,7 @@ struct PairSmem {
   static constexpr int OFF_W = X_BYTES;      // bf16: W inside the stage
   static constexpr int OFF_C = X_BYTES;      // NF4: codes inside the stage
   static constexpr int STAGE_BYTES = X_BYTES + (NF4 ? C_BYTES : W_BYTES);
-  static constexpr int W_STAGES = NF4 ? 4 : 0;
+  static constexpr int W_STAGES = NF4 ? 6 : 0;
   static constexpr int WRING_BYTES = W_STAGES * W_BYTES;
   static constexpr int EPI_BYTES = 4 * 2 * 2048;  // per epilogue warp: two 2 KB staging buffers
   static constexpr int AMAX_PRE = NF4 ? 4 : 0;    // absmax prefetch distance (a group's K-blocks)

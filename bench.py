@@ -494,6 +494,55 @@ def run_reference(args, world, rank):
     }
 
 
+# ------------------------------------------------- standalone nf4_dequant
+NF4_DEQUANT_SHAPES = [  # W [n, k] of the Llama-3-8B and Qwen1.5-32B QLoRA projections
+    (4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336),
+    (5120, 5120), (1024, 5120), (27392, 5120), (5120, 27392)]
+
+
+def run_nf4_dequant(args):
+    """HBM throughput of ``nf4_dequant`` on the QLoRA weight shapes: bytes =
+    codes n·k/2 + absmax n·k/32 + bf16 output 2·n·k, CUDA-event time per call
+    with a 512 MiB L2 flush between calls (outside the events)."""
+    import lora_qlora_linear_fwd_b300 as L
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peak = measured_peaks()["hbm_gbs"]
+    g = torch.Generator(device="cpu").manual_seed(0)
+    rows = []
+    for n, k in NF4_DEQUANT_SHAPES:
+        W = (torch.randn(n, k, generator=g) / math.sqrt(k)).to(torch.bfloat16).to(dev)
+        codes = torch.empty(n, k // 2, dtype=torch.uint8, device=dev)
+        absmax = torch.empty(n, k // 64, dtype=torch.bfloat16, device=dev)
+        L.nf4_quantize(W, codes, absmax)
+        out = torch.empty(n, k, dtype=torch.bfloat16, device=dev)
+        del W
+        for _ in range(args.warmup):
+            L.nf4_dequant(codes, absmax, out)
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            L.nf4_dequant(codes, absmax, out)
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        t = statistics.median(ts)
+        nbytes = n * k // 2 + n * k // 32 + 2 * n * k
+        gbs = nbytes / (t * 1e-3) / 1e9
+        rows.append({"n": n, "k": k, "us": round(t * 1e3, 2), "GBps": round(gbs, 1),
+                     "frac_hbm": round(gbs / peak, 3)})
+        del codes, absmax, out
+    return {"component": "nf4_dequant", "unit": "GB/s", "peak_hbm_gbs": peak,
+            "peak_source": measured_peaks()["source"], "steps": args.steps,
+            "warmup": args.warmup, "l2": "flushed between calls (512 MiB write, outside events)",
+            "data": "synthetic: NF4 codes of W ~ N(0, 1/k) quantised by nf4_quantize",
+            "shapes": rows}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -504,9 +553,15 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=128,
                     help="token sample for the oracle timing (CPU baseline / reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--component", default="step", choices=["step", "nf4_dequant"],
+                    help="step: the fwd+bwd step (default); nf4_dequant: the standalone "
+                         "dequantisation on the QLoRA weight shapes (1 GPU)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.component == "nf4_dequant":
+        print(json.dumps(run_nf4_dequant(args)), flush=True)
+        return 0
     world, rank, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, world, rank)

@@ -51,7 +51,7 @@ constexpr int pair_threads(bool nf4) { return nf4 ? 448 : 192; }
 // number of slots (each slot belongs to one group), and the code-landing
 // barrier of a TMA stage is split in two, one per group, armed by the
 // producer for the group of the K-block.
-template <bool NF4>
+template <bool NF4, bool STAGED_ROPE = false>
 struct PairSmem {
   static constexpr int X_BYTES = 128 * 128;  // own 128 rows x 64 K
   static constexpr int W_BYTES = 128 * 128;  // own 128 N-rows x 64 K
@@ -64,16 +64,19 @@ struct PairSmem {
   static constexpr int EPI_BYTES = 4 * 2 * 2048;  // per epilogue warp: two 2 KB staging buffers
   static constexpr int AMAX_PRE = NF4 ? 4 : 0;    // absmax prefetch distance (a group's K-blocks)
   static constexpr int AMAX_BYTES = AMAX_PRE * 256 * 4;  // per decode thread
+  // RoPE with staged cos / sin: per epilogue warp 32 rows of one half
+  static constexpr int CS_BYTES = STAGED_ROPE ? 4 * 32 * kRopeRowPitch : 0;
   static constexpr int MISC_BYTES = 1024;
-  static constexpr int FIXED = WRING_BYTES + EPI_BYTES + AMAX_BYTES + MISC_BYTES + 1024;
+  static constexpr int FIXED = WRING_BYTES + EPI_BYTES + AMAX_BYTES + CS_BYTES + MISC_BYTES + 1024;
   static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int OFF_WRING = STAGES * STAGE_BYTES;
   static constexpr int OFF_EPI = OFF_WRING + WRING_BYTES;
   static constexpr int OFF_AMAX = OFF_EPI + EPI_BYTES;
-  static constexpr int OFF_MISC = OFF_AMAX + AMAX_BYTES;
+  static constexpr int OFF_CS = OFF_AMAX + AMAX_BYTES;
+  static constexpr int OFF_MISC = OFF_CS + CS_BYTES;
   static constexpr int TOTAL = OFF_MISC + MISC_BYTES + 1024;
-  static constexpr int NUM_BARS = 4 * STAGES + 2 * W_STAGES + 5;
+  static constexpr int NUM_BARS = 4 * STAGES + 2 * W_STAGES + 5 + (STAGED_ROPE ? 4 : 0);
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 3 && (!NF4 || W_STAGES >= 4), "pipeline depth");
   static_assert(!NF4 || W_STAGES % 2 == 0, "one decode group per W slot");
@@ -138,7 +141,9 @@ struct Nf4Cursor {
 template <int MODE, bool NF4, bool ROPE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1)
     lora_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
-  using L = PairSmem<NF4>;
+  // RoPE cos / sin staged in shared memory (bf16 W; the NF4 rings leave no room)
+  constexpr bool STAGED = ROPE && !NF4;
+  using L = PairSmem<NF4, STAGED>;
   constexpr int STAGES = L::STAGES;
   constexpr int BN = 256;
   constexpr bool DX = MODE == kModeDx;
@@ -166,6 +171,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   const uint32_t bar_acc_full = bar_wempty + 8 * WST; // [2] both: accumulator b ready
   const uint32_t bar_acc_empty = bar_acc_full + 16;   // [2] leader: 8 warps drained b
   const uint32_t bar_drain = bar_acc_empty + 16;      // leader
+  const uint32_t bar_cs = bar_drain + 8;              // [4] STAGED: cos / sin of epilogue warp q
   const int misc_words = (8 * L::NUM_BARS) / 4;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC) + misc_words;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -186,6 +192,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     mbar_init(bar_acc_empty, 8);
     mbar_init(bar_acc_empty + 8, 8);
     mbar_init(bar_drain, 1);
+    if constexpr (STAGED)
+      for (int q = 0; q < 4; ++q) mbar_init(bar_cs + 8 * q, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -354,6 +362,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     const int row = q * 32 + lane;
     const uint32_t t_lane = (uint32_t)(q * 32) << 16;
     const uint32_t epi_buf = base + L::OFF_EPI + (uint32_t)q * 4096u;
+    const uint32_t cs_bar = bar_cs + 8 * q;
+    const uint32_t srow = base + L::OFF_CS + (uint32_t)row * kRopeRowPitch;
+    uint32_t cs_phase = 0;
+    bool cs_pending = false;  // a staged half has not been waited for
     int tile_count = 0;
     TileIter it;
     for (it.init(p.sched, pair); it.valid(); it.next(), ++tile_count) {
@@ -363,21 +375,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       const int grow = m * 256 + (int)crank * 128 + row;
       const bool row_ok = grow < p.M;
       const int buf = tile_count & 1;
+      const float *cs = ROPE ? rope_row(p, grow, row_ok) : nullptr;
+      if constexpr (STAGED) {  // fetched while the accumulator is still being produced
+        rope_stage(cs, 0, srow, cs_bar, lane);
+        cs_pending = true;
+      }
       if (!warp_wait(bar_acc_full + 8 * buf, (tile_count >> 1) & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const int ncols = min(BN, G.ncols - n0);
-      const float *cs = ROPE ? rope_row(p, grow, row_ok) : nullptr;
       if (DX && p.accumulate) {  // read-modify-write of dX: plain loads and stores
         __nv_bfloat16 *orow = G.out + (size_t)(row_ok ? grow : 0) * G.ncols + n0;
         epi_store_tile<BN, false>(tmem + t_lane + buf * BN, orow, row_ok, ncols, true, nullptr);
       } else {
-        epi_store_tile_tma<BN, ROPE>(tmem + t_lane + buf * BN, epi_buf, &G.tm_out, n0,
-                                     m * 256 + (int)crank * 128 + q * 32, ncols, cs, lane);
+        if (!epi_store_tile_tma<BN, ROPE, STAGED>(tmem + t_lane + buf * BN, epi_buf, &G.tm_out, n0,
+                                                  m * 256 + (int)crank * 128 + q * 32, ncols, cs,
+                                                  srow, cs_bar, cs_phase, lane, abort_flag,
+                                                  p.status))
+          break;
+        cs_pending = false;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lead_acc_empty + 8 * buf);
     }
+    if (STAGED && cs_pending)  // no copy may land after the CTA exits
+      mbar_wait_quiet(cs_bar, cs_phase, 100000000ull);
     if (lane == 0) bulk_wait_all();  // every output store has completed
     __syncwarp();
   } else if constexpr (NF4) {
@@ -509,7 +531,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
 
 template <int MODE, bool NF4, bool ROPE>
 static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t st) {
-  using L = PairSmem<NF4>;
+  using L = PairSmem<NF4, ROPE && !NF4>;
   auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -522,7 +544,7 @@ static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t 
 
 template <int MODE, bool NF4, bool ROPE>
 static int pair_capacity() {
-  using L = PairSmem<NF4>;
+  using L = PairSmem<NF4, ROPE && !NF4>;
   auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE>;
   static int cached = -1;
   if (cached < 0) {

@@ -178,6 +178,39 @@ LORA_DEV void epi_store_tile(uint32_t t_acc, __nv_bfloat16 *orow, bool row_ok, i
   }
 }
 
+// cos / sin of one half (32 rotation pairs) of a cache row, in registers.
+struct RopeHalf {
+  float4 c[8], s[8];
+  // from a staged row [32 cos | 32 sin]
+  LORA_DEV void load_shared(uint32_t srow) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 a = ld_shared_v4(srow + 16 * i), b = ld_shared_v4(srow + 128 + 16 * i);
+      c[i] = make_float4(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
+                         __uint_as_float(a.w));
+      s[i] = make_float4(__uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z),
+                         __uint_as_float(b.w));
+    }
+  }
+};
+
+// Row pitch of a staged cos / sin half: 256 bytes of data plus 16 of padding,
+// so that 32 lanes reading 16 bytes each of their own rows fall on distinct
+// bank quads (four wavefronts, the minimum for 512 bytes).
+constexpr int kRopeRowPitch = 272;
+
+// Stages half `half` of this lane's cache row `cs` (32 cos, then 32 sin
+// values) into its shared-memory row `srow` with two bulk copies, which the
+// copy engine rather than the load/store pipe carries (the 32 lanes of a
+// warp read 32 different rows: as plain loads each instruction would touch
+// 32 cache lines).  Lane 0 arms the warp's barrier for all 32 rows.
+LORA_DEV void rope_stage(const float *cs, int half, uint32_t srow, uint32_t bar, int lane) {
+  if (lane == 0) mbar_arrive_expect_tx(bar, 32 * 256);
+  fence_proxy_async_smem();  // this lane's reads of its row precede the overwrite
+  bulk_load(srow, cs + half * 32, 128, bar);
+  bulk_load(srow + 128, cs + 64 + half * 32, 128, bar);
+}
+
 // Output epilogue through shared memory and TMA for one warp (32 rows of
 // the CTA's 128): per 32-column chunk, TMEM -> (RoPE) -> bf16 into one of
 // two 2 KB staging buffers [32 rows x 64 bytes, 64-byte swizzle, the layout
@@ -185,9 +218,18 @@ LORA_DEV void epi_store_tile(uint32_t t_acc, __nv_bfloat16 *orow, bool row_ok, i
 // tensor copy (whole lines, clipped at the tensor's extent).  `buf` is the
 // warp's staging area; `cs` the cos/sin row of this lane's output row.  The
 // epilogue of a tile overlaps the next tile's K loop, so two buffers do.
-template <int BN, bool ROPE>
-LORA_DEV void epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap *tm_out,
-                                 int col0, int row0, int ncols, const float *cs, int lane) {
+// RoPE takes the row's cos / sin one half (32 rotation pairs) at a time,
+// both heads of the tile per half.  STAGED: the halves come from the lane's
+// shared-memory row `srow`, filled by rope_stage() on barrier `cs_bar` (the
+// caller stages half 0 before the accumulator is ready; half 1 is staged
+// here as soon as half 0 sits in registers).  Otherwise each 32-column
+// chunk reads its cos / sin from the cache directly.  Returns false when a
+// wait gave up.
+template <int BN, bool ROPE, bool STAGED>
+LORA_DEV bool epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap *tm_out,
+                                 int col0, int row0, int ncols, const float *cs, uint32_t srow,
+                                 uint32_t cs_bar, uint32_t &cs_phase, int lane,
+                                 volatile int *abort_flag, uint32_t *status) {
   // byte offset of 16-byte chunk q of this lane's row in a staging buffer
   auto at = [&](int q) -> uint32_t {
     return (uint32_t)(lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4));
@@ -215,7 +257,9 @@ LORA_DEV void epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap
         bulk_commit();
       }
     }
-  } else {
+  } else if constexpr (!STAGED) {
+    // cos / sin straight from the cache (the register budget of the NF4
+    // kernel holds one 32-column chunk of them at a time)
 #pragma unroll 1
     for (int h = 0; h < BN / 128; ++h) {
 #pragma unroll 1
@@ -260,7 +304,56 @@ LORA_DEV void epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap
         }
       }
     }
+  } else {
+    RopeHalf v;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      if (!warp_wait(cs_bar, cs_phase, abort_flag, status)) return false;
+      cs_phase ^= 1u;
+      v.load_shared(srow);
+      if (half == 0) rope_stage(cs, 1, srow, cs_bar, lane);  // the row is in registers now
+#pragma unroll 1
+      for (int h = 0; h < BN / 128; ++h) {
+        const int c0 = h * 128 + half * 32;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(t_acc + c0, ra);
+        tmem_ld32(t_acc + c0 + 64, rb);
+        tmem_ld_wait();
+        if (c0 >= ncols) continue;
+        const uint32_t ba = buf;
+        const uint32_t bb = buf + 2048u;
+        if (lane == 0) bulk_wait_read<0>();  // both buffers are free again
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float co[8] = {v.c[2 * q].x,     v.c[2 * q].y,     v.c[2 * q].z,     v.c[2 * q].w,
+                               v.c[2 * q + 1].x, v.c[2 * q + 1].y, v.c[2 * q + 1].z, v.c[2 * q + 1].w};
+          const float si[8] = {v.s[2 * q].x,     v.s[2 * q].y,     v.s[2 * q].z,     v.s[2 * q].w,
+                               v.s[2 * q + 1].x, v.s[2 * q + 1].y, v.s[2 * q + 1].z, v.s[2 * q + 1].w};
+          float oa[8], ob[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float a = __uint_as_float(ra[8 * q + e]);
+            const float bv = __uint_as_float(rb[8 * q + e]);
+            oa[e] = a * co[e] - bv * si[e];
+            ob[e] = bv * co[e] + a * si[e];
+          }
+          st_shared_v4(ba + at(q), pack_bf16x2(oa[0], oa[1]), pack_bf16x2(oa[2], oa[3]),
+                       pack_bf16x2(oa[4], oa[5]), pack_bf16x2(oa[6], oa[7]));
+          st_shared_v4(bb + at(q), pack_bf16x2(ob[0], ob[1]), pack_bf16x2(ob[2], ob[3]),
+                       pack_bf16x2(ob[4], ob[5]), pack_bf16x2(ob[6], ob[7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(tm_out, ba, col0 + c0, row0);
+          tma_store_2d(tm_out, bb, col0 + c0 + 64, row0);
+          bulk_commit();
+        }
+      }
+    }
   }
+  return true;
 }
 
 // Position of output row `grow` for the RoPE epilogue; an out-of-range

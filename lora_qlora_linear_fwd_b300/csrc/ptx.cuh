@@ -105,6 +105,17 @@ LORA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, in
       : "memory");
 }
 
+// Contiguous bulk copy global -> shared (the issuing thread's own CTA),
+// completing `bar`'s transaction count.  dst, src and bytes are multiples
+// of 16.
+LORA_DEV void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tensor core operand reads, TMA).
 LORA_DEV void fence_proxy_async_smem() {

@@ -16,9 +16,10 @@
 // half of the W bytes a one-SM 128 x 256 tile would need.
 //
 // Roles (both CTAs unless noted; NF4 rings as in PairSmem):
-//   warp 0     TMA producer: own halves of x/dY and of W (or NF4 codes) per
-//              main K-block; own halves of s·v / s·u and of B / A per rank
-//              K-block.  Completion is counted on the even CTA's barriers.
+//   warp 0     TMA producer: own halves of x/dY and (bf16) of W per main
+//              K-block; own halves of s·v / s·u and (bf16) of B / A per
+//              rank K-block.  Completion is counted on the even CTA's
+//              barriers.
 //   warp 1     TMEM owner (pair allocation, 2 x 256 columns); in the even
 //              CTA also the single MMA issuer, whose commits are multicast
 //              to both CTAs.  Accumulators alternate between the two
@@ -33,33 +34,38 @@
 //              §显存优化策略: NF4 base weight).  Two groups of four warps take
 //              alternate K-blocks, one thread per 64-element row piece, so
 //              each group has two stage times per K-block it decodes.
+//   warp 14    NF4 only: TMA producer of the CTA's own code bytes, into a
+//              ring of its own that runs ahead of the x ring.
 #include "gemm_common.cuh"
 
 namespace lora {
 
-// Threads per CTA: producer, MMA, 4 epilogue warps (+ 8 NF4 decode warps).
-constexpr int pair_threads(bool nf4) { return nf4 ? 448 : 192; }
+// Threads per CTA: producer, MMA, 4 epilogue warps (+ 8 NF4 decode warps
+// and the NF4 code producer).
+constexpr int pair_threads(bool nf4) { return nf4 ? 480 : 192; }
+constexpr int kNf4DecodeWarps = 8;
 
 // Shared-memory layout.  bf16 W: each pipeline stage holds the x tile and
-// the W tile.  NF4 W: the TMA ring holds the x tile and the code bytes, and
-// the decoded W tiles have a ring of their own (decoding sits between the
-// copy landing and the MMA, so the copies need the deeper ring); a rank
-// K-block's B or A tile is copied straight into the W ring.  The two NF4
-// decode groups take alternate K-blocks.  A parity wait is only
+// the W tile.  NF4 W: three rings.  The x ring (released by the MMA) holds
+// the activation tiles; the code ring holds the 4-bit codes of the CTA's W
+// half and is released by the decoders as soon as they have read a slot, so
+// that the codes run well ahead of the MMA (decoding sits between their
+// landing and the MMA); the decoded W tiles have a ring of their own.  A
+// rank K-block's B or A tile is copied straight into the W ring.  The two
+// NF4 decode groups take alternate K-blocks.  A parity wait is only
 // unambiguous for a waiter at most one phase ahead of the barrier, so each
-// waiter must see every phase of its barrier: the W ring has an even
-// number of slots (each slot belongs to one group), and the code-landing
-// barrier of a TMA stage is split in two, one per group, armed by the
-// producer for the group of the K-block.
+// waiter must see every phase of its barrier: the code and W rings have an
+// even number of slots, so that each slot belongs to one group.
 template <bool NF4, bool STAGED_ROPE = false>
 struct PairSmem {
   static constexpr int X_BYTES = 128 * 128;  // own 128 rows x 64 K
   static constexpr int W_BYTES = 128 * 128;  // own 128 N-rows x 64 K
-  static constexpr int C_BYTES = NF4 ? 128 * 32 : 0;
+  static constexpr int C_BYTES = NF4 ? 128 * 32 : 0;  // own half of a K-block's codes
   static constexpr int OFF_W = X_BYTES;      // bf16: W inside the stage
-  static constexpr int OFF_C = X_BYTES;      // NF4: codes inside the stage
-  static constexpr int STAGE_BYTES = X_BYTES + (NF4 ? C_BYTES : W_BYTES);
+  static constexpr int STAGE_BYTES = X_BYTES + (NF4 ? 0 : W_BYTES);
+  static constexpr int C_STAGES = NF4 ? 4 : 0;
   static constexpr int W_STAGES = NF4 ? 6 : 0;
+  static constexpr int CRING_BYTES = C_STAGES * C_BYTES;
   static constexpr int WRING_BYTES = W_STAGES * W_BYTES;
   static constexpr int EPI_BYTES = 4 * 2 * 2048;  // per epilogue warp: two 2 KB staging buffers
   static constexpr int AMAX_PRE = NF4 ? 4 : 0;    // absmax prefetch distance (a group's K-blocks)
@@ -67,26 +73,29 @@ struct PairSmem {
   // RoPE with staged cos / sin: per epilogue warp 32 rows of one half
   static constexpr int CS_BYTES = STAGED_ROPE ? 4 * 32 * kRopeRowPitch : 0;
   static constexpr int MISC_BYTES = 1024;
-  static constexpr int FIXED = WRING_BYTES + EPI_BYTES + AMAX_BYTES + CS_BYTES + MISC_BYTES + 1024;
+  static constexpr int FIXED =
+      WRING_BYTES + CRING_BYTES + EPI_BYTES + AMAX_BYTES + CS_BYTES + MISC_BYTES + 1024;
   static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int OFF_WRING = STAGES * STAGE_BYTES;
-  static constexpr int OFF_EPI = OFF_WRING + WRING_BYTES;
+  static constexpr int OFF_CRING = OFF_WRING + WRING_BYTES;
+  static constexpr int OFF_EPI = OFF_CRING + CRING_BYTES;
   static constexpr int OFF_AMAX = OFF_EPI + EPI_BYTES;
   static constexpr int OFF_CS = OFF_AMAX + AMAX_BYTES;
   static constexpr int OFF_MISC = OFF_CS + CS_BYTES;
   static constexpr int TOTAL = OFF_MISC + MISC_BYTES + 1024;
-  static constexpr int NUM_BARS = 4 * STAGES + 2 * W_STAGES + 5 + (STAGED_ROPE ? 4 : 0);
+  static constexpr int NUM_BARS =
+      2 * STAGES + 2 * C_STAGES + 2 * W_STAGES + 5 + (STAGED_ROPE ? 4 : 0);
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-  static_assert(STAGES >= 3 && (!NF4 || W_STAGES >= 4), "pipeline depth");
-  static_assert(!NF4 || W_STAGES % 2 == 0, "one decode group per W slot");
+  static_assert(STAGES >= 3 && (!NF4 || (W_STAGES >= 4 && C_STAGES >= 4)), "pipeline depth");
+  static_assert(!NF4 || (W_STAGES % 2 == 0 && C_STAGES % 2 == 0), "one decode group per slot");
   static_assert(8 * NUM_BARS + 16 <= MISC_BYTES, "barriers fit");
   static_assert(TOTAL <= kSmemLimit, "shared memory budget");
 };
 
 // Walk of one NF4 decode thread over its absmax elements, K-block by
 // K-block, across the tiles of its CTA pair (FWD: row nh + pc, column kb;
-// DX: row kb·64 + pc % 64 of the K-group's W, column nh/64 + pc/64).
+// DX: row kb·64 + pc/2 of the K-group's W, column nh/64 + pc%2).
 template <bool DX>
 struct Nf4Cursor {
   TileIter it;
@@ -103,11 +112,11 @@ struct Nf4Cursor {
     len = nk + (DX ? p.grp[0].n_extra : G.n_extra);
     if constexpr (DX) {
       const int ld = p.grp[0].ld_absmax;
-      const int kblk = (nh >> 6) + (pc >> 6);
+      const int kblk = (nh >> 6) + (pc & 1);
       in = kblk < ld;
       step = 64ll * ld;
-      e = p.grp[0].absmax + (long long)(pc & 63) * ld + kblk;
-      p1 = p.kgroups > 1 ? p.grp[1].absmax + (long long)(pc & 63) * ld + kblk : e;
+      e = p.grp[0].absmax + (long long)(pc >> 1) * ld + kblk;
+      p1 = p.kgroups > 1 ? p.grp[1].absmax + (long long)(pc >> 1) * ld + kblk : e;
       split = p.kgroups > 1 ? p.ksplit : nk;
     } else {
       const int wrow = nh + pc;
@@ -147,7 +156,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   constexpr int STAGES = L::STAGES;
   constexpr int BN = 256;
   constexpr bool DX = MODE == kModeDx;
-  constexpr int NUM_DEC_WARPS = (pair_threads(NF4) - 192) / 32;
+  constexpr int NUM_DEC_WARPS = kNf4DecodeWarps;
   constexpr uint16_t kBoth = 0x3;
 
   extern __shared__ uint8_t smem_raw[];
@@ -162,11 +171,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   const int pair = blockIdx.x >> 1;
 
   constexpr int WST = L::W_STAGES;
+  constexpr int CST = L::C_STAGES;
   const uint32_t bar_full = base + L::OFF_MISC;       // [S] leader: TMA of both CTAs
   const uint32_t bar_empty = bar_full + 8 * STAGES;   // [S] both: pair MMA done
-  const uint32_t bar_raw = bar_empty + 8 * STAGES;    // [S][2] both: own NF4 codes (or B) landed,
-                                                      //   one barrier per decode group
-  const uint32_t bar_wfull = bar_raw + 16 * STAGES;   // [WST] leader: W slot of both CTAs ready
+  const uint32_t bar_cfull = bar_empty + 8 * STAGES;  // [CST] both: own NF4 codes (or B) landed
+  const uint32_t bar_cempty = bar_cfull + 8 * CST;    // [CST] both: the decode group read the slot
+  const uint32_t bar_wfull = bar_cempty + 8 * CST;    // [WST] leader: W slot of both CTAs ready
   const uint32_t bar_wempty = bar_wfull + 8 * WST;    // [WST] both: pair MMA done with W slot
   const uint32_t bar_acc_full = bar_wempty + 8 * WST; // [2] both: accumulator b ready
   const uint32_t bar_acc_empty = bar_acc_full + 16;   // [2] leader: 8 warps drained b
@@ -180,8 +190,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
-      mbar_init(bar_raw + 16 * s, 1);
-      mbar_init(bar_raw + 16 * s + 8, 1);
+    }
+    for (int c = 0; c < CST; ++c) {
+      mbar_init(bar_cfull + 8 * c, 1);
+      mbar_init(bar_cempty + 8 * c, NUM_DEC_WARPS / 2);  // the four warps of one group
     }
     for (int w = 0; w < WST; ++w) {
       mbar_init(bar_wfull + 8 * w, NUM_DEC_WARPS);  // one decode group in each of 2 CTAs
@@ -220,9 +232,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       tma_prefetch_desc(&p.tm_sv);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t kpar = 0;  // parity of the running K-block index: its decode group
-      int fills[STAGES];
-      for (int s = 0; s < STAGES; ++s) fills[s] = 0;
+      int issued = 0;  // K-blocks issued: stage s took every STAGES-th from the s-th
       bool ok = true;
       TileIter it;
       for (it.init(p.sched, pair); ok && it.valid(); it.next()) {
@@ -248,14 +258,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
             const int gk = (DX && p.kgroups > 1 && kb >= p.ksplit) ? 1 : 0;
             const CUtensorMap *tw = DX ? &p.grp[gk].tm_w : &G.tm_w;
             const int wk = kb - (gk ? p.ksplit : 0);
-            if constexpr (NF4) {
-              const uint32_t rb = bar_raw + 16 * stage + 8 * kpar;
-              mbar_arrive_expect_tx(rb, L::C_BYTES);
-              if constexpr (DX)  // codes [64 rows of W, 64 bytes = 128 k-columns]
-                tma_load_2d(sx + L::OFF_C, tw, rb, nh / 2, wk * kBK);
-              else               // codes [128 rows of W, 32 bytes]
-                tma_load_2d(sx + L::OFF_C, tw, rb, kb * (kBK / 2), nh);
-            } else {
+            if constexpr (!NF4) {
               if constexpr (DX) {  // W as MN-major operand: 2 boxes [64 rows x 64]
                 tma_load_2d_pair(sx + L::OFF_W, tw, fb, nh, wk * kBK);
                 tma_load_2d_pair(sx + L::OFF_W + 8192, tw, fb, nh + 64, wk * kBK);
@@ -268,12 +271,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
             const int e = kb - nk;
             const GemmGroup &R = DX ? p.grp[0] : G;
             if constexpr (NF4) {
-              // B / A goes straight into the W ring: the decode group that
-              // owns the slot copies it once the slot is free; its landing is
-              // counted on this stage's raw barrier, armed here
+              // B / A goes straight into the W ring (copied by the decode
+              // group that owns the slot, see the code producer)
               if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * L::X_BYTES);
               tma_load_2d_pair(sx, &p.tm_sv, fb, R.sv_col + e * kBK, row0);
-              mbar_arrive_expect_tx(bar_raw + 16 * stage + 8 * kpar, L::W_BYTES);
             } else {
               if (leader)
                 mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (L::X_BYTES + L::W_BYTES));
@@ -286,16 +287,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
               }
             }
           }
-          ++fills[stage];
+          ++issued;
           if (++stage == STAGES) stage = 0, phase ^= 1u;
-          kpar ^= 1u;
         }
       }
       // Let every completion the leader multicasts to this CTA land before
       // the CTA may exit (bounded: after an abort some never come).
       const uint64_t lim = *abort_flag ? 20000000ull : 1000000000ull;
-      for (int s = 0; s < STAGES; ++s)
-        if (fills[s] > 0) mbar_wait_quiet(bar_empty + 8 * s, (uint32_t)((fills[s] - 1) & 1), lim);
+      for (int s = 0; s < STAGES; ++s) {
+        const int fills = issued > s ? (issued - s + STAGES - 1) / STAGES : 0;
+        if (fills > 0) mbar_wait_quiet(bar_empty + 8 * s, (uint32_t)((fills - 1) & 1), lim);
+      }
     }
   } else if (warp == 1) {
     // ===================================================== MMA (even CTA)
@@ -403,22 +405,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     if (lane == 0) bulk_wait_all();  // every output store has completed
     __syncwarp();
   } else if constexpr (NF4) {
+    if (warp < 6 + kNf4DecodeWarps) {
     // ============================================================= NF4 decode
     // Group gr = 0 / 1 (warps 6-9 / 10-13) decodes the K-blocks whose running
     // index across the CTA's tiles is even / odd; thread pc of a group
     // decodes row piece pc:
     // FWD: piece pc = row pc of this CTA's W half [128 rows x 64].
     // DX:  the half is [64 n-rows x 128 k-columns] = two boxes of [64 x 64];
-    //      piece pc = row (pc % 64) of box (pc / 64).
+    //      piece pc = row pc / 2 of box pc % 2 (a warp's pieces are then
+    //      one contiguous kilobyte of the code slot).
+    // The codes of running K-block g sit in code slot g % CST; the group
+    // releases the slot once it has decoded them.
     // A rank K-block's B / A tile is copied into the W slot by one lane of
-    // the group (counted on the stage's raw barrier); the group waits for
+    // the group (counted on the code slot's barrier); the group waits for
     // it and passes the slot on.
     // Decoded tiles go to the W ring (slot g % WST for running K-block g),
     // whose slots the MMA releases through bar_wempty.
     // The absmax of a piece is fetched AMAX_PRE of the group's K-blocks
     // ahead (cp.async into a per-thread shared ring) by a look-ahead cursor:
-    // loaded at decode time it would stall every stage by a memory latency,
-    // since the stage's codes usually land first.
+    // loaded at decode time it would stall every K-block by a memory latency.
     const int dt = threadIdx.x - 192;  // 0..255
     const int gr = dt >> 7, pc = dt & 127;
     constexpr int PRE = L::AMAX_PRE;
@@ -440,21 +445,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       ahead.advance(p, pc, (int)crank, nk);
     };
     for (int j = 0; j < PRE; ++j) prefetch((uint32_t)j);
-    // running K-block index of this group (gr, gr + 2, ...): its TMA stage
-    // is gk % S; the group visits a stage every RAW_PERIOD K-blocks, so its
-    // raw barrier's phase is (gk / RAW_PERIOD) & 1
-    constexpr int RAW_PERIOD = (STAGES % 2) ? 2 * STAGES : STAGES;
-    int gk = gr;
+    // 32-byte code pieces of consecutive threads are contiguous: threads
+    // whose pieces start in the same half of the 32 banks read their two
+    // 16-byte halves in opposite orders, so each load touches every bank
+    const uint32_t flip = (uint32_t)(pc >> 2) & 1u;
+    const uint32_t c_off = DX ? (uint32_t)((pc >> 1) * 64 + (pc & 1) * 32) : (uint32_t)(pc * 32);
+    const uint32_t w_off = DX ? (uint32_t)((pc & 1) * 8192 + (pc >> 1) * 128) : (uint32_t)(pc * 128);
+    int gk = gr;     // running K-block index of this group (gr, gr + 2, ...)
     int wslot = gr;  // and every other slot of the W ring
     uint32_t wphase = 0;
-    int wuses[WST / 2];  // uses of the group's W slots gr, gr + 2, ...
-    for (int j = 0; j < WST / 2; ++j) wuses[j] = 0;
+    int ng = 0;      // K-blocks this group took a W slot for
     uint32_t slot = 0;
     while (cur.valid()) {
       const int kb = cur.kb;
-      const int stage = gk % STAGES;
-      const uint32_t rphase = (uint32_t)(gk / RAW_PERIOD) & 1u;
-      const uint32_t rbar = bar_raw + 16 * stage + 8 * gr;
+      const int cst = gk % CST;
+      const uint32_t cphase = (uint32_t)(gk / CST) & 1u;
+      const uint32_t cbar = bar_cfull + 8 * cst;
       cp_async_wait<PRE - 1>();  // this K-block's absmax has landed
       float amax = 0.0f;
       if (kb < nk && cur.in) {
@@ -466,44 +472,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       if (++slot == (uint32_t)PRE) slot = 0;
       // the W slot is free once the MMA of its previous use has completed
       if (!warp_wait(bar_wempty + 8 * wslot, wphase ^ 1u, abort_flag, p.status)) break;
-      ++wuses[wslot >> 1];
+      ++ng;
+      const uint32_t sw = base + L::OFF_WRING + wslot * L::W_BYTES;
       if (kb >= nk && (warp & 3) == 2 && lane == 0) {
         // rank K-block e: this CTA's half of B [n, r] (K-major) or of A [rl, k]
-        // (MN-major) into the W slot, counted on the group's raw barrier of
-        // the stage (armed by the producer)
+        // (MN-major) into the W slot, counted on the code slot's barrier
+        // (armed by the code producer)
         const int e = kb - nk;
         const int nt = cur.it.nt();
         const GemmGroup &G = p.grp[group_of(p, nt)];
         const GemmGroup &R = DX ? p.grp[0] : G;
         const int nh = (nt - G.tile_begin) * BN + (int)crank * 128;
-        const uint32_t sw = base + L::OFF_WRING + wslot * L::W_BYTES;
         if constexpr (DX) {
-          tma_load_2d(sw, &R.tm_b, rbar, nh, e * kBK);
-          tma_load_2d(sw + 8192, &R.tm_b, rbar, nh + 64, e * kBK);
+          tma_load_2d(sw, &R.tm_b, cbar, nh, e * kBK);
+          tma_load_2d(sw + 8192, &R.tm_b, cbar, nh + 64, e * kBK);
         } else {
-          tma_load_2d(sw, &R.tm_b, rbar, e * kBK, nh);
+          tma_load_2d(sw, &R.tm_b, cbar, e * kBK, nh);
         }
       }
       // this K-block's codes (or rank tile) landed
-      if (!warp_wait(rbar, rphase, abort_flag, p.status)) break;
+      if (!warp_wait(cbar, cphase, abort_flag, p.status)) break;
       if (kb < nk) {
-        const Nf4Table tab = nf4_table(lvl, amax);
-        const uint32_t sx = base + stage * L::STAGE_BYTES;
-        const uint32_t sw = base + L::OFF_WRING + wslot * L::W_BYTES;
-        uint32_t src, dst;
-        if constexpr (DX) {
-          src = sx + L::OFF_C + (pc & 63) * 64 + (pc >> 6) * 32;
-          dst = sw + (pc >> 6) * 8192 + (pc & 63) * 128;
-        } else {
-          src = sx + L::OFF_C + pc * 32;
-          dst = sw + pc * 128;
-        }
-        nf4_decode_row(src, dst, tab);
+        uint32_t words[8];
+        nf4_load_codes(base + L::OFF_CRING + cst * L::C_BYTES + c_off, flip, words);
+        nf4_decode_words(words, sw + w_off, nf4_table(lvl, amax));
         fence_proxy_async_smem();
+        // the slot is released once its codes have been consumed: a release
+        // right after the loads let the next copy overwrite bytes that some
+        // lanes had not read yet
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_cempty + 8 * cst);
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_cempty + 8 * cst);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(lead_wfull + 8 * wslot);
-      // next K-block of this group: two stages (and W slots) on
+      // next K-block of this group: two code and W slots on
       gk += 2;
       wslot += 2;
       if (wslot >= WST) wslot -= WST, wphase ^= 1u;
@@ -512,12 +517,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     }
     cp_async_wait<0>();  // no copy may land after the CTA exits
     // and no release of the group's W slots (multicast by the MMA) may
-    // still be in flight (bounded: after an abort some never come)
+    // still be in flight (bounded: after an abort some never come); the
+    // group's j-th W slot took every (WST/2)-th of its K-blocks from the j-th
     if (lane == 0) {
       const uint64_t lim = *abort_flag ? 20000000ull : 1000000000ull;
-      for (int j = 0; j < WST / 2; ++j)
-        if (wuses[j] > 0)
-          mbar_wait_quiet(bar_wempty + 8 * (gr + 2 * j), (uint32_t)((wuses[j] - 1) & 1), lim);
+      for (int j = 0; j < WST / 2; ++j) {
+        const int uses = ng > j ? (ng - j + WST / 2 - 1) / (WST / 2) : 0;
+        if (uses > 0)
+          mbar_wait_quiet(bar_wempty + 8 * (gr + 2 * j), (uint32_t)((uses - 1) & 1), lim);
+      }
+    }
+    } else if (lane == 0) {
+      // ===================================================== NF4 code producer
+      // Fills the code ring in running K-block order, paced by the decode
+      // groups' releases only: the codes run up to CST K-blocks ahead of
+      // decoding.  A rank K-block's slot carries no codes; its barrier is
+      // armed for the B / A tile that the decode group copies into its W slot.
+      int cst = 0;
+      uint32_t cph = 0;
+      int issued = 0;
+      bool ok = true;
+      TileIter it;
+      for (it.init(p.sched, pair); ok && it.valid(); it.next()) {
+        const int nt = it.nt();
+        const GemmGroup &G = p.grp[group_of(p, nt)];
+        const int nh = (nt - G.tile_begin) * BN + (int)crank * 128;
+        const int ne = DX ? p.grp[0].n_extra : G.n_extra;
+        for (int kb = 0; kb < nk + ne; ++kb) {
+          if (!mbar_wait(bar_cempty + 8 * cst, cph ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t cb = bar_cfull + 8 * cst;
+          if (kb < nk) {
+            // DX: the reduction may run over two projections' W (K-groups)
+            const int gk = (DX && p.kgroups > 1 && kb >= p.ksplit) ? 1 : 0;
+            const CUtensorMap *tw = DX ? &p.grp[gk].tm_w : &G.tm_w;
+            const int wk = kb - (gk ? p.ksplit : 0);
+            const uint32_t sc = base + L::OFF_CRING + cst * L::C_BYTES;
+            mbar_arrive_expect_tx(cb, L::C_BYTES);
+            if constexpr (DX)  // codes [64 rows of W, 64 bytes = 128 k-columns]
+              tma_load_2d(sc, tw, cb, nh / 2, wk * kBK);
+            else               // codes [128 rows of W, 32 bytes]
+              tma_load_2d(sc, tw, cb, kb * (kBK / 2), nh);
+          } else {
+            mbar_arrive_expect_tx(cb, L::W_BYTES);
+          }
+          ++issued;
+          if (++cst == CST) cst = 0, cph ^= 1u;
+        }
+      }
+      // no copy may land after the CTA exits: the last phase of every slot
+      // completes (bounded: after an abort some never do)
+      const uint64_t lim = *abort_flag ? 20000000ull : 1000000000ull;
+      for (int c = 0; c < CST; ++c) {
+        const int uses = issued > c ? (issued - c + CST - 1) / CST : 0;
+        if (uses > 0) mbar_wait_quiet(bar_cfull + 8 * c, (uint32_t)((uses - 1) & 1), lim);
+      }
     }
   }
 

@@ -29,7 +29,8 @@ LORA_DEV uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
+               : "r"(addr)
+               : "memory");
   return v;
 }
 
@@ -72,12 +73,20 @@ LORA_DEV void nf4_lookup4(const Nf4Table &t, uint32_t c, uint32_t &p01, uint32_t
   p23 = __byte_perm(lo, hi, 0x7362 ^ 0x1111);  // bytes lo.3, hi.3, lo.2, hi.2 -> (e2, e3)
 }
 
-// Decode one 64-element row piece: 32 code bytes at `src` (shared) into a
+// The 32 code bytes of one 64-element row piece at `src` (shared), read as
+// two 16-byte halves in the order `flip` gives (flip = 1: second half
+// first), returned in order.
+LORA_DEV void nf4_load_codes(uint32_t src, uint32_t flip, uint32_t (&w)[8]) {
+  const uint4 a = ld_shared_v4(src + (flip << 4));
+  const uint4 b = ld_shared_v4(src + ((flip ^ 1u) << 4));
+  const uint4 lo = flip ? b : a, hi = flip ? a : b;
+  w[0] = lo.x, w[1] = lo.y, w[2] = lo.z, w[3] = lo.w;
+  w[4] = hi.x, w[5] = hi.y, w[6] = hi.z, w[7] = hi.w;
+}
+
+// Decode one 64-element row piece (its 32 code bytes in `words`) into a
 // 128-byte row of a 128-byte-swizzled tile at `dst`.
-LORA_DEV void nf4_decode_row(uint32_t src, uint32_t dst, const Nf4Table &t) {
-  const uint4 c01 = ld_shared_v4(src);
-  const uint4 c23 = ld_shared_v4(src + 16);
-  const uint32_t words[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
+LORA_DEV void nf4_decode_words(const uint32_t (&words)[8], uint32_t dst, const Nf4Table &t) {
   const uint32_t phase = (dst >> 7) & 7u;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {

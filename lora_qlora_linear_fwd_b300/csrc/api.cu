@@ -148,14 +148,6 @@ Schedule make_schedule(int m_blocks, int n_tiles, int slots) {
   return s;
 }
 
-// CTAs per cluster of the rank pass: split the reduction while the grid
-// still fits on the SMs at one CTA each and every CTA keeps >= 8 chunks.
-int pick_split(int tiles, int min_chunks, int sms, int max_split) {
-  int s = 1;
-  while (2 * s <= max_split && tiles * s * 2 <= sms && min_chunks >= 8 * s * 2) s *= 2;
-  return s;
-}
-
 // ------------------------------------------------------ fused GEMM set-up
 struct GroupArgs {
   lora_weight_t W;
@@ -300,24 +292,64 @@ lora_status_t mnmajor_problem(SkinnyProblem &P, const void *p_ptr, int M, int ro
   return LORA_OK;
 }
 
-lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, uint32_t *status, cudaStream_t st) {
+// CTAs per cluster of the cluster schedule: split the reduction while the
+// grid still fits on the SMs at one CTA each and every CTA keeps >= 8 chunks.
+int pick_split(int tiles, int min_chunks, int sms, int max_split) {
+  int s = 1;
+  while (2 * s <= max_split && tiles * s * 2 <= sms && min_chunks >= 8 * s * 2) s *= 2;
+  return s;
+}
+
+// A rank pass.  The cluster schedule (one tile per cluster) is taken unless
+// the stream-K schedule (equal unit ranges on one CTA per SM) cuts the
+// chunks of the busiest CTA to 3/4 or less: that happens when the tiles are
+// too few to fill the SMs, or of unequal lengths.  Measured on B300, the
+// stream-K form has a few microseconds of extra cost (parked partials, a
+// second segment per CTA), so near-balanced cluster launches stay as they
+// are.  `scratch` (skinny_scratch_bytes(rp)) holds the stream-K flags and
+// parked partials.
+lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, uint32_t *status, void *scratch,
+                         cudaStream_t st) {
+  static std::atomic<unsigned long long> epoch{0};
   DeviceInfo di;
   lora_status_t s;
   if ((s = device_info(&di))) return s;
   int tiles = 0, min_chunks = 1 << 30;
+  long long units = 0;
   for (int q = 0; q < sp.num_problems; ++q) {
     sp.pr[q].tile_begin = tiles;
+    sp.pr[q].unit_begin = units;
     tiles += sp.pr[q].row_tiles;
     min_chunks = std::min(min_chunks, sp.pr[q].chunks);
+    units += (long long)sp.pr[q].row_tiles * sp.pr[q].chunks;
   }
-  sp.split = pick_split(tiles, min_chunks, di.sms, skinny_max_split(mn, rp));
+  if (units < 1) return LORA_ERR_INVALID_ARG;
   sp.status = status;
-  return cuda_status(launch_skinny(sp, mn, rp, st));
+  sp.split = pick_split(tiles, min_chunks, di.sms, skinny_max_split(mn, rp));
+  long long w_cluster = 0;  // chunks of the busiest CTA
+  for (int q = 0; q < sp.num_problems; ++q)
+    w_cluster = std::max<long long>(w_cluster, (sp.pr[q].chunks + sp.split - 1) / sp.split);
+  // stream-K: one CTA per SM, each with at least 8 chunks (a finisher adds
+  // one parked partial per extra CTA on its tile)
+  const int ctas = (int)std::max<long long>(
+      1, std::min<long long>(std::min(di.sms, kSkinnyMaxCtas), units / 8));
+  const long long w_sk = (units + ctas - 1) / ctas;
+  if (4 * w_sk > 3 * w_cluster) return cuda_status(launch_skinny_cluster(sp, mn, rp, st));
+  sp.units = units;
+  sp.ctas = ctas;
+  uint8_t *s8 = static_cast<uint8_t *>(scratch);
+  sp.flags = reinterpret_cast<unsigned long long *>(s8);
+  sp.partials = reinterpret_cast<float *>(s8 + align256((size_t)kSkinnyMaxCtas * 8));
+  sp.epoch = ++epoch;
+  return cuda_status(launch_skinny_sk(sp, mn, rp, st));
 }
 
 // ------------------------------------------------------------------ forward
-// Workspace: status | s·v [M, rl] bf16.
-size_t fwd_bytes(int M, int rl) { return kStatusBytes + align256((size_t)M * rl * 2); }
+// Workspace: status | s·v [M, rl] bf16 | rank-pass scratch.
+size_t fwd_sv_bytes(int M, int rl) { return align256((size_t)M * rl * 2); }
+size_t fwd_bytes(int M, int rl) {
+  return kStatusBytes + fwd_sv_bytes(M, rl) + skinny_scratch_bytes(rank_pad(rl));
+}
 
 // s·v = s·x·[A1; A2]ᵀ into the workspace (A2 null: one projection).
 lora_status_t fwd_rank(const void *x, const void *A1, const void *A2, int M, int k, int r,
@@ -335,7 +367,7 @@ lora_status_t fwd_rank(const void *x, const void *A1, const void *A2, int M, int
   P.nproj = nproj;
   P.scale = scale;
   sp.num_problems = 1;
-  return run_skinny(sp, false, rp, status, st);
+  return run_skinny(sp, false, rp, status, static_cast<uint8_t *>(sv) + fwd_sv_bytes(M, rl), st);
 }
 
 // ----------------------------------------------------------------- backward
@@ -347,7 +379,7 @@ lora_status_t fwd_rank(const void *x, const void *A1, const void *A2, int M, int
 //   grads  dA = s·uᵀ·x, dB = s·dYᵀ·v                           (one launch)
 struct BwdPlan {
   int rp, Mp;
-  size_t off_bt, off_su, off_ut_hi, off_ut_lo, off_vt_hi, off_vt_lo, total;
+  size_t off_bt, off_su, off_ut_hi, off_ut_lo, off_vt_hi, off_vt_lo, off_scratch, total;
 };
 
 BwdPlan plan_bwd(int M, int n, int rl, size_t start) {
@@ -361,6 +393,7 @@ BwdPlan plan_bwd(int M, int n, int rl, size_t start) {
   b.off_ut_lo = o;  o = align256(o + (size_t)b.rp * b.Mp * 2);
   b.off_vt_hi = o;  o = align256(o + (size_t)b.rp * b.Mp * 2);
   b.off_vt_lo = o;  o = align256(o + (size_t)b.rp * b.Mp * 2);
+  b.off_scratch = o; o = align256(o + skinny_scratch_bytes(b.rp));
   b.total = o;
   return b;
 }
@@ -414,7 +447,7 @@ lora_status_t bwd_rank(const BwdCall &c, cudaStream_t st) {
   PU.nproj = nproj;
   PU.scale = c.scale;
   sp.num_problems = 2;
-  return run_skinny(sp, false, b.rp, c.status, st);
+  return run_skinny(sp, false, b.rp, c.status, c.at<void>(b.off_scratch), st);
 }
 
 lora_status_t bwd_dx(const BwdCall &c, cudaStream_t st) {
@@ -465,7 +498,7 @@ lora_status_t bwd_grads(const BwdCall &c, cudaStream_t st) {
   PB.split_row = c.n1;
   PB.scale = c.scale;
   sp.num_problems = 2;
-  return run_skinny(sp, true, b.rp, c.status, st);
+  return run_skinny(sp, true, b.rp, c.status, c.at<void>(b.off_scratch), st);
 }
 
 lora_status_t run_bwd_phases(const BwdCall &c, cudaStream_t st) {

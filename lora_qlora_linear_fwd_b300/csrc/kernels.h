@@ -101,10 +101,16 @@ int gemm_pair_capacity(int mode, bool rope, bool nf4);  // max co-resident pairs
 // Skinny rank-r products on the tensor cores:
 //   KMAJOR  (v, u):  g[t][j] = Σ_c P[t,c]·Q[j,c]            P = x or dY, Q = A or Bᵀ
 //   MNMAJOR (dA,dB): g[o][j] = Σ_t P[t,o]·(Qhi+Qlo)[j,t]    P = x or dY, Q = uᵀ or vᵀ
-// A cluster of `split` CTAs owns one 128-row output tile; CTA c of the
-// cluster reduces the 64-wide chunks [C·c/split, C·(c+1)/split) and the
-// partials are added in the leader CTA in cluster-rank order (on chip,
-// deterministic).  Output kinds (a bit set):
+// Two schedules over the units (problem, 128-row output tile, 64-wide
+// reduction chunk):
+//   cluster (skinny.cu):    a cluster of `split` CTAs owns one tile and adds
+//                           its partials over distributed shared memory;
+//   stream-K (skinny_sk.cu): `ctas` equal contiguous unit ranges, one per CTA;
+//                           a tile shared by several CTAs is finished by the
+//                           one holding its first chunks, which adds the
+//                           others' fp32 partials (parked in `partials`,
+//                           announced in `flags`) in CTA order.
+// Both sum in a fixed order (deterministic).  Output kinds (a bit set):
 //   kOutVt:      gᵀ as bf16 hi + lo parts [RP, ld_t] (unscaled; the Q operand
 //                of the MNMAJOR pass)
 //   kOutRowBf16: scale·g as bf16 [rows, ld_row] (the rank K-block of the
@@ -114,6 +120,8 @@ int gemm_pair_capacity(int mode, bool rope, bool nf4);  // max co-resident pairs
 //   kOutRow:     out[o][j] = scale·g[o][j] fp32 (dB [n, r]); with nproj == 2
 //                rows >= split_row go to out_f32b from columns [r, 2r)
 enum SkinnyOut { kOutVt = 1, kOutRowBf16 = 2, kOutRowT = 4, kOutRow = 8 };
+
+constexpr int kSkinnyMaxCtas = 160;  // scratch slots (the grid is at most one CTA per SM)
 
 struct SkinnyProblem {
   CUtensorMap tm_p;
@@ -135,20 +143,29 @@ struct SkinnyProblem {
   int rows;              // output rows
   int row_tiles;         // ceil(rows / 128)
   int chunks;            // 64-wide reduction chunks
-  int tile_begin;        // first cluster of this problem
+  int tile_begin;        // cluster: first cluster of this problem
+  long long unit_begin;  // stream-K: units of the problems before this one
 };
 
 struct SkinnyParams {
   SkinnyProblem pr[2];
   int num_problems;
-  int split;             // CTAs per cluster (1, 2, 4 or 8)
+  int split;                   // cluster: CTAs per cluster (1, 2, 4 or 8)
+  int ctas;                    // stream-K: grid size (<= kSkinnyMaxCtas, <= units)
+  long long units;             // Σ row_tiles · chunks
+  float *partials;             // [kSkinnyMaxCtas][RP][128] fp32: CTA c's parked partial
+  unsigned long long *flags;   // [kSkinnyMaxCtas]: CTA c's partial of this launch is parked
+  unsigned long long epoch;    // unique per launch (flags of other launches never match)
   uint32_t *status;
 };
 
-cudaError_t launch_skinny(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st);
-// Largest `split` the (mn_major, rp) kernel supports (its epilogue buffers
-// must fit in its pipeline ring).
+cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st);
+// Largest `split` the cluster kernel supports for (mn_major, rp) (its
+// epilogue buffers must fit in its pipeline ring).
 int skinny_max_split(bool mn_major, int rp);
+// Scratch of one stream-K launch: flags, then partials (256-byte aligned).
+size_t skinny_scratch_bytes(int rp);
+cudaError_t launch_skinny_sk(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st);
 
 // Elementwise / small helpers.
 // Backward set-up (one launch): inverse RoPE of dy1|dy2 into dy_out (when

@@ -215,8 +215,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
       tma_prefetch_desc(&P.tm_p);
       int stage = 0;
       uint32_t phase = 0;
-      int fills[STAGES];
-      for (int s = 0; s < STAGES; ++s) fills[s] = 0;
+      int issued = 0;  // chunks issued: stage s took every STAGES-th from the s-th
       for (int i = 0; i < n_chunks; ++i) {
         const int c = c_begin + (i + c_rot) % n_chunks;
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) break;
@@ -239,13 +238,16 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
             tma_load_2d(sq, &P.tm_q, fb, c * 64, 0);
           }
         }
-        ++fills[stage];
+        ++issued;
         if (++stage == STAGES) stage = 0, phase ^= 1u;
       }
       // drain: every issued copy has been consumed before the CTA may exit
+      // (bounded: after an abort some never are)
       const uint64_t lim = *abort_flag ? 20000000ull : 1000000000ull;
-      for (int s = 0; s < STAGES; ++s)
-        if (fills[s] > 0) mbar_wait_quiet(bar_empty + 8 * s, (uint32_t)((fills[s] - 1) & 1), lim);
+      for (int s = 0; s < STAGES; ++s) {
+        const int fills = issued > s ? (issued - s + STAGES - 1) / STAGES : 0;
+        if (fills > 0) mbar_wait_quiet(bar_empty + 8 * s, (uint32_t)((fills - 1) & 1), lim);
+      }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -411,7 +413,7 @@ int skinny_max_split(bool mn_major, int rp) {
   return 1;
 }
 
-cudaError_t launch_skinny(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st) {
+cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st) {
   if (p.split != 1 && p.split != 2 && p.split != 4 && p.split != 8) return cudaErrorInvalidValue;
   if (p.split > skinny_max_split(mn_major, rp)) return cudaErrorInvalidValue;
   switch (rp) {

@@ -42,10 +42,19 @@ def test_status_strings():
     assert L.lora_status_string(99) == "LORA_ERR_UNKNOWN"
 
 
+def _rank_scratch(rp):
+    # rank-pass scratch: one 8-byte flag per CTA slot (160), 256-byte aligned,
+    # then one parked fp32 partial [rp, 128] per slot
+    return (160 * 8 + 255) // 256 * 256 + 160 * rp * 128 * 4
+
+
 def test_workspace_sizes():
-    # forward: status word + the rank block s·x·Aᵀ [M, r] bf16
-    assert L.workspace_size(L.OP_FWD, 256, 512, 512, 8) == 256 + 256 * 8 * 2
-    assert L.workspace_size(L.OP_QK_ROPE_FWD, 256, 512, 512, 8) == 256 + 256 * 16 * 2
+    # forward: status word + the rank block s·x·Aᵀ [M, r] bf16 + rank-pass scratch
+    assert L.workspace_size(L.OP_FWD, 256, 512, 512, 8) == 256 + 256 * 8 * 2 + _rank_scratch(16)
+    assert L.workspace_size(L.OP_QK_ROPE_FWD, 256, 512, 512, 8) == (
+        256 + 256 * 16 * 2 + _rank_scratch(16))
+    assert L.workspace_size(L.OP_FWD, 8192, 4096, 4096, 64) == (
+        256 + 8192 * 64 * 2 + _rank_scratch(64))
     b = L.workspace_size(L.OP_BWD, 256, 512, 512, 8)
     assert b > 256 and b % 256 == 0
     assert L.workspace_size(L.OP_BWD, 8192, 4096, 4096, 64) > L.workspace_size(
@@ -61,7 +70,7 @@ def _w(ptr=FAKE, typ=0, absmax=None, bs=0):
     return L.Weight(typ, ptr, absmax, bs)
 
 
-def _fwd(M=256, k=512, n=512, r=8, x=FAKE, W=None, A=FAKE, B=FAKE, y=FAKE, ws=FAKE, wsb=1 << 20,
+def _fwd(M=256, k=512, n=512, r=8, x=FAKE, W=None, A=FAKE, B=FAKE, y=FAKE, ws=FAKE, wsb=8 << 20,
          alpha=16.0):
     return lib.lora_linear_fwd(x, W or _w(), A, B, y, M, k, n, r, alpha, ws, wsb, None)
 

@@ -7,8 +7,8 @@
 // must never enter the driver's allocator (which can synchronise the device
 // and stall every stream).  This entry point takes the same inputs and
 // outputs as lora_linear_bwd but no workspace: its scratch (the transposed B,
-// the bf16 hi/lo parts of uᵀ and vᵀ, the fp32 slice partials, the arrival
-// counters and the device status word) lives in one fixed array in the
+// the bf16 hi/lo parts of uᵀ and vᵀ, the rank-pass flags and parked
+// partials, and the device status word) lives in one fixed array in the
 // library's own device memory, declared below.
 //
 // Properties a caller must know:
@@ -21,8 +21,9 @@
 //     (cudaGetSymbolAddress, with that device current) and caches it; make
 //     that first call before any stream capture.
 //   * Every call uses the same array, which keeps the previous call's
-//     contents: each call zeroes the status word and the arrival counters
-//     it needs, and everything else is fully written before it is read.
+//     contents: each call zeroes the status word; the rank-pass flags
+//     carry a per-launch epoch (stale ones never match), and everything
+//     else is fully written before it is read.
 //     Two calls that overlap on the GPU (e.g. on two streams of one device)
 //     race on the array and give wrong results; serialise them.
 //   * Device-side failures (a pipeline wait past its time limit) are
@@ -86,8 +87,7 @@ extern "C" lora_status_t lora_linear_bwd_noalloc(const void *x, lora_weight_t W,
   cudaError_t err = cudaSuccess;
   void *scratch = scratch_address(&err);
   if (!scratch) return LORA_ERR_CUDA;
-  // the status word starts each call at zero (the counters are cleared by
-  // the backward itself)
+  // the status word starts each call at zero
   if (cudaMemsetAsync(scratch, 0, 256, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return LORA_ERR_CUDA;
   return lora_linear_bwd(x, W, A, B, dy, dx, accumulate_dx, dA, dB, M, k, n, r, alpha, scratch,

@@ -349,6 +349,10 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
               // launch, e.g. from a CUDA graph, carries the same epoch)
               for (int q = 1; q <= n_part; ++q) p.flags[cta + q] = 0ull;
               if (staged) {
+                // the partials were written with ordinary stores and made
+                // visible by the acquire; order them before the copy
+                // engine's reads
+                asm volatile("fence.proxy.async.global;" ::: "memory");
                 mbar_arrive_expect_tx(bar_ready, (uint32_t)n_part * kPartBytes);
                 for (int q = 1; q <= n_part; ++q)
                   bulk_load(base + (uint32_t)(q - 1) * kPartBytes,

@@ -96,9 +96,13 @@ enum {
  * lives at offset 0).  Besides the intermediates each call documents, every
  * operation holds a rank-pass scratch of 160 flags and 160 fp32 partials of
  * [r padded to 16/32/64/128, 128] (up to 10 MB), used when a rank pass runs
- * on its stream-K schedule; its previous contents are never taken for a new
- * call's (the flags carry a per-launch epoch), so a workspace needs no
- * clearing between calls.  For the q/k operations pass k = hidden and
+ * on its stream-K schedule.  A flag is matched against its launch's epoch (a
+ * random per-process tag plus a launch counter) and cleared by the CTA that
+ * consumes it, so stale or uninitialised workspace contents are not taken
+ * for a new call's and a workspace needs no clearing between calls.  After
+ * a call that reported LORA_ERR_TIMEOUT, zero the workspace before reusing
+ * it (a partial parked after the timeout may have left its flag set for a
+ * replay of the same launch).  For the q/k operations pass k = hidden and
  * n = (n_q_heads + n_kv_heads) * head_dim.  Returns 0 for an unknown op or
  * out-of-range sizes.  Pure host function. */
 size_t lora_workspace_size(int op, int M, int k, int n, int r);

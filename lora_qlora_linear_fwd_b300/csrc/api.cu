@@ -5,11 +5,13 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <random>
 
 #include "kernels.h"
 #include "lora_b300.h"
@@ -132,18 +134,13 @@ lora_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : L
 
 // ------------------------------------------------------------- schedule
 // Persistent GEMM schedule: as many CTA pairs as fit (one per two SMs),
-// grouped raster of `group_m` m-blocks (LORA_GROUP_M overrides the default
-// of 8, for measurements).
+// grouped raster of 8 m-blocks.
 Schedule make_schedule(int m_blocks, int n_tiles, int slots) {
-  static const int forced_gm = [] {
-    const char *v = std::getenv("LORA_GROUP_M");
-    return v ? std::atoi(v) : 0;
-  }();
   const long long total = (long long)m_blocks * n_tiles;
   Schedule s;
   s.m_blocks = m_blocks;
   s.n_tiles = n_tiles;
-  s.group_m = std::max(1, std::min(m_blocks, forced_gm > 0 ? forced_gm : 8));
+  s.group_m = std::max(1, std::min(m_blocks, 8));
   s.workers = (int)std::max<long long>(1, std::min<long long>(slots, total));
   return s;
 }
@@ -308,9 +305,24 @@ int pick_split(int tiles, int min_chunks, int sms, int max_split) {
 // second segment per CTA), so near-balanced cluster launches stay as they
 // are.  `scratch` (skinny_scratch_bytes(rp)) holds the stream-K flags and
 // parked partials.
+// Epoch of a stream-K launch: a random 40-bit tag drawn once per process in
+// the high bits and a launch counter in the low 24, so a flag word left in a
+// reused workspace by another process, by older launches or by unrelated
+// data (small integers, floats) does not equal this launch's epoch.
+unsigned long long next_epoch() {
+  static const unsigned long long tag = [] {
+    std::random_device rd;
+    const unsigned long long t = ((unsigned long long)rd() << 32) ^ rd() ^
+        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+    return (t & 0xFFFFFFFFFFull) | 1ull;  // never zero
+  }();
+  static std::atomic<unsigned long long> counter{0};
+  const unsigned long long c = (counter.fetch_add(1, std::memory_order_relaxed) + 1) & 0xFFFFFFull;
+  return (tag << 24) | c;
+}
+
 lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, uint32_t *status, void *scratch,
                          cudaStream_t st) {
-  static std::atomic<unsigned long long> epoch{0};
   DeviceInfo di;
   lora_status_t s;
   if ((s = device_info(&di))) return s;
@@ -340,7 +352,7 @@ lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, uint32_t *status, vo
   uint8_t *s8 = static_cast<uint8_t *>(scratch);
   sp.flags = reinterpret_cast<unsigned long long *>(s8);
   sp.partials = reinterpret_cast<float *>(s8 + align256((size_t)kSkinnyMaxCtas * 8));
-  sp.epoch = ++epoch;
+  sp.epoch = next_epoch();
   return cuda_status(launch_skinny_sk(sp, mn, rp, st));
 }
 
@@ -528,6 +540,26 @@ QkBwdPlan plan_qk_bwd(int M, int k, int n, int r) {
 
 }  // namespace
 
+namespace lora {
+lora_status_t check_bwd_args(const void *x, lora_weight_t W, const void *A, const void *B,
+                             const void *dy, const void *dx, const float *dA, const float *dB,
+                             int M, int k, int n, int r, float alpha) {
+  lora_status_t s;
+  if ((s = check_shape(M, k, n, r))) return s;
+  if ((s = check_weight(W))) return s;
+  if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(dy) || !aligned16(dx) ||
+      !aligned16(dA) || !aligned16(dB))
+    return LORA_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha)) return LORA_ERR_INVALID_ARG;
+  return LORA_OK;
+}
+
+lora_status_t check_current_device() {
+  DeviceInfo di;
+  return device_info(&di);
+}
+}  // namespace lora
+
 // =================================================================== C ABI
 extern "C" {
 
@@ -603,12 +635,8 @@ lora_status_t lora_linear_bwd(const void *x, lora_weight_t W, const void *A, con
                               int M, int k, int n, int r, float alpha, void *ws, size_t ws_bytes,
                               lora_stream_t stream) {
   lora_status_t s;
-  if ((s = check_shape(M, k, n, r))) return s;
-  if ((s = check_weight(W))) return s;
-  if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(dy) || !aligned16(dx) ||
-      !aligned16(dA) || !aligned16(dB) || !aligned16(ws))
-    return LORA_ERR_INVALID_ARG;
-  if (!std::isfinite(alpha)) return LORA_ERR_INVALID_ARG;
+  if ((s = lora::check_bwd_args(x, W, A, B, dy, dx, dA, dB, M, k, n, r, alpha))) return s;
+  if (!aligned16(ws)) return LORA_ERR_INVALID_ARG;
   if (ws_bytes < lora_workspace_size(LORA_OP_BWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
   DeviceInfo di;
   if ((s = device_info(&di))) return s;

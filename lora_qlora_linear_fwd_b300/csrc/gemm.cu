@@ -589,33 +589,37 @@ template <int MODE, bool NF4, bool ROPE>
 static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t st) {
   using L = PairSmem<NF4, ROPE && !NF4>;
   auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(2 * pairs), dim3(pair_threads(NF4)), L::TOTAL, st, 0u, p);
 }
 
+// Co-resident CTA pairs of one kernel on the current device (cached per
+// device; 0 if the query fails).
 template <int MODE, bool NF4, bool ROPE>
 static int pair_capacity() {
   using L = PairSmem<NF4, ROPE && !NF4>;
   auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE>;
-  static int cached = -1;
-  if (cached < 0) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL) !=
-        cudaSuccess)
-      return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(pair_threads(NF4), 1, 1);
-    cfg.dynamicSmemBytes = L::TOTAL;
-    int n = 0;  // cluster shape comes from the kernel's compile-time cluster dims
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
-    cached = n;
+  static std::atomic<uint64_t> attr_done{0};
+  static std::atomic<int> cached[kMaxDevices];  // pairs + 1; 0: not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  if (slot) {
+    const int v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v - 1;
   }
-  return cached;
+  if (smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(pair_threads(NF4), 1, 1);
+  cfg.dynamicSmemBytes = L::TOTAL;
+  int n = 0;  // cluster shape comes from the kernel's compile-time cluster dims
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+  if (slot) cached[dev].store(n + 1, std::memory_order_relaxed);
+  return n;
 }
 
 template <int MODE, bool NF4>

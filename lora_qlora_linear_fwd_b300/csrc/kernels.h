@@ -1,14 +1,54 @@
 // Internal interface between the C-ABI host code (api.cu) and the kernels.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "lora_b300.h"
 
 namespace lora {
+
+// ------------------------------------------------ per-device host state
+// Devices the per-device caches below track (ordinals 0..63); calls on a
+// higher ordinal skip the caches and query every time.
+constexpr int kMaxDevices = 64;
+
+// Raises the dynamic shared-memory limit of `kern` to `bytes` on the current
+// device, once per device: the attribute belongs to the (kernel, device)
+// pair, so a process that drives several GPUs sets it on each.  `done` is the
+// calling launcher's per-kernel record (one bit per device); concurrent
+// first calls may both set the attribute, which is harmless.
+inline cudaError_t smem_attr_once(std::atomic<uint64_t> &done, const void *kern, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < kMaxDevices) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// Streaming multiprocessors of the current device (cached per device);
+// 0 if the query fails.
+inline int current_device_sms() {
+  static std::atomic<int> cached[kMaxDevices];  // 0: not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  if (slot) {
+    const int v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (slot) cached[dev].store(sms, std::memory_order_relaxed);
+  return sms;
+}
 
 // The fused GEMM computes, per output tile, one reduction over the
 // concatenated K axis [ main | rank ]:
@@ -190,5 +230,17 @@ cudaError_t launch_nf4_dequant(const uint8_t *codes, const __nv_bfloat16 *absmax
                                __nv_bfloat16 *w, int n, int k, cudaStream_t st);
 cudaError_t launch_nf4_quantize(const __nv_bfloat16 *w, uint8_t *codes, __nv_bfloat16 *absmax,
                                 int n, int k, cudaStream_t st);
+
+// Argument checks of lora_linear_bwd other than the workspace (shape limits,
+// weight descriptor, pointer alignment, finite alpha), shared with
+// lora_linear_bwd_noalloc so that both reject the same calls before
+// touching the device.
+lora_status_t check_bwd_args(const void *x, lora_weight_t W, const void *A, const void *B,
+                             const void *dy, const void *dx, const float *dA, const float *dB,
+                             int M, int k, int n, int r, float alpha);
+
+// LORA_OK if the current device is an sm_103 part (else LORA_ERR_ARCH, or
+// LORA_ERR_CUDA if the query fails).
+lora_status_t check_current_device();
 
 }  // namespace lora

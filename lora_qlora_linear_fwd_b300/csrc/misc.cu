@@ -2,12 +2,18 @@
 // rotation of incoming gradients, merged A and Bᵀ), the cos/sin
 // cache builder, and the standalone NF4 dequantise / quantise.
 #include "kernels.h"
+#include "nf4_levels.cuh"
 
 namespace lora {
 
-static int grid_for(size_t items, int per_block, int cap) {
+// Blocks for `items` work items of `per_block` each, capped at
+// `per_sm` resident blocks on every SM of the current device (grid-stride
+// loops take the rest).
+static int grid_for(size_t items, int per_block, int per_sm) {
   const size_t g = (items + per_block - 1) / per_block;
-  return (int)(g < (size_t)cap ? (g > 0 ? g : 1) : (size_t)cap);
+  const int sms = current_device_sms();
+  const size_t cap = (size_t)(sms > 0 ? sms : 1) * (size_t)per_sm;
+  return (int)(g < cap ? (g > 0 ? g : 1) : cap);
 }
 
 // ------------------------------------------------------- backward set-up
@@ -88,7 +94,7 @@ cudaError_t launch_bwd_prep(const BwdPrep &p, cudaStream_t st) {
   const int n = p.n1 + p.n2, rl = p.nproj * p.r;
   const size_t total = (p.dy1 ? (size_t)p.M * (n / 128) * 8 : 0) +
                        (p.nproj > 1 ? (size_t)rl * p.k / 8 : 0) + (size_t)rl * n;
-  return launch_pdl(bwd_prep_kernel, dim3(grid_for(total, 256, 148 * 16)), dim3(256), 0, st, 0u,
+  return launch_pdl(bwd_prep_kernel, dim3(grid_for(total, 256, 16)), dim3(256), 0, st, 0u,
                     p);
 }
 
@@ -112,19 +118,13 @@ __global__ void rope_cache_kernel(float *__restrict__ cs, int max_pos, int D, do
 cudaError_t launch_rope_cache(float *cos_sin, int max_pos, int head_dim, double theta,
                               cudaStream_t st) {
   const size_t total = (size_t)max_pos * (head_dim / 2);
-  const int grid = grid_for(total, 256, 148 * 16);
+  const int grid = grid_for(total, 256, 16);
   rope_cache_kernel<<<grid, 256, 0, st>>>(cos_sin, max_pos, head_dim, theta);
   note_launch();
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------ NF4 dequant
-// The 16 NormalFloat4 levels (QLoRA, Dettmers et al. 2023, appendix table).
-__constant__ float kNf4LevelsMisc[16] = {
-    -1.0f, -0.6961928009986877f, -0.5250730514526367f, -0.39491748809814453f,
-    -0.28444138169288635f, -0.18477343022823334f, -0.09105003625154495f, 0.0f,
-    0.07958029955625534f, 0.16093020141124725f, 0.24611230194568634f, 0.33791524171829224f,
-    0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
 
 // One thread per 32-bit code word (8 elements, 16 output bytes), so a
 // warp's code loads are 128 contiguous bytes and its stores 512; the eight
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t *__restr
                                                           __nv_bfloat16 *__restrict__ w,
                                                           size_t n_words) {
   __shared__ float lv[16];
-  if (threadIdx.x < 16) lv[threadIdx.x] = kNf4LevelsMisc[threadIdx.x];
+  if (threadIdx.x < 16) lv[threadIdx.x] = kNf4Levels[threadIdx.x];
   __syncthreads();
   const uint32_t *c32 = reinterpret_cast<const uint32_t *>(codes);
   uint4 *w4 = reinterpret_cast<uint4 *>(w);
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t *__restr
 cudaError_t launch_nf4_dequant(const uint8_t *codes, const __nv_bfloat16 *absmax,
                                __nv_bfloat16 *w, int n, int k, cudaStream_t st) {
   const size_t words = (size_t)n * k / 8;
-  const int grid = grid_for(words, 256, 148 * 8);
+  const int grid = grid_for(words, 256, 8);
   nf4_dequant_kernel<<<grid, 256, 0, st>>>(codes, absmax, w, words);
   note_launch();
   return cudaGetLastError();
@@ -185,7 +185,7 @@ cudaError_t launch_nf4_dequant(const uint8_t *codes, const __nv_bfloat16 *absmax
 __global__ void nf4_quantize_kernel(const __nv_bfloat16 *__restrict__ w, uint8_t *__restrict__ codes,
                                     __nv_bfloat16 *__restrict__ absmax, size_t n_blocks) {
   __shared__ float lv[16];
-  if (threadIdx.x < 16) lv[threadIdx.x] = kNf4LevelsMisc[threadIdx.x];
+  if (threadIdx.x < 16) lv[threadIdx.x] = kNf4Levels[threadIdx.x];
   __syncthreads();
   for (size_t b = blockIdx.x * (size_t)blockDim.x + threadIdx.x; b < n_blocks;
        b += (size_t)gridDim.x * blockDim.x) {
@@ -239,7 +239,7 @@ __global__ void nf4_quantize_kernel(const __nv_bfloat16 *__restrict__ w, uint8_t
 cudaError_t launch_nf4_quantize(const __nv_bfloat16 *w, uint8_t *codes, __nv_bfloat16 *absmax,
                                 int n, int k, cudaStream_t st) {
   const size_t blocks = (size_t)n * k / 64;
-  const int grid = grid_for(blocks, 128, 148 * 8);
+  const int grid = grid_for(blocks, 128, 8);
   nf4_quantize_kernel<<<grid, 128, 0, st>>>(w, codes, absmax, blocks);
   note_launch();
   return cudaGetLastError();

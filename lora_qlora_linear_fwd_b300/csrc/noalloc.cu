@@ -34,6 +34,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "kernels.h"
 #include "lora_b300.h"
 
 namespace {
@@ -44,17 +45,15 @@ constexpr size_t kNoAllocScratchBytes = 32ull << 20;
 // this name is only a handle for cudaGetSymbolAddress, never an address.
 static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-
 // Device address of g_bwd_scratch on the current device, looked up once per
 // device.  Returns nullptr (and sets *err) if the lookup fails.
 void *scratch_address(cudaError_t *err) {
   static std::mutex mu;
-  static void *addr[kMaxDevices] = {};
+  static void *addr[lora::kMaxDevices] = {};
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= kMaxDevices) {
+  if (dev < 0 || dev >= lora::kMaxDevices) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
@@ -75,15 +74,14 @@ extern "C" lora_status_t lora_linear_bwd_noalloc(const void *x, lora_weight_t W,
                                                  int accumulate_dx, float *dA, float *dB, int M,
                                                  int k, int n, int r, float alpha,
                                                  lora_stream_t stream) {
-  // argument checks first, so a bad call touches no device state
-  auto aligned = [](const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  if (!aligned(x) || !aligned(A) || !aligned(B) || !aligned(dy) || !aligned(dx) || !aligned(dA) ||
-      !aligned(dB) || !aligned(W.w))
-    return LORA_ERR_INVALID_ARG;
+  // every check lora_linear_bwd makes comes first, so a call it would
+  // reject enqueues nothing (not even the status-word reset below)
+  lora_status_t s = lora::check_bwd_args(x, W, A, B, dy, dx, dA, dB, M, k, n, r, alpha);
+  if (s != LORA_OK) return s;
   const size_t need = lora_workspace_size(LORA_OP_BWD, M, k, n, r);
   if (need == 0) return LORA_ERR_INVALID_ARG;
-  if (k % 64 || n % 64) return LORA_ERR_UNSUPPORTED;
   if (need > kNoAllocScratchBytes) return LORA_ERR_WORKSPACE;
+  if ((s = lora::check_current_device()) != LORA_OK) return s;
   cudaError_t err = cudaSuccess;
   void *scratch = scratch_address(&err);
   if (!scratch) return LORA_ERR_CUDA;

@@ -383,12 +383,9 @@ template <bool MN, int RP>
 static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
   using L = SkinnySmem<MN, RP>;
   auto kern = lora_skinny_kernel<MN, RP>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
+  if (e != cudaSuccess) return e;
   int tiles = 0;
   for (int q = 0; q < p.num_problems; ++q) tiles += p.pr[q].row_tiles;
   return launch_pdl(kern, dim3((unsigned)(tiles * p.split)), dim3(192), L::TOTAL, st,

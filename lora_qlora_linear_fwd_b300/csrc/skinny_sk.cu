@@ -344,10 +344,12 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
           if (leader) {
             for (int q = 1; q <= n_part && ok; ++q)
               ok = wait_flag(p.flags + cta + q, p.epoch, abort_flag, p.status);
+            // consumed (or given up on) by this launch: clear them, since a
+            // replay of the same launch, e.g. from a CUDA graph, carries the
+            // same epoch.  A partial parked after a timeout can still leave a
+            // flag behind; the status word then reports the timeout.
+            for (int q = 1; q <= n_part; ++q) p.flags[cta + q] = 0ull;
             if (ok) {
-              // consumed by this launch: clear them (a replay of the same
-              // launch, e.g. from a CUDA graph, carries the same epoch)
-              for (int q = 1; q <= n_part; ++q) p.flags[cta + q] = 0ull;
               if (staged) {
                 // the partials were written with ordinary stores and made
                 // visible by the acquire; order them before the copy
@@ -408,12 +410,9 @@ template <bool MN, int RP>
 static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
   using L = SkSmem<MN, RP>;
   auto kern = lora_skinny_sk_kernel<MN, RP>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3((unsigned)p.ctas), dim3(192), L::TOTAL, st, 0u, p);
 }
 

@@ -1,23 +1,38 @@
 """Throughput of the fused LoRA / QLoRA projection, forward + backward.
 
-Default workload: Llama-3-8B-shaped q_proj + k_proj with the RoPE epilogue,
-M = 8192 tokens (1 x 8192), hidden 4096, q 32x128, k 8x128, r = 64,
-alpha = 16, theta = 5e5, positions 0..8191, bf16 W.  One step = one
-``lora_qk_rope_fwd`` + one ``lora_qk_rope_bwd`` over the batch; every other
-workload of ``lora_inputs.WORKLOADS`` runs ``lora_linear_fwd`` +
-``lora_linear_bwd`` per projection.
+Headline workload: the Qwen1.5-32B-shaped QLoRA step, all 7 projections
+(q/o 5120->5120, k/v 5120->1024, gate/up 5120->27392, down 27392->5120), NF4
+base weights (block 64, bf16 absmax), M = 8192 tokens (4 x 2048), r = 64,
+alpha = 16.  One step = ``lora_linear_fwd`` + ``lora_linear_bwd`` per
+projection; the Llama-3-8B q/k + RoPE workload runs ``lora_qk_rope_fwd`` +
+``lora_qk_rope_bwd`` instead.
 
-Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
-oracle instead (a bounded token sample per step) and prints the same line
-with ``"impl": "reference"``.  Under torchrun every rank runs its own
-replica on its own GPU (weak scaling, no data-path collective).
+Prints ONE JSON line (rank 0) with:
+  * value / ms_per_step: tokens per second of the headline step, timed with
+    CUDA events on the launching stream, L2 flushed between steps;
+  * peaks: HBM copy bandwidth and bf16 matmul throughput measured in this
+    run (beside the pool's MEASURED_PEAKS.json figures);
+  * kernels / roofline / hbm_rooflines: every launch of the same K steps run
+    again inside a per-launch timing session (lora_profile_begin), grouped by
+    kernel, each with its algorithmic FLOPs or bytes;
+  * per_workload: the other configurations' steps (parity shapes excepted);
+  * e2e: the same step with its inputs copied from pinned host memory and
+    all results read back, copies inside the timed region;
+  * cpu_baseline: the fp64 oracle on a bounded token sample (all cores, and
+    one core on a smaller sample).
+``--impl reference`` times the fp64 CPU oracle instead (a bounded token
+sample per step) and prints the same line with ``"impl": "reference"``.
+Under torchrun every rank runs its own replica on its own GPU (weak
+scaling, no data-path collective).
 """
 from __future__ import annotations
 
 import argparse
+import concurrent.futures as cf
 import hashlib
 import json
 import math
+import multiprocessing as mp
 import os
 import statistics
 import subprocess
@@ -35,11 +50,14 @@ if ROOT not in sys.path:
 from lora_inputs import WORKLOADS, draw_workload  # noqa: E402
 
 METRIC = "fused LoRA fwd+bwd tokens/s & TFLOP/s at 1 B300; % of bf16 tensor peak / HBM BW"
-DEFAULT_WORKLOAD = "llama8b_qk_rope"
+DEFAULT_WORKLOAD = "qwen32b_qlora_all7"
+# configurations timed beside the headline (the 256-token single linear is a
+# parity case, not a bench line)
+OTHER_WORKLOADS = ("llama8b_qk_rope", "llama8b_mlp", "llama8b_qlora_all7")
 FLUSH_BYTES = 512 << 20          # > 126 MB L2, written between timed steps
 
 
-# --------------------------------------------------------------------- flops
+# --------------------------------------------------------------------- work
 def step_flops(wl, M) -> float:
     """Algorithmic FLOPs of fwd+bwd for all projections (W frozen, no dW):
     4Mkn (x·Wᵀ, dY·W) + 2Mr(k+n) (x·Aᵀ, (s·v)·Bᵀ) + 2Mr(2n+3k) (dY·B, u·A,
@@ -52,11 +70,50 @@ def step_flops(wl, M) -> float:
     return f
 
 
-def fwd_kernel_flops(wl, M) -> float:
-    """FLOPs of one fused forward launch (all projections of the launch)."""
+def call_phases(wl, M):
+    """The library calls of one step, in order, each with the algorithmic work
+    of its launches in launch order: (call, [(phase, flops, bytes), ...]).
+
+    bytes count each operand and result once, as the phase needs it (NF4 W:
+    codes k/2 + bf16 absmax k/32 bytes per row); u and v of the backward are
+    fp32-equivalent (their bf16 hi + lo parts)."""
     r = wl.r
-    return sum(2.0 * M * p.k * p.n + 2.0 * M * r * p.k + 2.0 * M * r * p.n
-               for p in wl.projections)
+    out = []
+    if wl.rope:
+        (pq, pk) = wl.projections
+        k, n, rl = pq.k, pq.n + pk.n, 2 * r
+        rp = 16 if rl <= 16 else 32 if rl <= 32 else 64 if rl <= 64 else 128
+        wbytes = 2.0 * n * k
+        out.append(("fwd", [
+            ("fwd_rank", 2.0 * M * k * rl, 2.0 * M * k + 2.0 * rl * k + 2.0 * M * rl),
+            ("fwd_gemm", 2.0 * M * k * n + 2.0 * M * r * n,
+             2.0 * M * k + wbytes + 2.0 * M * n + 2.0 * M * rl + 2.0 * n * r)]))
+        out.append(("bwd", [
+            ("bwd_prep", 0.0, 4.0 * M * n + 4.0 * rl * k + 4.0 * n * rl),
+            ("bwd_rank", 2.0 * M * rl * (k + n),
+             2.0 * M * (k + n) + 2.0 * rl * (k + n) + 8.0 * rp * M + 2.0 * M * rl),
+            ("dx_gemm", 2.0 * M * n * k + 2.0 * M * rl * k,
+             2.0 * M * n + wbytes + 2.0 * M * k + 2.0 * M * rl + 2.0 * rl * k),
+            ("bwd_grads", 2.0 * M * rl * (k + n),
+             2.0 * M * (k + n) + 8.0 * rp * M + 4.0 * rl * (k + n))]))
+        return out
+    rp = 16 if r <= 16 else 32 if r <= 32 else 64
+    for p in wl.projections:
+        k, n = p.k, p.n
+        wbytes = (n * k / 2.0 + n * k / 32.0) if wl.nf4 else 2.0 * n * k
+        out.append(("fwd:" + p.name, [
+            ("fwd_rank", 2.0 * M * k * r, 2.0 * M * k + 2.0 * r * k + 2.0 * M * r),
+            ("fwd_gemm", 2.0 * M * k * n + 2.0 * M * r * n,
+             2.0 * M * k + wbytes + 2.0 * M * n + 2.0 * M * r + 2.0 * n * r)]))
+        out.append(("bwd:" + p.name, [
+            ("bwd_prep", 0.0, 4.0 * n * r),
+            ("bwd_rank", 2.0 * M * r * (k + n),
+             2.0 * M * (k + n) + 2.0 * r * (k + n) + 8.0 * rp * M + 2.0 * M * r),
+            ("dx_gemm", 2.0 * M * n * k + 2.0 * M * r * k,
+             2.0 * M * n + wbytes + 2.0 * M * k + 2.0 * M * r + 2.0 * r * k),
+            ("bwd_grads", 2.0 * M * r * (k + n),
+             2.0 * M * (k + n) + 8.0 * rp * M + 4.0 * r * (k + n))]))
+    return out
 
 
 # ------------------------------------------------------------ distributed
@@ -145,31 +202,88 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ peaks
-def measured_peaks():
+def pool_peaks():
+    """The machine's measured peaks (MEASURED_PEAKS.json), else the fallback."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d["bf16_tflops_sustained"], "source": "measured"}
+                "bf16_tflops_sustained": d["bf16_tflops_sustained"], "source": "measured (pool)"}
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
             "source": "fallback"}
 
 
+def measure_peaks(dev, sustained_s: float = 4.0):
+    """Peaks measured in this run the way the pool measures them: a copy_ of
+    1 Gi bf16 elements (read + write bytes, best of 10) and a bf16 8192^3
+    torch.matmul (best of 10 = burst; back to back for `sustained_s` seconds
+    = sustained), CUDA events on the current stream."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    a = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev).fill_(1.0)
+    b = torch.empty_like(a)
+    best = float("inf")
+    for i in range(12):
+        s, e = ev(), ev()
+        s.record()
+        b.copy_(a)
+        e.record()
+        torch.cuda.synchronize()
+        if i >= 2:
+            best = min(best, s.elapsed_time(e))
+    hbm = 2.0 * a.numel() * 2 / (best * 1e-3) / 1e9
+    del a, b
+    N = 8192
+    g = torch.Generator(device=dev).manual_seed(0)
+    x = torch.randn(N, N, device=dev, dtype=torch.bfloat16, generator=g)
+    y = torch.randn(N, N, device=dev, dtype=torch.bfloat16, generator=g)
+    best = float("inf")
+    for i in range(12):
+        s, e = ev(), ev()
+        s.record()
+        torch.matmul(x, y)
+        e.record()
+        torch.cuda.synchronize()
+        if i >= 2:
+            best = min(best, s.elapsed_time(e))
+    burst = 2.0 * N ** 3 / (best * 1e-3) / 1e12
+    s, e = ev(), ev()
+    count = 0
+    t_end = time.perf_counter() + sustained_s
+    s.record()
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            torch.matmul(x, y)
+        count += 20
+        torch.cuda.synchronize()
+    e.record()
+    torch.cuda.synchronize()
+    sustained = 2.0 * N ** 3 * count / (s.elapsed_time(e) * 1e-3) / 1e12
+    del x, y
+    torch.cuda.empty_cache()
+    return {"hbm_gbs": round(hbm, 1), "bf16_tflops": round(burst, 1),
+            "bf16_tflops_sustained": round(sustained, 1),
+            "how": "copy_ of 1 Gi bf16 (best of 10); bf16 matmul 8192^3 best of 10 (burst) and "
+                   f"back to back for {sustained_s:g} s (sustained); CUDA events"}
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in sorted(os.listdir(os.path.join(ROOT, "lora_qlora_linear_fwd_b300", "csrc"))):
-        h.update(open(os.path.join(ROOT, "lora_qlora_linear_fwd_b300", "csrc", f), "rb").read())
+    d = os.path.join(ROOT, "lora_qlora_linear_fwd_b300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the fused forward kernel from the committed ncu
-    summary, if it was taken on the current kernel sources (else None)."""
+    """ncu DRAM bytes per launch, by kernel name, from the committed summary
+    for `workload`, when it was taken on the current kernel sources."""
     p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
     if not os.path.exists(p):
-        return None
+        return {}
     d = json.load(open(p))
-    return d.get("dram_bytes_per_launch") if d.get("source_hash") == kernel_source_hash() else None
+    if d.get("source_hash") != kernel_source_hash():
+        return {}
+    return d.get("dram_bytes_per_launch", {})
 
 
 # ------------------------------------------------------------- GPU replica
@@ -180,16 +294,16 @@ class Replica:
     def __init__(self, name: str, device: str, seed: int = 0):
         import lora_qlora_linear_fwd_b300 as L
         self.L = L
+        self.name = name
         self.wl = wl = WORKLOADS[name]
         self.dev = device
         self.M = M = wl.M
         data = draw_workload(name, seed=seed)
         bf = dict(dtype=torch.bfloat16, device=device)
         f32 = dict(dtype=torch.float32, device=device)
-        self.keep = []
         self.projs = []
         for p in wl.projections:
-            d = {k: v.to(device) for k, v in data[p.name].items()}
+            d = {k: v.to(device) for k, v in data.pop(p.name).items()}
             if wl.nf4:   # quantise the drawn W on the GPU (setup, not timed)
                 codes = torch.empty(p.n, p.k // 2, dtype=torch.uint8, device=device)
                 absmax = torch.empty(p.n, p.k // 64, **bf)
@@ -216,10 +330,12 @@ class Replica:
             self.ws_b = L.workspace(L.OP_QK_ROPE_BWD, M, pq.k, n_tot, wl.r, device=device)
             self.dx = torch.empty(M, pq.k, **bf)
         else:
-            self.ws = {}
-            for p, d in self.projs:
-                self.ws[p.name] = (L.workspace(L.OP_FWD, M, p.k, p.n, wl.r, device=device),
-                                   L.workspace(L.OP_BWD, M, p.k, p.n, wl.r, device=device))
+            # calls run one after another on one stream: one workspace per op
+            # kind, sized for the largest projection
+            self.ws_f = torch.zeros(max(L.workspace_size(L.OP_FWD, M, p.k, p.n, wl.r)
+                                        for p in wl.projections), dtype=torch.uint8, device=device)
+            self.ws_b = torch.zeros(max(L.workspace_size(L.OP_BWD, M, p.k, p.n, wl.r)
+                                        for p in wl.projections), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
 
     def inputs(self):
@@ -241,69 +357,56 @@ class Replica:
             out += [d["y"], d["dx"], d["dA"], d["dB"]]
         return out
 
-    def fwd(self):
+    def calls(self):
+        """The library calls of one step, in order: [(name, fn)]."""
         L, wl = self.L, self.wl
         if wl.rope:
             (_, q), (_, k) = self.projs
-            L.lora_qk_rope_fwd(q["x"], q["Wdesc"], q["A"], q["B"], k["Wdesc"], k["A"], k["B"],
-                               q["y"], k["y"], wl.alpha, wl.rope_theta, self.pos, self.cache,
-                               self.max_pos, self.ws_f)
-        else:
-            for p, d in self.projs:
-                L.lora_linear_fwd(d["x"], d["Wdesc"], d["A"], d["B"], d["y"], wl.alpha,
-                                  self.ws[p.name][0])
+            return [
+                ("fwd", lambda: L.lora_qk_rope_fwd(
+                    q["x"], q["Wdesc"], q["A"], q["B"], k["Wdesc"], k["A"], k["B"], q["y"],
+                    k["y"], wl.alpha, wl.rope_theta, self.pos, self.cache, self.max_pos,
+                    self.ws_f)),
+                ("bwd", lambda: L.lora_qk_rope_bwd(
+                    q["x"], q["Wdesc"], q["A"], q["B"], k["Wdesc"], k["A"], k["B"], q["dY"],
+                    k["dY"], self.dx, q["dA"], q["dB"], k["dA"], k["dB"], wl.alpha,
+                    wl.rope_theta, self.pos, self.cache, self.max_pos, self.ws_b))]
+        out = []
+        for p, d in self.projs:
+            out.append(("fwd:" + p.name, lambda d=d: L.lora_linear_fwd(
+                d["x"], d["Wdesc"], d["A"], d["B"], d["y"], wl.alpha, self.ws_f)))
+        for p, d in self.projs:
+            out.append(("bwd:" + p.name, lambda d=d: L.lora_linear_bwd(
+                d["x"], d["Wdesc"], d["A"], d["B"], d["dY"], d["dx"], d["dA"], d["dB"],
+                wl.alpha, self.ws_b)))
+        return out
+
+    def fwd(self):
+        for name, fn in self.calls():
+            if name.startswith("fwd"):
+                fn()
 
     def bwd(self):
-        L, wl = self.L, self.wl
-        if wl.rope:
-            (_, q), (_, k) = self.projs
-            L.lora_qk_rope_bwd(q["x"], q["Wdesc"], q["A"], q["B"], k["Wdesc"], k["A"], k["B"],
-                               q["dY"], k["dY"], self.dx, q["dA"], q["dB"], k["dA"], k["dB"],
-                               wl.alpha, wl.rope_theta, self.pos, self.cache, self.max_pos,
-                               self.ws_b)
-        else:
-            for p, d in self.projs:
-                L.lora_linear_bwd(d["x"], d["Wdesc"], d["A"], d["B"], d["dY"], d["dx"], d["dA"],
-                                  d["dB"], wl.alpha, self.ws[p.name][1])
+        for name, fn in self.calls():
+            if name.startswith("bwd"):
+                fn()
 
     def step(self):
-        self.fwd()
-        self.bwd()
+        for _, fn in self.calls():
+            fn()
 
     def check_status(self):
-        wss = [self.ws_f, self.ws_b] if self.wl.rope else [w for pair in self.ws.values()
-                                                           for w in pair]
-        for w in wss:
+        for w in (self.ws_f, self.ws_b):
             s = self.L.lora_read_device_status(w)
             if s:
                 raise RuntimeError(f"device status {s:#x}")
 
 
-def run_gpu(args, world, rank, local):
-    torch.cuda.set_device(local)
-    dev = f"cuda:{local}"
-    rep = Replica(args.workload, dev)
-    wl, M = rep.wl, rep.M
-    L = rep.L
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        rep.step()
-    torch.cuda.synchronize()
-    rep.check_status()
-
+def time_steps(rep, steps, flush, stream):
+    """CUDA-event times (ms) of `steps` steps: (step, fwd part)."""
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    launches0 = L.lora_kernel_launch_count()
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(args.steps):
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
         flush.zero_()                      # L2 flush: not inside the step's events
         a, b, c = ev[i]
         a.record(stream)
@@ -312,37 +415,207 @@ def run_gpu(args, world, rank, local):
         rep.bwd()
         c.record(stream)
     torch.cuda.synchronize()
+    return [a.elapsed_time(c) for a, _, c in ev], [a.elapsed_time(b) for a, b, _ in ev]
+
+
+def profile_steps(rep, steps, flush):
+    """The same steps inside a per-launch timing session: every launch with
+    its kernel, phase and algorithmic work."""
+    L = rep.L
+    phases = {name: ph for name, ph in call_phases(rep.wl, rep.M)}
+    calls = rep.calls()
+    cap = steps * sum(len(ph) for ph in phases.values()) + 16
+    launches = []   # (call, phase, flops, bytes)
+    L.lora_profile_begin(cap)
+    try:
+        for _ in range(steps):
+            flush.zero_()
+            for name, fn in calls:
+                c0 = L.lora_kernel_launch_count()
+                fn()
+                n = L.lora_kernel_launch_count() - c0
+                ph = phases[name]
+                if n != len(ph):
+                    raise RuntimeError(f"{name}: {n} launches, expected {len(ph)}")
+                launches += [(name,) + x for x in ph]
+    finally:
+        timed = L.lora_profile_end(cap)
+    if len(timed) != len(launches):
+        raise RuntimeError(f"profile: {len(timed)} timed launches for {len(launches)}")
+    return [(kname, ms, call, phase, fl, by)
+            for (kname, ms), (call, phase, fl, by) in zip(timed, launches)]
+
+
+def summarise_kernels(rows, steps, peaks, pool):
+    """Per kernel name: launches per step, time per step, share, and the
+    algorithmic throughput of its launches (FLOP/s for the GEMMs, B/s for the
+    streaming passes)."""
+    total = sum(r[1] for r in rows)
+    by = {}
+    for kname, ms, call, phase, fl, b in rows:
+        e = by.setdefault(kname, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0,
+                                  "phases": set()})
+        e["launches"] += 1
+        e["ms"] += ms
+        e["flops"] += fl
+        e["bytes"] += b
+        e["phases"].add(phase)
+    out = []
+    for kname, e in sorted(by.items(), key=lambda kv: -kv[1]["ms"]):
+        gemm = kname.startswith("lora_gemm_pair_kernel")
+        row = {"kernel": kname, "phases": sorted(e["phases"]),
+               "launches_per_step": e["launches"] / steps,
+               "ms_per_step": round(e["ms"] / steps, 4),
+               "share": round(e["ms"] / total, 4),
+               "avg_launch_us": round(1e3 * e["ms"] / e["launches"], 2)}
+        if gemm:
+            tf = e["flops"] / (e["ms"] * 1e-3) / 1e12
+            row.update({"bound": "tensor", "tflops": round(tf, 1),
+                        "frac": round(tf / peaks["bf16_tflops"], 4),
+                        "frac_pool": round(tf / pool["bf16_tflops"], 4)})
+        else:
+            gbs = e["bytes"] / (e["ms"] * 1e-3) / 1e9
+            row.update({"bound": "hbm", "gbs": round(gbs, 1),
+                        "frac": round(gbs / peaks["hbm_gbs"], 4),
+                        "frac_pool": round(gbs / pool["hbm_gbs"], 4)})
+        out.append((row, e))
+    return out, total / steps
+
+
+def run_nf4_dequant_shapes(shapes, dev, flush, steps, warmup, peak):
+    """HBM throughput of ``nf4_dequant`` on weight shapes [(n, k)]: bytes =
+    codes n·k/2 + absmax n·k/32 + bf16 output 2·n·k, CUDA-event time per call
+    with a 512 MiB L2 flush between calls (outside the events)."""
+    import lora_qlora_linear_fwd_b300 as L
+    g = torch.Generator(device="cpu").manual_seed(0)
+    rows = []
+    for n, k in shapes:
+        W = (torch.randn(n, k, generator=g) / math.sqrt(k)).to(torch.bfloat16).to(dev)
+        codes = torch.empty(n, k // 2, dtype=torch.uint8, device=dev)
+        absmax = torch.empty(n, k // 64, dtype=torch.bfloat16, device=dev)
+        L.nf4_quantize(W, codes, absmax)
+        out = torch.empty(n, k, dtype=torch.bfloat16, device=dev)
+        del W
+        for _ in range(warmup):
+            L.nf4_dequant(codes, absmax, out)
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            L.nf4_dequant(codes, absmax, out)
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        t = statistics.median(ts)
+        nbytes = n * k // 2 + n * k // 32 + 2 * n * k
+        gbs = nbytes / (t * 1e-3) / 1e9
+        rows.append({"n": n, "k": k, "us": round(t * 1e3, 2), "GBps": round(gbs, 1),
+                     "frac_hbm": round(gbs / peak, 3)})
+        del codes, absmax, out
+    return rows
+
+
+def workload_line(rep, steps, warmup, flush, stream, peaks, pool):
+    """Step time of one workload (used for the configurations beside the
+    headline)."""
+    for _ in range(warmup):
+        flush.zero_()
+        rep.step()
+    torch.cuda.synchronize()
+    step_ms, fwd_ms = time_steps(rep, steps, flush, stream)
+    rep.check_status()
+    ms = statistics.mean(step_ms)
+    fl = step_flops(rep.wl, rep.M)
+    tf = fl / (ms * 1e-3) / 1e12
+    return {"ms_per_step": round(ms, 4), "ms_median": round(statistics.median(step_ms), 4),
+            "fwd_ms": round(statistics.mean(fwd_ms), 4),
+            "tokens_per_s": round(rep.M / (ms * 1e-3), 1), "tflops": round(tf, 1),
+            "frac_of_burst": round(tf / peaks["bf16_tflops"], 4),
+            "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+            "frac_of_pool_burst": round(tf / pool["bf16_tflops"], 4),
+            "steps": steps, "M": rep.M, "description": rep.wl.description}
+
+
+def run_gpu(args, world, rank, local):
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    import lora_qlora_linear_fwd_b300 as L
+    pool = pool_peaks()
+    peaks = measure_peaks(dev, args.sustained_s)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    rep = Replica(args.workload, dev)
+    wl, M = rep.wl, rep.M
+    for _ in range(args.warmup):
+        flush.zero_()
+        rep.step()
+    torch.cuda.synchronize()
+    rep.check_status()
+
+    # ---- the headline timed region (no instrumentation)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = L.lora_kernel_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    step_ms, fwd_ms = time_steps(rep, args.steps, flush, stream)
     barrier(world)
     wall = time.perf_counter() - t0
     launches = L.lora_kernel_launch_count() - launches0
     clocks = sampler.stop()
     rep.check_status()
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
     ms_local = statistics.mean(step_ms)
     ms = max_over_ranks(ms_local, world)
     fwd_ms_mean = statistics.mean(fwd_ms)
 
-    # end to end through the C ABI with host buffers (pinned), copies timed
+    # ---- the same steps again, each launch timed (per-kernel rooflines)
+    rows = profile_steps(rep, args.steps, flush)
+    rep.check_status()
+    kern, prof_ms_per_step = summarise_kernels(rows, args.steps, peaks, pool)
+    traffic = profiled_traffic(args.workload)
+    top_row, top = kern[0]
+    top_kind = "tensor" if top_row["bound"] == "tensor" else "hbm"
+    achieved = top_row["tflops"] if top_kind == "tensor" else top_row["gbs"]
+    peak = peaks["bf16_tflops"] if top_kind == "tensor" else peaks["hbm_gbs"]
+    tr = traffic.get(top_row["kernel"])
+    roofline = {
+        "kernel": top_row["kernel"], "bound": top_kind, "achieved": achieved, "peak": peak,
+        "unit": "TFLOP/s" if top_kind == "tensor" else "GB/s",
+        "frac": round(achieved / peak, 4),
+        "peak_source": "measured in this run (burst)",
+        "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)
+        if top_kind == "tensor" else None,
+        "frac_of_pool": top_row["frac_pool"],
+        "pool_peak": pool["bf16_tflops"] if top_kind == "tensor" else pool["hbm_gbs"],
+        "traffic": tr,
+        "algorithmic_per_launch": (top["flops"] if top_kind == "tensor" else top["bytes"])
+        / top["launches"],
+        "avg_launch_us": top_row["avg_launch_us"], "launches_per_step":
+        top_row["launches_per_step"], "share": top_row["share"],
+        "timing": "CUDA events around each launch on its stream (lora_profile_begin), over "
+                  f"{args.steps} steps run right after the timed region"}
+    hbm_lines = [dict(r, peak=peaks["hbm_gbs"]) for r, _ in kern if r["bound"] == "hbm"]
+    # nf4_dequant on the headline's weight shapes
+    if wl.nf4:
+        shapes = sorted({(p.n, p.k) for p in wl.projections})
+        dq = run_nf4_dequant_shapes(shapes, dev, flush, 10, 3, peaks["hbm_gbs"])
+        for row in dq:
+            hbm_lines.append({"kernel": "nf4_dequant_kernel", "shape": [row["n"], row["k"]],
+                              "bound": "hbm", "gbs": row["GBps"], "us": row["us"],
+                              "frac": row["frac_hbm"], "peak": peaks["hbm_gbs"],
+                              "frac_pool": round(row["GBps"] / pool["hbm_gbs"], 4)})
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
     e2e = run_e2e(rep, args, stream)
     e2e_ms = max_over_ranks(e2e["ms"], world)
 
     flops = step_flops(wl, M)
-    peaks = measured_peaks()
     tokens_per_s = world * M / (ms / 1e3)
-    # dominant kernel: the fused forward GEMM (one launch per fwd call)
-    fk = fwd_kernel_flops(wl, M) / len(wl.projections) if not wl.rope else fwd_kernel_flops(wl, M)
-    fwd_launch_ms = fwd_ms_mean / (1 if wl.rope else len(wl.projections))
-    achieved = fk / (fwd_launch_ms / 1e3) / 1e12
-    fwd_name = ("lora_qk_rope_fwd" if wl.rope else "lora_linear_fwd") + \
-        " (rank pass + fused GEMM, 2 launches)"
-    roofline = {"kernel": fwd_name, "bound": "tensor",
-                "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                "peak_source": peaks["source"] + " (burst)",
-                "traffic": profiled_traffic(args.workload),
-                "launch_ms": round(fwd_launch_ms, 4)}
     line = {
         "metric": METRIC,
         "value": round(tokens_per_s, 1),
@@ -358,15 +631,23 @@ def run_gpu(args, world, rank, local):
         "data": "synthetic (seeded, Llama/Qwen-shaped; no weights or datasets)",
         "tflops": round(world * flops / (ms / 1e3) / 1e12, 1),
         "tflops_frac_of_peak": round(flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+        "tflops_frac_of_sustained": round(
+            flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"], 4),
+        "tflops_frac_of_pool_peak": round(flops / (ms / 1e3) / 1e12 / pool["bf16_tflops"], 4),
         "fwd_ms": round(fwd_ms_mean, 4),
         "bwd_ms": round(ms_local - fwd_ms_mean, 4),
+        "ms_median": round(statistics.median(step_ms), 4),
         "region_wall_s": round(wall, 4),
         "config": {"workload": args.workload, "description": wl.description, "M": M,
                    "r": wl.r, "alpha": wl.alpha, "nf4": wl.nf4,
                    "projections": [[p.name, p.k, p.n] for p in wl.projections],
                    "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (512 MiB write, outside step events)"},
+        "peaks": {"this_run": peaks, "pool": pool},
         "roofline": roofline,
+        "hbm_rooflines": hbm_lines,
+        "kernels": [r for r, _ in kern],
+        "profiled_ms_per_step": round(prof_ms_per_step, 4),
         "e2e": {"value": round(world * M / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_ms, 4)},
@@ -374,8 +655,29 @@ def run_gpu(args, world, rank, local):
         "gpu_launches_per_step": launches / args.steps,
         "clocks": clocks,
     }
+    del rep
+    torch.cuda.empty_cache()
+
+    # ---- the other configurations (rank 0 only reports them)
+    if not args.no_per_workload:
+        per = {}
+        for name in OTHER_WORKLOADS:
+            if name == args.workload:
+                continue
+            r2 = Replica(name, dev)
+            per[name] = workload_line(r2, args.steps, args.warmup, flush, stream, peaks, pool)
+            del r2
+            torch.cuda.empty_cache()
+        per[args.workload] = {
+            "ms_per_step": line["ms_per_step"], "tokens_per_s": line["value"] / world,
+            "tflops": round(flops / (ms / 1e3) / 1e12, 1),
+            "frac_of_burst": line["tflops_frac_of_peak"],
+            "frac_of_sustained": line["tflops_frac_of_sustained"],
+            "frac_of_pool_burst": line["tflops_frac_of_pool_peak"], "steps": args.steps,
+            "M": M, "description": wl.description, "headline": True}
+        line["per_workload"] = per
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_tokens)
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_tokens, args.cpu_tokens_1core)
     return line
 
 
@@ -439,35 +741,73 @@ def oracle_step(name: str, data, M: int):
             ref.lora_bwd(f(d["x"]), W, f(d["A"]), f(d["B"]), f(d["dY"]), wl.alpha)
 
 
+def _quantize_rows(w_rows):
+    """Oracle NF4 quantisation of a block of W rows (rows are independent)."""
+    import oracle as ref
+    return ref.nf4_quantize(w_rows)
+
+
 def _oracle_sample(name: str, tokens: int):
+    """The workload's tensors with `tokens` rows of x and dY; NF4 weights are
+    quantised by the oracle (row blocks spread over a spawned process pool:
+    preparation of the oracle's inputs, outside its timing)."""
     import oracle as ref
     wl = WORKLOADS[name]
     data = draw_workload(name, seed=0, M=tokens)
     if wl.nf4:
-        for p in wl.projections:
-            d = data[p.name]
-            codes, absmax = ref.nf4_quantize(d["W"].float().numpy())
-            d["Wq"] = ref.nf4_dequant(codes, absmax)
+        workers = max(1, min(os.cpu_count() or 1, 32))
+        with cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn")) as ex:
+            for p in wl.projections:
+                d = data[p.name]
+                W = d["W"].float().numpy()
+                step = max(64, -(-W.shape[0] // workers))
+                parts = list(ex.map(_quantize_rows, [W[i:i + step]
+                                                     for i in range(0, W.shape[0], step)]))
+                codes = np.concatenate([c for c, _ in parts])
+                absmax = np.concatenate([a for _, a in parts])
+                d["Wq"] = ref.nf4_dequant(codes, absmax)
     return data
 
 
-def cpu_baseline(name: str, tokens: int):
+def _time_oracle(name, data, tokens, threads=None):
+    if threads is None:
+        t0 = time.perf_counter()
+        oracle_step(name, data, tokens)
+        return time.perf_counter() - t0
+    from threadpoolctl import threadpool_limits
+    with threadpool_limits(limits=threads):
+        t0 = time.perf_counter()
+        oracle_step(name, data, tokens)
+        return time.perf_counter() - t0
+
+
+def _slice(data, tokens):
+    return {p: {k: (v[:tokens] if k in ("x", "dY") else v) for k, v in d.items()}
+            for p, d in data.items()}
+
+
+def cpu_baseline(name: str, tokens: int, tokens_1core: int):
     """The fp64 oracle as it stands, on the host cores, over a bounded token
-    sample of the same workload; tokens/s = sample tokens / time."""
+    sample of the same workload; tokens/s = sample tokens / time.  Also one
+    BLAS thread on a smaller sample."""
     data = _oracle_sample(name, tokens)
-    t0 = time.perf_counter()
-    oracle_step(name, data, tokens)
-    dt = time.perf_counter() - t0
+    dt = _time_oracle(name, data, tokens)
+    small = _slice(data, tokens_1core)
+    dt1 = _time_oracle(name, small, tokens_1core, threads=1)
     return {"value": round(tokens / dt, 2), "unit": "tokens/s", "cores": _blas_threads(),
-            "kind": "oracle", "sample": f"{tokens} of {WORKLOADS[name].M} tokens, all "
-            f"projections, fwd+bwd in fp64 numpy ({dt:.1f} s)"}
+            "cpu_count": os.cpu_count(), "kind": "oracle",
+            "sample": f"{tokens} of {WORKLOADS[name].M} tokens, all projections, fwd+bwd in "
+                      f"fp64 numpy ({dt:.1f} s)",
+            "one_core": {"value": round(tokens_1core / dt1, 2), "unit": "tokens/s", "cores": 1,
+                         "sample": f"{tokens_1core} tokens, all projections, fwd+bwd, one BLAS "
+                                   f"thread ({dt1:.1f} s)"}}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return None
     wl = WORKLOADS[args.workload]
-    tokens = args.cpu_tokens
+    tokens = args.ref_tokens
     data = _oracle_sample(args.workload, tokens)
     for _ in range(args.warmup):
         oracle_step(args.workload, data, tokens)
@@ -477,17 +817,19 @@ def run_reference(args, world, rank):
         oracle_step(args.workload, data, tokens)
         times.append(time.perf_counter() - t0)
     per_token = statistics.mean(times) / tokens
-    ms_full = per_token * wl.M * 1e3
     value = 1.0 / per_token
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_full, 2), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": round(per_token * wl.M * 1e3, 2),
+        "ms_per_step_basis": f"scaled linearly from {tokens}-token samples to {wl.M} tokens",
+        "ms_per_sample_step": round(statistics.mean(times) * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "description": wl.description, "M": wl.M,
                    "sample_tokens_per_step": tokens},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "kind": "oracle",
-                         "cores": _blas_threads(),
+                         "cores": _blas_threads(), "cpu_count": os.cpu_count(),
                          "sample": f"{tokens} tokens per step of {wl.M}, fwd+bwd, fp64"},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -501,43 +843,14 @@ NF4_DEQUANT_SHAPES = [  # W [n, k] of the Llama-3-8B and Qwen1.5-32B QLoRA proje
 
 
 def run_nf4_dequant(args):
-    """HBM throughput of ``nf4_dequant`` on the QLoRA weight shapes: bytes =
-    codes n·k/2 + absmax n·k/32 + bf16 output 2·n·k, CUDA-event time per call
-    with a 512 MiB L2 flush between calls (outside the events)."""
-    import lora_qlora_linear_fwd_b300 as L
     dev = "cuda:0"
     torch.cuda.set_device(0)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    peak = measured_peaks()["hbm_gbs"]
-    g = torch.Generator(device="cpu").manual_seed(0)
-    rows = []
-    for n, k in NF4_DEQUANT_SHAPES:
-        W = (torch.randn(n, k, generator=g) / math.sqrt(k)).to(torch.bfloat16).to(dev)
-        codes = torch.empty(n, k // 2, dtype=torch.uint8, device=dev)
-        absmax = torch.empty(n, k // 64, dtype=torch.bfloat16, device=dev)
-        L.nf4_quantize(W, codes, absmax)
-        out = torch.empty(n, k, dtype=torch.bfloat16, device=dev)
-        del W
-        for _ in range(args.warmup):
-            L.nf4_dequant(codes, absmax, out)
-        ts = []
-        for _ in range(args.steps):
-            flush.zero_()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
-            L.nf4_dequant(codes, absmax, out)
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        t = statistics.median(ts)
-        nbytes = n * k // 2 + n * k // 32 + 2 * n * k
-        gbs = nbytes / (t * 1e-3) / 1e9
-        rows.append({"n": n, "k": k, "us": round(t * 1e3, 2), "GBps": round(gbs, 1),
-                     "frac_hbm": round(gbs / peak, 3)})
-        del codes, absmax, out
-    return {"component": "nf4_dequant", "unit": "GB/s", "peak_hbm_gbs": peak,
-            "peak_source": measured_peaks()["source"], "steps": args.steps,
+    pool = pool_peaks()
+    rows = run_nf4_dequant_shapes(NF4_DEQUANT_SHAPES, dev, flush, args.steps, args.warmup,
+                                  pool["hbm_gbs"])
+    return {"component": "nf4_dequant", "unit": "GB/s", "peak_hbm_gbs": pool["hbm_gbs"],
+            "peak_source": pool["source"], "steps": args.steps,
             "warmup": args.warmup, "l2": "flushed between calls (512 MiB write, outside events)",
             "data": "synthetic: NF4 codes of W ~ N(0, 1/k) quantised by nf4_quantize",
             "shapes": rows}
@@ -546,13 +859,21 @@ def run_nf4_dequant(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--cpu-tokens", type=int, default=128,
-                    help="token sample for the oracle timing (CPU baseline / reference arm)")
+    ap.add_argument("--cpu-tokens", type=int, default=512,
+                    help="token sample of the oracle timing on all cores (CPU baseline)")
+    ap.add_argument("--cpu-tokens-1core", type=int, default=32,
+                    help="token sample of the oracle timing on one BLAS thread")
+    ap.add_argument("--ref-tokens", type=int, default=128,
+                    help="token sample per step of the reference arm")
+    ap.add_argument("--sustained-s", type=float, default=4.0,
+                    help="seconds of back-to-back matmuls for the sustained peak")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the step lines of the other configurations")
     ap.add_argument("--component", default="step", choices=["step", "nf4_dequant"],
                     help="step: the fwd+bwd step (default); nf4_dequant: the standalone "
                          "dequantisation on the QLoRA weight shapes (1 GPU)")

@@ -229,6 +229,23 @@ lora_status_t lora_clear_device_status(void *ws, lora_stream_t stream);
  * (monotonic; a diagnostic for counting launches per step). */
 uint64_t lora_kernel_launch_count(void);
 
+/* Per-launch timing, a diagnostic (no counterpart in the pages): while a
+ * session is open, each of the library's next `capacity` kernel launches (any
+ * entry point, any stream) is bracketed by two timing events recorded on its
+ * stream, one just before and one just after the launch, so the time between
+ * them is that kernel's run time (it also keeps the kernel from starting
+ * early under the previous one, which the library otherwise allows).
+ * lora_profile_begin creates the 2*capacity events (host-side CUDA objects,
+ * no device memory) and returns LORA_ERR_INVALID_ARG if a session is already
+ * open or capacity is outside [1, 65536].  lora_profile_end waits for the
+ * recorded events, writes the kernel name (a static string) and time in ms
+ * of the first min(launches, capacity) launches, in launch order, to
+ * names/ms, sets *count, destroys the events and closes the session.  One
+ * session per process, driven from one host thread; do not capture the
+ * library's launches into a CUDA graph while it is open. */
+lora_status_t lora_profile_begin(int capacity);
+lora_status_t lora_profile_end(const char **names, float *ms, int capacity, int *count);
+
 /* Human-readable name of a status code. */
 const char *lora_status_string(lora_status_t s);
 

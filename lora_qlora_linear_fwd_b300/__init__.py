@@ -23,7 +23,7 @@ __all__ = [
     "lora_qk_rope_bwd",
     "nf4_dequant", "nf4_quantize", "lora_rope_cache_build", "lora_rope_cache_bytes",
     "lora_read_device_status", "lora_clear_device_status", "lora_status_string",
-    "lora_kernel_launch_count",
+    "lora_kernel_launch_count", "lora_profile_begin", "lora_profile_end",
     "OP_FWD", "OP_BWD", "OP_QK_ROPE_FWD", "OP_QK_ROPE_BWD", "EXPORTS", "library",
 ]
 
@@ -68,6 +68,9 @@ EXPORTS = {
     "lora_read_device_status": (_I, [_P, _U32P, _P]),
     "lora_clear_device_status": (_I, [_P, _P]),
     "lora_kernel_launch_count": (ctypes.c_uint64, []),
+    "lora_profile_begin": (_I, [_I]),
+    "lora_profile_end": (_I, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), _I,
+                              ctypes.POINTER(ctypes.c_int)]),
     "lora_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -131,6 +134,21 @@ def workspace(op: int, M: int, k: int, n: int, r: int, device="cuda", extra: int
 
 def lora_kernel_launch_count() -> int:
     return int(library.lora_kernel_launch_count())
+
+
+def lora_profile_begin(capacity: int):
+    """Open a per-launch timing session for the next ``capacity`` launches."""
+    _check(library.lora_profile_begin(int(capacity)), "lora_profile_begin")
+
+
+def lora_profile_end(capacity: int):
+    """Close the session: ``[(kernel_name, ms), ...]`` in launch order."""
+    names = (ctypes.c_char_p * capacity)()
+    ms = (ctypes.c_float * capacity)()
+    count = ctypes.c_int(0)
+    _check(library.lora_profile_end(names, ms, int(capacity), ctypes.byref(count)),
+           "lora_profile_end")
+    return [(names[i].decode(), float(ms[i])) for i in range(count.value)]
 
 
 def lora_status_string(s: int) -> str:

@@ -12,6 +12,7 @@
 #include <cstring>
 #include <mutex>
 #include <random>
+#include <vector>
 
 #include "kernels.h"
 #include "lora_b300.h"
@@ -20,7 +21,42 @@ using namespace lora;
 
 namespace lora {
 static std::atomic<uint64_t> g_launches{0};
-void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+// Per-launch timing session (lora_profile_begin / lora_profile_end): event
+// pairs created up front, consumed one pair per launch in launch order.
+struct ProfileSession {
+  std::mutex mu;
+  std::atomic<bool> open{false};
+  std::vector<cudaEvent_t> before, after;
+  std::vector<const char *> names;
+  int used = 0;
+  bool pending = false;  // launch_begin recorded before[used]
+};
+ProfileSession &profile() {
+  static ProfileSession s;
+  return s;
+}
+}  // namespace
+
+void launch_begin(cudaStream_t st) {
+  ProfileSession &s = profile();
+  if (!s.open.load(std::memory_order_acquire)) return;
+  std::lock_guard<std::mutex> g(s.mu);
+  if (s.used < (int)s.before.size()) s.pending = cudaEventRecord(s.before[s.used], st) == cudaSuccess;
+}
+
+void note_launch(const char *name, cudaStream_t st) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  ProfileSession &s = profile();
+  if (!s.open.load(std::memory_order_acquire)) return;
+  std::lock_guard<std::mutex> g(s.mu);
+  if (!s.pending || s.used >= (int)s.after.size()) return;
+  s.pending = false;
+  if (cudaEventRecord(s.after[s.used], st) != cudaSuccess) return;
+  s.names[s.used] = name;
+  ++s.used;
+}
 }  // namespace lora
 
 namespace {
@@ -564,6 +600,61 @@ lora_status_t check_current_device() {
 extern "C" {
 
 uint64_t lora_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+lora_status_t lora_profile_begin(int capacity) {
+  if (capacity < 1 || capacity > (1 << 16)) return LORA_ERR_INVALID_ARG;
+  ProfileSession &s = profile();
+  std::lock_guard<std::mutex> g(s.mu);
+  if (s.open.load(std::memory_order_acquire)) return LORA_ERR_INVALID_ARG;
+  s.before.assign(capacity, nullptr);
+  s.after.assign(capacity, nullptr);
+  s.names.assign(capacity, nullptr);
+  s.used = 0;
+  s.pending = false;
+  for (int i = 0; i < capacity; ++i) {
+    if (cudaEventCreate(&s.before[i]) != cudaSuccess || cudaEventCreate(&s.after[i]) != cudaSuccess) {
+      for (cudaEvent_t e : s.before)
+        if (e) cudaEventDestroy(e);
+      for (cudaEvent_t e : s.after)
+        if (e) cudaEventDestroy(e);
+      s.before.clear();
+      s.after.clear();
+      return LORA_ERR_CUDA;
+    }
+  }
+  s.open.store(true, std::memory_order_release);
+  return LORA_OK;
+}
+
+lora_status_t lora_profile_end(const char **names, float *ms, int capacity, int *count) {
+  ProfileSession &s = profile();
+  std::lock_guard<std::mutex> g(s.mu);
+  if (!s.open.load(std::memory_order_acquire)) return LORA_ERR_INVALID_ARG;
+  s.open.store(false, std::memory_order_release);
+  lora_status_t st = LORA_OK;
+  int n = 0;
+  for (int i = 0; i < s.used; ++i) {
+    float t = 0.0f;
+    if (cudaEventSynchronize(s.after[i]) != cudaSuccess ||
+        cudaEventElapsedTime(&t, s.before[i], s.after[i]) != cudaSuccess) {
+      st = LORA_ERR_CUDA;
+      break;
+    }
+    if (n < capacity && names && ms) {
+      names[n] = s.names[i];
+      ms[n] = t;
+    }
+    ++n;
+  }
+  if (count) *count = std::min(n, capacity);
+  for (cudaEvent_t e : s.before) cudaEventDestroy(e);
+  for (cudaEvent_t e : s.after) cudaEventDestroy(e);
+  s.before.clear();
+  s.after.clear();
+  s.names.clear();
+  s.used = 0;
+  return st;
+}
 
 const char *lora_status_string(lora_status_t s) {
   switch (s) {

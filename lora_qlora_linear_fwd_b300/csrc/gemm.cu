@@ -592,7 +592,11 @@ static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t 
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(2 * pairs), dim3(pair_threads(NF4)), L::TOTAL, st, 0u, p);
+  constexpr const char *name =
+      MODE == kModeFwd ? (NF4 ? (ROPE ? "lora_gemm_pair_kernel<fwd,nf4,rope>" : "lora_gemm_pair_kernel<fwd,nf4>")
+                              : (ROPE ? "lora_gemm_pair_kernel<fwd,bf16,rope>" : "lora_gemm_pair_kernel<fwd,bf16>"))
+                       : (NF4 ? "lora_gemm_pair_kernel<dx,nf4>" : "lora_gemm_pair_kernel<dx,bf16>");
+  return launch_pdl(name, kern, dim3(2 * pairs), dim3(pair_threads(NF4)), L::TOTAL, st, 0u, p);
 }
 
 // Co-resident CTA pairs of one kernel on the current device (cached per

@@ -99,16 +99,21 @@ struct GemmParams {
 
 enum GemmMode { kModeFwd = 0, kModeDx = 1 };
 
-// Count of kernel launches issued by the library (see lora_kernel_launch_count).
-void note_launch();
+// Launch bookkeeping around every kernel launch of the library:
+// launch_begin() just before it, note_launch() just after (with the kernel's
+// name and stream).  note_launch counts launches (lora_kernel_launch_count);
+// while a timing session is open (lora_profile_begin) the pair records a
+// timing event on the stream on each side of the launch.
+void launch_begin(cudaStream_t st);
+void note_launch(const char *name, cudaStream_t st);
 
 // Launch with programmatic stream serialization (the kernel calls
 // grid_dep_wait() before touching global memory), and optionally cluster
 // dimensions (cluster_x > 0; kernels with compile-time cluster dimensions
 // pass 0).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       unsigned cluster_x, Args... args) {
+cudaError_t launch_pdl(const char *name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, unsigned cluster_x, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -128,8 +133,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
+  launch_begin(st);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
-  note_launch();
+  note_launch(name, st);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -94,7 +94,7 @@ cudaError_t launch_bwd_prep(const BwdPrep &p, cudaStream_t st) {
   const int n = p.n1 + p.n2, rl = p.nproj * p.r;
   const size_t total = (p.dy1 ? (size_t)p.M * (n / 128) * 8 : 0) +
                        (p.nproj > 1 ? (size_t)rl * p.k / 8 : 0) + (size_t)rl * n;
-  return launch_pdl(bwd_prep_kernel, dim3(grid_for(total, 256, 16)), dim3(256), 0, st, 0u,
+  return launch_pdl("bwd_prep_kernel", bwd_prep_kernel, dim3(grid_for(total, 256, 16)), dim3(256), 0, st, 0u,
                     p);
 }
 
@@ -119,8 +119,9 @@ cudaError_t launch_rope_cache(float *cos_sin, int max_pos, int head_dim, double 
                               cudaStream_t st) {
   const size_t total = (size_t)max_pos * (head_dim / 2);
   const int grid = grid_for(total, 256, 16);
+  launch_begin(st);
   rope_cache_kernel<<<grid, 256, 0, st>>>(cos_sin, max_pos, head_dim, theta);
-  note_launch();
+  note_launch("rope_cache_kernel", st);
   return cudaGetLastError();
 }
 
@@ -173,8 +174,9 @@ cudaError_t launch_nf4_dequant(const uint8_t *codes, const __nv_bfloat16 *absmax
                                __nv_bfloat16 *w, int n, int k, cudaStream_t st) {
   const size_t words = (size_t)n * k / 8;
   const int grid = grid_for(words, 256, 8);
+  launch_begin(st);
   nf4_dequant_kernel<<<grid, 256, 0, st>>>(codes, absmax, w, words);
-  note_launch();
+  note_launch("nf4_dequant_kernel", st);
   return cudaGetLastError();
 }
 
@@ -240,8 +242,9 @@ cudaError_t launch_nf4_quantize(const __nv_bfloat16 *w, uint8_t *codes, __nv_bfl
                                 int n, int k, cudaStream_t st) {
   const size_t blocks = (size_t)n * k / 64;
   const int grid = grid_for(blocks, 128, 8);
+  launch_begin(st);
   nf4_quantize_kernel<<<grid, 128, 0, st>>>(w, codes, absmax, blocks);
-  note_launch();
+  note_launch("nf4_quantize_kernel", st);
   return cudaGetLastError();
 }
 

@@ -388,7 +388,8 @@ static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   int tiles = 0;
   for (int q = 0; q < p.num_problems; ++q) tiles += p.pr[q].row_tiles;
-  return launch_pdl(kern, dim3((unsigned)(tiles * p.split)), dim3(192), L::TOTAL, st,
+  return launch_pdl(MN ? "lora_skinny_kernel<mn_major>" : "lora_skinny_kernel<k_major>", kern,
+                    dim3((unsigned)(tiles * p.split)), dim3(192), L::TOTAL, st,
                     (unsigned)p.split, p);
 }
 

@@ -413,7 +413,8 @@ static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3((unsigned)p.ctas), dim3(192), L::TOTAL, st, 0u, p);
+  return launch_pdl(MN ? "lora_skinny_sk_kernel<mn_major>" : "lora_skinny_sk_kernel<k_major>", kern,
+                    dim3((unsigned)p.ctas), dim3(192), L::TOTAL, st, 0u, p);
 }
 
 }  // namespace sk

@@ -126,3 +126,11 @@ def test_valid_call_without_gpu_fails_loudly():
     """No CPU fallback: a well-formed call on a machine without a GPU
     returns a CUDA error instead of computing anything."""
     assert _fwd() in (4, 5)
+
+
+def test_profile_session_rejects_bad_use_without_a_gpu_call():
+    # capacity outside [1, 65536], or ending a session that is not open,
+    # is an argument error decided on the host
+    assert lib.lora_profile_begin(0) == 1
+    assert lib.lora_profile_begin(1 << 17) == 1
+    assert lib.lora_profile_end(None, None, 0, None) == 1

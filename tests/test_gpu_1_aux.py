@@ -6,7 +6,7 @@ import torch
 
 import lora_qlora_linear_fwd_b300 as L
 import oracle as ref
-from lora_inputs import draw_tensor
+from lora_inputs import draw_projection, draw_tensor
 from tests.gpu_util import cuda, np64
 
 pytestmark = pytest.mark.gpu
@@ -66,3 +66,24 @@ def test_nf4_quantize_parity(n, k):
         ratio = w[i, j] / a
         assert abs(abs(ratio - lv[gi[i, j]]) - abs(ratio - lv[ri[i, j]])) < 1e-6
     assert len(diff) <= 1e-4 * n * k
+
+
+@pytest.mark.gpu
+def test_profile_session_times_each_launch_of_a_call():
+    """Per-launch timing: one forward call is two launches (rank pass, fused
+    GEMM), each with a positive time, in launch order."""
+    d = draw_projection(torch.Generator().manual_seed(5), 512, 512, 768, 16)
+    x, W, A, B = (cuda(d[k]) for k in ("x", "W", "A", "B"))
+    y = torch.empty(512, 768, dtype=torch.bfloat16, device="cuda")
+    ws = L.workspace(L.OP_FWD, 512, 512, 768, 16)
+    L.lora_profile_begin(8)
+    c0 = L.lora_kernel_launch_count()
+    L.lora_linear_fwd(x, W, A, B, y, 16.0, ws)
+    n = L.lora_kernel_launch_count() - c0
+    got = L.lora_profile_end(8)
+    assert n == 2 and len(got) == 2
+    assert got[0][0].startswith("lora_skinny") and got[1][0] == "lora_gemm_pair_kernel<fwd,bf16>"
+    assert all(ms > 0.0 for _, ms in got)
+    # the session is closed: a second end is an argument error
+    with pytest.raises(L.LoraError):
+        L.lora_profile_end(8)

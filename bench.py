@@ -713,12 +713,19 @@ def run_e2e(rep, args, stream):
 
 # ----------------------------------------------------------- CPU (oracle)
 def _blas_threads():
+    """Threads numpy's BLAS uses (threadpoolctl when present, else the
+    thread-count environment, else every core)."""
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
-        return int(n[0]) if n else os.cpu_count()
+        if n:
+            return int(n[0])
     except Exception:
-        return os.cpu_count()
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    return os.cpu_count()
 
 
 def oracle_step(name: str, data, M: int):
@@ -747,58 +754,83 @@ def _quantize_rows(w_rows):
     return ref.nf4_quantize(w_rows)
 
 
-def _oracle_sample(name: str, tokens: int):
+def _quantize_workload(data, wl):
+    """Oracle NF4 codes and absmax of every projection's W, row blocks spread
+    over a spawned process pool (rows quantise independently)."""
+    import oracle  # noqa: F401  (the workers import it too)
+    workers = max(1, min(os.cpu_count() or 1, 32))
+    out = {}
+    with cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn")) as ex:
+        for p in wl.projections:
+            W = data[p.name]["W"].float().numpy()
+            step = max(64, -(-W.shape[0] // workers))
+            parts = list(ex.map(_quantize_rows, [W[i:i + step]
+                                                 for i in range(0, W.shape[0], step)]))
+            out[p.name] = (np.concatenate([c for c, _ in parts]),
+                           np.concatenate([a for _, a in parts]))
+    return out
+
+
+def _oracle_sample(name: str, tokens: int, quantized=None):
     """The workload's tensors with `tokens` rows of x and dY; NF4 weights are
-    quantised by the oracle (row blocks spread over a spawned process pool:
-    preparation of the oracle's inputs, outside its timing)."""
+    the oracle's quantisation of the drawn W (preparation of the oracle's
+    inputs, outside its timing).  Returns (data, quantized)."""
     import oracle as ref
     wl = WORKLOADS[name]
     data = draw_workload(name, seed=0, M=tokens)
     if wl.nf4:
-        workers = max(1, min(os.cpu_count() or 1, 32))
-        with cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn")) as ex:
-            for p in wl.projections:
-                d = data[p.name]
-                W = d["W"].float().numpy()
-                step = max(64, -(-W.shape[0] // workers))
-                parts = list(ex.map(_quantize_rows, [W[i:i + step]
-                                                     for i in range(0, W.shape[0], step)]))
-                codes = np.concatenate([c for c, _ in parts])
-                absmax = np.concatenate([a for _, a in parts])
-                d["Wq"] = ref.nf4_dequant(codes, absmax)
-    return data
+        if quantized is None:
+            quantized = _quantize_workload(data, wl)
+        for p in wl.projections:
+            data[p.name]["Wq"] = ref.nf4_dequant(*quantized[p.name])
+    return data, quantized
 
 
-def _time_oracle(name, data, tokens, threads=None):
-    if threads is None:
-        t0 = time.perf_counter()
-        oracle_step(name, data, tokens)
-        return time.perf_counter() - t0
-    from threadpoolctl import threadpool_limits
-    with threadpool_limits(limits=threads):
-        t0 = time.perf_counter()
-        oracle_step(name, data, tokens)
-        return time.perf_counter() - t0
+def _time_oracle(name, data, tokens):
+    t0 = time.perf_counter()
+    oracle_step(name, data, tokens)
+    return time.perf_counter() - t0
 
 
-def _slice(data, tokens):
-    return {p: {k: (v[:tokens] if k in ("x", "dY") else v) for k, v in d.items()}
-            for p, d in data.items()}
+def _time_oracle_one_core(name, tokens, quantized):
+    """Oracle step time on one BLAS thread: timed in a spawned interpreter
+    whose BLAS libraries load with one thread (environment set before numpy
+    is imported there)."""
+    keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+            "BLIS_NUM_THREADS", "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in keys}
+    try:
+        for k in keys:
+            os.environ[k] = "1"
+        with cf.ProcessPoolExecutor(1, mp_context=mp.get_context("spawn")) as ex:
+            return ex.submit(_one_core_child, name, tokens, quantized).result()
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def _one_core_child(name, tokens, quantized):
+    data, _ = _oracle_sample(name, tokens, quantized)
+    return _time_oracle(name, data, tokens), _blas_threads()
 
 
 def cpu_baseline(name: str, tokens: int, tokens_1core: int):
     """The fp64 oracle as it stands, on the host cores, over a bounded token
     sample of the same workload; tokens/s = sample tokens / time.  Also one
     BLAS thread on a smaller sample."""
-    data = _oracle_sample(name, tokens)
+    data, quantized = _oracle_sample(name, tokens)
     dt = _time_oracle(name, data, tokens)
-    small = _slice(data, tokens_1core)
-    dt1 = _time_oracle(name, small, tokens_1core, threads=1)
+    del data
+    dt1, threads1 = _time_oracle_one_core(name, tokens_1core, quantized)
     return {"value": round(tokens / dt, 2), "unit": "tokens/s", "cores": _blas_threads(),
             "cpu_count": os.cpu_count(), "kind": "oracle",
             "sample": f"{tokens} of {WORKLOADS[name].M} tokens, all projections, fwd+bwd in "
                       f"fp64 numpy ({dt:.1f} s)",
-            "one_core": {"value": round(tokens_1core / dt1, 2), "unit": "tokens/s", "cores": 1,
+            "one_core": {"value": round(tokens_1core / dt1, 2), "unit": "tokens/s",
+                         "cores": threads1,
                          "sample": f"{tokens_1core} tokens, all projections, fwd+bwd, one BLAS "
                                    f"thread ({dt1:.1f} s)"}}
 
@@ -808,7 +840,7 @@ def run_reference(args, world, rank):
         return None
     wl = WORKLOADS[args.workload]
     tokens = args.ref_tokens
-    data = _oracle_sample(args.workload, tokens)
+    data, _ = _oracle_sample(args.workload, tokens)
     for _ in range(args.warmup):
         oracle_step(args.workload, data, tokens)
     times = []

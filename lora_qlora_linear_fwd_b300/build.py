@@ -1,9 +1,13 @@
-"""Build the in-tree shared library ``_lib/liblora_b300.so`` with nvcc.
+"""Build the in-tree shared libraries with nvcc.
 
-Every ``csrc/*.cu`` file is compiled for sm_103a only
-(``-gencode arch=compute_103a,code=sm_103a``) and linked with the static CUDA
-runtime, so the library loads on a machine without a GPU (the C ABI then
-reports errors instead of launching).  Run ``python
+``_lib/liblora_b300.so`` is the product: every ``csrc/*.cu`` file compiled
+for sm_103a only (``-gencode arch=compute_103a,code=sm_103a``) and linked
+with the static CUDA runtime, so the library loads on a machine without a
+GPU (the C ABI then reports errors instead of launching).
+``_lib/liblora_b300_testhooks.so`` is the same sources built with
+``-DLORA_TEST_HOOKS``: it adds the test-only entry point of
+``include/lora_b300_test_hooks.h``, which lets a test make a device-side
+wait run out; nothing but that test loads it.  Run ``python
 lora_qlora_linear_fwd_b300/build.py`` (this file imports nothing from the
 package, so it also works while the library is missing or stale).
 """
@@ -23,6 +27,12 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIBNAME = "liblora_b300.so"
 OBJDIR = os.path.join(ROOT, "_build", "obj")
+# variant -> (library file, object directory, extra nvcc flags)
+VARIANTS = {
+    "product": (LIBNAME, OBJDIR, []),
+    "testhooks": ("liblora_b300_testhooks.so", os.path.join(ROOT, "_build", "obj_testhooks"),
+                  ["-DLORA_TEST_HOOKS"]),
+}
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
@@ -36,8 +46,8 @@ def nvcc() -> str:
     return exe
 
 
-def lib_path() -> str:
-    return os.path.join(LIBDIR, LIBNAME)
+def lib_path(variant: str = "product") -> str:
+    return os.path.join(LIBDIR, VARIANTS[variant][0])
 
 
 def _sources():
@@ -56,8 +66,8 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src: str, obj: str, log_dir: str) -> str:
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, obj: str, log_dir: str, extra=()) -> str:
+    cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     log = os.path.join(log_dir, os.path.basename(src) + ".ptxas.txt")
     with open(log, "w") as f:
@@ -67,33 +77,43 @@ def _compile(src: str, obj: str, log_dir: str) -> str:
     return obj
 
 
-def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -> str:
-    """Compile (if stale) and link the library; return its path."""
+def build_variant(variant: str, force: bool = False, jobs: int | None = None) -> str:
+    """Compile (if stale) and link one library variant; return its path."""
+    libname, objdir, extra = VARIANTS[variant]
     os.makedirs(LIBDIR, exist_ok=True)
-    os.makedirs(OBJDIR, exist_ok=True)
+    os.makedirs(objdir, exist_ok=True)
     hdrs = _headers()
     work = []
     objs = []
     for src in _sources():
-        obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, *hdrs]):
             work.append((src, obj))
     if work:
         jobs = jobs or min(len(work), os.cpu_count() or 4)
         with cf.ThreadPoolExecutor(jobs) as ex:
-            futs = [ex.submit(_compile, s, o, OBJDIR) for s, o in work]
+            futs = [ex.submit(_compile, s, o, objdir, extra) for s, o in work]
             for f in futs:
                 f.result()
-    out = lib_path()
+    out = os.path.join(LIBDIR, libname)
     if force or work or _stale(out, objs):
         cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", out, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
-    if verbose:
-        print(out)
     return out
+
+
+def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -> str:
+    """Build every variant; return the product library's path."""
+    with cf.ThreadPoolExecutor(len(VARIANTS)) as ex:
+        futs = {v: ex.submit(build_variant, v, force, jobs) for v in VARIANTS}
+        paths = {v: f.result() for v, f in futs.items()}
+    if verbose:
+        for p in paths.values():
+            print(p)
+    return paths["product"]
 
 
 if __name__ == "__main__":

@@ -144,6 +144,8 @@ int rank_pad(int rl) { return rl <= 16 ? 16 : (rl <= 32 ? 32 : (rl <= 64 ? 64 : 
 bool rank_ok(int r) { return r == 8 || r == 16 || r == 32 || r == 64; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 constexpr int kBN = 256;
+// Time of an NF4 GEMM tile of two m-blocks, in tiles of one m-block.
+constexpr double kMb2TileCost = 1.5;
 constexpr size_t kStatusBytes = 256;
 
 lora_status_t check_weight(const lora_weight_t &W) {
@@ -169,14 +171,14 @@ lora_status_t check_shape(int M, int k, int n, int r) {
 lora_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
 
 // ------------------------------------------------------------- schedule
-// Persistent GEMM schedule: as many CTA pairs as fit (one per two SMs),
-// grouped raster of 8 m-blocks.
-Schedule make_schedule(int m_blocks, int n_tiles, int slots) {
-  const long long total = (long long)m_blocks * n_tiles;
+// Persistent GEMM schedule over tiles of `mb` m-blocks: as many CTA pairs
+// as fit (one per two SMs), grouped raster of 8 m-blocks (8/mb tile rows).
+Schedule make_schedule(int m_tiles, int n_tiles, int slots, int mb) {
+  const long long total = (long long)m_tiles * n_tiles;
   Schedule s;
-  s.m_blocks = m_blocks;
+  s.m_blocks = m_tiles;
   s.n_tiles = n_tiles;
-  s.group_m = std::max(1, std::min(m_blocks, 8));
+  s.group_m = std::max(1, std::min(m_tiles, 8 / mb));
   s.workers = (int)std::max<long long>(1, std::min<long long>(slots, total));
   return s;
 }
@@ -277,15 +279,28 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
   }
   p.M = o.M;
   p.K = o.Kred;
-  const int slots = gemm_pair_capacity(o.mode, o.rope, nf4);
+  // Tiles of one or two m-blocks.  NF4: a two-m-block tile decodes each W
+  // K-block once for 512 rows instead of 256; it is taken unless its coarser
+  // waves of tiles cost more than that saves (an mb = 2 tile is timed at
+  // kMb2TileCost mb = 1 tiles).
+  const int m_blocks = (o.M + 255) / 256;
+  int mb = 1;
+  int slots = gemm_pair_capacity(o.mode, o.rope, nf4, 1);
   if (slots < 1) return LORA_ERR_CUDA;
-  p.sched = make_schedule((o.M + 255) / 256, tiles, slots);
+  if (nf4) {
+    const int slots2 = gemm_pair_capacity(o.mode, o.rope, nf4, 2);
+    if (slots2 < 1) return LORA_ERR_CUDA;
+    const long long w1 = ((long long)m_blocks * tiles + slots - 1) / slots;
+    const long long w2 = ((long long)((m_blocks + 1) / 2) * tiles + slots2 - 1) / slots2;
+    if ((double)w2 * kMb2TileCost < (double)w1) mb = 2, slots = slots2;
+  }
+  p.sched = make_schedule((m_blocks + mb - 1) / mb, tiles, slots, mb);
   p.accumulate = o.accumulate;
   p.positions = o.positions;
   p.cos_sin = o.cos_sin;
   p.max_pos = o.max_pos;
   p.status = o.status;
-  return cuda_status(launch_gemm_pair(p, o.mode, o.rope, nf4, p.sched.workers, st));
+  return cuda_status(launch_gemm_pair(p, o.mode, o.rope, nf4, mb, p.sched.workers, st));
 }
 
 // ------------------------------------------------------------ rank passes

@@ -9,11 +9,16 @@
 // tile's reduction, streamed through the same pipeline slots as the main
 // K-blocks.  Output tiles are therefore independent of each other.
 //
-// A cluster of two CTAs computes one 256 x 256 output tile with
-// tcgen05.mma.cta_group::2: CTA c (c = 0, 1) holds rows [128c, 128c+128) of
-// the activation tile and rows [128c, 128c+128) of the W tile (the N half);
-// the tensor cores of both SMs work on the pair tile, and each SM stages
-// half of the W bytes a one-SM 128 x 256 tile would need.
+// A cluster of two CTAs computes one (256·MB) x 256 output tile with
+// tcgen05.mma.cta_group::2: for each of the tile's MB m-blocks (256 rows),
+// CTA c (c = 0, 1) holds rows [128c, 128c+128) of the m-block's activation
+// rows, and rows [128c, 128c+128) of the W tile (the N half); the tensor
+// cores of both SMs work on the pair tile, and each SM stages half of the W
+// bytes a one-SM 128 x 256 tile would need.  MB = 1: the two 256-column
+// TMEM accumulators alternate between tiles, so a tile's epilogue overlaps
+// the next tile's main loop.  MB = 2: each W K-block (decoded once, for NF4)
+// feeds both m-blocks, one accumulator each; the MMA of a new tile waits for
+// the drain of the accumulator it writes, m-block 0 being drained first.
 //
 // Roles (both CTAs unless noted; NF4 rings as in PairSmem):
 //   warp 0     TMA producer: own halves of x/dY and (bf16) of W per main
@@ -22,9 +27,7 @@
 //              barriers.
 //   warp 1     TMEM owner (pair allocation, 2 x 256 columns); in the even
 //              CTA also the single MMA issuer, whose commits are multicast
-//              to both CTAs.  Accumulators alternate between the two
-//              256-column buffers so a tile's epilogue overlaps the next
-//              tile's main loop.
+//              to both CTAs.
 //   warps 2-5  epilogue of the CTA's own 128 rows: TMEM -> (RoPE) -> bf16
 //              -> shared-memory staging -> TMA bulk store of whole lines
 //              (dX with accumulate: plain loads/stores adding to the values
@@ -56,15 +59,15 @@ constexpr int kNf4DecodeWarps = 8;
 // unambiguous for a waiter at most one phase ahead of the barrier, so each
 // waiter must see every phase of its barrier: the code and W rings have an
 // even number of slots, so that each slot belongs to one group.
-template <bool NF4, bool STAGED_ROPE = false>
+template <bool NF4, bool STAGED_ROPE = false, int MB = 1>
 struct PairSmem {
-  static constexpr int X_BYTES = 128 * 128;  // own 128 rows x 64 K
+  static constexpr int X_BYTES = 128 * 128;  // own 128 rows x 64 K of one m-block
   static constexpr int W_BYTES = 128 * 128;  // own 128 N-rows x 64 K
   static constexpr int C_BYTES = NF4 ? 128 * 32 : 0;  // own half of a K-block's codes
-  static constexpr int OFF_W = X_BYTES;      // bf16: W inside the stage
-  static constexpr int STAGE_BYTES = X_BYTES + (NF4 ? 0 : W_BYTES);
+  static constexpr int OFF_W = MB * X_BYTES;  // bf16: W inside the stage
+  static constexpr int STAGE_BYTES = MB * X_BYTES + (NF4 ? 0 : W_BYTES);
   static constexpr int C_STAGES = NF4 ? 4 : 0;
-  static constexpr int W_STAGES = NF4 ? 6 : 0;
+  static constexpr int W_STAGES = NF4 ? (MB == 2 ? 4 : 6) : 0;
   static constexpr int CRING_BYTES = C_STAGES * C_BYTES;
   static constexpr int WRING_BYTES = W_STAGES * W_BYTES;
   static constexpr int EPI_BYTES = 4 * 2 * 2048;  // per epilogue warp: two 2 KB staging buffers
@@ -147,12 +150,13 @@ struct Nf4Cursor {
   }
 };
 
-template <int MODE, bool NF4, bool ROPE>
+template <int MODE, bool NF4, bool ROPE, int MB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1)
     lora_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   // RoPE cos / sin staged in shared memory (bf16 W; the NF4 rings leave no room)
   constexpr bool STAGED = ROPE && !NF4;
-  using L = PairSmem<NF4, STAGED>;
+  using L = PairSmem<NF4, STAGED, MB>;
+  static_assert(MB == 1 || MB == 2, "m-blocks per tile");
   constexpr int STAGES = L::STAGES;
   constexpr int BN = 256;
   constexpr bool DX = MODE == kModeDx;
@@ -240,7 +244,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
         const GemmGroup &G = p.grp[group_of(p, nt)];
         const int n0 = (nt - G.tile_begin) * BN;
         const int nh = n0 + (int)crank * 128;  // first N index of this CTA's half
-        const int row0 = m * 256 + (int)crank * 128;
+        const int row0 = m * (256 * MB) + (int)crank * 128;  // m-block mb: + 256·mb
         const int ne = DX ? p.grp[0].n_extra : G.n_extra;
         for (int kb = 0; kb < nk + ne; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
@@ -252,8 +256,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
           if (kb < nk) {
             if (leader)
               mbar_arrive_expect_tx(bar_full + 8 * stage,
-                                    2 * (L::X_BYTES + (NF4 ? 0 : L::W_BYTES)));
-            tma_load_2d_pair(sx, &p.tm_act, fb, kb * kBK, row0);
+                                    2 * (MB * L::X_BYTES + (NF4 ? 0 : L::W_BYTES)));
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb)
+              tma_load_2d_pair(sx + mb * L::X_BYTES, &p.tm_act, fb, kb * kBK, row0 + mb * 256);
             // DX: the reduction may run over two projections' W (K-groups)
             const int gk = (DX && p.kgroups > 1 && kb >= p.ksplit) ? 1 : 0;
             const CUtensorMap *tw = DX ? &p.grp[gk].tm_w : &G.tm_w;
@@ -273,12 +279,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
             if constexpr (NF4) {
               // B / A goes straight into the W ring (copied by the decode
               // group that owns the slot, see the code producer)
-              if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * L::X_BYTES);
-              tma_load_2d_pair(sx, &p.tm_sv, fb, R.sv_col + e * kBK, row0);
+              if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * MB * L::X_BYTES);
+#pragma unroll
+              for (int mb = 0; mb < MB; ++mb)
+                tma_load_2d_pair(sx + mb * L::X_BYTES, &p.tm_sv, fb, R.sv_col + e * kBK,
+                                 row0 + mb * 256);
             } else {
               if (leader)
-                mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (L::X_BYTES + L::W_BYTES));
-              tma_load_2d_pair(sx, &p.tm_sv, fb, R.sv_col + e * kBK, row0);
+                mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (MB * L::X_BYTES + L::W_BYTES));
+#pragma unroll
+              for (int mb = 0; mb < MB; ++mb)
+                tma_load_2d_pair(sx + mb * L::X_BYTES, &p.tm_sv, fb, R.sv_col + e * kBK,
+                                 row0 + mb * 256);
               if constexpr (DX) {  // A [rl, k] MN-major: 2 boxes [64 k-columns x 64 rank rows]
                 tma_load_2d_pair(sx + L::OFF_W, &R.tm_b, fb, nh, e * kBK);
                 tma_load_2d_pair(sx + L::OFF_W + 8192, &R.tm_b, fb, nh + 64, e * kBK);
@@ -314,14 +326,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       for (it.init(p.sched, pair); ok && it.valid(); it.next(), ++tile_count) {
         const GemmGroup &G = p.grp[group_of(p, it.nt())];
         const int ne = DX ? p.grp[0].n_extra : G.n_extra;
-        const int buf = tile_count & 1;
-        const uint32_t t_acc = tmem + buf * BN;
-        if (used[buf] > 0 &&
-            !mbar_wait_cluster(bar_acc_empty + 8 * buf, (used[buf] - 1) & 1, abort_flag, p.status))
-          break;
-        ++used[buf];
+        const int buf = tile_count & 1;  // MB = 1: the accumulator of this tile
+        if constexpr (MB == 1) {
+          if (used[buf] > 0 && !mbar_wait_cluster(bar_acc_empty + 8 * buf, (used[buf] - 1) & 1,
+                                                  abort_flag, p.status))
+            break;
+          ++used[buf];
+        }
         tc_fence_after();
-        for (int kb = 0; kb < nk + ne; ++kb) {
+        for (int kb = 0; ok && kb < nk + ne; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) {
             ok = false;
             break;
@@ -334,15 +347,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
           const uint32_t sx = base + stage * L::STAGE_BYTES;
           const uint32_t sw = NF4 ? base + L::OFF_WRING + wslot * L::W_BYTES : sx + L::OFF_W;
 #pragma unroll
-          for (int ks = 0; ks < kBK / 16; ++ks) {
-            const uint64_t da = make_sdesc(sx + ks * 32, 16, 1024, kSw128);
-            uint64_t dw;
-            if constexpr (DX)  // MN-major: 16 K-rows per step; two 64-wide blocks 8 KB apart
-              dw = make_sdesc(sw + ks * 2048, 8192, 1024, kSw128);
-            else
-              dw = make_sdesc(sw + ks * 32, 16, 1024, kSw128);
-            tc_mma_pair(t_acc, da, dw, idesc, (kb | ks) != 0 ? 1u : 0u);
+          for (int mb = 0; mb < MB; ++mb) {
+            if (MB == 2 && kb == 0 && tile_count > 0) {
+              // accumulator mb is free once the previous tile's m-block mb is drained
+              if (!mbar_wait_cluster(bar_acc_empty + 8 * mb, (tile_count - 1) & 1, abort_flag,
+                                     p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t t_acc = tmem + (MB == 1 ? buf : mb) * BN;
+#pragma unroll
+            for (int ks = 0; ks < kBK / 16; ++ks) {
+              const uint64_t da = make_sdesc(sx + mb * L::X_BYTES + ks * 32, 16, 1024, kSw128);
+              uint64_t dw;
+              if constexpr (DX)  // MN-major: 16 K-rows per step; two 64-wide blocks 8 KB apart
+                dw = make_sdesc(sw + ks * 2048, 8192, 1024, kSw128);
+              else
+                dw = make_sdesc(sw + ks * 32, 16, 1024, kSw128);
+              tc_mma_pair(t_acc, da, dw, idesc, (kb | ks) != 0 ? 1u : 0u);
+            }
+            // MB = 2: m-block mb's accumulator is complete after its last
+            // K-block, before the other m-block's MMAs of that K-block
+            if (MB == 2 && kb == nk + ne - 1) tc_commit_pair(bar_acc_full + 8 * mb, kBoth);
           }
+          if (!ok) break;
           tc_commit_pair(bar_empty + 8 * stage, kBoth);
           if (++stage == STAGES) stage = 0, phase ^= 1u;
           if constexpr (NF4) {
@@ -351,7 +381,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
           }
         }
         if (!ok) break;
-        tc_commit_pair(bar_acc_full + 8 * buf, kBoth);
+        if constexpr (MB == 1) tc_commit_pair(bar_acc_full + 8 * buf, kBoth);
       }
       if (*abort_flag) {
         tc_commit_pair(bar_drain, 0x1);
@@ -370,35 +400,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     bool cs_pending = false;  // a staged half has not been waited for
     int tile_count = 0;
     TileIter it;
-    for (it.init(p.sched, pair); it.valid(); it.next(), ++tile_count) {
+    bool ok = true;
+    for (it.init(p.sched, pair); ok && it.valid(); it.next(), ++tile_count) {
       const int m = it.m(), nt = it.nt();
       const GemmGroup &G = p.grp[group_of(p, nt)];
       const int n0 = (nt - G.tile_begin) * BN;
-      const int grow = m * 256 + (int)crank * 128 + row;
-      const bool row_ok = grow < p.M;
-      const int buf = tile_count & 1;
-      const float *cs = ROPE ? rope_row(p, grow, row_ok) : nullptr;
-      if constexpr (STAGED) {  // fetched while the accumulator is still being produced
-        rope_stage(cs, 0, srow, cs_bar, lane);
-        cs_pending = true;
-      }
-      if (!warp_wait(bar_acc_full + 8 * buf, (tile_count >> 1) & 1, abort_flag, p.status)) break;
-      tc_fence_after();
       const int ncols = min(BN, G.ncols - n0);
-      if (DX && p.accumulate) {  // read-modify-write of dX: plain loads and stores
-        __nv_bfloat16 *orow = G.out + (size_t)(row_ok ? grow : 0) * G.ncols + n0;
-        epi_store_tile<BN, false>(tmem + t_lane + buf * BN, orow, row_ok, ncols, true, nullptr);
-      } else {
-        if (!epi_store_tile_tma<BN, ROPE, STAGED>(tmem + t_lane + buf * BN, epi_buf, &G.tm_out, n0,
-                                                  m * 256 + (int)crank * 128 + q * 32, ncols, cs,
-                                                  srow, cs_bar, cs_phase, lane, abort_flag,
-                                                  p.status))
+#pragma unroll 1
+      for (int mb = 0; mb < MB; ++mb) {
+        const int acc = MB == 1 ? (tile_count & 1) : mb;
+        const uint32_t par = MB == 1 ? (uint32_t)(tile_count >> 1) & 1u : (uint32_t)tile_count & 1u;
+        const int wrow0 = (m * MB + mb) * 256 + (int)crank * 128 + q * 32;  // warp's first row
+        const int grow = wrow0 + lane;
+        const bool row_ok = grow < p.M;
+        const float *cs = ROPE ? rope_row(p, grow, row_ok) : nullptr;
+        if constexpr (STAGED) {  // fetched while the accumulator is still being produced
+          rope_stage(cs, 0, srow, cs_bar, lane);
+          cs_pending = true;
+        }
+        if (!warp_wait(bar_acc_full + 8 * acc, par, abort_flag, p.status)) {
+          ok = false;
           break;
-        cs_pending = false;
+        }
+        tc_fence_after();
+        if (DX && p.accumulate) {  // read-modify-write of dX: plain loads and stores
+          __nv_bfloat16 *orow = G.out + (size_t)(row_ok ? grow : 0) * G.ncols + n0;
+          epi_store_tile<BN, false>(tmem + t_lane + acc * BN, orow, row_ok, ncols, true, nullptr);
+        } else {
+          if (!epi_store_tile_tma<BN, ROPE, STAGED>(tmem + t_lane + acc * BN, epi_buf, &G.tm_out,
+                                                    n0, wrow0, ncols, cs, srow, cs_bar, cs_phase,
+                                                    lane, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          cs_pending = false;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lead_acc_empty + 8 * acc);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(lead_acc_empty + 8 * buf);
     }
     if (STAGED && cs_pending)  // no copy may land after the CTA exits
       mbar_wait_quiet(cs_bar, cs_phase, 100000000ull);
@@ -585,26 +625,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   }
 }
 
-template <int MODE, bool NF4, bool ROPE>
+template <int MODE, bool NF4, bool ROPE, int MB>
 static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t st) {
-  using L = PairSmem<NF4, ROPE && !NF4>;
-  auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE>;
+  using L = PairSmem<NF4, ROPE && !NF4, MB>;
+  auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE, MB>;
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
   if (e != cudaSuccess) return e;
   constexpr const char *name =
-      MODE == kModeFwd ? (NF4 ? (ROPE ? "lora_gemm_pair_kernel<fwd,nf4,rope>" : "lora_gemm_pair_kernel<fwd,nf4>")
-                              : (ROPE ? "lora_gemm_pair_kernel<fwd,bf16,rope>" : "lora_gemm_pair_kernel<fwd,bf16>"))
-                       : (NF4 ? "lora_gemm_pair_kernel<dx,nf4>" : "lora_gemm_pair_kernel<dx,bf16>");
+      MODE == kModeFwd
+          ? (NF4 ? (ROPE ? (MB == 2 ? "lora_gemm_pair_kernel<fwd,nf4,rope,mb2>"
+                                    : "lora_gemm_pair_kernel<fwd,nf4,rope>")
+                         : (MB == 2 ? "lora_gemm_pair_kernel<fwd,nf4,mb2>"
+                                    : "lora_gemm_pair_kernel<fwd,nf4>"))
+                 : (ROPE ? (MB == 2 ? "lora_gemm_pair_kernel<fwd,bf16,rope,mb2>"
+                                    : "lora_gemm_pair_kernel<fwd,bf16,rope>")
+                         : (MB == 2 ? "lora_gemm_pair_kernel<fwd,bf16,mb2>"
+                                    : "lora_gemm_pair_kernel<fwd,bf16>")))
+          : (NF4 ? (MB == 2 ? "lora_gemm_pair_kernel<dx,nf4,mb2>" : "lora_gemm_pair_kernel<dx,nf4>")
+                 : (MB == 2 ? "lora_gemm_pair_kernel<dx,bf16,mb2>" : "lora_gemm_pair_kernel<dx,bf16>"));
   return launch_pdl(name, kern, dim3(2 * pairs), dim3(pair_threads(NF4)), L::TOTAL, st, 0u, p);
 }
 
 // Co-resident CTA pairs of one kernel on the current device (cached per
 // device; 0 if the query fails).
-template <int MODE, bool NF4, bool ROPE>
+template <int MODE, bool NF4, bool ROPE, int MB>
 static int pair_capacity() {
-  using L = PairSmem<NF4, ROPE && !NF4>;
-  auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE>;
+  using L = PairSmem<NF4, ROPE && !NF4, MB>;
+  auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE, MB>;
   static std::atomic<uint64_t> attr_done{0};
   static std::atomic<int> cached[kMaxDevices];  // pairs + 1; 0: not queried yet
   int dev = 0;
@@ -626,41 +674,50 @@ static int pair_capacity() {
   return n;
 }
 
+// Launch (cap == nullptr) or capacity query (*cap) of the variant
+// (MODE, NF4, rope, mb).  RoPE applies to the forward only; two m-blocks
+// per tile are compiled for NF4 weights.
 template <int MODE, bool NF4>
-static cudaError_t pair_dispatch(const GemmParams &p, bool rope, int pairs, int *cap,
+static cudaError_t pair_dispatch(const GemmParams &p, bool rope, int mb, int pairs, int *cap,
                                  cudaStream_t st) {
-  if (MODE == kModeFwd && rope) {
-    if (cap) {
-      *cap = pair_capacity<MODE, NF4, true>();
-      return cudaSuccess;
+  constexpr bool kRope = MODE == kModeFwd;
+  if constexpr (NF4) {
+    if (mb == 2) {
+      if (kRope && rope) {
+        if (cap) return *cap = pair_capacity<MODE, NF4, kRope, 2>(), cudaSuccess;
+        return launch_pair_one<MODE, NF4, kRope, 2>(p, pairs, st);
+      }
+      if (cap) return *cap = pair_capacity<MODE, NF4, false, 2>(), cudaSuccess;
+      return launch_pair_one<MODE, NF4, false, 2>(p, pairs, st);
     }
-    return launch_pair_one<MODE, NF4, MODE == kModeFwd>(p, pairs, st);
   }
-  if (cap) {
-    *cap = pair_capacity<MODE, NF4, false>();
-    return cudaSuccess;
+  if (mb != 1) return cudaErrorInvalidValue;
+  if (kRope && rope) {
+    if (cap) return *cap = pair_capacity<MODE, NF4, kRope, 1>(), cudaSuccess;
+    return launch_pair_one<MODE, NF4, kRope, 1>(p, pairs, st);
   }
-  return launch_pair_one<MODE, NF4, false>(p, pairs, st);
+  if (cap) return *cap = pair_capacity<MODE, NF4, false, 1>(), cudaSuccess;
+  return launch_pair_one<MODE, NF4, false, 1>(p, pairs, st);
 }
 
-cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int pairs,
-                             cudaStream_t st) {
+cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int mb,
+                             int pairs, cudaStream_t st) {
   if (mode == kModeFwd)
-    return nf4 ? pair_dispatch<kModeFwd, true>(p, rope, pairs, nullptr, st)
-               : pair_dispatch<kModeFwd, false>(p, rope, pairs, nullptr, st);
-  return nf4 ? pair_dispatch<kModeDx, true>(p, false, pairs, nullptr, st)
-             : pair_dispatch<kModeDx, false>(p, false, pairs, nullptr, st);
+    return nf4 ? pair_dispatch<kModeFwd, true>(p, rope, mb, pairs, nullptr, st)
+               : pair_dispatch<kModeFwd, false>(p, rope, mb, pairs, nullptr, st);
+  return nf4 ? pair_dispatch<kModeDx, true>(p, false, mb, pairs, nullptr, st)
+             : pair_dispatch<kModeDx, false>(p, false, mb, pairs, nullptr, st);
 }
 
-int gemm_pair_capacity(int mode, bool rope, bool nf4) {
+int gemm_pair_capacity(int mode, bool rope, bool nf4, int mb) {
   int cap = 0;
   GemmParams dummy;
   if (mode == kModeFwd)
-    nf4 ? pair_dispatch<kModeFwd, true>(dummy, rope, 0, &cap, nullptr)
-        : pair_dispatch<kModeFwd, false>(dummy, rope, 0, &cap, nullptr);
+    nf4 ? pair_dispatch<kModeFwd, true>(dummy, rope, mb, 0, &cap, nullptr)
+        : pair_dispatch<kModeFwd, false>(dummy, rope, mb, 0, &cap, nullptr);
   else
-    nf4 ? pair_dispatch<kModeDx, true>(dummy, false, 0, &cap, nullptr)
-        : pair_dispatch<kModeDx, false>(dummy, false, 0, &cap, nullptr);
+    nf4 ? pair_dispatch<kModeDx, true>(dummy, false, mb, 0, &cap, nullptr)
+        : pair_dispatch<kModeDx, false>(dummy, false, mb, 0, &cap, nullptr);
   return cap;
 }
 

@@ -139,10 +139,11 @@ cudaError_t launch_pdl(const char *name, void (*kern)(KArgs...), dim3 grid, dim3
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Two-SM (CTA pair) fused GEMM: 256 x 256 tiles over `pairs` persistent pairs.
-cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int pairs,
-                             cudaStream_t st);
-int gemm_pair_capacity(int mode, bool rope, bool nf4);  // max co-resident pairs
+// Two-SM (CTA pair) fused GEMM: (256·mb) x 256 tiles over `pairs` persistent
+// pairs; p.sched counts tiles of mb m-blocks.  mb = 2 exists for NF4 weights.
+cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int mb,
+                             int pairs, cudaStream_t st);
+int gemm_pair_capacity(int mode, bool rope, bool nf4, int mb);  // max co-resident pairs
 
 // Skinny rank-r products on the tensor cores:
 //   KMAJOR  (v, u):  g[t][j] = Σ_c P[t,c]·Q[j,c]            P = x or dY, Q = A or Bᵀ

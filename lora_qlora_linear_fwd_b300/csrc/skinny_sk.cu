@@ -47,13 +47,28 @@ LORA_DEV void st_release_u64(unsigned long long *p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+#ifdef LORA_TEST_HOOKS
+// Test-only build (liblora_b300_testhooks.so): the host can shorten the flag
+// wait's limit and name one CTA that parks its partial without raising its
+// flag (lora_test_stream_k_hooks), so that a test makes the finisher's wait
+// run out and checks the reported status.  The product library has neither.
+static __device__ unsigned long long g_flag_wait_limit_ns = kWaitLimitNs;
+static __device__ int g_skip_flag_cta = -1;
+LORA_DEV uint64_t flag_wait_limit_ns() { return g_flag_wait_limit_ns; }
+LORA_DEV bool flag_skipped(int cta) { return cta == g_skip_flag_cta; }
+#else
+LORA_DEV uint64_t flag_wait_limit_ns() { return kWaitLimitNs; }
+LORA_DEV bool flag_skipped(int) { return false; }
+#endif
+
 // Bounded wait for another CTA's flag to carry `epoch`.
 LORA_DEV bool wait_flag(const unsigned long long *f, unsigned long long epoch,
                         volatile int *abort_flag, uint32_t *status) {
   const uint64_t t0 = global_timer_ns();
+  const uint64_t limit = flag_wait_limit_ns();
   while (ld_acquire_u64(f) != epoch) {
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit) {
       *abort_flag = 1;
       atomicOr(status, kDevTimeout);
       return false;
@@ -324,7 +339,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
         __threadfence();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_parked);
-        if (leader && mbar_wait(bar_parked, 0, abort_flag, p.status))
+        if (leader && mbar_wait(bar_parked, 0, abort_flag, p.status) && !flag_skipped(cta))
           st_release_u64(p.flags + cta, p.epoch);
       } else {
         // the tile's first chunks: add the partials of the CTAs that took
@@ -437,3 +452,18 @@ cudaError_t launch_skinny_sk(const SkinnyParams &p, bool mn_major, int rp, cudaS
 }
 
 }  // namespace lora
+
+#ifdef LORA_TEST_HOOKS
+// Test-only entry point of liblora_b300_testhooks.so (declared in
+// include/lora_b300_test_hooks.h): sets the stream-K flag wait's limit and
+// the CTA that skips raising its flag (-1: none).  Synchronous.
+extern "C" lora_status_t lora_test_stream_k_hooks(unsigned long long wait_limit_ns,
+                                                  int skip_flag_cta) {
+  if (cudaMemcpyToSymbol(lora::sk::g_flag_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns)) !=
+          cudaSuccess ||
+      cudaMemcpyToSymbol(lora::sk::g_skip_flag_cta, &skip_flag_cta, sizeof(skip_flag_cta)) !=
+          cudaSuccess)
+    return LORA_ERR_CUDA;
+  return LORA_OK;
+}
+#endif

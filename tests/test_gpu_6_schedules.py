@@ -1,0 +1,137 @@
+"""GPU parity of the schedule variants the host picks by shape, each asserted
+to have run (kernel names from the library's per-launch timing session):
+
+* the NF4 fused GEMM with two m-blocks per tile (each decoded W K-block
+  feeding 512 rows) in the forward and in dX, with a ragged second m-block;
+* NF4 weights holding an all-zero 64-block (absmax 0) and a block whose
+  absmax is a bf16 subnormal, through the fused forward and dX;
+* the rank passes on their cluster schedule and on their stream-K schedule.
+"""
+import numpy as np
+import pytest
+import torch
+
+import lora_qlora_linear_fwd_b300 as L
+import oracle as ref
+from lora_inputs import draw_projection
+from tests.gpu_util import TOL_BF16, TOL_F32, cuda, np64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+ALPHA = 16.0
+
+
+def _nf4(W):
+    codes, absmax = ref.nf4_quantize(np64(W))
+    c = cuda(torch.from_numpy(codes))
+    a = cuda(torch.from_numpy(absmax.astype(np.float32)).to(torch.bfloat16))
+    return codes, absmax, c, a
+
+
+def _profiled(fn, cap=16):
+    L.lora_profile_begin(cap)
+    try:
+        fn()
+    finally:
+        got = L.lora_profile_end(cap)
+    return [name for name, _ in got]
+
+
+def _fwd(d, W, r):
+    x, A, B = cuda(d["x"]), cuda(d["A"]), cuda(d["B"])
+    M, k = x.shape
+    n = d["W"].shape[0]
+    y = torch.full((M, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = L.workspace(L.OP_FWD, M, k, n, r)
+    names = _profiled(lambda: L.lora_linear_fwd(x, W, A, B, y, ALPHA, ws))
+    torch.cuda.synchronize()
+    assert L.lora_read_device_status(ws) == 0
+    return y, names
+
+
+def _bwd(d, W, r):
+    x, A, B, dy = cuda(d["x"]), cuda(d["A"]), cuda(d["B"]), cuda(d["dY"])
+    M, k = x.shape
+    n = dy.shape[1]
+    dx = torch.full((M, k), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dA = torch.full((r, k), float("nan"), dtype=torch.float32, device="cuda")
+    dB = torch.full((n, r), float("nan"), dtype=torch.float32, device="cuda")
+    ws = L.workspace(L.OP_BWD, M, k, n, r)
+    names = _profiled(lambda: L.lora_linear_bwd(x, W, A, B, dy, dx, dA, dB, ALPHA, ws))
+    torch.cuda.synchronize()
+    assert L.lora_read_device_status(ws) == 0
+    return (dx, dA, dB), names
+
+
+def test_nf4_forward_with_two_m_blocks_per_tile():
+    # 2 m-blocks (the second holds 44 rows) x 74 n-tiles (the last 64 wide):
+    # one wave of 512-row tiles beats two waves of 256-row tiles
+    M, k, n, r = 300, 512, 74 * 256 - 192, 16
+    d = draw_projection(torch.Generator().manual_seed(61), M, k, n, r)
+    codes, absmax, c, a = _nf4(d["W"])
+    y, names = _fwd(d, L.nf4_weight(c, a), r)
+    assert names[-1] == "lora_gemm_pair_kernel<fwd,nf4,mb2>", names
+    want = ref.lora_fwd(np64(d["x"]), ref.nf4_dequant(codes, absmax), np64(d["A"]),
+                        np64(d["B"]), ALPHA)
+    assert rel_err(np64(y), want) <= TOL_BF16
+
+
+def test_nf4_backward_dx_with_two_m_blocks_per_tile():
+    M, k, n, r = 300, 74 * 256 - 192, 512, 16
+    d = draw_projection(torch.Generator().manual_seed(62), M, k, n, r)
+    codes, absmax, c, a = _nf4(d["W"])
+    got, names = _bwd(d, L.nf4_weight(c, a), r)
+    assert "lora_gemm_pair_kernel<dx,nf4,mb2>" in names, names
+    want = ref.lora_bwd(np64(d["x"]), ref.nf4_dequant(codes, absmax), np64(d["A"]),
+                        np64(d["B"]), np64(d["dY"]), ALPHA)
+    assert rel_err(np64(got[0]), want[0]) <= TOL_BF16
+    assert rel_err(np64(got[1]), want[1]) <= TOL_F32
+    assert rel_err(np64(got[2]), want[2]) <= TOL_F32
+
+
+@pytest.mark.parametrize("M,k,n", [(200, 512, 320), (300, 512, 74 * 256 - 192)])
+def test_nf4_zero_and_subnormal_blocks_in_the_fused_gemms(M, k, n):
+    """An all-zero 64-block (absmax 0, every code 7) and a block of bf16
+    subnormals decode to zero / tiny values inside the fused forward and dX
+    (one- and two-m-block tiles)."""
+    r = 16
+    d = draw_projection(torch.Generator().manual_seed(63), M, k, n, r)
+    W = d["W"].clone()
+    W[0, :64] = 0
+    W[1, 64:128] = (torch.arange(64, dtype=torch.float32) - 32.0) * 1e-40
+    W[2:, 128:192] = 0
+    d["W"] = W
+    codes, absmax, c, a = _nf4(W)
+    assert absmax[0, 0] == 0.0 and 0.0 < absmax[1, 1] < 1.17e-38
+    Wq = ref.nf4_dequant(codes, absmax)
+    y, _ = _fwd(d, L.nf4_weight(c, a), r)
+    want = ref.lora_fwd(np64(d["x"]), Wq, np64(d["A"]), np64(d["B"]), ALPHA)
+    assert np.isfinite(np64(y)).all()
+    assert rel_err(np64(y), want) <= TOL_BF16
+    # dX over the same W: as the reduction operand (n rows of W)
+    db = draw_projection(torch.Generator().manual_seed(64), M, k, n, r)
+    db["W"] = W
+    got, _ = _bwd(db, L.nf4_weight(c, a), r)
+    want = ref.lora_bwd(np64(db["x"]), Wq, np64(db["A"]), np64(db["B"]), np64(db["dY"]), ALPHA)
+    assert np.isfinite(np64(got[0])).all()
+    assert rel_err(np64(got[0]), want[0]) <= TOL_BF16
+
+
+@pytest.mark.parametrize("M,k,n,r,schedule", [
+    (2048, 2048, 2048, 64, "lora_skinny_kernel"),     # even tiles: cluster split-K
+    (1024, 4096, 4096, 16, "lora_skinny_sk_kernel"),  # few long rank-16 tiles: stream-K
+])
+def test_rank_pass_schedule_runs_and_matches(M, k, n, r, schedule):
+    d = draw_projection(torch.Generator().manual_seed(65), M, k, n, r)
+    Wd = cuda(d["W"])
+    y, fnames = _fwd(d, L.bf16_weight(Wd), r)
+    got, bnames = _bwd(d, L.bf16_weight(Wd), r)
+    rank = [nm for nm in fnames + bnames if nm.startswith("lora_skinny")]
+    assert len(rank) == 3 and all(nm.startswith(schedule + "<") for nm in rank), rank
+    x, W, A, B, dY = (np64(d[t]) for t in ("x", "W", "A", "B", "dY"))
+    rows = np.random.default_rng(0).choice(M, 256, replace=False)
+    assert rel_err(np64(y)[rows], ref.lora_fwd(x[rows], W, A, B, ALPHA)) <= TOL_BF16
+    dx, dA, dB = ref.lora_bwd(x, W, A, B, dY, ALPHA)
+    assert rel_err(np64(got[0])[rows], dx[rows]) <= TOL_BF16
+    assert rel_err(np64(got[1]), dA) <= TOL_F32
+    assert rel_err(np64(got[2]), dB) <= TOL_F32

@@ -17,6 +17,13 @@ Sources (web pages about Unsloth; cited by title and section):
   trained; 4096x4096 at rank 16 -> about 1.3e5 trainable parameters).
 * [P5] "Unsloth自动化优化：无需手动调参的实现原理" — §3.2 (fused kernel also
   described as ``A@B + original_weight``), §3.3/§5 (NF4 is the default).
+* [P4] "Unsloth框架：高效LLM微调与LoRA优化实践" — §3.1 计算图重写引擎
+  (adjacent linear layers merged with their activation function).
+* [P5] also §1, 模型结构自识别 (the SwiGLU block is one of the modules it
+  recognises and optimises).
+* [SwiGLU] Shazeer 2020, "GLU Variants Improve Transformer", §2: the
+  gated unit ``Swish_1(x·W)·(x·V)`` with ``Swish_1(t) = t·sigmoid(t)``
+  (SiLU); the pages name SwiGLU but do not write it out.
 * [QLoRA] Dettmers et al. 2023, "QLoRA: Efficient Finetuning of Quantized
   LLMs", §3 "4-bit NormalFloat Quantization" and the NF4 table in its
   appendix: the pages name NF4 but do not give its levels.
@@ -41,6 +48,8 @@ __all__ = [
     "bf16_round", "nf4_codebook", "nf4_quantize", "nf4_unpack", "nf4_dequant",
     "rope_inv_freq", "rope_cos_sin", "rope_apply", "rope_apply_inverse",
     "qk_rope_fwd", "qk_rope_bwd",
+    "sigmoid", "silu", "swiglu_fwd", "swiglu_bwd",
+    "unmerged_weight", "nf4_merge",
 ]
 
 
@@ -109,6 +118,13 @@ def merged_weight(W, A, B, alpha: float):
     ([P2] §5.1; [P5] §3.2 "A@B + original_weight")."""
     W, A, B = _f64(W), _f64(A), _f64(B)
     return W + lora_scale(alpha, A.shape[0]) * (B @ A)
+
+
+def unmerged_weight(Wm, A, B, alpha: float):
+    """The inverse of :func:`merged_weight`: ``W = W' − s·B·A`` (taking the
+    adapter back out of a merged weight, so training can resume on W)."""
+    Wm, A, B = _f64(Wm), _f64(A), _f64(B)
+    return Wm - lora_scale(alpha, A.shape[0]) * (B @ A)
 
 
 def lora_param_count(k: int, n: int, r: int) -> int:
@@ -297,4 +313,75 @@ def qk_rope_bwd(x, Wq, Aq, Bq, Wk, Ak, Bk, dq, dk, alpha, positions, theta,
     dxq, dAq, dBq = lora_bwd(x, Wq, Aq, Bq, dq_pre, alpha)
     dxk, dAk, dBk = lora_bwd(x, Wk, Ak, Bk, dk_pre, alpha)
     return dxq + dxk, dAq, dBq, dAk, dBk
+
+
+# ---------------------------------------------------------------------------
+# Gate/up projections with the SwiGLU activation — [P4] §3.1 计算图重写引擎
+# (linear layers merged with the activation that follows them), [P5] §1
+# 模型结构自识别 (SwiGLU), [SwiGLU] §2
+# ---------------------------------------------------------------------------
+def sigmoid(t):
+    """``1 / (1 + e^{-t})``; for ``t < 0`` evaluated as ``e^t / (1 + e^t)``
+    (the same value) so that ``e^{-t}`` never overflows and the small tail
+    keeps its relative precision."""
+    t = _f64(t)
+    e = np.exp(-np.abs(t))                  # in (0, 1]: no overflow
+    return np.where(t >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def silu(t):
+    """SiLU (Swish_1), ``t·sigmoid(t)`` ([SwiGLU] §2)."""
+    t = _f64(t)
+    return t * sigmoid(t)
+
+
+def swiglu_fwd(x, Wg, Ag, Bg, Wu, Au, Bu, alpha: float):
+    """The MLP's gate and up LoRA projections of one x, joined by SwiGLU::
+
+        g = x·Wgᵀ + s·(x·Agᵀ)·Bgᵀ      (gate_proj, :func:`lora_fwd`)
+        u = x·Wuᵀ + s·(x·Auᵀ)·Buᵀ      (up_proj)
+        h = silu(g)·u                  (elementwise; h feeds down_proj)
+
+    Returns ``(h, g, u)`` [M,n] in fp64."""
+    g = lora_fwd(x, Wg, Ag, Bg, alpha)
+    u = lora_fwd(x, Wu, Au, Bu, alpha)
+    return silu(g) * u, g, u
+
+
+def swiglu_bwd(x, Wg, Ag, Bg, Wu, Au, Bu, dh, alpha: float):
+    """Backward of :func:`swiglu_fwd` for an incoming ``dh``.  With
+    ``σ = sigmoid(g)`` the chain rule through ``h = g·σ·u`` gives::
+
+        dg = dh·u·σ·(1 + g·(1 − σ))     (d silu(g)/dg = σ + g·σ·(1 − σ))
+        du = dh·silu(g)
+
+    then :func:`lora_bwd` of each projection; dX is their sum (both read x).
+    g and u are recomputed from the inputs.
+
+    Returns ``(dX, dAg, dBg, dAu, dBu)`` in fp64."""
+    g = lora_fwd(x, Wg, Ag, Bg, alpha)
+    u = lora_fwd(x, Wu, Au, Bu, alpha)
+    dh = _f64(dh)
+    sg = sigmoid(g)
+    dg = dh * u * sg * (1.0 + g * (1.0 - sg))
+    du = dh * g * sg
+    dxg, dAg, dBg = lora_bwd(x, Wg, Ag, Bg, dg, alpha)
+    dxu, dAu, dBu = lora_bwd(x, Wu, Au, Bu, du, alpha)
+    return dxg + dxu, dAg, dBg, dAu, dBu
+
+
+# ---------------------------------------------------------------------------
+# Merging the adapter into an NF4 base weight — [P2] §5.1, [P5] §3.2
+# ---------------------------------------------------------------------------
+def nf4_merge(codes, absmax, A, B, alpha: float, sign: float = 1.0):
+    """NF4 weight with the adapter merged in (``sign`` = +1) or taken out
+    (-1): dequantise, add ``sign·s·B·A``, quantise again (:func:`nf4_dequant`,
+    :func:`merged_weight`, :func:`nf4_quantize`).  The page describes the
+    merge for inference; the NF4 weight is re-quantised because the merged
+    weight is no longer representable in the old codes.
+
+    Returns ``(codes, absmax)`` as :func:`nf4_quantize` does."""
+    W = nf4_dequant(codes, absmax)
+    Wm = merged_weight(W, A, B, alpha) if sign > 0 else unmerged_weight(W, A, B, alpha)
+    return nf4_quantize(Wm)
 

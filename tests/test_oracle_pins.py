@@ -313,3 +313,106 @@ def test_param_count_closed_form():
     """4096x4096 at rank 16: 2 x 4096 x 16 = 131072 trainable parameters
     (the page's "约13万")."""
     assert ref.lora_param_count(4096, 4096, 16) == 131072
+
+
+# --------------------------------------------------------------------------
+# SwiGLU gate/up composition
+# --------------------------------------------------------------------------
+def test_silu_and_sigmoid_match_torch():
+    t = np.concatenate([_rand(200, scale=4.0), [-800.0, -40.0, -1e-300, 0.0, 1e-300, 40.0, 800.0]])
+    tt = torch.from_numpy(t)
+    np.testing.assert_allclose(ref.silu(t), torch.nn.functional.silu(tt).numpy(),
+                               rtol=1e-15, atol=1e-300)
+    np.testing.assert_allclose(ref.sigmoid(t), torch.sigmoid(tt).numpy(), rtol=1e-15,
+                               atol=1e-300)
+
+
+def _swiglu_torch(x, Wg, Ag, Bg, Wu, Au, Bu, alpha):
+    """The same composition written with torch layers (fp64) for autograd."""
+    F = torch.nn.functional
+    s = alpha / Ag.shape[0]
+    g = F.linear(x, Wg) + s * F.linear(F.linear(x, Ag), Bg)
+    u = F.linear(x, Wu) + s * F.linear(F.linear(x, Au), Bu)
+    return F.silu(g) * u
+
+
+def test_swiglu_forward_and_backward_match_torch_autograd():
+    M, k, n, r, alpha = 7, 24, 10, 4, 8.0
+    arrs = [_rand(M, k), _rand(n, k, scale=0.3), _rand(r, k, scale=0.3), _rand(n, r, scale=0.3),
+            _rand(n, k, scale=0.3), _rand(r, k, scale=0.3), _rand(n, r, scale=0.3)]
+    dh = _rand(M, n)
+    h, g, u = ref.swiglu_fwd(*arrs, alpha)
+    ts = [torch.tensor(a, requires_grad=True) for a in arrs]
+    ht = _swiglu_torch(*ts, alpha)
+    np.testing.assert_allclose(h, ht.detach().numpy(), rtol=1e-12, atol=1e-12)
+    ht.backward(torch.from_numpy(dh))
+    dx, dAg, dBg, dAu, dBu = ref.swiglu_bwd(*arrs, dh, alpha)
+    want = [ts[0].grad, ts[2].grad, ts[3].grad, ts[5].grad, ts[6].grad]
+    for got, w in zip((dx, dAg, dBg, dAu, dBu), want):
+        np.testing.assert_allclose(got, w.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_swiglu_backward_matches_finite_differences():
+    M, k, n, r, alpha = 3, 8, 5, 2, 4.0
+    x, Wg, Ag, Bg = _rand(M, k), _rand(n, k), _rand(r, k), _rand(n, r)
+    Wu, Au, Bu, G = _rand(n, k), _rand(r, k), _rand(n, r), _rand(M, n)
+    L = lambda: float(np.sum(G * ref.swiglu_fwd(x, Wg, Ag, Bg, Wu, Au, Bu, alpha)[0]))
+    dx, dAg, dBg, dAu, dBu = ref.swiglu_bwd(x, Wg, Ag, Bg, Wu, Au, Bu, G, alpha)
+    for P, an in ((x, dx), (Ag, dAg), (Bg, dBg), (Au, dAu), (Bu, dBu)):
+        np.testing.assert_allclose(an, _fd_grad(L, P), rtol=1e-6, atol=1e-7)
+
+
+def test_swiglu_with_a_zero_gate_has_closed_form_gradients():
+    """g ≡ 0 (Wg = 0, Bg = 0): h = 0, silu'(0) = 1/2 so dg = dh·u/2, du = 0,
+    and the up projection receives no gradient."""
+    M, k, n, r, alpha = 5, 16, 6, 2, 2.0
+    x, Ag, Wu, Au, Bu, dh = (_rand(M, k), _rand(r, k), _rand(n, k), _rand(r, k), _rand(n, r),
+                             _rand(M, n))
+    Wg, Bg = np.zeros((n, k)), np.zeros((n, r))
+    h, g, u = ref.swiglu_fwd(x, Wg, Ag, Bg, Wu, Au, Bu, alpha)
+    assert np.all(h == 0) and np.all(g == 0)
+    dx, dAg, dBg, dAu, dBu = ref.swiglu_bwd(x, Wg, Ag, Bg, Wu, Au, Bu, dh, alpha)
+    s = alpha / r
+    dg = 0.5 * dh * u
+    np.testing.assert_allclose(dx, s * (dg @ Bg) @ Ag + dg @ Wg, atol=1e-12)
+    np.testing.assert_allclose(dBg, s * dg.T @ (x @ Ag.T), rtol=1e-12, atol=1e-12)
+    assert np.all(dAg == 0) and np.all(dAu == 0) and np.all(dBu == 0)
+
+
+# --------------------------------------------------------------------------
+# merge / unmerge
+# --------------------------------------------------------------------------
+def test_unmerge_inverts_merge_elementwise_loops():
+    n, k, r, alpha = 5, 7, 3, 6.0
+    W, A, B = _rand(n, k), _rand(r, k), _rand(n, r)
+    Wm = ref.merged_weight(W, A, B, alpha)
+    s = alpha / r
+    for i in range(n):              # the merged element, summed by hand
+        for j in range(k):
+            assert abs(Wm[i, j] - (W[i, j] + s * sum(B[i, l] * A[l, j] for l in range(r)))) < 1e-12
+    np.testing.assert_allclose(ref.unmerged_weight(Wm, A, B, alpha), W, rtol=0, atol=1e-12)
+
+
+def test_nf4_merge_with_b_zero_keeps_codes_and_absmax():
+    """B = 0 adds nothing: dequantise then quantise gives back the same
+    codes and block scales (every level maps to itself, and each block's
+    largest level is ±1 times its bf16 absmax)."""
+    w = ref.bf16_round(_rand(6, 192))
+    codes, absmax = ref.nf4_quantize(w)
+    A, B = _rand(4, 192), np.zeros((6, 4))
+    for sign in (1.0, -1.0):
+        c2, a2 = ref.nf4_merge(codes, absmax, A, B, 16.0, sign)
+        np.testing.assert_array_equal(c2, codes)
+        np.testing.assert_array_equal(a2, absmax)
+
+
+def test_nf4_merge_is_within_the_quantisation_bound_of_the_merged_weight():
+    w = ref.bf16_round(_rand(8, 256, scale=0.05))
+    codes, absmax = ref.nf4_quantize(w)
+    A, B, alpha = _rand(4, 256, scale=0.1), _rand(8, 4, scale=0.1), 8.0
+    Wm = ref.merged_weight(ref.nf4_dequant(codes, absmax), A, B, alpha)
+    c2, a2 = ref.nf4_merge(codes, absmax, A, B, alpha)
+    got = ref.nf4_dequant(c2, a2)
+    gaps = np.diff(ref.nf4_codebook()).max()
+    bound = np.repeat(a2, 64, axis=1) * (gaps / 2) + np.abs(Wm) * 2.0 ** -8
+    assert np.all(np.abs(got - Wm) <= bound + 1e-15)

@@ -53,7 +53,7 @@ METRIC = "fused LoRA fwd+bwd tokens/s & TFLOP/s at 1 B300; % of bf16 tensor peak
 DEFAULT_WORKLOAD = "qwen32b_qlora_all7"
 # configurations timed beside the headline (the 256-token single linear is a
 # parity case, not a bench line)
-OTHER_WORKLOADS = ("llama8b_qk_rope", "llama8b_mlp", "llama8b_qlora_all7")
+OTHER_WORKLOADS = ("llama8b_qk_rope", "llama8b_mlp", "llama8b_mlp_swiglu", "llama8b_qlora_all7")
 FLUSH_BYTES = 512 << 20          # > 126 MB L2, written between timed steps
 
 
@@ -79,6 +79,37 @@ def call_phases(wl, M):
     fp32-equivalent (their bf16 hi + lo parts)."""
     r = wl.r
     out = []
+    if wl.extra.get("swiglu"):
+        (pg, pu, pd) = wl.projections
+        k, n, rl = pg.k, pg.n, 2 * r
+        rp = 16 if rl <= 16 else 32 if rl <= 32 else 64 if rl <= 64 else 128
+        kd, nd = pd.k, pd.n
+        out.append(("fwd:gate_up", [
+            ("fwd_rank", 2.0 * M * k * rl, 2.0 * M * k + 2.0 * rl * k + 2.0 * M * rl),
+            ("fwd_gemm", 2.0 * M * k * 2 * n + 2.0 * M * r * 2 * n,
+             2.0 * M * k + 4.0 * n * k + 6.0 * M * n + 2.0 * M * rl + 4.0 * n * r)]))
+        out.append(("fwd:down", [
+            ("fwd_rank", 2.0 * M * kd * r, 2.0 * M * kd + 2.0 * r * kd + 2.0 * M * r),
+            ("fwd_gemm", 2.0 * M * kd * nd + 2.0 * M * r * nd,
+             2.0 * M * kd + 2.0 * nd * kd + 2.0 * M * nd + 2.0 * M * r + 2.0 * nd * r)]))
+        rpd = 16 if r <= 16 else 32 if r <= 32 else 64
+        out.append(("bwd:down", [
+            ("bwd_prep", 0.0, 4.0 * nd * r),
+            ("bwd_rank", 2.0 * M * r * (kd + nd),
+             2.0 * M * (kd + nd) + 2.0 * r * (kd + nd) + 8.0 * rpd * M + 2.0 * M * r),
+            ("dx_gemm", 2.0 * M * nd * kd + 2.0 * M * r * kd,
+             2.0 * M * nd + 2.0 * nd * kd + 2.0 * M * kd + 2.0 * M * r + 2.0 * r * kd),
+            ("bwd_grads", 2.0 * M * r * (kd + nd),
+             2.0 * M * (kd + nd) + 8.0 * rpd * M + 4.0 * r * (kd + nd))]))
+        out.append(("bwd:gate_up", [
+            ("bwd_prep", 0.0, 10.0 * M * n + 4.0 * rl * k + 8.0 * n * rl),
+            ("bwd_rank", 2.0 * M * rl * (k + 2 * n),
+             2.0 * M * (k + 2 * n) + 2.0 * rl * (k + 2 * n) + 8.0 * rp * M + 2.0 * M * rl),
+            ("dx_gemm", 2.0 * M * 2 * n * k + 2.0 * M * rl * k,
+             4.0 * M * n + 4.0 * n * k + 2.0 * M * k + 2.0 * M * rl + 2.0 * rl * k),
+            ("bwd_grads", 2.0 * M * rl * (k + 2 * n),
+             2.0 * M * (k + 2 * n) + 8.0 * rp * M + 4.0 * rl * (k + 2 * n))]))
+        return out
     if wl.rope:
         (pq, pk) = wl.projections
         k, n, rl = pq.k, pq.n + pk.n, 2 * r
@@ -319,7 +350,19 @@ class Replica:
             d["dB"] = torch.empty(p.n, wl.r, **f32)
             self.projs.append((p, d))
         del data
-        if wl.rope:
+        if wl.extra.get("swiglu"):
+            (pg, dg), (pu, du), (pd, dd) = self.projs
+            self.h = torch.empty(M, pg.n, **bf)
+            self.g = torch.empty(M, pg.n, **bf)
+            self.u = torch.empty(M, pg.n, **bf)
+            self.dh = torch.empty(M, pg.n, **bf)
+            self.ws_f = torch.zeros(max(L.workspace_size(L.OP_SWIGLU_FWD, M, pg.k, pg.n, wl.r),
+                                        L.workspace_size(L.OP_FWD, M, pd.k, pd.n, wl.r)),
+                                    dtype=torch.uint8, device=device)
+            self.ws_b = torch.zeros(max(L.workspace_size(L.OP_SWIGLU_BWD, M, pg.k, pg.n, wl.r),
+                                        L.workspace_size(L.OP_BWD, M, pd.k, pd.n, wl.r)),
+                                    dtype=torch.uint8, device=device)
+        elif wl.rope:
             (pq, dq), (pk, dk) = self.projs
             self.max_pos = M
             self.pos = torch.arange(M, dtype=torch.int32, device=device)
@@ -340,6 +383,9 @@ class Replica:
 
     def inputs(self):
         """Per-step inputs (activations and incoming gradients)."""
+        if self.wl.extra.get("swiglu"):
+            (_, dg), _, (_, dd) = self.projs
+            return [dg["x"], dd["dY"]]
         if self.wl.rope:
             (_, dq), (_, dk) = self.projs
             return [dq["x"], dq["dY"], dk["dY"]]
@@ -349,6 +395,10 @@ class Replica:
         return out
 
     def outputs(self):
+        if self.wl.extra.get("swiglu"):
+            (_, dg), (_, du), (_, dd) = self.projs
+            return [dd["y"], dg["dx"], dg["dA"], dg["dB"], du["dA"], du["dB"], dd["dA"],
+                    dd["dB"]]
         if self.wl.rope:
             (_, dq), (_, dk) = self.projs
             return [dq["y"], dk["y"], self.dx, dq["dA"], dq["dB"], dk["dA"], dk["dB"]]
@@ -360,6 +410,21 @@ class Replica:
     def calls(self):
         """The library calls of one step, in order: [(name, fn)]."""
         L, wl = self.L, self.wl
+        if wl.extra.get("swiglu"):
+            (_, g), (_, u), (_, d) = self.projs
+            return [
+                ("fwd:gate_up", lambda: L.lora_swiglu_fwd(
+                    g["x"], g["Wdesc"], g["A"], g["B"], u["Wdesc"], u["A"], u["B"], self.h,
+                    wl.alpha, self.ws_f, g=self.g, u=self.u)),
+                ("fwd:down", lambda: L.lora_linear_fwd(
+                    self.h, d["Wdesc"], d["A"], d["B"], d["y"], wl.alpha, self.ws_f)),
+                ("bwd:down", lambda: L.lora_linear_bwd(
+                    self.h, d["Wdesc"], d["A"], d["B"], d["dY"], self.dh, d["dA"], d["dB"],
+                    wl.alpha, self.ws_b)),
+                ("bwd:gate_up", lambda: L.lora_swiglu_bwd(
+                    g["x"], g["Wdesc"], g["A"], g["B"], u["Wdesc"], u["A"], u["B"], self.g,
+                    self.u, self.dh, g["dx"], g["dA"], g["dB"], u["dA"], u["dB"], wl.alpha,
+                    self.ws_b))]
         if wl.rope:
             (_, q), (_, k) = self.projs
             return [
@@ -732,6 +797,15 @@ def oracle_step(name: str, data, M: int):
     import oracle as ref
     wl = WORKLOADS[name]
     f = lambda t: t.float().numpy().astype(np.float64)
+    if wl.extra.get("swiglu"):
+        g, u, d = data["gate_proj"], data["up_proj"], data["down_proj"]
+        W = lambda t: t["Wq"] if "Wq" in t else f(t["W"])
+        args = (f(g["x"]), W(g), f(g["A"]), f(g["B"]), W(u), f(u["A"]), f(u["B"]))
+        h = ref.swiglu_fwd(*args, wl.alpha)[0]
+        ref.lora_fwd(h, W(d), f(d["A"]), f(d["B"]), wl.alpha)
+        dh = ref.lora_bwd(h, W(d), f(d["A"]), f(d["B"]), f(d["dY"]), wl.alpha)[0]
+        ref.swiglu_bwd(*args, dh, wl.alpha)
+        return
     if wl.rope:
         q, k = data["q_proj"], data["k_proj"]
         pos = np.arange(M)

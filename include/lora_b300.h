@@ -89,7 +89,11 @@ enum {
   LORA_OP_FWD = 0,
   LORA_OP_BWD = 1,
   LORA_OP_QK_ROPE_FWD = 2,
-  LORA_OP_QK_ROPE_BWD = 3
+  LORA_OP_QK_ROPE_BWD = 3,
+  LORA_OP_SWIGLU_FWD = 4,
+  LORA_OP_SWIGLU_BWD = 5,
+  LORA_OP_MERGE = 6,     /* pass M = 1 */
+  LORA_OP_MERGE_NF4 = 7  /* pass M = 1 */
 };
 
 /* Bytes of workspace an operation needs (always >= 256: the status word
@@ -173,6 +177,43 @@ lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq,
                                const float *cos_sin_cache, int max_pos,
                                void *ws, size_t ws_bytes, lora_stream_t stream);
 
+/* Gate and up projections of an MLP joined by SwiGLU, [P4] "Unsloth框架：
+ * 高效LLM微调与LoRA优化实践" §3.1 计算图重写引擎 (adjacent linear layers merged
+ * with their activation) and [P5] "Unsloth自动化优化" §1 模型结构自识别
+ * (SwiGLU); SwiGLU itself as in Shazeer 2020, "GLU Variants Improve
+ * Transformer" §2, since the pages only name it:
+ *   g = x·Wgᵀ + s·(x·Agᵀ)·Bgᵀ,  u = x·Wuᵀ + s·(x·Auᵀ)·Buᵀ,
+ *   h = silu(g)·u = g·u / (1 + e^(−g)).
+ * One rank pass for both adapters (s·x·[Ag; Au]ᵀ, [M,2r] in the workspace),
+ * then ONE fused GEMM launch over both weights: each CTA pair computes 128
+ * columns of g and the same 128 of u into one accumulator and writes h
+ * from its epilogue, so neither g nor u needs a second pass.
+ *   x [M,k]; Wg, Wu [n,k] (both bf16 or both NF4); Ag, Au [r,k]; Bg, Bu [n,r];
+ *   h [M,n] bf16 (the input of down_proj).  g, u [M,n] bf16 receive the
+ *   pre-activation outputs, which lora_swiglu_bwd needs; pass both NULL to
+ *   skip them (inference).
+ *   ws: >= lora_workspace_size(LORA_OP_SWIGLU_FWD, M, k, n, r). */
+lora_status_t lora_swiglu_fwd(const void *x, lora_weight_t Wg, const void *Ag,
+                              const void *Bg, lora_weight_t Wu, const void *Au,
+                              const void *Bu, void *h, void *g, void *u, int M,
+                              int k, int n, int r, float alpha, void *ws,
+                              size_t ws_bytes, lora_stream_t stream);
+
+/* Backward of lora_swiglu_fwd for an incoming dh [M,n], from the saved g, u:
+ *   dg = dh·u·σ(g)·(1 + g·(1 − σ(g))),  du = dh·g·σ(g)   (σ = sigmoid, one
+ *   elementwise pass, rounded to bf16), then gate and up run as ONE
+ *   projection of rank 2r (A = [Ag; Au], B = diag(Bg, Bu), dY = [dg | du])
+ *   through the passes of lora_linear_bwd, with dX reduced over [Wg; Wu] in
+ *   one GEMM (accumulate_dx != 0: dX += the sum).  dAg, dBg, dAu, dBu float32,
+ *   overwritten.  ws: >= lora_workspace_size(LORA_OP_SWIGLU_BWD, M, k, n, r). */
+lora_status_t lora_swiglu_bwd(const void *x, lora_weight_t Wg, const void *Ag,
+                              const void *Bg, lora_weight_t Wu, const void *Au,
+                              const void *Bu, const void *g, const void *u,
+                              const void *dh, void *dx, int accumulate_dx,
+                              float *dAg, float *dBg, float *dAu, float *dBu,
+                              int M, int k, int n, int r, float alpha, void *ws,
+                              size_t ws_bytes, lora_stream_t stream);
+
 /* lora_linear_bwd without a workspace argument, for callers that cannot
  * allocate device memory where they run the backward (a plugin inside another
  * framework's runtime that is handed only its tensors; a latency-critical
@@ -191,6 +232,31 @@ lora_status_t lora_linear_bwd_noalloc(const void *x, lora_weight_t W, const void
                                       const void *B, const void *dy, void *dx,
                                       int accumulate_dx, float *dA, float *dB, int M, int k,
                                       int n, int r, float alpha, lora_stream_t stream);
+
+/* Merge the adapter into its base weight for inference, or take it back out:
+ * W <- W + sign·s·B·A (sign = +1 merge, -1 unmerge), s = alpha/r.  [P2]
+ * "微调太慢？试试Unsloth" §5.1 (for_inference folds the LoRA weights into the
+ * main weight so no adapter runs at generation time) and [P5] §3.2 (the
+ * "A@B + original_weight" kernel).  In place on a bf16 W [n,k]; B·A runs on
+ * the tensor cores (K = r) and each W element is read and written once
+ * (rounded once to bf16).  A [r,k], B [n,r] bf16.  n % 64 == 0, k % 64 == 0.
+ *   ws: >= lora_workspace_size(LORA_OP_MERGE, 1, k, n, r) (the status word). */
+lora_status_t lora_merge(void *W, const void *A, const void *B, int n, int k,
+                         int r, float alpha, int sign, void *ws, size_t ws_bytes,
+                         lora_stream_t stream);
+
+/* The same for an NF4 W (codes and absmax as in lora_weight_t, blocksize 64):
+ * dequantise into the workspace (bf16), merge there, and quantise back into
+ * codes/absmax in place (nf4_quantize's rule).  The merged weight is not
+ * representable in the old codes, so it is re-quantised; merging then
+ * unmerging returns a weight within NF4's quantisation error of the
+ * original, not the original codes.
+ *   ws: >= lora_workspace_size(LORA_OP_MERGE_NF4, 1, k, n, r) (2·n·k bytes
+ *   plus the status word). */
+lora_status_t lora_merge_nf4(uint8_t *codes, void *absmax, const void *A,
+                             const void *B, int n, int k, int r, float alpha,
+                             int sign, int blocksize, void *ws, size_t ws_bytes,
+                             lora_stream_t stream);
 
 /* Standalone NF4 dequantisation ([P3] 显存优化策略, [QLoRA] §3):
  *   w_out[i,j] = bf16( level[code(i,j)] * absmax[i, j/64] ), product in fp32.

@@ -72,6 +72,13 @@ WORKLOADS = {
         projections=(Projection("gate_proj", 4096, 14336), Projection("up_proj", 4096, 14336),
                      Projection("down_proj", 14336, 4096)),
         description="Llama-3-8B MLP gate/up 4096->14336, down 14336->4096, M=4096, r=16, bf16 W"),
+    "llama8b_mlp_swiglu": Workload(
+        "llama8b_mlp_swiglu", M=4096, r=16, alpha=16.0, nf4=False,
+        projections=(Projection("gate_proj", 4096, 14336), Projection("up_proj", 4096, 14336),
+                     Projection("down_proj", 14336, 4096)),
+        description="Llama-3-8B MLP block: gate/up 4096->14336 fused with SwiGLU, down "
+                    "14336->4096 on its output, M=4096, r=16, bf16 W",
+        extra={"swiglu": True}),
     "llama8b_qlora_all7": Workload(
         "llama8b_qlora_all7", M=4096, r=16, alpha=16.0, nf4=True, projections=_LLAMA8B,
         description="QLoRA Llama-3-8B all 7 projections, NF4 W (block 64, bf16 absmax), "
@@ -128,6 +135,19 @@ def draw_workload(name: str, seed: int = 0, M: int | None = None, only=None) -> 
     wl = WORKLOADS[name]
     M = wl.M if M is None else int(M)
     out = {}
+    if wl.extra.get("swiglu"):
+        # one stream: x shared by gate and up; down_proj's own x is drawn but
+        # the step feeds it the SwiGLU output, and its dY is the block's
+        # incoming gradient
+        g = _gen(seed)
+        gate, up, down = wl.projections
+        x = draw_shared_x(g, M, gate.k)
+        out[gate.name] = draw_projection(g, M, gate.k, gate.n, wl.r, x=x)
+        out[up.name] = draw_projection(g, M, up.k, up.n, wl.r, x=x)
+        out[down.name] = draw_projection(g, M, down.k, down.n, wl.r)
+        if only is not None:
+            out = {k_: v for k_, v in out.items() if k_ in only}
+        return out
     if wl.rope:
         g = _gen(seed)
         x = draw_shared_x(g, M, wl.projections[0].k)

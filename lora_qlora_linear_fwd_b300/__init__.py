@@ -20,14 +20,17 @@ from .build import lib_path
 __all__ = [
     "LoraError", "Weight", "bf16_weight", "nf4_weight", "workspace", "workspace_size",
     "lora_linear_fwd", "lora_linear_bwd", "lora_linear_bwd_noalloc", "lora_qk_rope_fwd",
-    "lora_qk_rope_bwd",
+    "lora_qk_rope_bwd", "lora_swiglu_fwd", "lora_swiglu_bwd", "lora_merge", "lora_merge_nf4",
     "nf4_dequant", "nf4_quantize", "lora_rope_cache_build", "lora_rope_cache_bytes",
     "lora_read_device_status", "lora_clear_device_status", "lora_status_string",
     "lora_kernel_launch_count", "lora_profile_begin", "lora_profile_end",
-    "OP_FWD", "OP_BWD", "OP_QK_ROPE_FWD", "OP_QK_ROPE_BWD", "EXPORTS", "library",
+    "OP_FWD", "OP_BWD", "OP_QK_ROPE_FWD", "OP_QK_ROPE_BWD", "OP_SWIGLU_FWD", "OP_SWIGLU_BWD",
+    "OP_MERGE", "OP_MERGE_NF4", "EXPORTS", "library",
 ]
 
 OP_FWD, OP_BWD, OP_QK_ROPE_FWD, OP_QK_ROPE_BWD = 0, 1, 2, 3
+OP_SWIGLU_FWD, OP_SWIGLU_BWD = 4, 5
+OP_MERGE, OP_MERGE_NF4 = 6, 7
 WEIGHT_BF16, WEIGHT_NF4 = 0, 1
 STATUS_NAMES = ["LORA_OK", "LORA_ERR_INVALID_ARG", "LORA_ERR_UNSUPPORTED", "LORA_ERR_WORKSPACE",
                 "LORA_ERR_ARCH", "LORA_ERR_CUDA", "LORA_ERR_TIMEOUT"]
@@ -59,8 +62,14 @@ EXPORTS = {
                               _F, _D, _P, _P, _I, _P, _Z, _P]),
     "lora_qk_rope_bwd": (_I, [_P, Weight, _P, _P, Weight, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
                               _I, _I, _I, _I, _I, _I, _F, _D, _P, _P, _I, _P, _Z, _P]),
+    "lora_swiglu_fwd": (_I, [_P, Weight, _P, _P, Weight, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F,
+                             _P, _Z, _P]),
+    "lora_swiglu_bwd": (_I, [_P, Weight, _P, _P, Weight, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P,
+                             _P, _I, _I, _I, _I, _F, _P, _Z, _P]),
     "lora_linear_bwd_noalloc": (_I, [_P, Weight, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _F,
                                      _P]),
+    "lora_merge": (_I, [_P, _P, _P, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "lora_merge_nf4": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
     "nf4_dequant": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "nf4_quantize": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "lora_rope_cache_bytes": (_Z, [_I, _I]),
@@ -208,6 +217,52 @@ def lora_qk_rope_bwd(x, Wq, Aq, Bq, Wk, Ak, Bk, dq, dk, dx, dAq, dBq, dAk, dBk, 
         _ptr(dBk), M, hidden, dq.shape[1] // head_dim, dk.shape[1] // head_dim, head_dim, r,
         float(alpha), float(rope_theta), _ptr(positions), _ptr(cos_sin_cache), int(max_pos),
         _ptr(ws), ws.numel(), _stream(stream)), "lora_qk_rope_bwd")
+
+
+def lora_swiglu_fwd(x, Wg, Ag, Bg, Wu, Au, Bu, h, alpha: float, ws, g=None, u=None,
+                    stream=None):
+    """h = silu(g)·u of the gate and up LoRA projections; g and u are also
+    written when given (the backward needs them)."""
+    M, k = x.shape
+    n, r = h.shape[1], Ag.shape[0]
+    _check(library.lora_swiglu_fwd(_ptr(x), _weight(Wg), _ptr(Ag), _ptr(Bg), _weight(Wu),
+                                   _ptr(Au), _ptr(Bu), _ptr(h), _ptr(g), _ptr(u), M, k, n, r,
+                                   float(alpha), _ptr(ws), ws.numel(), _stream(stream)),
+           "lora_swiglu_fwd")
+
+
+def lora_swiglu_bwd(x, Wg, Ag, Bg, Wu, Au, Bu, g, u, dh, dx, dAg, dBg, dAu, dBu, alpha: float,
+                    ws, accumulate_dx: bool = False, stream=None):
+    M, k = x.shape
+    n, r = dh.shape[1], Ag.shape[0]
+    _check(library.lora_swiglu_bwd(_ptr(x), _weight(Wg), _ptr(Ag), _ptr(Bg), _weight(Wu),
+                                   _ptr(Au), _ptr(Bu), _ptr(g), _ptr(u), _ptr(dh), _ptr(dx),
+                                   int(bool(accumulate_dx)), _ptr(dAg), _ptr(dBg), _ptr(dAu),
+                                   _ptr(dBu), M, k, n, r, float(alpha), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "lora_swiglu_bwd")
+
+
+def lora_merge(W, A, B, alpha: float, sign: int = 1, ws=None, stream=None):
+    """W <- W + sign·(alpha/r)·B·A in place (bf16 W [n, k])."""
+    n, k = W.shape
+    r = A.shape[0]
+    if ws is None:
+        ws = workspace(OP_MERGE, 1, k, n, r, device=W.device)
+    _check(library.lora_merge(_ptr(W), _ptr(A), _ptr(B), n, k, r, float(alpha), int(sign),
+                              _ptr(ws), ws.numel(), _stream(stream)), "lora_merge")
+
+
+def lora_merge_nf4(codes, absmax, A, B, alpha: float, sign: int = 1, ws=None, blocksize=64,
+                   stream=None):
+    """The NF4 weight (codes [n, k/2], absmax [n, k/64]) with the adapter
+    merged in (sign +1) or taken out (-1), re-quantised in place."""
+    n, k = codes.shape[0], codes.shape[1] * 2
+    r = A.shape[0]
+    if ws is None:
+        ws = workspace(OP_MERGE_NF4, 1, k, n, r, device=codes.device)
+    _check(library.lora_merge_nf4(_ptr(codes), _ptr(absmax), _ptr(A), _ptr(B), n, k, r,
+                                  float(alpha), int(sign), int(blocksize), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "lora_merge_nf4")
 
 
 def nf4_dequant(codes, absmax, w_out, blocksize: int = 64, stream=None):

@@ -190,6 +190,8 @@ struct GroupArgs {
   void *out;
   int ncols;       // output columns
   int sv_col;      // first column of this group's rank block in s·v / s·u
+  int b_cols = 0;  // FWD: columns of B (0: the launch's rank_k)
+  int b_shift = 0; // FWD: rank K-block e reads B from column 64·e + b_shift
 };
 
 struct GemmOpts {
@@ -211,6 +213,17 @@ struct GemmOpts {
   int max_pos = 0;
   int accumulate = 0;
   uint32_t *status = nullptr;
+  // SwiGLU pair (FWD, ng == 2: gate, up): h [M, n] out; the groups' `out`
+  // receive g and u when both are non-null
+  bool swiglu = false;
+  void *h = nullptr;
+  // DX read-modify-write scale (out = old + acc_scale·acc); overrides of the
+  // activation's column count and of W's rows as the MN-major operand (both
+  // default to Kred) for operands narrower than one 64-wide K-block, whose
+  // missing columns / rows the copies fill with zeros
+  float acc_scale = 1.0f;
+  int act_cols = 0;
+  int w_rows = 0;
 };
 
 bool make_w_map(CUtensorMap *m, const lora_weight_t &W, bool dx, bool nf4, int n, int k) {
@@ -232,39 +245,59 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   // activation [M, Kred] and rank block [M, rl]: K-major, box 64 x 128
-  if (!make_map(&p.tm_act, kBF16, 2, o.act, o.Kred, o.M, (uint64_t)o.Kred * 2, 64, 128, true) ||
-      !make_map(&p.tm_sv, kBF16, 2, o.sv, o.rl, o.M, (uint64_t)o.rl * 2, 64, 128, true))
+  const int act_cols = o.act_cols > 0 ? o.act_cols : o.Kred;
+  if (!make_map(&p.tm_act, kBF16, 2, o.act, act_cols, o.M, (uint64_t)act_cols * 2, 64, 128, true) ||
+      (o.rank_k > 0 &&
+       !make_map(&p.tm_sv, kBF16, 2, o.sv, o.rl, o.M, (uint64_t)o.rl * 2, 64, 128, true)))
     return LORA_ERR_CUDA;
   int tiles = 0;
+  const bool save_gu = o.swiglu && o.ga[0].out && o.ga[1].out;
   for (int g = 0; g < o.ng; ++g) {
     GemmGroup &G = p.grp[g];
     const GroupArgs &a = o.ga[g];
     const int ncols = a.ncols;
     if (!dx) {
       const int n = ncols, k = o.Kred;
+      const int bc = a.b_cols > 0 ? a.b_cols : o.rank_k;
       if (!make_w_map(&G.tm_w, a.W, false, nf4, n, k) ||
-          !make_map(&G.tm_b, kBF16, 2, a.b, o.rank_k, n, (uint64_t)o.rank_k * 2, 64, 128, true))
+          !make_map(&G.tm_b, kBF16, 2, a.b, bc, n, (uint64_t)bc * 2, 64, 128, true))
         return LORA_ERR_CUDA;
       G.ld_absmax = k / 64;
+      G.b_shift = a.b_shift;
     } else {
-      const int n = o.W2 ? o.ksplit * 64 : o.Kred, k = ncols;
+      const int n = o.W2 ? o.ksplit * 64 : (o.w_rows > 0 ? o.w_rows : o.Kred), k = ncols;
       if (!make_w_map(&G.tm_w, a.W, true, nf4, n, k) ||
-          !make_map(&G.tm_b, kBF16, 2, a.b, k, o.rl, (uint64_t)k * 2, 64, 64, true))
+          (o.rank_k > 0 &&
+           !make_map(&G.tm_b, kBF16, 2, a.b, k, o.rl, (uint64_t)k * 2, 64, 64, true)))
         return LORA_ERR_CUDA;
       G.ld_absmax = k / 64;
     }
-    if (!make_map(&G.tm_out, kBF16, 2, a.out, ncols, o.M, (uint64_t)ncols * 2, 32, 32, true))
+    if ((!o.swiglu || save_gu) &&
+        !make_map(&G.tm_out, kBF16, 2, a.out, ncols, o.M, (uint64_t)ncols * 2, 32, 32, true))
       return LORA_ERR_CUDA;
     G.out = static_cast<__nv_bfloat16 *>(a.out);
     G.absmax = static_cast<const __nv_bfloat16 *>(a.W.absmax);
     G.ncols = ncols;
-    G.n_tiles = (ncols + kBN - 1) / kBN;
-    G.tile_begin = tiles;
     G.sv_col = a.sv_col;
     G.n_extra = n_extra;
-    tiles += G.n_tiles;
+    if (o.swiglu) {  // both groups cover the same tiles of 128 output columns
+      G.n_tiles = (ncols + 127) / 128;
+      G.tile_begin = 0;
+      tiles = G.n_tiles;
+    } else {
+      G.n_tiles = (ncols + kBN - 1) / kBN;
+      G.tile_begin = tiles;
+      tiles += G.n_tiles;
+    }
   }
   p.num_groups = o.ng;
+  if (o.swiglu) {
+    p.swiglu = 1;
+    p.save_gu = save_gu ? 1 : 0;
+    if (!make_map(&p.tm_h, kBF16, 2, o.h, o.ga[0].ncols, o.M, (uint64_t)o.ga[0].ncols * 2, 32,
+                  32, true))
+      return LORA_ERR_CUDA;
+  }
   if (dx && o.W2) {  // second projection along the reduction
     GemmGroup &G1 = p.grp[1];
     const int k = o.ga[0].ncols, n2 = o.Kred - o.ksplit * 64;
@@ -296,6 +329,7 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
   }
   p.sched = make_schedule((m_blocks + mb - 1) / mb, tiles, slots, mb);
   p.accumulate = o.accumulate;
+  p.acc_scale = o.acc_scale;
   p.positions = o.positions;
   p.cos_sin = o.cos_sin;
   p.max_pos = o.max_pos;
@@ -695,6 +729,14 @@ size_t lora_workspace_size(int op, int M, int k, int n, int r) {
       return kStatusBytes + bwd_bytes(M, n, r);
     case LORA_OP_QK_ROPE_BWD:
       return plan_qk_bwd(M, k, n, r).total;
+    case LORA_OP_SWIGLU_FWD:
+      return fwd_bytes(M, 2 * r);
+    case LORA_OP_SWIGLU_BWD:
+      return plan_qk_bwd(M, k, 2 * n, r).total;
+    case LORA_OP_MERGE:
+      return kStatusBytes;
+    case LORA_OP_MERGE_NF4:
+      return kStatusBytes + align256((size_t)n * k * 2);
   }
   return 0;
 }
@@ -935,6 +977,191 @@ lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq, 
   pp.Bt = c.at<__nv_bfloat16>(c.b.off_bt);
   if ((s = cuda_status(launch_bwd_prep(pp, st)))) return s;
   return run_bwd_phases(c, st);
+}
+
+static lora_status_t check_pair(const void *x, lora_weight_t Wg, const void *Ag, const void *Bg,
+                                lora_weight_t Wu, const void *Au, const void *Bu, int M, int k,
+                                int n, int r, float alpha, const void *ws) {
+  lora_status_t s;
+  if ((s = check_shape(M, k, n, r))) return s;
+  if ((s = check_weight(Wg))) return s;
+  if ((s = check_weight(Wu))) return s;
+  if (Wg.type != Wu.type) return LORA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(Ag) || !aligned16(Bg) || !aligned16(Au) || !aligned16(Bu) ||
+      !aligned16(ws))
+    return LORA_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha)) return LORA_ERR_INVALID_ARG;
+  return LORA_OK;
+}
+
+lora_status_t lora_swiglu_fwd(const void *x, lora_weight_t Wg, const void *Ag, const void *Bg,
+                              lora_weight_t Wu, const void *Au, const void *Bu, void *h, void *g,
+                              void *u, int M, int k, int n, int r, float alpha, void *ws,
+                              size_t ws_bytes, lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = check_pair(x, Wg, Ag, Bg, Wu, Au, Bu, M, k, n, r, alpha, ws))) return s;
+  if (!aligned16(h) || (g == nullptr) != (u == nullptr) || (g && (!aligned16(g) || !aligned16(u))))
+    return LORA_ERR_INVALID_ARG;
+  if (ws_bytes < lora_workspace_size(LORA_OP_SWIGLU_FWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
+  DeviceInfo di;
+  if ((s = device_info(&di))) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t *status = static_cast<uint32_t *>(ws);
+  void *sv = static_cast<uint8_t *>(ws) + kStatusBytes;
+  const float scale = alpha / (float)r;
+  // rank pass over both projections: s·v = s·x·[Ag; Au]ᵀ [M, 2r]
+  if ((s = fwd_rank(x, Ag, Au, M, k, r, scale, sv, status, st))) return s;
+  // one fused GEMM: CTA 0 of a pair stages gate rows, CTA 1 the up rows of
+  // the same output columns; a rank K-block of [s·vg | s·vu] meets Bg in the
+  // gate half and Bu (read r columns to the left, so it lines up with s·vu)
+  // in the up half
+  GroupArgs ga[2] = {{Wg, Bg, g, n, 0, r, 0}, {Wu, Bu, u, n, 0, r, -r}};
+  GemmOpts o;
+  o.mode = kModeFwd;
+  o.act = x;
+  o.M = M;
+  o.Kred = k;
+  o.ga = ga;
+  o.ng = 2;
+  o.sv = sv;
+  o.rl = 2 * r;
+  o.rank_k = 2 * r;
+  o.status = status;
+  o.swiglu = true;
+  o.h = h;
+  return run_gemm(o, st);
+}
+
+lora_status_t lora_swiglu_bwd(const void *x, lora_weight_t Wg, const void *Ag, const void *Bg,
+                              lora_weight_t Wu, const void *Au, const void *Bu, const void *g,
+                              const void *u, const void *dh, void *dx, int accumulate_dx,
+                              float *dAg, float *dBg, float *dAu, float *dBu, int M, int k, int n,
+                              int r, float alpha, void *ws, size_t ws_bytes,
+                              lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = check_pair(x, Wg, Ag, Bg, Wu, Au, Bu, M, k, n, r, alpha, ws))) return s;
+  if (!aligned16(g) || !aligned16(u) || !aligned16(dh) || !aligned16(dx) || !aligned16(dAg) ||
+      !aligned16(dBg) || !aligned16(dAu) || !aligned16(dBu))
+    return LORA_ERR_INVALID_ARG;
+  if (ws_bytes < lora_workspace_size(LORA_OP_SWIGLU_BWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
+  DeviceInfo di;
+  if ((s = device_info(&di))) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *w8 = static_cast<uint8_t *>(ws);
+  // gate and up as one projection of rank 2r over n_total = 2n outputs:
+  // dY = [dg | du], A = [Ag; Au], B = diag(Bg, Bu), W = [Wg; Wu] along dX's
+  // reduction (the q/k layout)
+  const QkBwdPlan qp = plan_qk_bwd(M, k, 2 * n, r);
+  BwdCall c{};
+  c.x = x;
+  c.A = w8 + qp.off_a;
+  c.dy = w8 + qp.off_dy;
+  c.W = Wg;
+  c.W2 = Wu;
+  c.merged = true;
+  c.dx = dx;
+  c.accumulate = accumulate_dx;
+  c.dA = dAg;
+  c.dB = dBg;
+  c.dA2 = dAu;
+  c.dB2 = dBu;
+  c.M = M;
+  c.k = k;
+  c.n = 2 * n;
+  c.n1 = n;
+  c.r = r;
+  c.rl = 2 * r;
+  c.scale = alpha / (float)r;
+  c.status = static_cast<uint32_t *>(ws);
+  c.b = plan_bwd(M, 2 * n, 2 * r, 0);
+  c.ws = w8 + qp.off_area;
+  BwdPrep pp{};
+  pp.sw_dh = static_cast<const __nv_bfloat16 *>(dh);
+  pp.sw_g = static_cast<const __nv_bfloat16 *>(g);
+  pp.sw_u = static_cast<const __nv_bfloat16 *>(u);
+  pp.dy_out = reinterpret_cast<__nv_bfloat16 *>(w8 + qp.off_dy);
+  pp.status = c.status;
+  pp.M = M;
+  pp.n1 = n;
+  pp.n2 = n;
+  pp.k = k;
+  pp.r = r;
+  pp.nproj = 2;
+  pp.A1 = static_cast<const __nv_bfloat16 *>(Ag);
+  pp.A2 = static_cast<const __nv_bfloat16 *>(Au);
+  pp.A_out = reinterpret_cast<__nv_bfloat16 *>(w8 + qp.off_a);
+  pp.B1 = static_cast<const __nv_bfloat16 *>(Bg);
+  pp.B2 = static_cast<const __nv_bfloat16 *>(Bu);
+  pp.Bt = c.at<__nv_bfloat16>(c.b.off_bt);
+  if ((s = cuda_status(launch_bwd_prep(pp, st)))) return s;
+  return run_bwd_phases(c, st);
+}
+
+// W [n, k] bf16 (in place) += sign·s·B·A on the tensor cores: the dX GEMM
+// with B [n, r] as its activation (one 64-wide K-block, columns past r read
+// as zero), A [r, k] as its MN-major weight (rows past r zero) and the
+// read-modify-write epilogue scaled by sign·s.
+static lora_status_t merge_bf16(void *W, const void *A, const void *B, int n, int k, int r,
+                                float scale, uint32_t *status, cudaStream_t st) {
+  lora_weight_t wa{LORA_WEIGHT_BF16, A, nullptr, 0};
+  GroupArgs ga{wa, nullptr, W, k, 0};
+  GemmOpts o;
+  o.mode = kModeDx;
+  o.act = B;
+  o.act_cols = r;
+  o.M = n;
+  o.Kred = 64;
+  o.w_rows = r;
+  o.ga = &ga;
+  o.ng = 1;
+  o.rank_k = 0;
+  o.accumulate = 1;
+  o.acc_scale = scale;
+  o.status = status;
+  return run_gemm(o, st);
+}
+
+static lora_status_t check_merge(const void *A, const void *B, int n, int k, int r, float alpha,
+                                 int sign, const void *ws) {
+  if (n < 1 || k < 1 || n > (1 << 20) || k > (1 << 20)) return LORA_ERR_INVALID_ARG;
+  if (k % 64 || n % 64) return LORA_ERR_UNSUPPORTED;
+  if (!rank_ok(r)) return LORA_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(ws)) return LORA_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha) || (sign != 1 && sign != -1)) return LORA_ERR_INVALID_ARG;
+  return LORA_OK;
+}
+
+lora_status_t lora_merge(void *W, const void *A, const void *B, int n, int k, int r, float alpha,
+                         int sign, void *ws, size_t ws_bytes, lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = check_merge(A, B, n, k, r, alpha, sign, ws))) return s;
+  if (!aligned16(W)) return LORA_ERR_INVALID_ARG;
+  if (ws_bytes < lora_workspace_size(LORA_OP_MERGE, 1, k, n, r)) return LORA_ERR_WORKSPACE;
+  DeviceInfo di;
+  if ((s = device_info(&di))) return s;
+  return merge_bf16(W, A, B, n, k, r, (float)sign * alpha / (float)r, static_cast<uint32_t *>(ws),
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+lora_status_t lora_merge_nf4(uint8_t *codes, void *absmax, const void *A, const void *B, int n,
+                             int k, int r, float alpha, int sign, int blocksize, void *ws,
+                             size_t ws_bytes, lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = check_merge(A, B, n, k, r, alpha, sign, ws))) return s;
+  if (blocksize != 64) return LORA_ERR_UNSUPPORTED;
+  if (!aligned16(codes) || !aligned16(absmax)) return LORA_ERR_INVALID_ARG;
+  if (ws_bytes < lora_workspace_size(LORA_OP_MERGE_NF4, 1, k, n, r)) return LORA_ERR_WORKSPACE;
+  DeviceInfo di;
+  if ((s = device_info(&di))) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto *wbf = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(ws) + kStatusBytes);
+  auto *am = static_cast<__nv_bfloat16 *>(absmax);
+  // dequantise into the workspace, merge there, quantise back in place
+  if ((s = cuda_status(launch_nf4_dequant(codes, am, wbf, n, k, st)))) return s;
+  if ((s = merge_bf16(wbf, A, B, n, k, r, (float)sign * alpha / (float)r,
+                      static_cast<uint32_t *>(ws), st)))
+    return s;
+  return cuda_status(launch_nf4_quantize(wbf, codes, am, n, k, st));
 }
 
 lora_status_t nf4_dequant(const uint8_t *codes, const void *absmax, void *w_out, int n, int k,

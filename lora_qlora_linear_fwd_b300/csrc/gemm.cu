@@ -110,8 +110,9 @@ struct Nf4Cursor {
   bool in;                            // the piece lies inside W
   __device__ void tile(const GemmParams &p, int pc, int crank, int nk) {
     const int nt = it.nt();
-    const GemmGroup &G = p.grp[group_of(p, nt)];
-    const int nh = (nt - G.tile_begin) * 256 + crank * 128;
+    const WHalf wh = w_half(p, nt, (uint32_t)crank);
+    const GemmGroup &G = *wh.g;
+    const int nh = wh.nh;
     len = nk + (DX ? p.grp[0].n_extra : G.n_extra);
     if constexpr (DX) {
       const int ld = p.grp[0].ld_absmax;
@@ -241,9 +242,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       TileIter it;
       for (it.init(p.sched, pair); ok && it.valid(); it.next()) {
         const int m = it.m(), nt = it.nt();
-        const GemmGroup &G = p.grp[group_of(p, nt)];
-        const int n0 = (nt - G.tile_begin) * BN;
-        const int nh = n0 + (int)crank * 128;  // first N index of this CTA's half
+        const WHalf wh = w_half(p, nt, crank);
+        const GemmGroup &G = *wh.g;             // this CTA's weight group
+        const int nh = wh.nh;                   // first N index of this CTA's half
         const int row0 = m * (256 * MB) + (int)crank * 128;  // m-block mb: + 256·mb
         const int ne = DX ? p.grp[0].n_extra : G.n_extra;
         for (int kb = 0; kb < nk + ne; ++kb) {
@@ -295,7 +296,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
                 tma_load_2d_pair(sx + L::OFF_W, &R.tm_b, fb, nh, e * kBK);
                 tma_load_2d_pair(sx + L::OFF_W + 8192, &R.tm_b, fb, nh + 64, e * kBK);
               } else {             // B [n, r] K-major: own 128 rows x 64
-                tma_load_2d_pair(sx + L::OFF_W, &R.tm_b, fb, e * kBK, nh);
+                tma_load_2d_pair(sx + L::OFF_W, &R.tm_b, fb, e * kBK + R.b_shift, nh);
               }
             }
           }
@@ -397,6 +398,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     const uint32_t cs_bar = bar_cs + 8 * q;
     const uint32_t srow = base + L::OFF_CS + (uint32_t)row * kRopeRowPitch;
     uint32_t cs_phase = 0;
+    uint32_t nstore = 0;  // SwiGLU: stores issued by this warp
     bool cs_pending = false;  // a staged half has not been waited for
     int tile_count = 0;
     TileIter it;
@@ -404,8 +406,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     for (it.init(p.sched, pair); ok && it.valid(); it.next(), ++tile_count) {
       const int m = it.m(), nt = it.nt();
       const GemmGroup &G = p.grp[group_of(p, nt)];
-      const int n0 = (nt - G.tile_begin) * BN;
-      const int ncols = min(BN, G.ncols - n0);
+      // output columns of the tile (SwiGLU: 128 of h, g and u)
+      const int n0 = p.swiglu ? nt * 128 : (nt - G.tile_begin) * BN;
+      const int ncols = min(p.swiglu ? 128 : BN, G.ncols - n0);
 #pragma unroll 1
       for (int mb = 0; mb < MB; ++mb) {
         const int acc = MB == 1 ? (tile_count & 1) : mb;
@@ -423,9 +426,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
           break;
         }
         tc_fence_after();
-        if (DX && p.accumulate) {  // read-modify-write of dX: plain loads and stores
+        if (DX && p.accumulate) {  // read-modify-write of the output: plain loads and stores
           __nv_bfloat16 *orow = G.out + (size_t)(row_ok ? grow : 0) * G.ncols + n0;
-          epi_store_tile<BN, false>(tmem + t_lane + acc * BN, orow, row_ok, ncols, true, nullptr);
+          epi_accumulate_tile<BN>(tmem + t_lane + acc * BN, orow, row_ok, ncols, p.acc_scale);
+        } else if (!DX && !ROPE && p.swiglu) {
+          epi_store_swiglu(tmem + t_lane + acc * BN, epi_buf, p, n0, wrow0, ncols, lane, nstore);
         } else {
           if (!epi_store_tile_tma<BN, ROPE, STAGED>(tmem + t_lane + acc * BN, epi_buf, &G.tm_out,
                                                     n0, wrow0, ncols, cs, srow, cs_bar, cs_phase,
@@ -519,15 +524,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
         // (MN-major) into the W slot, counted on the code slot's barrier
         // (armed by the code producer)
         const int e = kb - nk;
-        const int nt = cur.it.nt();
-        const GemmGroup &G = p.grp[group_of(p, nt)];
-        const GemmGroup &R = DX ? p.grp[0] : G;
-        const int nh = (nt - G.tile_begin) * BN + (int)crank * 128;
+        const WHalf wh = w_half(p, cur.it.nt(), crank);
+        const GemmGroup &R = DX ? p.grp[0] : *wh.g;
+        const int nh = wh.nh;
         if constexpr (DX) {
           tma_load_2d(sw, &R.tm_b, cbar, nh, e * kBK);
           tma_load_2d(sw + 8192, &R.tm_b, cbar, nh + 64, e * kBK);
         } else {
-          tma_load_2d(sw, &R.tm_b, cbar, e * kBK, nh);
+          tma_load_2d(sw, &R.tm_b, cbar, e * kBK + R.b_shift, nh);
         }
       }
       // this K-block's codes (or rank tile) landed
@@ -580,8 +584,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       TileIter it;
       for (it.init(p.sched, pair); ok && it.valid(); it.next()) {
         const int nt = it.nt();
-        const GemmGroup &G = p.grp[group_of(p, nt)];
-        const int nh = (nt - G.tile_begin) * BN + (int)crank * 128;
+        const WHalf wh = w_half(p, nt, crank);
+        const GemmGroup &G = *wh.g;
+        const int nh = wh.nh;
         const int ne = DX ? p.grp[0].n_extra : G.n_extra;
         for (int kb = 0; kb < nk + ne; ++kb) {
           if (!mbar_wait(bar_cempty + 8 * cst, cph ^ 1u, abort_flag, p.status)) {

@@ -15,8 +15,24 @@ LORA_DEV bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
   return __all_sync(0xffffffffu, ok);
 }
 
+// Group of n-tile nt (its output columns, rank blocks and epilogue); the
+// SwiGLU pair's tiles belong to group 0 for these purposes.
 LORA_DEV int group_of(const GemmParams &p, int nt) {
-  return (p.num_groups > 1 && nt >= p.grp[1].tile_begin) ? 1 : 0;
+  return (!p.swiglu && p.num_groups > 1 && nt >= p.grp[1].tile_begin) ? 1 : 0;
+}
+
+// This CTA's half of the W tile of n-tile nt: its weight group and first N
+// row.  Normally rows [256·(nt − tile_begin) + 128·crank, +128) of the
+// tile's group; for the SwiGLU pair rows [128·nt, +128) of group crank
+// (gate or up).
+struct WHalf {
+  const GemmGroup *g;
+  int nh;
+};
+LORA_DEV WHalf w_half(const GemmParams &p, int nt, uint32_t crank) {
+  if (p.swiglu) return {&p.grp[crank], nt * 128};
+  const GemmGroup &G = p.grp[group_of(p, nt)];
+  return {&G, (nt - G.tile_begin) * 256 + (int)crank * 128};
 }
 
 LORA_DEV uint4 ld_shared_v4(uint32_t addr) {
@@ -91,91 +107,43 @@ LORA_DEV void nf4_decode_words(const uint32_t (&words)[8], uint32_t dst, const N
   }
 }
 
-// Output epilogue for one thread: BN accumulator columns at `t_acc` of one
-// output row -> bf16 at `orow` (ncols valid columns).  accumulate: add the
-// bf16 values already there.  ROPE: rotate-half per 128-wide head with the
-// cos/sin row `cs` (64 cos then 64 sin); columns (i, i+64) of a head are in
-// the same thread, so the pair is rotated in registers.
-template <int BN, bool ROPE>
-LORA_DEV void epi_store_tile(uint32_t t_acc, __nv_bfloat16 *orow, bool row_ok, int ncols,
-                             bool accumulate, const float *cs) {
-  if constexpr (!ROPE) {
+// Read-modify-write epilogue for one thread: BN accumulator columns at
+// `t_acc` of one output row are scaled by `scale` and added to the bf16
+// values already at `orow` (ncols valid columns), rounding once to bf16.
+// Used where the result accumulates into its destination (dX += ..., and
+// W ± s·B·A when merging an adapter into its weight).
+template <int BN>
+LORA_DEV void epi_accumulate_tile(uint32_t t_acc, __nv_bfloat16 *orow, bool row_ok, int ncols,
+                                  float scale) {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(t_acc + c * 32, r);
-      tmem_ld_wait();
-      if (row_ok && c * 32 < ncols) {
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-        float f[32];
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(t_acc + c * 32, r);
+    tmem_ld_wait();
+    if (row_ok && c * 32 < ncols) {
+      uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+      float f[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
-        if (accumulate) {
+      for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]) * scale;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 old = dst[j];
-            const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+      for (int j = 0; j < 4; ++j) {
+        const uint4 old = dst[j];
+        const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&ow[e]);
-              f[8 * j + 2 * e] += __low2float(h);
-              f[8 * j + 2 * e + 1] += __high2float(h);
-            }
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint4 w;
-          w.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
-          w.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
-          w.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
-          w.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
-          dst[j] = w;
+        for (int e = 0; e < 4; ++e) {
+          __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&ow[e]);
+          f[8 * j + 2 * e] += __low2float(h);
+          f[8 * j + 2 * e + 1] += __high2float(h);
         }
       }
-    }
-  } else {
-#pragma unroll 1
-    for (int h = 0; h < BN / 128; ++h) {
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        const int c0 = h * 128 + half * 32;
-        uint32_t ra[32], rb[32];
-        tmem_ld32(t_acc + c0, ra);
-        tmem_ld32(t_acc + c0 + 64, rb);
-        tmem_ld_wait();
-        if (row_ok && c0 < ncols) {
-          const float4 *cp = reinterpret_cast<const float4 *>(cs + half * 32);
-          const float4 *sp = reinterpret_cast<const float4 *>(cs + 64 + half * 32);
-          uint4 *da = reinterpret_cast<uint4 *>(orow + c0);
-          uint4 *db = reinterpret_cast<uint4 *>(orow + c0 + 64);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float4 c_lo = __ldg(cp + 2 * j), c_hi = __ldg(cp + 2 * j + 1);
-            const float4 s_lo = __ldg(sp + 2 * j), s_hi = __ldg(sp + 2 * j + 1);
-            const float co[8] = {c_lo.x, c_lo.y, c_lo.z, c_lo.w, c_hi.x, c_hi.y, c_hi.z, c_hi.w};
-            const float si[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
-            float oa[8], ob[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float a = __uint_as_float(ra[8 * j + e]);
-              const float b = __uint_as_float(rb[8 * j + e]);
-              oa[e] = a * co[e] - b * si[e];
-              ob[e] = b * co[e] + a * si[e];
-            }
-            uint4 wa, wb;
-            wa.x = pack_bf16x2(oa[0], oa[1]);
-            wa.y = pack_bf16x2(oa[2], oa[3]);
-            wa.z = pack_bf16x2(oa[4], oa[5]);
-            wa.w = pack_bf16x2(oa[6], oa[7]);
-            wb.x = pack_bf16x2(ob[0], ob[1]);
-            wb.y = pack_bf16x2(ob[2], ob[3]);
-            wb.z = pack_bf16x2(ob[4], ob[5]);
-            wb.w = pack_bf16x2(ob[6], ob[7]);
-            da[j] = wa;
-            db[j] = wb;
-          }
-        }
+      for (int j = 0; j < 4; ++j) {
+        uint4 w;
+        w.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
+        w.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
+        w.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
+        w.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
+        dst[j] = w;
       }
     }
   }
@@ -357,6 +325,57 @@ LORA_DEV bool epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap
     }
   }
   return true;
+}
+
+// SwiGLU epilogue for one warp (32 rows of the CTA's 128), [P4] §3.1 (the
+// activation joined to the linear layers before it): the tile's accumulator
+// holds the gate output g in columns [0, 128) and the up output u in
+// [128, 256).  Per 32-column chunk it stores g and u (when saved for the
+// backward) and h = silu(g)·u = g·u / (1 + e^{-g}), each rounded once from
+// fp32 to bf16, through the warp's two 2 KB staging buffers in turn and TMA
+// bulk stores at output column col0 + 32·chunk, row row0.  `nstore` counts
+// the warp's stores (it picks the buffer).
+LORA_DEV void epi_store_swiglu(uint32_t t_acc, uint32_t buf, const GemmParams &p, int col0,
+                               int row0, int ncols, int lane, uint32_t &nstore) {
+  auto at = [&](int q) -> uint32_t {
+    return (uint32_t)(lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4));
+  };
+  auto store = [&](const uint32_t (&v)[32], const CUtensorMap *map, int col) {
+    const uint32_t b = buf + (nstore & 1u) * 2048u;
+    ++nstore;
+    if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4(b + at(q), pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                   pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                   pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                   pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, b, col, row0);
+      bulk_commit();
+    }
+  };
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t rg[32], ru[32];
+    tmem_ld32(t_acc + c * 32, rg);
+    tmem_ld32(t_acc + 128 + c * 32, ru);
+    tmem_ld_wait();
+    if (c * 32 >= ncols) continue;
+    if (p.save_gu) {
+      store(rg, &p.grp[0].tm_out, col0 + c * 32);
+      store(ru, &p.grp[1].tm_out, col0 + c * 32);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float g = __uint_as_float(rg[j]);
+      rg[j] = __float_as_uint(g * __uint_as_float(ru[j]) / (1.0f + expf(-g)));
+    }
+    store(rg, &p.tm_h, col0 + c * 32);
+  }
 }
 
 // Position of output row `grow` for the RoPE epilogue; an out-of-range

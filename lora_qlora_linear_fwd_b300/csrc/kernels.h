@@ -74,6 +74,7 @@ struct GemmGroup {
   int ld_absmax;   // k / 64 (NF4)
   int sv_col;      // first column of this group's rank block in s·v / s·u
   int n_extra;     // extra 64-wide K-blocks (ceil(rank / 64))
+  int b_shift;     // FWD: x coordinate of rank K-block e in tm_b is 64·e + b_shift
 };
 
 struct GemmParams {
@@ -89,7 +90,16 @@ struct GemmParams {
   int kgroups;
   int ksplit;
   Schedule sched;
-  int accumulate;        // DX: dX += result instead of overwrite
+  int accumulate;        // DX: out += acc_scale·result instead of overwrite
+  float acc_scale;
+  // SwiGLU pair (FWD): n-tile t covers output columns [128t, 128t + 128);
+  // CTA c of a pair stages the rows of grp[c] (0: gate, 1: up), so a
+  // tile's accumulator holds g in columns [0, 128) and u in [128, 256).
+  // The epilogue stores h = silu(g)·u through tm_h and, when save_gu, g
+  // and u through grp[0].tm_out and grp[1].tm_out.
+  int swiglu;
+  int save_gu;
+  CUtensorMap tm_h;
   // RoPE epilogue (FWD mode)
   const int32_t *positions;
   const float *cos_sin;
@@ -216,9 +226,13 @@ cudaError_t launch_skinny_sk(const SkinnyParams &p, bool mn_major, int rp, cudaS
 
 // Elementwise / small helpers.
 // Backward set-up (one launch): inverse RoPE of dy1|dy2 into dy_out (when
-// dy1 is set), A_out = [A1; A2] (nproj == 2), Bt = diag(B1, B2)ᵀ.
+// dy1 is set) or the SwiGLU backward [dg | du] into dy_out (when sw_dh is
+// set), A_out = [A1; A2] (nproj == 2), Bt = diag(B1, B2)ᵀ.
 struct BwdPrep {
   const __nv_bfloat16 *dy1, *dy2;   // [M, n1], [M, n2]; dy1 null: no rotation
+  // SwiGLU (sw_dh set, n1 == n2 == n): dy_out = [dg | du] from the incoming
+  // dh and the saved gate / up outputs g, u [M, n]
+  const __nv_bfloat16 *sw_dh, *sw_g, *sw_u;
   __nv_bfloat16 *dy_out;            // [M, n1 + n2]
   const int32_t *pos;
   const float *cos_sin;

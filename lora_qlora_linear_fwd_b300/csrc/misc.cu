@@ -63,18 +63,66 @@ LORA_DEV void rope_bwd_item(const BwdPrep &p, size_t i) {
   *reinterpret_cast<uint4 *>(dst + g * 8 + 64) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
 }
 
+// SwiGLU backward of 8 consecutive columns of one row ("Unsloth框架" §3.1;
+// SwiGLU as in "GLU Variants Improve Transformer" §2): with σ = sigmoid(g),
+//   dg = dh·u·σ·(1 + g·(1 − σ)),   du = dh·g·σ,
+// in fp32 from the bf16 dh, g, u, each rounded once to bf16 into dY = [dg | du].
+LORA_DEV void swiglu_bwd_item(const BwdPrep &p, size_t i) {
+  const int n = p.n1;
+  const size_t m = i / (n / 8);
+  const int c = (int)(i % (n / 8)) * 8;
+  const size_t off = m * n + c;
+  const uint4 vh = *reinterpret_cast<const uint4 *>(p.sw_dh + off);
+  const uint4 vg = *reinterpret_cast<const uint4 *>(p.sw_g + off);
+  const uint4 vu = *reinterpret_cast<const uint4 *>(p.sw_u + off);
+  const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&vh);
+  const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&vg);
+  const __nv_bfloat162 *u2 = reinterpret_cast<const __nv_bfloat162 *>(&vu);
+  uint32_t og[4], ou[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float dg[2], du[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const float dh = t ? __high2float(h2[e]) : __low2float(h2[e]);
+      const float g = t ? __high2float(g2[e]) : __low2float(g2[e]);
+      const float u = t ? __high2float(u2[e]) : __low2float(u2[e]);
+      const float sg = 1.0f / (1.0f + expf(-g));
+      dg[t] = dh * u * sg * (1.0f + g * (1.0f - sg));
+      du[t] = dh * g * sg;
+    }
+    og[e] = pack_bf16x2(dg[0], dg[1]);
+    ou[e] = pack_bf16x2(du[0], du[1]);
+  }
+  __nv_bfloat16 *dst = p.dy_out + m * (size_t)(2 * n) + c;
+  *reinterpret_cast<uint4 *>(dst) = make_uint4(og[0], og[1], og[2], og[3]);
+  *reinterpret_cast<uint4 *>(dst + n) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+}
+
+// Work items of the gradient job: rotation (8 per row and head) or SwiGLU
+// (one per 8 columns of a row).
+__host__ __device__ static inline size_t dy_items(const BwdPrep &p) {
+  const int n = p.n1 + p.n2;
+  if (p.dy1) return (size_t)p.M * (n / 128) * 8;
+  if (p.sw_dh) return (size_t)p.M * (p.n1 / 8);
+  return 0;
+}
+
 __global__ void bwd_prep_kernel(const BwdPrep p) {
   grid_dep_launch();
   grid_dep_wait();
   const int n = p.n1 + p.n2, rl = p.nproj * p.r;
-  const size_t n_rope = p.dy1 ? (size_t)p.M * (n / 128) * 8 : 0;
+  const size_t n_rope = dy_items(p);
   const size_t n_a = p.nproj > 1 ? (size_t)rl * p.k / 8 : 0;   // 16-byte pieces
   const size_t n_b = (size_t)rl * n;
   const size_t total = n_rope + n_a + n_b;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
        i += (size_t)gridDim.x * blockDim.x) {
     if (i < n_rope) {
-      rope_bwd_item(p, i);
+      if (p.dy1)
+        rope_bwd_item(p, i);
+      else
+        swiglu_bwd_item(p, i);
     } else if (i < n_rope + n_a) {
       const size_t q = i - n_rope, half = (size_t)p.r * p.k / 8;
       const uint4 *src = reinterpret_cast<const uint4 *>(q < half ? p.A1 : p.A2);
@@ -92,8 +140,7 @@ __global__ void bwd_prep_kernel(const BwdPrep p) {
 
 cudaError_t launch_bwd_prep(const BwdPrep &p, cudaStream_t st) {
   const int n = p.n1 + p.n2, rl = p.nproj * p.r;
-  const size_t total = (p.dy1 ? (size_t)p.M * (n / 128) * 8 : 0) +
-                       (p.nproj > 1 ? (size_t)rl * p.k / 8 : 0) + (size_t)rl * n;
+  const size_t total = dy_items(p) + (p.nproj > 1 ? (size_t)rl * p.k / 8 : 0) + (size_t)rl * n;
   return launch_pdl("bwd_prep_kernel", bwd_prep_kernel, dim3(grid_for(total, 256, 16)), dim3(256), 0, st, 0u,
                     p);
 }

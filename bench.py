@@ -489,7 +489,7 @@ def profile_steps(rep, steps, flush):
     L = rep.L
     phases = {name: ph for name, ph in call_phases(rep.wl, rep.M)}
     calls = rep.calls()
-    cap = steps * sum(len(ph) for ph in phases.values()) + 16
+    cap = steps * sum(len(ph) for ph in phases.values()) + 16   # an upper bound
     launches = []   # (call, phase, flops, bytes)
     L.lora_profile_begin(cap)
     try:
@@ -500,6 +500,9 @@ def profile_steps(rep, steps, flush):
                 fn()
                 n = L.lora_kernel_launch_count() - c0
                 ph = phases[name]
+                if n == 1 and len(ph) == 2 and ph[0][0] == "fwd_rank":
+                    # bf16 W: x·Aᵀ is formed inside the fused GEMM (one launch)
+                    ph = [("fwd_gemm", ph[0][1] + ph[1][1], ph[1][2])]
                 if n != len(ph):
                     raise RuntimeError(f"{name}: {n} launches, expected {len(ph)}")
                 launches += [(name,) + x for x in ph]
@@ -580,6 +583,58 @@ def run_nf4_dequant_shapes(shapes, dev, flush, steps, warmup, peak):
                      "frac_hbm": round(gbs / peak, 3)})
         del codes, absmax, out
     return rows
+
+
+def nf4_fused_vs_unfused(name, proj, dev, flush, steps, warmup):
+    """The NF4 projection `proj` of workload `name`, forward and backward:
+    fused (NF4 codes decoded inside the GEMMs) against the unfused composition
+    the library also offers, nf4_dequant into a bf16 W followed by the bf16
+    calls; CUDA-event median over `steps` calls, L2 flushed between calls."""
+    import lora_qlora_linear_fwd_b300 as L
+    wl = WORKLOADS[name]
+    p = next(q for q in wl.projections if q.name == proj)
+    M, r = wl.M, wl.r
+    d = {k: v.to(dev) for k, v in draw_workload(name, seed=0, only=[proj])[proj].items()}
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    codes = torch.empty(p.n, p.k // 2, dtype=torch.uint8, device=dev)
+    absmax = torch.empty(p.n, p.k // 64, **bf)
+    L.nf4_quantize(d["W"], codes, absmax)
+    Wq = L.nf4_weight(codes, absmax)
+    Wb = torch.empty(p.n, p.k, **bf)
+    y = torch.empty(M, p.n, **bf)
+    dx = torch.empty(M, p.k, **bf)
+    dA = torch.empty(r, p.k, dtype=torch.float32, device=dev)
+    dB = torch.empty(p.n, r, dtype=torch.float32, device=dev)
+    wsf = L.workspace(L.OP_FWD, M, p.k, p.n, r, device=dev)
+    wsb = L.workspace(L.OP_BWD, M, p.k, p.n, r, device=dev)
+    calls = {
+        "fwd_fused": lambda: L.lora_linear_fwd(d["x"], Wq, d["A"], d["B"], y, wl.alpha, wsf),
+        "fwd_dequant_then_bf16": lambda: (L.nf4_dequant(codes, absmax, Wb),
+                                          L.lora_linear_fwd(d["x"], Wb, d["A"], d["B"], y,
+                                                            wl.alpha, wsf)),
+        "bwd_fused": lambda: L.lora_linear_bwd(d["x"], Wq, d["A"], d["B"], d["dY"], dx, dA, dB,
+                                               wl.alpha, wsb),
+        "bwd_dequant_then_bf16": lambda: (L.nf4_dequant(codes, absmax, Wb),
+                                          L.lora_linear_bwd(d["x"], Wb, d["A"], d["B"], d["dY"],
+                                                            dx, dA, dB, wl.alpha, wsb)),
+    }
+    out = {"workload": name, "projection": [proj, p.k, p.n], "M": M, "steps": steps}
+    for key, fn in calls.items():
+        for _ in range(warmup):
+            fn()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        out[key + "_ms"] = round(statistics.median(ts), 4)
+    out["fwd_unfused_over_fused"] = round(out["fwd_dequant_then_bf16_ms"] / out["fwd_fused_ms"], 3)
+    out["bwd_unfused_over_fused"] = round(out["bwd_dequant_then_bf16_ms"] / out["bwd_fused_ms"], 3)
+    return out
 
 
 def workload_line(rep, steps, warmup, flush, stream, peaks, pool):
@@ -741,6 +796,10 @@ def run_gpu(args, world, rank, local):
             "frac_of_pool_burst": line["tflops_frac_of_pool_peak"], "steps": args.steps,
             "M": M, "description": wl.description, "headline": True}
         line["per_workload"] = per
+        if wl.nf4:   # the fused NF4 GEMMs against dequantising first
+            line["nf4_fused_vs_unfused"] = nf4_fused_vs_unfused(args.workload, "gate_proj", dev,
+                                                                flush, 10, 3)
+            torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_tokens, args.cpu_tokens_1core)
     return line

@@ -180,7 +180,24 @@ Schedule make_schedule(int m_tiles, int n_tiles, int slots, int mb) {
   s.n_tiles = n_tiles;
   s.group_m = std::max(1, std::min(m_tiles, 8 / mb));
   s.workers = (int)std::max<long long>(1, std::min<long long>(slots, total));
+  s.contiguous = 0;
   return s;
+}
+
+// Whether a bf16 forward forms s·x·Aᵀ inside its GEMM (one launch) rather
+// than in a rank pass before it.  Inside the GEMM, x·Aᵀ is formed once per
+// m-block by the pair that meets it, so each pair must take its tiles as one
+// contiguous m-major run; on B300 that spreads the pairs over all of x and W
+// at once and loses the grouped raster's L2 reuse.  Measured on the
+// Llama-3-8B q/k + RoPE and MLP forwards (8 to 12 tiles per pair) the
+// one-launch form was 29-31% slower, so it is taken only when every tile has
+// a pair of its own (one wave), where the rank pass's launch and its extra
+// stream of x are what remains.
+bool fused_fwd_pays(int M, int n_tiles, int rl, bool rope) {
+  const long long tiles = (long long)((M + 255) / 256) * n_tiles;
+  const int fv = rank_pad(rl) <= 64 ? 64 : 128;
+  const int pairs = gemm_pair_capacity(kModeFwd, rope, false, 1, fv);
+  return pairs > 0 && tiles <= pairs;
 }
 
 // ------------------------------------------------------ fused GEMM set-up
@@ -224,6 +241,11 @@ struct GemmOpts {
   float acc_scale = 1.0f;
   int act_cols = 0;
   int w_rows = 0;
+  // FWD, bf16 W: form s·v = s·x·[a1; a2]ᵀ inside the GEMM (no rank pass, no
+  // s·v in memory; sv unused).  a2 null: one projection.
+  bool fused_v = false;
+  const void *a1 = nullptr, *a2 = nullptr;
+  float fv_scale = 0.0f;
 };
 
 bool make_w_map(CUtensorMap *m, const lora_weight_t &W, bool dx, bool nf4, int n, int k) {
@@ -246,10 +268,25 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
   std::memset(&p, 0, sizeof(p));
   // activation [M, Kred] and rank block [M, rl]: K-major, box 64 x 128
   const int act_cols = o.act_cols > 0 ? o.act_cols : o.Kred;
+  // the down-projection in the GEMM (bf16 forward): v up to fv columns
+  const int fv = (o.fused_v && !nf4 && !dx) ? (rank_pad(o.rl) <= 64 ? 64 : 128) : 0;
   if (!make_map(&p.tm_act, kBF16, 2, o.act, act_cols, o.M, (uint64_t)act_cols * 2, 64, 128, true) ||
-      (o.rank_k > 0 &&
+      (o.rank_k > 0 && !fv &&
        !make_map(&p.tm_sv, kBF16, 2, o.sv, o.rl, o.M, (uint64_t)o.rl * 2, 64, 128, true)))
     return LORA_ERR_CUDA;
+  if (fv) {
+    // CTA c stages rows [c·nv/2, +nv/2) of [a1; a2] (padded with zero rows)
+    const int nv = rank_pad(o.rl), h = nv / 2;
+    const bool two = o.a2 != nullptr;
+    const int rows = two ? o.rl / 2 : o.rl;
+    if (!make_map(&p.tm_a[0], kBF16, 2, o.a1, o.Kred, rows, (uint64_t)o.Kred * 2, 64, h, true) ||
+        (two &&
+         !make_map(&p.tm_a[1], kBF16, 2, o.a2, o.Kred, rows, (uint64_t)o.Kred * 2, 64, h, true)))
+      return LORA_ERR_CUDA;
+    p.fv_nv = nv;
+    p.fv_two = two ? 1 : 0;
+    p.fv_scale = o.fv_scale;
+  }
   int tiles = 0;
   const bool save_gu = o.swiglu && o.ga[0].out && o.ga[1].out;
   for (int g = 0; g < o.ng; ++g) {
@@ -280,6 +317,13 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
     G.ncols = ncols;
     G.sv_col = a.sv_col;
     G.n_extra = n_extra;
+    if (fv) {
+      // rank K-blocks run over the 64-column atoms of the staged s·v from the
+      // one holding sv_col; B is read shifted so its columns meet this
+      // group's rank columns inside the atom
+      G.b_shift = a.b_shift - a.sv_col % 64;
+      G.n_extra = (a.sv_col % 64 + o.rank_k + 63) / 64;
+    }
     if (o.swiglu) {  // both groups cover the same tiles of 128 output columns
       G.n_tiles = (ncols + 127) / 128;
       G.tile_begin = 0;
@@ -318,23 +362,24 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
   // kMb2TileCost mb = 1 tiles).
   const int m_blocks = (o.M + 255) / 256;
   int mb = 1;
-  int slots = gemm_pair_capacity(o.mode, o.rope, nf4, 1);
+  int slots = gemm_pair_capacity(o.mode, o.rope, nf4, 1, fv);
   if (slots < 1) return LORA_ERR_CUDA;
   if (nf4) {
-    const int slots2 = gemm_pair_capacity(o.mode, o.rope, nf4, 2);
+    const int slots2 = gemm_pair_capacity(o.mode, o.rope, nf4, 2, 0);
     if (slots2 < 1) return LORA_ERR_CUDA;
     const long long w1 = ((long long)m_blocks * tiles + slots - 1) / slots;
     const long long w2 = ((long long)((m_blocks + 1) / 2) * tiles + slots2 - 1) / slots2;
     if ((double)w2 * kMb2TileCost < (double)w1) mb = 2, slots = slots2;
   }
   p.sched = make_schedule((m_blocks + mb - 1) / mb, tiles, slots, mb);
+  p.sched.contiguous = fv ? 1 : 0;  // one run of tiles per m-block and pair
   p.accumulate = o.accumulate;
   p.acc_scale = o.acc_scale;
   p.positions = o.positions;
   p.cos_sin = o.cos_sin;
   p.max_pos = o.max_pos;
   p.status = o.status;
-  return cuda_status(launch_gemm_pair(p, o.mode, o.rope, nf4, mb, p.sched.workers, st));
+  return cuda_status(launch_gemm_pair(p, o.mode, o.rope, nf4, mb, fv, p.sched.workers, st));
 }
 
 // ------------------------------------------------------------ rank passes
@@ -762,7 +807,10 @@ lora_status_t lora_linear_fwd(const void *x, lora_weight_t W, const void *A, con
   uint32_t *status = static_cast<uint32_t *>(ws);
   void *sv = static_cast<uint8_t *>(ws) + kStatusBytes;
   const float scale = alpha / (float)r;
-  if ((s = fwd_rank(x, A, nullptr, M, k, r, scale, sv, status, st))) return s;
+  // bf16 W, one wave of tiles: one launch, s·x·Aᵀ formed in the GEMM;
+  // otherwise a rank pass first
+  const bool fused = W.type == LORA_WEIGHT_BF16 && fused_fwd_pays(M, (n + 255) / 256, r, false);
+  if (!fused && (s = fwd_rank(x, A, nullptr, M, k, r, scale, sv, status, st))) return s;
   GroupArgs ga{W, B, y, n, 0};
   GemmOpts o;
   o.mode = kModeFwd;
@@ -775,6 +823,9 @@ lora_status_t lora_linear_fwd(const void *x, lora_weight_t W, const void *A, con
   o.rl = r;
   o.rank_k = r;
   o.status = status;
+  o.fused_v = fused;
+  o.a1 = A;
+  o.fv_scale = scale;
   return run_gemm(o, st);
 }
 
@@ -871,10 +922,13 @@ lora_status_t lora_qk_rope_fwd(const void *x, lora_weight_t Wq, const void *Aq, 
     if ((s = cuda_status(launch_rope_cache(cb, max_pos, head_dim, rope_theta, st)))) return s;
     cache = cb;
   }
-  // rank pass over both projections at once: s·v = s·x·[Aq; Ak]ᵀ [M, 2r]
+  // s·v = s·x·[Aq; Ak]ᵀ [M, 2r]: formed in the GEMM for bf16 W, else by a
+  // rank pass over both projections at once
   void *sv = w8 + kStatusBytes;
   const float scale = alpha / (float)r;
-  if ((s = fwd_rank(x, Aq, Ak, M, hidden, r, scale, sv, status, st))) return s;
+  const bool fused = Wq.type == LORA_WEIGHT_BF16 &&
+                     fused_fwd_pays(M, (nq + 255) / 256 + (nk + 255) / 256, 2 * r, true);
+  if (!fused && (s = fwd_rank(x, Aq, Ak, M, hidden, r, scale, sv, status, st))) return s;
   // one GEMM launch over both weights; group g reduces over its r columns of s·v
   GroupArgs ga[2] = {{Wq, Bq, q, nq, 0}, {Wk, Bk, k_out, nk, r}};
   GemmOpts o;
@@ -892,6 +946,10 @@ lora_status_t lora_qk_rope_fwd(const void *x, lora_weight_t Wq, const void *Aq, 
   o.cos_sin = cache;
   o.max_pos = max_pos;
   o.status = status;
+  o.fused_v = fused;
+  o.a1 = Aq;
+  o.a2 = Ak;
+  o.fv_scale = scale;
   return run_gemm(o, st);
 }
 
@@ -1009,8 +1067,10 @@ lora_status_t lora_swiglu_fwd(const void *x, lora_weight_t Wg, const void *Ag, c
   uint32_t *status = static_cast<uint32_t *>(ws);
   void *sv = static_cast<uint8_t *>(ws) + kStatusBytes;
   const float scale = alpha / (float)r;
-  // rank pass over both projections: s·v = s·x·[Ag; Au]ᵀ [M, 2r]
-  if ((s = fwd_rank(x, Ag, Au, M, k, r, scale, sv, status, st))) return s;
+  // s·v = s·x·[Ag; Au]ᵀ [M, 2r]: formed in the GEMM for bf16 W, else by a
+  // rank pass over both projections
+  const bool fused = Wg.type == LORA_WEIGHT_BF16 && fused_fwd_pays(M, (n + 127) / 128, 2 * r, false);
+  if (!fused && (s = fwd_rank(x, Ag, Au, M, k, r, scale, sv, status, st))) return s;
   // one fused GEMM: CTA 0 of a pair stages gate rows, CTA 1 the up rows of
   // the same output columns; a rank K-block of [s·vg | s·vu] meets Bg in the
   // gate half and Bu (read r columns to the left, so it lines up with s·vu)
@@ -1029,6 +1089,10 @@ lora_status_t lora_swiglu_fwd(const void *x, lora_weight_t Wg, const void *Ag, c
   o.status = status;
   o.swiglu = true;
   o.h = h;
+  o.fused_v = fused;
+  o.a1 = Ag;
+  o.a2 = Au;
+  o.fv_scale = scale;
   return run_gemm(o, st);
 }
 

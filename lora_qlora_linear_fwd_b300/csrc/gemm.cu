@@ -59,7 +59,7 @@ constexpr int kNf4DecodeWarps = 8;
 // unambiguous for a waiter at most one phase ahead of the barrier, so each
 // waiter must see every phase of its barrier: the code and W rings have an
 // even number of slots, so that each slot belongs to one group.
-template <bool NF4, bool STAGED_ROPE = false, int MB = 1>
+template <bool NF4, bool STAGED_ROPE = false, int MB = 1, int FV = 0>
 struct PairSmem {
   static constexpr int X_BYTES = 128 * 128;  // own 128 rows x 64 K of one m-block
   static constexpr int W_BYTES = 128 * 128;  // own 128 N-rows x 64 K
@@ -75,9 +75,15 @@ struct PairSmem {
   static constexpr int AMAX_BYTES = AMAX_PRE * 256 * 4;  // per decode thread
   // RoPE with staged cos / sin: per epilogue warp 32 rows of one half
   static constexpr int CS_BYTES = STAGED_ROPE ? 4 * 32 * kRopeRowPitch : 0;
+  // Down-projection in the GEMM (FV = padded width of v, 64 or 128): the s·v
+  // operand of this CTA's 128 rows [FV/64 atoms of 128 rows x 128 B, 128-byte
+  // swizzle], whose bytes also serve, while a segment's first tile forms v,
+  // as a ring of four A tiles [FV/2 rows x 64 K each]
+  static constexpr int SV_BYTES = FV * 256;
+  static constexpr int A_SLOT_BYTES = FV * 64;
   static constexpr int MISC_BYTES = 1024;
-  static constexpr int FIXED =
-      WRING_BYTES + CRING_BYTES + EPI_BYTES + AMAX_BYTES + CS_BYTES + MISC_BYTES + 1024;
+  static constexpr int FIXED = WRING_BYTES + CRING_BYTES + EPI_BYTES + AMAX_BYTES + CS_BYTES +
+                               SV_BYTES + MISC_BYTES + 1024;
   static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int OFF_WRING = STAGES * STAGE_BYTES;
@@ -85,10 +91,12 @@ struct PairSmem {
   static constexpr int OFF_EPI = OFF_CRING + CRING_BYTES;
   static constexpr int OFF_AMAX = OFF_EPI + EPI_BYTES;
   static constexpr int OFF_CS = OFF_AMAX + AMAX_BYTES;
-  static constexpr int OFF_MISC = OFF_CS + CS_BYTES;
+  static constexpr int OFF_SV = OFF_CS + CS_BYTES;
+  static constexpr int OFF_MISC = OFF_SV + SV_BYTES;
   static constexpr int TOTAL = OFF_MISC + MISC_BYTES + 1024;
-  static constexpr int NUM_BARS =
-      2 * STAGES + 2 * C_STAGES + 2 * W_STAGES + 5 + (STAGED_ROPE ? 4 : 0);
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * C_STAGES + 2 * W_STAGES + 5 +
+                                  (STAGED_ROPE ? 4 : 0) + (FV ? 11 : 0);
+  static_assert(OFF_SV % 1024 == 0, "s·v region alignment");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 3 && (!NF4 || (W_STAGES >= 4 && C_STAGES >= 4)), "pipeline depth");
   static_assert(!NF4 || (W_STAGES % 2 == 0 && C_STAGES % 2 == 0), "one decode group per slot");
@@ -151,13 +159,15 @@ struct Nf4Cursor {
   }
 };
 
-template <int MODE, bool NF4, bool ROPE, int MB>
+template <int MODE, bool NF4, bool ROPE, int MB, int FV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1)
     lora_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   // RoPE cos / sin staged in shared memory (bf16 W; the NF4 rings leave no room)
   constexpr bool STAGED = ROPE && !NF4;
-  using L = PairSmem<NF4, STAGED, MB>;
+  using L = PairSmem<NF4, STAGED, MB, FV>;
   static_assert(MB == 1 || MB == 2, "m-blocks per tile");
+  static_assert(FV == 0 || (MODE == kModeFwd && !NF4 && MB == 1 && (FV == 64 || FV == 128)),
+                "down-projection in the GEMM: bf16 forward, one m-block per tile");
   constexpr int STAGES = L::STAGES;
   constexpr int BN = 256;
   constexpr bool DX = MODE == kModeDx;
@@ -187,6 +197,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   const uint32_t bar_acc_empty = bar_acc_full + 16;   // [2] leader: 8 warps drained b
   const uint32_t bar_drain = bar_acc_empty + 16;      // leader
   const uint32_t bar_cs = bar_drain + 8;              // [4] STAGED: cos / sin of epilogue warp q
+  // FV: A-tile ring in the s·v region, v complete, s·v staged, s·v free
+  const uint32_t bar_afull = bar_cs + (STAGED ? 32 : 0);  // [4] leader: A tiles of both CTAs
+  const uint32_t bar_aempty = bar_afull + 32;              // [4] both: v MMAs done with the slot
+  const uint32_t bar_vfull = bar_aempty + 32;              // both: v of the segment complete
+  const uint32_t bar_svready = bar_vfull + 8;              // leader: 8 warps staged s·v
+  const uint32_t bar_svfree = bar_svready + 8;             // both: the segment's MMAs read s·v
   const int misc_words = (8 * L::NUM_BARS) / 4;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC) + misc_words;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -211,6 +227,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     mbar_init(bar_drain, 1);
     if constexpr (STAGED)
       for (int q = 0; q < 4; ++q) mbar_init(bar_cs + 8 * q, 1);
+    if constexpr (FV > 0) {
+      for (int a = 0; a < 4; ++a) {
+        mbar_init(bar_afull + 8 * a, 1);
+        mbar_init(bar_aempty + 8 * a, 1);
+      }
+      mbar_init(bar_vfull, 1);
+      mbar_init(bar_svready, 8);
+      mbar_init(bar_svfree, 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -229,6 +254,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   const uint32_t lead_full = map_shared_rank(bar_full, 0);
   const uint32_t lead_wfull = map_shared_rank(bar_wfull, 0);
   const uint32_t lead_acc_empty = map_shared_rank(bar_acc_empty, 0);
+  const uint32_t lead_afull = FV > 0 ? map_shared_rank(bar_afull, 0) : 0u;
+  const uint32_t lead_svready = FV > 0 ? map_shared_rank(bar_svready, 0) : 0u;
+  const uint32_t sv_base = base + L::OFF_SV;
 
   if (warp == 0) {
     // ================================================================ producer
@@ -238,9 +266,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;  // K-blocks issued: stage s took every STAGES-th from the s-th
+      int aslot = 0;   // FV: A-tile ring
+      uint32_t aphase = 0;
+      int a_issued = 0;
+      int segs = 0;    // FV: segments started
+      const int fv_h = p.fv_nv / 2;  // A rows per CTA
       bool ok = true;
       TileIter it;
       for (it.init(p.sched, pair); ok && it.valid(); it.next()) {
+        const bool vtile = FV > 0 && it.seg_start();
+        if (vtile) {
+          // the previous segment's rank MMAs are done with the s·v region
+          if (segs > 0 &&
+              !mbar_wait(bar_svfree, (uint32_t)(segs - 1) & 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          ++segs;
+        }
         const int m = it.m(), nt = it.nt();
         const WHalf wh = w_half(p, nt, crank);
         const GemmGroup &G = *wh.g;             // this CTA's weight group
@@ -273,6 +316,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
                 tma_load_2d_pair(sx + L::OFF_W, tw, fb, kb * kBK, nh);
               }
             }
+            if (vtile) {
+              // this CTA's rows of the A tile of K-block kb into the ring
+              if (!mbar_wait(bar_aempty + 8 * aslot, aphase ^ 1u, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              if (leader) mbar_arrive_expect_tx(bar_afull + 8 * aslot, 2 * fv_h * 128);
+              tma_load_2d_pair(sv_base + aslot * L::A_SLOT_BYTES,
+                               p.fv_two ? &p.tm_a[crank] : &p.tm_a[0], lead_afull + 8 * aslot,
+                               kb * kBK, p.fv_two ? 0 : (int)crank * fv_h);
+              ++a_issued;
+              if (++aslot == 4) aslot = 0, aphase ^= 1u;
+            }
+          } else if (FV > 0) {
+            // rank K-block e: B only (s·v is staged in shared memory)
+            const int e = kb - nk;
+            if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * L::W_BYTES);
+            tma_load_2d_pair(sx + L::OFF_W, &G.tm_b, fb, e * kBK + G.b_shift, nh);
           } else {
             // rank K-block e: s·v (or s·u) columns and the matching B (or A)
             const int e = kb - nk;
@@ -311,15 +372,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
         const int fills = issued > s ? (issued - s + STAGES - 1) / STAGES : 0;
         if (fills > 0) mbar_wait_quiet(bar_empty + 8 * s, (uint32_t)((fills - 1) & 1), lim);
       }
+      if constexpr (FV > 0) {
+        for (int a = 0; a < 4; ++a) {
+          const int uses = a_issued > a ? (a_issued - a + 3) / 4 : 0;
+          if (uses > 0) mbar_wait_quiet(bar_aempty + 8 * a, (uint32_t)((uses - 1) & 1), lim);
+        }
+        if (segs > 0) mbar_wait_quiet(bar_svfree, (uint32_t)((segs - 1) & 1), lim);
+      }
     }
   } else if (warp == 1) {
     // ===================================================== MMA (even CTA)
     if (leader && lane == 0) {
       constexpr uint32_t idesc = make_idesc_bf16(256, BN, false, DX);
+      const uint32_t idesc_v = make_idesc_bf16(256, FV > 0 ? p.fv_nv : 16, false, false);
       int stage = 0;
       uint32_t phase = 0;
       int wslot = 0;
       uint32_t wphase = 0;
+      int aslot = 0;  // FV: A-tile ring
+      uint32_t aphase = 0;
+      int segs = 0;
       int tile_count = 0;
       int used[2] = {0, 0};  // tiles issued into each accumulator buffer
       bool ok = true;
@@ -328,12 +400,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
         const GemmGroup &G = p.grp[group_of(p, it.nt())];
         const int ne = DX ? p.grp[0].n_extra : G.n_extra;
         const int buf = tile_count & 1;  // MB = 1: the accumulator of this tile
+        const bool vtile = FV > 0 && it.seg_start();
         if constexpr (MB == 1) {
           if (used[buf] > 0 && !mbar_wait_cluster(bar_acc_empty + 8 * buf, (used[buf] - 1) & 1,
                                                   abort_flag, p.status))
             break;
           ++used[buf];
+          // v goes to the other buffer's first columns: its previous tile
+          // must be drained
+          if (vtile && used[buf ^ 1] > 0 &&
+              !mbar_wait_cluster(bar_acc_empty + 8 * (buf ^ 1), (used[buf ^ 1] - 1) & 1,
+                                 abort_flag, p.status))
+            break;
         }
+        if (vtile) ++segs;
         tc_fence_after();
         for (int kb = 0; ok && kb < nk + ne; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) {
@@ -344,9 +424,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
             ok = false;
             break;
           }
+          if (vtile && kb < nk &&
+              !mbar_wait(bar_afull + 8 * aslot, aphase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (FV > 0 && vtile && kb == nk &&
+              !mbar_wait_cluster(bar_svready, (uint32_t)(segs - 1) & 1u, abort_flag, p.status)) {
+            ok = false;  // the first rank K-block needs the segment's s·v staged
+            break;
+          }
           tc_fence_after();
           const uint32_t sx = base + stage * L::STAGE_BYTES;
           const uint32_t sw = NF4 ? base + L::OFF_WRING + wslot * L::W_BYTES : sx + L::OFF_W;
+          // FV rank K-block: the activation is atom (sv_col/64 + e) of s·v
+          const uint32_t sa = (FV > 0 && kb >= nk)
+                                  ? sv_base + (uint32_t)(G.sv_col / 64 + (kb - nk)) * 16384u
+                                  : sx;
 #pragma unroll
           for (int mb = 0; mb < MB; ++mb) {
             if (MB == 2 && kb == 0 && tile_count > 0) {
@@ -361,7 +455,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
             const uint32_t t_acc = tmem + (MB == 1 ? buf : mb) * BN;
 #pragma unroll
             for (int ks = 0; ks < kBK / 16; ++ks) {
-              const uint64_t da = make_sdesc(sx + mb * L::X_BYTES + ks * 32, 16, 1024, kSw128);
+              const uint64_t da = make_sdesc(sa + mb * L::X_BYTES + ks * 32, 16, 1024, kSw128);
               uint64_t dw;
               if constexpr (DX)  // MN-major: 16 K-rows per step; two 64-wide blocks 8 KB apart
                 dw = make_sdesc(sw + ks * 2048, 8192, 1024, kSw128);
@@ -374,6 +468,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
             if (MB == 2 && kb == nk + ne - 1) tc_commit_pair(bar_acc_full + 8 * mb, kBoth);
           }
           if (!ok) break;
+          if (vtile && kb < nk) {
+            // v += x·Aᵀ on the same x tile (v in the other buffer's columns)
+            const uint32_t t_v = tmem + (buf ^ 1) * BN;
+            const uint32_t sa_ring = sv_base + aslot * L::A_SLOT_BYTES;
+#pragma unroll
+            for (int ks = 0; ks < kBK / 16; ++ks)
+              tc_mma_pair(t_v, make_sdesc(sx + ks * 32, 16, 1024, kSw128),
+                          make_sdesc(sa_ring + ks * 32, 16, 1024, kSw128), idesc_v,
+                          (kb | ks) != 0 ? 1u : 0u);
+            tc_commit_pair(bar_aempty + 8 * aslot, kBoth);
+            if (++aslot == 4) aslot = 0, aphase ^= 1u;
+            if (kb == nk - 1) tc_commit_pair(bar_vfull, kBoth);  // v complete
+          }
           tc_commit_pair(bar_empty + 8 * stage, kBoth);
           if (++stage == STAGES) stage = 0, phase ^= 1u;
           if constexpr (NF4) {
@@ -382,6 +489,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
           }
         }
         if (!ok) break;
+        // the run's last tile: its rank MMAs were the last reads of s·v
+        if (FV > 0 && it.seg_last()) tc_commit_pair(bar_svfree, kBoth);
         if constexpr (MB == 1) tc_commit_pair(bar_acc_full + 8 * buf, kBoth);
       }
       if (*abort_flag) {
@@ -399,6 +508,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     const uint32_t srow = base + L::OFF_CS + (uint32_t)row * kRopeRowPitch;
     uint32_t cs_phase = 0;
     uint32_t nstore = 0;  // SwiGLU: stores issued by this warp
+    int segs = 0;         // FV: segments whose s·v this warp staged
     bool cs_pending = false;  // a staged half has not been waited for
     int tile_count = 0;
     TileIter it;
@@ -406,6 +516,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
     for (it.init(p.sched, pair); ok && it.valid(); it.next(), ++tile_count) {
       const int m = it.m(), nt = it.nt();
       const GemmGroup &G = p.grp[group_of(p, nt)];
+      if (FV > 0 && it.seg_start()) {
+        // v of the segment (in the other buffer): s·v into the operand region
+        if (!warp_wait(bar_vfull, (uint32_t)segs & 1u, abort_flag, p.status)) break;
+        ++segs;
+        tc_fence_after();
+        stage_sv<FV>(tmem + t_lane + ((tile_count & 1) ^ 1) * BN, base + L::OFF_SV, row, p.fv_nv,
+                     p.fv_scale);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lead_svready);
+      }
       // output columns of the tile (SwiGLU: 128 of h, g and u)
       const int n0 = p.swiglu ? nt * 128 : (nt - G.tile_begin) * BN;
       const int ncols = min(p.swiglu ? 128 : BN, G.ncols - n0);
@@ -630,10 +752,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
   }
 }
 
-template <int MODE, bool NF4, bool ROPE, int MB>
+template <int MODE, bool NF4, bool ROPE, int MB, int FV>
 static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t st) {
-  using L = PairSmem<NF4, ROPE && !NF4, MB>;
-  auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE, MB>;
+  using L = PairSmem<NF4, ROPE && !NF4, MB, FV>;
+  auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE, MB, FV>;
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
   if (e != cudaSuccess) return e;
@@ -643,21 +765,21 @@ static cudaError_t launch_pair_one(const GemmParams &p, int pairs, cudaStream_t 
                                     : "lora_gemm_pair_kernel<fwd,nf4,rope>")
                          : (MB == 2 ? "lora_gemm_pair_kernel<fwd,nf4,mb2>"
                                     : "lora_gemm_pair_kernel<fwd,nf4>"))
-                 : (ROPE ? (MB == 2 ? "lora_gemm_pair_kernel<fwd,bf16,rope,mb2>"
-                                    : "lora_gemm_pair_kernel<fwd,bf16,rope>")
-                         : (MB == 2 ? "lora_gemm_pair_kernel<fwd,bf16,mb2>"
-                                    : "lora_gemm_pair_kernel<fwd,bf16>")))
+                 : (ROPE ? (FV ? "lora_gemm_pair_kernel<fwd,bf16,rope,xa>"
+                               : "lora_gemm_pair_kernel<fwd,bf16,rope>")
+                         : (FV ? "lora_gemm_pair_kernel<fwd,bf16,xa>"
+                               : "lora_gemm_pair_kernel<fwd,bf16>")))
           : (NF4 ? (MB == 2 ? "lora_gemm_pair_kernel<dx,nf4,mb2>" : "lora_gemm_pair_kernel<dx,nf4>")
-                 : (MB == 2 ? "lora_gemm_pair_kernel<dx,bf16,mb2>" : "lora_gemm_pair_kernel<dx,bf16>"));
+                 : "lora_gemm_pair_kernel<dx,bf16>");
   return launch_pdl(name, kern, dim3(2 * pairs), dim3(pair_threads(NF4)), L::TOTAL, st, 0u, p);
 }
 
 // Co-resident CTA pairs of one kernel on the current device (cached per
 // device; 0 if the query fails).
-template <int MODE, bool NF4, bool ROPE, int MB>
+template <int MODE, bool NF4, bool ROPE, int MB, int FV>
 static int pair_capacity() {
-  using L = PairSmem<NF4, ROPE && !NF4, MB>;
-  auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE, MB>;
+  using L = PairSmem<NF4, ROPE && !NF4, MB, FV>;
+  auto kern = lora_gemm_pair_kernel<MODE, NF4, ROPE, MB, FV>;
   static std::atomic<uint64_t> attr_done{0};
   static std::atomic<int> cached[kMaxDevices];  // pairs + 1; 0: not queried yet
   int dev = 0;
@@ -679,50 +801,57 @@ static int pair_capacity() {
   return n;
 }
 
-// Launch (cap == nullptr) or capacity query (*cap) of the variant
-// (MODE, NF4, rope, mb).  RoPE applies to the forward only; two m-blocks
-// per tile are compiled for NF4 weights.
-template <int MODE, bool NF4>
-static cudaError_t pair_dispatch(const GemmParams &p, bool rope, int mb, int pairs, int *cap,
-                                 cudaStream_t st) {
-  constexpr bool kRope = MODE == kModeFwd;
-  if constexpr (NF4) {
-    if (mb == 2) {
-      if (kRope && rope) {
-        if (cap) return *cap = pair_capacity<MODE, NF4, kRope, 2>(), cudaSuccess;
-        return launch_pair_one<MODE, NF4, kRope, 2>(p, pairs, st);
-      }
-      if (cap) return *cap = pair_capacity<MODE, NF4, false, 2>(), cudaSuccess;
-      return launch_pair_one<MODE, NF4, false, 2>(p, pairs, st);
-    }
-  }
-  if (mb != 1) return cudaErrorInvalidValue;
-  if (kRope && rope) {
-    if (cap) return *cap = pair_capacity<MODE, NF4, kRope, 1>(), cudaSuccess;
-    return launch_pair_one<MODE, NF4, kRope, 1>(p, pairs, st);
-  }
-  if (cap) return *cap = pair_capacity<MODE, NF4, false, 1>(), cudaSuccess;
-  return launch_pair_one<MODE, NF4, false, 1>(p, pairs, st);
+template <int MODE, bool NF4, bool ROPE, int MB, int FV>
+static cudaError_t run_or_query(const GemmParams &p, int pairs, int *cap, cudaStream_t st) {
+  if (cap) return *cap = pair_capacity<MODE, NF4, ROPE, MB, FV>(), cudaSuccess;
+  return launch_pair_one<MODE, NF4, ROPE, MB, FV>(p, pairs, st);
 }
 
-cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int mb,
+// Launch (cap == nullptr) or capacity query (*cap) of the variant
+// (MODE, NF4, rope, mb, fv).  RoPE applies to the forward only; two
+// m-blocks per tile are compiled for NF4 weights, the down-projection in the
+// GEMM (fv = 64 or 128, the padded width of v it stages) for the bf16
+// forward.
+template <int MODE, bool NF4>
+static cudaError_t pair_dispatch(const GemmParams &p, bool rope, int mb, int fv, int pairs,
+                                 int *cap, cudaStream_t st) {
+  constexpr bool FWD = MODE == kModeFwd;
+  if constexpr (NF4) {
+    if (fv != 0) return cudaErrorInvalidValue;
+    if (mb == 2)
+      return (FWD && rope) ? run_or_query<MODE, NF4, FWD, 2, 0>(p, pairs, cap, st)
+                           : run_or_query<MODE, NF4, false, 2, 0>(p, pairs, cap, st);
+  } else if constexpr (FWD) {
+    if (fv == 64)
+      return rope ? run_or_query<MODE, NF4, true, 1, 64>(p, pairs, cap, st)
+                  : run_or_query<MODE, NF4, false, 1, 64>(p, pairs, cap, st);
+    if (fv == 128)
+      return rope ? run_or_query<MODE, NF4, true, 1, 128>(p, pairs, cap, st)
+                  : run_or_query<MODE, NF4, false, 1, 128>(p, pairs, cap, st);
+  }
+  if (mb != 1 || fv != 0) return cudaErrorInvalidValue;
+  return (FWD && rope) ? run_or_query<MODE, NF4, FWD, 1, 0>(p, pairs, cap, st)
+                       : run_or_query<MODE, NF4, false, 1, 0>(p, pairs, cap, st);
+}
+
+cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int mb, int fv,
                              int pairs, cudaStream_t st) {
   if (mode == kModeFwd)
-    return nf4 ? pair_dispatch<kModeFwd, true>(p, rope, mb, pairs, nullptr, st)
-               : pair_dispatch<kModeFwd, false>(p, rope, mb, pairs, nullptr, st);
-  return nf4 ? pair_dispatch<kModeDx, true>(p, false, mb, pairs, nullptr, st)
-             : pair_dispatch<kModeDx, false>(p, false, mb, pairs, nullptr, st);
+    return nf4 ? pair_dispatch<kModeFwd, true>(p, rope, mb, fv, pairs, nullptr, st)
+               : pair_dispatch<kModeFwd, false>(p, rope, mb, fv, pairs, nullptr, st);
+  return nf4 ? pair_dispatch<kModeDx, true>(p, false, mb, fv, pairs, nullptr, st)
+             : pair_dispatch<kModeDx, false>(p, false, mb, fv, pairs, nullptr, st);
 }
 
-int gemm_pair_capacity(int mode, bool rope, bool nf4, int mb) {
+int gemm_pair_capacity(int mode, bool rope, bool nf4, int mb, int fv) {
   int cap = 0;
   GemmParams dummy;
   if (mode == kModeFwd)
-    nf4 ? pair_dispatch<kModeFwd, true>(dummy, rope, mb, 0, &cap, nullptr)
-        : pair_dispatch<kModeFwd, false>(dummy, rope, mb, 0, &cap, nullptr);
+    nf4 ? pair_dispatch<kModeFwd, true>(dummy, rope, mb, fv, 0, &cap, nullptr)
+        : pair_dispatch<kModeFwd, false>(dummy, rope, mb, fv, 0, &cap, nullptr);
   else
-    nf4 ? pair_dispatch<kModeDx, true>(dummy, false, mb, 0, &cap, nullptr)
-        : pair_dispatch<kModeDx, false>(dummy, false, mb, 0, &cap, nullptr);
+    nf4 ? pair_dispatch<kModeDx, true>(dummy, false, mb, fv, 0, &cap, nullptr)
+        : pair_dispatch<kModeDx, false>(dummy, false, mb, fv, 0, &cap, nullptr);
   return cap;
 }
 

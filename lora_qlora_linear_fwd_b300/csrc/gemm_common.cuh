@@ -378,6 +378,36 @@ LORA_DEV void epi_store_swiglu(uint32_t t_acc, uint32_t buf, const GemmParams &p
   }
 }
 
+// Down-projection in the GEMM: this thread's row of v (TMEM columns
+// [0, nv) at t_v, fp32) scaled by `scale`, rounded to bf16 and written into
+// the s·v operand region `sv` [FV/64 atoms][128 rows x 128 B] in the
+// 128-byte-swizzled K-major layout the MMA reads.  Columns from nv on are
+// written as zeros (the rank K-blocks read whole 64-column atoms).
+template <int FV>
+LORA_DEV void stage_sv(uint32_t t_v, uint32_t sv, int row, int nv, float scale) {
+#pragma unroll 1
+  for (int c = 0; c < FV / 32; ++c) {
+    uint32_t r[32];
+    if (c * 32 < nv) {  // nv is uniform across the warp
+      tmem_ld32(t_v + c * 32, r);
+      tmem_ld_wait();
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      r[j] = __float_as_uint(c * 32 + j < nv ? __uint_as_float(r[j]) * scale : 0.0f);
+    const uint32_t rowp = sv + (uint32_t)(c >> 1) * 16384u + (uint32_t)row * 128u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t chunk = (uint32_t)((c & 1) * 4 + q);
+      st_shared_v4(rowp + ((chunk ^ ((uint32_t)row & 7u)) << 4),
+                   pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1])),
+                   pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
+                   pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
+                   pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+    }
+  }
+}
+
 // Position of output row `grow` for the RoPE epilogue; an out-of-range
 // position is reported in the status word and replaced by 0 (no read
 // outside the cache).

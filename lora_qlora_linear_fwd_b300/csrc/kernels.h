@@ -100,6 +100,16 @@ struct GemmParams {
   int swiglu;
   int save_gu;
   CUtensorMap tm_h;
+  // Down-projection in the GEMM (FWD, contiguous schedule): on the first
+  // tile of each m-block's run of tiles the pair also forms v = x·Aᵀ
+  // (N = fv_nv, the padded rank; CTA c stages rows [c·fv_nv/2, +fv_nv/2) of
+  // [A1; A2] from tm_a[c] when fv_two, else from tm_a[0] at that row), and
+  // stages s·v (scaled by fv_scale) in shared memory as the rank K-blocks'
+  // activation for every tile of the run.
+  CUtensorMap tm_a[2];
+  int fv_nv;
+  int fv_two;
+  float fv_scale;
   // RoPE epilogue (FWD mode)
   const int32_t *positions;
   const float *cos_sin;
@@ -150,10 +160,12 @@ cudaError_t launch_pdl(const char *name, void (*kern)(KArgs...), dim3 grid, dim3
 }
 
 // Two-SM (CTA pair) fused GEMM: (256·mb) x 256 tiles over `pairs` persistent
-// pairs; p.sched counts tiles of mb m-blocks.  mb = 2 exists for NF4 weights.
-cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int mb,
+// pairs; p.sched counts tiles of mb m-blocks.  mb = 2 exists for NF4
+// weights; fv = 64 / 128 (the bf16 forward with the down-projection formed in
+// the GEMM, v up to fv columns wide) needs p.sched.contiguous.
+cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int mb, int fv,
                              int pairs, cudaStream_t st);
-int gemm_pair_capacity(int mode, bool rope, bool nf4, int mb);  // max co-resident pairs
+int gemm_pair_capacity(int mode, bool rope, bool nf4, int mb, int fv);  // max co-resident pairs
 
 // Skinny rank-r products on the tensor cores:
 //   KMAJOR  (v, u):  g[t][j] = Σ_c P[t,c]·Q[j,c]            P = x or dY, Q = A or Bᵀ

@@ -70,19 +70,24 @@ def test_nf4_quantize_parity(n, k):
 
 @pytest.mark.gpu
 def test_profile_session_times_each_launch_of_a_call():
-    """Per-launch timing: one forward call is two launches (rank pass, fused
-    GEMM), each with a positive time, in launch order."""
-    d = draw_projection(torch.Generator().manual_seed(5), 512, 512, 768, 16)
-    x, W, A, B = (cuda(d[k]) for k in ("x", "W", "A", "B"))
-    y = torch.empty(512, 768, dtype=torch.bfloat16, device="cuda")
-    ws = L.workspace(L.OP_FWD, 512, 512, 768, 16)
+    """Per-launch timing: one backward call is four launches (set-up, rank
+    pass, dX GEMM, dA/dB pass), each with a positive time, in launch order."""
+    M, k, n, r = 512, 512, 768, 16
+    d = draw_projection(torch.Generator().manual_seed(5), M, k, n, r)
+    x, W, A, B, dy = (cuda(d[t]) for t in ("x", "W", "A", "B", "dY"))
+    dx = torch.empty(M, k, dtype=torch.bfloat16, device="cuda")
+    dA = torch.empty(r, k, dtype=torch.float32, device="cuda")
+    dB = torch.empty(n, r, dtype=torch.float32, device="cuda")
+    ws = L.workspace(L.OP_BWD, M, k, n, r)
     L.lora_profile_begin(8)
     c0 = L.lora_kernel_launch_count()
-    L.lora_linear_fwd(x, W, A, B, y, 16.0, ws)
-    n = L.lora_kernel_launch_count() - c0
+    L.lora_linear_bwd(x, W, A, B, dy, dx, dA, dB, 16.0, ws)
+    n_launch = L.lora_kernel_launch_count() - c0
     got = L.lora_profile_end(8)
-    assert n == 2 and len(got) == 2
-    assert got[0][0].startswith("lora_skinny") and got[1][0] == "lora_gemm_pair_kernel<fwd,bf16>"
+    assert n_launch == 4 and len(got) == 4
+    names = [nm for nm, _ in got]
+    assert names[0] == "bwd_prep_kernel" and names[2] == "lora_gemm_pair_kernel<dx,bf16>"
+    assert names[1].startswith("lora_skinny") and names[3].startswith("lora_skinny")
     assert all(ms > 0.0 for _, ms in got)
     # the session is closed: a second end is an argument error
     with pytest.raises(L.LoraError):

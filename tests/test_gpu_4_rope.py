@@ -72,8 +72,9 @@ def test_qk_rope_position_zero_is_plain_projection():
     assert rel_err(np64(yq), wq) <= TOL_BF16 and rel_err(np64(yk), wk) <= TOL_BF16
 
 
-@pytest.mark.parametrize("M,hidden,nqh,nkh,r", [(300, 256, 2, 1, 16), (256, 512, 4, 2, 64)])
-def test_qk_rope_bwd_parity(M, hidden, nqh, nkh, r):
+@pytest.mark.parametrize("M,hidden,nqh,nkh,r,accumulate", [
+    (300, 256, 2, 1, 16, False), (256, 512, 4, 2, 64, False), (300, 256, 2, 1, 16, True)])
+def test_qk_rope_bwd_parity(M, hidden, nqh, nkh, r, accumulate):
     x, q, k = _draw(M, hidden, nqh, nkh, r, seed=7 * M + r)
     max_pos = 8192
     pos = np.random.default_rng(M + 1).integers(0, max_pos, size=M)
@@ -84,19 +85,23 @@ def test_qk_rope_bwd_parity(M, hidden, nqh, nkh, r):
     nq, nk = q["W"].shape[0], k["W"].shape[0]
     cache = torch.empty(max_pos, 128, dtype=torch.float32, device="cuda")
     L.lora_rope_cache_build(cache, max_pos, 128, THETA)
-    dx = torch.full((M, hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dx0 = draw_shared_x(torch.Generator().manual_seed(M + 99), M, hidden)  # prior dX (bf16)
+    dx = (cuda(dx0) if accumulate else
+          torch.full((M, hidden), float("nan"), dtype=torch.bfloat16, device="cuda"))
     f32 = dict(dtype=torch.float32, device="cuda")
     dAq, dBq = torch.empty(r, hidden, **f32), torch.empty(nq, r, **f32)
     dAk, dBk = torch.empty(r, hidden, **f32), torch.empty(nk, r, **f32)
     ws = L.workspace(L.OP_QK_ROPE_BWD, M, hidden, nq + nk, r)
     L.lora_qk_rope_bwd(dev["x"], dev["Wq"], dev["Aq"], dev["Bq"], dev["Wk"], dev["Ak"],
                        dev["Bk"], dev["dq"], dev["dk"], dx, dAq, dBq, dAk, dBk, 16.0, THETA,
-                       posd, cache, max_pos, ws)
+                       posd, cache, max_pos, ws, accumulate_dx=accumulate)
     torch.cuda.synchronize()
     assert L.lora_read_device_status(ws) == 0
-    want = ref.qk_rope_bwd(np64(x), np64(q["W"]), np64(q["A"]), np64(q["B"]), np64(k["W"]),
-                           np64(k["A"]), np64(k["B"]), np64(q["dY"]), np64(k["dY"]), 16.0, pos,
-                           THETA)
+    want = list(ref.qk_rope_bwd(np64(x), np64(q["W"]), np64(q["A"]), np64(q["B"]),
+                                np64(k["W"]), np64(k["A"]), np64(k["B"]), np64(q["dY"]),
+                                np64(k["dY"]), 16.0, pos, THETA))
+    if accumulate:       # dX += the q/k gradient
+        want[0] = want[0] + np64(dx0)
     got = (dx, dAq, dBq, dAk, dBk)
     errs = [rel_err(np64(g), w) for g, w in zip(got, want)]
     if errs[0] > TOL_BF16 or max(errs[1:]) > TOL_F32:

@@ -126,8 +126,10 @@ def test_rank_pass_schedule_runs_and_matches(M, k, n, r, schedule):
     Wd = cuda(d["W"])
     y, fnames = _fwd(d, L.bf16_weight(Wd), r)
     got, bnames = _bwd(d, L.bf16_weight(Wd), r)
-    rank = [nm for nm in fnames + bnames if nm.startswith("lora_skinny")]
-    assert len(rank) == 3 and all(nm.startswith(schedule + "<") for nm in rank), rank
+    # the bf16 forward forms s·x·Aᵀ in its GEMM; the backward has two rank passes
+    assert not any(nm.startswith("lora_skinny") for nm in fnames), fnames
+    rank = [nm for nm in bnames if nm.startswith("lora_skinny")]
+    assert len(rank) == 2 and all(nm.startswith(schedule + "<") for nm in rank), rank
     x, W, A, B, dY = (np64(d[t]) for t in ("x", "W", "A", "B", "dY"))
     rows = np.random.default_rng(0).choice(M, 256, replace=False)
     assert rel_err(np64(y)[rows], ref.lora_fwd(x[rows], W, A, B, ALPHA)) <= TOL_BF16
@@ -135,3 +137,25 @@ def test_rank_pass_schedule_runs_and_matches(M, k, n, r, schedule):
     assert rel_err(np64(got[0])[rows], dx[rows]) <= TOL_BF16
     assert rel_err(np64(got[1]), dA) <= TOL_F32
     assert rel_err(np64(got[2]), dB) <= TOL_F32
+
+
+@pytest.mark.parametrize("M,k,n,r,fused", [
+    (700, 1024, 2048, 16, True),     # 3 x 8 tiles: one wave of pairs
+    (257, 256, 768, 64, True),
+    (2304, 512, 4096, 64, False),    # 9 x 16 tiles: more than one wave
+])
+def test_bf16_forward_launches(M, k, n, r, fused):
+    """A bf16 forward whose tiles fit in one wave of CTA pairs forms s·x·Aᵀ
+    inside the fused GEMM ("UnSloth加速微调体验" §算子融合: one pass, no
+    intermediate): one launch, s·v only in shared memory.  Larger ones run
+    the rank pass first (the measured faster form on B300)."""
+    d = draw_projection(torch.Generator().manual_seed(66), M, k, n, r)
+    Wd = cuda(d["W"])
+    y, names = _fwd(d, L.bf16_weight(Wd), r)
+    if fused:
+        assert names == ["lora_gemm_pair_kernel<fwd,bf16,xa>"], names
+    else:
+        assert len(names) == 2 and names[0].startswith("lora_skinny"), names
+        assert names[1] == "lora_gemm_pair_kernel<fwd,bf16>", names
+    want = ref.lora_fwd(np64(d["x"]), np64(d["W"]), np64(d["A"]), np64(d["B"]), ALPHA)
+    assert rel_err(np64(y), want) <= TOL_BF16

@@ -24,6 +24,9 @@ Sources (web pages about Unsloth; cited by title and section):
 * [SwiGLU] Shazeer 2020, "GLU Variants Improve Transformer", §2: the
   gated unit ``Swish_1(x·W)·(x·V)`` with ``Swish_1(t) = t·sigmoid(t)``
   (SiLU); the pages name SwiGLU but do not write it out.
+* [Philox] Salmon, Moraes, Dror, Shaw 2011, "Parallel random numbers: as easy
+  as 1, 2, 3", §4 (the Philox counter-based generator; 4x64 words, 10
+  rounds): the generator the dropout mask is drawn from.
 * [QLoRA] Dettmers et al. 2023, "QLoRA: Efficient Finetuning of Quantized
   LLMs", §3 "4-bit NormalFloat Quantization" and the NF4 table in its
   appendix: the pages name NF4 but do not give its levels.
@@ -50,6 +53,8 @@ __all__ = [
     "qk_rope_fwd", "qk_rope_bwd",
     "sigmoid", "silu", "swiglu_fwd", "swiglu_bwd",
     "unmerged_weight", "nf4_merge",
+    "philox4x64", "dropout_keep", "dropout_keep_prob", "lora_fwd_dropout",
+    "lora_bwd_dropout",
 ]
 
 
@@ -384,4 +389,102 @@ def nf4_merge(codes, absmax, A, B, alpha: float, sign: float = 1.0):
     W = nf4_dequant(codes, absmax)
     Wm = merged_weight(W, A, B, alpha) if sign > 0 else unmerged_weight(W, A, B, alpha)
     return nf4_quantize(Wm)
+
+
+# ---------------------------------------------------------------------------
+# LoRA dropout on the adapter input — [P2] §3.3 table (dropout 0.05), [P4]
+# §2.2 example (lora_dropout=0.1); mask drawn from [Philox]
+# ---------------------------------------------------------------------------
+_PHILOX_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)   # round multipliers
+_PHILOX_W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)   # key increments (Weyl)
+_U64 = (1 << 64) - 1
+
+
+def _mulhilo64(a, b):
+    """128-bit product of uint64 arrays a·b as (high, low) words, from 32-bit
+    halves (numpy has no 128-bit integers)."""
+    a = np.asarray(a, dtype=np.uint64)
+    b = np.asarray(b, dtype=np.uint64)
+    m32 = np.uint64(0xFFFFFFFF)
+    s32 = np.uint64(32)
+    a0, a1 = a & m32, a >> s32
+    b0, b1 = b & m32, b >> s32
+    p00, p01, p10, p11 = a0 * b0, a0 * b1, a1 * b0, a1 * b1   # each < 2^64
+    mid = (p00 >> s32) + (p01 & m32) + (p10 & m32)              # < 3·2^32
+    lo = (p00 & m32) | ((mid & m32) << s32)
+    hi = p11 + (p01 >> s32) + (p10 >> s32) + (mid >> s32)
+    return hi, lo
+
+
+def philox4x64(counter, key, rounds: int = 10):
+    """[Philox] Philox4x64-R: four 64-bit counter words and two key words in,
+    four 64-bit words out.  Each round multiplies words 0 and 2 by the two
+    round multipliers and mixes the halves of the products with words 1 and
+    3 and the key (``c = (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0)``); the key
+    advances by the two Weyl constants between rounds.  ``counter`` is
+    ``[..., 4]`` and ``key`` ``[2]`` (uint64); returns ``[..., 4]`` uint64."""
+    c = np.array(counter, dtype=np.uint64, copy=True)
+    k0, k1 = np.uint64(key[0]), np.uint64(key[1])
+    with np.errstate(over="ignore"):
+        for rnd in range(rounds):
+            if rnd > 0:
+                k0 = k0 + np.uint64(_PHILOX_W[0])
+                k1 = k1 + np.uint64(_PHILOX_W[1])
+            hi0, lo0 = _mulhilo64(np.uint64(_PHILOX_M[0]), c[..., 0])
+            hi1, lo1 = _mulhilo64(np.uint64(_PHILOX_M[1]), c[..., 2])
+            c = np.stack([hi1 ^ c[..., 1] ^ k0, lo1, hi0 ^ c[..., 3] ^ k1, lo0], axis=-1)
+    return c
+
+
+def dropout_keep_prob(p: float) -> float:
+    """Keep probability of the mask for a dropout rate ``p``: the drop
+    threshold is ``t = round(p·65536)`` on 16-bit uniforms, so an element
+    is kept with probability ``q = 1 − t/65536``."""
+    return 1.0 - round(float(p) * 65536.0) / 65536.0
+
+
+def dropout_keep(M: int, k: int, p: float, seed: int, offset: int):
+    """Keep mask ``[M, k]`` (bool) of LoRA dropout on x [M, k].
+
+    Element ``e = i·k + j`` of x takes 16-bit uniform number ``e mod 16`` of
+    the Philox4x64-10 block with counter ``(e // 16, offset, 0, 0)`` and key
+    ``(seed, 0)`` (the four 64-bit words read as sixteen 16-bit numbers,
+    low half first); it is kept iff that number is at least
+    ``round(p·65536)``.  The same (seed, offset) gives the same mask in the
+    backward: nothing is stored."""
+    n = M * k
+    blocks = (n + 15) // 16
+    ctr = np.zeros((blocks, 4), dtype=np.uint64)
+    ctr[:, 0] = np.arange(blocks, dtype=np.uint64)
+    ctr[:, 1] = np.uint64(offset)
+    words = philox4x64(ctr, (int(seed) & _U64, 0))                  # [blocks, 4]
+    u16 = np.stack([(words >> np.uint64(16 * h)) & np.uint64(0xFFFF) for h in range(4)],
+                   axis=-1).reshape(blocks * 16)[:n]                  # word w, half h -> 4w+h
+    t = round(float(p) * 65536.0)
+    return (u16 >= t).reshape(M, k)
+
+
+def lora_fwd_dropout(x, W, A, B, alpha: float, p: float, seed: int, offset: int):
+    """:func:`lora_fwd` with dropout on the adapter's input only (the base
+    product sees x unchanged): ``x̃ = x ⊙ keep / q``,
+    ``y = x·Wᵀ + s·(x̃·Aᵀ)·Bᵀ``."""
+    x = _f64(x)
+    keep = dropout_keep(x.shape[0], x.shape[1], p, seed, offset)
+    xd = x * keep / dropout_keep_prob(p)
+    s = lora_scale(alpha, _f64(A).shape[0])
+    return x @ _f64(W).T + s * ((xd @ _f64(A).T) @ _f64(B).T)
+
+
+def lora_bwd_dropout(x, W, A, B, dy, alpha: float, p: float, seed: int, offset: int):
+    """Backward of :func:`lora_fwd_dropout` (mask regenerated from the seed):
+    ``u = dY·B``; ``dX = dY·W + s·(u·A) ⊙ keep / q``; ``dA = s·uᵀ·x̃``;
+    ``dB = s·dYᵀ·(x̃·Aᵀ)``.  Returns ``(dX, dA, dB)``."""
+    x, W, A, B, dy = _f64(x), _f64(W), _f64(A), _f64(B), _f64(dy)
+    keep = dropout_keep(x.shape[0], x.shape[1], p, seed, offset)
+    q = dropout_keep_prob(p)
+    xd = x * keep / q
+    s = lora_scale(alpha, A.shape[0])
+    u = dy @ B
+    dx = dy @ W + s * (u @ A) * keep / q
+    return dx, s * (u.T @ xd), s * (dy.T @ (xd @ A.T))
 

@@ -416,3 +416,79 @@ def test_nf4_merge_is_within_the_quantisation_bound_of_the_merged_weight():
     gaps = np.diff(ref.nf4_codebook()).max()
     bound = np.repeat(a2, 64, axis=1) * (gaps / 2) + np.abs(Wm) * 2.0 ** -8
     assert np.all(np.abs(got - Wm) <= bound + 1e-15)
+
+
+# --------------------------------------------------------------------------
+# LoRA dropout: Philox4x64-10 mask
+# --------------------------------------------------------------------------
+def test_mulhilo64_matches_python_integers():
+    r = np.random.default_rng(5)
+    a = r.integers(0, 2**63, size=200, dtype=np.uint64) * np.uint64(2) + np.uint64(1)
+    b = r.integers(0, 2**63, size=200, dtype=np.uint64) | np.uint64(1 << 63)
+    from oracle import lora_ref
+    hi, lo = lora_ref._mulhilo64(a, b)
+    for x, y, h, l in zip(a, b, hi, lo):
+        prod = int(x) * int(y)
+        assert int(h) == prod >> 64 and int(l) == prod & ((1 << 64) - 1)
+
+
+@pytest.mark.parametrize("counter,key", [([0, 0, 0, 0], [0, 0]), ([41, 9, 2, 1], [7, 11]),
+                                         ([2**64 - 1, 5, 0, 3], [2**64 - 2, 2**63])])
+def test_philox4x64_matches_numpy_bit_generator(counter, key):
+    """numpy's Philox bit generator is Philox4x64-10; it advances its 256-bit
+    counter before each block of four words."""
+    c = [int(v) for v in counter]
+    prev = (c[0] + (c[1] << 64) + (c[2] << 128) + (c[3] << 192) - 1) % (1 << 256)
+    prev_words = [(prev >> (64 * i)) & ((1 << 64) - 1) for i in range(4)]
+    bg = np.random.Philox(key=np.array(key, dtype=np.uint64),
+                          counter=np.array(prev_words, dtype=np.uint64))
+    want = [int(v) for v in bg.random_raw(4)]
+    got = [int(v) for v in ref.philox4x64(np.array([c], dtype=np.uint64), key)[0]]
+    assert got == want
+
+
+def test_dropout_mask_element_mapping_and_rate():
+    M, k, p, seed, off = 37, 96, 0.25, 2024, 5
+    keep = ref.dropout_keep(M, k, p, seed, off)
+    t = round(p * 65536)
+    # a few elements recomputed one by one from the Philox block they index
+    for e in (0, 1, 15, 16, 17, 1000, M * k - 1):
+        words = ref.philox4x64(np.array([[e // 16, off, 0, 0]], dtype=np.uint64), (seed, 0))[0]
+        u16 = (int(words[(e % 16) // 4]) >> (16 * (e % 4))) & 0xFFFF
+        assert keep[e // k, e % k] == (u16 >= t)
+    big = ref.dropout_keep(256, 1024, 0.1, 1, 0)
+    q = ref.dropout_keep_prob(0.1)
+    sd = math.sqrt(q * (1 - q) / big.size)
+    assert abs(big.mean() - q) < 5 * sd
+    assert np.array_equal(ref.dropout_keep(M, k, p, seed, off), keep)          # regenerated
+    assert not np.array_equal(ref.dropout_keep(M, k, p, seed, off + 1), keep)  # per-step offset
+    assert ref.dropout_keep(M, k, 0.0, seed, off).all()                         # p = 0 keeps all
+
+
+def test_dropout_zero_is_plain_lora_and_gradients_match_autograd():
+    M, k, n, r, alpha = 9, 32, 12, 4, 8.0
+    x, W, A, B, dy = _rand(M, k), _rand(n, k), _rand(r, k), _rand(n, r), _rand(M, n)
+    np.testing.assert_allclose(ref.lora_fwd_dropout(x, W, A, B, alpha, 0.0, 3, 0),
+                               ref.lora_fwd(x, W, A, B, alpha), rtol=1e-13, atol=1e-13)
+    p, seed, off = 0.3, 77, 2
+    keep = torch.from_numpy(ref.dropout_keep(M, k, p, seed, off).astype(np.float64))
+    q = ref.dropout_keep_prob(p)
+    ts = [torch.tensor(a, requires_grad=True) for a in (x, W, A, B)]
+    s = alpha / r
+    F = torch.nn.functional
+    yt = F.linear(ts[0], ts[1]) + s * F.linear(F.linear(ts[0] * keep / q, ts[2]), ts[3])
+    np.testing.assert_allclose(ref.lora_fwd_dropout(x, W, A, B, alpha, p, seed, off),
+                               yt.detach().numpy(), rtol=1e-12, atol=1e-12)
+    yt.backward(torch.from_numpy(dy))
+    dx, dA, dB = ref.lora_bwd_dropout(x, W, A, B, dy, alpha, p, seed, off)
+    for got, t in zip((dx, dA, dB), (ts[0], ts[2], ts[3])):
+        np.testing.assert_allclose(got, t.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_dropout_backward_matches_finite_differences():
+    M, k, n, r, alpha, p, seed, off = 3, 16, 5, 2, 4.0, 0.4, 9, 1
+    x, W, A, B, G = _rand(M, k), _rand(n, k), _rand(r, k), _rand(n, r), _rand(M, n)
+    L = lambda: float(np.sum(G * ref.lora_fwd_dropout(x, W, A, B, alpha, p, seed, off)))
+    dx, dA, dB = ref.lora_bwd_dropout(x, W, A, B, G, alpha, p, seed, off)
+    for P, an in ((x, dx), (A, dA), (B, dB)):
+        np.testing.assert_allclose(an, _fd_grad(L, P), rtol=1e-6, atol=1e-7)

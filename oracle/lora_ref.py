@@ -29,7 +29,14 @@ Sources (web pages about Unsloth; cited by title and section):
   rounds): the generator the dropout mask is drawn from.
 * [QLoRA] Dettmers et al. 2023, "QLoRA: Efficient Finetuning of Quantized
   LLMs", §3 "4-bit NormalFloat Quantization" and the NF4 table in its
-  appendix: the pages name NF4 but do not give its levels.
+  appendix: the pages name NF4 but do not give its levels; §3 "Double
+  Quantization" (8-bit float second-level quantisation of the block scales,
+  blocks of 256, mean subtracted), which the pages do not mention.
+* [OCP FP8] "OCP 8-bit Floating Point Specification (OFP8)" rev. 1.0, E4M3:
+  the 8-bit float format of the double-quantised block scales.
+* [IEEE 754] binary16 (fp16): the second 16-bit type; the pages'
+  usage example "UnSloth加速微调体验" passes ``dtype = torch.float16`` and
+  "Unsloth自动化优化" §3.1 falls back to fp16 where bf16 is unsupported.
 
 Conventions (row-vector form of [P1] 算子融合, which writes column vectors):
 ``x [M,k]``, ``W [n,k]`` (out x in), ``A [r,k]``, ``B [n,r]``,
@@ -55,6 +62,8 @@ __all__ = [
     "unmerged_weight", "nf4_merge",
     "philox4x64", "dropout_keep", "dropout_keep_prob", "lora_fwd_dropout",
     "lora_bwd_dropout",
+    "f16_round", "round16", "e4m3_values", "e4m3_round", "e4m3_encode", "dq_encode",
+    "dq_decode", "nf4_quantize_dq", "nf4_dequant_dq",
 ]
 
 
@@ -161,6 +170,36 @@ def bf16_round(a):
     return out
 
 
+def f16_round(a):
+    """Round fp64 values to the nearest IEEE binary16 (ties to even), in fp64.
+
+    binary16 keeps 11 significant bits with exponents down to -14 (below
+    that, subnormals spaced 2**-24), so the spacing around ``|a|`` is
+    ``2**(max(floor(log2|a|), -14) - 10)``.  Magnitudes that round past the
+    largest finite value 65504 (from 65520 up) become ``inf``.
+    """
+    a = _f64(a)
+    out = np.zeros_like(a)
+    nz = (a != 0) & np.isfinite(a)
+    e = np.floor(np.log2(np.abs(a[nz])))
+    e = np.maximum(e, -14.0)
+    q = np.exp2(e - 10.0)
+    out[nz] = np.rint(a[nz] / q) * q
+    out[~np.isfinite(a)] = a[~np.isfinite(a)]
+    big = np.abs(out) > 65504.0
+    out[big] = np.sign(out[big]) * np.inf
+    return out
+
+
+def round16(a, dtype: str):
+    """Round to the call's 16-bit type: ``"bf16"`` or ``"fp16"``."""
+    if dtype == "bf16":
+        return bf16_round(a)
+    if dtype == "fp16":
+        return f16_round(a)
+    raise ValueError(dtype)
+
+
 # ---------------------------------------------------------------------------
 # NF4 (QLoRA NormalFloat4) — [P3] 显存优化策略, [P5] §3.3/§5, [QLoRA] §3
 # ---------------------------------------------------------------------------
@@ -246,6 +285,144 @@ def nf4_dequant(codes, absmax, blocksize: int = 64):
     levels = nf4_codebook()
     scale = np.repeat(absmax, blocksize, axis=1)
     return levels[idx] * scale
+
+
+# ---------------------------------------------------------------------------
+# Double quantisation of the NF4 block scales — [QLoRA] §3, [OCP FP8] E4M3
+# ---------------------------------------------------------------------------
+E4M3_MAX = 448.0
+DQ_GROUP = 256
+
+
+def e4m3_values():
+    """Value of each of the 256 E4M3 codes ([OCP FP8]): sign bit 7, exponent
+    bits 6..3 with bias 7, mantissa bits 2..0; exponent 0 is subnormal
+    (``m · 2**-9``); exponent 15 with mantissa 7 is NaN (there is no inf), so
+    the largest finite magnitude is ``1.75 · 2**8 = 448``."""
+    v = np.empty(256, dtype=np.float64)
+    for c in range(256):
+        e, m = (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            mag = np.nan
+        elif e == 0:
+            mag = m * 2.0 ** -9
+        else:
+            mag = (1.0 + m / 8.0) * 2.0 ** (e - 7)
+        v[c] = -mag if c & 0x80 else mag
+    return v
+
+
+def e4m3_round(a):
+    """Nearest E4M3 value to ``a`` (ties to the even mantissa), saturating at
+    ±448 (magnitudes from 448 up map to 448, the reading of a saturating
+    conversion).  Spacing: ``2**(max(floor(log2|a|), -6) - 3)``."""
+    a = _f64(a)
+    out = np.zeros_like(a)
+    nz = a != 0
+    e = np.maximum(np.floor(np.log2(np.abs(a[nz]))), -6.0)
+    q = np.exp2(e - 3.0)
+    out[nz] = np.rint(a[nz] / q) * q
+    return np.clip(out, -E4M3_MAX, E4M3_MAX)
+
+
+def e4m3_encode(a):
+    """E4M3 code (uint8) of :func:`e4m3_round` of ``a``; the sign bit follows
+    the sign of ``a`` (a negative value that rounds to zero is code 0x80)."""
+    a = _f64(a)
+    r = e4m3_round(a)
+    table = e4m3_values()
+    pos = {float(table[c]): c for c in range(0x7F)}    # finite non-negative codes
+    mag = np.vectorize(lambda t: pos[float(t)], otypes=[np.int64])(np.abs(r))
+    sign = np.signbit(a).astype(np.int64) << 7
+    return (mag | sign).astype(np.uint8)
+
+
+def dq_encode(c1, group: int = DQ_GROUP):
+    """Double quantisation of first-level constants ``c1`` (block order),
+    [QLoRA] §3: subtract the mean, then quantise blockwise (``group``
+    constants per block) to 8-bit floats, here E4M3.
+
+    Reading of the steps the paper leaves open, in IEEE fp32 (the paper's
+    second-level constants are fp32): ``offset = fp32(mean(c1))``;
+    ``d = fp32(c1 - offset)``; per group ``scale = fp32(max|d| / 448)`` (448
+    being the largest E4M3 magnitude, so the absmax element lands on it);
+    ``code = E4M3(fp32(d / scale))`` (0 when ``scale`` is 0).
+
+    Returns ``(codes uint8 [len(c1)], scale float32 [ceil(len/group)],
+    offset float32)``.
+    """
+    c1 = np.asarray(c1, dtype=np.float32).reshape(-1)
+    nb = c1.size
+    ng = (nb + group - 1) // group
+    offset = np.float32(np.mean(c1.astype(np.float64)))
+    d = (c1 - offset).astype(np.float32)
+    scale = np.empty(ng, dtype=np.float32)
+    codes = np.zeros(nb, dtype=np.uint8)
+    for g in range(ng):
+        dg = d[g * group:(g + 1) * group]
+        s = np.float32(np.max(np.abs(dg)) / np.float32(E4M3_MAX))
+        scale[g] = s
+        if s > 0:
+            codes[g * group:(g + 1) * group] = e4m3_encode((dg / s).astype(np.float32))
+    return codes, scale, offset
+
+
+def dq_decode(codes, scale, offset, group: int = DQ_GROUP):
+    """Block scales from double-quantised form: ``bf16(fp32(fp32(e4m3(code) ·
+    scale[b // group]) + offset))`` (each fp32 operation rounded to nearest;
+    the result is rounded to bf16, the type a single-level block scale is
+    stored in).  Returned in fp64, same shape as ``codes``."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    flat = codes.reshape(-1)
+    v = e4m3_values()[flat].astype(np.float32)
+    s = np.repeat(np.asarray(scale, dtype=np.float32), group)[:flat.size]
+    a = (v * s).astype(np.float32) + np.float32(offset)
+    return bf16_round(a.astype(np.float32).astype(np.float64)).reshape(codes.shape)
+
+
+def nf4_quantize_dq(W, blocksize: int = 64, decision: str = "fp32", group: int = DQ_GROUP):
+    """NF4 quantisation with double-quantised block scales ([QLoRA] §3).
+
+    The first-level constants are ``c1 = max|w|`` per block (exact);
+    :func:`dq_encode` compresses them; the element codes are then chosen as
+    in :func:`nf4_quantize` but against the block scale the decoder will use,
+    ``dq_decode(...)`` (reading: codes are fitted to the scale they are
+    decoded with; w/scale is clamped to [-1, 1], a zero scale gives code 7).
+
+    Returns ``(codes uint8 [n, k/2], absmax_codes uint8 [n, k/blocksize],
+    scale float32 [ceil(n·k/blocksize/group)], offset float32)``.
+    """
+    W = _f64(W)
+    n, k = W.shape
+    assert k % blocksize == 0
+    blocks = W.reshape(n, k // blocksize, blocksize)
+    c1 = np.max(np.abs(blocks), axis=2)
+    qc, scale, offset = dq_encode(c1, group)
+    qc = qc.reshape(n, k // blocksize)
+    am = dq_decode(qc, scale, offset, group)
+    levels = nf4_codebook()
+    safe = np.where(am == 0.0, 1.0, am)[:, :, None]
+    if decision == "fp64":
+        ratio = np.clip(blocks / safe, -1.0, 1.0)
+        dist = np.abs(ratio[..., None] - levels)
+    elif decision == "fp32":
+        ratio = blocks.astype(np.float32) / safe.astype(np.float32)
+        ratio = np.clip(ratio, np.float32(-1.0), np.float32(1.0))
+        dist = np.abs(ratio[..., None] - levels.astype(np.float32))
+    else:
+        raise ValueError(decision)
+    code = np.argmin(dist, axis=-1).astype(np.uint8)
+    code[am == 0.0] = 7
+    code = code.reshape(n, k)
+    packed = (code[:, 0::2] << 4) | code[:, 1::2]
+    return packed.astype(np.uint8), qc, scale, offset
+
+
+def nf4_dequant_dq(codes, absmax_codes, scale, offset, blocksize: int = 64,
+                   group: int = DQ_GROUP):
+    """``W = level[code] · dq_decode(...)`` in fp64 (the decoded scale is
+    already a bf16 value)."""
+    return nf4_dequant(codes, dq_decode(absmax_codes, scale, offset, group), blocksize)
 
 
 # ---------------------------------------------------------------------------

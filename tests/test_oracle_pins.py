@@ -492,3 +492,116 @@ def test_dropout_backward_matches_finite_differences():
     dx, dA, dB = ref.lora_bwd_dropout(x, W, A, B, G, alpha, p, seed, off)
     for P, an in ((x, dx), (A, dA), (B, dB)):
         np.testing.assert_allclose(an, _fd_grad(L, P), rtol=1e-6, atol=1e-7)
+
+
+# --------------------------------------------------------------------------
+# fp16 rounding and double-quantised NF4 block scales
+# --------------------------------------------------------------------------
+def test_f16_round_matches_numpy():
+    v = rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 5, 20000)
+    # exact ties between neighbours, subnormals and the overflow edge
+    ties = np.array([1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 2.0 ** -24 * 1.5, 2.0 ** -24 * 2.5,
+                     65504.0, 65519.99, 65520.0, -65520.0, 2.0 ** -25, -2.0 ** -26, 0.0])
+    v = np.concatenate([v, ties])
+    with np.errstate(over="ignore"):                      # 65520 overflows to inf
+        theirs = v.astype(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(ref.f16_round(v), theirs)
+
+
+def test_e4m3_table_matches_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    theirs = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = ref.e4m3_values()
+    np.testing.assert_array_equal(np.isnan(mine), np.isnan(theirs))
+    ok = ~np.isnan(mine)
+    np.testing.assert_array_equal(mine[ok], theirs[ok])
+    assert np.nanmax(mine) == 448.0 and np.sum(np.isnan(mine)) == 2
+
+
+def test_e4m3_round_and_encode_match_torch():
+    mag = np.exp2(rng.uniform(-12, np.log2(460.0), 20000))
+    v = (mag * rng.choice([-1.0, 1.0], 20000)).astype(np.float32)
+    # ties (midpoints of the grid), tiny negatives and the saturation edge
+    extra = np.array([1.0625, 1.1875, 136.0, 152.0, -2.0 ** -10, 2.0 ** -10, -1e-6, 447.9,
+                      448.0, 455.0, -455.0, 0.0], dtype=np.float32)
+    v = np.concatenate([v, extra])
+    t = torch.tensor(v).to(torch.float8_e4m3fn)
+    np.testing.assert_array_equal(ref.e4m3_round(v.astype(np.float64)),
+                                  t.to(torch.float64).numpy())
+    np.testing.assert_array_equal(ref.e4m3_encode(v.astype(np.float64)),
+                                  t.view(torch.uint8).numpy())
+
+
+def test_dq_hand_example():
+    g = _golden_kv("dq_worked_example.txt")
+    codes, scale, offset = ref.dq_encode(np.array([0.5, 1.0, 1.5, 2.0]))
+    assert float(offset) == float(g["offset"][0])
+    assert [int(c) for c in codes] == [int(c, 16) for c in g["codes"]]
+    assert float(scale[0]) == float(np.float32(0.75) / np.float32(448.0))
+    np.testing.assert_array_equal(ref.dq_decode(codes, scale, offset),
+                                  [float(x) for x in g["decoded"]])
+
+
+def test_dq_invariants_over_groups_of_different_spread():
+    # three groups of 256 with very different spreads, and a ragged last group
+    c1 = np.concatenate([0.02 + 0.001 * rng.random(256), 0.02 + 0.02 * rng.random(256),
+                         0.5 * rng.random(256), 0.03 + 0.001 * rng.random(64)])
+    c1 = ref.bf16_round(c1).astype(np.float32)
+    codes, scale, offset = ref.dq_encode(c1)
+    assert scale.shape == (4,)
+    # the offset is the fp32 of the exact mean
+    assert float(offset) == float(np.float32(math.fsum(map(float, c1)) / c1.size))
+    dec = ref.dq_decode(codes, scale, offset)
+    d = (c1 - offset).astype(np.float32).astype(np.float64)
+    for g in range(4):
+        sl = slice(256 * g, 256 * (g + 1))
+        assert scale[g] == np.float32(np.max(np.abs(d[sl])) / np.float32(448.0))
+        # the element of largest |d| lands on the format's end, ±448
+        j = np.argmax(np.abs(d[sl]))
+        assert codes[sl][j] in (0x7E, 0xFE)
+    r = np.abs(d) / np.repeat(scale.astype(np.float64), 256)[:c1.size]
+    step = np.exp2(np.maximum(np.floor(np.log2(np.maximum(r, 2.0 ** -20))), -6) - 3)
+    s_el = np.repeat(scale.astype(np.float64), 256)[:c1.size]
+    bound = s_el * step / 2 * (1 + 1e-6) + 2.0 ** -8 * np.abs(c1) + 1e-12
+    assert np.all(np.abs(dec - c1) <= bound)
+    # the narrow first group is reproduced far better than the wide third one
+    err = np.abs(dec - c1)
+    assert err[:256].max() < err[512:768].max() / 10
+
+
+def test_dq_of_constant_scales_is_exact():
+    c1 = np.full(300, 0.0390625, dtype=np.float32)      # a bf16 value
+    codes, scale, offset = ref.dq_encode(c1)
+    assert np.all(scale == 0) and np.all(codes == 0)
+    np.testing.assert_array_equal(ref.dq_decode(codes, scale, offset), c1.astype(np.float64))
+
+
+def test_nf4_quantize_dq_is_brute_force_nearest_against_the_decoded_scale():
+    w = ref.bf16_round(_rand(4, 256, scale=0.05))
+    w[1, 64:128] = 0.0                                    # an all-zero block
+    codes, qc, scale, offset = ref.nf4_quantize_dq(w, decision="fp64", group=4)
+    assert scale.shape == (4,) and qc.shape == (4, 4)
+    am = ref.dq_decode(qc, scale, offset, group=4)
+    lv = ref.nf4_codebook()
+    idx = ref.nf4_unpack(codes)
+    for i in range(4):
+        for j in range(256):
+            a = am[i, j // 64]
+            if a == 0.0:
+                assert idx[i, j] == 7
+                continue
+            t = min(max(w[i, j] / a, -1.0), 1.0)
+            best = min(range(16), key=lambda q: (abs(t - lv[q]), q))
+            assert idx[i, j] == best, (i, j)
+    assert np.all(idx[1, 64:128] == 7)
+
+
+def test_nf4_dequant_dq_error_bound():
+    w = ref.bf16_round(_rand(8, 1024, scale=0.02))
+    codes, qc, scale, offset = ref.nf4_quantize_dq(w)
+    wd = ref.nf4_dequant_dq(codes, qc, scale, offset)
+    c1 = np.repeat(np.max(np.abs(w.reshape(8, 16, 64)), axis=2), 64, axis=1)
+    am = np.repeat(ref.dq_decode(qc, scale, offset), 64, axis=1)
+    gap = np.max(np.diff(ref.nf4_codebook())) / 2
+    bound = np.maximum(c1 - am, 0.0) + am * gap
+    assert np.all(np.abs(wd - w) <= bound * (1 + 1e-6) + 1e-15)

@@ -322,7 +322,10 @@ class Replica:
     """Device-resident inputs and outputs of one workload plus the calls of
     one step through the C ABI."""
 
-    def __init__(self, name: str, device: str, seed: int = 0):
+    def __init__(self, name: str, device: str, seed: int = 0, stage_nf4: bool = True):
+        """stage_nf4: give NF4 calls room to stage W in bf16 (the library then
+        dequantises once per call and runs the bf16 GEMMs at M >= 2048);
+        False: workspaces of exactly lora_workspace_size (in-GEMM decode)."""
         import lora_qlora_linear_fwd_b300 as L
         self.L = L
         self.name = name
@@ -338,8 +341,8 @@ class Replica:
             if wl.nf4:   # quantise the drawn W on the GPU (setup, not timed)
                 codes = torch.empty(p.n, p.k // 2, dtype=torch.uint8, device=device)
                 absmax = torch.empty(p.n, p.k // 64, **bf)
-                L.nf4_quantize(d["W"], codes, absmax)
                 d["Wdesc"] = L.nf4_weight(codes, absmax)
+                L.nf4_quantize(d["W"], d["Wdesc"])
                 d["codes"], d["absmax"] = codes, absmax
                 del d["W"]
             else:
@@ -374,10 +377,12 @@ class Replica:
             self.dx = torch.empty(M, pq.k, **bf)
         else:
             # calls run one after another on one stream: one workspace per op
-            # kind, sized for the largest projection
-            self.ws_f = torch.zeros(max(L.workspace_size(L.OP_FWD, M, p.k, p.n, wl.r)
+            # kind, sized for the largest projection (and its staged W)
+            stage = (lambda p: L.lora_nf4_stage_bytes(p.n, p.k)) if (wl.nf4 and stage_nf4) \
+                else (lambda p: 0)
+            self.ws_f = torch.zeros(max(L.workspace_size(L.OP_FWD, M, p.k, p.n, wl.r) + stage(p)
                                         for p in wl.projections), dtype=torch.uint8, device=device)
-            self.ws_b = torch.zeros(max(L.workspace_size(L.OP_BWD, M, p.k, p.n, wl.r)
+            self.ws_b = torch.zeros(max(L.workspace_size(L.OP_BWD, M, p.k, p.n, wl.r) + stage(p)
                                         for p in wl.projections), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
 
@@ -485,12 +490,15 @@ def time_steps(rep, steps, flush, stream):
 
 def profile_steps(rep, steps, flush):
     """The same steps inside a per-launch timing session: every launch with
-    its kernel, phase and algorithmic work."""
+    its kernel, phase and algorithmic work.  Launches are matched to the
+    call's phases by kernel name: an NF4 weight staged in bf16 adds an
+    nf4_dequant launch, and a forward that forms x·Aᵀ in its GEMM (`xa`)
+    has no rank pass (its GEMM carries the rank pass's FLOPs)."""
     L = rep.L
     phases = {name: ph for name, ph in call_phases(rep.wl, rep.M)}
     calls = rep.calls()
-    cap = steps * sum(len(ph) for ph in phases.values()) + 16   # an upper bound
-    launches = []   # (call, phase, flops, bytes)
+    cap = steps * (sum(len(ph) for ph in phases.values()) + 2 * len(calls)) + 16
+    counts = []   # (call, launches)
     L.lora_profile_begin(cap)
     try:
         for _ in range(steps):
@@ -498,20 +506,36 @@ def profile_steps(rep, steps, flush):
             for name, fn in calls:
                 c0 = L.lora_kernel_launch_count()
                 fn()
-                n = L.lora_kernel_launch_count() - c0
-                ph = phases[name]
-                if n == 1 and len(ph) == 2 and ph[0][0] == "fwd_rank":
-                    # bf16 W: x·Aᵀ is formed inside the fused GEMM (one launch)
-                    ph = [("fwd_gemm", ph[0][1] + ph[1][1], ph[1][2])]
-                if n != len(ph):
-                    raise RuntimeError(f"{name}: {n} launches, expected {len(ph)}")
-                launches += [(name,) + x for x in ph]
+                counts.append((name, L.lora_kernel_launch_count() - c0))
     finally:
         timed = L.lora_profile_end(cap)
-    if len(timed) != len(launches):
-        raise RuntimeError(f"profile: {len(timed)} timed launches for {len(launches)}")
-    return [(kname, ms, call, phase, fl, by)
-            for (kname, ms), (call, phase, fl, by) in zip(timed, launches)]
+    if len(timed) != sum(n for _, n in counts):
+        raise RuntimeError(f"profile: {len(timed)} timed launches for {sum(n for _, n in counts)}")
+    rows, i = [], 0
+    for name, n in counts:
+        ph = dict((x[0], x) for x in phases[name])
+        skinny = [x for x in phases[name] if x[0] in ("fwd_rank", "bwd_rank", "bwd_grads")]
+        for kname, ms in timed[i:i + n]:
+            if kname.startswith("nf4_dequant"):
+                p_ = next(q for q in rep.wl.projections if name.endswith(q.name)) \
+                    if not rep.wl.rope and not rep.wl.extra.get("swiglu") else None
+                nk = (p_.n * p_.k) if p_ else 0
+                work = ("nf4_stage", 0.0, nk * (0.5 + 1.0 / 32 + 2.0))
+            elif kname.startswith("bwd_prep"):
+                work = ph["bwd_prep"]
+            elif kname.startswith("lora_skinny"):
+                work = skinny.pop(0)
+            elif kname.startswith("lora_gemm_pair_kernel<fwd"):
+                work = ph["fwd_gemm"]
+                if kname.endswith(",xa>") and "fwd_rank" in ph:
+                    work = ("fwd_gemm", work[1] + ph["fwd_rank"][1], work[2])
+            elif kname.startswith("lora_gemm_pair_kernel<dx"):
+                work = ph["dx_gemm"]
+            else:
+                raise RuntimeError(f"{name}: unexpected launch {kname}")
+            rows.append((kname, ms, name) + work)
+        i += n
+    return rows
 
 
 def summarise_kernels(rows, steps, peaks, pool):
@@ -561,18 +585,19 @@ def run_nf4_dequant_shapes(shapes, dev, flush, steps, warmup, peak):
         W = (torch.randn(n, k, generator=g) / math.sqrt(k)).to(torch.bfloat16).to(dev)
         codes = torch.empty(n, k // 2, dtype=torch.uint8, device=dev)
         absmax = torch.empty(n, k // 64, dtype=torch.bfloat16, device=dev)
-        L.nf4_quantize(W, codes, absmax)
+        Wq = L.nf4_weight(codes, absmax)
+        L.nf4_quantize(W, Wq)
         out = torch.empty(n, k, dtype=torch.bfloat16, device=dev)
         del W
         for _ in range(warmup):
-            L.nf4_dequant(codes, absmax, out)
+            L.nf4_dequant(Wq, out)
         ts = []
         for _ in range(steps):
             flush.zero_()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()
-            L.nf4_dequant(codes, absmax, out)
+            L.nf4_dequant(Wq, out)
             b.record()
             torch.cuda.synchronize()
             ts.append(a.elapsed_time(b))
@@ -598,23 +623,24 @@ def nf4_fused_vs_unfused(name, proj, dev, flush, steps, warmup):
     bf = dict(dtype=torch.bfloat16, device=dev)
     codes = torch.empty(p.n, p.k // 2, dtype=torch.uint8, device=dev)
     absmax = torch.empty(p.n, p.k // 64, **bf)
-    L.nf4_quantize(d["W"], codes, absmax)
     Wq = L.nf4_weight(codes, absmax)
+    L.nf4_quantize(d["W"], Wq)
     Wb = torch.empty(p.n, p.k, **bf)
     y = torch.empty(M, p.n, **bf)
     dx = torch.empty(M, p.k, **bf)
     dA = torch.empty(r, p.k, dtype=torch.float32, device=dev)
     dB = torch.empty(p.n, r, dtype=torch.float32, device=dev)
+    # exact-size workspaces: the NF4 calls decode inside the GEMMs
     wsf = L.workspace(L.OP_FWD, M, p.k, p.n, r, device=dev)
     wsb = L.workspace(L.OP_BWD, M, p.k, p.n, r, device=dev)
     calls = {
         "fwd_fused": lambda: L.lora_linear_fwd(d["x"], Wq, d["A"], d["B"], y, wl.alpha, wsf),
-        "fwd_dequant_then_bf16": lambda: (L.nf4_dequant(codes, absmax, Wb),
+        "fwd_dequant_then_bf16": lambda: (L.nf4_dequant(Wq, Wb),
                                           L.lora_linear_fwd(d["x"], Wb, d["A"], d["B"], y,
                                                             wl.alpha, wsf)),
         "bwd_fused": lambda: L.lora_linear_bwd(d["x"], Wq, d["A"], d["B"], d["dY"], dx, dA, dB,
                                                wl.alpha, wsb),
-        "bwd_dequant_then_bf16": lambda: (L.nf4_dequant(codes, absmax, Wb),
+        "bwd_dequant_then_bf16": lambda: (L.nf4_dequant(Wq, Wb),
                                           L.lora_linear_bwd(d["x"], Wb, d["A"], d["B"], d["dY"],
                                                             dx, dA, dB, wl.alpha, wsb)),
     }
@@ -796,6 +822,12 @@ def run_gpu(args, world, rank, local):
             "frac_of_pool_burst": line["tflops_frac_of_pool_peak"], "steps": args.steps,
             "M": M, "description": wl.description, "headline": True}
         line["per_workload"] = per
+        if wl.nf4:   # the headline step with the NF4 codes decoded inside the GEMMs
+            r2 = Replica(args.workload, dev, stage_nf4=False)
+            per[args.workload + ":nf4_decoded_in_gemm"] = workload_line(
+                r2, args.steps, args.warmup, flush, stream, peaks, pool)
+            del r2
+            torch.cuda.empty_cache()
         if wl.nf4:   # the fused NF4 GEMMs against dequantising first
             line["nf4_fused_vs_unfused"] = nf4_fused_vs_unfused(args.workload, "gate_proj", dev,
                                                                 flush, 10, 3)

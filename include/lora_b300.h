@@ -12,17 +12,22 @@
  *   [P3] "Unsloth教程：本地微调大模型速度提升数倍，显存节省60%":
  *        显存优化策略 (QLoRA: frozen 4-bit NormalFloat4 base weight, only the
  *        adapter is trained).
- *   [QLoRA] Dettmers et al. 2023, §3 (the NF4 levels; the pages only name
- *        the format).
+ *   [QLoRA] Dettmers et al. 2023, §3 (the NF4 levels, and Double
+ *        Quantization of the block scales; the pages only name the format).
  *
  * Conventions shared by every entry point
  *   - Row-major, contiguous tensors: x [M,k], W [n,k] (out x in), A [r,k],
  *     B [n,r], y and dY [M,n], dX [M,k], dA [r,k], dB [n,r].  The pages write
  *     column vectors (y = Wx + BAx); this is the same map in row form.
  *   - LoRA scale s = alpha / r multiplies the adapter branch.
- *   - x, W (bf16 form), A, B, y, dY, dX are bfloat16; dA, dB are float32;
- *     accumulation is float32 on the tensor cores; rounding to bf16 is
- *     round-to-nearest-even.
+ *   - x, W (dense form), A, B, y, dY, dX and every other 16-bit tensor of a
+ *     call are of the call's 16-bit type, W.dtype: bfloat16 (the default) or
+ *     float16 (the pages' API takes dtype = torch.float16 or torch.bfloat16,
+ *     "UnSloth加速微调体验" usage example; "Unsloth自动化优化" §3.1 picks fp16
+ *     where bf16 is unsupported).  dA, dB are float32; accumulation is
+ *     float32 on the tensor cores; rounding to the 16-bit type is
+ *     round-to-nearest-even.  fp16 has bf16's precision plus 3 bits but a
+ *     range of ±65504: values past it become ±inf, as in any fp16 GEMM.
  *   - Every pointer is a DEVICE pointer owned by the caller, 16-byte
  *     aligned.  The library allocates no device memory (except the fixed
  *     scratch of lora_linear_bwd_noalloc) and keeps no state between calls
@@ -69,19 +74,36 @@ typedef enum {
 #define LORA_DEVSTAT_TIMEOUT 0x1u     /* an mbarrier wait exceeded its limit */
 #define LORA_DEVSTAT_BAD_POSITION 0x2u /* a RoPE position was outside [0,max_pos) */
 
-/* Base weight descriptor.
- *   type == LORA_WEIGHT_BF16: w -> bf16 [n,k]; absmax NULL; blocksize ignored.
+/* Base weight descriptor (zero-initialise it, then set the fields).
+ *   dtype: LORA_DTYPE_BF16 (0) or LORA_DTYPE_FP16 (1), the call's 16-bit type.
+ *   type == LORA_WEIGHT_DENSE: w -> [n,k] of that type; absmax, absmax_scale,
+ *     absmax_offset NULL; blocksize ignored.
  *   type == LORA_WEIGHT_NF4 : w -> uint8 codes [n, k/2] (byte j of a row holds
- *     element 2j in the high nibble, 2j+1 in the low nibble); absmax -> bf16
- *     [n, k/blocksize], the per-block scale (16-byte aligned, like every
- *     other pointer); blocksize must be 64.  An element
- *     decodes to level[code] * absmax with the 16 NF4 levels of [QLoRA]. */
-enum { LORA_WEIGHT_BF16 = 0, LORA_WEIGHT_NF4 = 1 };
+ *     element 2j in the high nibble, 2j+1 in the low nibble); blocksize must
+ *     be 64; an element decodes to level[code] * absmax[block], rounded to
+ *     the 16-bit type, with the 16 NF4 levels of [QLoRA].  The block scales
+ *     (blocks numbered row-major, b = row·k/64 + j/64):
+ *       absmax_scale == NULL: absmax -> bf16 [n·k/64].
+ *       double quantisation ([QLoRA] §3; absmax_scale and absmax_offset
+ *       both set): absmax -> uint8 E4M3 codes [n·k/64] (OCP FP8, 4 exponent
+ *       bits, bias 7, 3 mantissa bits), absmax_scale -> float32
+ *       [ceil(n·k/64 / 256)] (one per 256 consecutive blocks), absmax_offset
+ *       -> one float32; block b's scale is
+ *         bf16( e4m3(code[b]) · absmax_scale[b/256] + *absmax_offset )
+ *       with the product and the sum each rounded to float32.  0.52 instead
+ *       of 0.53 bytes per weight.
+ *   Every pointer is 16-byte aligned. */
+enum { LORA_WEIGHT_DENSE = 0, LORA_WEIGHT_NF4 = 1 };
+#define LORA_WEIGHT_BF16 LORA_WEIGHT_DENSE /* earlier name of the dense type */
+enum { LORA_DTYPE_BF16 = 0, LORA_DTYPE_FP16 = 1 };
 typedef struct {
   int type;
   const void *w;
   const void *absmax;
   int blocksize;
+  int dtype;
+  const float *absmax_scale;
+  const float *absmax_offset;
 } lora_weight_t;
 
 /* Operation ids for lora_workspace_size(). */
@@ -93,8 +115,14 @@ enum {
   LORA_OP_SWIGLU_FWD = 4,
   LORA_OP_SWIGLU_BWD = 5,
   LORA_OP_MERGE = 6,     /* pass M = 1 */
-  LORA_OP_MERGE_NF4 = 7  /* pass M = 1 */
+  LORA_OP_MERGE_NF4 = 7, /* pass M = 1 */
+  LORA_OP_FWD_DROPOUT = 8,
+  LORA_OP_BWD_DROPOUT = 9
 };
+/* OR'ed into the op of lora_workspace_size(): the call's NF4 weight (either
+ * weight of a pair) has double-quantised block scales.  Adds room for their
+ * bf16 expansion (n·k/32 bytes per weight), which the in-GEMM decode reads. */
+#define LORA_OP_FLAG_DQ 0x100
 
 /* Bytes of workspace an operation needs (always >= 256: the status word
  * lives at offset 0).  Besides the intermediates each call documents, every
@@ -110,6 +138,20 @@ enum {
  * n = (n_q_heads + n_kv_heads) * head_dim.  Returns 0 for an unknown op or
  * out-of-range sizes.  Pure host function. */
 size_t lora_workspace_size(int op, int M, int k, int n, int r);
+
+/* Room for NF4 weights staged in bf16 (n·k·2 bytes, 256-aligned).  An NF4
+ * call (any of the forward and backward calls below) with M >= 2048 whose
+ * workspace holds, past what lora_workspace_size() (plus the RoPE cache when
+ * the call builds it) asks for, lora_nf4_stage_bytes() for each of its
+ * weights (both weights of a q/k or gate/up pair, in that order), first
+ * dequantises them there (nf4_dequant's rule) and then runs the bf16
+ * kernels.  At that size the GEMMs are tensor-bound and the in-kernel
+ * decode costs MMA throughput: on a B300, Qwen1.5-32B gate_proj at
+ * M = 8192 ran forward 1.62 -> 1.38 ms and backward 2.31 -> 1.68 ms this way.
+ * With a workspace of exactly lora_workspace_size(), or M < 2048, the NF4
+ * codes are decoded inside the GEMMs while each W tile is staged.  Returns 0
+ * for non-positive sizes. */
+size_t lora_nf4_stage_bytes(int n, int k);
 
 /* Fused forward, [P1] 算子融合:  y = x·Wᵀ + s·(x·Aᵀ)·Bᵀ.
  * Two launches.  The rank pass streams x once and writes the rank block
@@ -177,6 +219,36 @@ lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq,
                                const float *cos_sin_cache, int max_pos,
                                void *ws, size_t ws_bytes, lora_stream_t stream);
 
+/* LoRA dropout on the adapter's input ([P2] "微调太慢？试试Unsloth" §3.3 table,
+ * row E: lora_dropout 0.05; [P4] §2.2: lora_dropout=0.1): the base product
+ * sees x, the adapter x̃ = x ⊙ keep / q.
+ *   y = x·Wᵀ + s·(x̃·Aᵀ)·Bᵀ.
+ * The mask is drawn from Philox4x64-10 (Salmon et al. 2011) and never
+ * stored: element e = i·k + j of x takes 16-bit number e mod 16 of the block
+ * with counter (e/16, offset, 0, 0) and key (seed, 0), and is kept iff that
+ * number is >= round(dropout_p·65536); q = 1 − round(dropout_p·65536)/65536.
+ * Pass the same (seed, offset) to the backward; change offset every step.
+ * dropout_p in [0, 1).  Three launches: x̃ into the workspace (bf16), the rank
+ * pass over x̃, the fused GEMM.
+ *   ws: >= lora_workspace_size(LORA_OP_FWD_DROPOUT, M, k, n, r). */
+lora_status_t lora_linear_fwd_dropout(const void *x, lora_weight_t W, const void *A,
+                                      const void *B, void *y, int M, int k, int n,
+                                      int r, float alpha, float dropout_p,
+                                      uint64_t seed, uint64_t offset, void *ws,
+                                      size_t ws_bytes, lora_stream_t stream);
+
+/* Backward of lora_linear_fwd_dropout, the mask regenerated from (seed,
+ * offset):  u = dY·B,  dX = dY·W + s·(u·A) ⊙ keep / q,  dA = s·uᵀ·x̃,
+ * dB = s·dYᵀ·(x̃·Aᵀ) (x̃·Aᵀ recomputed).  dX's adapter term is its own K = r
+ * tensor-core pass whose read-modify-write epilogue applies the mask.
+ *   ws: >= lora_workspace_size(LORA_OP_BWD_DROPOUT, M, k, n, r). */
+lora_status_t lora_linear_bwd_dropout(const void *x, lora_weight_t W, const void *A,
+                                      const void *B, const void *dy, void *dx,
+                                      int accumulate_dx, float *dA, float *dB, int M,
+                                      int k, int n, int r, float alpha, float dropout_p,
+                                      uint64_t seed, uint64_t offset, void *ws,
+                                      size_t ws_bytes, lora_stream_t stream);
+
 /* Gate and up projections of an MLP joined by SwiGLU, [P4] "Unsloth框架：
  * 高效LLM微调与LoRA优化实践" §3.1 计算图重写引擎 (adjacent linear layers merged
  * with their activation) and [P5] "Unsloth自动化优化" §1 模型结构自识别
@@ -237,39 +309,48 @@ lora_status_t lora_linear_bwd_noalloc(const void *x, lora_weight_t W, const void
  * W <- W + sign·s·B·A (sign = +1 merge, -1 unmerge), s = alpha/r.  [P2]
  * "微调太慢？试试Unsloth" §5.1 (for_inference folds the LoRA weights into the
  * main weight so no adapter runs at generation time) and [P5] §3.2 (the
- * "A@B + original_weight" kernel).  In place on a bf16 W [n,k]; B·A runs on
- * the tensor cores (K = r) and each W element is read and written once
- * (rounded once to bf16).  A [r,k], B [n,r] bf16.  n % 64 == 0, k % 64 == 0.
- *   ws: >= lora_workspace_size(LORA_OP_MERGE, 1, k, n, r) (the status word). */
-lora_status_t lora_merge(void *W, const void *A, const void *B, int n, int k,
-                         int r, float alpha, int sign, void *ws, size_t ws_bytes,
-                         lora_stream_t stream);
+ * "A@B + original_weight" kernel).  In place, through W's pointers (the
+ * descriptor's const qualifiers notwithstanding).  A [r,k], B [n,r] of
+ * W.dtype.  n % 64 == 0, k % 64 == 0.
+ *   Dense W [n,k]: B·A runs on the tensor cores (K = r) and each W element
+ *   is read and written once (rounded once to W.dtype).
+ *     ws: >= lora_workspace_size(LORA_OP_MERGE, 1, k, n, r) (status word).
+ *   NF4 W: dequantised into the workspace (nf4_dequant's rule), merged
+ *   there, and quantised back into the codes and block scales in place
+ *   (nf4_quantize's rule, with double quantisation when W has it).  The
+ *   merged weight is not representable in the old codes, so it is
+ *   re-quantised; merging then unmerging returns a weight within NF4's
+ *   quantisation error of the original, not the original codes.
+ *     ws: >= lora_workspace_size(LORA_OP_MERGE_NF4, 1, k, n, r) (2·n·k
+ *     bytes plus the status word). */
+lora_status_t lora_merge(lora_weight_t W, const void *A, const void *B, int n,
+                         int k, int r, float alpha, int sign, void *ws,
+                         size_t ws_bytes, lora_stream_t stream);
 
-/* The same for an NF4 W (codes and absmax as in lora_weight_t, blocksize 64):
- * dequantise into the workspace (bf16), merge there, and quantise back into
- * codes/absmax in place (nf4_quantize's rule).  The merged weight is not
- * representable in the old codes, so it is re-quantised; merging then
- * unmerging returns a weight within NF4's quantisation error of the
- * original, not the original codes.
- *   ws: >= lora_workspace_size(LORA_OP_MERGE_NF4, 1, k, n, r) (2·n·k bytes
- *   plus the status word). */
-lora_status_t lora_merge_nf4(uint8_t *codes, void *absmax, const void *A,
-                             const void *B, int n, int k, int r, float alpha,
-                             int sign, int blocksize, void *ws, size_t ws_bytes,
-                             lora_stream_t stream);
+/* Standalone NF4 dequantisation ([P3] 显存优化策略, [QLoRA] §3) of an NF4
+ * descriptor (either scale form):
+ *   w_out[i,j] = dtype( level[code(i,j)] * scale[block(i,j)] ), product in
+ *   fp32, w_out [n,k] of W.dtype.  k % 64 == 0. */
+lora_status_t nf4_dequant(lora_weight_t W, void *w_out, int n, int k,
+                          lora_stream_t stream);
 
-/* Standalone NF4 dequantisation ([P3] 显存优化策略, [QLoRA] §3):
- *   w_out[i,j] = bf16( level[code(i,j)] * absmax[i, j/64] ), product in fp32.
- * codes uint8 [n, k/2], absmax bf16 [n, k/64], w_out bf16 [n,k]. */
-lora_status_t nf4_dequant(const uint8_t *codes, const void *absmax, void *w_out,
-                          int n, int k, int blocksize, lora_stream_t stream);
-
-/* NF4 quantisation of a bf16 W [n,k] (the inverse step of nf4_dequant):
- * absmax = bf16(max|w|) per 64-block; code = index of the nearest level to
- * w/absmax, decided in IEEE fp32 (ties to the lower index; an all-zero block
- * is code 7).  Packing as in lora_weight_t. */
-lora_status_t nf4_quantize(const void *w, uint8_t *codes, void *absmax, int n,
-                           int k, int blocksize, lora_stream_t stream);
+/* NF4 quantisation of a 16-bit w [n,k] of W_out.dtype into W_out's codes
+ * and block scales (written through its pointers; type NF4, blocksize 64):
+ *   absmax_scale NULL: absmax = bf16(max|w|) per 64-block (round to nearest
+ *     even); code = index of the nearest level to w/absmax decided in IEEE
+ *     fp32 (w/absmax clamped to [-1, 1]; ties to the lower index; absmax 0
+ *     gives code 7, the exact zero).  One launch.
+ *   double quantisation (absmax_scale, absmax_offset set; [QLoRA] §3):
+ *     c[b] = max|w| of block b (exact in fp32); *absmax_offset = fp32 of the
+ *     mean of all c[b]; per group G of 256 blocks, absmax_scale[G] =
+ *     fp32( max_G |fp32(c[b] - offset)| / 448 ); code[b] = E4M3 of
+ *     fp32((c[b] - offset) / scale) (round to nearest even; 0 when the
+ *     group's scale is 0); then the NF4 codes as above against the scale
+ *     code[b] decodes to (lora_weight_t).  Three launches.
+ * k % 64 == 0; with double quantisation also n·k/64 % 16 == 0 (true
+ * whenever n % 16 == 0). */
+lora_status_t nf4_quantize(const void *w, lora_weight_t W_out, int n, int k,
+                           lora_stream_t stream);
 
 /* Bytes of a cos/sin cache for max_pos positions. */
 size_t lora_rope_cache_bytes(int max_pos, int head_dim);

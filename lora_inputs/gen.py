@@ -10,7 +10,8 @@ dataset are used).  Value distributions, read as N(mean, variance):
   (std ``sqrt(0.02)``; B is non-zero so the adapter branch is exercised)
 
 Every tensor is drawn in fp32 from one CPU ``torch.Generator`` in the order
-x, W, A, B, dY and rounded to bf16 (round to nearest even).  Projections
+x, W, A, B, dY and rounded to bf16 (round to nearest even), or to fp16 when
+``dtype=torch.float16`` is asked for.  Projections
 that share an activation (q and k of the RoPE workload) draw x once.
 """
 from __future__ import annotations
@@ -96,8 +97,9 @@ def _gen(seed: int) -> torch.Generator:
     return g
 
 
-def draw_tensor(g: torch.Generator, shape, kind: str, scale: float = 1.0) -> torch.Tensor:
-    """One bf16 tensor: ``kind`` 'normal' (std ``scale``) or 'uniform'
+def draw_tensor(g: torch.Generator, shape, kind: str, scale: float = 1.0,
+                dtype=torch.bfloat16) -> torch.Tensor:
+    """One 16-bit tensor: ``kind`` 'normal' (std ``scale``) or 'uniform'
     (in ``[-scale, scale)``)."""
     if kind == "normal":
         t = torch.randn(shape, generator=g, dtype=torch.float32) * scale
@@ -105,21 +107,22 @@ def draw_tensor(g: torch.Generator, shape, kind: str, scale: float = 1.0) -> tor
         t = (torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0) * scale
     else:
         raise ValueError(kind)
-    return t.to(torch.bfloat16)
+    return t.to(dtype)
 
 
-def draw_shared_x(g: torch.Generator, M: int, k: int) -> torch.Tensor:
-    return draw_tensor(g, (M, k), "normal", 1.0)
+def draw_shared_x(g: torch.Generator, M: int, k: int, dtype=torch.bfloat16) -> torch.Tensor:
+    return draw_tensor(g, (M, k), "normal", 1.0, dtype)
 
 
-def draw_projection(g: torch.Generator, M: int, k: int, n: int, r: int, x=None) -> dict:
+def draw_projection(g: torch.Generator, M: int, k: int, n: int, r: int, x=None,
+                    dtype=torch.bfloat16) -> dict:
     """Draw x (unless given), W, A, B, dY for one projection, in that order."""
     if x is None:
-        x = draw_shared_x(g, M, k)
-    W = draw_tensor(g, (n, k), "normal", 1.0 / math.sqrt(k))
-    A = draw_tensor(g, (r, k), "uniform", 1.0 / math.sqrt(k))
-    B = draw_tensor(g, (n, r), "normal", math.sqrt(0.02))
-    dY = draw_tensor(g, (M, n), "normal", 1.0)
+        x = draw_shared_x(g, M, k, dtype)
+    W = draw_tensor(g, (n, k), "normal", 1.0 / math.sqrt(k), dtype)
+    A = draw_tensor(g, (r, k), "uniform", 1.0 / math.sqrt(k), dtype)
+    B = draw_tensor(g, (n, r), "normal", math.sqrt(0.02), dtype)
+    dY = draw_tensor(g, (M, n), "normal", 1.0, dtype)
     return {"x": x, "W": W, "A": A, "B": B, "dY": dY}
 
 

@@ -18,20 +18,26 @@ import torch
 from .build import lib_path
 
 __all__ = [
-    "LoraError", "Weight", "bf16_weight", "nf4_weight", "workspace", "workspace_size",
-    "lora_linear_fwd", "lora_linear_bwd", "lora_linear_bwd_noalloc", "lora_qk_rope_fwd",
-    "lora_qk_rope_bwd", "lora_swiglu_fwd", "lora_swiglu_bwd", "lora_merge", "lora_merge_nf4",
-    "nf4_dequant", "nf4_quantize", "lora_rope_cache_build", "lora_rope_cache_bytes",
+    "LoraError", "Weight", "dense_weight", "bf16_weight", "nf4_weight", "workspace",
+    "workspace_size", "dtype_code",
+    "lora_linear_fwd", "lora_linear_bwd", "lora_linear_bwd_noalloc", "lora_linear_fwd_dropout",
+    "lora_linear_bwd_dropout", "lora_qk_rope_fwd",
+    "lora_qk_rope_bwd", "lora_swiglu_fwd", "lora_swiglu_bwd", "lora_merge",
+    "nf4_dequant", "nf4_quantize", "lora_rope_cache_build", "lora_rope_cache_bytes", "lora_nf4_stage_bytes",
     "lora_read_device_status", "lora_clear_device_status", "lora_status_string",
     "lora_kernel_launch_count", "lora_profile_begin", "lora_profile_end",
     "OP_FWD", "OP_BWD", "OP_QK_ROPE_FWD", "OP_QK_ROPE_BWD", "OP_SWIGLU_FWD", "OP_SWIGLU_BWD",
-    "OP_MERGE", "OP_MERGE_NF4", "EXPORTS", "library",
+    "OP_MERGE", "OP_MERGE_NF4", "OP_FWD_DROPOUT", "OP_BWD_DROPOUT", "OP_FLAG_DQ", "EXPORTS",
+    "library", "DTYPE_BF16", "DTYPE_FP16",
 ]
 
 OP_FWD, OP_BWD, OP_QK_ROPE_FWD, OP_QK_ROPE_BWD = 0, 1, 2, 3
 OP_SWIGLU_FWD, OP_SWIGLU_BWD = 4, 5
 OP_MERGE, OP_MERGE_NF4 = 6, 7
-WEIGHT_BF16, WEIGHT_NF4 = 0, 1
+OP_FWD_DROPOUT, OP_BWD_DROPOUT = 8, 9
+OP_FLAG_DQ = 0x100
+WEIGHT_DENSE, WEIGHT_NF4 = 0, 1
+DTYPE_BF16, DTYPE_FP16 = 0, 1
 STATUS_NAMES = ["LORA_OK", "LORA_ERR_INVALID_ARG", "LORA_ERR_UNSUPPORTED", "LORA_ERR_WORKSPACE",
                 "LORA_ERR_ARCH", "LORA_ERR_CUDA", "LORA_ERR_TIMEOUT"]
 
@@ -46,11 +52,13 @@ class LoraError(RuntimeError):
 class Weight(ctypes.Structure):
     """``lora_weight_t``."""
     _fields_ = [("type", ctypes.c_int), ("w", ctypes.c_void_p), ("absmax", ctypes.c_void_p),
-                ("blocksize", ctypes.c_int)]
+                ("blocksize", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("absmax_scale", ctypes.c_void_p), ("absmax_offset", ctypes.c_void_p)]
 
 
 _P, _I, _F, _D, _Z, _U32P = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double,
                              ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint32))
+_U64 = ctypes.c_uint64
 
 # name -> (restype, argtypes); mirrors include/lora_b300.h
 EXPORTS = {
@@ -68,11 +76,15 @@ EXPORTS = {
                              _P, _I, _I, _I, _I, _F, _P, _Z, _P]),
     "lora_linear_bwd_noalloc": (_I, [_P, Weight, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _F,
                                      _P]),
-    "lora_merge": (_I, [_P, _P, _P, _I, _I, _I, _F, _I, _P, _Z, _P]),
-    "lora_merge_nf4": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
-    "nf4_dequant": (_I, [_P, _P, _P, _I, _I, _I, _P]),
-    "nf4_quantize": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+    "lora_linear_fwd_dropout": (_I, [_P, Weight, _P, _P, _P, _I, _I, _I, _I, _F, _F, _U64,
+                                     _U64, _P, _Z, _P]),
+    "lora_linear_bwd_dropout": (_I, [_P, Weight, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I,
+                                     _F, _F, _U64, _U64, _P, _Z, _P]),
+    "lora_merge": (_I, [Weight, _P, _P, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "nf4_dequant": (_I, [Weight, _P, _I, _I, _P]),
+    "nf4_quantize": (_I, [_P, Weight, _I, _I, _P]),
     "lora_rope_cache_bytes": (_Z, [_I, _I]),
+    "lora_nf4_stage_bytes": (_Z, [_I, _I]),
     "lora_rope_cache_build": (_I, [_P, _I, _I, _D, _P]),
     "lora_read_device_status": (_I, [_P, _U32P, _P]),
     "lora_clear_device_status": (_I, [_P, _P]),
@@ -117,16 +129,36 @@ def _check(status: int, where: str):
         raise LoraError(status, where)
 
 
-def bf16_weight(w: torch.Tensor) -> Weight:
-    return Weight(WEIGHT_BF16, w.data_ptr(), None, 0)
+def dtype_code(dtype) -> int:
+    """``LORA_DTYPE_*`` of a torch 16-bit floating dtype."""
+    if dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if dtype == torch.float16:
+        return DTYPE_FP16
+    raise TypeError(f"16-bit type bf16 or fp16 expected, got {dtype}")
 
 
-def nf4_weight(codes: torch.Tensor, absmax: torch.Tensor, blocksize: int = 64) -> Weight:
-    return Weight(WEIGHT_NF4, codes.data_ptr(), absmax.data_ptr(), blocksize)
+def dense_weight(w: torch.Tensor) -> Weight:
+    """A dense W [n, k] (bf16 or fp16: the call's 16-bit type)."""
+    return Weight(WEIGHT_DENSE, w.data_ptr(), None, 0, dtype_code(w.dtype), None, None)
+
+
+bf16_weight = dense_weight
+
+
+def nf4_weight(codes: torch.Tensor, absmax: torch.Tensor, blocksize: int = 64,
+               dtype=torch.bfloat16, absmax_scale=None, absmax_offset=None) -> Weight:
+    """An NF4 W: codes [n, k/2] and bf16 absmax [n, k/64], or with double
+    quantisation uint8 E4M3 absmax codes, fp32 absmax_scale [ceil(n·k/16384)]
+    and a one-element fp32 absmax_offset.  ``dtype`` is the call's 16-bit
+    type."""
+    return Weight(WEIGHT_NF4, codes.data_ptr(), absmax.data_ptr(), blocksize, dtype_code(dtype),
+                  None if absmax_scale is None else absmax_scale.data_ptr(),
+                  None if absmax_offset is None else absmax_offset.data_ptr())
 
 
 def _weight(W) -> Weight:
-    return W if isinstance(W, Weight) else bf16_weight(W)
+    return W if isinstance(W, Weight) else dense_weight(W)
 
 
 def workspace_size(op: int, M: int, k: int, n: int, r: int) -> int:
@@ -134,7 +166,8 @@ def workspace_size(op: int, M: int, k: int, n: int, r: int) -> int:
 
 
 def workspace(op: int, M: int, k: int, n: int, r: int, device="cuda", extra: int = 0):
-    """A zeroed workspace (status word cleared) of the size the op needs."""
+    """A zeroed workspace (status word cleared) of the size the op needs
+    (``op`` may carry OP_FLAG_DQ)."""
     nbytes = workspace_size(op, M, k, n, r)
     if nbytes == 0:
         raise LoraError(1, "lora_workspace_size")
@@ -242,39 +275,57 @@ def lora_swiglu_bwd(x, Wg, Ag, Bg, Wu, Au, Bu, g, u, dh, dx, dAg, dBg, dAu, dBu,
                                    _stream(stream)), "lora_swiglu_bwd")
 
 
+def lora_linear_fwd_dropout(x, W, A, B, y, alpha: float, dropout_p: float, seed: int,
+                            offset: int, ws, stream=None):
+    M, k = x.shape
+    n, r = y.shape[1], A.shape[0]
+    _check(library.lora_linear_fwd_dropout(_ptr(x), _weight(W), _ptr(A), _ptr(B), _ptr(y), M, k,
+                                           n, r, float(alpha), float(dropout_p), int(seed),
+                                           int(offset), _ptr(ws), ws.numel(), _stream(stream)),
+           "lora_linear_fwd_dropout")
+
+
+def lora_linear_bwd_dropout(x, W, A, B, dy, dx, dA, dB, alpha: float, dropout_p: float,
+                            seed: int, offset: int, ws, accumulate_dx: bool = False,
+                            stream=None):
+    M, k = x.shape
+    n, r = dy.shape[1], A.shape[0]
+    _check(library.lora_linear_bwd_dropout(_ptr(x), _weight(W), _ptr(A), _ptr(B), _ptr(dy),
+                                           _ptr(dx), int(bool(accumulate_dx)), _ptr(dA),
+                                           _ptr(dB), M, k, n, r, float(alpha), float(dropout_p),
+                                           int(seed), int(offset), _ptr(ws), ws.numel(),
+                                           _stream(stream)), "lora_linear_bwd_dropout")
+
+
 def lora_merge(W, A, B, alpha: float, sign: int = 1, ws=None, stream=None):
-    """W <- W + sign·(alpha/r)·B·A in place (bf16 W [n, k])."""
-    n, k = W.shape
-    r = A.shape[0]
+    """W <- W + sign·(alpha/r)·B·A in place: a dense W tensor [n, k], or an
+    NF4 ``Weight`` (dequantised, merged and re-quantised in place)."""
+    n, r = B.shape
+    k = A.shape[1]
+    Wd = _weight(W)
+    op = OP_MERGE_NF4 if Wd.type == WEIGHT_NF4 else OP_MERGE
     if ws is None:
-        ws = workspace(OP_MERGE, 1, k, n, r, device=W.device)
-    _check(library.lora_merge(_ptr(W), _ptr(A), _ptr(B), n, k, r, float(alpha), int(sign),
-                              _ptr(ws), ws.numel(), _stream(stream)), "lora_merge")
+        ws = workspace(op, 1, k, n, r, device=A.device)
+    _check(library.lora_merge(Wd, _ptr(A), _ptr(B), n, k, r, float(alpha), int(sign), _ptr(ws),
+                              ws.numel(), _stream(stream)), "lora_merge")
 
 
-def lora_merge_nf4(codes, absmax, A, B, alpha: float, sign: int = 1, ws=None, blocksize=64,
-                   stream=None):
-    """The NF4 weight (codes [n, k/2], absmax [n, k/64]) with the adapter
-    merged in (sign +1) or taken out (-1), re-quantised in place."""
-    n, k = codes.shape[0], codes.shape[1] * 2
-    r = A.shape[0]
-    if ws is None:
-        ws = workspace(OP_MERGE_NF4, 1, k, n, r, device=codes.device)
-    _check(library.lora_merge_nf4(_ptr(codes), _ptr(absmax), _ptr(A), _ptr(B), n, k, r,
-                                  float(alpha), int(sign), int(blocksize), _ptr(ws), ws.numel(),
-                                  _stream(stream)), "lora_merge_nf4")
-
-
-def nf4_dequant(codes, absmax, w_out, blocksize: int = 64, stream=None):
+def nf4_dequant(W: Weight, w_out, stream=None):
+    """w_out [n, k] (the weight's 16-bit type) from an NF4 ``Weight``."""
     n, k = w_out.shape
-    _check(library.nf4_dequant(_ptr(codes), _ptr(absmax), _ptr(w_out), n, k, blocksize,
-                               _stream(stream)), "nf4_dequant")
+    _check(library.nf4_dequant(W, _ptr(w_out), n, k, _stream(stream)), "nf4_dequant")
 
 
-def nf4_quantize(w, codes, absmax, blocksize: int = 64, stream=None):
+def nf4_quantize(w, W_out: Weight, stream=None):
+    """Quantise a 16-bit w [n, k] into the codes and block scales W_out
+    points at (double-quantised when W_out has absmax_scale)."""
     n, k = w.shape
-    _check(library.nf4_quantize(_ptr(w), _ptr(codes), _ptr(absmax), n, k, blocksize,
-                                _stream(stream)), "nf4_quantize")
+    _check(library.nf4_quantize(_ptr(w), W_out, n, k, _stream(stream)), "nf4_quantize")
+
+
+def lora_nf4_stage_bytes(n: int, k: int) -> int:
+    """Workspace bytes that let an NF4 call stage W [n, k] in 16-bit."""
+    return int(library.lora_nf4_stage_bytes(int(n), int(k)))
 
 
 def lora_rope_cache_bytes(max_pos: int, head_dim: int = 128) -> int:

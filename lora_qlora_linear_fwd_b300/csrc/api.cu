@@ -133,8 +133,11 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *ptr
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr CUtensorMapDataType kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 constexpr CUtensorMapDataType kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+// Tensor-map type of the call's 16-bit tensors.
+CUtensorMapDataType t16(bool f16) {
+  return f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
 
 // ---------------------------------------------------------------- checks
 bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -149,15 +152,25 @@ constexpr double kMb2TileCost = 1.5;
 constexpr size_t kStatusBytes = 256;
 
 lora_status_t check_weight(const lora_weight_t &W) {
-  if (W.type == LORA_WEIGHT_BF16) {
-    if (!aligned16(W.w)) return LORA_ERR_INVALID_ARG;
+  if (W.dtype != LORA_DTYPE_BF16 && W.dtype != LORA_DTYPE_FP16) return LORA_ERR_INVALID_ARG;
+  if (W.type == LORA_WEIGHT_DENSE) {
+    if (!aligned16(W.w) || W.absmax_scale || W.absmax_offset) return LORA_ERR_INVALID_ARG;
   } else if (W.type == LORA_WEIGHT_NF4) {
     if (!aligned16(W.w) || !aligned16(W.absmax)) return LORA_ERR_INVALID_ARG;
+    if ((W.absmax_scale == nullptr) != (W.absmax_offset == nullptr)) return LORA_ERR_INVALID_ARG;
+    if (W.absmax_scale && (!aligned16(W.absmax_scale) || !aligned16(W.absmax_offset)))
+      return LORA_ERR_INVALID_ARG;
     if (W.blocksize != 64) return LORA_ERR_UNSUPPORTED;
   } else {
     return LORA_ERR_INVALID_ARG;
   }
   return LORA_OK;
+}
+
+bool is_f16(const lora_weight_t &W) { return W.dtype == LORA_DTYPE_FP16; }
+bool is_dq(const lora_weight_t &W) { return W.type == LORA_WEIGHT_NF4 && W.absmax_scale; }
+Nf4Scales scales_of(const lora_weight_t &W) {
+  return Nf4Scales{W.absmax, W.absmax_scale, W.absmax_offset};
 }
 
 lora_status_t check_shape(int M, int k, int n, int r) {
@@ -200,6 +213,64 @@ bool fused_fwd_pays(int M, int n_tiles, int rl, bool rope) {
   return pairs > 0 && tiles <= pairs;
 }
 
+// NF4 weights staged in 16-bit.  The fused NF4 GEMMs decode the 4-bit codes
+// while staging each W tile, reading 0.53 bytes per weight; at large M the
+// kernels are tensor-bound and the decode costs MMA throughput (measured on
+// B300: Qwen1.5-32B gate_proj at M = 8192, fused forward 1.62 ms against
+// 1.38 ms for nf4_dequant followed by the bf16 GEMM; backward 2.31 against
+// 1.68 ms).  So when M >= kNf4StageMinM and the caller's workspace has room
+// past what the call needs, an NF4 weight is dequantised once into it and
+// the call runs on the 16-bit copy; otherwise the fused decode runs.
+constexpr int kNf4StageMinM = 2048;
+size_t nf4_stage_bytes(int rows, int k) { return align256((size_t)rows * k * 2); }
+// Room for the bf16 block scales of a double-quantised NF4 weight.
+size_t dq_expand_bytes(int rows, int k) { return align256((size_t)rows * (k / 64) * 2); }
+
+// Prepares NF4 descriptors W1 (n1 rows) and W2 (n2 rows; null: none) for the
+// kernels: when staging applies (see above; stage area at `stage_off`)
+// they are replaced by 16-bit copies dequantised there; otherwise
+// double-quantised block scales are expanded to bf16 at `dq_off` (room:
+// dq_expand_bytes per weight), the form the fused decode reads.
+lora_status_t prepare_nf4(lora_weight_t *W1, int n1, lora_weight_t *W2, int n2, int k, int M,
+                          void *ws, size_t ws_bytes, size_t dq_off, size_t stage_off,
+                          cudaStream_t st) {
+  if (W1->type != LORA_WEIGHT_NF4) return LORA_OK;
+  lora_weight_t *W[2] = {W1, W2};
+  const int rows[2] = {n1, n2};
+  const int nw = W2 ? 2 : 1;
+  uint8_t *w8 = static_cast<uint8_t *>(ws);
+  stage_off = align256(stage_off);
+  const size_t b1 = nf4_stage_bytes(n1, k), b2 = W2 ? nf4_stage_bytes(n2, k) : 0;
+  if (M >= kNf4StageMinM && ws_bytes >= stage_off + b1 + b2) {
+    for (int i = 0; i < nw; ++i) {
+      auto *dst = reinterpret_cast<uint16_t *>(w8 + stage_off + (i ? b1 : 0));
+      const cudaError_t e = launch_nf4_dequant(static_cast<const uint8_t *>(W[i]->w),
+                                               scales_of(*W[i]), dst, rows[i], k, is_f16(*W[i]),
+                                               st);
+      if (e != cudaSuccess) return LORA_ERR_CUDA;
+      lora_weight_t d{};
+      d.type = LORA_WEIGHT_DENSE;
+      d.w = dst;
+      d.dtype = W[i]->dtype;
+      *W[i] = d;
+    }
+    return LORA_OK;
+  }
+  size_t o = dq_off;
+  for (int i = 0; i < nw; ++i) {
+    if (!is_dq(*W[i])) continue;
+    auto *dst = reinterpret_cast<uint16_t *>(w8 + o);
+    const cudaError_t e =
+        launch_nf4_dq_expand(scales_of(*W[i]), dst, (size_t)rows[i] * (k / 64), st);
+    if (e != cudaSuccess) return LORA_ERR_CUDA;
+    o += dq_expand_bytes(rows[i], k);
+    W[i]->absmax = dst;
+    W[i]->absmax_scale = nullptr;
+    W[i]->absmax_offset = nullptr;
+  }
+  return LORA_OK;
+}
+
 // ------------------------------------------------------ fused GEMM set-up
 struct GroupArgs {
   lora_weight_t W;
@@ -213,6 +284,7 @@ struct GroupArgs {
 
 struct GemmOpts {
   int mode = kModeFwd;
+  bool f16 = false;           // 16-bit tensors are fp16 (else bf16)
   const void *act = nullptr;  // FWD: x [M, k]; DX: dY [M, n]
   int M = 0, Kred = 0;        // rows; main reduction length (k in FWD, n in DX)
   const GroupArgs *ga = nullptr;
@@ -246,15 +318,21 @@ struct GemmOpts {
   bool fused_v = false;
   const void *a1 = nullptr, *a2 = nullptr;
   float fv_scale = 0.0f;
+  // DX read-modify-write masked by LoRA dropout (bf16 kernel)
+  bool dropout = false;
+  uint32_t drop_thresh = 0;
+  float drop_scale = 1.0f;
+  uint64_t drop_seed = 0, drop_offset = 0;
 };
 
 bool make_w_map(CUtensorMap *m, const lora_weight_t &W, bool dx, bool nf4, int n, int k) {
+  const CUtensorMapDataType dt = t16(is_f16(W));
   if (!dx) {
     if (nf4) return make_map(m, kU8, 1, W.w, k / 2, n, (uint64_t)k / 2, 32, 128, false);
-    return make_map(m, kBF16, 2, W.w, k, n, (uint64_t)k * 2, 64, 128, true);
+    return make_map(m, dt, 2, W.w, k, n, (uint64_t)k * 2, 64, 128, true);
   }
   if (nf4) return make_map(m, kU8, 1, W.w, k / 2, n, (uint64_t)k / 2, 64, 64, false);
-  return make_map(m, kBF16, 2, W.w, k, n, (uint64_t)k * 2, 64, 64, true);
+  return make_map(m, dt, 2, W.w, k, n, (uint64_t)k * 2, 64, 64, true);
 }
 
 lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
@@ -262,6 +340,10 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
   lora_status_t s = device_info(&di);
   if (s != LORA_OK) return s;
   const bool nf4 = o.ga[0].W.type == LORA_WEIGHT_NF4;
+  const CUtensorMapDataType dt = t16(o.f16);
+  // double-quantised scales reach the GEMMs expanded (prepare_nf4)
+  if (is_dq(o.ga[0].W) || (o.ng > 1 && is_dq(o.ga[1].W)) || (o.W2 && is_dq(*o.W2)))
+    return LORA_ERR_INVALID_ARG;
   const bool dx = o.mode == kModeDx;
   const int n_extra = (o.rank_k + 63) / 64;
   GemmParams p;
@@ -270,18 +352,18 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
   const int act_cols = o.act_cols > 0 ? o.act_cols : o.Kred;
   // the down-projection in the GEMM (bf16 forward): v up to fv columns
   const int fv = (o.fused_v && !nf4 && !dx) ? (rank_pad(o.rl) <= 64 ? 64 : 128) : 0;
-  if (!make_map(&p.tm_act, kBF16, 2, o.act, act_cols, o.M, (uint64_t)act_cols * 2, 64, 128, true) ||
+  if (!make_map(&p.tm_act, dt, 2, o.act, act_cols, o.M, (uint64_t)act_cols * 2, 64, 128, true) ||
       (o.rank_k > 0 && !fv &&
-       !make_map(&p.tm_sv, kBF16, 2, o.sv, o.rl, o.M, (uint64_t)o.rl * 2, 64, 128, true)))
+       !make_map(&p.tm_sv, dt, 2, o.sv, o.rl, o.M, (uint64_t)o.rl * 2, 64, 128, true)))
     return LORA_ERR_CUDA;
   if (fv) {
     // CTA c stages rows [c·nv/2, +nv/2) of [a1; a2] (padded with zero rows)
     const int nv = rank_pad(o.rl), h = nv / 2;
     const bool two = o.a2 != nullptr;
     const int rows = two ? o.rl / 2 : o.rl;
-    if (!make_map(&p.tm_a[0], kBF16, 2, o.a1, o.Kred, rows, (uint64_t)o.Kred * 2, 64, h, true) ||
+    if (!make_map(&p.tm_a[0], dt, 2, o.a1, o.Kred, rows, (uint64_t)o.Kred * 2, 64, h, true) ||
         (two &&
-         !make_map(&p.tm_a[1], kBF16, 2, o.a2, o.Kred, rows, (uint64_t)o.Kred * 2, 64, h, true)))
+         !make_map(&p.tm_a[1], dt, 2, o.a2, o.Kred, rows, (uint64_t)o.Kred * 2, 64, h, true)))
       return LORA_ERR_CUDA;
     p.fv_nv = nv;
     p.fv_two = two ? 1 : 0;
@@ -297,7 +379,7 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
       const int n = ncols, k = o.Kred;
       const int bc = a.b_cols > 0 ? a.b_cols : o.rank_k;
       if (!make_w_map(&G.tm_w, a.W, false, nf4, n, k) ||
-          !make_map(&G.tm_b, kBF16, 2, a.b, bc, n, (uint64_t)bc * 2, 64, 128, true))
+          !make_map(&G.tm_b, dt, 2, a.b, bc, n, (uint64_t)bc * 2, 64, 128, true))
         return LORA_ERR_CUDA;
       G.ld_absmax = k / 64;
       G.b_shift = a.b_shift;
@@ -305,14 +387,14 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
       const int n = o.W2 ? o.ksplit * 64 : (o.w_rows > 0 ? o.w_rows : o.Kred), k = ncols;
       if (!make_w_map(&G.tm_w, a.W, true, nf4, n, k) ||
           (o.rank_k > 0 &&
-           !make_map(&G.tm_b, kBF16, 2, a.b, k, o.rl, (uint64_t)k * 2, 64, 64, true)))
+           !make_map(&G.tm_b, dt, 2, a.b, k, o.rl, (uint64_t)k * 2, 64, 64, true)))
         return LORA_ERR_CUDA;
       G.ld_absmax = k / 64;
     }
     if ((!o.swiglu || save_gu) &&
-        !make_map(&G.tm_out, kBF16, 2, a.out, ncols, o.M, (uint64_t)ncols * 2, 32, 32, true))
+        !make_map(&G.tm_out, dt, 2, a.out, ncols, o.M, (uint64_t)ncols * 2, 32, 32, true))
       return LORA_ERR_CUDA;
-    G.out = static_cast<__nv_bfloat16 *>(a.out);
+    G.out = static_cast<uint16_t *>(a.out);
     G.absmax = static_cast<const __nv_bfloat16 *>(a.W.absmax);
     G.ncols = ncols;
     G.sv_col = a.sv_col;
@@ -338,7 +420,7 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
   if (o.swiglu) {
     p.swiglu = 1;
     p.save_gu = save_gu ? 1 : 0;
-    if (!make_map(&p.tm_h, kBF16, 2, o.h, o.ga[0].ncols, o.M, (uint64_t)o.ga[0].ncols * 2, 32,
+    if (!make_map(&p.tm_h, dt, 2, o.h, o.ga[0].ncols, o.M, (uint64_t)o.ga[0].ncols * 2, 32,
                   32, true))
       return LORA_ERR_CUDA;
   }
@@ -375,27 +457,36 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
   p.sched.contiguous = fv ? 1 : 0;  // one run of tiles per m-block and pair
   p.accumulate = o.accumulate;
   p.acc_scale = o.acc_scale;
+  if (o.dropout) {
+    p.dropout = 1;
+    p.drop_thresh = o.drop_thresh;
+    p.drop_ld = o.ga[0].ncols;
+    p.drop_scale = o.drop_scale;
+    p.drop_seed = o.drop_seed;
+    p.drop_offset = o.drop_offset;
+  }
   p.positions = o.positions;
   p.cos_sin = o.cos_sin;
   p.max_pos = o.max_pos;
   p.status = o.status;
-  return cuda_status(launch_gemm_pair(p, o.mode, o.rope, nf4, mb, fv, p.sched.workers, st));
+  return cuda_status(launch_gemm_pair(p, o.mode, o.rope, nf4, mb, fv, p.sched.workers, o.f16, st));
 }
 
 // ------------------------------------------------------------ rank passes
 // One KMAJOR problem of the rank pass: g = P·Qᵀ over `K` (P [rows, K],
 // Q [rl, K] bf16, or Q = [Q1; Q2] with q_rows1 rows each).
 lora_status_t kmajor_problem(SkinnyProblem &P, const void *p_ptr, int rows, int K,
-                             const void *q1, const void *q2, int q_rows1, int rl, int rp) {
-  if (!make_map(&P.tm_p, kBF16, 2, p_ptr, K, rows, (uint64_t)K * 2, 64, 128, true))
+                             const void *q1, const void *q2, int q_rows1, int rl, int rp,
+                             CUtensorMapDataType dt) {
+  if (!make_map(&P.tm_p, dt, 2, p_ptr, K, rows, (uint64_t)K * 2, 64, 128, true))
     return LORA_ERR_CUDA;
   if (q2) {
-    if (!make_map(&P.tm_q, kBF16, 2, q1, K, q_rows1, (uint64_t)K * 2, 64, q_rows1, true) ||
-        !make_map(&P.tm_q2, kBF16, 2, q2, K, q_rows1, (uint64_t)K * 2, 64, q_rows1, true))
+    if (!make_map(&P.tm_q, dt, 2, q1, K, q_rows1, (uint64_t)K * 2, 64, q_rows1, true) ||
+        !make_map(&P.tm_q2, dt, 2, q2, K, q_rows1, (uint64_t)K * 2, 64, q_rows1, true))
       return LORA_ERR_CUDA;
     P.q_rows1 = q_rows1;
   } else {
-    if (!make_map(&P.tm_q, kBF16, 2, q1, K, rl, (uint64_t)K * 2, 64, rp, true))
+    if (!make_map(&P.tm_q, dt, 2, q1, K, rl, (uint64_t)K * 2, 64, rp, true))
       return LORA_ERR_CUDA;
     P.q_rows1 = 0;
   }
@@ -408,10 +499,11 @@ lora_status_t kmajor_problem(SkinnyProblem &P, const void *p_ptr, int rows, int 
 // One MNMAJOR problem: g = Pᵀ·(Qhi + Qlo)ᵀ over M tokens (P [M, rows],
 // Q hi/lo [rp, ld]).
 lora_status_t mnmajor_problem(SkinnyProblem &P, const void *p_ptr, int M, int rows,
-                              const void *q_hi, const void *q_lo, int ld, int rp) {
-  if (!make_map(&P.tm_p, kBF16, 2, p_ptr, rows, M, (uint64_t)rows * 2, 64, 64, true) ||
-      !make_map(&P.tm_q, kBF16, 2, q_hi, M, rp, (uint64_t)ld * 2, 64, rp, true) ||
-      !make_map(&P.tm_q2, kBF16, 2, q_lo, M, rp, (uint64_t)ld * 2, 64, rp, true))
+                              const void *q_hi, const void *q_lo, int ld, int rp,
+                              CUtensorMapDataType dt) {
+  if (!make_map(&P.tm_p, dt, 2, p_ptr, rows, M, (uint64_t)rows * 2, 64, 64, true) ||
+      !make_map(&P.tm_q, dt, 2, q_hi, M, rp, (uint64_t)ld * 2, 64, rp, true) ||
+      !make_map(&P.tm_q2, dt, 2, q_lo, M, rp, (uint64_t)ld * 2, 64, rp, true))
     return LORA_ERR_CUDA;
   P.rows = rows;
   P.row_tiles = (rows + 127) / 128;
@@ -451,8 +543,8 @@ unsigned long long next_epoch() {
   return (tag << 24) | c;
 }
 
-lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, uint32_t *status, void *scratch,
-                         cudaStream_t st) {
+lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, bool f16, uint32_t *status,
+                         void *scratch, cudaStream_t st) {
   DeviceInfo di;
   lora_status_t s;
   if ((s = device_info(&di))) return s;
@@ -476,14 +568,14 @@ lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, uint32_t *status, vo
   const int ctas = (int)std::max<long long>(
       1, std::min<long long>(std::min(di.sms, kSkinnyMaxCtas), units / 8));
   const long long w_sk = (units + ctas - 1) / ctas;
-  if (4 * w_sk > 3 * w_cluster) return cuda_status(launch_skinny_cluster(sp, mn, rp, st));
+  if (4 * w_sk > 3 * w_cluster) return cuda_status(launch_skinny_cluster(sp, mn, rp, f16, st));
   sp.units = units;
   sp.ctas = ctas;
   uint8_t *s8 = static_cast<uint8_t *>(scratch);
   sp.flags = reinterpret_cast<unsigned long long *>(s8);
   sp.partials = reinterpret_cast<float *>(s8 + align256((size_t)kSkinnyMaxCtas * 8));
   sp.epoch = next_epoch();
-  return cuda_status(launch_skinny_sk(sp, mn, rp, st));
+  return cuda_status(launch_skinny_sk(sp, mn, rp, f16, st));
 }
 
 // ------------------------------------------------------------------ forward
@@ -495,21 +587,22 @@ size_t fwd_bytes(int M, int rl) {
 
 // s·v = s·x·[A1; A2]ᵀ into the workspace (A2 null: one projection).
 lora_status_t fwd_rank(const void *x, const void *A1, const void *A2, int M, int k, int r,
-                       float scale, void *sv, uint32_t *status, cudaStream_t st) {
+                       float scale, void *sv, uint32_t *status, bool f16, cudaStream_t st) {
   const int nproj = A2 ? 2 : 1, rl = nproj * r, rp = rank_pad(rl);
   SkinnyParams sp;
   std::memset(&sp, 0, sizeof(sp));
   SkinnyProblem &P = sp.pr[0];
   lora_status_t s;
-  if ((s = kmajor_problem(P, x, M, k, A1, A2, r, rl, rp))) return s;
+  if ((s = kmajor_problem(P, x, M, k, A1, A2, r, rl, rp, t16(f16)))) return s;
   P.out_kind = kOutRowBf16;
-  P.out_bf16 = static_cast<__nv_bfloat16 *>(sv);
+  P.out_bf16 = static_cast<uint16_t *>(sv);
   P.ld_row = rl;
   P.r = r;
   P.nproj = nproj;
   P.scale = scale;
   sp.num_problems = 1;
-  return run_skinny(sp, false, rp, status, static_cast<uint8_t *>(sv) + fwd_sv_bytes(M, rl), st);
+  return run_skinny(sp, false, rp, f16, status, static_cast<uint8_t *>(sv) + fwd_sv_bytes(M, rl),
+                    st);
 }
 
 // ----------------------------------------------------------------- backward
@@ -547,6 +640,7 @@ struct BwdCall {
   lora_weight_t W;               // W [n1, k] (the whole n unless merged)
   lora_weight_t W2;              // merged: W of projection 2, [n - n1, k]
   bool merged;
+  bool f16;                      // 16-bit tensors are fp16 (else bf16)
   void *dx;
   int accumulate;
   float *dA, *dB, *dA2, *dB2;    // per projection
@@ -568,34 +662,36 @@ lora_status_t bwd_rank(const BwdCall &c, cudaStream_t st) {
   SkinnyProblem &PV = sp.pr[0];
   SkinnyProblem &PU = sp.pr[1];
   lora_status_t s;
-  if ((s = kmajor_problem(PV, c.x, c.M, c.k, c.A, nullptr, 0, c.rl, b.rp)) ||
-      (s = kmajor_problem(PU, c.dy, c.M, c.n, c.at<void>(b.off_bt), nullptr, 0, c.rl, b.rp)))
+  const CUtensorMapDataType dt = t16(c.f16);
+  if ((s = kmajor_problem(PV, c.x, c.M, c.k, c.A, nullptr, 0, c.rl, b.rp, dt)) ||
+      (s = kmajor_problem(PU, c.dy, c.M, c.n, c.at<void>(b.off_bt), nullptr, 0, c.rl, b.rp, dt)))
     return s;
   const int nproj = c.merged ? 2 : 1;
   PV.out_kind = kOutVt;
-  PV.out_hi = c.at<__nv_bfloat16>(b.off_vt_hi);
-  PV.out_lo = c.at<__nv_bfloat16>(b.off_vt_lo);
+  PV.out_hi = c.at<uint16_t>(b.off_vt_hi);
+  PV.out_lo = c.at<uint16_t>(b.off_vt_lo);
   PV.ld_t = b.Mp;
   PV.r = c.r;
   PV.nproj = nproj;
   PV.scale = 1.0f;
   PU.out_kind = kOutVt | kOutRowBf16;
-  PU.out_hi = c.at<__nv_bfloat16>(b.off_ut_hi);
-  PU.out_lo = c.at<__nv_bfloat16>(b.off_ut_lo);
+  PU.out_hi = c.at<uint16_t>(b.off_ut_hi);
+  PU.out_lo = c.at<uint16_t>(b.off_ut_lo);
   PU.ld_t = b.Mp;
-  PU.out_bf16 = c.at<__nv_bfloat16>(b.off_su);
+  PU.out_bf16 = c.at<uint16_t>(b.off_su);
   PU.ld_row = c.rl;
   PU.r = c.r;
   PU.nproj = nproj;
   PU.scale = c.scale;
   sp.num_problems = 2;
-  return run_skinny(sp, false, b.rp, c.status, c.at<void>(b.off_scratch), st);
+  return run_skinny(sp, false, b.rp, c.f16, c.status, c.at<void>(b.off_scratch), st);
 }
 
 lora_status_t bwd_dx(const BwdCall &c, cudaStream_t st) {
   GroupArgs ga{c.W, c.A, c.dx, c.k, 0};
   GemmOpts o;
   o.mode = kModeDx;
+  o.f16 = c.f16;
   o.act = c.dy;
   o.M = c.M;
   o.Kred = c.n;
@@ -620,10 +716,11 @@ lora_status_t bwd_grads(const BwdCall &c, cudaStream_t st) {
   SkinnyProblem &PA = sp.pr[0];
   SkinnyProblem &PB = sp.pr[1];
   lora_status_t s;
+  const CUtensorMapDataType dt = t16(c.f16);
   if ((s = mnmajor_problem(PA, c.x, c.M, c.k, c.at<void>(b.off_ut_hi), c.at<void>(b.off_ut_lo),
-                           b.Mp, b.rp)) ||
+                           b.Mp, b.rp, dt)) ||
       (s = mnmajor_problem(PB, c.dy, c.M, c.n, c.at<void>(b.off_vt_hi), c.at<void>(b.off_vt_lo),
-                           b.Mp, b.rp)))
+                           b.Mp, b.rp, dt)))
     return s;
   const int nproj = c.merged ? 2 : 1;
   PA.out_kind = kOutRowT;
@@ -640,7 +737,7 @@ lora_status_t bwd_grads(const BwdCall &c, cudaStream_t st) {
   PB.split_row = c.n1;
   PB.scale = c.scale;
   sp.num_problems = 2;
-  return run_skinny(sp, true, b.rp, c.status, c.at<void>(b.off_scratch), st);
+  return run_skinny(sp, true, b.rp, c.f16, c.status, c.at<void>(b.off_scratch), st);
 }
 
 lora_status_t run_bwd_phases(const BwdCall &c, cudaStream_t st) {
@@ -763,8 +860,11 @@ const char *lora_status_string(lora_status_t s) {
   return "LORA_ERR_UNKNOWN";
 }
 
-size_t lora_workspace_size(int op, int M, int k, int n, int r) {
-  if (M < 1 || k < 1 || n < 1 || !rank_ok(r) || M > (1 << 30)) return 0;
+}  // extern "C"
+
+namespace {
+// Workspace of an operation without the room for double-quantised scales.
+size_t ws_base(int op, int M, int k, int n, int r) {
   switch (op) {
     case LORA_OP_FWD:
       return fwd_bytes(M, r);
@@ -778,12 +878,57 @@ size_t lora_workspace_size(int op, int M, int k, int n, int r) {
       return fwd_bytes(M, 2 * r);
     case LORA_OP_SWIGLU_BWD:
       return plan_qk_bwd(M, k, 2 * n, r).total;
+    case LORA_OP_FWD_DROPOUT:
+      return fwd_bytes(M, r) + align256((size_t)M * k * 2);
+    case LORA_OP_BWD_DROPOUT:
+      return kStatusBytes + bwd_bytes(M, n, r) + align256((size_t)M * k * 2);
     case LORA_OP_MERGE:
       return kStatusBytes;
     case LORA_OP_MERGE_NF4:
       return kStatusBytes + align256((size_t)n * k * 2);
   }
   return 0;
+}
+
+// Room for the bf16 expansion of double-quantised block scales, past
+// ws_base: one weight [n, k] (two for the q/k pair, whose n is the sum, and
+// for gate / up); merges decode the scales directly.
+size_t ws_dq(int op, int k, int n) {
+  switch (op) {
+    case LORA_OP_FWD:
+    case LORA_OP_BWD:
+    case LORA_OP_FWD_DROPOUT:
+    case LORA_OP_BWD_DROPOUT:
+      return dq_expand_bytes(n, k);
+    case LORA_OP_QK_ROPE_FWD:
+    case LORA_OP_QK_ROPE_BWD:
+      return dq_expand_bytes(n, k) + 512;
+    case LORA_OP_SWIGLU_FWD:
+    case LORA_OP_SWIGLU_BWD:
+      return 2 * dq_expand_bytes(n, k);
+  }
+  return 0;
+}
+
+int op_flags(const lora_weight_t &W1, const lora_weight_t *W2 = nullptr) {
+  return (is_dq(W1) || (W2 && is_dq(*W2))) ? LORA_OP_FLAG_DQ : 0;
+}
+}  // namespace
+
+extern "C" {
+
+size_t lora_workspace_size(int op, int M, int k, int n, int r) {
+  if (M < 1 || k < 1 || n < 1 || !rank_ok(r) || M > (1 << 30)) return 0;
+  const bool dq = (op & LORA_OP_FLAG_DQ) != 0;
+  op &= ~LORA_OP_FLAG_DQ;
+  const size_t base = ws_base(op, M, k, n, r);
+  if (base == 0) return 0;
+  return base + (dq ? ws_dq(op, k, n) : 0);
+}
+
+size_t lora_nf4_stage_bytes(int n, int k) {
+  if (n < 1 || k < 1) return 0;
+  return nf4_stage_bytes(n, k);
 }
 
 size_t lora_rope_cache_bytes(int max_pos, int head_dim) {
@@ -800,20 +945,26 @@ lora_status_t lora_linear_fwd(const void *x, lora_weight_t W, const void *A, con
   if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(y) || !aligned16(ws))
     return LORA_ERR_INVALID_ARG;
   if (!std::isfinite(alpha)) return LORA_ERR_INVALID_ARG;
-  if (ws_bytes < lora_workspace_size(LORA_OP_FWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
+  const size_t need = lora_workspace_size(LORA_OP_FWD | op_flags(W), M, k, n, r);
+  if (ws_bytes < need) return LORA_ERR_WORKSPACE;
   DeviceInfo di;
   if ((s = device_info(&di))) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint32_t *status = static_cast<uint32_t *>(ws);
   void *sv = static_cast<uint8_t *>(ws) + kStatusBytes;
   const float scale = alpha / (float)r;
-  // bf16 W, one wave of tiles: one launch, s·x·Aᵀ formed in the GEMM;
+  const bool f16 = is_f16(W);
+  if ((s = prepare_nf4(&W, n, nullptr, 0, k, M, ws, ws_bytes, ws_base(LORA_OP_FWD, M, k, n, r),
+                       need, st)))
+    return s;
+  // 16-bit W, one wave of tiles: one launch, s·x·Aᵀ formed in the GEMM;
   // otherwise a rank pass first
-  const bool fused = W.type == LORA_WEIGHT_BF16 && fused_fwd_pays(M, (n + 255) / 256, r, false);
-  if (!fused && (s = fwd_rank(x, A, nullptr, M, k, r, scale, sv, status, st))) return s;
+  const bool fused = W.type == LORA_WEIGHT_DENSE && fused_fwd_pays(M, (n + 255) / 256, r, false);
+  if (!fused && (s = fwd_rank(x, A, nullptr, M, k, r, scale, sv, status, f16, st))) return s;
   GroupArgs ga{W, B, y, n, 0};
   GemmOpts o;
   o.mode = kModeFwd;
+  o.f16 = f16;
   o.act = x;
   o.M = M;
   o.Kred = k;
@@ -836,17 +987,23 @@ lora_status_t lora_linear_bwd(const void *x, lora_weight_t W, const void *A, con
   lora_status_t s;
   if ((s = lora::check_bwd_args(x, W, A, B, dy, dx, dA, dB, M, k, n, r, alpha))) return s;
   if (!aligned16(ws)) return LORA_ERR_INVALID_ARG;
-  if (ws_bytes < lora_workspace_size(LORA_OP_BWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
+  const size_t need = lora_workspace_size(LORA_OP_BWD | op_flags(W), M, k, n, r);
+  if (ws_bytes < need) return LORA_ERR_WORKSPACE;
   DeviceInfo di;
   if ((s = device_info(&di))) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *w8 = static_cast<uint8_t *>(ws);
+  const bool f16 = is_f16(W);
+  if ((s = prepare_nf4(&W, n, nullptr, 0, k, M, ws, ws_bytes, ws_base(LORA_OP_BWD, M, k, n, r),
+                       need, st)))
+    return s;
   BwdCall c{};
   c.x = x;
   c.A = A;
   c.dy = dy;
   c.W = W;
   c.merged = false;
+  c.f16 = f16;
   c.dx = dx;
   c.accumulate = accumulate_dx;
   c.dA = dA;
@@ -868,10 +1025,177 @@ lora_status_t lora_linear_bwd(const void *x, lora_weight_t W, const void *A, con
   pp.k = k;
   pp.r = r;
   pp.nproj = 1;
-  pp.B1 = static_cast<const __nv_bfloat16 *>(B);
-  pp.Bt = c.at<__nv_bfloat16>(c.b.off_bt);
-  if ((s = cuda_status(launch_bwd_prep(pp, st)))) return s;
+  pp.B1 = static_cast<const uint16_t *>(B);
+  pp.Bt = c.at<uint16_t>(c.b.off_bt);
+  if ((s = cuda_status(launch_bwd_prep(pp, f16, st)))) return s;
   return run_bwd_phases(c, st);
+}
+
+// ------------------------------------------------------------- dropout
+// Drop threshold on 16-bit uniforms and 1/q for a dropout rate p (the keep
+// probability is q = 1 − thresh/65536); false if p is outside [0, 1).
+static bool dropout_params(float p, uint32_t *thresh, float *inv_q) {
+  if (!(p >= 0.0f && p < 1.0f)) return false;
+  const double t = std::nearbyint((double)p * 65536.0);
+  if (t >= 65536.0) return false;
+  *thresh = (uint32_t)t;
+  *inv_q = (float)(1.0 / (1.0 - t / 65536.0));
+  return true;
+}
+
+lora_status_t lora_linear_fwd_dropout(const void *x, lora_weight_t W, const void *A,
+                                      const void *B, void *y, int M, int k, int n, int r,
+                                      float alpha, float dropout_p, uint64_t seed,
+                                      uint64_t offset, void *ws, size_t ws_bytes,
+                                      lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = check_shape(M, k, n, r))) return s;
+  if ((s = check_weight(W))) return s;
+  if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(y) || !aligned16(ws))
+    return LORA_ERR_INVALID_ARG;
+  uint32_t thresh = 0;
+  float inv_q = 1.0f;
+  if (!std::isfinite(alpha) || !dropout_params(dropout_p, &thresh, &inv_q))
+    return LORA_ERR_INVALID_ARG;
+  const size_t need = lora_workspace_size(LORA_OP_FWD_DROPOUT | op_flags(W), M, k, n, r);
+  if (ws_bytes < need) return LORA_ERR_WORKSPACE;
+  DeviceInfo di;
+  if ((s = device_info(&di))) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *w8 = static_cast<uint8_t *>(ws);
+  uint32_t *status = static_cast<uint32_t *>(ws);
+  void *sv = w8 + kStatusBytes;
+  auto *xd = reinterpret_cast<uint16_t *>(w8 + fwd_bytes(M, r));
+  const float scale = alpha / (float)r;
+  const bool f16 = is_f16(W);
+  if ((s = prepare_nf4(&W, n, nullptr, 0, k, M, ws, ws_bytes,
+                       ws_base(LORA_OP_FWD_DROPOUT, M, k, n, r), need, st)))
+    return s;
+  // x̃ = x ⊙ keep / q feeds the down-projection only; the base GEMM reads x
+  if ((s = cuda_status(launch_dropout_x(static_cast<const uint16_t *>(x), xd, M, k, seed, offset,
+                                        thresh, inv_q, f16, st))))
+    return s;
+  if ((s = fwd_rank(xd, A, nullptr, M, k, r, scale, sv, status, f16, st))) return s;
+  GroupArgs ga{W, B, y, n, 0};
+  GemmOpts o;
+  o.mode = kModeFwd;
+  o.f16 = f16;
+  o.act = x;
+  o.M = M;
+  o.Kred = k;
+  o.ga = &ga;
+  o.ng = 1;
+  o.sv = sv;
+  o.rl = r;
+  o.rank_k = r;
+  o.status = status;
+  return run_gemm(o, st);
+}
+
+lora_status_t lora_linear_bwd_dropout(const void *x, lora_weight_t W, const void *A,
+                                      const void *B, const void *dy, void *dx, int accumulate_dx,
+                                      float *dA, float *dB, int M, int k, int n, int r,
+                                      float alpha, float dropout_p, uint64_t seed,
+                                      uint64_t offset, void *ws, size_t ws_bytes,
+                                      lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = lora::check_bwd_args(x, W, A, B, dy, dx, dA, dB, M, k, n, r, alpha))) return s;
+  if (!aligned16(ws)) return LORA_ERR_INVALID_ARG;
+  uint32_t thresh = 0;
+  float inv_q = 1.0f;
+  if (!dropout_params(dropout_p, &thresh, &inv_q)) return LORA_ERR_INVALID_ARG;
+  const size_t need = lora_workspace_size(LORA_OP_BWD_DROPOUT | op_flags(W), M, k, n, r);
+  if (ws_bytes < need) return LORA_ERR_WORKSPACE;
+  DeviceInfo di;
+  if ((s = device_info(&di))) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *w8 = static_cast<uint8_t *>(ws);
+  auto *xd = reinterpret_cast<uint16_t *>(w8 + kStatusBytes + bwd_bytes(M, n, r));
+  const bool f16 = is_f16(W);
+  const int dtype = W.dtype;
+  if ((s = prepare_nf4(&W, n, nullptr, 0, k, M, ws, ws_bytes,
+                       ws_base(LORA_OP_BWD_DROPOUT, M, k, n, r), need, st)))
+    return s;
+  BwdCall c{};
+  c.x = xd;  // the rank passes reduce over the dropped-out x (v and dA)
+  c.A = A;
+  c.dy = dy;
+  c.W = W;
+  c.merged = false;
+  c.f16 = f16;
+  c.dx = dx;
+  c.accumulate = accumulate_dx;
+  c.dA = dA;
+  c.dB = dB;
+  c.M = M;
+  c.k = k;
+  c.n = n;
+  c.n1 = n;
+  c.r = r;
+  c.rl = r;
+  c.scale = alpha / (float)r;
+  c.status = static_cast<uint32_t *>(ws);
+  c.b = plan_bwd(M, n, r, kStatusBytes);
+  c.ws = w8;
+  BwdPrep pp{};
+  pp.M = M;
+  pp.n1 = n;
+  pp.k = k;
+  pp.r = r;
+  pp.nproj = 1;
+  pp.B1 = static_cast<const uint16_t *>(B);
+  pp.Bt = c.at<uint16_t>(c.b.off_bt);
+  if ((s = cuda_status(launch_bwd_prep(pp, f16, st)))) return s;
+  // the same mask as the forward, regenerated from (seed, offset)
+  if ((s = cuda_status(launch_dropout_x(static_cast<const uint16_t *>(x), xd, M, k, seed, offset,
+                                        thresh, inv_q, f16, st))))
+    return s;
+  if ((s = bwd_rank(c, st))) return s;
+  // dX = dY·W (no adapter K-blocks) ...
+  {
+    GroupArgs ga{W, nullptr, dx, k, 0};
+    GemmOpts o;
+    o.mode = kModeDx;
+    o.f16 = f16;
+    o.act = dy;
+    o.M = M;
+    o.Kred = n;
+    o.ga = &ga;
+    o.ng = 1;
+    o.rank_k = 0;
+    o.accumulate = accumulate_dx;
+    o.status = c.status;
+    if ((s = run_gemm(o, st))) return s;
+  }
+  // ... + (s·u·A) ⊙ keep / q: the adapter term as its own K = r GEMM whose
+  // read-modify-write epilogue applies the mask
+  {
+    lora_weight_t wa{};
+    wa.type = LORA_WEIGHT_DENSE;
+    wa.w = A;
+    wa.dtype = dtype;
+    GroupArgs ga{wa, nullptr, dx, k, 0};
+    GemmOpts o;
+    o.mode = kModeDx;
+    o.f16 = f16;
+    o.act = c.at<void>(c.b.off_su);
+    o.act_cols = r;
+    o.M = M;
+    o.Kred = 64;
+    o.w_rows = r;
+    o.ga = &ga;
+    o.ng = 1;
+    o.rank_k = 0;
+    o.accumulate = 1;
+    o.status = c.status;
+    o.dropout = true;
+    o.drop_thresh = thresh;
+    o.drop_scale = inv_q;
+    o.drop_seed = seed;
+    o.drop_offset = offset;
+    if ((s = run_gemm(o, st))) return s;
+  }
+  return bwd_grads(c, st);
 }
 
 static lora_status_t check_qk(const void *x, lora_weight_t Wq, const void *Aq, const void *Bq,
@@ -885,7 +1209,7 @@ static lora_status_t check_qk(const void *x, lora_weight_t Wq, const void *Aq, c
   if ((s = check_shape(M, hidden, nqh * head_dim, r))) return s;
   if ((s = check_weight(Wq))) return s;
   if ((s = check_weight(Wk))) return s;
-  if (Wq.type != Wk.type) return LORA_ERR_UNSUPPORTED;
+  if (Wq.type != Wk.type || Wq.dtype != Wk.dtype) return LORA_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(Aq) || !aligned16(Bq) || !aligned16(Ak) || !aligned16(Bk) ||
       !aligned16(ws) || !positions || (reinterpret_cast<uintptr_t>(positions) & 3u))
     return LORA_ERR_INVALID_ARG;
@@ -907,7 +1231,7 @@ lora_status_t lora_qk_rope_fwd(const void *x, lora_weight_t Wq, const void *Aq, 
     return s;
   if (!aligned16(q) || !aligned16(k_out)) return LORA_ERR_INVALID_ARG;
   const int nq = n_q_heads * head_dim, nk = n_kv_heads * head_dim;
-  size_t need = lora_workspace_size(LORA_OP_QK_ROPE_FWD, M, hidden, nq + nk, r);
+  size_t need = lora_workspace_size(LORA_OP_QK_ROPE_FWD | op_flags(Wq, &Wk), M, hidden, nq + nk, r);
   const size_t cache_off = align256(need);
   if (!cos_sin_cache) need = cache_off + lora_rope_cache_bytes(max_pos, head_dim);
   if (ws_bytes < need) return LORA_ERR_WORKSPACE;
@@ -916,6 +1240,10 @@ lora_status_t lora_qk_rope_fwd(const void *x, lora_weight_t Wq, const void *Aq, 
   if ((s = device_info(&di))) return s;
   uint8_t *w8 = static_cast<uint8_t *>(ws);
   uint32_t *status = static_cast<uint32_t *>(ws);
+  const bool f16 = is_f16(Wq);
+  if ((s = prepare_nf4(&Wq, nq, &Wk, nk, hidden, M, ws, ws_bytes,
+                       ws_base(LORA_OP_QK_ROPE_FWD, M, hidden, nq + nk, r), need, st)))
+    return s;
   const float *cache = cos_sin_cache;
   if (!cache) {
     float *cb = reinterpret_cast<float *>(w8 + cache_off);
@@ -926,13 +1254,14 @@ lora_status_t lora_qk_rope_fwd(const void *x, lora_weight_t Wq, const void *Aq, 
   // rank pass over both projections at once
   void *sv = w8 + kStatusBytes;
   const float scale = alpha / (float)r;
-  const bool fused = Wq.type == LORA_WEIGHT_BF16 &&
+  const bool fused = Wq.type == LORA_WEIGHT_DENSE &&
                      fused_fwd_pays(M, (nq + 255) / 256 + (nk + 255) / 256, 2 * r, true);
-  if (!fused && (s = fwd_rank(x, Aq, Ak, M, hidden, r, scale, sv, status, st))) return s;
+  if (!fused && (s = fwd_rank(x, Aq, Ak, M, hidden, r, scale, sv, status, f16, st))) return s;
   // one GEMM launch over both weights; group g reduces over its r columns of s·v
   GroupArgs ga[2] = {{Wq, Bq, q, nq, 0}, {Wk, Bk, k_out, nk, r}};
   GemmOpts o;
   o.mode = kModeFwd;
+  o.f16 = f16;
   o.act = x;
   o.M = M;
   o.Kred = hidden;
@@ -969,7 +1298,7 @@ lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq, 
       !aligned16(dAk) || !aligned16(dBk))
     return LORA_ERR_INVALID_ARG;
   const int nq = n_q_heads * head_dim, nk = n_kv_heads * head_dim;
-  size_t need = lora_workspace_size(LORA_OP_QK_ROPE_BWD, M, hidden, nq + nk, r);
+  size_t need = lora_workspace_size(LORA_OP_QK_ROPE_BWD | op_flags(Wq, &Wk), M, hidden, nq + nk, r);
   const size_t cache_off = align256(need);
   if (!cos_sin_cache) need = cache_off + lora_rope_cache_bytes(max_pos, head_dim);
   if (ws_bytes < need) return LORA_ERR_WORKSPACE;
@@ -978,6 +1307,10 @@ lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq, 
   if ((s = device_info(&di))) return s;
   uint8_t *w8 = static_cast<uint8_t *>(ws);
   uint32_t *status = static_cast<uint32_t *>(ws);
+  const bool f16 = is_f16(Wq);
+  if ((s = prepare_nf4(&Wq, nq, &Wk, nk, hidden, M, ws, ws_bytes,
+                       ws_base(LORA_OP_QK_ROPE_BWD, M, hidden, nq + nk, r), need, st)))
+    return s;
   const float *cache = cos_sin_cache;
   if (!cache) {
     float *cb = reinterpret_cast<float *>(w8 + cache_off);
@@ -995,6 +1328,7 @@ lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq, 
   c.W = Wq;
   c.W2 = Wk;
   c.merged = true;
+  c.f16 = f16;
   c.dx = dx;
   c.accumulate = accumulate_dx;
   c.dA = dAq;
@@ -1014,9 +1348,9 @@ lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq, 
   // set-up: dq, dk rotated back (RoPE is orthogonal) into one [M, nq+nk]
   // gradient, A_qk, B_qkᵀ
   BwdPrep pp{};
-  pp.dy1 = static_cast<const __nv_bfloat16 *>(dq);
-  pp.dy2 = static_cast<const __nv_bfloat16 *>(dk);
-  pp.dy_out = reinterpret_cast<__nv_bfloat16 *>(w8 + qp.off_dy);
+  pp.dy1 = static_cast<const uint16_t *>(dq);
+  pp.dy2 = static_cast<const uint16_t *>(dk);
+  pp.dy_out = reinterpret_cast<uint16_t *>(w8 + qp.off_dy);
   pp.pos = positions;
   pp.cos_sin = cache;
   pp.max_pos = max_pos;
@@ -1027,13 +1361,13 @@ lora_status_t lora_qk_rope_bwd(const void *x, lora_weight_t Wq, const void *Aq, 
   pp.k = hidden;
   pp.r = r;
   pp.nproj = 2;
-  pp.A1 = static_cast<const __nv_bfloat16 *>(Aq);
-  pp.A2 = static_cast<const __nv_bfloat16 *>(Ak);
-  pp.A_out = reinterpret_cast<__nv_bfloat16 *>(w8 + qp.off_a);
-  pp.B1 = static_cast<const __nv_bfloat16 *>(Bq);
-  pp.B2 = static_cast<const __nv_bfloat16 *>(Bk);
-  pp.Bt = c.at<__nv_bfloat16>(c.b.off_bt);
-  if ((s = cuda_status(launch_bwd_prep(pp, st)))) return s;
+  pp.A1 = static_cast<const uint16_t *>(Aq);
+  pp.A2 = static_cast<const uint16_t *>(Ak);
+  pp.A_out = reinterpret_cast<uint16_t *>(w8 + qp.off_a);
+  pp.B1 = static_cast<const uint16_t *>(Bq);
+  pp.B2 = static_cast<const uint16_t *>(Bk);
+  pp.Bt = c.at<uint16_t>(c.b.off_bt);
+  if ((s = cuda_status(launch_bwd_prep(pp, f16, st)))) return s;
   return run_bwd_phases(c, st);
 }
 
@@ -1044,7 +1378,7 @@ static lora_status_t check_pair(const void *x, lora_weight_t Wg, const void *Ag,
   if ((s = check_shape(M, k, n, r))) return s;
   if ((s = check_weight(Wg))) return s;
   if ((s = check_weight(Wu))) return s;
-  if (Wg.type != Wu.type) return LORA_ERR_UNSUPPORTED;
+  if (Wg.type != Wu.type || Wg.dtype != Wu.dtype) return LORA_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(Ag) || !aligned16(Bg) || !aligned16(Au) || !aligned16(Bu) ||
       !aligned16(ws))
     return LORA_ERR_INVALID_ARG;
@@ -1060,17 +1394,22 @@ lora_status_t lora_swiglu_fwd(const void *x, lora_weight_t Wg, const void *Ag, c
   if ((s = check_pair(x, Wg, Ag, Bg, Wu, Au, Bu, M, k, n, r, alpha, ws))) return s;
   if (!aligned16(h) || (g == nullptr) != (u == nullptr) || (g && (!aligned16(g) || !aligned16(u))))
     return LORA_ERR_INVALID_ARG;
-  if (ws_bytes < lora_workspace_size(LORA_OP_SWIGLU_FWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
+  const size_t need = lora_workspace_size(LORA_OP_SWIGLU_FWD | op_flags(Wg, &Wu), M, k, n, r);
+  if (ws_bytes < need) return LORA_ERR_WORKSPACE;
   DeviceInfo di;
   if ((s = device_info(&di))) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint32_t *status = static_cast<uint32_t *>(ws);
+  const bool f16 = is_f16(Wg);
+  if ((s = prepare_nf4(&Wg, n, &Wu, n, k, M, ws, ws_bytes,
+                       ws_base(LORA_OP_SWIGLU_FWD, M, k, n, r), need, st)))
+    return s;
   void *sv = static_cast<uint8_t *>(ws) + kStatusBytes;
   const float scale = alpha / (float)r;
   // s·v = s·x·[Ag; Au]ᵀ [M, 2r]: formed in the GEMM for bf16 W, else by a
   // rank pass over both projections
-  const bool fused = Wg.type == LORA_WEIGHT_BF16 && fused_fwd_pays(M, (n + 127) / 128, 2 * r, false);
-  if (!fused && (s = fwd_rank(x, Ag, Au, M, k, r, scale, sv, status, st))) return s;
+  const bool fused = Wg.type == LORA_WEIGHT_DENSE && fused_fwd_pays(M, (n + 127) / 128, 2 * r, false);
+  if (!fused && (s = fwd_rank(x, Ag, Au, M, k, r, scale, sv, status, f16, st))) return s;
   // one fused GEMM: CTA 0 of a pair stages gate rows, CTA 1 the up rows of
   // the same output columns; a rank K-block of [s·vg | s·vu] meets Bg in the
   // gate half and Bu (read r columns to the left, so it lines up with s·vu)
@@ -1078,6 +1417,7 @@ lora_status_t lora_swiglu_fwd(const void *x, lora_weight_t Wg, const void *Ag, c
   GroupArgs ga[2] = {{Wg, Bg, g, n, 0, r, 0}, {Wu, Bu, u, n, 0, r, -r}};
   GemmOpts o;
   o.mode = kModeFwd;
+  o.f16 = f16;
   o.act = x;
   o.M = M;
   o.Kred = k;
@@ -1107,11 +1447,16 @@ lora_status_t lora_swiglu_bwd(const void *x, lora_weight_t Wg, const void *Ag, c
   if (!aligned16(g) || !aligned16(u) || !aligned16(dh) || !aligned16(dx) || !aligned16(dAg) ||
       !aligned16(dBg) || !aligned16(dAu) || !aligned16(dBu))
     return LORA_ERR_INVALID_ARG;
-  if (ws_bytes < lora_workspace_size(LORA_OP_SWIGLU_BWD, M, k, n, r)) return LORA_ERR_WORKSPACE;
+  const size_t need = lora_workspace_size(LORA_OP_SWIGLU_BWD | op_flags(Wg, &Wu), M, k, n, r);
+  if (ws_bytes < need) return LORA_ERR_WORKSPACE;
   DeviceInfo di;
   if ((s = device_info(&di))) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *w8 = static_cast<uint8_t *>(ws);
+  const bool f16 = is_f16(Wg);
+  if ((s = prepare_nf4(&Wg, n, &Wu, n, k, M, ws, ws_bytes,
+                       ws_base(LORA_OP_SWIGLU_BWD, M, k, n, r), need, st)))
+    return s;
   // gate and up as one projection of rank 2r over n_total = 2n outputs:
   // dY = [dg | du], A = [Ag; Au], B = diag(Bg, Bu), W = [Wg; Wu] along dX's
   // reduction (the q/k layout)
@@ -1123,6 +1468,7 @@ lora_status_t lora_swiglu_bwd(const void *x, lora_weight_t Wg, const void *Ag, c
   c.W = Wg;
   c.W2 = Wu;
   c.merged = true;
+  c.f16 = f16;
   c.dx = dx;
   c.accumulate = accumulate_dx;
   c.dA = dAg;
@@ -1140,10 +1486,10 @@ lora_status_t lora_swiglu_bwd(const void *x, lora_weight_t Wg, const void *Ag, c
   c.b = plan_bwd(M, 2 * n, 2 * r, 0);
   c.ws = w8 + qp.off_area;
   BwdPrep pp{};
-  pp.sw_dh = static_cast<const __nv_bfloat16 *>(dh);
-  pp.sw_g = static_cast<const __nv_bfloat16 *>(g);
-  pp.sw_u = static_cast<const __nv_bfloat16 *>(u);
-  pp.dy_out = reinterpret_cast<__nv_bfloat16 *>(w8 + qp.off_dy);
+  pp.sw_dh = static_cast<const uint16_t *>(dh);
+  pp.sw_g = static_cast<const uint16_t *>(g);
+  pp.sw_u = static_cast<const uint16_t *>(u);
+  pp.dy_out = reinterpret_cast<uint16_t *>(w8 + qp.off_dy);
   pp.status = c.status;
   pp.M = M;
   pp.n1 = n;
@@ -1151,26 +1497,30 @@ lora_status_t lora_swiglu_bwd(const void *x, lora_weight_t Wg, const void *Ag, c
   pp.k = k;
   pp.r = r;
   pp.nproj = 2;
-  pp.A1 = static_cast<const __nv_bfloat16 *>(Ag);
-  pp.A2 = static_cast<const __nv_bfloat16 *>(Au);
-  pp.A_out = reinterpret_cast<__nv_bfloat16 *>(w8 + qp.off_a);
-  pp.B1 = static_cast<const __nv_bfloat16 *>(Bg);
-  pp.B2 = static_cast<const __nv_bfloat16 *>(Bu);
-  pp.Bt = c.at<__nv_bfloat16>(c.b.off_bt);
-  if ((s = cuda_status(launch_bwd_prep(pp, st)))) return s;
+  pp.A1 = static_cast<const uint16_t *>(Ag);
+  pp.A2 = static_cast<const uint16_t *>(Au);
+  pp.A_out = reinterpret_cast<uint16_t *>(w8 + qp.off_a);
+  pp.B1 = static_cast<const uint16_t *>(Bg);
+  pp.B2 = static_cast<const uint16_t *>(Bu);
+  pp.Bt = c.at<uint16_t>(c.b.off_bt);
+  if ((s = cuda_status(launch_bwd_prep(pp, f16, st)))) return s;
   return run_bwd_phases(c, st);
 }
 
-// W [n, k] bf16 (in place) += sign·s·B·A on the tensor cores: the dX GEMM
+// W [n, k] 16-bit (in place) += sign·s·B·A on the tensor cores: the dX GEMM
 // with B [n, r] as its activation (one 64-wide K-block, columns past r read
 // as zero), A [r, k] as its MN-major weight (rows past r zero) and the
 // read-modify-write epilogue scaled by sign·s.
-static lora_status_t merge_bf16(void *W, const void *A, const void *B, int n, int k, int r,
-                                float scale, uint32_t *status, cudaStream_t st) {
-  lora_weight_t wa{LORA_WEIGHT_BF16, A, nullptr, 0};
+static lora_status_t merge_dense(void *W, int dtype, const void *A, const void *B, int n, int k,
+                                 int r, float scale, uint32_t *status, cudaStream_t st) {
+  lora_weight_t wa{};
+  wa.type = LORA_WEIGHT_DENSE;
+  wa.w = A;
+  wa.dtype = dtype;
   GroupArgs ga{wa, nullptr, W, k, 0};
   GemmOpts o;
   o.mode = kModeDx;
+  o.f16 = dtype == LORA_DTYPE_FP16;
   o.act = B;
   o.act_cols = r;
   o.M = n;
@@ -1195,67 +1545,69 @@ static lora_status_t check_merge(const void *A, const void *B, int n, int k, int
   return LORA_OK;
 }
 
-lora_status_t lora_merge(void *W, const void *A, const void *B, int n, int k, int r, float alpha,
-                         int sign, void *ws, size_t ws_bytes, lora_stream_t stream) {
+lora_status_t lora_merge(lora_weight_t W, const void *A, const void *B, int n, int k, int r,
+                         float alpha, int sign, void *ws, size_t ws_bytes, lora_stream_t stream) {
   lora_status_t s;
   if ((s = check_merge(A, B, n, k, r, alpha, sign, ws))) return s;
-  if (!aligned16(W)) return LORA_ERR_INVALID_ARG;
-  if (ws_bytes < lora_workspace_size(LORA_OP_MERGE, 1, k, n, r)) return LORA_ERR_WORKSPACE;
-  DeviceInfo di;
-  if ((s = device_info(&di))) return s;
-  return merge_bf16(W, A, B, n, k, r, (float)sign * alpha / (float)r, static_cast<uint32_t *>(ws),
-                    reinterpret_cast<cudaStream_t>(stream));
-}
-
-lora_status_t lora_merge_nf4(uint8_t *codes, void *absmax, const void *A, const void *B, int n,
-                             int k, int r, float alpha, int sign, int blocksize, void *ws,
-                             size_t ws_bytes, lora_stream_t stream) {
-  lora_status_t s;
-  if ((s = check_merge(A, B, n, k, r, alpha, sign, ws))) return s;
-  if (blocksize != 64) return LORA_ERR_UNSUPPORTED;
-  if (!aligned16(codes) || !aligned16(absmax)) return LORA_ERR_INVALID_ARG;
-  if (ws_bytes < lora_workspace_size(LORA_OP_MERGE_NF4, 1, k, n, r)) return LORA_ERR_WORKSPACE;
+  if ((s = check_weight(W))) return s;
+  const bool nf4 = W.type == LORA_WEIGHT_NF4;
+  if (ws_bytes < lora_workspace_size(nf4 ? LORA_OP_MERGE_NF4 : LORA_OP_MERGE, 1, k, n, r))
+    return LORA_ERR_WORKSPACE;
   DeviceInfo di;
   if ((s = device_info(&di))) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  auto *wbf = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(ws) + kStatusBytes);
-  auto *am = static_cast<__nv_bfloat16 *>(absmax);
+  const float scale = (float)sign * alpha / (float)r;
+  uint32_t *status = static_cast<uint32_t *>(ws);
+  if (!nf4)
+    return merge_dense(const_cast<void *>(W.w), W.dtype, A, B, n, k, r, scale, status, st);
   // dequantise into the workspace, merge there, quantise back in place
-  if ((s = cuda_status(launch_nf4_dequant(codes, am, wbf, n, k, st)))) return s;
-  if ((s = merge_bf16(wbf, A, B, n, k, r, (float)sign * alpha / (float)r,
-                      static_cast<uint32_t *>(ws), st)))
+  // (the weight's own scale form: bf16 absmax or double-quantised)
+  auto *wd = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + kStatusBytes);
+  auto *codes = static_cast<uint8_t *>(const_cast<void *>(W.w));
+  if ((s = cuda_status(launch_nf4_dequant(codes, scales_of(W), wd, n, k, is_f16(W), st))))
     return s;
-  return cuda_status(launch_nf4_quantize(wbf, codes, am, n, k, st));
+  if ((s = merge_dense(wd, W.dtype, A, B, n, k, r, scale, status, st))) return s;
+  return cuda_status(launch_nf4_quantize(wd, codes, const_cast<void *>(W.absmax),
+                                         const_cast<float *>(W.absmax_scale),
+                                         const_cast<float *>(W.absmax_offset), n, k, is_f16(W),
+                                         st));
 }
 
-lora_status_t nf4_dequant(const uint8_t *codes, const void *absmax, void *w_out, int n, int k,
-                          int blocksize, lora_stream_t stream) {
-  if (blocksize != 64) return LORA_ERR_UNSUPPORTED;
-  if (n < 1 || k < 1 || k % 64) return LORA_ERR_INVALID_ARG;
-  if (!aligned16(codes) || !absmax || (reinterpret_cast<uintptr_t>(absmax) & 1u) ||
-      !aligned16(w_out))
-    return LORA_ERR_INVALID_ARG;
-  DeviceInfo di;
+static lora_status_t check_nf4_call(const lora_weight_t &W, int n, int k) {
   lora_status_t s;
+  if (W.type != LORA_WEIGHT_NF4) return LORA_ERR_INVALID_ARG;
+  if ((s = check_weight(W))) return s;
+  if (n < 1 || k < 1 || n > (1 << 20) || k > (1 << 20)) return LORA_ERR_INVALID_ARG;
+  if (k % 64) return LORA_ERR_UNSUPPORTED;
+  // double quantisation: the quantiser parks 16 bytes of statistics in each
+  // group's scale codes, so the last group needs 16 blocks (n·k/64 % 16 == 0)
+  if (W.absmax_scale && ((size_t)n * (k / 64)) % 16) return LORA_ERR_UNSUPPORTED;
+  return LORA_OK;
+}
+
+lora_status_t nf4_dequant(lora_weight_t W, void *w_out, int n, int k, lora_stream_t stream) {
+  lora_status_t s;
+  if ((s = check_nf4_call(W, n, k))) return s;
+  if (!aligned16(w_out)) return LORA_ERR_INVALID_ARG;
+  DeviceInfo di;
   if ((s = device_info(&di))) return s;
-  return cuda_status(launch_nf4_dequant(codes, static_cast<const __nv_bfloat16 *>(absmax),
-                                        static_cast<__nv_bfloat16 *>(w_out), n, k,
+  return cuda_status(launch_nf4_dequant(static_cast<const uint8_t *>(W.w), scales_of(W),
+                                        static_cast<uint16_t *>(w_out), n, k, is_f16(W),
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
-lora_status_t nf4_quantize(const void *w, uint8_t *codes, void *absmax, int n, int k,
-                           int blocksize, lora_stream_t stream) {
-  if (blocksize != 64) return LORA_ERR_UNSUPPORTED;
-  if (n < 1 || k < 1 || k % 64) return LORA_ERR_INVALID_ARG;
-  if (!aligned16(w) || !aligned16(codes) || !absmax ||
-      (reinterpret_cast<uintptr_t>(absmax) & 1u))
-    return LORA_ERR_INVALID_ARG;
-  DeviceInfo di;
+lora_status_t nf4_quantize(const void *w, lora_weight_t W_out, int n, int k,
+                           lora_stream_t stream) {
   lora_status_t s;
+  if ((s = check_nf4_call(W_out, n, k))) return s;
+  if (!aligned16(w)) return LORA_ERR_INVALID_ARG;
+  DeviceInfo di;
   if ((s = device_info(&di))) return s;
-  return cuda_status(launch_nf4_quantize(static_cast<const __nv_bfloat16 *>(w), codes,
-                                         static_cast<__nv_bfloat16 *>(absmax), n, k,
-                                         reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_nf4_quantize(
+      static_cast<const uint16_t *>(w), static_cast<uint8_t *>(const_cast<void *>(W_out.w)),
+      const_cast<void *>(W_out.absmax), const_cast<float *>(W_out.absmax_scale),
+      const_cast<float *>(W_out.absmax_offset), n, k, is_f16(W_out),
+      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 lora_status_t lora_rope_cache_build(float *cos_sin, int max_pos, int head_dim, double theta,

@@ -5,6 +5,7 @@
 
 #include "kernels.h"
 #include "nf4_levels.cuh"
+#include "philox.cuh"
 
 namespace lora {
 
@@ -55,10 +56,11 @@ struct Nf4Table {
   uint32_t lo[4], hi[4];
 };
 
+template <bool F16>
 LORA_DEV Nf4Table nf4_table(const float (&lv)[16], float a) {
   uint32_t pk[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) pk[j] = pack_bf16x2(lv[2 * j] * a, lv[2 * j + 1] * a);
+  for (int j = 0; j < 8; ++j) pk[j] = pack2<F16>(lv[2 * j] * a, lv[2 * j + 1] * a);
   Nf4Table t;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -112,9 +114,12 @@ LORA_DEV void nf4_decode_words(const uint32_t (&words)[8], uint32_t dst, const N
 // values already at `orow` (ncols valid columns), rounding once to bf16.
 // Used where the result accumulates into its destination (dX += ..., and
 // W ± s·B·A when merging an adapter into its weight).
-template <int BN>
-LORA_DEV void epi_accumulate_tile(uint32_t t_acc, __nv_bfloat16 *orow, bool row_ok, int ncols,
-                                  float scale) {
+// DROPOUT: the result is multiplied by the dropout keep bit of its output
+// element (row `grow`, column col0 + column in tile) times p.drop_scale.
+template <int BN, bool F16, bool DROPOUT = false>
+LORA_DEV void epi_accumulate_tile(uint32_t t_acc, uint16_t *orow, bool row_ok, int ncols,
+                                  float scale, const GemmParams *p = nullptr, int grow = 0,
+                                  int col0 = 0) {
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t r[32];
@@ -125,24 +130,37 @@ LORA_DEV void epi_accumulate_tile(uint32_t t_acc, __nv_bfloat16 *orow, bool row_
       float f[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]) * scale;
+      if constexpr (DROPOUT) {
+        // 32 columns = two 16-element Philox blocks (row·ld and the column are
+        // multiples of 16)
+        const uint64_t e0 = (uint64_t)grow * (uint64_t)p->drop_ld + (uint64_t)(col0 + c * 32);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t keep =
+              dropout_keep16(e0 / 16 + h, p->drop_seed, p->drop_offset, p->drop_thresh);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            f[16 * h + j] = (keep >> j) & 1u ? f[16 * h + j] * p->drop_scale : 0.0f;
+        }
+      }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint4 old = dst[j];
         const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&ow[e]);
-          f[8 * j + 2 * e] += __low2float(h);
-          f[8 * j + 2 * e + 1] += __high2float(h);
+          const float2 h = unpack2<F16>(ow[e]);
+          f[8 * j + 2 * e] += h.x;
+          f[8 * j + 2 * e + 1] += h.y;
         }
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         uint4 w;
-        w.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
-        w.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
-        w.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
-        w.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
+        w.x = pack2<F16>(f[8 * j + 0], f[8 * j + 1]);
+        w.y = pack2<F16>(f[8 * j + 2], f[8 * j + 3]);
+        w.z = pack2<F16>(f[8 * j + 4], f[8 * j + 5]);
+        w.w = pack2<F16>(f[8 * j + 6], f[8 * j + 7]);
         dst[j] = w;
       }
     }
@@ -196,7 +214,7 @@ LORA_DEV void rope_stage(const float *cs, int half, uint32_t srow, uint32_t bar,
 // here as soon as half 0 sits in registers).  Otherwise each 32-column
 // chunk reads its cos / sin from the cache directly.  Returns false when a
 // wait gave up.
-template <int BN, bool ROPE, bool STAGED>
+template <int BN, bool ROPE, bool STAGED, bool F16>
 LORA_DEV bool epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap *tm_out,
                                  int col0, int row0, int ncols, const float *cs, uint32_t srow,
                                  uint32_t cs_bar, uint32_t &cs_phase, int lane,
@@ -217,10 +235,10 @@ LORA_DEV bool epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap
       __syncwarp();
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        st_shared_v4(b + at(q), pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1])),
-                     pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
-                     pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
-                     pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+        st_shared_v4(b + at(q), pack2<F16>(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1])),
+                     pack2<F16>(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
+                     pack2<F16>(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
+                     pack2<F16>(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -261,10 +279,10 @@ LORA_DEV bool epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap
             oa[e] = a * co[e] - bv * si[e];
             ob[e] = bv * co[e] + a * si[e];
           }
-          st_shared_v4(ba + at(q), pack_bf16x2(oa[0], oa[1]), pack_bf16x2(oa[2], oa[3]),
-                       pack_bf16x2(oa[4], oa[5]), pack_bf16x2(oa[6], oa[7]));
-          st_shared_v4(bb + at(q), pack_bf16x2(ob[0], ob[1]), pack_bf16x2(ob[2], ob[3]),
-                       pack_bf16x2(ob[4], ob[5]), pack_bf16x2(ob[6], ob[7]));
+          st_shared_v4(ba + at(q), pack2<F16>(oa[0], oa[1]), pack2<F16>(oa[2], oa[3]),
+                       pack2<F16>(oa[4], oa[5]), pack2<F16>(oa[6], oa[7]));
+          st_shared_v4(bb + at(q), pack2<F16>(ob[0], ob[1]), pack2<F16>(ob[2], ob[3]),
+                       pack2<F16>(ob[4], ob[5]), pack2<F16>(ob[6], ob[7]));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -309,10 +327,10 @@ LORA_DEV bool epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap
             oa[e] = a * co[e] - bv * si[e];
             ob[e] = bv * co[e] + a * si[e];
           }
-          st_shared_v4(ba + at(q), pack_bf16x2(oa[0], oa[1]), pack_bf16x2(oa[2], oa[3]),
-                       pack_bf16x2(oa[4], oa[5]), pack_bf16x2(oa[6], oa[7]));
-          st_shared_v4(bb + at(q), pack_bf16x2(ob[0], ob[1]), pack_bf16x2(ob[2], ob[3]),
-                       pack_bf16x2(ob[4], ob[5]), pack_bf16x2(ob[6], ob[7]));
+          st_shared_v4(ba + at(q), pack2<F16>(oa[0], oa[1]), pack2<F16>(oa[2], oa[3]),
+                       pack2<F16>(oa[4], oa[5]), pack2<F16>(oa[6], oa[7]));
+          st_shared_v4(bb + at(q), pack2<F16>(ob[0], ob[1]), pack2<F16>(ob[2], ob[3]),
+                       pack2<F16>(ob[4], ob[5]), pack2<F16>(ob[6], ob[7]));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -335,6 +353,7 @@ LORA_DEV bool epi_store_tile_tma(uint32_t t_acc, uint32_t buf, const CUtensorMap
 // fp32 to bf16, through the warp's two 2 KB staging buffers in turn and TMA
 // bulk stores at output column col0 + 32·chunk, row row0.  `nstore` counts
 // the warp's stores (it picks the buffer).
+template <bool F16>
 LORA_DEV void epi_store_swiglu(uint32_t t_acc, uint32_t buf, const GemmParams &p, int col0,
                                int row0, int ncols, int lane, uint32_t &nstore) {
   auto at = [&](int q) -> uint32_t {
@@ -347,10 +366,10 @@ LORA_DEV void epi_store_swiglu(uint32_t t_acc, uint32_t buf, const GemmParams &p
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      st_shared_v4(b + at(q), pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
-                   pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                   pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                   pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+      st_shared_v4(b + at(q), pack2<F16>(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                   pack2<F16>(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                   pack2<F16>(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                   pack2<F16>(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
@@ -383,7 +402,7 @@ LORA_DEV void epi_store_swiglu(uint32_t t_acc, uint32_t buf, const GemmParams &p
 // the s·v operand region `sv` [FV/64 atoms][128 rows x 128 B] in the
 // 128-byte-swizzled K-major layout the MMA reads.  Columns from nv on are
 // written as zeros (the rank K-blocks read whole 64-column atoms).
-template <int FV>
+template <int FV, bool F16>
 LORA_DEV void stage_sv(uint32_t t_v, uint32_t sv, int row, int nv, float scale) {
 #pragma unroll 1
   for (int c = 0; c < FV / 32; ++c) {
@@ -400,10 +419,10 @@ LORA_DEV void stage_sv(uint32_t t_v, uint32_t sv, int row, int nv, float scale) 
     for (int q = 0; q < 4; ++q) {
       const uint32_t chunk = (uint32_t)((c & 1) * 4 + q);
       st_shared_v4(rowp + ((chunk ^ ((uint32_t)row & 7u)) << 4),
-                   pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1])),
-                   pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
-                   pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
-                   pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+                   pack2<F16>(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1])),
+                   pack2<F16>(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
+                   pack2<F16>(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
+                   pack2<F16>(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
     }
   }
 }

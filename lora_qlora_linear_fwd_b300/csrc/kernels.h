@@ -65,8 +65,8 @@ inline int current_device_sms() {
 struct GemmGroup {
   CUtensorMap tm_w;
   CUtensorMap tm_b;
-  CUtensorMap tm_out;  // out [M, ncols] bf16: box 32 x 32, 64-byte swizzle
-  __nv_bfloat16 *out;
+  CUtensorMap tm_out;  // out [M, ncols] 16-bit: box 32 x 32, 64-byte swizzle
+  uint16_t *out;       // raw 16-bit words (bf16 or fp16, the kernel's type)
   const __nv_bfloat16 *absmax;
   int ncols;       // output columns of this group (n in FWD, k in DX)
   int n_tiles;     // ceil(ncols / 256)
@@ -92,6 +92,14 @@ struct GemmParams {
   Schedule sched;
   int accumulate;        // DX: out += acc_scale·result instead of overwrite
   float acc_scale;
+  // DX read-modify-write of the bf16 kernel under LoRA dropout: the added
+  // result is masked by the dropout keep bits of the output element
+  // (philox.cuh; element index row·drop_ld + column) and scaled by drop_scale
+  int dropout;
+  uint32_t drop_thresh;
+  int drop_ld;
+  float drop_scale;
+  uint64_t drop_seed, drop_offset;
   // SwiGLU pair (FWD): n-tile t covers output columns [128t, 128t + 128);
   // CTA c of a pair stages the rows of grp[c] (0: gate, 1: up), so a
   // tile's accumulator holds g in columns [0, 128) and u in [128, 256).
@@ -161,11 +169,25 @@ cudaError_t launch_pdl(const char *name, void (*kern)(KArgs...), dim3 grid, dim3
 
 // Two-SM (CTA pair) fused GEMM: (256·mb) x 256 tiles over `pairs` persistent
 // pairs; p.sched counts tiles of mb m-blocks.  mb = 2 exists for NF4
-// weights; fv = 64 / 128 (the bf16 forward with the down-projection formed in
-// the GEMM, v up to fv columns wide) needs p.sched.contiguous.
-cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int mb, int fv,
-                             int pairs, cudaStream_t st);
-int gemm_pair_capacity(int mode, bool rope, bool nf4, int mb, int fv);  // max co-resident pairs
+// weights; fv = 64 / 128 (the 16-bit-W forward with the down-projection
+// formed in the GEMM, v up to fv columns wide) needs p.sched.contiguous.
+// F16: the 16-bit operands and outputs are fp16 (else bf16).
+template <bool F16>
+cudaError_t launch_gemm_pair_t(const GemmParams &p, int mode, bool rope, bool nf4, int mb, int fv,
+                               int pairs, cudaStream_t st);
+template <bool F16>
+int gemm_pair_capacity_t(int mode, bool rope, bool nf4, int mb, int fv);
+
+inline cudaError_t launch_gemm_pair(const GemmParams &p, int mode, bool rope, bool nf4, int mb,
+                                    int fv, int pairs, bool f16, cudaStream_t st) {
+  return f16 ? launch_gemm_pair_t<true>(p, mode, rope, nf4, mb, fv, pairs, st)
+             : launch_gemm_pair_t<false>(p, mode, rope, nf4, mb, fv, pairs, st);
+}
+// max co-resident pairs (the same for both element types: one pair per two
+// SMs, bounded by shared memory)
+inline int gemm_pair_capacity(int mode, bool rope, bool nf4, int mb, int fv) {
+  return gemm_pair_capacity_t<false>(mode, rope, nf4, mb, fv);
+}
 
 // Skinny rank-r products on the tensor cores:
 //   KMAJOR  (v, u):  g[t][j] = Σ_c P[t,c]·Q[j,c]            P = x or dY, Q = A or Bᵀ
@@ -199,9 +221,9 @@ struct SkinnyProblem {
   int q_rows1;           // KMAJOR: rows taken from tm_q when Q comes from two tensors, else 0
   float *out_f32;
   float *out_f32b;
-  __nv_bfloat16 *out_hi;
-  __nv_bfloat16 *out_lo;
-  __nv_bfloat16 *out_bf16;
+  uint16_t *out_hi;  // 16-bit words (bf16 or fp16, the kernel's type)
+  uint16_t *out_lo;
+  uint16_t *out_bf16;
   int ld_t;              // leading dimension of the kOutVt output
   int ld_row;            // leading dimension of the kOutRowBf16 output
   int out_kind;
@@ -228,41 +250,63 @@ struct SkinnyParams {
   uint32_t *status;
 };
 
-cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st);
+// f16: the 16-bit operands (P, Q) and outputs (hi/lo, kOutRowBf16) are fp16.
+cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, bool f16,
+                                  cudaStream_t st);
 // Largest `split` the cluster kernel supports for (mn_major, rp) (its
 // epilogue buffers must fit in its pipeline ring).
 int skinny_max_split(bool mn_major, int rp);
 // Scratch of one stream-K launch: flags, then partials (256-byte aligned).
 size_t skinny_scratch_bytes(int rp);
-cudaError_t launch_skinny_sk(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st);
+cudaError_t launch_skinny_sk(const SkinnyParams &p, bool mn_major, int rp, bool f16,
+                             cudaStream_t st);
 
 // Elementwise / small helpers.
 // Backward set-up (one launch): inverse RoPE of dy1|dy2 into dy_out (when
 // dy1 is set) or the SwiGLU backward [dg | du] into dy_out (when sw_dh is
 // set), A_out = [A1; A2] (nproj == 2), Bt = diag(B1, B2)ᵀ.
 struct BwdPrep {
-  const __nv_bfloat16 *dy1, *dy2;   // [M, n1], [M, n2]; dy1 null: no rotation
+  const uint16_t *dy1, *dy2;   // [M, n1], [M, n2]; dy1 null: no rotation
   // SwiGLU (sw_dh set, n1 == n2 == n): dy_out = [dg | du] from the incoming
   // dh and the saved gate / up outputs g, u [M, n]
-  const __nv_bfloat16 *sw_dh, *sw_g, *sw_u;
-  __nv_bfloat16 *dy_out;            // [M, n1 + n2]
+  const uint16_t *sw_dh, *sw_g, *sw_u;
+  uint16_t *dy_out;            // [M, n1 + n2]
   const int32_t *pos;
   const float *cos_sin;
   int max_pos;
   uint32_t *status;
   int M, n1, n2, k, r, nproj;       // n2 = 0 for one projection
-  const __nv_bfloat16 *A1, *A2;     // [r, k] each
-  __nv_bfloat16 *A_out;             // [2r, k]
-  const __nv_bfloat16 *B1, *B2;     // [n1, r], [n2, r]
-  __nv_bfloat16 *Bt;                // [nproj·r, n1 + n2]
+  const uint16_t *A1, *A2;     // [r, k] each
+  uint16_t *A_out;                  // [2r, k]
+  const uint16_t *B1, *B2;     // [n1, r], [n2, r]
+  uint16_t *Bt;                     // [nproj·r, n1 + n2]
 };
-cudaError_t launch_bwd_prep(const BwdPrep &p, cudaStream_t st);
+cudaError_t launch_bwd_prep(const BwdPrep &p, bool f16, cudaStream_t st);
 cudaError_t launch_rope_cache(float *cos_sin, int max_pos, int head_dim, double theta,
                               cudaStream_t st);
-cudaError_t launch_nf4_dequant(const uint8_t *codes, const __nv_bfloat16 *absmax,
-                               __nv_bfloat16 *w, int n, int k, cudaStream_t st);
-cudaError_t launch_nf4_quantize(const __nv_bfloat16 *w, uint8_t *codes, __nv_bfloat16 *absmax,
-                                int n, int k, cudaStream_t st);
+// LoRA dropout on x [M, k]: out = x ⊙ keep / q (keep per philox.cuh).
+cudaError_t launch_dropout_x(const uint16_t *x, uint16_t *out, int M, int k, uint64_t seed,
+                             uint64_t offset, uint32_t thresh, float inv_q, bool f16,
+                             cudaStream_t st);
+// Block scales of an NF4 weight [n, k] (nb = n·k/64 blocks of 64): bf16
+// absmax [nb] (dq_scale null), or double-quantised (nf4_levels.cuh): E4M3
+// codes [nb] in `absmax`, fp32 scale per 256 blocks, one fp32 offset.
+struct Nf4Scales {
+  const void *absmax;
+  const float *dq_scale;
+  const float *dq_offset;
+};
+// W [n, k] in the 16-bit type (f16: fp16, else bf16) from codes and scales.
+cudaError_t launch_nf4_dequant(const uint8_t *codes, const Nf4Scales &sc, uint16_t *w, int n,
+                               int k, bool f16, cudaStream_t st);
+// Double-quantised scales decoded to bf16 absmax [nb] (nb % 8 == 0).
+cudaError_t launch_nf4_dq_expand(const Nf4Scales &sc, uint16_t *absmax_out, size_t nb,
+                                 cudaStream_t st);
+// Quantise W [n, k] (16-bit type per f16): codes and bf16 absmax, or with
+// dq_scale set, E4M3 scale codes in `absmax`, dq_scale [ceil(nb/256)] and
+// *dq_offset (three launches).
+cudaError_t launch_nf4_quantize(const uint16_t *w, uint8_t *codes, void *absmax, float *dq_scale,
+                                float *dq_offset, int n, int k, bool f16, cudaStream_t st);
 
 // Argument checks of lora_linear_bwd other than the workspace (shape limits,
 // weight descriptor, pointer alignment, finite alpha), shared with

@@ -7,14 +7,15 @@
 // must never enter the driver's allocator (which can synchronise the device
 // and stall every stream).  This entry point takes the same inputs and
 // outputs as lora_linear_bwd but no workspace: its scratch (the transposed B,
-// the bf16 hi/lo parts of uᵀ and vᵀ, the rank-pass flags and parked
+// the 16-bit hi/lo parts of uᵀ and vᵀ, the rank-pass flags and parked
 // partials, and the device status word) lives in one fixed array in the
 // library's own device memory, declared below.
 //
 // Properties a caller must know:
 //   * The array holds kNoAllocScratchBytes (32 MiB) on every GPU that loads
 //     this library, from module load until the process exits.
-//   * Shapes whose scratch need (lora_workspace_size(LORA_OP_BWD, ...))
+//   * Shapes whose scratch need (lora_workspace_size(LORA_OP_BWD, ...), with
+//     LORA_OP_FLAG_DQ for double-quantised NF4 scales)
 //     exceeds that size are rejected with LORA_ERR_WORKSPACE before anything
 //     is launched.
 //   * The first call on each device looks up the array's device address
@@ -78,7 +79,8 @@ extern "C" lora_status_t lora_linear_bwd_noalloc(const void *x, lora_weight_t W,
   // reject enqueues nothing (not even the status-word reset below)
   lora_status_t s = lora::check_bwd_args(x, W, A, B, dy, dx, dA, dB, M, k, n, r, alpha);
   if (s != LORA_OK) return s;
-  const size_t need = lora_workspace_size(LORA_OP_BWD, M, k, n, r);
+  const int dq = (W.type == LORA_WEIGHT_NF4 && W.absmax_scale) ? LORA_OP_FLAG_DQ : 0;
+  const size_t need = lora_workspace_size(LORA_OP_BWD | dq, M, k, n, r);
   if (need == 0) return LORA_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return LORA_ERR_WORKSPACE;
   if ((s = lora::check_current_device()) != LORA_OK) return s;

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #define LORA_DEV __device__ __forceinline__
 
@@ -160,14 +161,19 @@ LORA_DEV void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t
       : "memory");
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
-//   15 A major (1 = MN-major), 16 B major, 17-22 N>>3, 24-28 M>>4.
+// Instruction descriptor for kind::f16 with 16-bit A/B (bf16, or fp16 when
+// f16) and fp32 D.
+//   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16, 1 = bf16), 10-12 B
+//   format, 15 A major (1 = MN-major), 16 B major, 17-22 N>>3, 24-28 M>>4.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                  bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_major,
                                                        bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+  return make_idesc(M, N, a_mn_major, b_mn_major, false);
 }
 
 // Shared-memory matrix descriptor.
@@ -395,6 +401,46 @@ LORA_DEV uint32_t swz_offset(uint32_t row, uint32_t chunk, uint32_t row_bytes) {
 LORA_DEV uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// The 16-bit floating element type of a call's tensors: bf16 (F16 false) or
+// IEEE fp16.  Conversions from fp32 round to nearest even.
+template <bool F16>
+LORA_DEV uint32_t pack2(float lo, float hi) {
+  if constexpr (F16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  } else {
+    return pack_bf16x2(lo, hi);
+  }
+}
+template <bool F16>
+LORA_DEV float2 unpack2(uint32_t w) {
+  if constexpr (F16) {
+    const __half2 h = *reinterpret_cast<const __half2 *>(&w);
+    return __half22float2(h);
+  } else {
+    const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+    return __bfloat1622float2(h);
+  }
+}
+template <bool F16>
+LORA_DEV uint16_t to16(float f) {
+  if constexpr (F16) {
+    const __half h = __float2half_rn(f);
+    return *reinterpret_cast<const uint16_t *>(&h);
+  } else {
+    const __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<const uint16_t *>(&h);
+  }
+}
+template <bool F16>
+LORA_DEV float from16(uint16_t v) {
+  if constexpr (F16) {
+    return __half2float(*reinterpret_cast<const __half *>(&v));
+  } else {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(&v));
+  }
 }
 
 LORA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {

@@ -57,6 +57,7 @@ LORA_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 // Copy-out of one CTA's column block [col0, col0 + cw) of row tile rt from
 // the staging buffers, by the 128 epilogue threads (e = 0..127).  Every
 // warp-wide store covers contiguous runs of 256 to 512 bytes.
+template <bool F16>
 LORA_DEV void skinny_copy_out(const SkinnyProblem &P, int rt, int col0, int cw,
                               const float *stage_t, const float *stage_r, int e) {
   const int cols = P.nproj * P.r;  // valid rank columns
@@ -72,14 +73,14 @@ LORA_DEV void skinny_copy_out(const SkinnyProblem &P, int rt, int col0, int cw,
       const float f[4] = {t.x, t.y, t.z, t.w};
       const int jg = col0 + j;
       if (P.out_kind & kOutVt) {
-        __nv_bfloat16 hi[4], lo[4];
+        uint16_t hi[4], lo[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          hi[q] = __float2bfloat16_rn(f[q]);
-          lo[q] = __float2bfloat16_rn(f[q] - __bfloat162float(hi[q]));
+          hi[q] = to16<F16>(f[q]);
+          lo[q] = to16<F16>(f[q] - from16<F16>(hi[q]));
         }
-        __nv_bfloat16 *dh = P.out_hi + (size_t)jg * P.ld_t + orow;
-        __nv_bfloat16 *dl = P.out_lo + (size_t)jg * P.ld_t + orow;
+        uint16_t *dh = P.out_hi + (size_t)jg * P.ld_t + orow;
+        uint16_t *dl = P.out_lo + (size_t)jg * P.ld_t + orow;
         if (full) {
           *reinterpret_cast<uint2 *>(dh) = *reinterpret_cast<const uint2 *>(hi);
           *reinterpret_cast<uint2 *>(dl) = *reinterpret_cast<const uint2 *>(lo);
@@ -113,18 +114,18 @@ LORA_DEV void skinny_copy_out(const SkinnyProblem &P, int rt, int col0, int cw,
       const float *src = stage_r + rr * (cw + 4) + c;
       const float4 a = *reinterpret_cast<const float4 *>(src);
       const float4 b = *reinterpret_cast<const float4 *>(src + 4);
-      __nv_bfloat16 *dst = P.out_bf16 + (size_t)orow * P.ld_row + col0 + c;
+      uint16_t *dst = P.out_bf16 + (size_t)orow * P.ld_row + col0 + c;
       if (col0 + c + 8 <= cols) {
         uint4 o;
-        o.x = pack_bf16x2(a.x * P.scale, a.y * P.scale);
-        o.y = pack_bf16x2(a.z * P.scale, a.w * P.scale);
-        o.z = pack_bf16x2(b.x * P.scale, b.y * P.scale);
-        o.w = pack_bf16x2(b.z * P.scale, b.w * P.scale);
+        o.x = pack2<F16>(a.x * P.scale, a.y * P.scale);
+        o.y = pack2<F16>(a.z * P.scale, a.w * P.scale);
+        o.z = pack2<F16>(b.x * P.scale, b.y * P.scale);
+        o.w = pack2<F16>(b.z * P.scale, b.w * P.scale);
         *reinterpret_cast<uint4 *>(dst) = o;
       } else {
         const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         for (int q = 0; q < 8; ++q)
-          if (col0 + c + q < cols) dst[q] = __float2bfloat16_rn(f[q] * P.scale);
+          if (col0 + c + q < cols) dst[q] = to16<F16>(f[q] * P.scale);
       }
     }
   }
@@ -156,7 +157,7 @@ LORA_DEV void skinny_copy_out(const SkinnyProblem &P, int rt, int col0, int cw,
   }
 }
 
-template <bool MN, int RP>
+template <bool MN, int RP, bool F16>
 __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_constant__ SkinnyParams p) {
   using L = SkinnySmem<MN, RP>;
   static_assert(SkinnyEpi(RP, 1).bytes <= L::OFF_MISC, "epilogue buffers fit in the ring");
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(128, RP, MN, false);
+      constexpr uint32_t idesc = make_idesc(128, RP, MN, false, F16);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   }
   if (epi) {
     epi_bar();
-    if (acc_ok) skinny_copy_out(P, rt, srank * CW, CW, stage_t, stage_r, threadIdx.x - 64);
+    if (acc_ok) skinny_copy_out<F16>(P, rt, srank * CW, CW, stage_t, stage_r, threadIdx.x - 64);
   }
   tc_fence_before();
   __syncthreads();
@@ -379,16 +380,18 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   }
 }
 
-template <bool MN, int RP>
+template <bool MN, int RP, bool F16>
 static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
   using L = SkinnySmem<MN, RP>;
-  auto kern = lora_skinny_kernel<MN, RP>;
+  auto kern = lora_skinny_kernel<MN, RP, F16>;
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
   if (e != cudaSuccess) return e;
   int tiles = 0;
   for (int q = 0; q < p.num_problems; ++q) tiles += p.pr[q].row_tiles;
-  return launch_pdl(MN ? "lora_skinny_kernel<mn_major>" : "lora_skinny_kernel<k_major>", kern,
+  const char *name = MN ? (F16 ? "lora_skinny_kernel<mn_major,f16>" : "lora_skinny_kernel<mn_major>")
+                        : (F16 ? "lora_skinny_kernel<k_major,f16>" : "lora_skinny_kernel<k_major>");
+  return launch_pdl(name, kern,
                     dim3((unsigned)(tiles * p.split)), dim3(192), L::TOTAL, st,
                     (unsigned)p.split, p);
 }
@@ -411,16 +414,24 @@ int skinny_max_split(bool mn_major, int rp) {
   return 1;
 }
 
-cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st) {
-  if (p.split != 1 && p.split != 2 && p.split != 4 && p.split != 8) return cudaErrorInvalidValue;
-  if (p.split > skinny_max_split(mn_major, rp)) return cudaErrorInvalidValue;
+template <bool F16>
+static cudaError_t launch_skinny_cluster_t(const SkinnyParams &p, bool mn_major, int rp,
+                                           cudaStream_t st) {
   switch (rp) {
-    case 16: return mn_major ? launch_skinny_t<true, 16>(p, st) : launch_skinny_t<false, 16>(p, st);
-    case 32: return mn_major ? launch_skinny_t<true, 32>(p, st) : launch_skinny_t<false, 32>(p, st);
-    case 64: return mn_major ? launch_skinny_t<true, 64>(p, st) : launch_skinny_t<false, 64>(p, st);
-    case 128: return mn_major ? launch_skinny_t<true, 128>(p, st) : launch_skinny_t<false, 128>(p, st);
+    case 16: return mn_major ? launch_skinny_t<true, 16, F16>(p, st) : launch_skinny_t<false, 16, F16>(p, st);
+    case 32: return mn_major ? launch_skinny_t<true, 32, F16>(p, st) : launch_skinny_t<false, 32, F16>(p, st);
+    case 64: return mn_major ? launch_skinny_t<true, 64, F16>(p, st) : launch_skinny_t<false, 64, F16>(p, st);
+    case 128: return mn_major ? launch_skinny_t<true, 128, F16>(p, st) : launch_skinny_t<false, 128, F16>(p, st);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, bool f16,
+                                  cudaStream_t st) {
+  if (p.split != 1 && p.split != 2 && p.split != 4 && p.split != 8) return cudaErrorInvalidValue;
+  if (p.split > skinny_max_split(mn_major, rp)) return cudaErrorInvalidValue;
+  return f16 ? launch_skinny_cluster_t<true>(p, mn_major, rp, st)
+             : launch_skinny_cluster_t<false>(p, mn_major, rp, st);
 }
 
 }  // namespace lora

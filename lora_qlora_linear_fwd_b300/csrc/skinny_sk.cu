@@ -104,6 +104,7 @@ LORA_DEV long long range_begin(const SkinnyParams &p, int cta) {
 // values, unscaled).  Transposed kinds: lanes hold consecutive rows, so
 // each column is one contiguous run per warp; row-major kinds: each thread
 // stores its row's 16 columns in 16-byte pieces.
+template <bool F16>
 LORA_DEV void skinny_store16(const SkinnyProblem &P, int rt, int row, int j0, const float (&v)[16]) {
   const int grow = rt * 128 + row;
   if (grow >= P.rows) return;
@@ -111,8 +112,8 @@ LORA_DEV void skinny_store16(const SkinnyProblem &P, int rt, int row, int j0, co
   if (P.out_kind & kOutVt) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v[j]);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(v[j] - __bfloat162float(hi));
+      const uint16_t hi = to16<F16>(v[j]);
+      const uint16_t lo = to16<F16>(v[j] - from16<F16>(hi));
       P.out_hi[(size_t)(j0 + j) * P.ld_t + grow] = hi;
       P.out_lo[(size_t)(j0 + j) * P.ld_t + grow] = lo;
     }
@@ -128,17 +129,17 @@ LORA_DEV void skinny_store16(const SkinnyProblem &P, int rt, int row, int j0, co
     }
   }
   if (P.out_kind & kOutRowBf16) {
-    __nv_bfloat16 *dst = P.out_bf16 + (size_t)grow * P.ld_row + j0;
+    uint16_t *dst = P.out_bf16 + (size_t)grow * P.ld_row + j0;
     if (j0 + 16 <= cols) {
       uint32_t w[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) w[q] = pack_bf16x2(v[2 * q] * P.scale, v[2 * q + 1] * P.scale);
+      for (int q = 0; q < 8; ++q) w[q] = pack2<F16>(v[2 * q] * P.scale, v[2 * q + 1] * P.scale);
       reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
       reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
     } else {
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        if (j0 + j < cols) dst[j] = __float2bfloat16_rn(v[j] * P.scale);
+        if (j0 + j < cols) dst[j] = to16<F16>(v[j] * P.scale);
     }
   }
   if (P.out_kind & kOutRow) {
@@ -161,7 +162,7 @@ LORA_DEV void skinny_store16(const SkinnyProblem &P, int rt, int row, int j0, co
   }
 }
 
-template <bool MN, int RP>
+template <bool MN, int RP, bool F16>
 __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_constant__ SkinnyParams p) {
   using L = SkSmem<MN, RP>;
   constexpr int STAGES = L::STAGES;
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(128, RP, MN, false);
+      constexpr uint32_t idesc = make_idesc(128, RP, MN, false, F16);
       int stage = 0;
       uint32_t phase = 0;
       int k = 0;  // segments issued: accumulator k & 1
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
                 for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (c * 16 + j) * 128);
               }
             }
-            skinny_store16(P, sg.rt, row, c * 16, v);
+            skinny_store16<F16>(P, sg.rt, row, c * 16, v);
           }
         }
       }
@@ -421,14 +422,17 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
   }
 }
 
-template <bool MN, int RP>
+template <bool MN, int RP, bool F16>
 static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
   using L = SkSmem<MN, RP>;
-  auto kern = lora_skinny_sk_kernel<MN, RP>;
+  auto kern = lora_skinny_sk_kernel<MN, RP, F16>;
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
   if (e != cudaSuccess) return e;
-  return launch_pdl(MN ? "lora_skinny_sk_kernel<mn_major>" : "lora_skinny_sk_kernel<k_major>", kern,
+  const char *name =
+      MN ? (F16 ? "lora_skinny_sk_kernel<mn_major,f16>" : "lora_skinny_sk_kernel<mn_major>")
+         : (F16 ? "lora_skinny_sk_kernel<k_major,f16>" : "lora_skinny_sk_kernel<k_major>");
+  return launch_pdl(name, kern,
                     dim3((unsigned)p.ctas), dim3(192), L::TOTAL, st, 0u, p);
 }
 
@@ -438,17 +442,25 @@ size_t skinny_scratch_bytes(int rp) {
   return (((size_t)kSkinnyMaxCtas * 8 + 255) & ~(size_t)255) + (size_t)kSkinnyMaxCtas * rp * 128 * 4;
 }
 
-cudaError_t launch_skinny_sk(const SkinnyParams &p, bool mn_major, int rp, cudaStream_t st) {
+template <bool F16>
+static cudaError_t launch_skinny_sk_t(const SkinnyParams &p, bool mn_major, int rp,
+                                      cudaStream_t st) {
   using namespace sk;
-  if (p.ctas < 1 || p.ctas > kSkinnyMaxCtas || p.units < p.ctas) return cudaErrorInvalidValue;
   switch (rp) {
-    case 16: return mn_major ? launch_skinny_t<true, 16>(p, st) : launch_skinny_t<false, 16>(p, st);
-    case 32: return mn_major ? launch_skinny_t<true, 32>(p, st) : launch_skinny_t<false, 32>(p, st);
-    case 64: return mn_major ? launch_skinny_t<true, 64>(p, st) : launch_skinny_t<false, 64>(p, st);
+    case 16: return mn_major ? launch_skinny_t<true, 16, F16>(p, st) : launch_skinny_t<false, 16, F16>(p, st);
+    case 32: return mn_major ? launch_skinny_t<true, 32, F16>(p, st) : launch_skinny_t<false, 32, F16>(p, st);
+    case 64: return mn_major ? launch_skinny_t<true, 64, F16>(p, st) : launch_skinny_t<false, 64, F16>(p, st);
     case 128:
-      return mn_major ? launch_skinny_t<true, 128>(p, st) : launch_skinny_t<false, 128>(p, st);
+      return mn_major ? launch_skinny_t<true, 128, F16>(p, st) : launch_skinny_t<false, 128, F16>(p, st);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_skinny_sk(const SkinnyParams &p, bool mn_major, int rp, bool f16,
+                             cudaStream_t st) {
+  if (p.ctas < 1 || p.ctas > kSkinnyMaxCtas || p.units < p.ctas) return cudaErrorInvalidValue;
+  return f16 ? launch_skinny_sk_t<true>(p, mn_major, rp, st)
+             : launch_skinny_sk_t<false>(p, mn_major, rp, st);
 }
 
 }  // namespace lora

@@ -37,7 +37,7 @@ def test_nf4_dequant_parity(n, k):
     c = cuda(torch.from_numpy(codes))
     a = cuda(torch.from_numpy(absmax.astype(np.float32)).to(torch.bfloat16))
     out = torch.empty(n, k, dtype=torch.bfloat16, device="cuda")
-    L.nf4_dequant(c, a, out)
+    L.nf4_dequant(L.nf4_weight(c, a), out)
     torch.cuda.synchronize()
     want = ref.nf4_dequant(codes, absmax)
     got = np64(out)
@@ -53,7 +53,7 @@ def test_nf4_quantize_parity(n, k):
     codes_ref, absmax_ref = ref.nf4_quantize(np64(W), decision="fp32")
     codes = torch.empty(n, k // 2, dtype=torch.uint8, device="cuda")
     absmax = torch.empty(n, k // 64, dtype=torch.bfloat16, device="cuda")
-    L.nf4_quantize(cuda(W), codes, absmax)
+    L.nf4_quantize(cuda(W), L.nf4_weight(codes, absmax))
     torch.cuda.synchronize()
     np.testing.assert_array_equal(np64(absmax), absmax_ref)
     gi = ref.nf4_unpack(codes.cpu().numpy())

@@ -159,3 +159,84 @@ def test_bf16_forward_launches(M, k, n, r, fused):
         assert names[1] == "lora_gemm_pair_kernel<fwd,bf16>", names
     want = ref.lora_fwd(np64(d["x"]), np64(d["W"]), np64(d["A"]), np64(d["B"]), ALPHA)
     assert rel_err(np64(y), want) <= TOL_BF16
+
+
+def _nf4_ws(op, M, k, n, r, stage_rows):
+    extra = sum(L.lora_nf4_stage_bytes(rows, k) for rows in stage_rows)
+    return L.workspace(op, M, k, n, r, extra=extra)
+
+
+@pytest.mark.parametrize("stage", [True, False])
+def test_nf4_linear_staged_in_bf16_when_the_workspace_has_room(stage):
+    """M >= 2048 and room past the workspace: W is dequantised once into it
+    and the bf16 kernels run; otherwise the codes are decoded in the GEMMs."""
+    M, k, n, r = 2048, 512, 768, 16
+    d = draw_projection(torch.Generator().manual_seed(67), M, k, n, r)
+    codes, absmax, c, a = _nf4(d["W"])
+    W = L.nf4_weight(c, a)
+    x, A, B, dy = cuda(d["x"]), cuda(d["A"]), cuda(d["B"]), cuda(d["dY"])
+    y = torch.empty(M, n, dtype=torch.bfloat16, device="cuda")
+    wsf = _nf4_ws(L.OP_FWD, M, k, n, r, [n] if stage else [])
+    fn = _profiled(lambda: L.lora_linear_fwd(x, W, A, B, y, ALPHA, wsf))
+    dx = torch.empty(M, k, dtype=torch.bfloat16, device="cuda")
+    dA = torch.empty(r, k, dtype=torch.float32, device="cuda")
+    dB = torch.empty(n, r, dtype=torch.float32, device="cuda")
+    wsb = _nf4_ws(L.OP_BWD, M, k, n, r, [n] if stage else [])
+    bn = _profiled(lambda: L.lora_linear_bwd(x, W, A, B, dy, dx, dA, dB, ALPHA, wsb))
+    torch.cuda.synchronize()
+    assert L.lora_read_device_status(wsf) == 0 and L.lora_read_device_status(wsb) == 0
+    if stage:
+        assert fn[0] == "nf4_dequant_kernel", fn
+        assert any(nm.startswith("lora_gemm_pair_kernel<fwd,bf16") for nm in fn), fn
+        assert bn[0] == "nf4_dequant_kernel" and "lora_gemm_pair_kernel<dx,bf16>" in bn, bn
+    else:
+        assert "nf4_dequant_kernel" not in fn + bn
+        assert any(nm.startswith("lora_gemm_pair_kernel<fwd,nf4") for nm in fn), fn
+    Wq = ref.nf4_dequant(codes, absmax)
+    x64, A64, B64 = np64(d["x"]), np64(d["A"]), np64(d["B"])
+    assert rel_err(np64(y), ref.lora_fwd(x64, Wq, A64, B64, ALPHA)) <= TOL_BF16
+    want = ref.lora_bwd(x64, Wq, A64, B64, np64(d["dY"]), ALPHA)
+    assert rel_err(np64(dx), want[0]) <= TOL_BF16
+    assert rel_err(np64(dA), want[1]) <= TOL_F32 and rel_err(np64(dB), want[2]) <= TOL_F32
+
+
+def test_nf4_qk_pair_staged_in_bf16():
+    """Both weights of the q/k pair staged (q then k) for the forward with
+    RoPE and the merged backward."""
+    from lora_inputs import draw_shared_x
+    M, hidden, r, theta = 2048, 256, 16, 500000.0
+    g = torch.Generator().manual_seed(68)
+    x = draw_shared_x(g, M, hidden)
+    q = draw_projection(g, M, hidden, 256, r, x=x)
+    k = draw_projection(g, M, hidden, 128, r, x=x)
+    (cq, aq, cqd, aqd), (ck, ak, ckd, akd) = _nf4(q["W"]), _nf4(k["W"])
+    Wq, Wk = L.nf4_weight(cqd, aqd), L.nf4_weight(ckd, akd)
+    pos = np.arange(M)
+    posd = cuda(torch.as_tensor(pos, dtype=torch.int32))
+    cache = torch.empty(M, 128, dtype=torch.float32, device="cuda")
+    L.lora_rope_cache_build(cache, M, 128, theta)
+    yq = torch.empty(M, 256, dtype=torch.bfloat16, device="cuda")
+    yk = torch.empty(M, 128, dtype=torch.bfloat16, device="cuda")
+    wsf = _nf4_ws(L.OP_QK_ROPE_FWD, M, hidden, 384, r, [256, 128])
+    dev = {t: cuda(v) for t, v in (("x", x), ("Aq", q["A"]), ("Bq", q["B"]), ("Ak", k["A"]),
+                                    ("Bk", k["B"]), ("dq", q["dY"]), ("dk", k["dY"]))}
+    fn = _profiled(lambda: L.lora_qk_rope_fwd(dev["x"], Wq, dev["Aq"], dev["Bq"], Wk, dev["Ak"],
+                                              dev["Bk"], yq, yk, ALPHA, theta, posd, cache, M,
+                                              wsf))
+    assert fn[:2] == ["nf4_dequant_kernel", "nf4_dequant_kernel"], fn
+    dx = torch.empty(M, hidden, dtype=torch.bfloat16, device="cuda")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    grads = [torch.empty(s, **f32) for s in ((r, hidden), (256, r), (r, hidden), (128, r))]
+    wsb = _nf4_ws(L.OP_QK_ROPE_BWD, M, hidden, 384, r, [256, 128])
+    L.lora_qk_rope_bwd(dev["x"], Wq, dev["Aq"], dev["Bq"], Wk, dev["Ak"], dev["Bk"], dev["dq"],
+                       dev["dk"], dx, *grads, ALPHA, theta, posd, cache, M, wsb)
+    torch.cuda.synchronize()
+    assert L.lora_read_device_status(wsf) == 0 and L.lora_read_device_status(wsb) == 0
+    Wq64, Wk64 = ref.nf4_dequant(cq, aq), ref.nf4_dequant(ck, ak)
+    P = (np64(x), Wq64, np64(q["A"]), np64(q["B"]), Wk64, np64(k["A"]), np64(k["B"]))
+    wq, wk = ref.qk_rope_fwd(*P, ALPHA, pos, theta)
+    assert rel_err(np64(yq), wq) <= TOL_BF16 and rel_err(np64(yk), wk) <= TOL_BF16
+    want = ref.qk_rope_bwd(*P, np64(q["dY"]), np64(k["dY"]), ALPHA, pos, theta)
+    assert rel_err(np64(dx), want[0]) <= TOL_BF16
+    for got, w in zip(grads, want[1:]):
+        assert rel_err(np64(got), w) <= TOL_F32

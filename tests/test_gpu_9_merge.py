@@ -76,7 +76,7 @@ def test_merge_nf4_requantises_the_merged_weight(n, k, r, sign):
     codes, absmax = ref.nf4_quantize(np64(d["W"]))
     c = cuda(torch.from_numpy(codes))
     a = cuda(torch.from_numpy(absmax.astype(np.float32)).to(torch.bfloat16))
-    L.lora_merge_nf4(c, a, cuda(d["A"]), cuda(d["B"]), alpha, sign=sign)
+    L.lora_merge(L.nf4_weight(c, a), cuda(d["A"]), cuda(d["B"]), alpha, sign=sign)
     torch.cuda.synchronize()
     got = ref.nf4_dequant(c.cpu().numpy(), np64(a))
     Wm = ref.nf4_dequant(codes, absmax)

@@ -574,10 +574,40 @@ def summarise_kernels(rows, steps, peaks, pool):
     return out, total / steps
 
 
+def flush_clean(flush):
+    """L2 flush for short kernels: write the 512 MiB buffer (evicts the
+    working set), then read half of it, so the dirty lines the write leaves
+    in L2 go back to HBM before the timed launch instead of during it."""
+    flush.zero_()
+    flush[: flush.numel() // 2].max()
+
+
+def launch_floor_us(dev, flush, steps=20):
+    """CUDA-event time of the smallest nf4_dequant launch (64 x 64): the
+    fixed launch-to-completion cost that a short launch cannot go below."""
+    import lora_qlora_linear_fwd_b300 as L
+    codes = torch.zeros(64, 32, dtype=torch.uint8, device=dev)
+    absmax = torch.ones(64, 1, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(64, 64, dtype=torch.bfloat16, device=dev)
+    Wq = L.nf4_weight(codes, absmax)
+    ts = []
+    for i in range(steps + 3):
+        flush_clean(flush)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        L.nf4_dequant(Wq, out)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            ts.append(a.elapsed_time(b))
+    return round(statistics.median(ts) * 1e3, 2)
+
+
 def run_nf4_dequant_shapes(shapes, dev, flush, steps, warmup, peak):
     """HBM throughput of ``nf4_dequant`` on weight shapes [(n, k)]: bytes =
     codes n·k/2 + absmax n·k/32 + bf16 output 2·n·k, CUDA-event time per call
-    with a 512 MiB L2 flush between calls (outside the events)."""
+    with an L2 flush between calls (flush_clean, outside the events)."""
     import lora_qlora_linear_fwd_b300 as L
     g = torch.Generator(device="cpu").manual_seed(0)
     rows = []
@@ -593,7 +623,7 @@ def run_nf4_dequant_shapes(shapes, dev, flush, steps, warmup, peak):
             L.nf4_dequant(Wq, out)
         ts = []
         for _ in range(steps):
-            flush.zero_()
+            flush_clean(flush)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()
@@ -749,12 +779,19 @@ def run_gpu(args, world, rank, local):
     # nf4_dequant on the headline's weight shapes
     if wl.nf4:
         shapes = sorted({(p.n, p.k) for p in wl.projections})
-        dq = run_nf4_dequant_shapes(shapes, dev, flush, 10, 3, peaks["hbm_gbs"])
+        dq = run_nf4_dequant_shapes(shapes, dev, flush, 20, 3, peaks["hbm_gbs"])
+        floor = launch_floor_us(dev, flush)
         for row in dq:
+            nbytes = row["GBps"] * row["us"] * 1e3
+            # the best a launch of these bytes can do: the launch floor plus
+            # the bytes at the measured HBM rate
+            best_us = floor + nbytes / (peaks["hbm_gbs"] * 1e3)
             hbm_lines.append({"kernel": "nf4_dequant_kernel", "shape": [row["n"], row["k"]],
                               "bound": "hbm", "gbs": row["GBps"], "us": row["us"],
                               "frac": row["frac_hbm"], "peak": peaks["hbm_gbs"],
-                              "frac_pool": round(row["GBps"] / pool["hbm_gbs"], 4)})
+                              "frac_pool": round(row["GBps"] / pool["hbm_gbs"], 4),
+                              "launch_floor_us": floor,
+                              "frac_of_floor_bound": round(best_us / row["us"], 3)})
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     e2e = run_e2e(rep, args, stream)

@@ -709,6 +709,99 @@ def nf4_fused_vs_unfused(name, proj, dev, flush, steps, warmup):
     return out
 
 
+def nf4_small_m_probe(wl, dev, flush, peak, ms=(16, 32, 64), steps=20):
+    """Supplementary probe: the fused NF4 forward at a few tokens per call,
+    where it is bound by the weight stream.  Per NF4 weight shape and M, the
+    CUDA-event time of lora_linear_fwd (codes decoded in the GEMM) and its
+    bytes: codes n·k/2 + absmax n·k/32 + x, y, A, B in bf16."""
+    import lora_qlora_linear_fwd_b300 as L
+    g = torch.Generator(device="cpu").manual_seed(0)
+    r, rows = wl.r, []
+    for n, k in sorted({(p.n, p.k) for p in wl.projections}):
+        W = (torch.randn(n, k, generator=g) / math.sqrt(k)).to(torch.bfloat16).to(dev)
+        codes = torch.empty(n, k // 2, dtype=torch.uint8, device=dev)
+        absmax = torch.empty(n, k // 64, dtype=torch.bfloat16, device=dev)
+        Wq = L.nf4_weight(codes, absmax)
+        L.nf4_quantize(W, Wq)
+        del W
+        A = (torch.rand(r, k, generator=g) * 2 - 1).mul(1 / math.sqrt(k)).to(torch.bfloat16).to(dev)
+        B = (torch.randn(n, r, generator=g) * math.sqrt(0.02)).to(torch.bfloat16).to(dev)
+        for M in ms:
+            x = torch.randn(M, k, generator=g).to(torch.bfloat16).to(dev)
+            y = torch.empty(M, n, dtype=torch.bfloat16, device=dev)
+            ws = L.workspace(L.OP_FWD, M, k, n, r, device=dev)
+            ts = []
+            for i in range(steps + 3):
+                flush_clean(flush)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+                L.lora_linear_fwd(x, Wq, A, B, y, wl.alpha, ws)
+                b.record()
+                torch.cuda.synchronize()
+                if i >= 3:
+                    ts.append(a.elapsed_time(b))
+            if L.lora_read_device_status(ws):
+                raise RuntimeError("device status after the small-M probe")
+            t = statistics.median(ts)
+            nbytes = n * k // 2 + n * k // 32 + 2 * (M * k + M * n + r * (k + n))
+            gbs = nbytes / (t * 1e-3) / 1e9
+            rows.append({"n": n, "k": k, "M": M, "us": round(t * 1e3, 2), "GBps": round(gbs, 1),
+                         "frac_hbm": round(gbs / peak, 3)})
+        del codes, absmax, Wq, A, B
+        torch.cuda.empty_cache()
+    return rows
+
+
+def torch_unfused_step(name, dev, flush, steps=10, warmup=3):
+    """Context, not a target: the same step as plain torch bf16 autograd
+    (cuBLAS), the shape of a PEFT LoRA layer: y = x·Wᵀ + s·(x·Aᵀ)·Bᵀ, then
+    backward from dY into x, A and B (W frozen).  For NF4 workloads the drawn
+    bf16 W stands in for the dequantised weight (same shape; no dequantise
+    is timed)."""
+    import torch.nn.functional as F
+    wl = WORKLOADS[name]
+    if wl.rope or wl.extra.get("swiglu"):
+        return None
+    data = draw_workload(name, seed=0)
+    s = wl.alpha / wl.r
+    projs = []
+    for p in wl.projections:
+        d = {k: v.to(dev) for k, v in data.pop(p.name).items()}
+        x = d["x"].requires_grad_(True)
+        A = d["A"].clone().requires_grad_(True)
+        B = d["B"].clone().requires_grad_(True)
+        projs.append((x, d["W"], A, B, d["dY"]))
+    del data
+
+    def step():
+        for x, W, A, B, dY in projs:
+            y = F.linear(x, W) + s * F.linear(F.linear(x, A), B)
+            y.backward(dY)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.median(ts)
+    del projs
+    torch.cuda.empty_cache()
+    return {"ms_per_step": round(ms, 4), "tokens_per_s": round(wl.M / (ms * 1e-3), 1),
+            "tflops": round(step_flops(wl, wl.M) / (ms * 1e-3) / 1e12, 1),
+            "what": "torch bf16 autograd per projection (F.linear, cuBLAS), unfused LoRA "
+                    "branch, W frozen (bf16 W for NF4 workloads, no dequantise timed); "
+                    f"median of {steps} steps, L2 flushed between steps"}
+
+
 def workload_line(rep, steps, warmup, flush, stream, peaks, pool):
     """Step time of one workload (used for the configurations beside the
     headline)."""
@@ -888,6 +981,8 @@ def run_gpu(args, world, rank, local):
             line["nf4_fused_vs_unfused"] = nf4_fused_vs_unfused(args.workload, "gate_proj", dev,
                                                                 flush, 10, 3)
             torch.cuda.empty_cache()
+            line["nf4_small_m_probe"] = nf4_small_m_probe(wl, dev, flush, peaks["hbm_gbs"])
+        line["torch_unfused_bf16"] = torch_unfused_step(args.workload, dev, flush)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_tokens, args.cpu_tokens_1core)
     return line

@@ -313,6 +313,7 @@ struct GemmOpts {
   float acc_scale = 1.0f;
   int act_cols = 0;
   int w_rows = 0;
+  int w_cols = 0;  // FWD: columns of a 16-bit W narrower than Kred (read as zeros past it)
   // FWD, bf16 W: form s·v = s·x·[a1; a2]ᵀ inside the GEMM (no rank pass, no
   // s·v in memory; sv unused).  a2 null: one projection.
   bool fused_v = false;
@@ -378,8 +379,9 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
     if (!dx) {
       const int n = ncols, k = o.Kred;
       const int bc = a.b_cols > 0 ? a.b_cols : o.rank_k;
-      if (!make_w_map(&G.tm_w, a.W, false, nf4, n, k) ||
-          !make_map(&G.tm_b, dt, 2, a.b, bc, n, (uint64_t)bc * 2, 64, 128, true))
+      if (!make_w_map(&G.tm_w, a.W, false, nf4, n, o.w_cols > 0 ? o.w_cols : k) ||
+          (o.rank_k > 0 &&
+           !make_map(&G.tm_b, dt, 2, a.b, bc, n, (uint64_t)bc * 2, 64, 128, true)))
         return LORA_ERR_CUDA;
       G.ld_absmax = k / 64;
       G.b_shift = a.b_shift;
@@ -544,7 +546,8 @@ unsigned long long next_epoch() {
 }
 
 lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, bool f16, uint32_t *status,
-                         void *scratch, cudaStream_t st) {
+                         void *scratch, cudaStream_t st, bool cluster_only = false,
+                         bool dec = false) {
   DeviceInfo di;
   lora_status_t s;
   if ((s = device_info(&di))) return s;
@@ -559,7 +562,7 @@ lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, bool f16, uint32_t *
   }
   if (units < 1) return LORA_ERR_INVALID_ARG;
   sp.status = status;
-  sp.split = pick_split(tiles, min_chunks, di.sms, skinny_max_split(mn, rp));
+  sp.split = pick_split(tiles, min_chunks, di.sms, skinny_max_split(mn, rp, dec));
   long long w_cluster = 0;  // chunks of the busiest CTA
   for (int q = 0; q < sp.num_problems; ++q)
     w_cluster = std::max<long long>(w_cluster, (sp.pr[q].chunks + sp.split - 1) / sp.split);
@@ -568,7 +571,8 @@ lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, bool f16, uint32_t *
   const int ctas = (int)std::max<long long>(
       1, std::min<long long>(std::min(di.sms, kSkinnyMaxCtas), units / 8));
   const long long w_sk = (units + ctas - 1) / ctas;
-  if (4 * w_sk > 3 * w_cluster) return cuda_status(launch_skinny_cluster(sp, mn, rp, f16, st));
+  if (cluster_only || 4 * w_sk > 3 * w_cluster)
+    return cuda_status(launch_skinny_cluster(sp, mn, rp, f16, st, dec));
   sp.units = units;
   sp.ctas = ctas;
   uint8_t *s8 = static_cast<uint8_t *>(scratch);
@@ -603,6 +607,89 @@ lora_status_t fwd_rank(const void *x, const void *A1, const void *A2, int M, int
   sp.num_problems = 1;
   return run_skinny(sp, false, rp, f16, status, static_cast<uint8_t *>(sv) + fwd_sv_bytes(M, rl),
                     st);
+}
+
+// Small-M forward: with at most kSmallM tokens a GEMM tile of 256 rows is
+// mostly empty and the n/256 tiles leave most SMs idle, so the forward runs
+// as a rank pass over the rows of W instead, in two launches:
+//   1. one rank-pass launch with two problems over the same x (the narrow
+//      operand, tokens padded to 64 or 128): yᵀ = W·xᵀ over the rows of W,
+//      and (s·v)ᵀ = s·A·xᵀ over the rows of A; the reduction over k split
+//      across the CTAs of a cluster, both written transposed (y [M, n],
+//      s·v [M, r]);
+//   2. y += (s·v)·Bᵀ: the GEMM with s·v as its activation (K = r) and B as
+//      its weight, adding to y in its epilogue.
+// Every SM streams a share of W in the first launch; the second touches only
+// y, s·v and B.
+constexpr int kSmallM = 128;
+
+// Whether a forward of M tokens takes the small-M form.  A dense W: always
+// at M <= kSmallM.  An NF4 W: the decode, about three integer instructions
+// per weight, bounds both forms, so the small-M form is taken only while the
+// GEMM's n/256 tiles leave CTA pairs idle (measured on B300 at M = 16:
+// Qwen1.5-32B down_proj 164 us against 350 us, q_proj 47 against 76,
+// k_proj 33 against 86; gate_proj, 107 tiles, 135 against 123).
+bool small_m_pays(int M, int n, bool nf4) {
+  if (M > kSmallM) return false;
+  if (!nf4) return true;
+  const int pairs = gemm_pair_capacity(kModeFwd, false, true, 1, 0);
+  return pairs > 0 && (n + 255) / 256 < pairs;
+}
+
+lora_status_t small_m_fwd(const void *x, const lora_weight_t &W, const void *A, const void *B,
+                          void *y, int M, int k, int n, int r, float scale, void *sv,
+                          uint32_t *status, bool f16, cudaStream_t st) {
+  lora_status_t s;
+  const CUtensorMapDataType dt = t16(f16);
+  // the token axis padded to 64 (or 128): narrower tiles would leave no room
+  // to split the reduction across a cluster (16-column blocks per CTA)
+  const int rp = M <= 64 ? 64 : 128;
+  SkinnyParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  SkinnyProblem &PW = sp.pr[0];
+  SkinnyProblem &PA = sp.pr[1];
+  const bool nf4 = W.type == LORA_WEIGHT_NF4;
+  if ((s = kmajor_problem(PW, W.w, n, k, x, nullptr, 0, M, rp, dt)) ||
+      (s = kmajor_problem(PA, A, r, k, x, nullptr, 0, M, rp, dt)))
+    return s;
+  if (nf4) {  // P from the 4-bit codes, decoded in the kernel
+    if (!make_map(&PW.tm_p, kU8, 1, W.w, k / 2, n, (uint64_t)k / 2, 32, 128, false))
+      return LORA_ERR_CUDA;
+    PW.nf4 = 1;
+    PW.absmax = static_cast<const __nv_bfloat16 *>(W.absmax);
+    PW.ld_absmax = k / 64;
+  }
+  PW.out_kind = PA.out_kind = kOutT16;
+  PW.out_bf16 = static_cast<uint16_t *>(y);
+  PW.ld_t = n;
+  PW.scale = 1.0f;
+  PA.out_bf16 = static_cast<uint16_t *>(sv);
+  PA.ld_t = r;
+  PA.scale = scale;
+  PW.r = PA.r = M;  // valid columns of the transposed outputs
+  PW.nproj = PA.nproj = 1;
+  sp.num_problems = 2;
+  if ((s = run_skinny(sp, false, rp, f16, status, nullptr, st, true, nf4))) return s;
+  lora_weight_t wb{};
+  wb.type = LORA_WEIGHT_DENSE;
+  wb.w = B;
+  wb.dtype = W.dtype;
+  GroupArgs ga{wb, nullptr, y, n, 0};
+  GemmOpts o;
+  o.mode = kModeFwd;
+  o.f16 = f16;
+  o.act = sv;
+  o.act_cols = r;
+  o.M = M;
+  o.Kred = 64;
+  o.w_cols = r;
+  o.ga = &ga;
+  o.ng = 1;
+  o.rank_k = 0;
+  o.accumulate = 1;
+  o.acc_scale = 1.0f;
+  o.status = status;
+  return run_gemm(o, st);
 }
 
 // ----------------------------------------------------------------- backward
@@ -957,6 +1044,8 @@ lora_status_t lora_linear_fwd(const void *x, lora_weight_t W, const void *A, con
   if ((s = prepare_nf4(&W, n, nullptr, 0, k, M, ws, ws_bytes, ws_base(LORA_OP_FWD, M, k, n, r),
                        need, st)))
     return s;
+  if (small_m_pays(M, n, W.type == LORA_WEIGHT_NF4))
+    return small_m_fwd(x, W, A, B, y, M, k, n, r, scale, sv, status, f16, st);
   // 16-bit W, one wave of tiles: one launch, s·x·Aᵀ formed in the GEMM;
   // otherwise a rank pass first
   const bool fused = W.type == LORA_WEIGHT_DENSE && fused_fwd_pays(M, (n + 255) / 256, r, false);

@@ -551,7 +551,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(NF4), 1
           break;
         }
         tc_fence_after();
-        if (DX && p.accumulate) {  // read-modify-write of the output: plain loads and stores
+        if ((DX || !ROPE) && p.accumulate) {  // read-modify-write of the output: plain loads and stores
           uint16_t *orow = G.out + (size_t)(row_ok ? grow : 0) * G.ncols + n0;
           if (!NF4 && p.dropout)   // the masked adapter term of dX under LoRA dropout
             epi_accumulate_tile<BN, F16, !NF4>(tmem + t_lane + acc * BN, orow, row_ok, ncols,

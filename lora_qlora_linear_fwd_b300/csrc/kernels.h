@@ -90,7 +90,7 @@ struct GemmParams {
   int kgroups;
   int ksplit;
   Schedule sched;
-  int accumulate;        // DX: out += acc_scale·result instead of overwrite
+  int accumulate;        // out += acc_scale·result instead of overwrite (DX; FWD without RoPE)
   float acc_scale;
   // DX read-modify-write of the bf16 kernel under LoRA dropout: the added
   // result is masked by the dropout keep bits of the output element
@@ -210,7 +210,9 @@ inline int gemm_pair_capacity(int mode, bool rope, bool nf4, int mb, int fv) {
 //                columns [r, 2r) go to out_f32b
 //   kOutRow:     out[o][j] = scale·g[o][j] fp32 (dB [n, r]); with nproj == 2
 //                rows >= split_row go to out_f32b from columns [r, 2r)
-enum SkinnyOut { kOutVt = 1, kOutRowBf16 = 2, kOutRowT = 4, kOutRow = 8 };
+//   kOutT16:     out_bf16[j][o] = scale·g[o][j], 16-bit, columns j < r only
+//                (the small-M forward's y [M, n] and s·v [M, r], ld_t = n or r)
+enum SkinnyOut { kOutVt = 1, kOutRowBf16 = 2, kOutRowT = 4, kOutRow = 8, kOutT16 = 16 };
 
 constexpr int kSkinnyMaxCtas = 160;  // scratch slots (the grid is at most one CTA per SM)
 
@@ -219,6 +221,11 @@ struct SkinnyProblem {
   CUtensorMap tm_q;      // Q (MNMAJOR: its hi part)
   CUtensorMap tm_q2;     // MNMAJOR: lo part; KMAJOR with q_rows1 > 0: Q rows [q_rows1, 2·q_rows1)
   int q_rows1;           // KMAJOR: rows taken from tm_q when Q comes from two tensors, else 0
+  // NF4 P (the decoding variant): tm_p maps the codes [rows, K/2] bytes
+  // (box 32 x 128), absmax the bf16 block scales [rows, ld_absmax]
+  int nf4;
+  const __nv_bfloat16 *absmax;
+  int ld_absmax;
   float *out_f32;
   float *out_f32b;
   uint16_t *out_hi;  // 16-bit words (bf16 or fp16, the kernel's type)
@@ -251,11 +258,13 @@ struct SkinnyParams {
 };
 
 // f16: the 16-bit operands (P, Q) and outputs (hi/lo, kOutRowBf16) are fp16.
+// dec: the NF4-decoding variant (KMAJOR, rp 64 or 128; problems with `nf4`
+// set stream codes through tm_p and absmax instead of P).
 cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, bool f16,
-                                  cudaStream_t st);
-// Largest `split` the cluster kernel supports for (mn_major, rp) (its
+                                  cudaStream_t st, bool dec = false);
+// Largest `split` the cluster kernel supports for (mn_major, rp, dec) (its
 // epilogue buffers must fit in its pipeline ring).
-int skinny_max_split(bool mn_major, int rp);
+int skinny_max_split(bool mn_major, int rp, bool dec = false);
 // Scratch of one stream-K launch: flags, then partials (256-byte aligned).
 size_t skinny_scratch_bytes(int rp);
 cudaError_t launch_skinny_sk(const SkinnyParams &p, bool mn_major, int rp, bool f16,

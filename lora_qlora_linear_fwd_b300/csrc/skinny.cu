@@ -14,18 +14,39 @@
 // mode the right-hand operand comes as bf16 hi + lo parts of an fp32 value
 // (about 2^-17 relative) and both are multiplied, keeping near-fp32
 // accuracy for dA and dB.
+//
+// DEC variant (KMAJOR, the small-M forward over the rows of an NF4 W): eight
+// more warps decode P from 4-bit codes.  A problem with `nf4` set streams its
+// codes [128 rows x 32 bytes] per chunk instead of P, through a deep ring of
+// (Q, codes) stages (the codes are a quarter of P's bytes, so many chunks are
+// in flight); each decode thread takes half a row (32 codes), looks them up
+// in a 16-entry table scaled by the block's absmax (fetched a few chunks
+// ahead by cp.async) and writes the 16-bit values, 128-byte swizzled, into a
+// short ring of P tiles that the MMA reads.  A problem without codes loads P
+// into that ring by TMA.
+#include "gemm_common.cuh"
 #include "kernels.h"
 
 namespace lora {
 
-template <bool MN, int RP>
+template <bool MN, int RP, bool DEC = false>
 struct SkinnySmem {
   static constexpr int P_BYTES = 128 * 128;  // [128 x 64] bf16 either way
   static constexpr int Q_BYTES = RP * 128;
-  static constexpr int STAGE_BYTES = P_BYTES + (MN ? 2 : 1) * Q_BYTES;
-  static constexpr int STAGES_FIT = (kSmemLimit - 4096) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
-  static constexpr int OFF_MISC = STAGES * STAGE_BYTES;
+  static constexpr int C_BYTES = DEC ? 128 * 32 : 0;  // NF4 codes of a P tile
+  static constexpr int AMAX_PRE = 8;                  // absmax prefetch distance (chunks)
+  static constexpr int DEC_THREADS = DEC ? 256 : 0;   // two per P row
+  static constexpr int AMAX_BYTES = DEC ? AMAX_PRE * DEC_THREADS * 4 : 0;
+  static constexpr int PST = DEC ? 4 : 0;             // DEC: ring of P tiles
+  // a TMA stage: P (not DEC) and Q (MN: its hi and lo parts), codes (DEC)
+  static constexpr int STAGE_BYTES = (DEC ? 0 : P_BYTES) + (MN ? 2 : 1) * Q_BYTES + C_BYTES;
+  static constexpr int STAGES_FIT =
+      (kSmemLimit - 4096 - AMAX_BYTES - PST * P_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES_MAX = DEC ? 16 : 10;
+  static constexpr int STAGES = STAGES_FIT > STAGES_MAX ? STAGES_MAX : STAGES_FIT;
+  static constexpr int OFF_PRING = STAGES * STAGE_BYTES;
+  static constexpr int OFF_AMAX = OFF_PRING + PST * P_BYTES;
+  static constexpr int OFF_MISC = OFF_AMAX + AMAX_BYTES;
   static constexpr int TOTAL = OFF_MISC + 512 + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 4, "pipeline depth");
@@ -65,7 +86,7 @@ LORA_DEV void skinny_copy_out(const SkinnyProblem &P, int rt, int col0, int cw,
   const int w = e >> 5, l = e & 31;
   // transposed outputs: warp w takes block columns j = w, w + 4, ...; lane l
   // takes rows [4l, 4l + 4) of the tile
-  if (P.out_kind & (kOutVt | kOutRowT)) {
+  if (P.out_kind & (kOutVt | kOutRowT | kOutT16)) {
     const int orow = row0 + 4 * l;
     const bool full = orow + 4 <= P.rows;
     for (int j = w; j < cw; j += 4) {
@@ -87,6 +108,17 @@ LORA_DEV void skinny_copy_out(const SkinnyProblem &P, int rt, int col0, int cw,
         } else {
           for (int q = 0; q < 4; ++q)
             if (orow + q < P.rows) dh[q] = hi[q], dl[q] = lo[q];
+        }
+      }
+      if ((P.out_kind & kOutT16) && jg < cols) {
+        uint16_t *dst = P.out_bf16 + (size_t)jg * P.ld_t + orow;
+        const uint32_t w0 = pack2<F16>(f[0] * P.scale, f[1] * P.scale);
+        const uint32_t w1 = pack2<F16>(f[2] * P.scale, f[3] * P.scale);
+        if (full) {
+          *reinterpret_cast<uint2 *>(dst) = make_uint2(w0, w1);
+        } else {
+          for (int q = 0; q < 4; ++q)
+            if (orow + q < P.rows) dst[q] = to16<F16>(f[q] * P.scale);
         }
       }
       if ((P.out_kind & kOutRowT) && jg < cols) {
@@ -157,10 +189,12 @@ LORA_DEV void skinny_copy_out(const SkinnyProblem &P, int rt, int col0, int cw,
   }
 }
 
-template <bool MN, int RP, bool F16>
-__global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_constant__ SkinnyParams p) {
-  using L = SkinnySmem<MN, RP>;
-  static_assert(SkinnyEpi(RP, 1).bytes <= L::OFF_MISC, "epilogue buffers fit in the ring");
+template <bool MN, int RP, bool F16, bool DEC>
+__global__ void __launch_bounds__(DEC ? 448 : 192, 1)
+    lora_skinny_kernel(const __grid_constant__ SkinnyParams p) {
+  using L = SkinnySmem<MN, RP, DEC>;
+  static_assert(!DEC || !MN, "NF4 decode: KMAJOR only");
+  static_assert(SkinnyEpi(RP, 1).bytes <= L::OFF_AMAX, "epilogue buffers fit in the ring");
   constexpr int STAGES = L::STAGES;
   constexpr uint32_t kTmemCols = RP >= 32 ? RP : 32;
   extern __shared__ uint8_t smem_raw[];
@@ -186,7 +220,19 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   const uint32_t bar_empty = bar_full + 8 * STAGES;
   const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
   const uint32_t bar_drain = bar_acc_full + 8;
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC + 8 * (2 * STAGES + 2));
+  constexpr int PST = L::PST;
+  const uint32_t bar_pfull = bar_drain + 8;      // [PST] DEC: P tile ready (eight decode warps)
+  const uint32_t bar_pempty = bar_pfull + 8 * PST;  // [PST] DEC: the MMA read the P tile
+  uint32_t *tmem_holder =
+      reinterpret_cast<uint32_t *>(smem + L::OFF_MISC + 8 * (2 * STAGES + 2 + 2 * PST));
+  // Q of TMA stage s; P of TMA stage s or (DEC) of P-ring slot ps
+  auto slot_q = [&](int st) {
+    return base + (uint32_t)st * L::STAGE_BYTES + (DEC ? 0u : (uint32_t)L::P_BYTES);
+  };
+  auto slot_p = [&](int st, int ps) {
+    return DEC ? base + L::OFF_PRING + (uint32_t)ps * L::P_BYTES
+               : base + (uint32_t)st * L::STAGE_BYTES;
+  };
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
   if (threadIdx.x == 0) {
@@ -196,6 +242,10 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_drain, 1);
+    for (int s = 0; s < PST; ++s) {
+      mbar_init(bar_pfull + 8 * s, 8);
+      mbar_init(bar_pempty + 8 * s, 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -217,12 +267,31 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;  // chunks issued: stage s took every STAGES-th from the s-th
+      int pslot = 0, pissued = 0;  // DEC, P by TMA: the P ring
+      uint32_t pphase = 0;
       for (int i = 0; i < n_chunks; ++i) {
         const int c = c_begin + (i + c_rot) % n_chunks;
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) break;
-        const uint32_t sp = base + stage * L::STAGE_BYTES;
-        const uint32_t sq = sp + L::P_BYTES;
+        const uint32_t sp = slot_p(stage, 0);
+        const uint32_t sq = slot_q(stage);
         const uint32_t fb = bar_full + 8 * stage;
+        if constexpr (DEC) {
+          if (P.nf4) {  // Q and the codes of the P tile (decoded by the decode warps)
+            mbar_arrive_expect_tx(fb, L::C_BYTES + L::Q_BYTES);
+            tma_load_2d(sq + L::Q_BYTES, &P.tm_p, fb, c * 32, rt * 128);
+            tma_load_2d(sq, &P.tm_q, fb, c * 64, 0);
+          } else {      // Q, and P straight into the P ring
+            if (!mbar_wait(bar_pempty + 8 * pslot, pphase ^ 1u, abort_flag, p.status)) break;
+            mbar_arrive_expect_tx(fb, L::P_BYTES + L::Q_BYTES);
+            tma_load_2d(slot_p(stage, pslot), &P.tm_p, fb, c * 64, rt * 128);
+            tma_load_2d(sq, &P.tm_q, fb, c * 64, 0);
+            ++pissued;
+            if (++pslot == PST) pslot = 0, pphase ^= 1u;
+          }
+          ++issued;
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+          continue;
+        }
         mbar_arrive_expect_tx(fb, L::STAGE_BYTES);
         if constexpr (MN) {
           // P [tokens, rows]: two boxes of [64 rows-of-output x 64 tokens]
@@ -249,6 +318,10 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
         const int fills = issued > s ? (issued - s + STAGES - 1) / STAGES : 0;
         if (fills > 0) mbar_wait_quiet(bar_empty + 8 * s, (uint32_t)((fills - 1) & 1), lim);
       }
+      for (int s = 0; s < PST; ++s) {
+        const int fills = pissued > s ? (pissued - s + PST - 1) / PST : 0;
+        if (fills > 0) mbar_wait_quiet(bar_pempty + 8 * s, (uint32_t)((fills - 1) & 1), lim);
+      }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -257,14 +330,17 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      int pslot = 0;  // DEC: P ring
+      uint32_t pphase = 0;
       for (int i = 0; i < n_chunks; ++i) {
-        if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) {
+        if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status) ||
+            (DEC && !mbar_wait(bar_pfull + 8 * pslot, pphase, abort_flag, p.status))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sp = base + stage * L::STAGE_BYTES;
-        const uint32_t sq = sp + L::P_BYTES;
+        const uint32_t sp = slot_p(stage, pslot);
+        const uint32_t sq = slot_q(stage);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint32_t accum = (i != 0 || ks != 0) ? 1u : 0u;
@@ -279,6 +355,10 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
         }
         tc_commit(bar_empty + 8 * stage);
         if (++stage == STAGES) stage = 0, phase ^= 1u;
+        if constexpr (DEC) {
+          tc_commit(bar_pempty + 8 * pslot);
+          if (++pslot == PST) pslot = 0, pphase ^= 1u;
+        }
       }
       if (ok) tc_commit(bar_acc_full);
       if (*abort_flag) {
@@ -286,6 +366,73 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
         mbar_wait_quiet(bar_drain, 0, 100000000ull);
       }
     }
+  } else if (DEC && warp >= 6) {
+    // ------------------------------------------------------- NF4 decode
+    // thread t decodes half h = t & 1 (codes 32h..32h+31) of row t >> 1 of
+    // each P tile; a problem without codes passes its stages straight on
+    const int t = threadIdx.x - 192;  // 0..255
+    const int h = t & 1, prow = t >> 1;
+    const bool dec = P.nf4 != 0;
+    const int wrow = rt * 128 + prow;
+    const bool row_in = wrow < P.rows;
+    constexpr int PRE = L::AMAX_PRE;
+    constexpr uint32_t kSlot = L::DEC_THREADS * 4;
+    const uint32_t ring = base + L::OFF_AMAX + (uint32_t)t * 4u;  // slot j at ring + kSlot j
+    float lvl[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) lvl[i] = kNf4Levels[i];
+    const __nv_bfloat16 *arow = P.absmax + (size_t)(row_in ? wrow : 0) * P.ld_absmax;
+    // the absmax of sequence position i (chunk c_begin + (i + c_rot) % n_chunks)
+    auto amax_ptr = [&](int i) { return arow + c_begin + (i + c_rot) % n_chunks; };
+    auto prefetch = [&](int i, uint32_t slot) {
+      if (dec && row_in && i < n_chunks)
+        cp_async_4(ring + slot * kSlot, reinterpret_cast<const void *>(
+                                            reinterpret_cast<uintptr_t>(amax_ptr(i)) & ~uintptr_t(3)));
+      cp_async_commit();
+    };
+    for (int j = 0; j < PRE; ++j) prefetch(j, (uint32_t)j);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t slot = 0;
+    int pslot = 0;
+    uint32_t pphase = 0;
+    for (int i = 0; i < n_chunks; ++i) {
+      if (!warp_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) break;
+      // the P slot is free once the MMA of its previous use has completed
+      // (for P loaded by TMA the producer waited for that)
+      if (dec && !warp_wait(bar_pempty + 8 * pslot, pphase ^ 1u, abort_flag, p.status)) break;
+      if (dec) {
+        cp_async_wait<PRE - 1>();  // this chunk's absmax has landed
+        float amax = 0.0f;
+        if (row_in) {
+          const uint32_t w = ld_shared_u32(ring + slot * kSlot);
+          const bool high = (reinterpret_cast<uintptr_t>(amax_ptr(i)) & 2u) != 0;
+          amax = __uint_as_float((high ? (w >> 16) : (w & 0xFFFFu)) << 16);
+        }
+        prefetch(i + PRE, slot);  // the slot just read refills for PRE chunks ahead
+        if (++slot == (uint32_t)PRE) slot = 0;
+        // a warp reads 16 rows x 32 contiguous code bytes: conflict-free
+        const uint4 cw = ld_shared_v4(slot_q(stage) + L::Q_BYTES + (uint32_t)t * 16u);
+        const Nf4Table tab = nf4_table<F16>(lvl, amax);
+        const uint32_t dst = slot_p(stage, pslot) + (uint32_t)prow * 128u;
+        const uint32_t ph = (uint32_t)prow & 7u;
+        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+        for (int ql = 0; ql < 4; ++ql) {
+          uint32_t o[4];
+          nf4_lookup4(tab, words[ql] & 0xFFFFu, o[0], o[1]);
+          nf4_lookup4(tab, words[ql] >> 16, o[2], o[3]);
+          const uint32_t q = (uint32_t)(4 * h + ql);
+          st_shared_v4(dst + ((q ^ ph) << 4), o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pfull + 8 * pslot);
+      if (++stage == STAGES) stage = 0, phase ^= 1u;
+      if (++pslot == PST) pslot = 0, pphase ^= 1u;
+    }
+    cp_async_wait<0>();  // no copy may land after the CTA exits
   }
 
   // ---------------------------------------------- epilogue (warps 2-5)
@@ -294,7 +441,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   //    their recv slots (distributed shared memory stores)
   // 3. each CTA adds the S partials of its own block in cluster-rank order
   //    (deterministic), stages the result and copies it out
-  const bool epi = warp >= 2;
+  const bool epi = warp >= 2 && warp < 6;
   const int row = (warp & 3) * 32 + lane;
   const uint32_t t_lane = (uint32_t)((warp & 3) * 32) << 16;
   const SkinnyEpi E(RP, S);
@@ -328,7 +475,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   }
   __syncwarp();
   if (S > 1) cluster_sync_all();  // pushed partials have landed
-  const bool want_t = (P.out_kind & (kOutVt | kOutRowT)) != 0;
+  const bool want_t = (P.out_kind & (kOutVt | kOutRowT | kOutT16)) != 0;
   const bool want_r = (P.out_kind & (kOutRowBf16 | kOutRow)) != 0;
   if (epi && acc_ok) {
 #pragma unroll 1
@@ -380,31 +527,36 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_kernel(const __grid_consta
   }
 }
 
-template <bool MN, int RP, bool F16>
+template <bool MN, int RP, bool F16, bool DEC>
 static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
-  using L = SkinnySmem<MN, RP>;
-  auto kern = lora_skinny_kernel<MN, RP, F16>;
+  using L = SkinnySmem<MN, RP, DEC>;
+  auto kern = lora_skinny_kernel<MN, RP, F16, DEC>;
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
   if (e != cudaSuccess) return e;
   int tiles = 0;
   for (int q = 0; q < p.num_problems; ++q) tiles += p.pr[q].row_tiles;
-  const char *name = MN ? (F16 ? "lora_skinny_kernel<mn_major,f16>" : "lora_skinny_kernel<mn_major>")
-                        : (F16 ? "lora_skinny_kernel<k_major,f16>" : "lora_skinny_kernel<k_major>");
-  return launch_pdl(name, kern,
-                    dim3((unsigned)(tiles * p.split)), dim3(192), L::TOTAL, st,
-                    (unsigned)p.split, p);
+  const char *name =
+      DEC ? (F16 ? "lora_skinny_kernel<k_major,nf4,f16>" : "lora_skinny_kernel<k_major,nf4>")
+      : MN ? (F16 ? "lora_skinny_kernel<mn_major,f16>" : "lora_skinny_kernel<mn_major>")
+           : (F16 ? "lora_skinny_kernel<k_major,f16>" : "lora_skinny_kernel<k_major>");
+  return launch_pdl(name, kern, dim3((unsigned)(tiles * p.split)), dim3(DEC ? 448 : 192),
+                    L::TOTAL, st, (unsigned)p.split, p);
 }
 
-template <bool MN, int RP>
+template <bool MN, int RP, bool DEC = false>
 static int max_split_t() {
-  using L = SkinnySmem<MN, RP>;
+  using L = SkinnySmem<MN, RP, DEC>;
   int s = 1;
-  while (s < 8 && RP / (2 * s) >= 16 && SkinnyEpi(RP, 2 * s).bytes <= L::OFF_MISC) s *= 2;
+  while (s < 8 && RP / (2 * s) >= 16 && SkinnyEpi(RP, 2 * s).bytes <= L::OFF_AMAX) s *= 2;
   return s;
 }
 
-int skinny_max_split(bool mn_major, int rp) {
+int skinny_max_split(bool mn_major, int rp, bool dec) {
+  if (dec) {
+    if (mn_major) return 1;
+    return rp == 64 ? max_split_t<false, 64, true>() : rp == 128 ? max_split_t<false, 128, true>() : 1;
+  }
   switch (rp) {
     case 16: return mn_major ? max_split_t<true, 16>() : max_split_t<false, 16>();
     case 32: return mn_major ? max_split_t<true, 32>() : max_split_t<false, 32>();
@@ -415,23 +567,29 @@ int skinny_max_split(bool mn_major, int rp) {
 }
 
 template <bool F16>
-static cudaError_t launch_skinny_cluster_t(const SkinnyParams &p, bool mn_major, int rp,
+static cudaError_t launch_skinny_cluster_t(const SkinnyParams &p, bool mn_major, int rp, bool dec,
                                            cudaStream_t st) {
+  if (dec) {
+    if (mn_major) return cudaErrorInvalidValue;
+    if (rp == 64) return launch_skinny_t<false, 64, F16, true>(p, st);
+    if (rp == 128) return launch_skinny_t<false, 128, F16, true>(p, st);
+    return cudaErrorInvalidValue;
+  }
   switch (rp) {
-    case 16: return mn_major ? launch_skinny_t<true, 16, F16>(p, st) : launch_skinny_t<false, 16, F16>(p, st);
-    case 32: return mn_major ? launch_skinny_t<true, 32, F16>(p, st) : launch_skinny_t<false, 32, F16>(p, st);
-    case 64: return mn_major ? launch_skinny_t<true, 64, F16>(p, st) : launch_skinny_t<false, 64, F16>(p, st);
-    case 128: return mn_major ? launch_skinny_t<true, 128, F16>(p, st) : launch_skinny_t<false, 128, F16>(p, st);
+    case 16: return mn_major ? launch_skinny_t<true, 16, F16, false>(p, st) : launch_skinny_t<false, 16, F16, false>(p, st);
+    case 32: return mn_major ? launch_skinny_t<true, 32, F16, false>(p, st) : launch_skinny_t<false, 32, F16, false>(p, st);
+    case 64: return mn_major ? launch_skinny_t<true, 64, F16, false>(p, st) : launch_skinny_t<false, 64, F16, false>(p, st);
+    case 128: return mn_major ? launch_skinny_t<true, 128, F16, false>(p, st) : launch_skinny_t<false, 128, F16, false>(p, st);
   }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, bool f16,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, bool dec) {
   if (p.split != 1 && p.split != 2 && p.split != 4 && p.split != 8) return cudaErrorInvalidValue;
-  if (p.split > skinny_max_split(mn_major, rp)) return cudaErrorInvalidValue;
-  return f16 ? launch_skinny_cluster_t<true>(p, mn_major, rp, st)
-             : launch_skinny_cluster_t<false>(p, mn_major, rp, st);
+  if (p.split > skinny_max_split(mn_major, rp, dec)) return cudaErrorInvalidValue;
+  return f16 ? launch_skinny_cluster_t<true>(p, mn_major, rp, dec, st)
+             : launch_skinny_cluster_t<false>(p, mn_major, rp, dec, st);
 }
 
 }  // namespace lora

@@ -240,3 +240,56 @@ def test_nf4_qk_pair_staged_in_bf16():
     assert rel_err(np64(dx), want[0]) <= TOL_BF16
     for got, w in zip(grads, want[1:]):
         assert rel_err(np64(got), w) <= TOL_F32
+
+
+@pytest.mark.parametrize("M,k,n,r,dtype,kind", [
+    (1, 512, 768, 16, torch.bfloat16, "dense"),       # a single token
+    (16, 1024, 2048, 64, torch.bfloat16, "dense"),
+    (37, 4096, 1024, 8, torch.float16, "dense"),      # ragged token count
+    (64, 512, 4096, 32, torch.bfloat16, "dense"),
+    (100, 2048, 640, 16, torch.float16, "dense"),     # M in (64, 128]: tokens padded to 128
+    (128, 320, 1280, 64, torch.bfloat16, "dense"),
+    (1, 1024, 768, 16, torch.bfloat16, "nf4"),
+    (16, 4096, 1088, 64, torch.bfloat16, "nf4"),      # W rows not a multiple of 128
+    (50, 2048, 2048, 8, torch.float16, "nf4"),
+    (100, 576, 640, 32, torch.bfloat16, "nf4"),
+    (24, 1024, 1536, 16, torch.bfloat16, "nf4dq"),
+])
+def test_small_m_forward_runs_over_the_rows_of_w(M, k, n, r, dtype, kind):
+    """With at most 128 tokens the forward is one rank-pass launch over the
+    rows of W and of A (yᵀ = W·xᵀ and (s·v)ᵀ = s·A·xᵀ, the reduction split
+    across a cluster, so every SM streams a share of W; an NF4 W is decoded
+    from its codes inside that launch), then the GEMM adding (s·v)·Bᵀ to y
+    in its epilogue."""
+    d = draw_projection(torch.Generator().manual_seed(M + k), M, k, n, r, dtype=dtype)
+    x, A, B = (cuda(d[t]) for t in ("x", "A", "B"))
+    flag = 0
+    if kind == "dense":
+        Wt = cuda(d["W"])
+        Wd, keep, W64 = L.dense_weight(Wt), [Wt], np64(d["W"])
+    elif kind == "nf4":
+        codes, absmax = ref.nf4_quantize(np64(d["W"]))
+        c = cuda(torch.from_numpy(codes))
+        a = cuda(torch.from_numpy(absmax.astype(np.float32)).to(torch.bfloat16))
+        Wd, keep, W64 = L.nf4_weight(c, a, dtype=dtype), [c, a], ref.nf4_dequant(codes, absmax)
+    else:
+        codes, qc, sc, off = ref.nf4_quantize_dq(np64(d["W"]))
+        keep = [cuda(torch.from_numpy(codes)), cuda(torch.from_numpy(qc)),
+                cuda(torch.from_numpy(sc)), cuda(torch.tensor([off], dtype=torch.float32))]
+        Wd = L.nf4_weight(keep[0], keep[1], dtype=dtype, absmax_scale=keep[2],
+                          absmax_offset=keep[3])
+        W64 = ref.nf4_dequant_dq(codes, qc, sc, off)
+        flag = L.OP_FLAG_DQ
+    y = torch.full((M, n), float("nan"), dtype=dtype, device="cuda")
+    ws = L.workspace(L.OP_FWD | flag, M, k, n, r)
+    names = _profiled(lambda: L.lora_linear_fwd(x, Wd, A, B, y, ALPHA, ws))
+    torch.cuda.synchronize()
+    assert L.lora_read_device_status(ws) == 0
+    f16 = ",f16" if dtype == torch.float16 else ""
+    want_names = (["nf4_dq_expand_kernel"] if kind == "nf4dq" else []) + [
+        "lora_skinny_kernel<k_major" + (",nf4" if kind != "dense" else "") + f16 + ">",
+        "lora_gemm_pair_kernel<fwd," + ("f16" if f16 else "bf16") + ">"]
+    assert names == want_names, names
+    want = ref.lora_fwd(np64(d["x"]), W64, np64(d["A"]), np64(d["B"]), ALPHA)
+    tol = TOL_BF16 if dtype == torch.bfloat16 else 4e-3
+    assert rel_err(np64(y), want) <= tol

@@ -479,7 +479,7 @@ lora_status_t run_gemm(const GemmOpts &o, cudaStream_t st) {
 // Q [rl, K] bf16, or Q = [Q1; Q2] with q_rows1 rows each).
 lora_status_t kmajor_problem(SkinnyProblem &P, const void *p_ptr, int rows, int K,
                              const void *q1, const void *q2, int q_rows1, int rl, int rp,
-                             CUtensorMapDataType dt) {
+                             CUtensorMapDataType dt, bool tight_q = false) {
   if (!make_map(&P.tm_p, dt, 2, p_ptr, K, rows, (uint64_t)K * 2, 64, 128, true))
     return LORA_ERR_CUDA;
   if (q2) {
@@ -488,10 +488,16 @@ lora_status_t kmajor_problem(SkinnyProblem &P, const void *p_ptr, int rows, int 
       return LORA_ERR_CUDA;
     P.q_rows1 = q_rows1;
   } else {
-    if (!make_map(&P.tm_q, dt, 2, q1, K, rl, (uint64_t)K * 2, 64, rp, true))
+    // tight_q (cluster schedule only): the box covers the rl real rows and
+    // the kernel keeps the rest of the tile zero; rows past rl would be
+    // zero-filled copies that still cross the L2-to-SM fabric
+    const int box = tight_q ? rl : rp;
+    if (!make_map(&P.tm_q, dt, 2, q1, K, rl, (uint64_t)K * 2, 64, box, true))
       return LORA_ERR_CUDA;
     P.q_rows1 = 0;
+    P.q_rows = box;
   }
+  if (q2) P.q_rows = rp;
   P.rows = rows;
   P.row_tiles = (rows + 127) / 128;
   P.chunks = K / 64;
@@ -547,7 +553,7 @@ unsigned long long next_epoch() {
 
 lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, bool f16, uint32_t *status,
                          void *scratch, cudaStream_t st, bool cluster_only = false,
-                         bool dec = false) {
+                         bool dec = false, bool two = false) {
   DeviceInfo di;
   lora_status_t s;
   if ((s = device_info(&di))) return s;
@@ -562,7 +568,9 @@ lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, bool f16, uint32_t *
   }
   if (units < 1) return LORA_ERR_INVALID_ARG;
   sp.status = status;
-  sp.split = pick_split(tiles, min_chunks, di.sms, skinny_max_split(mn, rp, dec));
+  // `two`: two CTAs share an SM, so twice the SMs' count of CTAs fit one wave
+  sp.split = pick_split(tiles, min_chunks, two ? 2 * di.sms : di.sms,
+                        skinny_max_split(mn, rp, dec, two));
   long long w_cluster = 0;  // chunks of the busiest CTA
   for (int q = 0; q < sp.num_problems; ++q)
     w_cluster = std::max<long long>(w_cluster, (sp.pr[q].chunks + sp.split - 1) / sp.split);
@@ -572,7 +580,7 @@ lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, bool f16, uint32_t *
       1, std::min<long long>(std::min(di.sms, kSkinnyMaxCtas), units / 8));
   const long long w_sk = (units + ctas - 1) / ctas;
   if (cluster_only || 4 * w_sk > 3 * w_cluster)
-    return cuda_status(launch_skinny_cluster(sp, mn, rp, f16, st, dec));
+    return cuda_status(launch_skinny_cluster(sp, mn, rp, f16, st, dec, two));
   sp.units = units;
   sp.ctas = ctas;
   uint8_t *s8 = static_cast<uint8_t *>(scratch);
@@ -649,8 +657,8 @@ lora_status_t small_m_fwd(const void *x, const lora_weight_t &W, const void *A, 
   SkinnyProblem &PW = sp.pr[0];
   SkinnyProblem &PA = sp.pr[1];
   const bool nf4 = W.type == LORA_WEIGHT_NF4;
-  if ((s = kmajor_problem(PW, W.w, n, k, x, nullptr, 0, M, rp, dt)) ||
-      (s = kmajor_problem(PA, A, r, k, x, nullptr, 0, M, rp, dt)))
+  if ((s = kmajor_problem(PW, W.w, n, k, x, nullptr, 0, M, rp, dt, true)) ||
+      (s = kmajor_problem(PA, A, r, k, x, nullptr, 0, M, rp, dt, true)))
     return s;
   if (nf4) {  // P from the 4-bit codes, decoded in the kernel
     if (!make_map(&PW.tm_p, kU8, 1, W.w, k / 2, n, (uint64_t)k / 2, 32, 128, false))
@@ -669,7 +677,10 @@ lora_status_t small_m_fwd(const void *x, const lora_weight_t &W, const void *A, 
   PW.r = PA.r = M;  // valid columns of the transposed outputs
   PW.nproj = PA.nproj = 1;
   sp.num_problems = 2;
-  if ((s = run_skinny(sp, false, rp, f16, status, nullptr, st, true, nf4))) return s;
+  // a dense W at up to 64 tokens: half-depth rings, two CTAs per SM (measured
+  // 16-18% faster on the Qwen1.5-32B gate / down projections at M <= 64)
+  const bool two = !nf4 && rp == 64;
+  if ((s = run_skinny(sp, false, rp, f16, status, nullptr, st, true, nf4, two))) return s;
   lora_weight_t wb{};
   wb.type = LORA_WEIGHT_DENSE;
   wb.w = B;

@@ -221,6 +221,7 @@ struct SkinnyProblem {
   CUtensorMap tm_q;      // Q (MNMAJOR: its hi part)
   CUtensorMap tm_q2;     // MNMAJOR: lo part; KMAJOR with q_rows1 > 0: Q rows [q_rows1, 2·q_rows1)
   int q_rows1;           // KMAJOR: rows taken from tm_q when Q comes from two tensors, else 0
+  int q_rows;            // KMAJOR: rows of the RP-row Q tile the copies fill; the rest is zero
   // NF4 P (the decoding variant): tm_p maps the codes [rows, K/2] bytes
   // (box 32 x 128), absmax the bf16 block scales [rows, ld_absmax]
   int nf4;
@@ -260,11 +261,13 @@ struct SkinnyParams {
 // f16: the 16-bit operands (P, Q) and outputs (hi/lo, kOutRowBf16) are fp16.
 // dec: the NF4-decoding variant (KMAJOR, rp 64 or 128; problems with `nf4`
 // set stream codes through tm_p and absmax instead of P).
+// two: the variant with half-depth rings that runs two CTAs per SM (KMAJOR,
+// rp 64, no decode).
 cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, bool f16,
-                                  cudaStream_t st, bool dec = false);
-// Largest `split` the cluster kernel supports for (mn_major, rp, dec) (its
-// epilogue buffers must fit in its pipeline ring).
-int skinny_max_split(bool mn_major, int rp, bool dec = false);
+                                  cudaStream_t st, bool dec = false, bool two = false);
+// Largest `split` the cluster kernel supports for (mn_major, rp, dec, two)
+// (its epilogue buffers must fit in its pipeline ring).
+int skinny_max_split(bool mn_major, int rp, bool dec = false, bool two = false);
 // Scratch of one stream-K launch: flags, then partials (256-byte aligned).
 size_t skinny_scratch_bytes(int rp);
 cudaError_t launch_skinny_sk(const SkinnyParams &p, bool mn_major, int rp, bool f16,

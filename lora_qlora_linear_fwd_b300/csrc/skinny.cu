@@ -29,8 +29,11 @@
 
 namespace lora {
 
-template <bool MN, int RP, bool DEC = false>
+// PER_SM = 2: a ring half as deep, so that two CTAs share an SM (the
+// small-M forward's pass over W, where more CTAs in flight pay).
+template <bool MN, int RP, bool DEC = false, int PER_SM = 1>
 struct SkinnySmem {
+  static constexpr int SMEM_BUDGET = PER_SM == 2 ? 115712 : kSmemLimit;
   static constexpr int P_BYTES = 128 * 128;  // [128 x 64] bf16 either way
   static constexpr int Q_BYTES = RP * 128;
   static constexpr int C_BYTES = DEC ? 128 * 32 : 0;  // NF4 codes of a P tile
@@ -41,7 +44,7 @@ struct SkinnySmem {
   // a TMA stage: P (not DEC) and Q (MN: its hi and lo parts), codes (DEC)
   static constexpr int STAGE_BYTES = (DEC ? 0 : P_BYTES) + (MN ? 2 : 1) * Q_BYTES + C_BYTES;
   static constexpr int STAGES_FIT =
-      (kSmemLimit - 4096 - AMAX_BYTES - PST * P_BYTES) / STAGE_BYTES;
+      (SMEM_BUDGET - 4096 - AMAX_BYTES - PST * P_BYTES) / STAGE_BYTES;
   static constexpr int STAGES_MAX = DEC ? 16 : 10;
   static constexpr int STAGES = STAGES_FIT > STAGES_MAX ? STAGES_MAX : STAGES_FIT;
   static constexpr int OFF_PRING = STAGES * STAGE_BYTES;
@@ -50,7 +53,7 @@ struct SkinnySmem {
   static constexpr int TOTAL = OFF_MISC + 512 + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 4, "pipeline depth");
-  static_assert(TOTAL <= kSmemLimit, "shared memory budget");
+  static_assert(TOTAL <= SMEM_BUDGET, "shared memory budget");
 };
 
 // Epilogue buffers, laid over the (then idle) TMA ring.  A CTA of a cluster
@@ -189,10 +192,10 @@ LORA_DEV void skinny_copy_out(const SkinnyProblem &P, int rt, int col0, int cw,
   }
 }
 
-template <bool MN, int RP, bool F16, bool DEC>
-__global__ void __launch_bounds__(DEC ? 448 : 192, 1)
+template <bool MN, int RP, bool F16, bool DEC, int PER_SM = 1>
+__global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
     lora_skinny_kernel(const __grid_constant__ SkinnyParams p) {
-  using L = SkinnySmem<MN, RP, DEC>;
+  using L = SkinnySmem<MN, RP, DEC, PER_SM>;
   static_assert(!DEC || !MN, "NF4 decode: KMAJOR only");
   static_assert(SkinnyEpi(RP, 1).bytes <= L::OFF_AMAX, "epilogue buffers fit in the ring");
   constexpr int STAGES = L::STAGES;
@@ -253,6 +256,16 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, 1)
     tmem_alloc(smem_addr(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
+  if (!MN && P.q_rows < RP) {
+    // rows [q_rows, RP) of every Q slot stay zero (the copies fill the rest)
+    const uint32_t row_bytes = (uint32_t)(RP - P.q_rows) * 128u;
+    for (uint32_t o = threadIdx.x * 16u; o < (uint32_t)STAGES * row_bytes; o += blockDim.x * 16u) {
+      const uint32_t st = o / row_bytes;
+      st_shared_v4(slot_q((int)st) + (uint32_t)P.q_rows * 128u + (o - st * row_bytes), 0u, 0u, 0u,
+                   0u);
+    }
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -277,12 +290,12 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, 1)
         const uint32_t fb = bar_full + 8 * stage;
         if constexpr (DEC) {
           if (P.nf4) {  // Q and the codes of the P tile (decoded by the decode warps)
-            mbar_arrive_expect_tx(fb, L::C_BYTES + L::Q_BYTES);
+            mbar_arrive_expect_tx(fb, L::C_BYTES + P.q_rows * 128);
             tma_load_2d(sq + L::Q_BYTES, &P.tm_p, fb, c * 32, rt * 128);
             tma_load_2d(sq, &P.tm_q, fb, c * 64, 0);
           } else {      // Q, and P straight into the P ring
             if (!mbar_wait(bar_pempty + 8 * pslot, pphase ^ 1u, abort_flag, p.status)) break;
-            mbar_arrive_expect_tx(fb, L::P_BYTES + L::Q_BYTES);
+            mbar_arrive_expect_tx(fb, L::P_BYTES + P.q_rows * 128);
             tma_load_2d(slot_p(stage, pslot), &P.tm_p, fb, c * 64, rt * 128);
             tma_load_2d(sq, &P.tm_q, fb, c * 64, 0);
             ++pissued;
@@ -292,7 +305,7 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, 1)
           if (++stage == STAGES) stage = 0, phase ^= 1u;
           continue;
         }
-        mbar_arrive_expect_tx(fb, L::STAGE_BYTES);
+        mbar_arrive_expect_tx(fb, MN ? L::STAGE_BYTES : L::P_BYTES + P.q_rows * 128);
         if constexpr (MN) {
           // P [tokens, rows]: two boxes of [64 rows-of-output x 64 tokens]
           tma_load_2d(sp, &P.tm_p, fb, rt * 128, c * 64);
@@ -527,10 +540,10 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, 1)
   }
 }
 
-template <bool MN, int RP, bool F16, bool DEC>
+template <bool MN, int RP, bool F16, bool DEC, int PER_SM = 1>
 static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
-  using L = SkinnySmem<MN, RP, DEC>;
-  auto kern = lora_skinny_kernel<MN, RP, F16, DEC>;
+  using L = SkinnySmem<MN, RP, DEC, PER_SM>;
+  auto kern = lora_skinny_kernel<MN, RP, F16, DEC, PER_SM>;
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void *>(kern), L::TOTAL);
   if (e != cudaSuccess) return e;
@@ -538,21 +551,23 @@ static cudaError_t launch_skinny_t(const SkinnyParams &p, cudaStream_t st) {
   for (int q = 0; q < p.num_problems; ++q) tiles += p.pr[q].row_tiles;
   const char *name =
       DEC ? (F16 ? "lora_skinny_kernel<k_major,nf4,f16>" : "lora_skinny_kernel<k_major,nf4>")
+      : PER_SM == 2 ? (F16 ? "lora_skinny_kernel<k_major,2cta,f16>" : "lora_skinny_kernel<k_major,2cta>")
       : MN ? (F16 ? "lora_skinny_kernel<mn_major,f16>" : "lora_skinny_kernel<mn_major>")
            : (F16 ? "lora_skinny_kernel<k_major,f16>" : "lora_skinny_kernel<k_major>");
   return launch_pdl(name, kern, dim3((unsigned)(tiles * p.split)), dim3(DEC ? 448 : 192),
                     L::TOTAL, st, (unsigned)p.split, p);
 }
 
-template <bool MN, int RP, bool DEC = false>
+template <bool MN, int RP, bool DEC = false, int PER_SM = 1>
 static int max_split_t() {
-  using L = SkinnySmem<MN, RP, DEC>;
+  using L = SkinnySmem<MN, RP, DEC, PER_SM>;
   int s = 1;
   while (s < 8 && RP / (2 * s) >= 16 && SkinnyEpi(RP, 2 * s).bytes <= L::OFF_AMAX) s *= 2;
   return s;
 }
 
-int skinny_max_split(bool mn_major, int rp, bool dec) {
+int skinny_max_split(bool mn_major, int rp, bool dec, bool two) {
+  if (two) return (!mn_major && !dec && rp == 64) ? max_split_t<false, 64, false, 2>() : 1;
   if (dec) {
     if (mn_major) return 1;
     return rp == 64 ? max_split_t<false, 64, true>() : rp == 128 ? max_split_t<false, 128, true>() : 1;
@@ -568,7 +583,11 @@ int skinny_max_split(bool mn_major, int rp, bool dec) {
 
 template <bool F16>
 static cudaError_t launch_skinny_cluster_t(const SkinnyParams &p, bool mn_major, int rp, bool dec,
-                                           cudaStream_t st) {
+                                           bool two, cudaStream_t st) {
+  if (two) {
+    if (mn_major || dec || rp != 64) return cudaErrorInvalidValue;
+    return launch_skinny_t<false, 64, F16, false, 2>(p, st);
+  }
   if (dec) {
     if (mn_major) return cudaErrorInvalidValue;
     if (rp == 64) return launch_skinny_t<false, 64, F16, true>(p, st);
@@ -585,11 +604,11 @@ static cudaError_t launch_skinny_cluster_t(const SkinnyParams &p, bool mn_major,
 }
 
 cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, bool f16,
-                                  cudaStream_t st, bool dec) {
+                                  cudaStream_t st, bool dec, bool two) {
   if (p.split != 1 && p.split != 2 && p.split != 4 && p.split != 8) return cudaErrorInvalidValue;
-  if (p.split > skinny_max_split(mn_major, rp, dec)) return cudaErrorInvalidValue;
-  return f16 ? launch_skinny_cluster_t<true>(p, mn_major, rp, dec, st)
-             : launch_skinny_cluster_t<false>(p, mn_major, rp, dec, st);
+  if (p.split > skinny_max_split(mn_major, rp, dec, two)) return cudaErrorInvalidValue;
+  return f16 ? launch_skinny_cluster_t<true>(p, mn_major, rp, dec, two, st)
+             : launch_skinny_cluster_t<false>(p, mn_major, rp, dec, two, st);
 }
 
 }  // namespace lora

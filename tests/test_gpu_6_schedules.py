@@ -286,8 +286,9 @@ def test_small_m_forward_runs_over_the_rows_of_w(M, k, n, r, dtype, kind):
     torch.cuda.synchronize()
     assert L.lora_read_device_status(ws) == 0
     f16 = ",f16" if dtype == torch.float16 else ""
+    variant = ",nf4" if kind != "dense" else (",2cta" if M <= 64 else "")
     want_names = (["nf4_dq_expand_kernel"] if kind == "nf4dq" else []) + [
-        "lora_skinny_kernel<k_major" + (",nf4" if kind != "dense" else "") + f16 + ">",
+        "lora_skinny_kernel<k_major" + variant + f16 + ">",
         "lora_gemm_pair_kernel<fwd," + ("f16" if f16 else "bf16") + ">"]
     assert names == want_names, names
     want = ref.lora_fwd(np64(d["x"]), W64, np64(d["A"]), np64(d["B"]), ALPHA)

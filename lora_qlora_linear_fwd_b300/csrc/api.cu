@@ -838,11 +838,14 @@ lora_status_t bwd_grads(const BwdCall &c, cudaStream_t st) {
   return run_skinny(sp, true, b.rp, c.f16, c.status, c.at<void>(b.off_scratch), st);
 }
 
+// dA/dB run before dX: the dA/dB pass re-reads x and dY right after the
+// u/v pass has read them, so on the smaller projections (x and dY within
+// the L2) it reads them from the L2; dX does not depend on either.
 lora_status_t run_bwd_phases(const BwdCall &c, cudaStream_t st) {
   lora_status_t s;
   if ((s = bwd_rank(c, st))) return s;
-  if ((s = bwd_dx(c, st))) return s;
-  return bwd_grads(c, st);
+  if ((s = bwd_grads(c, st))) return s;
+  return bwd_dx(c, st);
 }
 
 // The q/k backward runs q and k as one projection of rank 2r:
@@ -1251,6 +1254,7 @@ lora_status_t lora_linear_bwd_dropout(const void *x, lora_weight_t W, const void
                                         thresh, inv_q, f16, st))))
     return s;
   if ((s = bwd_rank(c, st))) return s;
+  if ((s = bwd_grads(c, st))) return s;  // before dX, as in run_bwd_phases
   // dX = dY·W (no adapter K-blocks) ...
   {
     GroupArgs ga{W, nullptr, dx, k, 0};
@@ -1293,9 +1297,8 @@ lora_status_t lora_linear_bwd_dropout(const void *x, lora_weight_t W, const void
     o.drop_scale = inv_q;
     o.drop_seed = seed;
     o.drop_offset = offset;
-    if ((s = run_gemm(o, st))) return s;
+    return run_gemm(o, st);
   }
-  return bwd_grads(c, st);
 }
 
 static lora_status_t check_qk(const void *x, lora_weight_t Wq, const void *Aq, const void *Bq,

@@ -71,7 +71,7 @@ def test_nf4_quantize_parity(n, k):
 @pytest.mark.gpu
 def test_profile_session_times_each_launch_of_a_call():
     """Per-launch timing: one backward call is four launches (set-up, rank
-    pass, dX GEMM, dA/dB pass), each with a positive time, in launch order."""
+    pass, dA/dB pass, dX GEMM), each with a positive time, in launch order."""
     M, k, n, r = 512, 512, 768, 16
     d = draw_projection(torch.Generator().manual_seed(5), M, k, n, r)
     x, W, A, B, dy = (cuda(d[t]) for t in ("x", "W", "A", "B", "dY"))
@@ -86,8 +86,8 @@ def test_profile_session_times_each_launch_of_a_call():
     got = L.lora_profile_end(8)
     assert n_launch == 4 and len(got) == 4
     names = [nm for nm, _ in got]
-    assert names[0] == "bwd_prep_kernel" and names[2] == "lora_gemm_pair_kernel<dx,bf16>"
-    assert names[1].startswith("lora_skinny") and names[3].startswith("lora_skinny")
+    assert names[0] == "bwd_prep_kernel" and names[3] == "lora_gemm_pair_kernel<dx,bf16>"
+    assert names[1].startswith("lora_skinny") and names[2].startswith("lora_skinny")
     assert all(ms > 0.0 for _, ms in got)
     # the session is closed: a second end is an argument error
     with pytest.raises(L.LoraError):

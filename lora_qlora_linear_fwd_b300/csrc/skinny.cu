@@ -82,7 +82,7 @@ LORA_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 // the staging buffers, by the 128 epilogue threads (e = 0..127).  Every
 // warp-wide store covers contiguous runs of 256 to 512 bytes.
 template <bool F16>
-LORA_DEV void skinny_copy_out(const SkinnyProblem &P, int rt, int col0, int cw,
+LORA_DEV void skinny_copy_out(const SkinnyDest &P, int rt, int col0, int cw,
                               const float *stage_t, const float *stage_r, int e) {
   const int cols = P.nproj * P.r;  // valid rank columns
   const int row0 = rt * 128;
@@ -530,7 +530,8 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
   }
   if (epi) {
     epi_bar();
-    if (acc_ok) skinny_copy_out<F16>(P, rt, srank * CW, CW, stage_t, stage_r, threadIdx.x - 64);
+    if (acc_ok)
+      skinny_copy_out<F16>(skinny_dest(P), rt, srank * CW, CW, stage_t, stage_r, threadIdx.x - 64);
   }
   tc_fence_before();
   __syncthreads();

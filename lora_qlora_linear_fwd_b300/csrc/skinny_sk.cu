@@ -105,7 +105,7 @@ LORA_DEV long long range_begin(const SkinnyParams &p, int cta) {
 // each column is one contiguous run per warp; row-major kinds: each thread
 // stores its row's 16 columns in 16-byte pieces.
 template <bool F16>
-LORA_DEV void skinny_store16(const SkinnyProblem &P, int rt, int row, int j0, const float (&v)[16]) {
+LORA_DEV void skinny_store16(const SkinnyDest &P, int rt, int row, int j0, const float (&v)[16]) {
   const int grow = rt * 128 + row;
   if (grow >= P.rows) return;
   const int cols = P.nproj * P.r;  // valid rank columns
@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
           ok = __all_sync(0xffffffffu, mbar_wait(bar_ready, 0, abort_flag, p.status));
         }
         if (ok) {
+          const SkinnyDest out = skinny_dest(P);
           const float *ring = reinterpret_cast<const float *>(smem) + row;
 #pragma unroll 1
           for (int c = 0; c < RP / 16; ++c) {
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
                 for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (c * 16 + j) * 128);
               }
             }
-            skinny_store16<F16>(P, sg.rt, row, c * 16, v);
+            skinny_store16<F16>(out, sg.rt, row, c * 16, v);
           }
         }
       }

@@ -20,6 +20,7 @@
 // fp32 value (about 2^-17 relative) and both are multiplied, keeping
 // near-fp32 accuracy for dA and dB.
 #include "kernels.h"
+#include "skinny_out.cuh"
 
 namespace lora {
 namespace sk {
@@ -185,7 +186,8 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
   // last segment)
   const uint32_t bar_parked = bar_drain + 8;   // four epilogue warps stored the partial
   const uint32_t bar_ready = bar_parked + 8;   // the other CTAs' partials are visible
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC + 8 * (2 * STAGES + 7));
+  const uint32_t bar_staged = bar_ready + 8;   // four epilogue warps staged the last tile
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC + 8 * (2 * STAGES + 8));
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
   if (threadIdx.x == 0) {
@@ -200,6 +202,7 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
     mbar_init(bar_drain, 1);
     mbar_init(bar_parked, 4);
     mbar_init(bar_ready, 1);
+    mbar_init(bar_staged, 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -382,8 +385,19 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
           }
           ok = __all_sync(0xffffffffu, mbar_wait(bar_ready, 0, abort_flag, p.status));
         }
+        // The CTA's last segment leaves its ring idle: the tile is staged
+        // there, behind the partials, and copied out with wide stores (each
+        // thread's own row-by-row stores are many and narrow).
+        constexpr SkinnyEpi E(RP, 1);
+        const uint32_t soff = staged ? (uint32_t)n_part * kPartBytes : 0u;
+        const bool stage_out =
+            sg.u >= sg.end && soff + (uint32_t)E.bytes <= (uint32_t)L::OFF_MISC;
+        const SkinnyDest out = skinny_dest(P);
+        float *stage_t = reinterpret_cast<float *>(smem + soff + E.off_stage_t);
+        float *stage_r = reinterpret_cast<float *>(smem + soff + E.off_stage_r);
+        const bool want_t = (out.out_kind & (kOutVt | kOutRowT | kOutT16)) != 0;
+        const bool want_r = (out.out_kind & (kOutRowBf16 | kOutRow)) != 0;
         if (ok) {
-          const SkinnyDest out = skinny_dest(P);
           const float *ring = reinterpret_cast<const float *>(smem) + row;
 #pragma unroll 1
           for (int c = 0; c < RP / 16; ++c) {
@@ -404,8 +418,29 @@ __global__ void __launch_bounds__(192, 1) lora_skinny_sk_kernel(const __grid_con
                 for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (c * 16 + j) * 128);
               }
             }
-            skinny_store16<F16>(out, sg.rt, row, c * 16, v);
+            if (stage_out) {
+              if (want_t) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) stage_t[(c * 16 + j) * 132 + row] = v[j];
+              }
+              if (want_r) {
+                float4 *dst = reinterpret_cast<float4 *>(stage_r + row * (RP + 4) + c * 16);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              }
+            } else {
+              skinny_store16<F16>(out, sg.rt, row, c * 16, v);
+            }
           }
+        }
+        if (stage_out) {
+          // every epilogue warp arrives, also one that gave up above (it has
+          // raised the abort flag, so the others' bounded wait ends)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_staged);
+          if (__all_sync(0xffffffffu, mbar_wait(bar_staged, 0, abort_flag, p.status)) && ok)
+            skinny_copy_out<F16>(out, sg.rt, 0, RP, stage_t, stage_r, threadIdx.x - 64);
         }
       }
       tc_fence_before();

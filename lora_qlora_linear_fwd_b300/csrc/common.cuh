@@ -20,10 +20,12 @@ constexpr int kSmemLimit = 232448;
 // takes tiles t = w, w + W, w + 2W, ... of a grouped raster order: the
 // order sweeps `group_m` m-blocks for one n-tile, then the same m-blocks for
 // the next n-tile, and moves on to the next group of m-blocks when every
-// n-tile is done.  The W tiles in flight at any moment then cover about
-// group_m m-blocks and W / group_m n-tiles, whose x rows and W rows stay in
-// L2 while the neighbouring workers reuse them.  Tiles are independent (the
-// rank-r term arrives as extra K-blocks), so any order is valid.
+// n-tile is done; odd groups sweep the n-tiles backwards, so the wave that
+// crosses into a new group meets the W rows the last one left in L2.  The W
+// tiles in flight at any moment then cover about group_m m-blocks and
+// W / group_m n-tiles, whose x rows and W rows stay in L2 while the
+// neighbouring workers reuse them.  Tiles are independent (the rank-r term
+// arrives as extra K-blocks), so any order is valid.
 //
 // Contiguous form (`contiguous` set): the tiles are ordered m-block by
 // m-block (all n-tiles of an m-block in a row) and worker w takes the range
@@ -54,7 +56,7 @@ struct TileIter {
     const int gsize = min(group_m, m_blocks - first_m);
     const int rr = t - g * span;
     m_ = first_m + rr % gsize;
-    nt_ = rr / gsize;
+    nt_ = (g & 1) ? n_tiles - 1 - rr / gsize : rr / gsize;
   }
   __device__ void init(const Schedule &s, int worker) {
     n_tiles = s.n_tiles;

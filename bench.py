@@ -1243,6 +1243,20 @@ def run_nf4_dequant(args):
             "shapes": rows}
 
 
+def run_nf4_small_m(args):
+    """The small-M NF4 forward probe alone (the step line carries it too)."""
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    pool = pool_peaks()
+    rows = nf4_small_m_probe(WORKLOADS[args.workload], dev, flush, pool["hbm_gbs"],
+                             steps=args.steps)
+    return {"component": "nf4_small_m", "workload": args.workload, "unit": "us",
+            "peak_hbm_gbs": pool["hbm_gbs"], "peak_source": pool["source"],
+            "steps": args.steps, "l2": "flushed between calls (512 MiB write, outside events)",
+            "rows": rows}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1261,14 +1275,18 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the step lines of the other configurations")
-    ap.add_argument("--component", default="step", choices=["step", "nf4_dequant"],
+    ap.add_argument("--component", default="step", choices=["step", "nf4_dequant", "nf4_small_m"],
                     help="step: the fwd+bwd step (default); nf4_dequant: the standalone "
-                         "dequantisation on the QLoRA weight shapes (1 GPU)")
+                         "dequantisation on the QLoRA weight shapes; nf4_small_m: the fused "
+                         "NF4 forward at 16-64 tokens on the workload's weight shapes (1 GPU)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.component == "nf4_dequant":
         print(json.dumps(run_nf4_dequant(args)), flush=True)
+        return 0
+    if args.component == "nf4_small_m":
+        print(json.dumps(run_nf4_small_m(args)), flush=True)
         return 0
     world, rank, local = dist_env()
     if args.impl == "reference":

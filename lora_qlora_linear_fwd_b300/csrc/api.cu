@@ -519,12 +519,13 @@ lora_status_t mnmajor_problem(SkinnyProblem &P, const void *p_ptr, int M, int ro
   return LORA_OK;
 }
 
-// CTAs per cluster of the cluster schedule: split the reduction while the
-// grid still fits on the SMs at one CTA each and every CTA keeps >= 8 chunks.
-int pick_split(int tiles, int min_chunks, int sms, int max_split) {
-  int s = 1;
-  while (2 * s <= max_split && tiles * s * 2 <= sms && min_chunks >= 8 * s * 2) s *= 2;
-  return s;
+// CTAs per cluster of the cluster schedule: the largest split the pass
+// supports for which the grid still fits on the SMs at one CTA each and
+// every CTA keeps >= 8 chunks.
+int pick_split(int tiles, int min_chunks, int sms, bool mn, int rp, bool dec, bool two) {
+  for (int s = 8; s > 1; --s)
+    if (skinny_split_ok(mn, rp, dec, two, s) && tiles * s <= sms && min_chunks >= 8 * s) return s;
+  return 1;
 }
 
 // A rank pass.  The cluster schedule (one tile per cluster) is taken unless
@@ -569,8 +570,7 @@ lora_status_t run_skinny(SkinnyParams &sp, bool mn, int rp, bool f16, uint32_t *
   if (units < 1) return LORA_ERR_INVALID_ARG;
   sp.status = status;
   // `two`: two CTAs share an SM, so twice the SMs' count of CTAs fit one wave
-  sp.split = pick_split(tiles, min_chunks, two ? 2 * di.sms : di.sms,
-                        skinny_max_split(mn, rp, dec, two));
+  sp.split = pick_split(tiles, min_chunks, two ? 2 * di.sms : di.sms, mn, rp, dec, two);
   long long w_cluster = 0;  // chunks of the busiest CTA
   for (int q = 0; q < sp.num_problems; ++q)
     w_cluster = std::max<long long>(w_cluster, (sp.pr[q].chunks + sp.split - 1) / sp.split);
@@ -650,13 +650,15 @@ lora_status_t small_m_fwd(const void *x, const lora_weight_t &W, const void *A, 
   lora_status_t s;
   const CUtensorMapDataType dt = t16(f16);
   // the token axis padded to 64 (or 128): narrower tiles would leave no room
-  // to split the reduction across a cluster (16-column blocks per CTA)
-  const int rp = M <= 64 ? 64 : 128;
+  // to split the reduction across a cluster (16-column blocks per CTA).  An
+  // NF4 W pads to 96 up to 96 tokens: its decoding pass then splits a tile
+  // over 3 or 6 CTAs, and a 5120-row W fills 123 SMs rather than 82.
+  const bool nf4 = W.type == LORA_WEIGHT_NF4;
+  const int rp = nf4 && M <= 96 ? 96 : M <= 64 ? 64 : 128;
   SkinnyParams sp;
   std::memset(&sp, 0, sizeof(sp));
   SkinnyProblem &PW = sp.pr[0];
   SkinnyProblem &PA = sp.pr[1];
-  const bool nf4 = W.type == LORA_WEIGHT_NF4;
   if ((s = kmajor_problem(PW, W.w, n, k, x, nullptr, 0, M, rp, dt, true)) ||
       (s = kmajor_problem(PA, A, r, k, x, nullptr, 0, M, rp, dt, true)))
     return s;

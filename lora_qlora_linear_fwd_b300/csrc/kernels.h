@@ -277,7 +277,7 @@ struct SkinnyParams {
 };
 
 // f16: the 16-bit operands (P, Q) and outputs (hi/lo, kOutRowBf16) are fp16.
-// dec: the NF4-decoding variant (KMAJOR, rp 64 or 128; problems with `nf4`
+// dec: the NF4-decoding variant (KMAJOR, rp 64, 96 or 128; problems with `nf4`
 // set stream codes through tm_p and absmax instead of P).
 // two: the variant with half-depth rings that runs two CTAs per SM (KMAJOR,
 // rp 64, no decode).
@@ -286,6 +286,8 @@ cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, 
 // Largest `split` the cluster kernel supports for (mn_major, rp, dec, two)
 // (its epilogue buffers must fit in its pipeline ring).
 int skinny_max_split(bool mn_major, int rp, bool dec = false, bool two = false);
+// Whether `split` CTAs per cluster is a valid cluster schedule for the pass.
+bool skinny_split_ok(bool mn_major, int rp, bool dec, bool two, int split);
 // Scratch of one stream-K launch: flags, then partials (256-byte aligned).
 size_t skinny_scratch_bytes(int rp);
 cudaError_t launch_skinny_sk(const SkinnyParams &p, bool mn_major, int rp, bool f16,

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
   static_assert(!DEC || !MN, "NF4 decode: KMAJOR only");
   static_assert(SkinnyEpi(RP, 1).bytes <= L::OFF_AMAX, "epilogue buffers fit in the ring");
   constexpr int STAGES = L::STAGES;
-  constexpr uint32_t kTmemCols = RP >= 32 ? RP : 32;
+  constexpr uint32_t kTmemCols = RP <= 32 ? 32 : RP <= 64 ? 64 : RP <= 128 ? 128 : 256;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_addr(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -432,10 +432,24 @@ static int max_split_t() {
   return s;
 }
 
+// The NF4 decoding pass with 96 token columns splits a tile over 1, 2, 3 or
+// 6 CTAs (16-column blocks); 41 row tiles (a 5120-row W and A) then fill 123
+// SMs instead of 82.
+static_assert(SkinnyEpi(96, 6).bytes <= SkinnySmem<false, 96, true>::OFF_AMAX,
+              "epilogue buffers of the 96-column decoding pass fit in its ring");
+
+bool skinny_split_ok(bool mn_major, int rp, bool dec, bool two, int split) {
+  if (split < 1 || split > 8 || rp % (16 * split) != 0) return false;
+  if (dec && !mn_major && !two && rp == 96) return split == 1 || split == 2 || split == 3 || split == 6;
+  if ((split & (split - 1)) != 0) return false;
+  return split <= skinny_max_split(mn_major, rp, dec, two);
+}
+
 int skinny_max_split(bool mn_major, int rp, bool dec, bool two) {
   if (two) return (!mn_major && !dec && rp == 64) ? max_split_t<false, 64, false, 2>() : 1;
   if (dec) {
     if (mn_major) return 1;
+    if (rp == 96) return 6;
     return rp == 64 ? max_split_t<false, 64, true>() : rp == 128 ? max_split_t<false, 128, true>() : 1;
   }
   switch (rp) {
@@ -457,6 +471,7 @@ static cudaError_t launch_skinny_cluster_t(const SkinnyParams &p, bool mn_major,
   if (dec) {
     if (mn_major) return cudaErrorInvalidValue;
     if (rp == 64) return launch_skinny_t<false, 64, F16, true>(p, st);
+    if (rp == 96) return launch_skinny_t<false, 96, F16, true>(p, st);
     if (rp == 128) return launch_skinny_t<false, 128, F16, true>(p, st);
     return cudaErrorInvalidValue;
   }
@@ -471,8 +486,7 @@ static cudaError_t launch_skinny_cluster_t(const SkinnyParams &p, bool mn_major,
 
 cudaError_t launch_skinny_cluster(const SkinnyParams &p, bool mn_major, int rp, bool f16,
                                   cudaStream_t st, bool dec, bool two) {
-  if (p.split != 1 && p.split != 2 && p.split != 4 && p.split != 8) return cudaErrorInvalidValue;
-  if (p.split > skinny_max_split(mn_major, rp, dec, two)) return cudaErrorInvalidValue;
+  if (!skinny_split_ok(mn_major, rp, dec, two, p.split)) return cudaErrorInvalidValue;
   return f16 ? launch_skinny_cluster_t<true>(p, mn_major, rp, dec, two, st)
              : launch_skinny_cluster_t<false>(p, mn_major, rp, dec, two, st);
 }

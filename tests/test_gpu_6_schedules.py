@@ -253,6 +253,8 @@ def test_nf4_qk_pair_staged_in_bf16():
     (16, 4096, 1088, 64, torch.bfloat16, "nf4"),      # W rows not a multiple of 128
     (50, 2048, 2048, 8, torch.float16, "nf4"),
     (100, 576, 640, 32, torch.bfloat16, "nf4"),
+    (96, 3072, 1024, 16, torch.bfloat16, "nf4"),      # 96 token columns, 6 CTAs per tile
+    (72, 1536, 2560, 32, torch.float16, "nf4"),       # 96 token columns, 3 CTAs per tile
     (24, 1024, 1536, 16, torch.bfloat16, "nf4dq"),
 ])
 def test_small_m_forward_runs_over_the_rows_of_w(M, k, n, r, dtype, kind):

@@ -259,14 +259,20 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
     float lvl[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) lvl[i] = kNf4Levels[i];
-    const __nv_bfloat16 *arow = P.absmax + (size_t)(row_in ? wrow : 0) * P.ld_absmax;
-    // the absmax of sequence position i (chunk c_begin + (i + c_rot) % n_chunks)
-    auto amax_ptr = [&](int i) { return arow + c_begin + (i + c_rot) % n_chunks; };
+    const __nv_bfloat16 *arow = P.absmax + (size_t)(row_in ? wrow : 0) * P.ld_absmax + c_begin;
+    // The absmax of sequence position i is arow[(i + c_rot) % n_chunks]; the
+    // offsets of the chunk being decoded (cur) and of the one PRE positions
+    // ahead (ahead) advance with wrap-around instead of a division per chunk.
+    int cur = n_chunks > 0 ? c_rot : 0, ahead = cur;
+    auto step = [&](int &o) {
+      if (++o == n_chunks) o = 0;
+    };
     auto prefetch = [&](int i, uint32_t slot) {
       if (dec && row_in && i < n_chunks)
         cp_async_4(ring + slot * kSlot, reinterpret_cast<const void *>(
-                                            reinterpret_cast<uintptr_t>(amax_ptr(i)) & ~uintptr_t(3)));
+                                            reinterpret_cast<uintptr_t>(arow + ahead) & ~uintptr_t(3)));
       cp_async_commit();
+      step(ahead);
     };
     for (int j = 0; j < PRE; ++j) prefetch(j, (uint32_t)j);
     int stage = 0;
@@ -284,9 +290,10 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
         float amax = 0.0f;
         if (row_in) {
           const uint32_t w = ld_shared_u32(ring + slot * kSlot);
-          const bool high = (reinterpret_cast<uintptr_t>(amax_ptr(i)) & 2u) != 0;
+          const bool high = (reinterpret_cast<uintptr_t>(arow + cur) & 2u) != 0;
           amax = __uint_as_float((high ? (w >> 16) : (w & 0xFFFFu)) << 16);
         }
+        step(cur);
         prefetch(i + PRE, slot);  // the slot just read refills for PRE chunks ahead
         if (++slot == (uint32_t)PRE) slot = 0;
         // a warp reads 16 rows x 32 contiguous code bytes: conflict-free

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
   const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
   const uint32_t bar_drain = bar_acc_full + 8;
   constexpr int PST = L::PST;
-  const uint32_t bar_pfull = bar_drain + 8;      // [PST] DEC: P tile ready (eight decode warps)
+  const uint32_t bar_pfull = bar_drain + 8;      // [PST] DEC: P tile ready (four warps of a decode group)
   const uint32_t bar_pempty = bar_pfull + 8 * PST;  // [PST] DEC: the MMA read the P tile
   uint32_t *tmem_holder =
       reinterpret_cast<uint32_t *>(smem + L::OFF_MISC + 8 * (2 * STAGES + 2 + 2 * PST));
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_drain, 1);
     for (int s = 0; s < PST; ++s) {
-      mbar_init(bar_pfull + 8 * s, 8);
+      mbar_init(bar_pfull + 8 * s, 4);  // the four warps of one decode group
       mbar_init(bar_pempty + 8 * s, 1);
     }
     *abort_flag = 0;
@@ -246,10 +246,12 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
     }
   } else if (DEC && warp >= 6) {
     // ------------------------------------------------------- NF4 decode
-    // thread t decodes half h = t & 1 (codes 32h..32h+31) of row t >> 1 of
-    // each P tile; a problem without codes passes its stages straight on
+    // Two groups of four warps take alternate chunks (group gr: chunks gr,
+    // gr + 2, ...); thread pr of a group decodes row pr of the chunk's P
+    // tile (64 codes, one scaled table).  A problem without codes passes its
+    // stages straight on.
     const int t = threadIdx.x - 192;  // 0..255
-    const int h = t & 1, prow = t >> 1;
+    const int gr = t >> 7, prow = t & 127;
     const bool dec = P.nf4 != 0;
     const int wrow = rt * 128 + prow;
     const bool row_in = wrow < P.rows;
@@ -260,27 +262,34 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
 #pragma unroll
     for (int i = 0; i < 16; ++i) lvl[i] = kNf4Levels[i];
     const __nv_bfloat16 *arow = P.absmax + (size_t)(row_in ? wrow : 0) * P.ld_absmax + c_begin;
-    // The absmax of sequence position i is arow[(i + c_rot) % n_chunks]; the
-    // offsets of the chunk being decoded (cur) and of the one PRE positions
-    // ahead (ahead) advance with wrap-around instead of a division per chunk.
-    int cur = n_chunks > 0 ? c_rot : 0, ahead = cur;
-    auto step = [&](int &o) {
-      if (++o == n_chunks) o = 0;
+    // The absmax of chunk i is arow[(i + c_rot) % n_chunks]; the offsets of
+    // the group's chunk being decoded (cur) and of its chunk PRE of its own
+    // chunks ahead (ahead) advance by two with wrap-around.
+    auto step2 = [&](int &o) {
+      o += 2;
+      while (o >= n_chunks && n_chunks > 0) o -= n_chunks;
     };
-    auto prefetch = [&](int i, uint32_t slot) {
-      if (dec && row_in && i < n_chunks)
+    int cur = n_chunks > 0 ? (c_rot + gr) % n_chunks : 0, ahead = cur;
+    int ia = gr;  // chunk of the next prefetch
+    auto prefetch = [&](uint32_t slot) {
+      if (dec && row_in && ia < n_chunks)
         cp_async_4(ring + slot * kSlot, reinterpret_cast<const void *>(
                                             reinterpret_cast<uintptr_t>(arow + ahead) & ~uintptr_t(3)));
       cp_async_commit();
-      step(ahead);
+      step2(ahead);
+      ia += 2;
     };
-    for (int j = 0; j < PRE; ++j) prefetch(j, (uint32_t)j);
-    int stage = 0;
+    for (int j = 0; j < PRE; ++j) prefetch((uint32_t)j);
+    // 32-byte code rows of consecutive threads are contiguous: threads whose
+    // rows start in the same half of the 32 banks read their two 16-byte
+    // halves in opposite orders, so each load touches every bank
+    const uint32_t flip = (uint32_t)(prow >> 2) & 1u;
+    int stage = gr;
     uint32_t phase = 0;
     uint32_t slot = 0;
-    int pslot = 0;
+    int pslot = gr;
     uint32_t pphase = 0;
-    for (int i = 0; i < n_chunks; ++i) {
+    for (int i = gr; i < n_chunks; i += 2) {
       if (!warp_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) break;
       // the P slot is free once the MMA of its previous use has completed
       // (for P loaded by TMA the producer waited for that)
@@ -293,29 +302,21 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
           const bool high = (reinterpret_cast<uintptr_t>(arow + cur) & 2u) != 0;
           amax = __uint_as_float((high ? (w >> 16) : (w & 0xFFFFu)) << 16);
         }
-        step(cur);
-        prefetch(i + PRE, slot);  // the slot just read refills for PRE chunks ahead
+        step2(cur);
+        prefetch(slot);  // the slot just read refills for PRE of the group's chunks ahead
         if (++slot == (uint32_t)PRE) slot = 0;
-        // a warp reads 16 rows x 32 contiguous code bytes: conflict-free
-        const uint4 cw = ld_shared_v4(slot_q(stage) + L::Q_BYTES + (uint32_t)t * 16u);
-        const Nf4Table tab = nf4_table<F16>(lvl, amax);
-        const uint32_t dst = slot_p(stage, pslot) + (uint32_t)prow * 128u;
-        const uint32_t ph = (uint32_t)prow & 7u;
-        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-        for (int ql = 0; ql < 4; ++ql) {
-          uint32_t o[4];
-          nf4_lookup4(tab, words[ql] & 0xFFFFu, o[0], o[1]);
-          nf4_lookup4(tab, words[ql] >> 16, o[2], o[3]);
-          const uint32_t q = (uint32_t)(4 * h + ql);
-          st_shared_v4(dst + ((q ^ ph) << 4), o[0], o[1], o[2], o[3]);
-        }
+        uint32_t words[8];
+        nf4_load_codes(slot_q(stage) + L::Q_BYTES + (uint32_t)prow * 32u, flip, words);
+        nf4_decode_words(words, slot_p(stage, pslot) + (uint32_t)prow * 128u,
+                         nf4_table<F16>(lvl, amax));
         fence_proxy_async_smem();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pfull + 8 * pslot);
-      if (++stage == STAGES) stage = 0, phase ^= 1u;
-      if (++pslot == PST) pslot = 0, pphase ^= 1u;
+      stage += 2;
+      if (stage >= STAGES) stage -= STAGES, phase ^= 1u;
+      pslot += 2;
+      if (pslot >= PST) pslot -= PST, pphase ^= 1u;
     }
     cp_async_wait<0>();  // no copy may land after the CTA exits
   }

@@ -621,7 +621,7 @@ lora_status_t fwd_rank(const void *x, const void *A1, const void *A2, int M, int
 // mostly empty and the n/256 tiles leave most SMs idle, so the forward runs
 // as a rank pass over the rows of W instead, in two launches:
 //   1. one rank-pass launch with two problems over the same x (the narrow
-//      operand, tokens padded to 64 or 128): yᵀ = W·xᵀ over the rows of W,
+//      operand, tokens padded to 64, 96 or 128): yᵀ = W·xᵀ over the rows of W,
 //      and (s·v)ᵀ = s·A·xᵀ over the rows of A; the reduction over k split
 //      across the CTAs of a cluster, both written transposed (y [M, n],
 //      s·v [M, r]);
@@ -631,18 +631,13 @@ lora_status_t fwd_rank(const void *x, const void *A1, const void *A2, int M, int
 // y, s·v and B.
 constexpr int kSmallM = 128;
 
-// Whether a forward of M tokens takes the small-M form.  A dense W: always
-// at M <= kSmallM.  An NF4 W: the decode, about three integer instructions
-// per weight, bounds both forms, so the small-M form is taken only while the
-// GEMM's n/256 tiles leave CTA pairs idle (measured on B300 at M = 16:
-// Qwen1.5-32B down_proj 164 us against 350 us, q_proj 47 against 76,
-// k_proj 33 against 86; gate_proj, 107 tiles, 135 against 123).
-bool small_m_pays(int M, int n, bool nf4) {
-  if (M > kSmallM) return false;
-  if (!nf4) return true;
-  const int pairs = gemm_pair_capacity(kModeFwd, false, true, 1, 0);
-  return pairs > 0 && (n + 255) / 256 < pairs;
-}
+// Whether a forward of M tokens takes the small-M form: at M <= kSmallM,
+// for a dense and an NF4 W alike.  Measured on B300 at M = 16-64 with the
+// NF4 decoding pass (a 64-code row per thread, 96 token columns): Qwen1.5-32B
+// down_proj 86 us against 350 us for the fused NF4 GEMM, q_proj 35 against
+// 76, k_proj 29 against 86, and gate_proj (107 GEMM tiles, so its pass runs
+// in two waves of CTAs) 102-106 against 125.
+bool small_m_pays(int M, int, bool) { return M <= kSmallM; }
 
 lora_status_t small_m_fwd(const void *x, const lora_weight_t &W, const void *A, const void *B,
                           void *y, int M, int k, int n, int r, float scale, void *sv,

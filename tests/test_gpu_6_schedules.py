@@ -89,11 +89,11 @@ def test_nf4_backward_dx_with_two_m_blocks_per_tile():
     assert rel_err(np64(got[2]), want[2]) <= TOL_F32
 
 
-@pytest.mark.parametrize("M,k,n", [(200, 512, 320), (300, 512, 74 * 256 - 192)])
+@pytest.mark.parametrize("M,k,n", [(16, 512, 320), (200, 512, 320), (300, 512, 74 * 256 - 192)])
 def test_nf4_zero_and_subnormal_blocks_in_the_fused_gemms(M, k, n):
     """An all-zero 64-block (absmax 0, every code 7) and a block of bf16
     subnormals decode to zero / tiny values inside the fused forward and dX
-    (one- and two-m-block tiles)."""
+    (one- and two-m-block tiles; at 16 tokens the forward's decoding pass)."""
     r = 16
     d = draw_projection(torch.Generator().manual_seed(63), M, k, n, r)
     W = d["W"].clone()

@@ -196,9 +196,11 @@ __global__ void __launch_bounds__(DEC ? 448 : 192, PER_SM)
         const int fills = issued > s ? (issued - s + STAGES - 1) / STAGES : 0;
         if (fills > 0) mbar_wait_quiet(bar_empty + 8 * s, (uint32_t)((fills - 1) & 1), lim);
       }
-      for (int s = 0; s < PST; ++s) {
-        const int fills = pissued > s ? (pissued - s + PST - 1) / PST : 0;
-        if (fills > 0) mbar_wait_quiet(bar_pempty + 8 * s, (uint32_t)((fills - 1) & 1), lim);
+      if constexpr (DEC) {  // the P ring exists only in the decoding variant
+        for (int s = 0; s < PST; ++s) {
+          const int fills = pissued > s ? (pissued - s + PST - 1) / PST : 0;
+          if (fills > 0) mbar_wait_quiet(bar_pempty + 8 * s, (uint32_t)((fills - 1) & 1), lim);
+        }
       }
     }
   } else if (warp == 1) {

@@ -161,6 +161,12 @@ size_t lora_nf4_stage_bytes(int n, int k);
  * tensor-memory accumulator before the single bf16 store of y, so neither
  * x·Wᵀ nor the adapter output goes to HBM.  An NF4 W is decoded tile by tile
  * in shared memory ([P3] 显存优化策略).
+ * One launch when every 256 x 256 output tile has a CTA pair of its own and
+ * W is 16-bit: s·x·Aᵀ is then formed inside the GEMM from the x tiles it
+ * already holds and never leaves shared memory.
+ * At M <= 128 the forward runs over the rows of W instead: one rank-pass
+ * launch computes yᵀ = W·xᵀ and (s·v)ᵀ (NF4 codes decoded in that pass),
+ * and a GEMM adds (s·v)·Bᵀ to y in its epilogue.
  *   x [M,k] bf16, W per lora_weight_t, A [r,k] bf16, B [n,r] bf16,
  *   y [M,n] bf16 (overwritten).  ws: >= lora_workspace_size(LORA_OP_FWD,...). */
 lora_status_t lora_linear_fwd(const void *x, lora_weight_t W, const void *A,

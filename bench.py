@@ -297,11 +297,39 @@ def measure_peaks(dev, sustained_s: float = 4.0):
                    f"back to back for {sustained_s:g} s (sustained); CUDA events"}
 
 
+def _code_only(src: str) -> str:
+    """C/C++/CUDA source without its comments and blank space, so that an
+    edit of the comments alone does not count as a change of the kernels
+    (string literals are kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the code (comments and spacing left out) of every file under
+    csrc: the traffic record applies while it is unchanged."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "lora_qlora_linear_fwd_b300", "csrc")
     for f in sorted(os.listdir(d)):
-        h.update(open(os.path.join(d, f), "rb").read())
+        h.update(f.encode() + b"\0")
+        h.update(_code_only(open(os.path.join(d, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 
